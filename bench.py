@@ -1,0 +1,542 @@
+"""Benchmark: paged GQA decode attention on GB300.
+
+One step = the whole hot path over one batch: append the new token of every
+sequence into the paged pool, then decode attention for every sequence
+(decode kernel + split-KV merge).  The default workload is the Llama3-8B
+attention shape (n_q=32, n_kv=8, d_head=128, batch 64, lengths uniform in
+[1024, 2048], bf16 KV); ``--workload`` picks another.
+
+Prints one JSON line.  ``value`` is achieved KV-read bandwidth (algorithmic
+bytes: K and V of every cached token + q + out, per step) in GB/s over the
+device-timed region, summed over ranks; ``calls_per_s`` is decode calls per
+second.  ``--impl reference`` times the CPU oracle instead.
+
+Run:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+N > 1 runs under torchrun as independent replicas (one per GPU, no
+collective on the data path; a barrier and a max over ranks for timing).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged GQA decode: achieved KV-read GB/s vs GB300 HBM peak; attention calls/s"
+L2_BYTES = 129 * 1000 * 1000
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="llama3_8b")
+    p.add_argument("--partition-tokens", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--flush-l2", action="store_true", help="write 512 MB between steps")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas; timing only)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def allreduce_max(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def allreduce_sum(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# byte accounting
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(w) -> dict:
+    """Bytes one decode call must move: K and V of every cached token of every
+    sequence (logical), the same counted once per distinct slot (unique), q
+    and out."""
+    import numpy as np
+
+    e = w.elem_bytes
+    per_token = 2 * w.n_kv * w.d_head * e
+    logical_tokens = int(w.context_lens.astype(np.int64).sum())
+    slots = set()
+    if w.shared_prefix_tokens:
+        for b in range(w.batch):
+            C = int(w.context_lens[b])
+            nb = (C + w.block_size - 1) // w.block_size
+            for j in range(nb):
+                n = min(w.block_size, C - j * w.block_size)
+                slots.update(int(w.block_tables[b, j]) * w.block_size + o for o in range(n))
+        unique_tokens = len(slots)
+    else:
+        unique_tokens = logical_tokens
+    qo = 2 * w.batch * w.n_q * w.d_head * 2
+    return {
+        "kv_logical": logical_tokens * per_token,
+        "kv_unique": unique_tokens * per_token,
+        "q_out": qo,
+        "logical": logical_tokens * per_token + qo,
+        "unique": unique_tokens * per_token + qo,
+        "flops": 4 * w.n_q * w.d_head * logical_tokens,
+    }
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, no MEASURED_PEAKS.json)"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for rel in ("gqa_decode_attention_paged_gb300/csrc/decode.cu",
+                "gqa_decode_attention_paged_gb300/csrc/pkv_internal.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, sha: str):
+    """dram bytes per decode launch from profiles/traffic.txt, if taken on this source."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None, None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == "decode_kernel" and parts[1] == workload:
+            if parts[2] == sha:
+                return float(parts[3]), " ".join(parts[4:])
+    return None, None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, "t_" + which, time.time())
+
+    def stop(self):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        rows = []
+        for t, line in self.samples:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                rows.append((t, float(parts[0]), float(parts[1]), float(parts[2]), parts[3:7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [r for r in rows if self.t_start and self.t_stop and self.t_start <= r[0] <= self.t_stop]
+        used = inside
+        note = "samples taken during the timed region"
+        if not used:  # region shorter than the sampling period: nearest samples after its start
+            used = sorted(rows, key=lambda r: abs(r[0] - (self.t_stop or r[0])))[:2]
+            note = "timed region shorter than the 100 ms sampling period; nearest samples"
+        reasons = sorted({self.NAMES[i] for r in used for i, v in enumerate(r[4]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
+                "power_w_max": max(r[3] for r in used), "reasons": reasons, "samples": len(used),
+                "note": note}
+
+
+def gpu_id_for(device_index: int) -> str:
+    import torch
+
+    try:
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        if u and not u.startswith("GPU-"):
+            u = "GPU-" + u
+        return u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[device_index] if vis else str(device_index)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+def oracle_setup(w):
+    import oracle
+
+    dt = oracle.BF16 if w.dtype == "bf16" else oracle.E4M3
+    m = oracle.PoolMirror(w.num_blocks, w.block_size, w.n_kv, w.d_head, dt, w.k_scale, w.v_scale)
+    m.append(w.fill_k, w.fill_v, w.fill_slots)
+    return m
+
+
+def oracle_step(m, w, seqs):
+    """The oracle's step on the sequences `seqs`: append their new tokens, decode them."""
+    import numpy as np
+
+    idx = np.asarray(seqs)
+    m.append(w.step_k[idx], w.step_v[idx], w.step_slots[idx])
+    return m.decode(w.q[idx], w.block_tables[idx], w.context_lens[idx], w.scale)
+
+
+def time_oracle(w, m, budget_s: float, max_reps: int = 1000):
+    """Time oracle steps over rotating single sequences until budget_s; returns
+    (GB/s, seconds, sequences done, threads)."""
+    import numpy as np
+
+    import oracle
+
+    per_seq = [int(c) * 2 * w.n_kv * w.d_head * w.elem_bytes + 2 * w.n_q * w.d_head * 2 for c in w.context_lens]
+    done_bytes, n, t0 = 0, 0, time.perf_counter()
+    b = 0
+    while n < max_reps:
+        oracle_step(m, w, [b])
+        done_bytes += per_seq[b]
+        n += 1
+        b = (b + 1) % w.batch
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done_bytes / dt / 1e9, dt, n, oracle.hardware_threads(), np.mean(per_seq)
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    import workloads as wl
+
+    w = wl.NAMED[args.workload]()
+    m = oracle_setup(w)
+    # Each step decodes one sequence (rotating); sized so the run ends in minutes.
+    times = []
+    per_seq = [int(c) * 2 * w.n_kv * w.d_head * w.elem_bytes + 2 * w.n_q * w.d_head * 2 for c in w.context_lens]
+    total_bytes = 0
+    budget = 150.0
+    t_run = time.perf_counter()
+    steps = args.steps
+    for i in range(args.warmup + args.steps):
+        if time.perf_counter() - t_run > budget and i >= args.warmup + 1:
+            steps = i - args.warmup
+            break
+        b = i % w.batch
+        t0 = time.perf_counter()
+        oracle_step(m, w, [b])
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            total_bytes += per_seq[b]
+    import oracle
+
+    secs = sum(times)
+    gbs = total_bytes / secs / 1e9 if secs > 0 else 0.0
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": len(times),
+        "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, len(times)), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(w.describe(), parallelism="replicas"),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": oracle.hardware_threads(), "kind": "oracle",
+                         "sample": f"one sequence (all {w.n_q} heads) per step, rotating over the "
+                                   f"{w.batch} sequences of the workload; steps requested {args.steps}, "
+                                   f"run {len(times)} within a {budget:.0f} s budget"},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import gqa_decode_attention_paged_gb300 as pkv
+    import workloads as wl
+
+    rank, local_rank, world = dist_env()
+    if world != args.gpus and world > 1:
+        print(f"warning: WORLD_SIZE={world} but --gpus={args.gpus}", file=sys.stderr)
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    init_dist(world, "nccl")
+
+    w = wl.NAMED[args.workload]()
+    acct = algorithmic_bytes(w)
+    use_unique = w.shared_prefix_tokens > 0
+    step_bytes = acct["unique"] if use_unique else acct["logical"]
+
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(device).view(dt)  # noqa: E731
+    dt = pkv.BF16 if w.dtype == "bf16" else pkv.FP8_E4M3
+    pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head, dt)
+    if w.dtype == "fp8":
+        pool.set_fp8_scales(w.k_scale, w.v_scale)
+    if args.partition_tokens:
+        pool.set_partition_tokens(args.partition_tokens)
+    pool.reserve_workspace(w.batch, w.n_q, w.max_blocks_per_seq)
+    T = w.fill_slots.shape[0]
+    for s in range(0, T, 1 << 20):
+        e = min(T, s + (1 << 20))
+        pkv.paged_kv_append(pool, dev(w.fill_k[s:e].view(np.int16), torch.bfloat16),
+                            dev(w.fill_v[s:e].view(np.int16), torch.bfloat16), dev(w.fill_slots[s:e], torch.int64))
+    k_new = dev(w.step_k.view(np.int16), torch.bfloat16)
+    v_new = dev(w.step_v.view(np.int16), torch.bfloat16)
+    slots = dev(w.step_slots, torch.int64)
+    q = dev(w.q.view(np.int16), torch.bfloat16)
+    tables = dev(w.block_tables, torch.int32)
+    lens = dev(w.context_lens, torch.int32)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device) if args.flush_l2 else None
+
+    def step():
+        pkv.paged_kv_append(pool, k_new, v_new, slots, stream)
+        pkv.paged_decode_attention(pool, q, tables, lens, float(w.scale), out, stream)
+
+    for _ in range(args.warmup):
+        step()
+        if flush is not None:
+            flush.fill_(1)
+    torch.cuda.synchronize()
+    assert pool.get_error() == 0, "device error during warm-up"
+
+    # ---- device-timed region ----
+    sampler = ClockSampler(gpu_id_for(local_rank)) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    pool.timing_read(reset=True)
+    pool.timing_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ms = []
+    barrier(world)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark("start")
+    if flush is None:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        elapsed_ms = ev0.elapsed_time(ev1)
+    else:  # L2 flushed between steps; only the steps are timed
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        step_ms = [a.elapsed_time(b) for a, b in evs]
+        elapsed_ms = sum(step_ms)
+    if sampler:
+        sampler.mark("stop")
+    barrier(world)
+    pool.timing_enable(False)
+    tm = pool.timing_read(reset=True)
+    if sampler:
+        sampler.stop()
+    assert pool.get_error() == 0, "device error in the timed region"
+    max_ms = allreduce_max(elapsed_ms, world, device)
+    total_bytes = allreduce_sum(step_bytes * args.steps, world, device)
+    value = total_bytes / (max_ms / 1e3) / 1e9
+    calls = allreduce_sum(args.steps, world, device) / (max_ms / 1e3)
+
+    # ---- end to end through the public API, host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+        h = {"k": pin(w.step_k.view(np.int16)), "v": pin(w.step_v.view(np.int16)), "s": pin(w.step_slots),
+             "q": pin(w.q.view(np.int16)), "t": pin(w.block_tables), "c": pin(w.context_lens)}
+        h_out = torch.empty(tuple(q.shape), dtype=torch.int16).pin_memory()
+        d = {k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in h.items()}
+        h2d = sum(v.numel() * v.element_size() for v in h.values())
+        d2h = h_out.numel() * h_out.element_size()
+
+        def e2e_step():
+            for k in h:
+                d[k].copy_(h[k], non_blocking=True)
+            pkv.paged_kv_append(pool, d["k"].view(torch.bfloat16), d["v"].view(torch.bfloat16), d["s"], stream)
+            o = pkv.paged_decode_attention(pool, d["q"].view(torch.bfloat16), d["t"], d["c"], float(w.scale),
+                                           out, stream)
+            h_out.copy_(o.view(torch.int16), non_blocking=True)
+            stream.synchronize()  # the host reads the step's result
+
+        for _ in range(min(args.warmup, 10)):
+            e2e_step()
+        n_e2e = max(1, min(args.steps, 2000))
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        e2e_s = allreduce_max(time.perf_counter() - t0, world, device)
+        e2e_total = allreduce_sum(step_bytes * n_e2e, world, device)
+        e2e = {"value": e2e_total / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": n_e2e, "ms_per_step": 1e3 * e2e_s / n_e2e,
+               "calls_per_s": allreduce_sum(n_e2e, world, device) / e2e_s}
+
+    if rank != 0:
+        pool.close()
+        return 0
+
+    # ---- parity on this very launch configuration (oracle, CPU) ----
+    import oracle  # noqa: F401  (test infrastructure: parity check and CPU baseline only)
+
+    m = oracle_setup(w)
+    ref = oracle_step(m, w, list(range(w.batch)))
+    got = out.float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)
+    parity = {"max_abs": float(err.max()), "mean_abs": float(err.mean()), "tol_max_abs": 1e-2,
+              "tol_mean_abs": 1e-3, "ok": bool(err.max() <= 1e-2 and err.mean() <= 1e-3)}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        gbs, secs, nseq, threads, _ = time_oracle(w, m, budget_s=12.0)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{nseq} single-sequence oracle steps (append + decode, all {w.n_q} heads, "
+                         f"fp64, {threads} threads) rotating over the workload's sequences, {secs:.1f} s"}
+
+    peak, peak_note = measured_peaks()
+    dec_ms = tm["decode_ms"] / max(1, tm["timed_decode"])
+    mer_ms = tm["merge_ms"] / max(1, tm["timed_merge"]) if tm["timed_merge"] else 0.0
+    app_ms = tm["append_ms"] / max(1, tm["timed_append"])
+    sha = kernel_source_sha()
+    traffic, traffic_note = ncu_traffic(w.name, sha)
+    achieved = step_bytes / (dec_ms / 1e3) / 1e9
+    clocks = sampler.summary() if sampler else None
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "calls_per_s": calls,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": max_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": dict(w.describe(), parallelism="replicas" if world > 1 else "single GPU",
+                       bytes_per_step=step_bytes, bytes_basis="unique KV slots" if use_unique else "logical KV",
+                       kv_bytes_logical=acct["kv_logical"], kv_bytes_unique=acct["kv_unique"],
+                       l2=("flushed (512 MB write) between steps" if args.flush_l2 else
+                           f"inputs larger than L2: {acct['kv_unique'] / 1e6:.0f} MB of KV per call vs 129 MB L2"),
+                       partition_tokens=args.partition_tokens or 512),
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "bytes_per_launch": step_bytes, "avg_launch_ms": dec_ms, "peak_source": peak_note,
+                     "traffic_source": traffic_note, "kernel_source_sha": sha},
+        "kernels_ms_avg": {"decode_kernel": dec_ms, "merge_kernel": mer_ms, "append_kernel": app_ms},
+        "step_frac_of_peak": value / world / peak,
+        "gpu_launches": int(tm["launches"]),
+        "clocks": clocks,
+        "parity": parity,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "flops_per_step": acct["flops"],
+    }
+    if use_unique:
+        line["effective_logical_gbs"] = acct["logical"] * args.steps * world / (max_ms / 1e3) / 1e9
+    print(json.dumps(line))
+    pool.close()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,270 @@
+"""Python binding of libpagedkv.so: paged GQA decode attention for GB300.
+
+Argument marshalling only: every step runs in the library's CUDA kernels
+(see ``include/pagedkv.h``).  torch supplies device memory and streams.  The
+library must be built (``__graft_entry__.build()`` or
+``python -m gqa_decode_attention_paged_gb300._build``); there is no fallback,
+and a missing or unloadable library raises.
+
+Names follow the C ABI: ``kv_pool_create``, ``paged_kv_append``,
+``paged_decode_attention``, ``kv_bytes_per_token``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+BF16 = 0
+FP8_E4M3 = 1
+
+STATUS = {0: "PKV_OK", 1: "PKV_EINVAL", 2: "PKV_ERANGE", 3: "PKV_ENOMEM", 4: "PKV_ECUDA",
+          5: "PKV_EUNSUPPORTED", 6: "PKV_EDEVICE"}
+
+DEVERR_SLOT_RANGE = 0x1
+DEVERR_BLOCK_RANGE = 0x2
+DEVERR_CTX_RANGE = 0x4
+DEVERR_TIMEOUT = 0x8
+
+_lib = None
+_lock = threading.Lock()
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class _Layout(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("stride_block", ctypes.c_int64),
+                ("stride_head", ctypes.c_int64), ("stride_token", ctypes.c_int64),
+                ("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
+                ("n_kv", ctypes.c_int32), ("d_head", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("bytes_per_array", ctypes.c_int64)]
+
+
+class _Timing(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int64), ("append_launches", ctypes.c_int64),
+                ("decode_launches", ctypes.c_int64), ("merge_launches", ctypes.c_int64),
+                ("append_ms", ctypes.c_double), ("decode_ms", ctypes.c_double),
+                ("merge_ms", ctypes.c_double), ("timed_append", ctypes.c_int64),
+                ("timed_decode", ctypes.c_int64), ("timed_merge", ctypes.c_int64)]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libpagedkv.so (building it first if it is missing and nvcc exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path) and build_if_missing:
+            _build.build()
+        if not os.path.exists(path):
+            raise ImportError(f"libpagedkv.so not found at {path}; run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        c = ctypes
+        P = c.c_void_p
+        lib.kv_pool_create.argtypes = [c.c_int64, c.c_int32, c.c_int32, c.c_int32, c.c_int32,
+                                       c.POINTER(P)]
+        lib.kv_pool_destroy.argtypes = [P]
+        lib.kv_pool_set_fp8_scales.argtypes = [P, P, P]
+        lib.kv_pool_layout.argtypes = [P, c.POINTER(_Layout)]
+        lib.kv_pool_set_partition_tokens.argtypes = [P, c.c_int32]
+        lib.kv_pool_reserve_workspace.argtypes = [P, c.c_int32, c.c_int32, c.c_int32]
+        lib.paged_kv_append.argtypes = [P, P, P, P, c.c_int64, P]
+        lib.paged_decode_attention.argtypes = [P, P, c.c_int32, P, c.c_int32, P, c.c_int32,
+                                               c.c_float, P, P]
+        lib.kv_bytes_per_token.argtypes = [c.c_int32, c.c_int32, c.c_int32, c.c_double]
+        lib.kv_bytes_per_token.restype = c.c_double
+        lib.pkv_get_error.argtypes = [P, c.c_int32, c.POINTER(c.c_uint32)]
+        lib.pkv_timing_enable.argtypes = [P, c.c_int32]
+        lib.pkv_timing_read.argtypes = [P, c.c_int32, c.POINTER(_Timing)]
+        lib.pkv_status_string.argtypes = [c.c_int]
+        lib.pkv_status_string.restype = c.c_char_p
+        lib.pkv_last_error_message.argtypes = []
+        lib.pkv_last_error_message.restype = c.c_char_p
+        for name in ("kv_pool_create", "kv_pool_destroy", "kv_pool_set_fp8_scales", "kv_pool_layout",
+                     "kv_pool_set_partition_tokens", "kv_pool_reserve_workspace", "paged_kv_append",
+                     "paged_decode_attention", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read"):
+            getattr(lib, name).restype = c.c_int
+        _lib = lib
+        return lib
+
+
+def _check(status: int, allow=(0,)):
+    if status not in allow:
+        msg = load().pkv_last_error_message().decode(errors="replace")
+        raise PagedKVError(status, msg)
+    return status
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dev_ptr(t, name, dtype=None, ndim=None, shape=None):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if shape is not None:
+        for i, s in enumerate(shape):
+            if s is not None and t.shape[i] != s:
+                raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def kv_bytes_per_token(layers: int, n_kv: int, d_head: int, bytes_per_value: float) -> float:
+    """2 x layers x n_kv x d_head x bytes_per_value (host arithmetic in the library)."""
+    return float(load().kv_bytes_per_token(layers, n_kv, d_head, float(bytes_per_value)))
+
+
+class Pool:
+    """A K/V block pool owned by the library (one layer).  Use kv_pool_create()."""
+
+    def __init__(self, handle, num_blocks, block_size, n_kv, d_head, dtype):
+        self._h = handle
+        self.num_blocks, self.block_size, self.n_kv, self.d_head, self.dtype = (
+            num_blocks, block_size, n_kv, d_head, dtype)
+
+    @property
+    def handle(self):
+        if not self._h:
+            raise ValueError("pool is closed")
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            load().kv_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def set_fp8_scales(self, k_scale, v_scale):
+        import numpy as np
+
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+        if ks.shape != (self.n_kv,) or vs.shape != (self.n_kv,):
+            raise ValueError(f"scales must have shape ({self.n_kv},)")
+        _check(load().kv_pool_set_fp8_scales(self.handle, ks.ctypes.data_as(ctypes.c_void_p),
+                                             vs.ctypes.data_as(ctypes.c_void_p)))
+
+    def layout(self) -> dict:
+        lay = _Layout()
+        _check(load().kv_pool_layout(self.handle, ctypes.byref(lay)))
+        return {f: getattr(lay, f) for f, _ in _Layout._fields_}
+
+    def set_partition_tokens(self, tokens: int):
+        _check(load().kv_pool_set_partition_tokens(self.handle, int(tokens)))
+
+    def reserve_workspace(self, batch: int, n_q: int, max_blocks_per_seq: int):
+        _check(load().kv_pool_reserve_workspace(self.handle, batch, n_q, max_blocks_per_seq))
+
+    def get_error(self, clear: bool = False) -> int:
+        bits = ctypes.c_uint32(0)
+        _check(load().pkv_get_error(self.handle, int(clear), ctypes.byref(bits)), allow=(0, 6))
+        return int(bits.value)
+
+    def timing_enable(self, on: bool = True):
+        _check(load().pkv_timing_enable(self.handle, int(on)))
+
+    def timing_read(self, reset: bool = False) -> dict:
+        t = _Timing()
+        _check(load().pkv_timing_read(self.handle, int(reset), ctypes.byref(t)))
+        return {f: getattr(t, f) for f, _ in _Timing._fields_}
+
+    def k_view(self):
+        """The K pool as a torch uint8 tensor view [num_blocks, n_kv, block_size, d_head * elem]."""
+        return self._view("k")
+
+    def v_view(self):
+        return self._view("v")
+
+    def _view(self, which):
+        import torch
+
+        lay = self.layout()
+        elem = 2 if self.dtype == BF16 else 1
+        n = lay["bytes_per_array"]
+        ptr = lay[which]
+
+        class _Holder:  # exposes the pool's memory through the CUDA array interface
+            __cuda_array_interface__ = {"shape": (n,), "typestr": "|u1", "data": (ptr, False),
+                                        "version": 3, "strides": None}
+
+        flat = torch.as_tensor(_Holder(), device="cuda")
+        return flat.view(self.num_blocks, self.n_kv, self.block_size, self.d_head * elem)
+
+
+def kv_pool_create(num_blocks: int, block_size: int, n_kv: int, d_head: int, dtype: int = BF16) -> Pool:
+    h = ctypes.c_void_p()
+    _check(load().kv_pool_create(int(num_blocks), int(block_size), int(n_kv), int(d_head), int(dtype),
+                                 ctypes.byref(h)))
+    return Pool(h, int(num_blocks), int(block_size), int(n_kv), int(d_head), int(dtype))
+
+
+def paged_kv_append(pool: Pool, k_new, v_new, slot_mapping, stream=None):
+    """k_new, v_new: bf16 [T, n_kv, d_head]; slot_mapping: int64 [T] (all CUDA)."""
+    import torch
+
+    T = int(slot_mapping.shape[0]) if slot_mapping is not None else 0
+    shape = (T, pool.n_kv, pool.d_head)
+    kp = _dev_ptr(k_new, "k_new", torch.bfloat16, 3, shape)
+    vp = _dev_ptr(v_new, "v_new", torch.bfloat16, 3, shape)
+    sp = _dev_ptr(slot_mapping, "slot_mapping", torch.int64, 1)
+    _check(load().paged_kv_append(pool.handle, kp, vp, sp, T, _stream_handle(stream)))
+
+
+def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: float, out=None,
+                           stream=None):
+    """q: bf16 [B, n_q, d_head]; block_tables: int32 [B, W]; context_lens: int32 [B].
+    Returns ``out`` (bf16 [B, n_q, d_head]), allocated if not given."""
+    import torch
+
+    qp = _dev_ptr(q, "q", torch.bfloat16, 3, (None, None, pool.d_head))
+    B, n_q = int(q.shape[0]), int(q.shape[1])
+    tp = _dev_ptr(block_tables, "block_tables", torch.int32, 2, (B, None))
+    cp = _dev_ptr(context_lens, "context_lens", torch.int32, 1, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    op = _dev_ptr(out, "out", torch.bfloat16, 3, tuple(q.shape))
+    _check(load().paged_decode_attention(pool.handle, qp, n_q, tp, int(block_tables.shape[1]), cp, B,
+                                         float(scale), op, _stream_handle(stream)))
+    return out
+
+
+__all__ = ["BF16", "FP8_E4M3", "Pool", "PagedKVError", "kv_pool_create", "paged_kv_append",
+           "paged_decode_attention", "kv_bytes_per_token", "load", "library_path"]

@@ -1,0 +1,149 @@
+// Append / scatter: write each token's new key and value rows into its slot
+// of the block pool ("The KV Cache from First Principles", "Deriving the
+// cache": k_t and v_t are computed once and appended; "KV cache,
+// PagedAttention and FlashAttention", Problem 4: slot = physical block x B +
+// offset).  FP8 pools quantise on the way in: E4M3(fp32(x) / scale[g]),
+// round to nearest even, saturating.
+//
+// Work split: one group of D/8 lanes per (token, KV head) row, each lane
+// moving 8 elements (one 16-byte load of bf16 per array).  Grid-stride over
+// rows, so a per-step append (tens of rows) and a bulk prefill (millions)
+// use the same kernel.  Memory-bound: per row it reads 2*D*2 bytes and
+// writes 2*D*e bytes.
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+struct AppendArgs {
+    uint8_t *k_pool, *v_pool;
+    int64_t num_blocks;
+    int n_kv;
+    const __nv_bfloat16 *k_new, *v_new;  // [T][n_kv][D]
+    const int64_t *slot_mapping;          // [T]
+    int64_t n_tokens;
+    const float *scales;                  // [2*n_kv] (FP8 only)
+    unsigned *err;
+};
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(256) append_kernel(AppendArgs a)
+{
+    constexpr int LPR = D / 8;  // lanes per row
+    constexpr int E = FP8 ? 1 : 2;
+    const int64_t rows = a.n_tokens * a.n_kv;
+    const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int sub = (int)(gid % LPR);
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x / LPR;
+    const int64_t slots = a.num_blocks * kBlockSize;
+    for (int64_t row = gid / LPR; row < rows; row += stride) {
+        const int64_t t = row / a.n_kv;
+        const int g = (int)(row - t * a.n_kv);
+        const int64_t slot = a.slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= slots) {
+            if (sub == 0) atomicOr(a.err, PKV_DEVERR_SLOT_RANGE);
+            continue;
+        }
+        const int64_t blk = slot / kBlockSize;
+        const int64_t off = slot - blk * kBlockSize;
+        const int64_t dst = (((blk * a.n_kv + g) * kBlockSize + off) * D + sub * 8) * E;
+        const int64_t src = (t * a.n_kv + g) * D + sub * 8;
+        const uint4 kr = ldg_nc_v4(a.k_new + src);
+        const uint4 vr = ldg_nc_v4(a.v_new + src);
+        if constexpr (!FP8) {
+            *reinterpret_cast<uint4 *>(a.k_pool + dst) = kr;
+            *reinterpret_cast<uint4 *>(a.v_pool + dst) = vr;
+        } else {
+            const float ks = a.scales[g];
+            const float vs = a.scales[a.n_kv + g];
+            const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+            const uint32_t vw[4] = {vr.x, vr.y, vr.z, vr.w};
+            uint32_t ko[2], vo[2];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 kf = bf16x2_to_f32x2(kw[i]);
+                const float2 vf = bf16x2_to_f32x2(vw[i]);
+                // correctly rounded fp32 division, then RN + satfinite to E4M3
+                const uint32_t kq = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(kf.x, ks), __fdiv_rn(kf.y, ks)), __NV_SATFINITE, __NV_E4M3);
+                const uint32_t vq = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(vf.x, vs), __fdiv_rn(vf.y, vs)), __NV_SATFINITE, __NV_E4M3);
+                if (i & 1) {
+                    ko[i >> 1] |= kq << 16;
+                    vo[i >> 1] |= vq << 16;
+                } else {
+                    ko[i >> 1] = kq;
+                    vo[i >> 1] = vq;
+                }
+            }
+            *reinterpret_cast<uint2 *>(a.k_pool + dst) = make_uint2(ko[0], ko[1]);
+            *reinterpret_cast<uint2 *>(a.v_pool + dst) = make_uint2(vo[0], vo[1]);
+        }
+    }
+}
+
+template <int D, bool FP8>
+static cudaError_t launch_append(const AppendArgs &a, int num_sms, cudaStream_t s)
+{
+    constexpr int LPR = D / 8;
+    constexpr int kThreads = 256;
+    const int64_t lanes = a.n_tokens * a.n_kv * LPR;
+    int64_t blocks = (lanes + kThreads - 1) / kThreads;
+    const int64_t cap = (int64_t)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    append_kernel<D, FP8><<<(unsigned)blocks, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+pkv_status probe_kernels()
+{
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, append_kernel<128, false>);
+    if (e != cudaSuccess)
+        return fail(e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver ? PKV_ECUDA : PKV_EUNSUPPORTED,
+                    "this library runs on sm_103 (GB300) only: %s", cudaGetErrorString(e));
+    return PKV_OK;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" pkv_status paged_kv_append(pkv_pool *pool, const void *k_new, const void *v_new,
+                                      const int64_t *slot_mapping, int64_t n_tokens, void *stream)
+{
+    if (!pool) return fail(PKV_EINVAL, "paged_kv_append: NULL pool");
+    if (n_tokens < 0) return fail(PKV_EINVAL, "paged_kv_append: n_tokens < 0");
+    if (n_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping)
+        return fail(PKV_EINVAL, "paged_kv_append: NULL device pointer");
+    if (((uintptr_t)k_new | (uintptr_t)v_new) & 15u)
+        return fail(PKV_EINVAL, "paged_kv_append: k_new/v_new must be 16-byte aligned");
+    if ((uintptr_t)slot_mapping & 7u)
+        return fail(PKV_EINVAL, "paged_kv_append: slot_mapping must be 8-byte aligned");
+    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
+    if (fp8 && !pool->scales_set)
+        return fail(PKV_EINVAL, "paged_kv_append: FP8 pool needs kv_pool_set_fp8_scales first");
+    AppendArgs a;
+    a.k_pool = static_cast<uint8_t *>(pool->k);
+    a.v_pool = static_cast<uint8_t *>(pool->v);
+    a.num_blocks = pool->num_blocks;
+    a.n_kv = pool->n_kv;
+    a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    a.slot_mapping = slot_mapping;
+    a.n_tokens = n_tokens;
+    a.scales = pool->scales;
+    a.err = pool->err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    LaunchScope ls(pool, kAppend, s);
+    cudaError_t e;
+    if (pool->d_head == 128)
+        e = fp8 ? launch_append<128, true>(a, pool->num_sms, s) : launch_append<128, false>(a, pool->num_sms, s);
+    else
+        e = fp8 ? launch_append<64, true>(a, pool->num_sms, s) : launch_append<64, false>(a, pool->num_sms, s);
+    ls.done();
+    if (e != cudaSuccess) return cuda_fail(e, "paged_kv_append launch");
+    return PKV_OK;
+}

@@ -1,0 +1,188 @@
+// Internal declarations shared by the library's translation units: the pool
+// object, status helpers and the inline-PTX wrappers for mbarriers and bulk
+// (TMA) copies used by the kernels.  sm_103a only.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <vector>
+
+#include "pagedkv.h"
+
+namespace pkv {
+
+constexpr int kBlockSize = 16;               // token slots per block
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded mbarrier waits: 2 s
+constexpr int kDefaultPartitionTokens = 512;
+
+enum KernelKind { kAppend = 0, kDecode = 1, kMerge = 2, kNumKinds = 3 };
+
+struct EventPair {
+    cudaEvent_t start, stop;
+    int kind;
+};
+
+}  // namespace pkv
+
+struct pkv_pool {
+    int device = 0;
+    int num_sms = 0;
+    int64_t num_blocks = 0;
+    int block_size = 0, n_kv = 0, d_head = 0, dtype = 0;
+    void *k = nullptr, *v = nullptr;  // device, [num_blocks][n_kv][block_size][d_head]
+    size_t bytes_per_array = 0;
+    float *scales = nullptr;          // device [2 * n_kv]: k scales then v scales
+    bool scales_set = false;
+    unsigned *err = nullptr;          // device sticky error word
+    void *ws = nullptr;               // split-KV workspace (grow-only)
+    size_t ws_bytes = 0;
+    int partition_tokens = pkv::kDefaultPartitionTokens;
+    // timing / launch accounting
+    std::mutex mu;
+    bool timing = false;
+    std::vector<pkv::EventPair> pending;
+    std::vector<cudaEvent_t> free_events;
+    int64_t launches[pkv::kNumKinds] = {0, 0, 0};
+    int64_t timed[pkv::kNumKinds] = {0, 0, 0};
+    double ms[pkv::kNumKinds] = {0, 0, 0};
+};
+
+namespace pkv {
+
+// Records a failure message for pkv_last_error_message() and returns `s`.
+pkv_status fail(pkv_status s, const char *fmt, ...);
+pkv_status cuda_fail(cudaError_t e, const char *what);
+
+// Brackets a kernel launch with a timing event pair when timing is on, and
+// counts the launch.  Usage: LaunchScope ls(pool, kind, stream); launch...;
+// ls.done();
+struct LaunchScope {
+    pkv_pool *pool;
+    int kind;
+    cudaStream_t stream;
+    cudaEvent_t a = nullptr, b = nullptr;
+    LaunchScope(pkv_pool *p, int k, cudaStream_t s);
+    void done();
+};
+
+pkv_status ensure_workspace(pkv_pool *pool, size_t bytes);
+
+// ---------------------------------------------------------------------------
+// Device helpers (inline PTX)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Order this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// One-dimensional bulk copy global -> shared (TMA engine), completing
+// `bytes` of transaction count on `bar`.  dst and src 16-byte aligned, bytes a
+// multiple of 16.  evict-first L2 policy: K/V tiles are streamed once.
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, uint32_t bytes,
+                                         uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// bf16 pair packed in a 32-bit word -> two fp32 (exact).
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t u)
+{
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+// Two E4M3 codes packed in 16 bits (low byte first) -> two fp32 (exact).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t u16)
+{
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u16), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<__half2 *>(&h));
+}
+
+}  // namespace pkv

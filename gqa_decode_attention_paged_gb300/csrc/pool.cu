@@ -1,0 +1,308 @@
+// Pool lifetime, layout, FP8 scales, workspace, error word, timing and the
+// host-only entry points of the C ABI (include/pagedkv.h).
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+static thread_local char g_msg[512] = "";
+
+pkv_status fail(pkv_status s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char *what)
+{
+    snprintf(g_msg, sizeof g_msg, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+    if (e == cudaErrorMemoryAllocation) return PKV_ENOMEM;
+    return PKV_ECUDA;
+}
+
+LaunchScope::LaunchScope(pkv_pool *p, int k, cudaStream_t s) : pool(p), kind(k), stream(s)
+{
+    std::lock_guard<std::mutex> g(pool->mu);
+    pool->launches[kind] += 1;
+    if (!pool->timing) return;
+    for (cudaEvent_t *ev : {&a, &b}) {
+        if (!pool->free_events.empty()) {
+            *ev = pool->free_events.back();
+            pool->free_events.pop_back();
+        } else if (cudaEventCreate(ev) != cudaSuccess) {
+            *ev = nullptr;
+        }
+    }
+    if (a && b) cudaEventRecord(a, stream);
+}
+
+void LaunchScope::done()
+{
+    if (!a || !b) return;
+    cudaEventRecord(b, stream);
+    std::lock_guard<std::mutex> g(pool->mu);
+    pool->pending.push_back(EventPair{a, b, kind});
+}
+
+pkv_status ensure_workspace(pkv_pool *pool, size_t bytes)
+{
+    if (bytes <= pool->ws_bytes) return PKV_OK;
+    size_t want = bytes + bytes / 4;  // grow with headroom
+    want = (want + (1u << 20) - 1) & ~size_t((1u << 20) - 1);
+    if (pool->ws) {
+        cudaError_t e = cudaFree(pool->ws);  // synchronises: no kernel still uses it
+        pool->ws = nullptr;
+        pool->ws_bytes = 0;
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+    }
+    cudaError_t e = cudaMalloc(&pool->ws, want);
+    if (e != cudaSuccess) {
+        pool->ws = nullptr;
+        return cuda_fail(e, "cudaMalloc(workspace)");
+    }
+    pool->ws_bytes = want;
+    return PKV_OK;
+}
+
+// Defined in append.cu / decode.cu: confirm the device can run our kernels.
+pkv_status probe_kernels();
+size_t decode_workspace_bytes(int batch, int n_q, int n_kv, int d_head, int max_blocks_per_seq,
+                              int partition_tokens);
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char *pkv_status_string(pkv_status s)
+{
+    switch (s) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_EINVAL: return "PKV_EINVAL";
+    case PKV_ERANGE: return "PKV_ERANGE";
+    case PKV_ENOMEM: return "PKV_ENOMEM";
+    case PKV_ECUDA: return "PKV_ECUDA";
+    case PKV_EUNSUPPORTED: return "PKV_EUNSUPPORTED";
+    case PKV_EDEVICE: return "PKV_EDEVICE";
+    }
+    return "PKV_UNKNOWN";
+}
+
+const char *pkv_last_error_message(void) { return g_msg; }
+
+double kv_bytes_per_token(int32_t layers, int32_t n_kv, int32_t d_head, double bytes_per_value)
+{
+    if (layers < 0 || n_kv < 0 || d_head < 0 || !(bytes_per_value >= 0.0)) return -1.0;
+    // keys and values (2) x layers x KV heads x head dim x bytes per value
+    return 2.0 * (double)layers * (double)n_kv * (double)d_head * bytes_per_value;
+}
+
+pkv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv, int32_t d_head,
+                          int32_t dtype, pkv_pool **out)
+{
+    g_msg[0] = '\0';
+    if (!out) return fail(PKV_EINVAL, "kv_pool_create: out is NULL");
+    *out = nullptr;
+    if (num_blocks <= 0 || block_size <= 0 || n_kv <= 0 || d_head <= 0)
+        return fail(PKV_EINVAL, "kv_pool_create: sizes must be positive");
+    if (block_size != kBlockSize)
+        return fail(PKV_EUNSUPPORTED, "kv_pool_create: block_size %d unsupported (16 only)", block_size);
+    if (d_head != 64 && d_head != 128)
+        return fail(PKV_EUNSUPPORTED, "kv_pool_create: d_head %d unsupported (64 or 128)", d_head);
+    if (n_kv > 256) return fail(PKV_EUNSUPPORTED, "kv_pool_create: n_kv %d > 256", n_kv);
+    if (dtype != PKV_BF16 && dtype != PKV_FP8_E4M3)
+        return fail(PKV_EINVAL, "kv_pool_create: unknown dtype %d", dtype);
+    const size_t elem = dtype == PKV_BF16 ? 2 : 1;
+    const size_t per_block = (size_t)n_kv * block_size * d_head * elem;
+    if ((size_t)num_blocks > ((size_t)1 << 46) / per_block)
+        return fail(PKV_ERANGE, "kv_pool_create: pool too large");
+
+    pkv_status st = probe_kernels();
+    if (st != PKV_OK) return st;
+
+    pkv_pool *p = new (std::nothrow) pkv_pool();
+    if (!p) return fail(PKV_ENOMEM, "kv_pool_create: host allocation failed");
+    cudaError_t e = cudaGetDevice(&p->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+    if (e != cudaSuccess) {
+        delete p;
+        return cuda_fail(e, "kv_pool_create: device query");
+    }
+    p->num_blocks = num_blocks;
+    p->block_size = block_size;
+    p->n_kv = n_kv;
+    p->d_head = d_head;
+    p->dtype = dtype;
+    p->bytes_per_array = per_block * (size_t)num_blocks;
+    const char *what = "cudaMalloc(K pool)";
+    e = cudaMalloc(&p->k, p->bytes_per_array);
+    if (e == cudaSuccess) { what = "cudaMalloc(V pool)"; e = cudaMalloc(&p->v, p->bytes_per_array); }
+    if (e == cudaSuccess) { what = "cudaMalloc(scales)"; e = cudaMalloc(&p->scales, sizeof(float) * 2 * n_kv); }
+    if (e == cudaSuccess) { what = "cudaMalloc(error word)"; e = cudaMalloc(&p->err, sizeof(unsigned)); }
+    if (e == cudaSuccess) { what = "cudaMemset"; e = cudaMemset(p->k, 0, p->bytes_per_array); }
+    if (e == cudaSuccess) e = cudaMemset(p->v, 0, p->bytes_per_array);
+    if (e == cudaSuccess) e = cudaMemset(p->scales, 0, sizeof(float) * 2 * n_kv);
+    if (e == cudaSuccess) e = cudaMemset(p->err, 0, sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        pkv_status s = cuda_fail(e, what);
+        kv_pool_destroy(p);
+        return s;
+    }
+    *out = p;
+    return PKV_OK;
+}
+
+pkv_status kv_pool_destroy(pkv_pool *pool)
+{
+    if (!pool) return PKV_OK;
+    cudaDeviceSynchronize();
+    cudaFree(pool->k);
+    cudaFree(pool->v);
+    cudaFree(pool->scales);
+    cudaFree(pool->err);
+    cudaFree(pool->ws);
+    for (auto &pe : pool->pending) {
+        cudaEventDestroy(pe.start);
+        cudaEventDestroy(pe.stop);
+    }
+    for (cudaEvent_t ev : pool->free_events) cudaEventDestroy(ev);
+    delete pool;
+    return PKV_OK;
+}
+
+pkv_status kv_pool_set_fp8_scales(pkv_pool *pool, const float *k_scale_host, const float *v_scale_host)
+{
+    if (!pool || !k_scale_host || !v_scale_host)
+        return fail(PKV_EINVAL, "kv_pool_set_fp8_scales: NULL argument");
+    if (pool->dtype != PKV_FP8_E4M3)
+        return fail(PKV_EINVAL, "kv_pool_set_fp8_scales: pool is not FP8");
+    std::vector<float> s(2 * pool->n_kv);
+    for (int g = 0; g < pool->n_kv; ++g) {
+        s[g] = k_scale_host[g];
+        s[pool->n_kv + g] = v_scale_host[g];
+    }
+    for (float x : s)
+        if (!(x > 0.0f) || !isfinite(x))
+            return fail(PKV_EINVAL, "kv_pool_set_fp8_scales: scales must be finite and > 0");
+    cudaError_t e = cudaMemcpy(pool->scales, s.data(), sizeof(float) * s.size(), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "kv_pool_set_fp8_scales");
+    pool->scales_set = true;
+    return PKV_OK;
+}
+
+pkv_status kv_pool_layout(const pkv_pool *pool, pkv_layout *out)
+{
+    if (!pool || !out) return fail(PKV_EINVAL, "kv_pool_layout: NULL argument");
+    out->k = pool->k;
+    out->v = pool->v;
+    out->stride_token = pool->d_head;
+    out->stride_head = (int64_t)pool->block_size * pool->d_head;
+    out->stride_block = (int64_t)pool->n_kv * out->stride_head;
+    out->num_blocks = pool->num_blocks;
+    out->block_size = pool->block_size;
+    out->n_kv = pool->n_kv;
+    out->d_head = pool->d_head;
+    out->dtype = pool->dtype;
+    out->bytes_per_array = (int64_t)pool->bytes_per_array;
+    return PKV_OK;
+}
+
+pkv_status kv_pool_set_partition_tokens(pkv_pool *pool, int32_t tokens)
+{
+    if (!pool) return fail(PKV_EINVAL, "kv_pool_set_partition_tokens: NULL pool");
+    if (tokens == 0) tokens = kDefaultPartitionTokens;
+    if (tokens < 64 || tokens > 65536 || tokens % 64)
+        return fail(PKV_ERANGE, "kv_pool_set_partition_tokens: %d not a multiple of 64 in [64, 65536]",
+                    tokens);
+    pool->partition_tokens = tokens;
+    return PKV_OK;
+}
+
+pkv_status kv_pool_reserve_workspace(pkv_pool *pool, int32_t batch, int32_t n_q, int32_t max_blocks_per_seq)
+{
+    if (!pool || batch < 0 || n_q <= 0 || max_blocks_per_seq <= 0 || n_q % pool->n_kv)
+        return fail(PKV_EINVAL, "kv_pool_reserve_workspace: bad argument");
+    return ensure_workspace(pool, decode_workspace_bytes(batch, n_q, pool->n_kv, pool->d_head,
+                                                         max_blocks_per_seq, pool->partition_tokens));
+}
+
+pkv_status pkv_get_error(pkv_pool *pool, int32_t clear, uint32_t *bits)
+{
+    if (!pool) return fail(PKV_EINVAL, "pkv_get_error: NULL pool");
+    unsigned v = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&v, pool->err, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && clear) e = cudaMemset(pool->err, 0, sizeof(unsigned));
+    if (e == cudaSuccess && clear) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_get_error");
+    if (bits) *bits = v;
+    if (v) return fail(PKV_EDEVICE, "device error bits 0x%x", v);
+    return PKV_OK;
+}
+
+pkv_status pkv_timing_enable(pkv_pool *pool, int32_t on)
+{
+    if (!pool) return fail(PKV_EINVAL, "pkv_timing_enable: NULL pool");
+    std::lock_guard<std::mutex> g(pool->mu);
+    pool->timing = on != 0;
+    return PKV_OK;
+}
+
+pkv_status pkv_timing_read(pkv_pool *pool, int32_t reset, pkv_timing *out)
+{
+    if (!pool) return fail(PKV_EINVAL, "pkv_timing_read: NULL pool");
+    std::vector<EventPair> pend;
+    {
+        std::lock_guard<std::mutex> g(pool->mu);
+        pend.swap(pool->pending);
+    }
+    pkv_status st = PKV_OK;
+    for (auto &pe : pend) {
+        cudaError_t e = cudaEventSynchronize(pe.stop);
+        float ms = 0.0f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, pe.start, pe.stop);
+        if (e != cudaSuccess && st == PKV_OK) st = cuda_fail(e, "pkv_timing_read");
+        std::lock_guard<std::mutex> g(pool->mu);
+        if (e == cudaSuccess) {
+            pool->ms[pe.kind] += ms;
+            pool->timed[pe.kind] += 1;
+        }
+        pool->free_events.push_back(pe.start);
+        pool->free_events.push_back(pe.stop);
+    }
+    std::lock_guard<std::mutex> g(pool->mu);
+    if (out) {
+        out->append_launches = pool->launches[kAppend];
+        out->decode_launches = pool->launches[kDecode];
+        out->merge_launches = pool->launches[kMerge];
+        out->launches = out->append_launches + out->decode_launches + out->merge_launches;
+        out->append_ms = pool->ms[kAppend];
+        out->decode_ms = pool->ms[kDecode];
+        out->merge_ms = pool->ms[kMerge];
+        out->timed_append = pool->timed[kAppend];
+        out->timed_decode = pool->timed[kDecode];
+        out->timed_merge = pool->timed[kMerge];
+    }
+    if (reset) {
+        for (int k = 0; k < kNumKinds; ++k) {
+            pool->launches[k] = 0;
+            pool->timed[k] = 0;
+            pool->ms[k] = 0.0;
+        }
+    }
+    return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,214 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 paged GQA decode-attention library
+ * (libpagedkv.so, CUDA kernels for sm_103a).
+ *
+ * The library keeps one layer's key/value cache in a fixed pool of
+ * fixed-size blocks in HBM, appends each step's new keys and values into
+ * their slots, and runs single-token decode attention for a batch of
+ * sequences that reach their blocks through per-sequence block tables, with
+ * grouped-query attention (n_q query heads share n_kv KV heads).
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" must point to GPU memory of the device the pool
+ *     was created on; "host" pointers to ordinary CPU memory.  The caller owns
+ *     every buffer it passes and keeps it alive until the work enqueued on
+ *     `stream` has finished.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls that take a stream only enqueue work and never
+ *     synchronise the host.
+ *   - A call returns PKV_OK or an error status.  Argument errors are found on
+ *     the host before anything is enqueued.  Range errors met on the device
+ *     (a slot or block id outside the pool, a context length beyond the block
+ *     table) skip the offending item and set a sticky bit read with
+ *     pkv_get_error(); kernels never trap.
+ *   - pkv_last_error_message() gives a one-line description of the last
+ *     failure on the calling thread.
+ *   - A pool is not safe to use from two host threads or two streams at once
+ *     (it owns one split-KV workspace).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_EINVAL = 1,        /* bad argument (null pointer, shape, alignment) */
+    PKV_ERANGE = 2,        /* a size outside what the call accepts */
+    PKV_ENOMEM = 3,        /* device allocation failed */
+    PKV_ECUDA = 4,         /* a CUDA runtime call failed (see message) */
+    PKV_EUNSUPPORTED = 5,  /* valid but unsupported configuration or device */
+    PKV_EDEVICE = 6        /* pkv_get_error: the device recorded range errors */
+} pkv_status;
+
+typedef enum {
+    PKV_BF16 = 0,      /* keys and values stored as bf16 */
+    PKV_FP8_E4M3 = 1   /* stored as FP8 E4M3 with a per-KV-head fp32 scale */
+} pkv_dtype;
+
+/* Bits of the sticky device error word (pkv_get_error). */
+#define PKV_DEVERR_SLOT_RANGE  0x1u  /* append: slot >= num_blocks * block_size */
+#define PKV_DEVERR_BLOCK_RANGE 0x2u  /* decode: block id outside [0, num_blocks) */
+#define PKV_DEVERR_CTX_RANGE   0x4u  /* decode: context_len < 0 or > W * block_size */
+#define PKV_DEVERR_TIMEOUT     0x8u  /* a bounded wait on the kernel's own copies ran out */
+
+typedef struct pkv_pool pkv_pool; /* opaque; owns its device memory */
+
+/* Where a pool's blocks live.  K and V are two separate device arrays, each
+ * laid out [num_blocks][n_kv][block_size][d_head]: element (blk, g, off, d)
+ * of either array sits at blk*stride_block + g*stride_head + off*stride_token
+ * + d (strides in elements), so one (block, KV head) tile is contiguous. */
+typedef struct {
+    void *k;                 /* device */
+    void *v;                 /* device */
+    int64_t stride_block;    /* n_kv * block_size * d_head */
+    int64_t stride_head;     /* block_size * d_head */
+    int64_t stride_token;    /* d_head */
+    int64_t num_blocks;
+    int32_t block_size;
+    int32_t n_kv;
+    int32_t d_head;
+    int32_t dtype;           /* pkv_dtype */
+    int64_t bytes_per_array; /* bytes of K (and, equally, of V) */
+} pkv_layout;
+
+/* Per-kernel timing gathered with CUDA events while timing is enabled. */
+typedef struct {
+    int64_t launches;        /* every kernel launch the library enqueued */
+    int64_t append_launches;
+    int64_t decode_launches;
+    int64_t merge_launches;
+    double append_ms;        /* summed event time of timed launches */
+    double decode_ms;
+    double merge_ms;
+    int64_t timed_append, timed_decode, timed_merge;
+} pkv_timing;
+
+/* Create a pool of `num_blocks` blocks of `block_size` token slots, for
+ * `n_kv` KV heads of `d_head` values, stored as `dtype`.  The pool splits the
+ * cache into fixed-size blocks that any sequence may own in any order
+ * ("KV cache, PagedAttention and FlashAttention", Problem 4, "The idea";
+ * "Memory Management in LLM Serving Systems", "Method 3: PagedAttention").
+ * One pool holds one layer.  Memory is allocated on the current CUDA device
+ * and zero-filled; the pool owns it.
+ * Supported: block_size == 16, d_head in {64, 128}, 1 <= n_kv <= 256.
+ * Errors: EINVAL (null out, non-positive sizes), EUNSUPPORTED (other block
+ * or head sizes, a device that is not sm_103), ENOMEM, ECUDA. */
+pkv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv, int32_t d_head,
+                          int32_t dtype, pkv_pool **out);
+
+/* Free the pool and everything it owns (synchronises the device first).
+ * NULL is accepted. */
+pkv_status kv_pool_destroy(pkv_pool *pool);
+
+/* FP8 pools: set the per-KV-head dequantisation scales from two host arrays
+ * of n_kv fp32 values (stored value = E4M3(x / scale), read back as
+ * E4M3 * scale).  Must be called before the first append or decode of an FP8
+ * pool; scales must be finite and > 0.  Changing them later does not
+ * rewrite stored bytes.  The pages name FP8 KV ("KV cache, PagedAttention
+ * and FlashAttention", Problem 3 trade-offs: FP8 halves the bytes of BF16);
+ * the per-head scale is this library's reading.  Errors: EINVAL. */
+pkv_status kv_pool_set_fp8_scales(pkv_pool *pool, const float *k_scale_host,
+                                  const float *v_scale_host);
+
+/* Report the pool's device pointers and layout (see pkv_layout). */
+pkv_status kv_pool_layout(const pkv_pool *pool, pkv_layout *out);
+
+/* Tokens per split-KV partition used by paged_decode_attention: 0 picks the
+ * default (512); otherwise a multiple of 64 in [64, 65536].  Errors: ERANGE. */
+pkv_status kv_pool_set_partition_tokens(pkv_pool *pool, int32_t tokens);
+
+/* Grow the pool's split-KV workspace now (it otherwise grows inside the
+ * first decode call that needs more), so that later decode calls with at
+ * most `batch` sequences, `n_q` query heads and `max_blocks_per_seq` table
+ * entries allocate nothing.  Errors: EINVAL, ENOMEM. */
+pkv_status kv_pool_reserve_workspace(pkv_pool *pool, int32_t batch, int32_t n_q,
+                                     int32_t max_blocks_per_seq);
+
+/* Append: write token t's key and value rows into slot slot_mapping[t] of
+ * the pool ("The KV Cache from First Principles", "Deriving the cache": each
+ * step computes one new key and value per KV head and appends them; "Prefill
+ * populates the cache" uses the same call with many tokens).
+ *   k_new, v_new  device bf16 [n_tokens][n_kv][d_head], 16-byte aligned.
+ *   slot_mapping  device int64 [n_tokens]; slot = physical block *
+ *                 block_size + offset ("KV cache, PagedAttention and
+ *                 FlashAttention", Problem 4, address arithmetic).  A negative
+ *                 slot skips the token; a slot >= num_blocks * block_size is
+ *                 skipped and sets PKV_DEVERR_SLOT_RANGE.  Two tokens with the
+ *                 same slot in one call leave either one (unspecified).
+ * FP8 pools store E4M3(fp32(x) / scale[g]) rounded to nearest even and
+ * saturated to +-448.  n_tokens == 0 is a no-op.
+ * Errors: EINVAL (null/misaligned pointers, n_tokens < 0, FP8 scales unset). */
+pkv_status paged_kv_append(pkv_pool *pool, const void *k_new, const void *v_new,
+                           const int64_t *slot_mapping, int64_t n_tokens, void *stream);
+
+/* Decode attention for one new query token per sequence:
+ *   out[b][h] = sum_p softmax_p(scale * q[b][h] . K_b[p][g]) V_b[p][g]
+ * over positions p < context_lens[b] of sequence b, with g = h / (n_q/n_kv)
+ * ("The KV Cache from First Principles", "Implementation" and
+ * "Grouped-query attention: the compromise").  K_b[p] lives in block
+ * block_tables[b][p / block_size] at offset p % block_size ("KV cache,
+ * PagedAttention and FlashAttention", Problem 4, "The idea": the kernel
+ * reads keys and values through the block table).  The result equals the
+ * plain softmax; internally the kernel keeps a running max and sum
+ * (same page, Problem 5, online softmax) and splits long sequences across
+ * thread blocks whose partial results are merged by their log-sum-exp
+ * (Problem 5, "Serving note").
+ *   q             device bf16 [batch][n_q][d_head], 16-byte aligned.
+ *   n_q           query heads; a multiple of the pool's n_kv with
+ *                 n_q / n_kv in {1, 2, 4, 8}.
+ *   block_tables  device int32 [batch][max_blocks_per_seq]; entries past
+ *                 ceil(context_len / block_size) are never read.  An entry
+ *                 that is read and lies outside [0, num_blocks) is skipped
+ *                 (its tokens count as masked) and sets
+ *                 PKV_DEVERR_BLOCK_RANGE.
+ *   context_lens  device int32 [batch]: tokens cached for each sequence,
+ *                 including the one appended this step.  0 gives a zero
+ *                 output row; values < 0 or > max_blocks_per_seq *
+ *                 block_size are clamped to that range and set
+ *                 PKV_DEVERR_CTX_RANGE.
+ *   scale         fp32 factor on q.k (normally 1/sqrt(d_head)).
+ *   out           device bf16 [batch][n_q][d_head], 16-byte aligned; rounded
+ *                 to nearest even from fp32.
+ * batch == 0 is a no-op.  Uses the pool's split-KV workspace, growing it
+ * (cudaMalloc, outside any stream capture) when the call needs more.
+ * Errors: EINVAL, EUNSUPPORTED (group size), ENOMEM, ECUDA. */
+pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int32_t n_q,
+                                  const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t *context_lens, int32_t batch, float scale,
+                                  void *out, void *stream);
+
+/* KV-cache bytes per token: 2 x layers x n_kv x d_head x bytes_per_value
+ * ("KV cache, PagedAttention and FlashAttention", Problem 3, "The concepts";
+ * "Memory Management in LLM Serving Systems", "KV cache sizing").
+ * bytes_per_value may be fractional (0.5 for 4-bit; scales not counted).
+ * Host arithmetic only.  Returns a negative value for negative inputs. */
+double kv_bytes_per_token(int32_t layers, int32_t n_kv, int32_t d_head, double bytes_per_value);
+
+/* Read the pool's sticky device error word into *bits (NULL allowed),
+ * synchronising the device; clear != 0 resets it.  Returns PKV_OK when no
+ * bit is set, PKV_EDEVICE when some are, or ECUDA. */
+pkv_status pkv_get_error(pkv_pool *pool, int32_t clear, uint32_t *bits);
+
+/* Timing: while enabled, the library records a CUDA event pair around every
+ * kernel it launches, on the launching stream.  pkv_timing_read synchronises
+ * those events, fills *out and, if reset != 0, clears the counters.  The
+ * launch counters count every launch whether or not timing is enabled. */
+pkv_status pkv_timing_enable(pkv_pool *pool, int32_t on);
+pkv_status pkv_timing_read(pkv_pool *pool, int32_t reset, pkv_timing *out);
+
+/* Static name of a status; never NULL. */
+const char *pkv_status_string(pkv_status s);
+
+/* Description of the last failure on this thread ("" if none). */
+const char *pkv_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -124,14 +124,16 @@ static void orc_e4m3_fill(void)
 /* Brute-force encoder: among all finite codes of the same sign as y, take
  * the one nearest to y; on an exact tie take the code whose mantissa LSB is
  * 0 (neighbouring codes of one sign differ by one in the code, so "even code"
- * is "even mantissa").  Anything above 448 in magnitude lands on +-448
- * because only finite codes are candidates.  The sign of zero is kept.  NaN
- * maps to the NaN code 0x7F. */
+ * is "even mantissa").  Anything above 448 in magnitude, infinity
+ * included, lands on +-448 because only finite codes are candidates.  The
+ * sign of zero is kept.  NaN maps to the NaN code 0x7F. */
 uint8_t orc_e4m3_encode(float y)
 {
     pthread_once(&orc_e4m3_once, orc_e4m3_fill);
     if (isnan(y)) return 0x7F;
     int want_sign = signbit(y) ? 1 : 0;
+    /* An infinite quotient is beyond the largest finite value too. */
+    if (isinf(y)) return (uint8_t)((want_sign << 7) | 0x7E);
     uint8_t best = (uint8_t)(want_sign << 7);
     double best_dist = INFINITY;
     for (int c = 0; c < 256; ++c) {

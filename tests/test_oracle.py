@@ -124,6 +124,10 @@ def test_e4m3_landmarks():
     assert oracle.e4m3_encode(1e6) == 0x7E
     assert oracle.e4m3_encode(-1e6) == 0xFE
     assert oracle.e4m3_encode(449.0) == 0x7E
+    assert oracle.e4m3_encode(float("inf")) == 0x7E
+    assert oracle.e4m3_encode(float("-inf")) == 0xFE
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+    assert oracle.e4m3_encode(-1e-30) == 0x80
     assert oracle.e4m3_encode(0.0) == 0x00
     assert oracle.e4m3_encode(-0.0) == 0x80
 
