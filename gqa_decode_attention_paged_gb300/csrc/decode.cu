@@ -584,7 +584,14 @@ static pkv_status launch_decode(pkv_pool *pool, const DecodeArgs &a, int nps, cu
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        // The opt-in limit covers static plus dynamic shared memory.
+        int optin = 0;
+        cudaFuncAttributes fa;
+        attr_err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, pool->device);
+        if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, kern);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            optin - (int)fa.sharedSizeBytes);
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(decode)");
     const size_t smem = C::smem_bytes(a.batch);

@@ -132,8 +132,11 @@ uint8_t orc_e4m3_encode(float y)
     pthread_once(&orc_e4m3_once, orc_e4m3_fill);
     if (isnan(y)) return 0x7F;
     int want_sign = signbit(y) ? 1 : 0;
-    /* An infinite quotient is beyond the largest finite value too. */
-    if (isinf(y)) return (uint8_t)((want_sign << 7) | 0x7E);
+    /* Saturation: a magnitude at or beyond the largest finite value (448),
+     * infinity included, is +-448.  Stated directly rather than left to the
+     * nearest-code search, whose fp64 distances stop telling codes apart once
+     * |y| passes about 2^53 times their spacing. */
+    if (fabs((double)y) >= 448.0) return (uint8_t)((want_sign << 7) | 0x7E);
     uint8_t best = (uint8_t)(want_sign << 7);
     double best_dist = INFINITY;
     for (int c = 0; c < 256; ++c) {

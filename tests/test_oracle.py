@@ -128,6 +128,8 @@ def test_e4m3_landmarks():
     assert oracle.e4m3_encode(float("-inf")) == 0xFE
     assert oracle.e4m3_encode(float("nan")) == 0x7F
     assert oracle.e4m3_encode(-1e-30) == 0x80
+    for big in (1.16e18, 3.0e38, 2.0 ** 100, 464.0, 500.0):
+        assert oracle.e4m3_encode(big) == 0x7E and oracle.e4m3_encode(-big) == 0xFE
     assert oracle.e4m3_encode(0.0) == 0x00
     assert oracle.e4m3_encode(-0.0) == 0x80
 
