@@ -510,7 +510,8 @@ def run_ours(args):
                        kv_bytes_logical=acct["kv_logical"], kv_bytes_unique=acct["kv_unique"],
                        l2=("flushed (512 MB write) between steps" if args.flush_l2 else
                            f"inputs larger than L2: {acct['kv_unique'] / 1e6:.0f} MB of KV per call vs 129 MB L2"),
-                       partition_tokens=args.partition_tokens or 512),
+                       work_split=(f"slices of {args.partition_tokens} tokens" if args.partition_tokens
+                                   else "one equal slice of the batch's blocks per resident CTA")),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "bytes_per_launch": step_bytes, "avg_launch_ms": dec_ms, "peak_source": peak_note,

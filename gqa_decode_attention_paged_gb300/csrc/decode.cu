@@ -7,34 +7,42 @@
 //   g = h / (n_q / n_kv), p < context_len[b], K/V of position p in block
 //   block_table[b][p / 16] at offset p % 16.
 //
-// How (GB300 design, see the file-level notes in the header):
-//   * Work unit = (sequence, KV head, partition of `part_blocks` blocks).
-//     Long sequences split across thread blocks ("Serving note" of Problem 5;
-//     "Memory Management in LLM Serving Systems", FlashAttention-2: parallelise
-//     over the sequence dimension).  A persistent grid of
-//     (#SMs x resident CTAs) walks the units; the partition count of every
-//     sequence comes from an in-kernel prefix sum over context_lens, so the
-//     host never reads lengths and the call never synchronises.
-//   * Each CTA has 4 warps.  Each warp owns a ring of shared-memory stages;
-//     lane 0 fetches the (block, KV head) K tile and V tile of its next blocks
-//     with 1-D bulk TMA copies (cp.async.bulk, evict-first L2 hint) that
-//     complete on an mbarrier.  Every wait is bounded.
+// How:
+//   * Work list.  The (sequence, KV head, block) items of the whole batch form
+//     one stream ordered by sequence, head, block.  It is cut into equal
+//     slices, one per warp of a persistent grid (#SMs x resident CTAs x warps
+//     per CTA), so every warp gets the same number of blocks whatever the
+//     length mix, and long sequences are split across warps and SMs ("KV
+//     cache, PagedAttention and FlashAttention", Problem 5, "Serving note";
+//     "Memory Management in LLM Serving Systems", FlashAttention-2:
+//     parallelise over the sequence dimension).  Block counts per sequence
+//     come from an in-kernel prefix sum over context_lens, so the host never
+//     reads lengths and the call never synchronises.
+//   * Warps are independent: after the prologue there is no CTA barrier.  A
+//     warp's slice meets one or more (sequence, head) runs; each meeting is a
+//     "piece".  The warp owns a ring of shared-memory stages that its lane 0
+//     fills with tiled TMA copies (cp.async.bulk.tensor, 128-byte swizzle,
+//     evict-first) of a block's K and V tiles, completing on an mbarrier;
+//     block-table entries are fetched a segment ahead with one coalesced
+//     load.  Every wait is bounded.
 //   * All G query heads of the group are served from one read of each tile
-//     ("Memory Management in LLM Serving Systems", FlashAttention: several
-//     query heads against the same KV block cut KV reads by the group factor).
-//   * Scores: each lane dots 8 elements of a key with the G query rows held
-//     in registers, then a transpose-reduce over the key's lanes leaves one
-//     (token, head) score per lane.  Online softmax in fp32 with exp2 (q is
-//     pre-scaled by scale*log2 e): running max m and sum l per head, the
-//     accumulator rescaled only when the max moves (Problem 5's recurrence;
-//     FlashAttention-2's deferred 1/l).
-//   * P.V: each lane owns D/32 output columns of all G heads.
-//   * Unit end: the 4 warps' (m, l, o) merge in shared memory; a sequence with
-//     one partition writes bf16 `out` directly, otherwise (m, l, o) go to the
-//     workspace and merge_kernel combines partitions by log-sum-exp:
-//     M = max m_p, L = sum 2^(m_p-M) l_p, out = sum 2^(m_p-M) o_p / L.
-//   * FP8 KV: tiles are E4M3, converted in registers; the K scale is folded
-//     into q and the V scale into the final normalisation.
+//     ("Memory Management in LLM Serving Systems", FlashAttention: query
+//     heads sharing a KV head cut KV reads by the group factor): they are the
+//     N dimension of 16x8x16 tensor-core MMAs, S^T = K Q^T then O^T += V^T P^T.
+//   * Online softmax in fp32 with exp2 (scores pre-scaled by scale*log2 e):
+//     running max and sum per head, the accumulator rescaled only when the max
+//     moves, 1/l applied once at the end (Problem 5's recurrence;
+//     FlashAttention-2's deferred normalisation).
+//   * Piece end: a piece that is its whole (sequence, head) writes bf16 `out`.
+//     Otherwise it stores (m, l, O) in the workspace and bumps that
+//     (sequence, head)'s counter; the warp that completes the count merges
+//     all pieces, in slice order, by log-sum-exp, M = max m_p,
+//     L = sum 2^(m_p-M) l_p, out = sum 2^(m_p-M) O_p / L, and resets the
+//     counter.  No warp ever waits for another, and the result does not
+//     depend on which warp finished last.
+//   * FP8 KV: tiles are E4M3, converted to f16 pairs in registers for f16
+//     MMAs; the K scale is folded into the score scale and the V scale into
+//     the final normalisation.
 #include <algorithm>
 #include <mutex>
 
@@ -42,14 +50,11 @@
 
 namespace pkv {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
 constexpr int kMaxBatch = 8192;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeArgs {
-    const uint8_t *k_pool, *v_pool;
     int64_t num_blocks;
     int n_kv, n_q;
     const __nv_bfloat16 *q;
@@ -60,34 +65,61 @@ struct DecodeArgs {
     float qscale;          // scale * log2(e)
     const float *scales;   // FP8: [2 * n_kv] (k then v)
     __nv_bfloat16 *out;
-    int32_t *part_start;   // workspace [batch + 1]
-    float2 *ws_ml;         // workspace [P][n_kv][G] (max in log2 units, sum)
-    float *ws_o;           // workspace [P][n_kv][G][D], unnormalised
-    int part_blocks;       // blocks per partition (multiple of kWarps)
+    int *counters;         // workspace [batch * n_kv], zero between calls
+    float2 *ws_ml;         // workspace [slots][G] (max in log2 units, sum)
+    float *ws_o;           // workspace [slots][G][D], unnormalised
+    int slice_blocks;      // blocks per slice; 0 = ceil(total / all warps)
     unsigned *err;
+};
+
+// Shared-memory geometry of one (block, KV head) tile as the TMA boxes lay it
+// out: NREG boxes of 16 rows x BOXB bytes (128-byte rows, or 64 bytes for
+// FP8 with d_head 64), each box swizzled within its own region.
+template <int D, bool FP8>
+struct Geo {
+    static constexpr int E = FP8 ? 1 : 2;
+    static constexpr int ROWB = D * E;                    // bytes of one token row
+    static constexpr int BOXB = ROWB > 128 ? 128 : ROWB;  // bytes of one box row
+    static constexpr int NREG = ROWB / BOXB;              // boxes per tile
+    static constexpr int RGN = kBlockSize * BOXB;         // bytes per box
+    static constexpr int TILE = NREG * RGN;               // K tile (or V tile) bytes
+    static constexpr int STAGE = 2 * TILE;                // K tile + V tile
+    static constexpr int BOX_ELEMS = BOXB / E;
+};
+
+// Warps per CTA and shared memory for their copy rings, per instantiation.
+// More warps hide the per-block dependency chain; each warp keeps at least
+// two stages so that one copy is in flight while it computes.  (Build-time
+// overrides PKV_DECODE_WARPS / PKV_RING_KIB exist for tuning sweeps.)
+template <int D, int G, bool FP8>
+struct Tune {
+#if defined(PKV_DECODE_WARPS) && defined(PKV_RING_KIB)
+    static constexpr int NW = PKV_DECODE_WARPS;
+    static constexpr int RING_KIB = PKV_RING_KIB;
+#else
+    // 4 warps, 48 KiB of stages: bf16 d128 keeps 2 stages of 8 KiB per warp
+    // (3 CTAs = 12 warps per SM), FP8 d128 3 stages of 4 KiB (4 CTAs per SM).
+    // Swept on GB300 over 2..8 warps and 32..128 KiB.
+    static constexpr int NW = 4;
+    static constexpr int RING_KIB = 48;
+#endif
 };
 
 template <int D, int G, bool FP8>
 struct Cfg {
-    static constexpr int E = FP8 ? 1 : 2;
-    static constexpr int kTileBytes = kBlockSize * D * E;   // one (block, head) tile
-    static constexpr int kStageBytes = 2 * kTileBytes;      // K tile + V tile
-    static constexpr int kStages = std::min(8, std::max(2, 16384 / kStageBytes));
-    static constexpr int LPT = D / 8;        // lanes per key row in the score phase
-    static constexpr int TPR = 32 / LPT;     // keys per round
-    static constexpr int SPAN = LPT / G;     // lanes sharing one head after the halving
-    static constexpr int DPL = D / 32;       // output columns per lane in the P.V phase
-    // shared-memory layout (bytes)
-    static constexpr int kRing = kWarps * kStages * kStageBytes;
+    using Gm = Geo<D, FP8>;
+    static constexpr int NW = Tune<D, G, FP8>::NW;
+    static constexpr int kThreads = NW * 32;
+    static constexpr int kStages = std::min(8, std::max(2, Tune<D, G, FP8>::RING_KIB * 1024 / (NW * Gm::STAGE)));
+    // shared-memory layout (bytes from a 1024-byte aligned base)
+    static constexpr int kRing = NW * kStages * Gm::STAGE;
     static constexpr int kBars = kRing;
-    static constexpr int kPhys = kBars + kWarps * kStages * 8;
-    static constexpr int kSp = kPhys + kWarps * kStages * 4;
-    static constexpr int kMergeM = kSp + kWarps * kBlockSize * 8 * 4;
-    static constexpr int kMergeL = kMergeM + kWarps * 8 * 4;
-    static constexpr int kMergeO = kMergeL + kWarps * 8 * 4;
-    static constexpr int kPartStart = kMergeO + kWarps * G * D * 4;
-    static size_t smem_bytes(int batch) { return (size_t)kPartStart + 4 * (size_t)(batch + 1); }
-    static_assert(G <= LPT, "group larger than lanes per key");
+    static constexpr int kPhys = kBars + NW * kStages * 8;
+    static constexpr int kScratch = kPhys + NW * kStages * 4;  // [NW][16] floats: merge max/sum per head
+    static constexpr int kWarpTot = kScratch + NW * 16 * 4;
+    static constexpr int kPs = kWarpTot + 4 * NW;  // ps[batch + 1]
+    static size_t smem_bytes(int batch) { return 1024 + (size_t)kPs + 4 * (size_t)(batch + 1); }
+    static_assert(G <= 8, "at most 8 query heads per KV head");
 };
 
 __device__ __forceinline__ int clamp_ctx(int c, int W, unsigned *err, bool report)
@@ -100,20 +132,18 @@ __device__ __forceinline__ int clamp_ctx(int c, int W, unsigned *err, bool repor
     return c;
 }
 
-// Exclusive prefix sum of partitions per sequence into ps[0..batch].
-__device__ void scan_partitions(const DecodeArgs &a, int32_t *ps)
+// Exclusive prefix sum of block counts per sequence into ps[0..batch];
+// warp_tot is scratch for NW ints.
+template <int NW>
+__device__ void scan_blocks(const DecodeArgs &a, int32_t *ps, int *warp_tot)
 {
-    __shared__ int warp_tot[kWarps];
+    constexpr int NT = NW * 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int carry = 0;
-    for (int base = 0; base < a.batch; base += kThreads) {
+    for (int base = 0; base < a.batch; base += NT) {
         const int b = base + tid;
         int n = 0;
-        if (b < a.batch) {
-            const int c = clamp_ctx(a.context_lens[b], a.W, a.err, blockIdx.x == 0);
-            const int nblk = (c + kBlockSize - 1) / kBlockSize;
-            n = (nblk + a.part_blocks - 1) / a.part_blocks;
-        }
+        if (b < a.batch) n = (clamp_ctx(a.context_lens[b], a.W, a.err, blockIdx.x == 0) + kBlockSize - 1) / kBlockSize;
         int x = n;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -124,7 +154,7 @@ __device__ void scan_partitions(const DecodeArgs &a, int32_t *ps)
         __syncthreads();
         int before = 0, tot = 0;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
             const int t = warp_tot[w];
             before += (w < warp) ? t : 0;
             tot += t;
@@ -137,447 +167,624 @@ __device__ void scan_partitions(const DecodeArgs &a, int32_t *ps)
     __syncthreads();
 }
 
-struct Unit {
-    int b, g, pidx, nparts, j0, j1, C;
+// The stream: item f (0 <= f < total = n_kv * ps[batch]) is block j of head g
+// of sequence b with f = n_kv * ps[b] + g * nblk_b + j.  Slice s covers items
+// [s * share, (s + 1) * share); warp `me` of the grid takes slices me,
+// me + n_warps, ...
+struct Stream {
+    const int32_t *ps;
+    int batch, n_kv, total, share, n_slices, n_warps;
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const DecodeArgs &a, const int32_t *ps)
+// One piece: blocks [j0, j1) of (b, g), starting at stream item f, in slice.
+struct Piece {
+    int b, g, j0, j1, nblk, f, slice;
+};
+
+__device__ __forceinline__ Piece locate(const Stream &st, int f, int slice)
 {
-    Unit r;
-    r.pidx = u / a.n_kv;
-    r.g = u - r.pidx * a.n_kv;
-    int lo = 0, hi = a.batch - 1;  // largest b with ps[b] <= pidx
+    Piece p;
+    int lo = 0, hi = st.batch - 1;  // largest b with n_kv * ps[b] <= f
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (ps[mid] <= r.pidx) lo = mid; else hi = mid - 1;
+        if (st.n_kv * st.ps[mid] <= f) lo = mid; else hi = mid - 1;
     }
-    r.b = lo;
-    r.nparts = ps[lo + 1] - ps[lo];
-    r.C = clamp_ctx(a.context_lens[lo], a.W, a.err, false);
-    const int nblk = (r.C + kBlockSize - 1) / kBlockSize;
-    r.j0 = (r.pidx - ps[lo]) * a.part_blocks;
-    r.j1 = min(r.j0 + a.part_blocks, nblk);
-    return r;
+    p.b = lo;
+    p.nblk = st.ps[lo + 1] - st.ps[lo];
+    const int r = f - st.n_kv * st.ps[lo];
+    p.g = r / p.nblk;
+    p.j0 = r - p.g * p.nblk;
+    const int slice_end = min(st.total, (slice + 1) * st.share);
+    p.j1 = min(p.nblk, p.j0 + (slice_end - f));
+    p.f = f;
+    p.slice = slice;
+    return p;
 }
 
-// The sequence of (unit, block) items one warp consumes, in order.
-struct Iter {
-    int u, j, j1, b, g;
-};
-
-__device__ __forceinline__ bool iter_next(Iter &it, int warp, int total_units, const DecodeArgs &a,
-                                          const int32_t *ps)
+// The piece after p in this warp's walk.
+__device__ __forceinline__ bool next_piece(const Stream &st, Piece &p)
 {
-    it.j += kWarps;
-    while (it.j >= it.j1) {
-        it.u += gridDim.x;
-        if (it.u >= total_units) return false;
-        const Unit un = decode_unit(it.u, a, ps);
-        it.b = un.b;
-        it.g = un.g;
-        it.j = un.j0 + warp;
-        it.j1 = un.j1;
+    int f = p.f + (p.j1 - p.j0);
+    int slice = p.slice;
+    if (f >= min(st.total, (slice + 1) * st.share)) {
+        slice += st.n_warps;
+        if (slice >= st.n_slices) return false;
+        f = slice * st.share;
     }
+    p = locate(st, f, slice);
     return true;
 }
 
-// 8 consecutive stored elements -> fp32.
-template <bool FP8>
-__device__ __forceinline__ void load8(const uint8_t *p, float (&f)[8])
+__device__ __forceinline__ bool first_piece(const Stream &st, int me, Piece &p)
 {
-    if constexpr (!FP8) {
-        const uint4 r = *reinterpret_cast<const uint4 *>(p);
-        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 x = bf16x2_to_f32x2(w[i]);
-            f[2 * i] = x.x;
-            f[2 * i + 1] = x.y;
+    if (me >= st.n_slices) return false;
+    p = locate(st, me * st.share, me);
+    return true;
+}
+
+// The producer walks the warp's blocks in segments of at most 32 consecutive
+// blocks j .. j+n-1 of one piece.  One coalesced load fetches a segment's
+// block-table entries (lane k holds block j+k's), one segment ahead of use,
+// so no table read sits in front of a copy.
+struct Seg {
+    Piece p;
+    int j, n;
+    bool live;
+};
+
+__device__ __forceinline__ void seg_first(Seg &s, const Stream &st, int me)
+{
+    s.live = first_piece(st, me, s.p);
+    s.j = s.live ? s.p.j0 : 0;
+    s.n = s.live ? min(32, s.p.j1 - s.j) : 0;
+}
+
+__device__ __forceinline__ void seg_next(Seg &s, const Stream &st)
+{
+    if (!s.live) return;
+    s.j += s.n;
+    if (s.j >= s.p.j1) {
+        s.live = next_piece(st, s.p);
+        if (!s.live) {
+            s.n = 0;
+            return;
         }
+        s.j = s.p.j0;
+    }
+    s.n = min(32, s.p.j1 - s.j);
+}
+
+__device__ __forceinline__ int seg_load(const Seg &s, int lane, const DecodeArgs &a)
+{
+    return (s.live && lane < s.n) ? a.block_tables[(int64_t)s.p.b * a.W + s.j + lane] : -1;
+}
+
+// ---------------------------------------------------------------------------
+// Warp-level tensor-core helpers (16x8x16 MMA, bf16 or f16 in, fp32 out)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+template <bool F16>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    if constexpr (F16)
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+                     "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                     : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+                     "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                     : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                     : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 matrix of 16-bit values held one row-pair per thread.
+__device__ __forceinline__ uint32_t movm_t(uint32_t x)
+{
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Four E4M3 bytes -> two f16x2 words (bytes 0,1 -> lo; bytes 2,3 -> hi); exact.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t &lo, uint32_t &hi)
+{
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    if constexpr (F16) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
     } else {
-        const uint2 r = *reinterpret_cast<const uint2 *>(p);
-        const uint32_t w[2] = {r.x, r.y};
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float2 lo = e4m3x2_to_f32x2(w[i] & 0xffffu);
-            const float2 hi = e4m3x2_to_f32x2(w[i] >> 16);
-            f[4 * i] = lo.x;
-            f[4 * i + 1] = lo.y;
-            f[4 * i + 2] = hi.x;
-            f[4 * i + 3] = hi.y;
-        }
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
     }
 }
 
-// N (= 2 or 4) consecutive stored elements -> fp32.
-template <bool FP8, int N>
-__device__ __forceinline__ void loadN(const uint8_t *p, float (&f)[N])
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
 {
-    if constexpr (!FP8) {
-        if constexpr (N == 4) {
-            const uint2 r = *reinterpret_cast<const uint2 *>(p);
-            const float2 a = bf16x2_to_f32x2(r.x), b = bf16x2_to_f32x2(r.y);
-            f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-        } else {
-            const float2 a = bf16x2_to_f32x2(*reinterpret_cast<const uint32_t *>(p));
-            f[0] = a.x; f[1] = a.y;
-        }
-    } else {
-        if constexpr (N == 4) {
-            const uint32_t r = *reinterpret_cast<const uint32_t *>(p);
-            const float2 a = e4m3x2_to_f32x2(r & 0xffffu), b = e4m3x2_to_f32x2(r >> 16);
-            f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-        } else {
-            const float2 a = e4m3x2_to_f32x2(*reinterpret_cast<const uint16_t *>(p));
-            f[0] = a.x; f[1] = a.y;
-        }
-    }
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
 }
 
-// Halving steps of the transpose-reduce: N values per lane, exchanged across
-// lane bit OFF; the upper lane keeps the upper half.  After log2(G) steps
-// lane `sub` holds head sub / SPAN, summed over its partner lanes.
-template <int N, int OFF, int G>
-__device__ __forceinline__ void halve(float (&v)[G], int lane)
+__device__ __forceinline__ uint2 lds64(uint32_t addr)
 {
-    if constexpr (N > 1) {
-        const bool upper = (lane & OFF) != 0;
-#pragma unroll
-        for (int i = 0; i < N / 2; ++i) {
-            const float send = upper ? v[i] : v[i + N / 2];
-            const float keep = upper ? v[i + N / 2] : v[i];
-            v[i] = keep + __shfl_xor_sync(kFull, send, OFF);
-        }
-        halve<N / 2, OFF / 2, G>(v, lane);
-    }
+    uint2 v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
 }
 
+// Byte offset inside a TMA box region (aligned to its swizzle atom) after the
+// box's swizzle: 16-byte chunk index XOR the 128-byte line index (mod 8) for
+// 128-byte rows, XOR (line index mod 4) for 64-byte rows.
+template <int BOXB>
+__device__ __forceinline__ uint32_t swz(uint32_t off)
+{
+    if constexpr (BOXB == 128) return off ^ ((off >> 3) & 0x70u);
+    else return off ^ ((off >> 3) & 0x30u);
+}
+
+// q rows of one (sequence, KV head) group as m16n8k16 B fragments: thread
+// (g8, c4) holds head g8's pairs of d for every k-step (zero for padding
+// heads g8 >= G).  bf16 KV: k-step ks covers d 16ks + {2c, 2c+1} and
+// 16ks + 8 + {2c, 2c+1}.  FP8 KV (f16 MMA): k-step 2kk+j covers
+// d 32kk + 8c + 4j + {0,1} and {2,3}, the order the E4M3 K fragments use.
 template <int D, int G, bool FP8>
-__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeArgs a)
+__device__ __forceinline__ void load_q_frags(const DecodeArgs &a, int b, int g, int g8, int c4,
+                                             uint32_t (&qf)[D / 16][2])
+{
+    const bool live = g8 < G;
+    const __nv_bfloat16 *qrow = a.q + ((int64_t)b * a.n_q + g * G + (live ? g8 : 0)) * D;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        if constexpr (!FP8) {
+            qf[ks][0] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c4) : 0u;
+            qf[ks][1] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * c4) : 0u;
+        } else {
+            const int d0 = 32 * (ks >> 1) + 8 * c4 + 4 * (ks & 1);
+            const uint2 r = live ? *reinterpret_cast<const uint2 *>(qrow + d0) : make_uint2(0, 0);
+            const float2 x0 = bf16x2_to_f32x2(r.x), x1 = bf16x2_to_f32x2(r.y);
+            qf[ks][0] = pack2<true>(x0.x, x0.y);
+            qf[ks][1] = pack2<true>(x1.x, x1.y);
+        }
+    }
+}
+
+// Log-sum-exp merge of the n pieces of (b, g), stored in workspace slots
+// s_first + b*n_kv + g, ..., in slice order, by one warp:
+//   M = max m_p, L = sum 2^(m_p - M) l_p, out = sum 2^(m_p - M) O_p / L.
+// Lanes first split the pieces to get M and L per head (warp reductions, kept
+// in `scratch`), then each lane sums 4-column chunks of O over the pieces with
+// independent loads.  Reads go to L2 (other SMs wrote the pieces).
+template <int D, int G>
+__device__ __noinline__ void merge_pieces(const DecodeArgs &a, int b, int g, int s_first, int n, int lane,
+                                          float *scratch)
+{
+    __threadfence();
+    const int64_t base = (int64_t)s_first + (int64_t)b * a.n_kv + g;  // slot of piece 0
+    float M[G], L[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        M[h] = -INFINITY;
+        L[h] = 0.0f;
+    }
+    for (int p = lane; p < n; p += 32) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], __ldcg(&a.ws_ml[(base + p) * G + h]).x);
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) M[h] = fmaxf(M[h], __shfl_xor_sync(kFull, M[h], off));
+    for (int p = lane; p < n; p += 32) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float2 v = __ldcg(&a.ws_ml[(base + p) * G + h]);
+            if (M[h] != -INFINITY) L[h] = fmaf(exp2f(v.x - M[h]), v.y, L[h]);
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) L[h] += __shfl_xor_sync(kFull, L[h], off);
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            scratch[h] = M[h];
+            scratch[8 + h] = L[h];
+        }
+    }
+    __syncwarp();
+    constexpr int CHUNKS = G * D / 4;  // float4 chunks of the G x D output
+    __nv_bfloat16 *ob = a.out + ((int64_t)b * a.n_q + g * G) * D;
+    for (int q = lane; q < CHUNKS; q += 32) {
+        const int h = (q * 4) / D;
+        const float Mh = scratch[h], Lh = scratch[8 + h];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (Mh != -INFINITY) {
+#pragma unroll 4
+            for (int p = 0; p < n; ++p) {
+                const float sc = exp2f(__ldcg(&a.ws_ml[(base + p) * G + h]).x - Mh);
+                const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.ws_o + (base + p) * G * D) + q);
+                acc.x = fmaf(sc, x.x, acc.x);
+                acc.y = fmaf(sc, x.y, acc.y);
+                acc.z = fmaf(sc, x.z, acc.z);
+                acc.w = fmaf(sc, x.w, acc.w);
+            }
+        }
+        const float r = Lh > 0.0f ? 1.0f / Lh : 0.0f;
+        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * r, acc.y * r);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * r, acc.w * r);
+        uint2 pk = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+        *reinterpret_cast<uint2 *>(ob + q * 4) = pk;
+    }
+    if (lane == 0) a.counters[b * a.n_kv + g] = 0;
+}
+
+// Decode kernel: per-warp TMA ring, tensor-core scores and P.V.
+//
+// Per 16-token block a warp computes S^T[16 tokens x 8 heads] = K . Q^T with
+// m16n8k16 MMAs (the G <= 8 query heads of the group are the N dimension,
+// padded with zero rows of q), runs the online softmax on the accumulator
+// fragments (thread: tokens g, g+8; heads 2c, 2c+1), turns P^T into the
+// B operand with movmatrix, and accumulates O^T[d x heads] += V^T . P^T.
+// bf16 KV: fragments come from ldmatrix (.trans for V) on the swizzled tiles.
+// FP8 KV: bytes are read with 32/64-bit shared loads and converted to f16
+// pairs in registers; the MMA's k (and, for V, its m) order is a fixed
+// permutation of d applied identically to both operands and undone when the
+// output is written, so the products are unchanged.
+template <int D, int G, bool FP8>
+__global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, DecodeArgs a)
 {
     using C = Cfg<D, G, FP8>;
+    using Gm = typename C::Gm;
     constexpr int S = C::kStages;
-    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int NW = C::NW;
+    constexpr int NT = D / 16;  // 16-wide MMA tiles along d
+    constexpr int kThreads = C::kThreads;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint8_t *ring = smem + warp * S * C::kStageBytes;
+    const int g8 = lane >> 2, c4 = lane & 3;  // MMA fragment coordinates
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *ring = smem + warp * S * Gm::STAGE;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBars) + warp * S;
     int *phys_st = reinterpret_cast<int *>(smem + C::kPhys) + warp * S;
-    float *sp = reinterpret_cast<float *>(smem + C::kSp) + warp * kBlockSize * 8;
-    float *merge_m = reinterpret_cast<float *>(smem + C::kMergeM);
-    float *merge_l = reinterpret_cast<float *>(smem + C::kMergeL);
-    float *merge_o = reinterpret_cast<float *>(smem + C::kMergeO);
-    int32_t *ps = reinterpret_cast<int32_t *>(smem + C::kPartStart);
+    int *warp_tot = reinterpret_cast<int *>(smem + C::kWarpTot);
+    int32_t *ps = reinterpret_cast<int32_t *>(smem + C::kPs);
+    float *scratch = reinterpret_cast<float *>(smem + C::kScratch) + warp * 16;
 
     if (tid == 0) {
-        for (int i = 0; i < kWarps * S; ++i)
-            mbar_init(reinterpret_cast<uint64_t *>(smem + C::kBars) + i, 1);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        for (int i = 0; i < NW * S; ++i) mbar_init(reinterpret_cast<uint64_t *>(smem + C::kBars) + i, 1);
         fence_mbarrier_init();
     }
-    scan_partitions(a, ps);  // ends with __syncthreads
-    const int total_units = ps[a.batch] * a.n_kv;
-    if (blockIdx.x == 0)
-        for (int i = tid; i <= a.batch; i += kThreads) a.part_start[i] = ps[i];
-    // Sequences with no cached tokens get a zero output row.
-    for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
+    scan_blocks<NW>(a, ps, warp_tot);  // ends with __syncthreads; the last CTA-wide barrier
+    Stream st;
+    st.ps = ps;
+    st.batch = a.batch;
+    st.n_kv = a.n_kv;
+    st.total = a.n_kv * ps[a.batch];
+    st.n_warps = (int)gridDim.x * NW;
+    st.share = a.slice_blocks > 0 ? a.slice_blocks : max(1, (st.total + st.n_warps - 1) / st.n_warps);
+    st.n_slices = (st.total + st.share - 1) / st.share;
+    const int me = (int)blockIdx.x * NW + warp;
+    for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {  // empty sequences: zero rows
         if (ps[b + 1] != ps[b]) continue;
         uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)b * a.n_q * D);
         for (int i = tid; i < a.n_q * D / 8; i += kThreads) o[i] = make_uint4(0, 0, 0, 0);
     }
 
     const uint64_t policy = l2_policy_evict_first();
-    const int sub = lane % C::LPT, tsub = lane / C::LPT;  // score phase
-    const int hl = lane & 7, tq = lane >> 3;              // softmax phase
     bool aborted = false;
-    int drain_from = -1;  // first item whose copy may still be in flight after a timeout
+    int drain_from = -1;
 
-    // Producer state (uniform across the warp; lane 0 issues).
-    Iter pit;
-    pit.u = blockIdx.x - gridDim.x;
-    pit.j = 0;
-    pit.j1 = 0;
-    pit.b = pit.g = 0;
-    bool prod_done = false;
-    int n_issued = 0;
-    auto issue = [&](int n) {
-        const int st = n % S;
+    // ---- producer (uniform across the warp; lane 0 issues the copies) ----
+    Seg cur;
+    seg_first(cur, st, me);
+    int tab_cur = seg_load(cur, lane, a);
+    Seg nxt = cur;
+    seg_next(nxt, st);
+    int tab_nxt = seg_load(nxt, lane, a);
+    int seg_k = 0, n_issued = 0;
+    auto issue_next = [&]() {
+        if (!cur.live) return;
+        const int phys = __shfl_sync(kFull, tab_cur, seg_k);
+        const int sidx = n_issued % S;
         if (lane == 0) {
-            const int64_t phys = a.block_tables[(int64_t)pit.b * a.W + pit.j];
             const bool ok = phys >= 0 && phys < a.num_blocks;
-            phys_st[st] = ok ? (int)phys : -1;
+            phys_st[sidx] = ok ? phys : -1;
             if (ok) {
-                const int64_t tile = (phys * a.n_kv + pit.g) * (int64_t)C::kTileBytes;
-                uint8_t *dst = ring + st * C::kStageBytes;
+                const int y = (int)(((int64_t)phys * a.n_kv + cur.p.g) * kBlockSize);
+                uint8_t *dst = ring + sidx * Gm::STAGE;
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(&bars[st], 2 * C::kTileBytes);
-                bulk_g2s(dst, a.k_pool + tile, C::kTileBytes, &bars[st], policy);
-                bulk_g2s(dst + C::kTileBytes, a.v_pool + tile, C::kTileBytes, &bars[st], policy);
+                mbar_arrive_expect_tx(&bars[sidx], Gm::STAGE);
+#pragma unroll
+                for (int r = 0; r < Gm::NREG; ++r) {
+                    tma_load_2d(dst + r * Gm::RGN, &tm_k, r * Gm::BOX_ELEMS, y, &bars[sidx], policy);
+                    tma_load_2d(dst + Gm::TILE + r * Gm::RGN, &tm_v, r * Gm::BOX_ELEMS, y, &bars[sidx], policy);
+                }
             } else {
                 atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
-                mbar_arrive(&bars[st]);
+                mbar_arrive(&bars[sidx]);
             }
+        }
+        ++n_issued;
+        if (++seg_k == cur.n) {
+            cur = nxt;
+            tab_cur = tab_nxt;
+            seg_k = 0;
+            seg_next(nxt, st);
+            tab_nxt = seg_load(nxt, lane, a);
         }
     };
-    for (; n_issued < S; ++n_issued) {
-        if (!iter_next(pit, warp, total_units, a, ps)) {
-            prod_done = true;
-            break;
-        }
-        issue(n_issued);
-    }
+    for (int i = 0; i < S; ++i) issue_next();
 
+    // ldmatrix lane roles: K (A operand, rows = tokens) and V (A = V^T via .trans)
+    const int row_k = (lane & 7) + ((lane >> 3) & 1) * 8, half_k = lane >> 4;
+    const int row_v = (lane & 7) + (lane >> 4) * 8, half_v = (lane >> 3) & 1;
+
+    Piece pc;
+    bool have = first_piece(st, me, pc);
+    uint32_t qn[NT][2];
+    if (have) load_q_frags<D, G, FP8>(a, pc.b, pc.g, g8, c4, qn);
     int consumed = 0;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-        const Unit un = decode_unit(u, a, ps);
-        // q rows of the group, pre-scaled so that scores come out in log2 units.
-        const float qs = a.qscale * (FP8 ? a.scales[un.g] : 1.0f);
-        float qf[G][8];
+    while (have) {
+        Piece nx = pc;
+        const bool have_nx = next_piece(st, nx);
+        // q of head g8 of the group as MMA B fragments (zero for padding heads);
+        // the next piece's are fetched now so their latency overlaps this one.
+        uint32_t qf[NT][2];
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-            const uint4 r = ldg_nc_v4(a.q + ((int64_t)un.b * a.n_q + un.g * G + hh) * D + sub * 8);
-            const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float2 x = bf16x2_to_f32x2(w[i]);
-                qf[hh][2 * i] = x.x * qs;
-                qf[hh][2 * i + 1] = x.y * qs;
-            }
+        for (int ks = 0; ks < NT; ++ks) {
+            qf[ks][0] = qn[ks][0];
+            qf[ks][1] = qn[ks][1];
         }
-        float acc[G][C::DPL];
+        if (have_nx) load_q_frags<D, G, FP8>(a, nx.b, nx.g, g8, c4, qn);
+        const float qs = a.qscale * (FP8 ? a.scales[pc.g] : 1.0f);
+        const int C_len = clamp_ctx(a.context_lens[pc.b], a.W, a.err, false);
+        float o[NT][4];
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-            for (int i = 0; i < C::DPL; ++i) acc[hh][i] = 0.0f;
-        float m_run = -INFINITY, l_run = 0.0f;  // per lane: head hl, tokens of quarter tq
+        for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // heads 2c, 2c+1
 
-        for (int j = un.j0 + warp; j < un.j1; j += kWarps) {
-            const int st = consumed % S;
+        for (int j = pc.j0; j < pc.j1; ++j) {
+            const int sidx = consumed % S;
             const uint32_t parity = (uint32_t)(consumed / S) & 1u;
             if (!aborted) {
-                const bool ok = mbar_wait_bounded(&bars[st], parity);
+                const bool ok = mbar_wait_bounded(&bars[sidx], parity);
                 aborted = __any_sync(kFull, !ok);
                 if (aborted) {
                     drain_from = consumed;
                     if (lane == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
                 }
             }
-            if (!aborted && phys_st[st] >= 0) {
-                const uint8_t *kt = ring + st * C::kStageBytes;
-                const uint8_t *vt = kt + C::kTileBytes;
-                const int nv = min(kBlockSize, un.C - j * kBlockSize);
-                // ---- scores for the block's 16 keys x G heads ----
+            if (!aborted && phys_st[sidx] >= 0) {
+                const uint32_t kb = smem_u32(ring + sidx * Gm::STAGE);
+                const uint32_t vb = kb + Gm::TILE;
+                const int nv = min(kBlockSize, C_len - j * kBlockSize);
+                // ---- S^T = K . Q^T ----
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (!FP8) {
 #pragma unroll
-                for (int r = 0; r < kBlockSize / C::TPR; ++r) {
-                    const int t = r * C::TPR + tsub;
-                    float kf[8];
-                    load8<FP8>(kt + (t * D + sub * 8) * C::E, kf);
-                    float part[G];
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh) {
-                        float s = 0.0f;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) s = fmaf(qf[hh][i], kf[i], s);
-                        part[hh] = s;
+                    for (int ks = 0; ks < NT; ++ks) {
+                        const int chunk = 2 * ks + half_k;
+                        const uint32_t off = (chunk >> 3) * Gm::RGN + swz<128>(row_k * 128 + (chunk & 7) * 16);
+                        uint32_t fa[4];
+                        ldsm_x4(kb + off, fa);
+                        mma16816<false>((ks & 1) ? sb : sa, fa, qf[ks][0], qf[ks][1]);
                     }
-                    halve<G, C::LPT / 2, G>(part, lane);
-                    float x = part[0];
+                } else {
 #pragma unroll
-                    for (int off = C::SPAN / 2; off >= 1; off >>= 1) x += __shfl_xor_sync(kFull, x, off);
-                    if (sub % C::SPAN == 0) sp[t * 8 + sub / C::SPAN] = (t < nv) ? x : -INFINITY;
-                }
-                __syncwarp();
-                // ---- online softmax update (lane: head hl, keys 4tq..4tq+3) ----
-                float s4[4];
-                float bm = -INFINITY;
-                if (hl < G) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        s4[i] = sp[(tq * 4 + i) * 8 + hl];
-                        bm = fmaxf(bm, s4[i]);
+                    for (int kk = 0; kk < D / 32; ++kk) {
+                        const uint32_t d0 = 32 * kk + 8 * c4;
+                        const uint2 x = lds64(kb + swz<Gm::BOXB>(g8 * Gm::ROWB + d0));
+                        const uint2 y = lds64(kb + swz<Gm::BOXB>((g8 + 8) * Gm::ROWB + d0));
+                        uint32_t f0[4], f1[4];
+                        e4m3x4_to_f16x4(x.x, f0[0], f0[2]);
+                        e4m3x4_to_f16x4(y.x, f0[1], f0[3]);
+                        e4m3x4_to_f16x4(x.y, f1[0], f1[2]);
+                        e4m3x4_to_f16x4(y.y, f1[1], f1[3]);
+                        mma16816<true>(sa, f0, qf[2 * kk][0], qf[2 * kk][1]);
+                        mma16816<true>(sb, f1, qf[2 * kk + 1][0], qf[2 * kk + 1][1]);
                     }
                 }
-                bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
-                bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 16));
-                const float m_new = fmaxf(m_run, bm);
-                float alpha = 1.0f;
-                if (hl < G) {
-                    float lsum = 0.0f;
-                    if (m_new != -INFINITY) {
-                        alpha = exp2f(m_run - m_new);
+                float s[4];
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float p = exp2f(s4[i] - m_new);
-                            sp[(tq * 4 + i) * 8 + hl] = p;
-                            lsum += p;
+                for (int i = 0; i < 4; ++i) s[i] = (sa[i] + sb[i]) * qs;
+                if (g8 >= nv) s[0] = s[1] = -INFINITY;
+                if (g8 + 8 >= nv) s[2] = s[3] = -INFINITY;
+                // ---- online softmax (token 0 of a block is always valid) ----
+                float bm0 = fmaxf(s[0], s[2]), bm1 = fmaxf(s[1], s[3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
+                    bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
+                }
+                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+                const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+                const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
+                const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
+                l0 = fmaf(l0, al0, p0 + p2);
+                l1 = fmaf(l1, al1, p1 + p3);
+                m0 = mn0;
+                m1 = mn1;
+                if (__any_sync(kFull, al0 != 1.0f || al1 != 1.0f)) {
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        o[t][0] *= al0;
+                        o[t][1] *= al1;
+                        o[t][2] *= al0;
+                        o[t][3] *= al1;
+                    }
+                }
+                const uint32_t pb0 = movm_t(pack2<FP8>(p0, p1));  // P^T rows: tokens 2c,2c+1 of head g
+                const uint32_t pb1 = movm_t(pack2<FP8>(p2, p3));  // tokens 2c+8, 2c+9
+                // masked tokens' V must not reach the MMA (0 * non-finite garbage)
+                const uint32_t mk01 = (2 * c4 < nv ? 0x0000ffffu : 0u) | (2 * c4 + 1 < nv ? 0xffff0000u : 0u);
+                const uint32_t mk23 = (2 * c4 + 8 < nv ? 0x0000ffffu : 0u) | (2 * c4 + 9 < nv ? 0xffff0000u : 0u);
+                // ---- O^T += V^T . P^T ----
+                if constexpr (!FP8) {
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        const int chunk = 2 * t + half_v;
+                        const uint32_t off = (chunk >> 3) * Gm::RGN + swz<128>(row_v * 128 + (chunk & 7) * 16);
+                        uint32_t fa[4];
+                        ldsm_x4_t(vb + off, fa);
+                        if (nv < kBlockSize) {
+                            fa[0] &= mk01;
+                            fa[1] &= mk01;
+                            fa[2] &= mk23;
+                            fa[3] &= mk23;
                         }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) sp[(tq * 4 + i) * 8 + hl] = 0.0f;
+                        mma16816<false>(o[t], fa, pb0, pb1);
                     }
-                    l_run = l_run * alpha + lsum;
-                    m_run = m_new;
-                }
-                __syncwarp();
-                if (__any_sync(kFull, alpha != 1.0f)) {
+                } else {
 #pragma unroll
-                    for (int hh = 0; hh < G; ++hh) {
-                        const float al = __shfl_sync(kFull, alpha, hh);
-#pragma unroll
-                        for (int i = 0; i < C::DPL; ++i) acc[hh][i] *= al;
+                    for (int P = 0; P < D / 32; ++P) {
+                        const uint32_t db = 32 * P + 4 * g8;
+                        const uint32_t r0 = lds32(vb + swz<Gm::BOXB>((2 * c4) * Gm::ROWB + db));
+                        const uint32_t r1 = lds32(vb + swz<Gm::BOXB>((2 * c4 + 1) * Gm::ROWB + db));
+                        const uint32_t r2 = lds32(vb + swz<Gm::BOXB>((2 * c4 + 8) * Gm::ROWB + db));
+                        const uint32_t r3 = lds32(vb + swz<Gm::BOXB>((2 * c4 + 9) * Gm::ROWB + db));
+                        uint32_t fa[4], fb[4];
+                        e4m3x4_to_f16x4(prmt(r0, r1, 0x5140u), fa[0], fa[1]);  // d0, d1 of tokens 2c,2c+1
+                        e4m3x4_to_f16x4(prmt(r0, r1, 0x7362u), fb[0], fb[1]);  // d2, d3
+                        e4m3x4_to_f16x4(prmt(r2, r3, 0x5140u), fa[2], fa[3]);  // tokens 2c+8, 2c+9
+                        e4m3x4_to_f16x4(prmt(r2, r3, 0x7362u), fb[2], fb[3]);
+                        if (nv < kBlockSize) {
+                            fa[0] &= mk01; fa[1] &= mk01; fa[2] &= mk23; fa[3] &= mk23;
+                            fb[0] &= mk01; fb[1] &= mk01; fb[2] &= mk23; fb[3] &= mk23;
+                        }
+                        mma16816<true>(o[2 * P], fa, pb0, pb1);
+                        mma16816<true>(o[2 * P + 1], fb, pb0, pb1);
                     }
-                }
-                // ---- P.V ----
-#pragma unroll 4
-                for (int t = 0; t < nv; ++t) {
-                    float p[G];
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh) p[hh] = sp[t * 8 + hh];
-                    float vf[C::DPL];
-                    loadN<FP8, C::DPL>(vt + (t * D + lane * C::DPL) * C::E, vf);
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-                        for (int i = 0; i < C::DPL; ++i) acc[hh][i] = fmaf(p[hh], vf[i], acc[hh][i]);
                 }
             }
             __syncwarp();
             ++consumed;
-            if (!prod_done && !aborted) {
-                if (iter_next(pit, warp, total_units, a, ps)) {
-                    issue(n_issued);
-                    ++n_issued;
-                } else {
-                    prod_done = true;
-                }
-            }
+            if (!aborted) issue_next();
         }
 
-        // ---- merge the 4 warps' (m, l, o) for this unit ----
-        float l_tot = l_run + __shfl_xor_sync(kFull, l_run, 8);
-        l_tot += __shfl_xor_sync(kFull, l_tot, 16);
-        if (lane < G) {
-            merge_m[warp * 8 + lane] = m_run;
-            merge_l[warp * 8 + lane] = l_tot;
+        // ---- piece end ----
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(kFull, l0, off);
+            l1 += __shfl_xor_sync(kFull, l1, off);
         }
+        const float vs = FP8 ? a.scales[a.n_kv + pc.g] : 1.0f;
+        const bool h0 = 2 * c4 < G, h1 = 2 * c4 + 1 < G;  // this thread's heads exist
+        if (pc.j0 == 0 && pc.j1 == pc.nblk) {
+            // the whole (b, g): normalise and write bf16 out
+            const float r0 = l0 > 0.0f ? vs / l0 : 0.0f, r1 = l1 > 0.0f ? vs / l1 : 0.0f;
+            __nv_bfloat16 *ob = a.out + ((int64_t)pc.b * a.n_q + pc.g * G) * D;
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh)
+            for (int t = 0; t < NT; ++t) {
 #pragma unroll
-            for (int i = 0; i < C::DPL; ++i) merge_o[(warp * G + hh) * D + lane * C::DPL + i] = acc[hh][i];
-        __syncthreads();
-        const float vs = FP8 ? a.scales[a.n_kv + un.g] : 1.0f;
-        for (int idx = tid; idx < G * D; idx += kThreads) {
-            const int hh = idx / D, d = idx - hh * D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, merge_m[w * 8 + hh]);
-            float L = 0.0f, o = 0.0f;
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const float sc = exp2f(merge_m[w * 8 + hh] - M);
-                    L = fmaf(sc, merge_l[w * 8 + hh], L);
-                    o = fmaf(sc, merge_o[(w * G + hh) * D + d], o);
+                for (int i = 0; i < 2; ++i) {
+                    const int d = FP8 ? 32 * (t >> 1) + 4 * g8 + 2 * (t & 1) + i : 16 * t + g8 + 8 * i;
+                    if (h0) ob[(2 * c4) * D + d] = __float2bfloat16_rn(o[t][2 * i] * r0);
+                    if (h1) ob[(2 * c4 + 1) * D + d] = __float2bfloat16_rn(o[t][2 * i + 1] * r1);
                 }
             }
-            o *= vs;
-            if (un.nparts == 1) {
-                a.out[((int64_t)un.b * a.n_q + un.g * G + hh) * D + d] =
-                    __float2bfloat16_rn(L > 0.0f ? o / L : 0.0f);
-            } else {
-                const int64_t r = ((int64_t)un.pidx * a.n_kv + un.g) * G + hh;
-                a.ws_o[r * D + d] = o;
-                if (d == 0) a.ws_ml[r] = make_float2(M, L);
+        } else {
+            // a part of (b, g): publish (m, l, O); the warp completing the count
+            // merges every piece of (b, g), i.e. the slices its run overlaps.
+            const int64_t slot = (int64_t)pc.slice + (int64_t)pc.b * a.n_kv + pc.g;  // unique along the stream
+            float *wo = a.ws_o + slot * G * D;
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int d = FP8 ? 32 * (t >> 1) + 4 * g8 + 2 * (t & 1) + i : 16 * t + g8 + 8 * i;
+                    if (h0) wo[(2 * c4) * D + d] = o[t][2 * i] * vs;
+                    if (h1) wo[(2 * c4 + 1) * D + d] = o[t][2 * i + 1] * vs;
+                }
             }
+            if (g8 == 0) {
+                if (h0) a.ws_ml[slot * G + 2 * c4] = make_float2(m0, l0);
+                if (h1) a.ws_ml[slot * G + 2 * c4 + 1] = make_float2(m1, l1);
+            }
+            __threadfence();
+            __syncwarp();
+            const int start = a.n_kv * ps[pc.b] + pc.g * pc.nblk;
+            const int s_first = start / st.share, s_last = (start + pc.nblk - 1) / st.share;
+            int prev = 0;
+            if (lane == 0) prev = atomicAdd(&a.counters[pc.b * a.n_kv + pc.g], 1);
+            prev = __shfl_sync(kFull, prev, 0);
+            if (prev == s_last - s_first)
+                merge_pieces<D, G>(a, pc.b, pc.g, s_first, s_last - s_first + 1, lane, scratch);
         }
-        __syncthreads();
+        pc = nx;
+        have = have_nx;
     }
 
-    // Only after a timeout can copies still be in flight: wait for them
-    // (bounded) before the CTA's shared memory goes away.
-    if (drain_from >= 0)
+    if (drain_from >= 0)  // copies may still be in flight only after a timeout
         for (int k = drain_from; k < n_issued; ++k)
             mbar_wait_bounded(&bars[k % S], (uint32_t)(k / S) & 1u, 100000000ull);
 }
 
-struct MergeArgs {
-    int batch, n_q, n_kv;
-    const int32_t *part_start;
-    const float2 *ws_ml;
-    const float *ws_o;
-    __nv_bfloat16 *out;
-};
-
-// One warp per (sequence, query head) with two or more partitions: lanes form
-// 4 groups of 8; group k combines partitions k, k+4, ...; each lane owns D/8
-// consecutive columns.  Log-sum-exp merge in log2 units.
-template <int D, int G>
-__global__ void __launch_bounds__(128) merge_kernel(MergeArgs a)
-{
-    constexpr int DPL = D / 8;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 4 + warp;
-    if (row >= a.batch * a.n_q) return;
-    const int b = row / a.n_q, h = row - b * a.n_q;
-    const int g = h / G, hh = h - g * G;
-    const int p0 = a.part_start[b], np = a.part_start[b + 1] - p0;
-    if (np <= 1) return;
-    float M = -INFINITY;
-    for (int p = lane; p < np; p += 32) M = fmaxf(M, a.ws_ml[((int64_t)(p0 + p) * a.n_kv + g) * G + hh].x);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
-    const int grp = lane >> 3, sl = lane & 7;
-    float acc[DPL];
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) acc[i] = 0.0f;
-    float L = 0.0f;
-#pragma unroll 2
-    for (int p = grp; p < np; p += 4) {
-        const int64_t r = ((int64_t)(p0 + p) * a.n_kv + g) * G + hh;
-        const float2 ml = a.ws_ml[r];
-        const float sc = (M == -INFINITY) ? 0.0f : exp2f(ml.x - M);
-        L = fmaf(sc, ml.y, L);
-        const float4 *src = reinterpret_cast<const float4 *>(a.ws_o + r * D + sl * DPL);
-#pragma unroll
-        for (int i = 0; i < DPL / 4; ++i) {
-            const float4 x = src[i];
-            acc[4 * i] = fmaf(sc, x.x, acc[4 * i]);
-            acc[4 * i + 1] = fmaf(sc, x.y, acc[4 * i + 1]);
-            acc[4 * i + 2] = fmaf(sc, x.z, acc[4 * i + 2]);
-            acc[4 * i + 3] = fmaf(sc, x.w, acc[4 * i + 3]);
-        }
-    }
-    L += __shfl_xor_sync(kFull, L, 8);
-    L += __shfl_xor_sync(kFull, L, 16);
-#pragma unroll
-    for (int i = 0; i < DPL; ++i) {
-        acc[i] += __shfl_xor_sync(kFull, acc[i], 8);
-        acc[i] += __shfl_xor_sync(kFull, acc[i], 16);
-    }
-    if (grp == 0) {
-        __nv_bfloat16 *o = a.out + (int64_t)row * D + sl * DPL;
-#pragma unroll
-        for (int i = 0; i < DPL; i += 2) {
-            const float x0 = L > 0.0f ? acc[i] / L : 0.0f;
-            const float x1 = L > 0.0f ? acc[i + 1] / L : 0.0f;
-            *reinterpret_cast<__nv_bfloat162 *>(o + i) = __floats2bfloat162_rn(x0, x1);
-        }
-    }
-}
-
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-size_t decode_workspace_bytes(int batch, int n_q, int n_kv, int d_head, int max_blocks_per_seq,
-                              int partition_tokens)
+// Workspace: counters [batch * n_kv] int (zero between calls), then partial
+// (max, sum) and O for up to n_slices + batch * n_kv pieces.
+struct WsLayout {
+    size_t counters, ml, o, total;
+};
+
+static WsLayout ws_layout(int batch, int n_q, int n_kv, int d_head, int64_t slots)
 {
-    const int part_blocks = partition_tokens / kBlockSize;
-    const int64_t nps = (max_blocks_per_seq + part_blocks - 1) / part_blocks;
-    const int64_t P = (int64_t)batch * nps;
     const int G = n_q / n_kv;
-    return align256(4 * (size_t)(batch + 1)) + align256(8 * (size_t)P * n_kv * G) +
-           4 * (size_t)P * n_kv * G * d_head;
+    WsLayout w;
+    w.counters = 0;
+    w.ml = align256(4 * (size_t)batch * n_kv);
+    w.o = w.ml + align256(8 * (size_t)slots * G);
+    w.total = w.o + 4 * (size_t)slots * G * d_head;
+    return w;
 }
 
+// Upper bound on pieces (workspace slots): one per slice plus one per
+// (sequence, head) run; `warps` is the grid's total warp count.
+static int64_t max_slots(pkv_pool *pool, int batch, int n_kv, int max_blocks_per_seq, int warps)
+{
+    const int slice_blocks = pool->partition_tokens / kBlockSize;
+    const int64_t total = (int64_t)batch * n_kv * max_blocks_per_seq;
+    const int64_t n_slices = slice_blocks > 0 ? (total + slice_blocks - 1) / slice_blocks : (int64_t)warps;
+    return n_slices + (int64_t)batch * n_kv;
+}
+
+// Persistent grid of the decode kernel for (d_head, G, dtype) at `batch`.
 template <int D, int G, bool FP8>
-static pkv_status launch_decode(pkv_pool *pool, const DecodeArgs &a, int nps, cudaStream_t s)
+static pkv_status decode_grid(pkv_pool *pool, int batch, int *grid, size_t *smem)
 {
     using C = Cfg<D, G, FP8>;
     auto kern = decode_kernel<D, G, FP8>;
@@ -594,49 +801,86 @@ static pkv_status launch_decode(pkv_pool *pool, const DecodeArgs &a, int nps, cu
                                             optin - (int)fa.sharedSizeBytes);
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(decode)");
-    const size_t smem = C::smem_bytes(a.batch);
+    *smem = C::smem_bytes(batch);
     int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::kThreads, *smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-    if (occ < 1) return fail(PKV_EUNSUPPORTED, "decode: %zu bytes of shared memory do not fit", smem);
-    const int64_t units_max = (int64_t)a.batch * nps * a.n_kv;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(units_max, (int64_t)pool->num_sms * occ));
-    {
-        LaunchScope ls(pool, kDecode, s);
-        kern<<<(unsigned)grid, kThreads, smem, s>>>(a);
-        e = cudaGetLastError();
-        ls.done();
-        if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-    }
-    if (nps > 1) {
-        MergeArgs m;
-        m.batch = a.batch;
-        m.n_q = a.n_q;
-        m.n_kv = a.n_kv;
-        m.part_start = a.part_start;
-        m.ws_ml = a.ws_ml;
-        m.ws_o = a.ws_o;
-        m.out = a.out;
-        const int rows = a.batch * a.n_q;
-        LaunchScope ls(pool, kMerge, s);
-        merge_kernel<D, G><<<(rows + 3) / 4, 128, 0, s>>>(m);
-        e = cudaGetLastError();
-        ls.done();
-        if (e != cudaSuccess) return cuda_fail(e, "merge launch");
-    }
+    if (occ < 1) return fail(PKV_EUNSUPPORTED, "decode: %zu bytes of shared memory do not fit", *smem);
+    *grid = pool->num_sms * occ;
+    return PKV_OK;
+}
+
+template <int D, int G, bool FP8>
+static pkv_status launch_decode(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
+{
+    using C = Cfg<D, G, FP8>;
+    int grid = 0;
+    size_t smem = 0;
+    pkv_status st = decode_grid<D, G, FP8>(pool, a.batch, &grid, &smem);
+    if (st != PKV_OK) return st;
+    const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
+    st = ensure_workspace(pool, L.total);
+    if (st != PKV_OK) return st;
+    uint8_t *ws = static_cast<uint8_t *>(pool->ws);
+    a.counters = reinterpret_cast<int *>(ws + L.counters);
+    a.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
+    a.ws_o = reinterpret_cast<float *>(ws + L.o);
+    LaunchScope ls(pool, kDecode, s);
+    decode_kernel<D, G, FP8><<<(unsigned)grid, C::kThreads, smem, s>>>(pool->tm_k, pool->tm_v, a);
+    cudaError_t e = cudaGetLastError();
+    ls.done();
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return PKV_OK;
 }
 
 template <int D, bool FP8>
-static pkv_status dispatch_g(pkv_pool *pool, const DecodeArgs &a, int G, int nps, cudaStream_t s)
+static pkv_status dispatch_g(pkv_pool *pool, const DecodeArgs &a, int G, cudaStream_t s)
 {
     switch (G) {
-    case 1: return launch_decode<D, 1, FP8>(pool, a, nps, s);
-    case 2: return launch_decode<D, 2, FP8>(pool, a, nps, s);
-    case 4: return launch_decode<D, 4, FP8>(pool, a, nps, s);
-    case 8: return launch_decode<D, 8, FP8>(pool, a, nps, s);
+    case 1: return launch_decode<D, 1, FP8>(pool, a, s);
+    case 2: return launch_decode<D, 2, FP8>(pool, a, s);
+    case 4: return launch_decode<D, 4, FP8>(pool, a, s);
+    case 8: return launch_decode<D, 8, FP8>(pool, a, s);
     }
     return fail(PKV_EUNSUPPORTED, "decode: group size %d unsupported (1, 2, 4 or 8)", G);
+}
+
+template <int D, int G, bool FP8>
+static pkv_status grid_warps(pkv_pool *pool, int batch, int *warps)
+{
+    size_t smem = 0;
+    int grid = 0;
+    pkv_status st = decode_grid<D, G, FP8>(pool, batch, &grid, &smem);
+    *warps = grid * Cfg<D, G, FP8>::NW;
+    return st;
+}
+
+template <int D, bool FP8>
+static pkv_status grid_g(pkv_pool *pool, int G, int batch, int *warps)
+{
+    switch (G) {
+    case 1: return grid_warps<D, 1, FP8>(pool, batch, warps);
+    case 2: return grid_warps<D, 2, FP8>(pool, batch, warps);
+    case 4: return grid_warps<D, 4, FP8>(pool, batch, warps);
+    case 8: return grid_warps<D, 8, FP8>(pool, batch, warps);
+    }
+    return fail(PKV_EUNSUPPORTED, "decode: group size %d unsupported (1, 2, 4 or 8)", G);
+}
+
+// Workspace bytes a decode call with these sizes needs on this pool.
+pkv_status decode_workspace_bytes(pkv_pool *pool, int batch, int n_q, int max_blocks_per_seq, size_t *bytes)
+{
+    const int G = n_q / pool->n_kv;
+    int warps = 0;
+    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
+    pkv_status st = pool->d_head == 128 ? (fp8 ? grid_g<128, true>(pool, G, batch, &warps)
+                                               : grid_g<128, false>(pool, G, batch, &warps))
+                                        : (fp8 ? grid_g<64, true>(pool, G, batch, &warps)
+                                               : grid_g<64, false>(pool, G, batch, &warps));
+    if (st != PKV_OK) return st;
+    *bytes = ws_layout(batch, n_q, pool->n_kv, pool->d_head,
+                       max_slots(pool, batch, pool->n_kv, max_blocks_per_seq, warps)).total;
+    return PKV_OK;
 }
 
 }  // namespace pkv
@@ -662,6 +906,8 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
     if (batch == 0) return PKV_OK;
     if (batch > kMaxBatch)
         return fail(PKV_EUNSUPPORTED, "paged_decode_attention: batch %d > %d", batch, kMaxBatch);
+    if ((int64_t)batch * pool->n_kv * max_blocks_per_seq >= ((int64_t)1 << 30))
+        return fail(PKV_EUNSUPPORTED, "paged_decode_attention: batch x n_kv x max_blocks_per_seq too large");
     if (!q || !block_tables || !context_lens || !out)
         return fail(PKV_EINVAL, "paged_decode_attention: NULL device pointer");
     if (((uintptr_t)q | (uintptr_t)out) & 15u)
@@ -672,20 +918,7 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
     if (fp8 && !pool->scales_set)
         return fail(PKV_EINVAL, "paged_decode_attention: FP8 pool needs kv_pool_set_fp8_scales first");
 
-    const int part_blocks = pool->partition_tokens / kBlockSize;
-    const int nps = (max_blocks_per_seq + part_blocks - 1) / part_blocks;
-    if ((int64_t)batch * nps * pool->n_kv * G >= ((int64_t)1 << 31))
-        return fail(PKV_EUNSUPPORTED, "paged_decode_attention: too many partitions; raise the partition size");
-    const size_t need = decode_workspace_bytes(batch, n_q, pool->n_kv, pool->d_head, max_blocks_per_seq,
-                                               pool->partition_tokens);
-    pkv_status st = ensure_workspace(pool, need);
-    if (st != PKV_OK) return st;
-
-    const int64_t P = (int64_t)batch * nps;
-    uint8_t *ws = static_cast<uint8_t *>(pool->ws);
     DecodeArgs a;
-    a.k_pool = static_cast<const uint8_t *>(pool->k);
-    a.v_pool = static_cast<const uint8_t *>(pool->v);
     a.num_blocks = pool->num_blocks;
     a.n_kv = pool->n_kv;
     a.n_q = n_q;
@@ -697,14 +930,13 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
     a.out = static_cast<__nv_bfloat16 *>(out);
-    a.part_start = reinterpret_cast<int32_t *>(ws);
-    a.ws_ml = reinterpret_cast<float2 *>(ws + align256(4 * (size_t)(batch + 1)));
-    a.ws_o = reinterpret_cast<float *>(ws + align256(4 * (size_t)(batch + 1)) +
-                                       align256(8 * (size_t)P * pool->n_kv * G));
-    a.part_blocks = part_blocks;
+    a.counters = nullptr;
+    a.ws_ml = nullptr;
+    a.ws_o = nullptr;
+    a.slice_blocks = pool->partition_tokens / kBlockSize;
     a.err = pool->err;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pool->d_head == 128)
-        return fp8 ? dispatch_g<128, true>(pool, a, G, nps, s) : dispatch_g<128, false>(pool, a, G, nps, s);
-    return fp8 ? dispatch_g<64, true>(pool, a, G, nps, s) : dispatch_g<64, false>(pool, a, G, nps, s);
+        return fp8 ? dispatch_g<128, true>(pool, a, G, s) : dispatch_g<128, false>(pool, a, G, s);
+    return fp8 ? dispatch_g<64, true>(pool, a, G, s) : dispatch_g<64, false>(pool, a, G, s);
 }

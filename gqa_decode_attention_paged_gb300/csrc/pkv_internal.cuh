@@ -3,6 +3,7 @@
 // (TMA) copies used by the kernels.  sm_103a only.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -18,7 +19,7 @@ namespace pkv {
 
 constexpr int kBlockSize = 16;               // token slots per block
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded mbarrier waits: 2 s
-constexpr int kDefaultPartitionTokens = 512;
+constexpr int kDefaultPartitionTokens = 0;  // 0: equal work per CTA
 
 enum KernelKind { kAppend = 0, kDecode = 1, kMerge = 2, kNumKinds = 3 };
 
@@ -37,6 +38,9 @@ struct pkv_pool {
     void *k = nullptr, *v = nullptr;  // device, [num_blocks][n_kv][block_size][d_head]
     size_t bytes_per_array = 0;
     float *scales = nullptr;          // device [2 * n_kv]: k scales then v scales
+    // TMA descriptors of the K and V arrays viewed as 2-D [rows = blocks*n_kv*16][d_head],
+    // boxes of 16 rows x min(row bytes, 128) bytes, swizzled (128 B, or 64 B for 64-byte rows).
+    CUtensorMap tm_k, tm_v;
     bool scales_set = false;
     unsigned *err = nullptr;          // device sticky error word
     void *ws = nullptr;               // split-KV workspace (grow-only)
@@ -71,6 +75,7 @@ struct LaunchScope {
 };
 
 pkv_status ensure_workspace(pkv_pool *pool, size_t bytes);
+pkv_status make_tensor_maps(pkv_pool *pool);
 
 // ---------------------------------------------------------------------------
 // Device helpers (inline PTX)
@@ -154,6 +159,23 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
         "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst_smem)),
         "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// Tiled 2-D TMA load of one box at element coordinates (x, y) of `map`
+// (a __grid_constant__ kernel parameter) into shared memory.
+__device__ __forceinline__ void tma_load_2d(void *dst_smem, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first()

@@ -7,6 +7,8 @@
 
 #include <new>
 
+#include <cudaTypedefs.h>
+
 #include "pkv_internal.cuh"
 
 namespace pkv {
@@ -69,14 +71,54 @@ pkv_status ensure_workspace(pkv_pool *pool, size_t bytes)
         pool->ws = nullptr;
         return cuda_fail(e, "cudaMalloc(workspace)");
     }
+    // The decode kernel's per-(sequence, head) piece counters live at the
+    // start of the workspace and must read zero between calls.
+    e = cudaMemset(pool->ws, 0, want);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
     pool->ws_bytes = want;
+    return PKV_OK;
+}
+
+// The K and V arrays as 2-D tensors [blocks * n_kv * block_size rows][d_head]
+// for tiled TMA: one box = 16 token rows of one (block, KV head) tile and up
+// to 128 bytes of each row, with the matching shared-memory swizzle so that
+// warp-wide fragment loads hit distinct banks.
+pkv_status make_tensor_maps(pkv_pool *pool)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static std::once_flag once;
+    static cudaError_t get_err = cudaSuccess;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        get_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", reinterpret_cast<void **>(&encode),
+                                                   12000, cudaEnableDefault, &q);
+        if (get_err == cudaSuccess && q != cudaDriverEntryPointSuccess) get_err = cudaErrorNotSupported;
+    });
+    if (get_err != cudaSuccess || !encode) return cuda_fail(get_err, "cuTensorMapEncodeTiled entry point");
+    const int elem = pool->dtype == PKV_BF16 ? 2 : 1;
+    const uint64_t row_bytes = (uint64_t)pool->d_head * elem;
+    const uint64_t rows = (uint64_t)pool->num_blocks * pool->n_kv * pool->block_size;
+    if (rows >= (1ull << 31)) return fail(PKV_EUNSUPPORTED, "kv_pool_create: more than 2^31 token rows");
+    const uint32_t box_bytes = row_bytes > 128 ? 128 : (uint32_t)row_bytes;
+    cuuint64_t dims[2] = {(cuuint64_t)pool->d_head, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_bytes / (uint32_t)elem, (cuuint32_t)pool->block_size};
+    cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt = elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const CUtensorMapSwizzle sw = box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    for (int which = 0; which < 2; ++which) {
+        CUresult r = encode(which ? &pool->tm_v : &pool->tm_k, dt, 2, which ? pool->v : pool->k, dims, strides,
+                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    }
     return PKV_OK;
 }
 
 // Defined in append.cu / decode.cu: confirm the device can run our kernels.
 pkv_status probe_kernels();
-size_t decode_workspace_bytes(int batch, int n_q, int n_kv, int d_head, int max_blocks_per_seq,
-                              int partition_tokens);
+pkv_status decode_workspace_bytes(pkv_pool *pool, int batch, int n_q, int max_blocks_per_seq, size_t *bytes);
 
 }  // namespace pkv
 
@@ -160,6 +202,11 @@ pkv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv, 
         kv_pool_destroy(p);
         return s;
     }
+    st = make_tensor_maps(p);
+    if (st != PKV_OK) {
+        kv_pool_destroy(p);
+        return st;
+    }
     *out = p;
     return PKV_OK;
 }
@@ -222,9 +269,8 @@ pkv_status kv_pool_layout(const pkv_pool *pool, pkv_layout *out)
 pkv_status kv_pool_set_partition_tokens(pkv_pool *pool, int32_t tokens)
 {
     if (!pool) return fail(PKV_EINVAL, "kv_pool_set_partition_tokens: NULL pool");
-    if (tokens == 0) tokens = kDefaultPartitionTokens;
-    if (tokens < 64 || tokens > 65536 || tokens % 64)
-        return fail(PKV_ERANGE, "kv_pool_set_partition_tokens: %d not a multiple of 64 in [64, 65536]",
+    if (tokens != 0 && (tokens < 16 || tokens > (1 << 20) || tokens % 16))
+        return fail(PKV_ERANGE, "kv_pool_set_partition_tokens: %d is neither 0 nor a multiple of 16 in [16, 2^20]",
                     tokens);
     pool->partition_tokens = tokens;
     return PKV_OK;
@@ -234,8 +280,10 @@ pkv_status kv_pool_reserve_workspace(pkv_pool *pool, int32_t batch, int32_t n_q,
 {
     if (!pool || batch < 0 || n_q <= 0 || max_blocks_per_seq <= 0 || n_q % pool->n_kv)
         return fail(PKV_EINVAL, "kv_pool_reserve_workspace: bad argument");
-    return ensure_workspace(pool, decode_workspace_bytes(batch, n_q, pool->n_kv, pool->d_head,
-                                                         max_blocks_per_seq, pool->partition_tokens));
+    size_t bytes = 0;
+    pkv_status st = decode_workspace_bytes(pool, batch, n_q, max_blocks_per_seq, &bytes);
+    if (st != PKV_OK) return st;
+    return ensure_workspace(pool, bytes);
 }
 
 pkv_status pkv_get_error(pkv_pool *pool, int32_t clear, uint32_t *bits)
@@ -245,6 +293,9 @@ pkv_status pkv_get_error(pkv_pool *pool, int32_t clear, uint32_t *bits)
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = cudaMemcpy(&v, pool->err, sizeof v, cudaMemcpyDeviceToHost);
     if (e == cudaSuccess && clear) e = cudaMemset(pool->err, 0, sizeof(unsigned));
+    // A timed-out decode may leave piece counters behind: reset the workspace.
+    if (e == cudaSuccess && clear && (v & PKV_DEVERR_TIMEOUT) && pool->ws)
+        e = cudaMemset(pool->ws, 0, pool->ws_bytes);
     if (e == cudaSuccess && clear) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "pkv_get_error");
     if (bits) *bits = v;

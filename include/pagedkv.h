@@ -81,7 +81,7 @@ typedef struct {
     int64_t launches;        /* every kernel launch the library enqueued */
     int64_t append_launches;
     int64_t decode_launches;
-    int64_t merge_launches;
+    int64_t merge_launches;  /* 0: partial results merge inside the decode kernel */
     double append_ms;        /* summed event time of timed launches */
     double decode_ms;
     double merge_ms;
@@ -118,8 +118,12 @@ pkv_status kv_pool_set_fp8_scales(pkv_pool *pool, const float *k_scale_host,
 /* Report the pool's device pointers and layout (see pkv_layout). */
 pkv_status kv_pool_layout(const pkv_pool *pool, pkv_layout *out);
 
-/* Tokens per split-KV partition used by paged_decode_attention: 0 picks the
- * default (512); otherwise a multiple of 64 in [64, 65536].  Errors: ERANGE. */
+/* How paged_decode_attention splits work.  0 (the default): the batch's
+ * (sequence, KV head, block) work is cut into one equal slice per resident
+ * CTA, so every SM gets the same number of blocks whatever the length mix.
+ * Otherwise: slices of `tokens` tokens (a multiple of 16 in [16, 2^20]),
+ * taken round-robin by the CTAs.  Results agree up to rounding either way.
+ * Errors: ERANGE. */
 pkv_status kv_pool_set_partition_tokens(pkv_pool *pool, int32_t tokens);
 
 /* Grow the pool's split-KV workspace now (it otherwise grows inside the
@@ -174,8 +178,13 @@ pkv_status paged_kv_append(pkv_pool *pool, const void *k_new, const void *v_new,
  *   scale         fp32 factor on q.k (normally 1/sqrt(d_head)).
  *   out           device bf16 [batch][n_q][d_head], 16-byte aligned; rounded
  *                 to nearest even from fp32.
- * batch == 0 is a no-op.  Uses the pool's split-KV workspace, growing it
- * (cudaMalloc, outside any stream capture) when the call needs more.
+ * batch == 0 is a no-op; batch <= 8192 and batch * n_kv * max_blocks_per_seq
+ * < 2^30.  One kernel launch: pieces of a sequence that land on different
+ * thread blocks are merged by whichever block finishes its piece last.  Uses
+ * the pool's split-KV workspace, growing it (cudaMalloc + cudaMemset,
+ * outside any stream capture) when the call needs more.  After a timeout
+ * bit (PKV_DEVERR_TIMEOUT), pkv_get_error(pool, 1, ...) also resets the
+ * workspace.
  * Errors: EINVAL, EUNSUPPORTED (group size), ENOMEM, ECUDA. */
 pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int32_t n_q,
                                   const int32_t *block_tables, int32_t max_blocks_per_seq,

@@ -79,11 +79,12 @@ def test_single_token_output_is_its_value_exactly():
 def test_partition_size_does_not_change_the_answer_beyond_rounding():
     w = wl.build("psz", 32, 8, 128, [3000, 100, 4100], seed=5)
     outs = []
-    for part in (64, 512, 4096):
+    for part in (0, 64, 512, 4096):
         with make_pool(w, part) as pool:
             fill(pool, w)
             outs.append(out_f64(run_step(pool, w)))
-    assert np.abs(outs[0] - outs[1]).max() < 1e-2 and np.abs(outs[1] - outs[2]).max() < 1e-2
+    for o in outs[1:]:
+        assert np.abs(outs[0] - o).max() < 1e-2
 
 
 def test_repeat_calls_are_bitwise_deterministic_and_stream_aware():
@@ -158,7 +159,7 @@ def test_timing_counts_launches():
         pool.timing_enable(True)
         run_step(pool, w)
         t = pool.timing_read(reset=True)
-    assert t["append_launches"] == 1 and t["decode_launches"] == 1 and t["merge_launches"] == 1
+    assert t["append_launches"] == 1 and t["decode_launches"] == 1 and t["merge_launches"] == 0
     assert t["timed_decode"] == 1 and t["decode_ms"] > 0
 
 
