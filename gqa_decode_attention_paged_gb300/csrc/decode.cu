@@ -117,8 +117,8 @@ struct Cfg {
     static constexpr int kPhys = kBars + NW * kStages * 8;
     static constexpr int kScratch = kPhys + NW * kStages * 4;  // [NW][16] floats: merge max/sum per head
     static constexpr int kWarpTot = kScratch + NW * 16 * 4;
-    static constexpr int kPs = kWarpTot + 4 * NW;  // ps[batch + 1]
-    static size_t smem_bytes(int batch) { return 1024 + (size_t)kPs + 4 * (size_t)(batch + 1); }
+    static constexpr int kPs = kWarpTot + 4 * NW;  // ps[batch + 1], then clamped lengths cl[batch]
+    static size_t smem_bytes(int batch) { return 1024 + (size_t)kPs + 4 * (size_t)(2 * batch + 1); }
     static_assert(G <= 8, "at most 8 query heads per KV head");
 };
 
@@ -135,7 +135,7 @@ __device__ __forceinline__ int clamp_ctx(int c, int W, unsigned *err, bool repor
 // Exclusive prefix sum of block counts per sequence into ps[0..batch];
 // warp_tot is scratch for NW ints.
 template <int NW>
-__device__ void scan_blocks(const DecodeArgs &a, int32_t *ps, int *warp_tot)
+__device__ void scan_blocks(const DecodeArgs &a, int32_t *ps, int32_t *cl, int *warp_tot)
 {
     constexpr int NT = NW * 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -143,7 +143,11 @@ __device__ void scan_blocks(const DecodeArgs &a, int32_t *ps, int *warp_tot)
     for (int base = 0; base < a.batch; base += NT) {
         const int b = base + tid;
         int n = 0;
-        if (b < a.batch) n = (clamp_ctx(a.context_lens[b], a.W, a.err, blockIdx.x == 0) + kBlockSize - 1) / kBlockSize;
+        if (b < a.batch) {
+            const int c = clamp_ctx(a.context_lens[b], a.W, a.err, blockIdx.x == 0);
+            cl[b] = c;
+            n = (c + kBlockSize - 1) / kBlockSize;
+        }
         int x = n;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -384,9 +388,16 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs &a, int b, int g, 
 // Lanes first split the pieces to get M and L per head (warp reductions, kept
 // in `scratch`), then each lane sums 4-column chunks of O over the pieces with
 // independent loads.  Reads go to L2 (other SMs wrote the pieces).
+struct MergeRefs {
+    const float2 *ws_ml;
+    const float *ws_o;
+    __nv_bfloat16 *out;
+    int *counters;
+    int n_kv, n_q;
+};
+
 template <int D, int G>
-__device__ __noinline__ void merge_pieces(const DecodeArgs &a, int b, int g, int s_first, int n, int lane,
-                                          float *scratch)
+__device__ __noinline__ void merge_pieces(MergeRefs a, int b, int g, int s_first, int n, int lane, float *scratch)
 {
     __threadfence();
     const int64_t base = (int64_t)s_first + (int64_t)b * a.n_kv + g;  // slot of piece 0
@@ -488,7 +499,8 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
         for (int i = 0; i < NW * S; ++i) mbar_init(reinterpret_cast<uint64_t *>(smem + C::kBars) + i, 1);
         fence_mbarrier_init();
     }
-    scan_blocks<NW>(a, ps, warp_tot);  // ends with __syncthreads; the last CTA-wide barrier
+    int32_t *cl = ps + a.batch + 1;
+    scan_blocks<NW>(a, ps, cl, warp_tot);  // ends with __syncthreads; the last CTA-wide barrier
     Stream st;
     st.ps = ps;
     st.batch = a.batch;
@@ -571,7 +583,7 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
         }
         if (have_nx) load_q_frags<D, G, FP8>(a, nx.b, nx.g, g8, c4, qn);
         const float qs = a.qscale * (FP8 ? a.scales[pc.g] : 1.0f);
-        const int C_len = clamp_ctx(a.context_lens[pc.b], a.W, a.err, false);
+        const int C_len = cl[pc.b];
         float o[NT][4];
 #pragma unroll
         for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
@@ -734,15 +746,19 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
                 if (h0) a.ws_ml[slot * G + 2 * c4] = make_float2(m0, l0);
                 if (h1) a.ws_ml[slot * G + 2 * c4 + 1] = make_float2(m1, l1);
             }
-            __threadfence();
-            __syncwarp();
+            __syncwarp();  // orders the lanes' stores before lane 0's fence (cumulative)
             const int start = a.n_kv * ps[pc.b] + pc.g * pc.nblk;
             const int s_first = start / st.share, s_last = (start + pc.nblk - 1) / st.share;
             int prev = 0;
-            if (lane == 0) prev = atomicAdd(&a.counters[pc.b * a.n_kv + pc.g], 1);
+            if (lane == 0) {
+                __threadfence();
+                prev = atomicAdd(&a.counters[pc.b * a.n_kv + pc.g], 1);
+            }
             prev = __shfl_sync(kFull, prev, 0);
-            if (prev == s_last - s_first)
-                merge_pieces<D, G>(a, pc.b, pc.g, s_first, s_last - s_first + 1, lane, scratch);
+            if (prev == s_last - s_first) {
+                MergeRefs mr{a.ws_ml, a.ws_o, a.out, a.counters, a.n_kv, a.n_q};
+                merge_pieces<D, G>(mr, pc.b, pc.g, s_first, s_last - s_first + 1, lane, scratch);
+            }
         }
         pc = nx;
         have = have_nx;
