@@ -82,6 +82,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.paged_kv_append.argtypes = [P, P, P, P, c.c_int64, P]
         lib.paged_decode_attention.argtypes = [P, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                                c.c_float, P, P]
+        lib.paged_decode_attention_noalloc.argtypes = [P, P, c.c_int32, P, c.c_int32, P, c.c_int32,
+                                                       c.c_float, P, P]
         lib.kv_bytes_per_token.argtypes = [c.c_int32, c.c_int32, c.c_int32, c.c_double]
         lib.kv_bytes_per_token.restype = c.c_double
         lib.pkv_get_error.argtypes = [P, c.c_int32, c.POINTER(c.c_uint32)]
@@ -93,7 +95,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pkv_last_error_message.restype = c.c_char_p
         for name in ("kv_pool_create", "kv_pool_destroy", "kv_pool_set_fp8_scales", "kv_pool_layout",
                      "kv_pool_set_partition_tokens", "kv_pool_reserve_workspace", "paged_kv_append",
-                     "paged_decode_attention", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read"):
+                     "paged_decode_attention", "paged_decode_attention_noalloc", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read"):
             getattr(lib, name).restype = c.c_int
         _lib = lib
         return lib
@@ -266,5 +268,26 @@ def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: flo
     return out
 
 
+def paged_decode_attention_noalloc(pool: Pool, q, block_tables, context_lens, scale: float, out=None,
+                                   stream=None):
+    """paged_decode_attention with its scratch in the library's fixed 16 MiB
+    device array instead of a workspace it allocates: for callers that cannot
+    allocate device memory while decoding.  Calls share that array, so calls
+    that overlap on the GPU race; see include/pagedkv.h."""
+    import torch
+
+    qp = _dev_ptr(q, "q", torch.bfloat16, 3, (None, None, pool.d_head))
+    B, n_q = int(q.shape[0]), int(q.shape[1])
+    tp = _dev_ptr(block_tables, "block_tables", torch.int32, 2, (B, None))
+    cp = _dev_ptr(context_lens, "context_lens", torch.int32, 1, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    op = _dev_ptr(out, "out", torch.bfloat16, 3, tuple(q.shape))
+    _check(load().paged_decode_attention_noalloc(pool.handle, qp, n_q, tp, int(block_tables.shape[1]), cp, B,
+                                                 float(scale), op, _stream_handle(stream)))
+    return out
+
+
 __all__ = ["BF16", "FP8_E4M3", "Pool", "PagedKVError", "kv_pool_create", "paged_kv_append",
-           "paged_decode_attention", "kv_bytes_per_token", "load", "library_path"]
+           "paged_decode_attention", "paged_decode_attention_noalloc", "kv_bytes_per_token", "load",
+           "library_path"]

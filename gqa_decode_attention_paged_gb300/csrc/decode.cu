@@ -956,3 +956,153 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
         return fp8 ? dispatch_g<128, true>(pool, a, G, s) : dispatch_g<128, false>(pool, a, G, s);
     return fp8 ? dispatch_g<64, true>(pool, a, G, s) : dispatch_g<64, false>(pool, a, G, s);
 }
+
+// ---------------------------------------------------------------------------
+// Decode without allocation
+//
+// paged_decode_attention grows a workspace with cudaMalloc the first time a
+// call needs more.  Some callers cannot allocate at that point: a serving
+// engine that hands nearly all free HBM to its KV pool at start-up (as the
+// memory-budget discussion of the pages describes engines doing) may have no
+// room left, and cudaMalloc/cudaFree can synchronise the whole device, which
+// a caller interleaving other streams' work cannot afford in its decode loop.
+// paged_decode_attention_noalloc runs the same kernel with its scratch in a
+// fixed, file-scope device array instead, so it never allocates.
+// ---------------------------------------------------------------------------
+
+constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB, held by every GPU that loads the library
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace pkv {
+
+constexpr int kMaxDevices = 64;
+static std::mutex g_noalloc_mu;
+static void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on `device` (which must be current).
+// Looked up once per device with cudaGetSymbolAddress; in host code the
+// array's name is only a host-side stand-in, never a device address.
+static pkv_status noalloc_scratch(int device, void **out)
+{
+    if (device < 0 || device >= kMaxDevices)
+        return fail(PKV_EUNSUPPORTED, "paged_decode_attention_noalloc: device ordinal %d >= %d", device, kMaxDevices);
+    std::lock_guard<std::mutex> g(g_noalloc_mu);
+    if (!g_noalloc_ptr[device]) {
+        void *ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
+        g_noalloc_ptr[device] = ptr;
+    }
+    *out = g_noalloc_ptr[device];
+    return PKV_OK;
+}
+
+template <int D, int G, bool FP8>
+static pkv_status launch_decode_noalloc(pkv_pool *pool, DecodeArgs a, uint8_t *scratch, cudaStream_t s)
+{
+    using C = Cfg<D, G, FP8>;
+    int grid = 0;
+    size_t smem = 0;
+    pkv_status st = decode_grid<D, G, FP8>(pool, a.batch, &grid, &smem);
+    if (st != PKV_OK) return st;
+    const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
+    if (L.total > kNoAllocScratchBytes)
+        return fail(PKV_ERANGE,
+                    "paged_decode_attention_noalloc: this call needs %zu bytes of scratch but the static array "
+                    "holds %zu; use paged_decode_attention (it grows a workspace) or a smaller batch",
+                    L.total, kNoAllocScratchBytes);
+    a.counters = reinterpret_cast<int *>(scratch + L.counters);
+    a.ws_ml = reinterpret_cast<float2 *>(scratch + L.ml);
+    a.ws_o = reinterpret_cast<float *>(scratch + L.o);
+    // The array keeps the previous call's contents; the piece counters must
+    // start at zero.
+    cudaError_t e = cudaMemsetAsync(a.counters, 0, sizeof(int) * (size_t)a.batch * a.n_kv, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(noalloc counters)");
+    {
+        std::lock_guard<std::mutex> g(pool->mu);
+        pool->launches[kDecode] += 1;
+    }
+    decode_kernel<D, G, FP8><<<(unsigned)grid, C::kThreads, smem, s>>>(pool->tm_k, pool->tm_v, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch (noalloc)");
+    return PKV_OK;
+}
+
+template <int D, bool FP8>
+static pkv_status dispatch_g_noalloc(pkv_pool *pool, const DecodeArgs &a, int G, uint8_t *scratch, cudaStream_t s)
+{
+    switch (G) {
+    case 1: return launch_decode_noalloc<D, 1, FP8>(pool, a, scratch, s);
+    case 2: return launch_decode_noalloc<D, 2, FP8>(pool, a, scratch, s);
+    case 4: return launch_decode_noalloc<D, 4, FP8>(pool, a, scratch, s);
+    case 8: return launch_decode_noalloc<D, 8, FP8>(pool, a, scratch, s);
+    }
+    return fail(PKV_EUNSUPPORTED, "decode: group size %d unsupported (1, 2, 4 or 8)", G);
+}
+
+}  // namespace pkv
+
+extern "C" pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void *q, int32_t n_q,
+                                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                                     const int32_t *context_lens, int32_t batch, float scale,
+                                                     void *out, void *stream)
+{
+    if (!pool) return fail(PKV_EINVAL, "paged_decode_attention_noalloc: NULL pool");
+    if (batch < 0) return fail(PKV_EINVAL, "paged_decode_attention_noalloc: batch < 0");
+    if (n_q <= 0 || n_q % pool->n_kv)
+        return fail(PKV_EINVAL, "paged_decode_attention_noalloc: n_q %d is not a positive multiple of n_kv %d", n_q,
+                    pool->n_kv);
+    const int G = n_q / pool->n_kv;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(PKV_EUNSUPPORTED, "paged_decode_attention_noalloc: n_q / n_kv = %d unsupported (1, 2, 4, 8)", G);
+    if (max_blocks_per_seq <= 0 || max_blocks_per_seq > (1 << 24))
+        return fail(PKV_EINVAL, "paged_decode_attention_noalloc: max_blocks_per_seq %d out of range",
+                    max_blocks_per_seq);
+    if (!isfinite(scale)) return fail(PKV_EINVAL, "paged_decode_attention_noalloc: scale is not finite");
+    if (batch == 0) return PKV_OK;
+    if (batch > kMaxBatch)
+        return fail(PKV_EUNSUPPORTED, "paged_decode_attention_noalloc: batch %d > %d", batch, kMaxBatch);
+    if ((int64_t)batch * pool->n_kv * max_blocks_per_seq >= ((int64_t)1 << 30))
+        return fail(PKV_EUNSUPPORTED, "paged_decode_attention_noalloc: batch x n_kv x max_blocks_per_seq too large");
+    if (!q || !block_tables || !context_lens || !out)
+        return fail(PKV_EINVAL, "paged_decode_attention_noalloc: NULL device pointer");
+    if (((uintptr_t)q | (uintptr_t)out) & 15u)
+        return fail(PKV_EINVAL, "paged_decode_attention_noalloc: q and out must be 16-byte aligned");
+    if (((uintptr_t)block_tables | (uintptr_t)context_lens) & 3u)
+        return fail(PKV_EINVAL, "paged_decode_attention_noalloc: tables and lengths must be 4-byte aligned");
+    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
+    if (fp8 && !pool->scales_set)
+        return fail(PKV_EINVAL, "paged_decode_attention_noalloc: FP8 pool needs kv_pool_set_fp8_scales first");
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attention_noalloc: cudaGetDevice");
+    if (cur != pool->device)
+        return fail(PKV_EINVAL, "paged_decode_attention_noalloc: make the pool's device (%d) current, not %d",
+                    pool->device, cur);
+    void *scratch = nullptr;
+    pkv_status st = noalloc_scratch(cur, &scratch);
+    if (st != PKV_OK) return st;
+
+    DecodeArgs a;
+    a.num_blocks = pool->num_blocks;
+    a.n_kv = pool->n_kv;
+    a.n_q = n_q;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.block_tables = block_tables;
+    a.W = max_blocks_per_seq;
+    a.context_lens = context_lens;
+    a.batch = batch;
+    a.qscale = scale * kLog2e;
+    a.scales = pool->scales;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.counters = nullptr;
+    a.ws_ml = nullptr;
+    a.ws_o = nullptr;
+    a.slice_blocks = pool->partition_tokens / kBlockSize;
+    a.err = pool->err;
+    uint8_t *sp = static_cast<uint8_t *>(scratch);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pool->d_head == 128)
+        return fp8 ? dispatch_g_noalloc<128, true>(pool, a, G, sp, s) : dispatch_g_noalloc<128, false>(pool, a, G, sp, s);
+    return fp8 ? dispatch_g_noalloc<64, true>(pool, a, G, sp, s) : dispatch_g_noalloc<64, false>(pool, a, G, sp, s);
+}

@@ -191,6 +191,34 @@ pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int32_t n_q,
                                   const int32_t *context_lens, int32_t batch, float scale,
                                   void *out, void *stream);
 
+/* paged_decode_attention without any allocation.  The pages have no
+ * counterpart to this call; it exists for callers that cannot allocate
+ * device memory when they decode: an engine that reserved nearly all free
+ * HBM for its KV pool at start-up has no room for a workspace, and
+ * cudaMalloc/cudaFree may synchronise the whole device, which a caller
+ * running other streams' work cannot accept in its decode loop.
+ * Same arguments, results and errors as paged_decode_attention, but the
+ * split-KV scratch is a fixed 16 MiB array inside the library (every GPU
+ * that loads the library holds it until the process exits) instead of the
+ * pool's workspace; nothing is allocated and no allocating routine is called.
+ *   - A call whose scratch would exceed 16 MiB (roughly: more pieces x query
+ *     heads x d_head x 4 bytes than fit) fails with PKV_ERANGE before
+ *     launching; use paged_decode_attention then.
+ *   - The pool's device must be current.  The first call on each device
+ *     looks the array's device address up (cudaGetSymbolAddress); make that
+ *     first call before any stream capture.
+ *   - All calls, from every pool and stream, share the one array and it
+ *     keeps the last call's contents; each call clears the counters it needs
+ *     (cudaMemsetAsync on `stream`).  Calls that overlap on the GPU race on
+ *     the array and give wrong results: order them on one stream, or
+ *     serialise them.
+ * Errors: as paged_decode_attention, plus ERANGE (scratch too small) and
+ * EINVAL (pool's device not current). */
+pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void *q, int32_t n_q,
+                                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t *context_lens, int32_t batch, float scale,
+                                          void *out, void *stream);
+
 /* KV-cache bytes per token: 2 x layers x n_kv x d_head x bytes_per_value
  * ("KV cache, PagedAttention and FlashAttention", Problem 3, "The concepts";
  * "Memory Management in LLM Serving Systems", "KV cache sizing").
