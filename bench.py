@@ -1,8 +1,10 @@
 """Benchmark: paged GQA decode attention on GB300.
 
 One step = the whole hot path over one batch: append the new token of every
-sequence into the paged pool, then decode attention for every sequence
-(decode kernel + split-KV merge).  The default workload is the Llama3-8B
+sequence into the paged pool and decode attention for every sequence, in one
+launch (paged_decode_step; the split-KV merge runs inside the kernel).  The
+same step as two calls (paged_kv_append, paged_decode_attention) is timed
+beside it.  The default workload is the Llama3-8B
 attention shape (n_q=32, n_kv=8, d_head=128, batch 64, lengths uniform in
 [1024, 2048], bf16 KV); ``--workload`` picks another.
 
@@ -376,6 +378,10 @@ def run_ours(args):
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device) if args.flush_l2 else None
 
     def step():
+        # one pass of the hot path: append every sequence's new token, decode (one launch)
+        pkv.paged_decode_step(pool, q, k_new, v_new, tables, lens, float(w.scale), out, stream)
+
+    def step_two_calls():
         pkv.paged_kv_append(pool, k_new, v_new, slots, stream)
         pkv.paged_decode_attention(pool, q, tables, lens, float(w.scale), out, stream)
 
@@ -425,6 +431,18 @@ def run_ours(args):
     assert pool.get_error() == 0, "device error in the timed region"
     max_ms = allreduce_max(elapsed_ms, world, device)
     total_bytes = allreduce_sum(step_bytes * args.steps, world, device)
+
+    # the same step as two calls (paged_kv_append, then paged_decode_attention), for comparison
+    n2 = max(1, min(args.steps, 1000))
+    for _ in range(3):
+        step_two_calls()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(n2):
+        step_two_calls()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    two_call_ms = ev0.elapsed_time(ev1) / n2
     value = total_bytes / (max_ms / 1e3) / 1e9
     calls = allreduce_sum(args.steps, world, device) / (max_ms / 1e3)
 
@@ -432,21 +450,14 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-        h = {"k": pin(w.step_k.view(np.int16)), "v": pin(w.step_v.view(np.int16)), "s": pin(w.step_slots),
-             "q": pin(w.q.view(np.int16)), "t": pin(w.block_tables), "c": pin(w.context_lens)}
-        h_out = torch.empty(tuple(q.shape), dtype=torch.int16).pin_memory()
-        d = {k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in h.items()}
-        h2d = sum(v.numel() * v.element_size() for v in h.values())
+        h_q, h_k, h_v = (pin(x.view(np.int16)).view(torch.bfloat16) for x in (w.q, w.step_k, w.step_v))
+        h_t, h_c = pin(w.block_tables), pin(w.context_lens)
+        h_out = torch.empty(tuple(q.shape), dtype=torch.bfloat16).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_t, h_c))
         d2h = h_out.numel() * h_out.element_size()
 
-        def e2e_step():
-            for k in h:
-                d[k].copy_(h[k], non_blocking=True)
-            pkv.paged_kv_append(pool, d["k"].view(torch.bfloat16), d["v"].view(torch.bfloat16), d["s"], stream)
-            o = pkv.paged_decode_attention(pool, d["q"].view(torch.bfloat16), d["t"], d["c"], float(w.scale),
-                                           out, stream)
-            h_out.copy_(o.view(torch.int16), non_blocking=True)
-            stream.synchronize()  # the host reads the step's result
+        def e2e_step():  # copies in, appends, decodes, copies out, synchronises
+            pkv.paged_decode_step_host(pool, h_q, h_k, h_v, h_t, h_c, float(w.scale), h_out, stream)
 
         for _ in range(min(args.warmup, 10)):
             e2e_step()
@@ -460,7 +471,8 @@ def run_ours(args):
         e2e_total = allreduce_sum(step_bytes * n_e2e, world, device)
         e2e = {"value": e2e_total / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": n_e2e, "ms_per_step": 1e3 * e2e_s / n_e2e,
-               "calls_per_s": allreduce_sum(n_e2e, world, device) / e2e_s}
+               "calls_per_s": allreduce_sum(n_e2e, world, device) / e2e_s,
+               "call": "paged_decode_step_host (pinned host inputs and output)"}
 
     if rank != 0:
         pool.close()
@@ -485,8 +497,6 @@ def run_ours(args):
 
     peak, peak_note = measured_peaks()
     dec_ms = tm["decode_ms"] / max(1, tm["timed_decode"])
-    mer_ms = tm["merge_ms"] / max(1, tm["timed_merge"]) if tm["timed_merge"] else 0.0
-    app_ms = tm["append_ms"] / max(1, tm["timed_append"])
     sha = kernel_source_sha()
     traffic, traffic_note = ncu_traffic(w.name, sha)
     achieved = step_bytes / (dec_ms / 1e3) / 1e9
@@ -516,7 +526,9 @@ def run_ours(args):
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "bytes_per_launch": step_bytes, "avg_launch_ms": dec_ms, "peak_source": peak_note,
                      "traffic_source": traffic_note, "kernel_source_sha": sha},
-        "kernels_ms_avg": {"decode_kernel": dec_ms, "merge_kernel": mer_ms, "append_kernel": app_ms},
+        "kernels_ms_avg": {"decode_kernel": dec_ms},
+        "step_call": "paged_decode_step (append + decode, one launch)",
+        "two_call_step_ms": two_call_ms,
         "step_frac_of_peak": value / world / peak,
         "gpu_launches": int(tm["launches"]),
         "clocks": clocks,

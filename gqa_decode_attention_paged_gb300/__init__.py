@@ -84,6 +84,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                                c.c_float, P, P]
         lib.paged_decode_attention_noalloc.argtypes = [P, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                                        c.c_float, P, P]
+        lib.paged_decode_step.argtypes = [P, P, P, P, c.c_int32, P, c.c_int32, P, c.c_int32, c.c_float, P, P]
+        lib.paged_decode_step_host.argtypes = [P, P, P, P, c.c_int32, P, c.c_int32, P, c.c_int32, c.c_float,
+                                               P, P]
         lib.kv_bytes_per_token.argtypes = [c.c_int32, c.c_int32, c.c_int32, c.c_double]
         lib.kv_bytes_per_token.restype = c.c_double
         lib.pkv_get_error.argtypes = [P, c.c_int32, c.POINTER(c.c_uint32)]
@@ -95,7 +98,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pkv_last_error_message.restype = c.c_char_p
         for name in ("kv_pool_create", "kv_pool_destroy", "kv_pool_set_fp8_scales", "kv_pool_layout",
                      "kv_pool_set_partition_tokens", "kv_pool_reserve_workspace", "paged_kv_append",
-                     "paged_decode_attention", "paged_decode_attention_noalloc", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read"):
+                     "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
+                     "paged_decode_step_host", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read"):
             getattr(lib, name).restype = c.c_int
         _lib = lib
         return lib
@@ -268,6 +272,55 @@ def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: flo
     return out
 
 
+def paged_decode_step(pool: Pool, q, k_new, v_new, block_tables, context_lens, scale: float, out=None,
+                      stream=None):
+    """Append each sequence's newest token (k_new, v_new: bf16 [B, n_kv, d])
+    at position context_lens[b]-1 and decode, in one launch."""
+    import torch
+
+    qp = _dev_ptr(q, "q", torch.bfloat16, 3, (None, None, pool.d_head))
+    B, n_q = int(q.shape[0]), int(q.shape[1])
+    kp = _dev_ptr(k_new, "k_new", torch.bfloat16, 3, (B, pool.n_kv, pool.d_head))
+    vp = _dev_ptr(v_new, "v_new", torch.bfloat16, 3, (B, pool.n_kv, pool.d_head))
+    tp = _dev_ptr(block_tables, "block_tables", torch.int32, 2, (B, None))
+    cp = _dev_ptr(context_lens, "context_lens", torch.int32, 1, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    op = _dev_ptr(out, "out", torch.bfloat16, 3, tuple(q.shape))
+    _check(load().paged_decode_step(pool.handle, qp, kp, vp, n_q, tp, int(block_tables.shape[1]), cp, B,
+                                    float(scale), op, _stream_handle(stream)))
+    return out
+
+
+def _host_ptr(t, name, dtype, shape):
+    import torch
+
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a CPU torch tensor")
+    if t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {shape}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def paged_decode_step_host(pool: Pool, q, k_new, v_new, block_tables, context_lens, scale: float, out,
+                           stream=None):
+    """paged_decode_step from host tensors (pin them for asynchronous copies):
+    copies in, steps, copies ``out`` back and synchronises the stream."""
+    import torch
+
+    B, n_q, D = (int(x) for x in q.shape)
+    W = int(block_tables.shape[1])
+    args = (_host_ptr(q, "q", torch.bfloat16, (B, n_q, D)),
+            _host_ptr(k_new, "k_new", torch.bfloat16, (B, pool.n_kv, D)),
+            _host_ptr(v_new, "v_new", torch.bfloat16, (B, pool.n_kv, D)))
+    tp = _host_ptr(block_tables, "block_tables", torch.int32, (B, W))
+    cp = _host_ptr(context_lens, "context_lens", torch.int32, (B,))
+    op = _host_ptr(out, "out", torch.bfloat16, (B, n_q, D))
+    _check(load().paged_decode_step_host(pool.handle, *args, n_q, tp, W, cp, B, float(scale), op,
+                                         _stream_handle(stream)))
+    return out
+
+
 def paged_decode_attention_noalloc(pool: Pool, q, block_tables, context_lens, scale: float, out=None,
                                    stream=None):
     """paged_decode_attention with its scratch in the library's fixed 16 MiB
@@ -289,5 +342,6 @@ def paged_decode_attention_noalloc(pool: Pool, q, block_tables, context_lens, sc
 
 
 __all__ = ["BF16", "FP8_E4M3", "Pool", "PagedKVError", "kv_pool_create", "paged_kv_append",
-           "paged_decode_attention", "paged_decode_attention_noalloc", "kv_bytes_per_token", "load",
+           "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
+           "paged_decode_step_host", "kv_bytes_per_token", "load",
            "library_path"]

@@ -44,6 +44,7 @@
 //     MMAs; the K scale is folded into the score scale and the V scale into
 //     the final normalisation.
 #include <algorithm>
+#include <type_traits>
 #include <mutex>
 
 #include "pkv_internal.cuh"
@@ -70,6 +71,10 @@ struct DecodeArgs {
     float *ws_o;           // workspace [slots][G][D], unnormalised
     int slice_blocks;      // blocks per slice; 0 = ceil(total / all warps)
     unsigned *err;
+    // fused step only: the token at position context_len-1 of each sequence,
+    // [batch][n_kv][D] bf16, and the pool arrays it is appended to
+    const __nv_bfloat16 *k_new, *v_new;
+    uint8_t *k_pool, *v_pool;
 };
 
 // Shared-memory geometry of one (block, KV head) tile as the TMA boxes lay it
@@ -116,7 +121,8 @@ struct Cfg {
     static constexpr int kBars = kRing;
     static constexpr int kPhys = kBars + NW * kStages * 8;
     static constexpr int kScratch = kPhys + NW * kStages * 4;  // [NW][16] floats: merge max/sum per head
-    static constexpr int kWarpTot = kScratch + NW * 16 * 4;
+    static constexpr int kNewRow = kScratch + NW * 16 * 4;     // [NW][2 * D * 2] bytes: fused step's new K, V rows
+    static constexpr int kWarpTot = kNewRow + NW * 4 * D;
     static constexpr int kPs = kWarpTot + 4 * NW;  // ps[batch + 1], then clamped lengths cl[batch]
     static size_t smem_bytes(int batch) { return 1024 + (size_t)kPs + 4 * (size_t)(2 * batch + 1); }
     static_assert(G <= 8, "at most 8 query heads per KV head");
@@ -460,6 +466,78 @@ __device__ __noinline__ void merge_pieces(MergeRefs a, int b, int g, int s_first
     if (lane == 0) a.counters[b * a.n_kv + g] = 0;
 }
 
+// Fused step, part 1 (start of the piece that holds a sequence's last
+// block): lane l < 2*NCH starts an asynchronous 16-byte copy of chunk l % NCH
+// of the new K row (l < NCH) or V row into the warp's row buffer in shared
+// memory, so nothing stays live in registers across the block loop.
+template <int D>
+__device__ __forceinline__ void fetch_new_row(const DecodeArgs &a, int b, int g, int lane, uint8_t *rowbuf)
+{
+    constexpr int NCH = D / 8;
+    if (lane < 2 * NCH) {
+        const __nv_bfloat16 *src = (lane >= NCH ? a.v_new : a.k_new) + ((int64_t)b * a.n_kv + g) * D + (lane % NCH) * 8;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(rowbuf + lane * 16)), "l"(src)
+                     : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// ... and its bytes as the pool stores them: the bf16 copy, or for an E4M3
+// pool E4M3(fp32(x) / scale) rounded to nearest even and saturated, from
+// __fdiv_rn and a satfinite convert, exactly what paged_kv_append writes.
+template <int D, bool FP8>
+__device__ __forceinline__ uint4 prepared_new_row(const DecodeArgs &a, int g, int lane, const uint8_t *rowbuf)
+{
+    constexpr int NCH = D / 8;
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
+    if (lane >= 2 * NCH) return make_uint4(0, 0, 0, 0);
+    const uint4 chunk = *reinterpret_cast<const uint4 *>(rowbuf + lane * 16);
+    if constexpr (!FP8) {
+        return chunk;
+    } else {
+        const float sc = a.scales[(lane >= NCH ? a.n_kv : 0) + g];
+        const uint32_t w[4] = {chunk.x, chunk.y, chunk.z, chunk.w};
+        uint32_t q[2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = bf16x2_to_f32x2(w[i]);
+            const uint32_t e = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(f.x, sc), __fdiv_rn(f.y, sc)),
+                                                        __NV_SATFINITE, __NV_E4M3);
+            if (i & 1) q[i >> 1] |= e << 16;
+            else q[i >> 1] = e;
+        }
+        return make_uint4(q[0], q[1], 0, 0);
+    }
+}
+
+// Fused step, part 2 (when the block has landed): write the prepared row into
+// the pool -- the append -- and into row r of the block's staged tiles, which
+// the TMA filled before the append.
+template <int D, bool FP8>
+__device__ __forceinline__ void append_row(const DecodeArgs &a, int g, int phys, int r, int lane, uint4 prepared,
+                                           uint8_t *stage)
+{
+    using Gm = Geo<D, FP8>;
+    constexpr int NCH = D / 8;  // 8-element chunks per row
+    if (lane >= 2 * NCH) return;
+    const bool isv = lane >= NCH;
+    const int c = lane % NCH;
+    const int64_t row = ((int64_t)phys * a.n_kv + g) * kBlockSize + r;
+    uint8_t *tile = stage + (isv ? Gm::TILE : 0);
+    uint8_t *pool = isv ? a.v_pool : a.k_pool;
+    if constexpr (!FP8) {
+        // chunk c is 16 bytes of the 256/128-byte row: box c / 8, 16-byte unit c % 8
+        const uint32_t off = (c >> 3) * Gm::RGN + swz<128>(r * 128 + (c & 7) * 16);
+        *reinterpret_cast<uint4 *>(tile + off) = prepared;
+        *reinterpret_cast<uint4 *>(pool + row * D * 2 + c * 16) = prepared;
+    } else {
+        const uint2 q = make_uint2(prepared.x, prepared.y);
+        *reinterpret_cast<uint2 *>(tile + swz<Gm::BOXB>(r * Gm::ROWB + c * 8)) = q;
+        *reinterpret_cast<uint2 *>(pool + row * D + c * 8) = q;
+    }
+}
+
 // Decode kernel: per-warp TMA ring, tensor-core scores and P.V.
 //
 // Per 16-token block a warp computes S^T[16 tokens x 8 heads] = K . Q^T with
@@ -472,7 +550,7 @@ __device__ __noinline__ void merge_pieces(MergeRefs a, int b, int g, int s_first
 // pairs in registers; the MMA's k (and, for V, its m) order is a fixed
 // permutation of d applied identically to both operands and undone when the
 // output is written, so the products are unchanged.
-template <int D, int G, bool FP8>
+template <int D, int G, bool FP8, bool APPEND = false>
 __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, DecodeArgs a)
 {
@@ -492,6 +570,7 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
     int *warp_tot = reinterpret_cast<int *>(smem + C::kWarpTot);
     int32_t *ps = reinterpret_cast<int32_t *>(smem + C::kPs);
     float *scratch = reinterpret_cast<float *>(smem + C::kScratch) + warp * 16;
+    uint8_t *rowbuf = smem + C::kNewRow + warp * 4 * D;  // fused step: this warp's new K and V rows
 
     if (tid == 0) {
         prefetch_tensormap(&tm_k);
@@ -584,12 +663,21 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
         if (have_nx) load_q_frags<D, G, FP8>(a, nx.b, nx.g, g8, c4, qn);
         const float qs = a.qscale * (FP8 ? a.scales[pc.g] : 1.0f);
         const int C_len = cl[pc.b];
+        // Fused step: the warp owning the block of position C_len-1 appends the
+        // new token (prepared here, written when that block has landed).
+        const bool has_new = APPEND && pc.j1 == pc.nblk && C_len > 0;
+        if constexpr (APPEND) {
+            if (has_new) fetch_new_row<D>(a, pc.b, pc.g, lane, rowbuf);
+        }
         float o[NT][4];
 #pragma unroll
         for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // heads 2c, 2c+1
 
-        for (int j = pc.j0; j < pc.j1; ++j) {
+        // One block: wait for its stage, (fused step, last block only) patch in
+        // the new token, then scores, softmax and P.V.  The patching variant is
+        // a separate instantiation so the hot loop carries no per-block check.
+        auto block = [&](int j, auto patch) {
             const int sidx = consumed % S;
             const uint32_t parity = (uint32_t)(consumed / S) & 1u;
             if (!aborted) {
@@ -604,6 +692,11 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
                 const uint32_t kb = smem_u32(ring + sidx * Gm::STAGE);
                 const uint32_t vb = kb + Gm::TILE;
                 const int nv = min(kBlockSize, C_len - j * kBlockSize);
+                if constexpr (decltype(patch)::value) {
+                    append_row<D, FP8>(a, pc.g, phys_st[sidx], nv - 1, lane,
+                                       prepared_new_row<D, FP8>(a, pc.g, lane, rowbuf), ring + sidx * Gm::STAGE);
+                    __syncwarp();
+                }
                 // ---- S^T = K . Q^T ----
                 float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
                 if constexpr (!FP8) {
@@ -705,6 +798,11 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
             __syncwarp();
             ++consumed;
             if (!aborted) issue_next();
+        };
+        const int j_plain = has_new ? pc.j1 - 1 : pc.j1;  // has_new: the piece ends with the last block
+        for (int j = pc.j0; j < j_plain; ++j) block(j, std::false_type{});
+        if constexpr (APPEND) {
+            if (has_new) block(j_plain, std::true_type{});
         }
 
         // ---- piece end ----
@@ -799,11 +897,11 @@ static int64_t max_slots(pkv_pool *pool, int batch, int n_kv, int max_blocks_per
 }
 
 // Persistent grid of the decode kernel for (d_head, G, dtype) at `batch`.
-template <int D, int G, bool FP8>
+template <int D, int G, bool FP8, bool APPEND = false>
 static pkv_status decode_grid(pkv_pool *pool, int batch, int *grid, size_t *smem)
 {
     using C = Cfg<D, G, FP8>;
-    auto kern = decode_kernel<D, G, FP8>;
+    auto kern = decode_kernel<D, G, FP8, APPEND>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -955,6 +1053,153 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
     if (pool->d_head == 128)
         return fp8 ? dispatch_g<128, true>(pool, a, G, s) : dispatch_g<128, false>(pool, a, G, s);
     return fp8 ? dispatch_g<64, true>(pool, a, G, s) : dispatch_g<64, false>(pool, a, G, s);
+}
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// Fused step: append each sequence's newest token and decode, one launch
+// ---------------------------------------------------------------------------
+
+template <int D, int G, bool FP8>
+static pkv_status launch_step(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
+{
+    using C = Cfg<D, G, FP8>;
+    int grid = 0;
+    size_t smem = 0;
+    pkv_status st = decode_grid<D, G, FP8, true>(pool, a.batch, &grid, &smem);
+    if (st != PKV_OK) return st;
+    const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
+    st = ensure_workspace(pool, L.total);
+    if (st != PKV_OK) return st;
+    uint8_t *ws = static_cast<uint8_t *>(pool->ws);
+    a.counters = reinterpret_cast<int *>(ws + L.counters);
+    a.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
+    a.ws_o = reinterpret_cast<float *>(ws + L.o);
+    LaunchScope ls(pool, kDecode, s);
+    decode_kernel<D, G, FP8, true><<<(unsigned)grid, C::kThreads, smem, s>>>(pool->tm_k, pool->tm_v, a);
+    cudaError_t e = cudaGetLastError();
+    ls.done();
+    if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
+    return PKV_OK;
+}
+
+template <int D, bool FP8>
+static pkv_status dispatch_step(pkv_pool *pool, const DecodeArgs &a, int G, cudaStream_t s)
+{
+    switch (G) {
+    case 1: return launch_step<D, 1, FP8>(pool, a, s);
+    case 2: return launch_step<D, 2, FP8>(pool, a, s);
+    case 4: return launch_step<D, 4, FP8>(pool, a, s);
+    case 8: return launch_step<D, 8, FP8>(pool, a, s);
+    }
+    return fail(PKV_EUNSUPPORTED, "decode step: group size %d unsupported (1, 2, 4 or 8)", G);
+}
+
+// Argument checks shared by the two step entry points (device pointers).
+static pkv_status check_step_args(const pkv_pool *pool, const char *who, int n_q, int max_blocks_per_seq, int batch,
+                                  float scale)
+{
+    if (!pool) return fail(PKV_EINVAL, "%s: NULL pool", who);
+    if (batch < 0) return fail(PKV_EINVAL, "%s: batch < 0", who);
+    if (n_q <= 0 || n_q % pool->n_kv)
+        return fail(PKV_EINVAL, "%s: n_q %d is not a positive multiple of n_kv %d", who, n_q, pool->n_kv);
+    const int G = n_q / pool->n_kv;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(PKV_EUNSUPPORTED, "%s: n_q / n_kv = %d unsupported (1, 2, 4, 8)", who, G);
+    if (max_blocks_per_seq <= 0 || max_blocks_per_seq > (1 << 24))
+        return fail(PKV_EINVAL, "%s: max_blocks_per_seq %d out of range", who, max_blocks_per_seq);
+    if (!isfinite(scale)) return fail(PKV_EINVAL, "%s: scale is not finite", who);
+    if (batch > kMaxBatch) return fail(PKV_EUNSUPPORTED, "%s: batch %d > %d", who, batch, kMaxBatch);
+    if ((int64_t)batch * pool->n_kv * max_blocks_per_seq >= ((int64_t)1 << 30))
+        return fail(PKV_EUNSUPPORTED, "%s: batch x n_kv x max_blocks_per_seq too large", who);
+    if (pool->dtype == PKV_FP8_E4M3 && !pool->scales_set)
+        return fail(PKV_EINVAL, "%s: FP8 pool needs kv_pool_set_fp8_scales first", who);
+    return PKV_OK;
+}
+
+static pkv_status step_device(pkv_pool *pool, const void *q, const void *k_new, const void *v_new, int n_q,
+                              const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                              int batch, float scale, void *out, cudaStream_t s)
+{
+    const int G = n_q / pool->n_kv;
+    DecodeArgs a;
+    a.num_blocks = pool->num_blocks;
+    a.n_kv = pool->n_kv;
+    a.n_q = n_q;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.block_tables = block_tables;
+    a.W = max_blocks_per_seq;
+    a.context_lens = context_lens;
+    a.batch = batch;
+    a.qscale = scale * kLog2e;
+    a.scales = pool->scales;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.counters = nullptr;
+    a.ws_ml = nullptr;
+    a.ws_o = nullptr;
+    a.slice_blocks = pool->partition_tokens / kBlockSize;
+    a.err = pool->err;
+    a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    a.k_pool = static_cast<uint8_t *>(pool->k);
+    a.v_pool = static_cast<uint8_t *>(pool->v);
+    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
+    if (pool->d_head == 128) return fp8 ? dispatch_step<128, true>(pool, a, G, s) : dispatch_step<128, false>(pool, a, G, s);
+    return fp8 ? dispatch_step<64, true>(pool, a, G, s) : dispatch_step<64, false>(pool, a, G, s);
+}
+
+}  // namespace pkv
+
+extern "C" pkv_status paged_decode_step(pkv_pool *pool, const void *q, const void *k_new, const void *v_new,
+                                        int32_t n_q, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t *context_lens, int32_t batch, float scale, void *out,
+                                        void *stream)
+{
+    pkv_status st = check_step_args(pool, "paged_decode_step", n_q, max_blocks_per_seq, batch, scale);
+    if (st != PKV_OK || batch == 0) return st;
+    if (!q || !k_new || !v_new || !block_tables || !context_lens || !out)
+        return fail(PKV_EINVAL, "paged_decode_step: NULL device pointer");
+    if (((uintptr_t)q | (uintptr_t)out | (uintptr_t)k_new | (uintptr_t)v_new) & 15u)
+        return fail(PKV_EINVAL, "paged_decode_step: q, k_new, v_new and out must be 16-byte aligned");
+    if (((uintptr_t)block_tables | (uintptr_t)context_lens) & 3u)
+        return fail(PKV_EINVAL, "paged_decode_step: tables and lengths must be 4-byte aligned");
+    return step_device(pool, q, k_new, v_new, n_q, block_tables, max_blocks_per_seq, context_lens, batch, scale,
+                       out, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host, const void *k_new_host,
+                                             const void *v_new_host, int32_t n_q, const int32_t *block_tables_host,
+                                             int32_t max_blocks_per_seq, const int32_t *context_lens_host,
+                                             int32_t batch, float scale, void *out_host, void *stream)
+{
+    pkv_status st = check_step_args(pool, "paged_decode_step_host", n_q, max_blocks_per_seq, batch, scale);
+    if (st != PKV_OK || batch == 0) return st;
+    if (!q_host || !k_new_host || !v_new_host || !block_tables_host || !context_lens_host || !out_host)
+        return fail(PKV_EINVAL, "paged_decode_step_host: NULL host pointer");
+    const size_t D = pool->d_head;
+    const size_t bq = (size_t)batch * n_q * D * 2, bkv = (size_t)batch * pool->n_kv * D * 2;
+    const size_t bt = (size_t)batch * max_blocks_per_seq * 4, bl = (size_t)batch * 4;
+    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t o_q = 0, o_k = al(bq), o_v = o_k + al(bkv), o_t = o_v + al(bkv), o_l = o_t + al(bt),
+                 o_o = o_l + al(bl), total = o_o + al(bq);
+    st = ensure_staging(pool, total);
+    if (st != PKV_OK) return st;
+    uint8_t *d = static_cast<uint8_t *>(pool->stage);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const void *srcs[5] = {q_host, k_new_host, v_new_host, block_tables_host, context_lens_host};
+    const size_t offs[5] = {o_q, o_k, o_v, o_t, o_l}, lens[5] = {bq, bkv, bkv, bt, bl};
+    for (int i = 0; i < 5; ++i) {
+        cudaError_t e = cudaMemcpyAsync(d + offs[i], srcs[i], lens[i], cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "paged_decode_step_host: copy in");
+    }
+    st = step_device(pool, d + o_q, d + o_k, d + o_v, n_q, reinterpret_cast<const int32_t *>(d + o_t),
+                     max_blocks_per_seq, reinterpret_cast<const int32_t *>(d + o_l), batch, scale, d + o_o, s);
+    if (st != PKV_OK) return st;
+    cudaError_t e = cudaMemcpyAsync(out_host, d + o_o, bq, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "paged_decode_step_host: copy out");
+    return PKV_OK;
 }
 
 // ---------------------------------------------------------------------------

@@ -45,6 +45,8 @@ struct pkv_pool {
     unsigned *err = nullptr;          // device sticky error word
     void *ws = nullptr;               // split-KV workspace (grow-only)
     size_t ws_bytes = 0;
+    void *stage = nullptr;            // device staging for paged_decode_step_host (grow-only)
+    size_t stage_bytes = 0;
     int partition_tokens = pkv::kDefaultPartitionTokens;
     // timing / launch accounting
     std::mutex mu;
@@ -75,6 +77,7 @@ struct LaunchScope {
 };
 
 pkv_status ensure_workspace(pkv_pool *pool, size_t bytes);
+pkv_status ensure_staging(pkv_pool *pool, size_t bytes);
 pkv_status make_tensor_maps(pkv_pool *pool);
 
 // ---------------------------------------------------------------------------

@@ -80,6 +80,24 @@ pkv_status ensure_workspace(pkv_pool *pool, size_t bytes)
     return PKV_OK;
 }
 
+pkv_status ensure_staging(pkv_pool *pool, size_t bytes)
+{
+    if (bytes <= pool->stage_bytes) return PKV_OK;
+    if (pool->stage) {
+        cudaError_t e = cudaFree(pool->stage);
+        pool->stage = nullptr;
+        pool->stage_bytes = 0;
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFree(staging)");
+    }
+    cudaError_t e = cudaMalloc(&pool->stage, bytes);
+    if (e != cudaSuccess) {
+        pool->stage = nullptr;
+        return cuda_fail(e, "cudaMalloc(staging)");
+    }
+    pool->stage_bytes = bytes;
+    return PKV_OK;
+}
+
 // The K and V arrays as 2-D tensors [blocks * n_kv * block_size rows][d_head]
 // for tiled TMA: one box = 16 token rows of one (block, KV head) tile and up
 // to 128 bytes of each row, with the matching shared-memory swizzle so that
@@ -220,6 +238,7 @@ pkv_status kv_pool_destroy(pkv_pool *pool)
     cudaFree(pool->scales);
     cudaFree(pool->err);
     cudaFree(pool->ws);
+    cudaFree(pool->stage);
     for (auto &pe : pool->pending) {
         cudaEventDestroy(pe.start);
         cudaEventDestroy(pe.stop);

@@ -191,6 +191,37 @@ pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int32_t n_q,
                                   const int32_t *context_lens, int32_t batch, float scale,
                                   void *out, void *stream);
 
+/* One decode step in one launch: append each sequence's newest token and
+ * attend over its whole cache ("The KV Cache from First Principles",
+ * "Deriving the cache": compute k_t, v_t, append them, attend with the full
+ * cached matrices; "append one row, attend over everything").
+ * Equivalent to paged_kv_append of the token at position context_lens[b]-1
+ * of every sequence b, into slot block_tables[b][(C-1)/16]*16 + (C-1)%16
+ * ("KV cache, PagedAttention and FlashAttention", Problem 4 address
+ * arithmetic), followed by paged_decode_attention -- the pool bytes and the
+ * output are the same -- but the row is written by the thread block that
+ * reads that block anyway, so the step costs one kernel launch.
+ *   k_new, v_new  device bf16 [batch][n_kv][d_head], 16-byte aligned: the
+ *                 new token of each sequence (ignored where context_len == 0).
+ *   other arguments as paged_decode_attention.  A sequence's last block must
+ *   not be shared with another sequence (as for any append).
+ * Errors: as paged_decode_attention. */
+pkv_status paged_decode_step(pkv_pool *pool, const void *q, const void *k_new, const void *v_new, int32_t n_q,
+                             const int32_t *block_tables, int32_t max_blocks_per_seq,
+                             const int32_t *context_lens, int32_t batch, float scale, void *out, void *stream);
+
+/* paged_decode_step for a caller holding its inputs in host memory: copies
+ * q, k_new, v_new, block_tables and context_lens (host pointers, same
+ * shapes; pinned memory makes the copies asynchronous) into a pool-owned
+ * device staging area (grown with cudaMalloc when a call needs more), runs
+ * the step on `stream`, copies the output back to out_host and synchronises
+ * `stream`, so out_host is ready on return.  Errors: as paged_decode_step,
+ * plus ENOMEM / ECUDA from staging and copies. */
+pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host, const void *k_new_host,
+                                  const void *v_new_host, int32_t n_q, const int32_t *block_tables_host,
+                                  int32_t max_blocks_per_seq, const int32_t *context_lens_host, int32_t batch,
+                                  float scale, void *out_host, void *stream);
+
 /* paged_decode_attention without any allocation.  The pages have no
  * counterpart to this call; it exists for callers that cannot allocate
  * device memory when they decode: an engine that reserved nearly all free
