@@ -396,8 +396,7 @@ def run_ours(args):
     sampler = ClockSampler(gpu_id_for(local_rank)) if rank == 0 else None
     if sampler:
         sampler.start()
-    pool.timing_read(reset=True)
-    pool.timing_enable(True)
+    pool.timing_read(reset=True)  # zero the launch counters; no per-kernel events in this region
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     step_ms = []
     barrier(world)
@@ -424,11 +423,22 @@ def run_ours(args):
     if sampler:
         sampler.mark("stop")
     barrier(world)
-    pool.timing_enable(False)
-    tm = pool.timing_read(reset=True)
+    launches = int(pool.timing_read(reset=True)["launches"])
     if sampler:
         sampler.stop()
     assert pool.get_error() == 0, "device error in the timed region"
+
+    # kernel durations: the same steps again, with a CUDA event pair recorded
+    # by the library around each of its launches on the launching stream
+    n_k = max(1, min(args.steps, 1000))
+    pool.timing_enable(True)
+    for _ in range(n_k):
+        if flush is not None:
+            flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    pool.timing_enable(False)
+    tm = pool.timing_read(reset=True)
     max_ms = allreduce_max(elapsed_ms, world, device)
     total_bytes = allreduce_sum(step_bytes * args.steps, world, device)
 
@@ -530,7 +540,8 @@ def run_ours(args):
         "step_call": "paged_decode_step (append + decode, one launch)",
         "two_call_step_ms": two_call_ms,
         "step_frac_of_peak": value / world / peak,
-        "gpu_launches": int(tm["launches"]),
+        "gpu_launches": launches,
+        "kernel_timing_steps": n_k,
         "clocks": clocks,
         "parity": parity,
         "cpu_baseline": cpu,

@@ -91,6 +91,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.kv_bytes_per_token.restype = c.c_double
         lib.pkv_get_error.argtypes = [P, c.c_int32, c.POINTER(c.c_uint32)]
         lib.pkv_timing_enable.argtypes = [P, c.c_int32]
+        lib.pkv_selftest_wait_timeout.argtypes = [P, c.c_uint64, P]
         lib.pkv_timing_read.argtypes = [P, c.c_int32, c.POINTER(_Timing)]
         lib.pkv_status_string.argtypes = [c.c_int]
         lib.pkv_status_string.restype = c.c_char_p
@@ -99,7 +100,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         for name in ("kv_pool_create", "kv_pool_destroy", "kv_pool_set_fp8_scales", "kv_pool_layout",
                      "kv_pool_set_partition_tokens", "kv_pool_reserve_workspace", "paged_kv_append",
                      "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
-                     "paged_decode_step_host", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read"):
+                     "paged_decode_step_host", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read",
+                     "pkv_selftest_wait_timeout"):
             getattr(lib, name).restype = c.c_int
         _lib = lib
         return lib
@@ -203,6 +205,11 @@ class Pool:
         bits = ctypes.c_uint32(0)
         _check(load().pkv_get_error(self.handle, int(clear), ctypes.byref(bits)), allow=(0, 6))
         return int(bits.value)
+
+    def selftest_wait_timeout(self, limit_ns: int = 1_000_000, stream=None):
+        """Run the bounded-wait check: a wait nothing completes gives up after
+        limit_ns and sets DEVERR_TIMEOUT (read it with get_error)."""
+        _check(load().pkv_selftest_wait_timeout(self.handle, int(limit_ns), _stream_handle(stream)))
 
     def timing_enable(self, on: bool = True):
         _check(load().pkv_timing_enable(self.handle, int(on)))

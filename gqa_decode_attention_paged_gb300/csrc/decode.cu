@@ -52,6 +52,7 @@
 namespace pkv {
 
 constexpr int kMaxBatch = 8192;
+constexpr int kMinBlocksPerWarp = 8;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -898,7 +899,7 @@ static int64_t max_slots(pkv_pool *pool, int batch, int n_kv, int max_blocks_per
 
 // Persistent grid of the decode kernel for (d_head, G, dtype) at `batch`.
 template <int D, int G, bool FP8, bool APPEND = false>
-static pkv_status decode_grid(pkv_pool *pool, int batch, int *grid, size_t *smem)
+static pkv_status decode_grid(pkv_pool *pool, int batch, int max_blocks_per_seq, int *grid, size_t *smem)
 {
     using C = Cfg<D, G, FP8>;
     auto kern = decode_kernel<D, G, FP8, APPEND>;
@@ -920,7 +921,12 @@ static pkv_status decode_grid(pkv_pool *pool, int batch, int *grid, size_t *smem
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, C::kThreads, *smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
     if (occ < 1) return fail(PKV_EUNSUPPORTED, "decode: %zu bytes of shared memory do not fit", *smem);
-    *grid = pool->num_sms * occ;
+    // At most every resident CTA, and no more CTAs than give each warp about
+    // kMinBlocksPerWarp blocks of the largest possible batch, so that small
+    // batches do not pay for launching and merging across idle warps.
+    const int64_t ub_blocks = (int64_t)batch * pool->n_kv * max_blocks_per_seq;
+    const int64_t want = (ub_blocks + (int64_t)C::NW * kMinBlocksPerWarp - 1) / ((int64_t)C::NW * kMinBlocksPerWarp);
+    *grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)pool->num_sms * occ, want));
     return PKV_OK;
 }
 
@@ -930,7 +936,7 @@ static pkv_status launch_decode(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
     using C = Cfg<D, G, FP8>;
     int grid = 0;
     size_t smem = 0;
-    pkv_status st = decode_grid<D, G, FP8>(pool, a.batch, &grid, &smem);
+    pkv_status st = decode_grid<D, G, FP8>(pool, a.batch, a.W, &grid, &smem);
     if (st != PKV_OK) return st;
     const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
     st = ensure_workspace(pool, L.total);
@@ -959,24 +965,27 @@ static pkv_status dispatch_g(pkv_pool *pool, const DecodeArgs &a, int G, cudaStr
     return fail(PKV_EUNSUPPORTED, "decode: group size %d unsupported (1, 2, 4 or 8)", G);
 }
 
+// Total warps of the decode grid (the larger of the plain and fused-step
+// kernels, which may differ in occupancy).
 template <int D, int G, bool FP8>
-static pkv_status grid_warps(pkv_pool *pool, int batch, int *warps)
+static pkv_status grid_warps(pkv_pool *pool, int batch, int max_blocks_per_seq, int *warps)
 {
     size_t smem = 0;
-    int grid = 0;
-    pkv_status st = decode_grid<D, G, FP8>(pool, batch, &grid, &smem);
-    *warps = grid * Cfg<D, G, FP8>::NW;
+    int g0 = 0, g1 = 0;
+    pkv_status st = decode_grid<D, G, FP8>(pool, batch, max_blocks_per_seq, &g0, &smem);
+    if (st == PKV_OK) st = decode_grid<D, G, FP8, true>(pool, batch, max_blocks_per_seq, &g1, &smem);
+    *warps = std::max(g0, g1) * Cfg<D, G, FP8>::NW;
     return st;
 }
 
 template <int D, bool FP8>
-static pkv_status grid_g(pkv_pool *pool, int G, int batch, int *warps)
+static pkv_status grid_g(pkv_pool *pool, int G, int batch, int max_blocks_per_seq, int *warps)
 {
     switch (G) {
-    case 1: return grid_warps<D, 1, FP8>(pool, batch, warps);
-    case 2: return grid_warps<D, 2, FP8>(pool, batch, warps);
-    case 4: return grid_warps<D, 4, FP8>(pool, batch, warps);
-    case 8: return grid_warps<D, 8, FP8>(pool, batch, warps);
+    case 1: return grid_warps<D, 1, FP8>(pool, batch, max_blocks_per_seq, warps);
+    case 2: return grid_warps<D, 2, FP8>(pool, batch, max_blocks_per_seq, warps);
+    case 4: return grid_warps<D, 4, FP8>(pool, batch, max_blocks_per_seq, warps);
+    case 8: return grid_warps<D, 8, FP8>(pool, batch, max_blocks_per_seq, warps);
     }
     return fail(PKV_EUNSUPPORTED, "decode: group size %d unsupported (1, 2, 4 or 8)", G);
 }
@@ -987,10 +996,11 @@ pkv_status decode_workspace_bytes(pkv_pool *pool, int batch, int n_q, int max_bl
     const int G = n_q / pool->n_kv;
     int warps = 0;
     const bool fp8 = pool->dtype == PKV_FP8_E4M3;
-    pkv_status st = pool->d_head == 128 ? (fp8 ? grid_g<128, true>(pool, G, batch, &warps)
-                                               : grid_g<128, false>(pool, G, batch, &warps))
-                                        : (fp8 ? grid_g<64, true>(pool, G, batch, &warps)
-                                               : grid_g<64, false>(pool, G, batch, &warps));
+    const int W = max_blocks_per_seq;
+    pkv_status st = pool->d_head == 128 ? (fp8 ? grid_g<128, true>(pool, G, batch, W, &warps)
+                                               : grid_g<128, false>(pool, G, batch, W, &warps))
+                                        : (fp8 ? grid_g<64, true>(pool, G, batch, W, &warps)
+                                               : grid_g<64, false>(pool, G, batch, W, &warps));
     if (st != PKV_OK) return st;
     *bytes = ws_layout(batch, n_q, pool->n_kv, pool->d_head,
                        max_slots(pool, batch, pool->n_kv, max_blocks_per_seq, warps)).total;
@@ -1067,7 +1077,7 @@ static pkv_status launch_step(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
     using C = Cfg<D, G, FP8>;
     int grid = 0;
     size_t smem = 0;
-    pkv_status st = decode_grid<D, G, FP8, true>(pool, a.batch, &grid, &smem);
+    pkv_status st = decode_grid<D, G, FP8, true>(pool, a.batch, a.W, &grid, &smem);
     if (st != PKV_OK) return st;
     const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
     st = ensure_workspace(pool, L.total);
@@ -1248,7 +1258,7 @@ static pkv_status launch_decode_noalloc(pkv_pool *pool, DecodeArgs a, uint8_t *s
     using C = Cfg<D, G, FP8>;
     int grid = 0;
     size_t smem = 0;
-    pkv_status st = decode_grid<D, G, FP8>(pool, a.batch, &grid, &smem);
+    pkv_status st = decode_grid<D, G, FP8>(pool, a.batch, a.W, &grid, &smem);
     if (st != PKV_OK) return st;
     const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
     if (L.total > kNoAllocScratchBytes)

@@ -134,6 +134,21 @@ pkv_status make_tensor_maps(pkv_pool *pool)
     return PKV_OK;
 }
 
+// One warp waits on an mbarrier that nothing ever arrives at, with the same
+// bounded wait the decode kernel uses; when the limit runs out it records
+// PKV_DEVERR_TIMEOUT and returns.
+__global__ void wait_selftest_kernel(unsigned *err, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbarrier_init();
+    }
+    __syncwarp();
+    const bool ok = mbar_wait_bounded(&bar, 0, limit_ns);
+    if (__any_sync(0xffffffffu, !ok) && threadIdx.x == 0) atomicOr(err, PKV_DEVERR_TIMEOUT);
+}
+
 // Defined in append.cu / decode.cu: confirm the device can run our kernels.
 pkv_status probe_kernels();
 pkv_status decode_workspace_bytes(pkv_pool *pool, int batch, int n_q, int max_blocks_per_seq, size_t *bytes);
@@ -319,6 +334,17 @@ pkv_status pkv_get_error(pkv_pool *pool, int32_t clear, uint32_t *bits)
     if (e != cudaSuccess) return cuda_fail(e, "pkv_get_error");
     if (bits) *bits = v;
     if (v) return fail(PKV_EDEVICE, "device error bits 0x%x", v);
+    return PKV_OK;
+}
+
+pkv_status pkv_selftest_wait_timeout(pkv_pool *pool, uint64_t limit_ns, void *stream)
+{
+    if (!pool) return fail(PKV_EINVAL, "pkv_selftest_wait_timeout: NULL pool");
+    if (limit_ns < 1000 || limit_ns > kWaitLimitNs)
+        return fail(PKV_ERANGE, "pkv_selftest_wait_timeout: limit must be in [1 us, 2 s]");
+    wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(pool->err, limit_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "pkv_selftest_wait_timeout launch");
     return PKV_OK;
 }
 

@@ -262,6 +262,13 @@ double kv_bytes_per_token(int32_t layers, int32_t n_kv, int32_t d_head, double b
  * bit is set, PKV_EDEVICE when some are, or ECUDA. */
 pkv_status pkv_get_error(pkv_pool *pool, int32_t clear, uint32_t *bits);
 
+/* Failure-detection check of the bounded waits every kernel uses: launches
+ * one warp on `stream` that waits on an mbarrier nothing ever arrives at,
+ * gives up after limit_ns (1 us .. 2 s), records PKV_DEVERR_TIMEOUT in the
+ * pool's error word and returns.  Nothing faults and the context stays
+ * usable; read the bit with pkv_get_error.  Errors: EINVAL, ERANGE, ECUDA. */
+pkv_status pkv_selftest_wait_timeout(pkv_pool *pool, uint64_t limit_ns, void *stream);
+
 /* Timing: while enabled, the library records a CUDA event pair around every
  * kernel it launches, on the launching stream.  pkv_timing_read synchronises
  * those events, fills *out and, if reset != 0, clears the counters.  The

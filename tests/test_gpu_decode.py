@@ -171,3 +171,18 @@ def test_workspace_reserve_then_decode():
         out = run_step(pool, w)
         ref = mirror(w).decode(w.q, w.block_tables, w.context_lens, w.scale)
         assert_close(out_f64(out), ref, "reserved")
+
+
+def test_bounded_wait_times_out_without_fault_and_context_stays_usable():
+    w = wl.build("to", 8, 2, 64, [40, 17], seed=16)
+    with make_pool(w) as pool:
+        pool.selftest_wait_timeout(2_000_000)  # 2 ms, nothing ever arrives
+        bits = pool.get_error(clear=True)
+        assert bits == pkv.DEVERR_TIMEOUT
+        assert pool.get_error() == 0
+        with pytest.raises(pkv.PagedKVError):
+            pool.selftest_wait_timeout(10)  # below the 1 us floor
+        fill(pool, w)
+        out = run_step(pool, w)  # the context still works
+        assert_close(out_f64(out), mirror(w).decode(w.q, w.block_tables, w.context_lens, w.scale), "after timeout")
+
