@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a)
 {
     constexpr int LPR = D / 8;  // lanes per row
     constexpr int E = FP8 ? 1 : 2;
+    griddep_wait();  // inputs may come from the previous kernel on the stream
+    griddep_launch_dependents();
     const int64_t rows = a.n_tokens * a.n_kv;
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int sub = (int)(gid % LPR);
@@ -92,8 +94,7 @@ static cudaError_t launch_append(const AppendArgs &a, int num_sms, cudaStream_t 
     const int64_t cap = (int64_t)num_sms * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    append_kernel<D, FP8><<<(unsigned)blocks, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(append_kernel<D, FP8>, dim3((unsigned)blocks), dim3(kThreads), 0, s, a);
 }
 
 pkv_status probe_kernels()

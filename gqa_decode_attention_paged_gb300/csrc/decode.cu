@@ -580,6 +580,8 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
         fence_mbarrier_init();
     }
     int32_t *cl = ps + a.batch + 1;
+    griddep_wait();  // inputs may come from the previous kernel on the stream
+    griddep_launch_dependents();
     scan_blocks<NW>(a, ps, cl, warp_tot);  // ends with __syncthreads; the last CTA-wide barrier
     Stream st;
     st.ps = ps;
@@ -946,8 +948,8 @@ static pkv_status launch_decode(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
     a.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
     a.ws_o = reinterpret_cast<float *>(ws + L.o);
     LaunchScope ls(pool, kDecode, s);
-    decode_kernel<D, G, FP8><<<(unsigned)grid, C::kThreads, smem, s>>>(pool->tm_k, pool->tm_v, a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(decode_kernel<D, G, FP8>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
+                               pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return PKV_OK;
@@ -1087,8 +1089,8 @@ static pkv_status launch_step(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
     a.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
     a.ws_o = reinterpret_cast<float *>(ws + L.o);
     LaunchScope ls(pool, kDecode, s);
-    decode_kernel<D, G, FP8, true><<<(unsigned)grid, C::kThreads, smem, s>>>(pool->tm_k, pool->tm_v, a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(decode_kernel<D, G, FP8, true>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
+                               pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
     return PKV_OK;
