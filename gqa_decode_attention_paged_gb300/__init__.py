@@ -84,6 +84,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                                c.c_float, P, P]
         lib.paged_decode_attention_noalloc.argtypes = [P, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                                        c.c_float, P, P]
+        lib.paged_decode_attention_prefix.argtypes = [P, P, c.c_int32, P, c.c_int32, P, c.c_int32, P, c.c_int32,
+                                                      c.c_float, P, P]
         lib.paged_decode_step.argtypes = [P, P, P, P, c.c_int32, P, c.c_int32, P, c.c_int32, c.c_float, P, P]
         lib.paged_decode_step_host.argtypes = [P, P, P, P, c.c_int32, P, c.c_int32, P, c.c_int32, c.c_float,
                                                P, P]
@@ -100,7 +102,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         for name in ("kv_pool_create", "kv_pool_destroy", "kv_pool_set_fp8_scales", "kv_pool_layout",
                      "kv_pool_set_partition_tokens", "kv_pool_reserve_workspace", "paged_kv_append",
                      "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
-                     "paged_decode_step_host", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read",
+                     "paged_decode_step_host", "paged_decode_attention_prefix", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read",
                      "pkv_selftest_wait_timeout"):
             getattr(lib, name).restype = c.c_int
         _lib = lib
@@ -279,6 +281,27 @@ def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: flo
     return out
 
 
+def paged_decode_attention_prefix(pool: Pool, q, prefix_blocks, block_tables, context_lens, scale: float,
+                                  out=None, stream=None):
+    """Cascade decode: every sequence starts with the shared prefix whose
+    physical block ids are ``prefix_blocks`` (int32, CUDA); the prefix is read
+    once for the batch.  Same result as paged_decode_attention."""
+    import torch
+
+    qp = _dev_ptr(q, "q", torch.bfloat16, 3, (None, None, pool.d_head))
+    B, n_q = int(q.shape[0]), int(q.shape[1])
+    pp = _dev_ptr(prefix_blocks, "prefix_blocks", torch.int32, 1)
+    tp = _dev_ptr(block_tables, "block_tables", torch.int32, 2, (B, None))
+    cp = _dev_ptr(context_lens, "context_lens", torch.int32, 1, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    op = _dev_ptr(out, "out", torch.bfloat16, 3, tuple(q.shape))
+    _check(load().paged_decode_attention_prefix(pool.handle, qp, n_q, pp, int(prefix_blocks.shape[0]), tp,
+                                                int(block_tables.shape[1]), cp, B, float(scale), op,
+                                                _stream_handle(stream)))
+    return out
+
+
 def paged_decode_step(pool: Pool, q, k_new, v_new, block_tables, context_lens, scale: float, out=None,
                       stream=None):
     """Append each sequence's newest token (k_new, v_new: bf16 [B, n_kv, d])
@@ -350,5 +373,5 @@ def paged_decode_attention_noalloc(pool: Pool, q, block_tables, context_lens, sc
 
 __all__ = ["BF16", "FP8_E4M3", "Pool", "PagedKVError", "kv_pool_create", "paged_kv_append",
            "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
-           "paged_decode_step_host", "kv_bytes_per_token", "load",
+           "paged_decode_step_host", "paged_decode_attention_prefix", "kv_bytes_per_token", "load",
            "library_path"]

@@ -76,6 +76,11 @@ struct DecodeArgs {
     // [batch][n_kv][D] bf16, and the pool arrays it is appended to
     const __nv_bfloat16 *k_new, *v_new;
     uint8_t *k_pool, *v_pool;
+    // cascade decode only: the first skip_blocks table entries of every
+    // sequence are a shared prefix whose attention comes from n_pre chunk
+    // partials (see MergeRefs); the kernel covers the blocks after it
+    int skip_blocks, n_pre;
+    int64_t pre_base;
 };
 
 // Shared-memory geometry of one (block, KV head) tile as the TMA boxes lay it
@@ -151,9 +156,13 @@ __device__ void scan_blocks(const DecodeArgs &a, int32_t *ps, int32_t *cl, int *
         const int b = base + tid;
         int n = 0;
         if (b < a.batch) {
-            const int c = clamp_ctx(a.context_lens[b], a.W, a.err, blockIdx.x == 0);
+            int c = clamp_ctx(a.context_lens[b], a.W, a.err, blockIdx.x == 0);
+            if (c < a.skip_blocks * kBlockSize) {  // cascade: every sequence holds the whole prefix
+                if (blockIdx.x == 0) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
+                c = a.skip_blocks * kBlockSize;
+            }
             cl[b] = c;
-            n = (c + kBlockSize - 1) / kBlockSize;
+            n = (c + kBlockSize - 1) / kBlockSize - a.skip_blocks;  // blocks after the shared prefix
         }
         int x = n;
 #pragma unroll
@@ -267,7 +276,7 @@ __device__ __forceinline__ void seg_next(Seg &s, const Stream &st)
 
 __device__ __forceinline__ int seg_load(const Seg &s, int lane, const DecodeArgs &a)
 {
-    return (s.live && lane < s.n) ? a.block_tables[(int64_t)s.p.b * a.W + s.j + lane] : -1;
+    return (s.live && lane < s.n) ? a.block_tables[(int64_t)s.p.b * a.W + a.skip_blocks + s.j + lane] : -1;
 }
 
 // ---------------------------------------------------------------------------
@@ -400,32 +409,47 @@ struct MergeRefs {
     const float *ws_o;
     __nv_bfloat16 *out;
     int *counters;
-    int n_kv, n_q;
+    int n_kv, n_q, batch;
+    int64_t pre_base;  // cascade: slot of prefix chunk 0 for (b=0, g=0); chunk k of (b, g) is
+    int n_pre;         // pre_base + (k * batch + b) * n_kv + g; n_pre = 0 without a shared prefix
 };
 
+// Log-sum-exp merge, by one warp, of every piece of (b, g): the n_pre prefix
+// chunks (cascade decode) and the n pieces in workspace slots
+// s_first + b*n_kv + g, ..., in that fixed order:
+//   M = max m_p, L = sum 2^(m_p - M) l_p, out = sum 2^(m_p - M) O_p / L.
+// Lanes first split the pieces to get M and L per head (warp reductions, kept
+// in `scratch`), then each lane sums 4-column chunks of O over the pieces with
+// independent loads.  Reads go to L2 (other SMs wrote the pieces).
 template <int D, int G>
 __device__ __noinline__ void merge_pieces(MergeRefs a, int b, int g, int s_first, int n, int lane, float *scratch)
 {
     __threadfence();
-    const int64_t base = (int64_t)s_first + (int64_t)b * a.n_kv + g;  // slot of piece 0
+    const int64_t base = (int64_t)s_first + (int64_t)b * a.n_kv + g;  // slot of tail piece 0
+    const int np = a.n_pre + n;
+    auto slot = [&](int p) -> int64_t {
+        return p < a.n_pre ? a.pre_base + ((int64_t)p * a.batch + b) * a.n_kv + g : base + (p - a.n_pre);
+    };
     float M[G], L[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         M[h] = -INFINITY;
         L[h] = 0.0f;
     }
-    for (int p = lane; p < n; p += 32) {
+    for (int p = lane; p < np; p += 32) {
+        const int64_t sp = slot(p);
 #pragma unroll
-        for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], __ldcg(&a.ws_ml[(base + p) * G + h]).x);
+        for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], __ldcg(&a.ws_ml[sp * G + h]).x);
     }
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) M[h] = fmaxf(M[h], __shfl_xor_sync(kFull, M[h], off));
-    for (int p = lane; p < n; p += 32) {
+    for (int p = lane; p < np; p += 32) {
+        const int64_t sp = slot(p);
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const float2 v = __ldcg(&a.ws_ml[(base + p) * G + h]);
+            const float2 v = __ldcg(&a.ws_ml[sp * G + h]);
             if (M[h] != -INFINITY) L[h] = fmaf(exp2f(v.x - M[h]), v.y, L[h]);
         }
     }
@@ -449,9 +473,10 @@ __device__ __noinline__ void merge_pieces(MergeRefs a, int b, int g, int s_first
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (Mh != -INFINITY) {
 #pragma unroll 4
-            for (int p = 0; p < n; ++p) {
-                const float sc = exp2f(__ldcg(&a.ws_ml[(base + p) * G + h]).x - Mh);
-                const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.ws_o + (base + p) * G * D) + q);
+            for (int p = 0; p < np; ++p) {
+                const int64_t sp = slot(p);
+                const float sc = exp2f(__ldcg(&a.ws_ml[sp * G + h]).x - Mh);
+                const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.ws_o + sp * G * D) + q);
                 acc.x = fmaf(sc, x.x, acc.x);
                 acc.y = fmaf(sc, x.y, acc.y);
                 acc.z = fmaf(sc, x.z, acc.z);
@@ -464,7 +489,7 @@ __device__ __noinline__ void merge_pieces(MergeRefs a, int b, int g, int s_first
         uint2 pk = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
         *reinterpret_cast<uint2 *>(ob + q * 4) = pk;
     }
-    if (lane == 0) a.counters[b * a.n_kv + g] = 0;
+    if (lane == 0 && n > 0) a.counters[b * a.n_kv + g] = 0;
 }
 
 // Fused step, part 1 (start of the piece that holds a sequence's last
@@ -592,10 +617,15 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
     st.share = a.slice_blocks > 0 ? a.slice_blocks : max(1, (st.total + st.n_warps - 1) / st.n_warps);
     st.n_slices = (st.total + st.share - 1) / st.share;
     const int me = (int)blockIdx.x * NW + warp;
-    for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {  // empty sequences: zero rows
+    for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {  // nothing to stream for b
         if (ps[b + 1] != ps[b]) continue;
-        uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)b * a.n_q * D);
-        for (int i = tid; i < a.n_q * D / 8; i += kThreads) o[i] = make_uint4(0, 0, 0, 0);
+        if (a.n_pre == 0) {  // empty sequence: zero rows
+            uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)b * a.n_q * D);
+            for (int i = tid; i < a.n_q * D / 8; i += kThreads) o[i] = make_uint4(0, 0, 0, 0);
+        } else {  // cascade, prefix only: the prefix chunks alone
+            MergeRefs mr{a.ws_ml, a.ws_o, a.out, a.counters, a.n_kv, a.n_q, a.batch, a.pre_base, a.n_pre};
+            for (int g = warp; g < a.n_kv; g += NW) merge_pieces<D, G>(mr, b, g, 0, 0, lane, scratch);
+        }
     }
 
     const uint64_t policy = l2_policy_evict_first();
@@ -694,7 +724,7 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
             if (!aborted && phys_st[sidx] >= 0) {
                 const uint32_t kb = smem_u32(ring + sidx * Gm::STAGE);
                 const uint32_t vb = kb + Gm::TILE;
-                const int nv = min(kBlockSize, C_len - j * kBlockSize);
+                const int nv = min(kBlockSize, C_len - (a.skip_blocks + j) * kBlockSize);
                 if constexpr (decltype(patch)::value) {
                     append_row<D, FP8>(a, pc.g, phys_st[sidx], nv - 1, lane,
                                        prepared_new_row<D, FP8>(a, pc.g, lane, rowbuf), ring + sidx * Gm::STAGE);
@@ -816,7 +846,7 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
         }
         const float vs = FP8 ? a.scales[a.n_kv + pc.g] : 1.0f;
         const bool h0 = 2 * c4 < G, h1 = 2 * c4 + 1 < G;  // this thread's heads exist
-        if (pc.j0 == 0 && pc.j1 == pc.nblk) {
+        if (pc.j0 == 0 && pc.j1 == pc.nblk && a.n_pre == 0) {
             // the whole (b, g): normalise and write bf16 out
             const float r0 = l0 > 0.0f ? vs / l0 : 0.0f, r1 = l1 > 0.0f ? vs / l1 : 0.0f;
             __nv_bfloat16 *ob = a.out + ((int64_t)pc.b * a.n_q + pc.g * G) * D;
@@ -857,7 +887,7 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
             }
             prev = __shfl_sync(kFull, prev, 0);
             if (prev == s_last - s_first) {
-                MergeRefs mr{a.ws_ml, a.ws_o, a.out, a.counters, a.n_kv, a.n_q};
+                MergeRefs mr{a.ws_ml, a.ws_o, a.out, a.counters, a.n_kv, a.n_q, a.batch, a.pre_base, a.n_pre};
                 merge_pieces<D, G>(mr, pc.b, pc.g, s_first, s_last - s_first + 1, lane, scratch);
             }
         }
@@ -1061,6 +1091,11 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
     a.ws_o = nullptr;
     a.slice_blocks = pool->partition_tokens / kBlockSize;
     a.err = pool->err;
+    a.k_new = a.v_new = nullptr;
+    a.k_pool = a.v_pool = nullptr;
+    a.skip_blocks = 0;
+    a.n_pre = 0;
+    a.pre_base = 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pool->d_head == 128)
         return fp8 ? dispatch_g<128, true>(pool, a, G, s) : dispatch_g<128, false>(pool, a, G, s);
@@ -1152,6 +1187,11 @@ static pkv_status step_device(pkv_pool *pool, const void *q, const void *k_new, 
     a.ws_o = nullptr;
     a.slice_blocks = pool->partition_tokens / kBlockSize;
     a.err = pool->err;
+    a.k_new = a.v_new = nullptr;
+    a.k_pool = a.v_pool = nullptr;
+    a.skip_blocks = 0;
+    a.n_pre = 0;
+    a.pre_base = 0;
     a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
     a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
     a.k_pool = static_cast<uint8_t *>(pool->k);
@@ -1212,6 +1252,312 @@ extern "C" pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host,
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "paged_decode_step_host: copy out");
     return PKV_OK;
+}
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// Cascade decode: a prefix shared by every sequence, read once
+// ---------------------------------------------------------------------------
+//
+// "Memory Management in LLM Serving Systems", "Prefix sharing": storing a
+// shared prefix once turns decode-time reads of n copies into one.  Stage 1
+// (prefix_kernel) attends all batch x G query rows of a KV head to the prefix
+// in one pass over its K and V tiles -- a real dense contraction, so the query
+// rows are the M dimension of 16x8x16 MMAs -- and stores a (max, sum, O)
+// partial per 256-token chunk of the prefix.  Stage 2 is the decode kernel
+// started past the prefix blocks; it merges its pieces with these partials.
+
+constexpr int kPrefixChunkBlocks = 16;  // prefix blocks per stage-1 CTA
+constexpr int kPrefixWarps = 4;         // 16 query rows per warp
+constexpr int kPrefixStages = 3;
+
+struct PrefixArgs {
+    const __nv_bfloat16 *q;
+    int n_q, n_kv, batch;
+    const int32_t *prefix_blocks;
+    int n_prefix_blocks;
+    int64_t num_blocks;
+    float qscale;
+    float2 *ws_ml;
+    float *ws_o;
+    int64_t pre_base;
+    unsigned *err;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kPrefixWarps * 32)
+    prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, PrefixArgs a)
+{
+    using Gm = Geo<D, false>;
+    constexpr int NT = D / 16;
+    constexpr int S = kPrefixStages;
+    __shared__ __align__(1024) uint8_t ring[S * Gm::STAGE];
+    __shared__ uint64_t bars[S];
+    __shared__ int phys_st[S];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g8 = lane >> 2, c4 = lane & 3;
+    const int chunk = blockIdx.x, g = blockIdx.y;
+    const int R = a.batch * G;  // query rows of KV head g
+    const int r0 = blockIdx.z * (kPrefixWarps * 16) + warp * 16;
+    const int j0 = chunk * kPrefixChunkBlocks, j1 = min(j0 + kPrefixChunkBlocks, a.n_prefix_blocks);
+    const uint64_t policy = l2_policy_evict_first();
+    if (tid == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+        fence_mbarrier_init();
+    }
+    griddep_wait();
+    griddep_launch_dependents();
+    __syncthreads();
+    auto issue = [&](int j) {  // thread 0: block j of the prefix into stage (j - j0) % S
+        const int st = (j - j0) % S;
+        const int phys = a.prefix_blocks[j];
+        const bool ok = phys >= 0 && phys < a.num_blocks;
+        phys_st[st] = ok ? phys : -1;
+        if (ok) {
+            const int y = (int)(((int64_t)phys * a.n_kv + g) * kBlockSize);
+            uint8_t *dst = ring + st * Gm::STAGE;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars[st], Gm::STAGE);
+#pragma unroll
+            for (int r = 0; r < Gm::NREG; ++r) {
+                tma_load_2d(dst + r * Gm::RGN, &tm_k, r * Gm::BOX_ELEMS, y, &bars[st], policy);
+                tma_load_2d(dst + Gm::TILE + r * Gm::RGN, &tm_v, r * Gm::BOX_ELEMS, y, &bars[st], policy);
+            }
+        } else {
+            atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
+            mbar_arrive(&bars[st]);
+        }
+    };
+    if (tid == 0)
+        for (int j = j0; j < min(j1, j0 + S); ++j) issue(j);
+
+    // Q rows r0 + g8 and r0 + g8 + 8 as A fragments: row r is head r % G of
+    // sequence r / G, i.e. query head g*G + r%G (zero past the last row).
+    uint32_t qa[NT][4];
+    {
+        const int ra = r0 + g8, rb = r0 + g8 + 8;
+        const __nv_bfloat16 *qa_row = a.q + ((int64_t)(ra / G) * a.n_q + g * G + ra % G) * D;
+        const __nv_bfloat16 *qb_row = a.q + ((int64_t)(rb / G) * a.n_q + g * G + rb % G) * D;
+#pragma unroll
+        for (int ks = 0; ks < NT; ++ks) {
+            const int d0 = 16 * ks + 2 * c4;
+            qa[ks][0] = ra < R ? *reinterpret_cast<const uint32_t *>(qa_row + d0) : 0u;
+            qa[ks][1] = rb < R ? *reinterpret_cast<const uint32_t *>(qb_row + d0) : 0u;
+            qa[ks][2] = ra < R ? *reinterpret_cast<const uint32_t *>(qa_row + d0 + 8) : 0u;
+            qa[ks][3] = rb < R ? *reinterpret_cast<const uint32_t *>(qb_row + d0 + 8) : 0u;
+        }
+    }
+    float o[2 * NT][4];  // O[16 rows x D]: n-tile t covers d 8t..8t+7
+#pragma unroll
+    for (int t = 0; t < 2 * NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // rows g8, g8 + 8
+    // ldmatrix lane roles: K as B (rows = tokens, non-trans), V as B (.trans)
+    const int tk = (lane & 7) + (lane >> 4) * 8, hk = (lane >> 3) & 1;  // K: mats (t0-7,c),(t0-7,c+1),(t8-15,c),(t8-15,c+1)
+    const int tv = (lane & 7) + ((lane >> 3) & 1) * 8, hv = lane >> 4;  // V: mats (t0-7,c),(t8-15,c),(t0-7,c+1),(t8-15,c+1)
+    bool aborted = false;
+
+    for (int j = j0; j < j1; ++j) {
+        const int st = (j - j0) % S;
+        const uint32_t parity = (uint32_t)((j - j0) / S) & 1u;
+        if (!aborted) {
+            const bool ok = mbar_wait_bounded(&bars[st], parity);
+            aborted = __any_sync(kFull, !ok);
+            if (aborted && lane == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+        }
+        if (!aborted && phys_st[st] >= 0) {
+            const uint32_t kb = smem_u32(ring + st * Gm::STAGE), vb = kb + Gm::TILE;
+            // S[16 rows x 16 tokens] = Q K^T: n-tiles of tokens 0-7 and 8-15
+            float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < NT; ++ks) {
+                const int ch = 2 * ks + hk;
+                uint32_t fb[4];
+                ldsm_x4(kb + (ch >> 3) * Gm::RGN + swz<128>(tk * 128 + (ch & 7) * 16), fb);
+                mma16816<false>(s0, qa[ks], fb[0], fb[1]);
+                mma16816<false>(s1, qa[ks], fb[2], fb[3]);
+            }
+            float sv[8] = {s0[0], s0[1], s1[0], s1[1], s0[2], s0[3], s1[2], s1[3]};  // row g8: 0..3, row g8+8: 4..7
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sv[i] *= a.qscale;
+            float bm0 = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+            float bm1 = fmaxf(fmaxf(sv[4], sv[5]), fmaxf(sv[6], sv[7]));
+#pragma unroll
+            for (int off = 1; off < 4; off <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
+            }
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+            float p[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                p[i] = exp2f(sv[i] - mn0);
+                p[4 + i] = exp2f(sv[4 + i] - mn1);
+            }
+            l0 = fmaf(l0, al0, (p[0] + p[1]) + (p[2] + p[3]));
+            l1 = fmaf(l1, al1, (p[4] + p[5]) + (p[6] + p[7]));
+            m0 = mn0;
+            m1 = mn1;
+            if (__any_sync(kFull, al0 != 1.0f || al1 != 1.0f)) {
+#pragma unroll
+                for (int t = 0; t < 2 * NT; ++t) {
+                    o[t][0] *= al0;
+                    o[t][1] *= al0;
+                    o[t][2] *= al1;
+                    o[t][3] *= al1;
+                }
+            }
+            // P as the A operand of O += P V: the score tiles' accumulator layout is the
+            // A layout of a 16x16 (rows x tokens) operand
+            const uint32_t pa[4] = {pack2<false>(p[0], p[1]), pack2<false>(p[4], p[5]), pack2<false>(p[2], p[3]),
+                                    pack2<false>(p[6], p[7])};
+#pragma unroll
+            for (int n2 = 0; n2 < NT; ++n2) {
+                const int ch = 2 * n2 + hv;
+                uint32_t fb[4];
+                ldsm_x4_t(vb + (ch >> 3) * Gm::RGN + swz<128>(tv * 128 + (ch & 7) * 16), fb);
+                mma16816<false>(o[2 * n2], pa, fb[0], fb[1]);
+                mma16816<false>(o[2 * n2 + 1], pa, fb[2], fb[3]);
+            }
+        }
+        __syncthreads();  // every warp is done with stage st
+        if (tid == 0 && !aborted && j + S < j1) issue(j + S);
+    }
+    if (aborted && tid == 0)  // drain this CTA's copies still in flight
+        for (int j = j0; j < min(j1, j0 + S); ++j) mbar_wait_bounded(&bars[(j - j0) % S], 0, 100000000ull);
+
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+        l0 += __shfl_xor_sync(kFull, l0, off);
+        l1 += __shfl_xor_sync(kFull, l1, off);
+    }
+    // partial of rows r0+g8 (o[][0..1]) and r0+g8+8 (o[][2..3]) for this chunk
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int r = r0 + g8 + 8 * half;
+        if (r >= R) continue;
+        const int b = r / G, hh = r % G;
+        const int64_t slot = a.pre_base + ((int64_t)chunk * a.batch + b) * a.n_kv + g;
+        float *wo = a.ws_o + (slot * G + hh) * D;
+#pragma unroll
+        for (int t = 0; t < 2 * NT; ++t)
+            *reinterpret_cast<float2 *>(wo + 8 * t + 2 * c4) = make_float2(o[t][2 * half], o[t][2 * half + 1]);
+        if (c4 == 0) a.ws_ml[slot * G + hh] = half ? make_float2(m1, l1) : make_float2(m0, l0);
+    }
+}
+
+template <int D, int G>
+static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32_t *prefix_blocks,
+                                       int n_prefix_blocks, cudaStream_t s)
+{
+    using C = Cfg<D, G, false>;
+    int grid = 0;
+    size_t smem = 0;
+    pkv_status st = decode_grid<D, G, false>(pool, a.batch, a.W, &grid, &smem);
+    if (st != PKV_OK) return st;
+    const int n_chunks = (n_prefix_blocks + kPrefixChunkBlocks - 1) / kPrefixChunkBlocks;
+    const int64_t tail_slots = max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW);
+    const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, tail_slots + (int64_t)n_chunks * a.batch * a.n_kv);
+    st = ensure_workspace(pool, L.total);
+    if (st != PKV_OK) return st;
+    uint8_t *ws = static_cast<uint8_t *>(pool->ws);
+    a.counters = reinterpret_cast<int *>(ws + L.counters);
+    a.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
+    a.ws_o = reinterpret_cast<float *>(ws + L.o);
+    a.skip_blocks = n_prefix_blocks;
+    a.n_pre = n_chunks;
+    a.pre_base = tail_slots;
+    PrefixArgs pa;
+    pa.q = a.q;
+    pa.n_q = a.n_q;
+    pa.n_kv = a.n_kv;
+    pa.batch = a.batch;
+    pa.prefix_blocks = prefix_blocks;
+    pa.n_prefix_blocks = n_prefix_blocks;
+    pa.num_blocks = a.num_blocks;
+    pa.qscale = a.qscale;
+    pa.ws_ml = a.ws_ml;
+    pa.ws_o = a.ws_o;
+    pa.pre_base = tail_slots;
+    pa.err = a.err;
+    const int row_tiles = (a.batch * G + kPrefixWarps * 16 - 1) / (kPrefixWarps * 16);
+    {
+        LaunchScope ls(pool, kMerge, s);  // counted as the cascade's extra launch
+        cudaError_t e = launch_pdl(prefix_kernel<D, G>, dim3(n_chunks, a.n_kv, row_tiles), dim3(kPrefixWarps * 32), 0,
+                                   s, pool->tm_k, pool->tm_v, pa);
+        ls.done();
+        if (e != cudaSuccess) return cuda_fail(e, "prefix launch");
+    }
+    LaunchScope ls(pool, kDecode, s);
+    cudaError_t e = launch_pdl(decode_kernel<D, G, false>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
+                               pool->tm_v, a);
+    ls.done();
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch (cascade tail)");
+    return PKV_OK;
+}
+
+template <int D>
+static pkv_status dispatch_prefix(pkv_pool *pool, const DecodeArgs &a, int G, const int32_t *pb, int npb, cudaStream_t s)
+{
+    switch (G) {
+    case 1: return launch_prefix_decode<D, 1>(pool, a, pb, npb, s);
+    case 2: return launch_prefix_decode<D, 2>(pool, a, pb, npb, s);
+    case 4: return launch_prefix_decode<D, 4>(pool, a, pb, npb, s);
+    case 8: return launch_prefix_decode<D, 8>(pool, a, pb, npb, s);
+    }
+    return fail(PKV_EUNSUPPORTED, "cascade decode: group size %d unsupported (1, 2, 4 or 8)", G);
+}
+
+}  // namespace pkv
+
+extern "C" pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *q, int32_t n_q,
+                                                    const int32_t *prefix_blocks, int32_t n_prefix_blocks,
+                                                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                                    const int32_t *context_lens, int32_t batch, float scale,
+                                                    void *out, void *stream)
+{
+    pkv_status st = check_step_args(pool, "paged_decode_attention_prefix", n_q, max_blocks_per_seq, batch, scale);
+    if (st != PKV_OK || batch == 0) return st;
+    if (pool->dtype != PKV_BF16)
+        return fail(PKV_EUNSUPPORTED, "paged_decode_attention_prefix: bf16 pools only");
+    if (n_prefix_blocks <= 0 || n_prefix_blocks > max_blocks_per_seq)
+        return fail(PKV_EINVAL, "paged_decode_attention_prefix: n_prefix_blocks %d not in [1, max_blocks_per_seq]",
+                    n_prefix_blocks);
+    if (!q || !prefix_blocks || !block_tables || !context_lens || !out)
+        return fail(PKV_EINVAL, "paged_decode_attention_prefix: NULL device pointer");
+    if (((uintptr_t)q | (uintptr_t)out) & 15u)
+        return fail(PKV_EINVAL, "paged_decode_attention_prefix: q and out must be 16-byte aligned");
+    if (((uintptr_t)block_tables | (uintptr_t)context_lens | (uintptr_t)prefix_blocks) & 3u)
+        return fail(PKV_EINVAL, "paged_decode_attention_prefix: tables and lengths must be 4-byte aligned");
+    const int G = n_q / pool->n_kv;
+    DecodeArgs a;
+    a.num_blocks = pool->num_blocks;
+    a.n_kv = pool->n_kv;
+    a.n_q = n_q;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.block_tables = block_tables;
+    a.W = max_blocks_per_seq;
+    a.context_lens = context_lens;
+    a.batch = batch;
+    a.qscale = scale * kLog2e;
+    a.scales = pool->scales;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.counters = nullptr;
+    a.ws_ml = nullptr;
+    a.ws_o = nullptr;
+    a.slice_blocks = pool->partition_tokens / kBlockSize;
+    a.err = pool->err;
+    a.k_new = a.v_new = nullptr;
+    a.k_pool = a.v_pool = nullptr;
+    a.skip_blocks = 0;
+    a.n_pre = 0;
+    a.pre_base = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pool->d_head == 128) return dispatch_prefix<128>(pool, a, G, prefix_blocks, n_prefix_blocks, s);
+    return dispatch_prefix<64>(pool, a, G, prefix_blocks, n_prefix_blocks, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -1357,6 +1703,11 @@ extern "C" pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void 
     a.ws_o = nullptr;
     a.slice_blocks = pool->partition_tokens / kBlockSize;
     a.err = pool->err;
+    a.k_new = a.v_new = nullptr;
+    a.k_pool = a.v_pool = nullptr;
+    a.skip_blocks = 0;
+    a.n_pre = 0;
+    a.pre_base = 0;
     uint8_t *sp = static_cast<uint8_t *>(scratch);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pool->d_head == 128)

@@ -81,7 +81,7 @@ typedef struct {
     int64_t launches;        /* every kernel launch the library enqueued */
     int64_t append_launches;
     int64_t decode_launches;
-    int64_t merge_launches;  /* 0: partial results merge inside the decode kernel */
+    int64_t merge_launches;  /* cascade prefix-stage launches (split-KV merges run inside decode) */
     double append_ms;        /* summed event time of timed launches */
     double decode_ms;
     double merge_ms;
@@ -221,6 +221,29 @@ pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host, const void
                                   const void *v_new_host, int32_t n_q, const int32_t *block_tables_host,
                                   int32_t max_blocks_per_seq, const int32_t *context_lens_host, int32_t batch,
                                   float scale, void *out_host, void *stream);
+
+/* Cascade decode for a batch whose sequences all start with the same
+ * prefix: the prefix's K and V are read once for the whole batch instead of
+ * once per sequence ("Memory Management in LLM Serving Systems", "Prefix
+ * sharing": decode-time reads for the shared part drop from n x p to p).
+ * Same result as paged_decode_attention (up to rounding order):
+ *   stage 1 attends every query row of each KV head to the prefix with
+ *   tensor-core tiles and keeps a (max, sum, output) partial per 256-token
+ *   chunk; stage 2 decodes each sequence's blocks after the prefix and
+ *   merges them with the prefix partials by log-sum-exp.  Two launches.
+ *   prefix_blocks    device int32 [n_prefix_blocks]: physical ids of the
+ *                    shared prefix, which is the first n_prefix_blocks * 16
+ *                    tokens of every sequence: block_tables[b][0..n) must
+ *                    equal prefix_blocks (not checked).
+ *   context_lens[b]  at least n_prefix_blocks * 16 (shorter ones are
+ *                    treated as prefix-only and set PKV_DEVERR_CTX_RANGE).
+ * bf16 pools only (EUNSUPPORTED for FP8).  Other arguments and errors as
+ * paged_decode_attention. */
+pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *q, int32_t n_q,
+                                         const int32_t *prefix_blocks, int32_t n_prefix_blocks,
+                                         const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t *context_lens, int32_t batch, float scale, void *out,
+                                         void *stream);
 
 /* paged_decode_attention without any allocation.  The pages have no
  * counterpart to this call; it exists for callers that cannot allocate

@@ -1,0 +1,66 @@
+"""Cascade decode for a shared prefix (read once for the batch) against the
+fp64 oracle and against plain paged decode."""
+import numpy as np
+import pytest
+import torch
+
+import gqa_decode_attention_paged_gb300 as pkv
+import workloads as wl
+from gpu_util import assert_close, fill, i32_dev, make_pool, mirror, out_f64, run_step, step_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _cascade(pool, w, d, n_pre, lens=None):
+    pre = i32_dev(w.block_tables[0, :n_pre])
+    return pkv.paged_decode_attention_prefix(pool, d["q"], pre, d["tables"], d["lens"] if lens is None else lens,
+                                             float(w.scale))
+
+
+@pytest.mark.parametrize("make,n_pre", [
+    (lambda: wl.shared_prefix(), 64),
+    (lambda: wl.build("cp_g8", 64, 8, 128, [321, 400, 257, 1000], seed=61, shared_prefix_tokens=256), 16),
+    (lambda: wl.build("cp_d64", 8, 2, 64, [90, 70, 65, 300, 81], seed=62, shared_prefix_tokens=64), 4),
+    (lambda: wl.build("cp_ragged", 32, 8, 128, [330, 500, 321], seed=63, shared_prefix_tokens=320), 20),
+    (lambda: wl.build("cp_b1", 32, 8, 128, [2000], seed=64, shared_prefix_tokens=1600), 100),
+])
+def test_cascade_matches_oracle_and_plain_decode(make, n_pre):
+    w = make()
+    ref = mirror(w).decode(w.q, w.block_tables, w.context_lens, w.scale)
+    with make_pool(w) as pool:
+        fill(pool, w)
+        d = step_inputs(w)
+        plain = out_f64(run_step(pool, w, d))  # appends the step token, then decodes
+        casc = out_f64(_cascade(pool, w, d, n_pre))
+        torch.cuda.synchronize()
+        assert pool.get_error() == 0
+    assert_close(casc, ref, w.name)
+    assert np.abs(casc - plain).max() < 1e-2
+
+
+def test_cascade_with_prefix_only_sequences():
+    w = wl.build("cp_empty", 32, 8, 128, [257, 300, 257], seed=65, shared_prefix_tokens=256)
+    lens = w.context_lens.copy()
+    lens[0] = lens[2] = 256  # nothing after the prefix
+    ref = mirror(w).decode(w.q, w.block_tables, lens, w.scale)
+    with make_pool(w) as pool:
+        fill(pool, w)
+        d = step_inputs(w)
+        pkv.paged_kv_append(pool, d["k"], d["v"], d["slots"])
+        casc = out_f64(_cascade(pool, w, d, 16, i32_dev(lens)))
+        assert pool.get_error() == 0
+    assert_close(casc, ref, "prefix-only rows")
+
+
+def test_cascade_rejects_fp8_and_bad_prefix():
+    with pkv.kv_pool_create(8, 16, 2, 64, pkv.FP8_E4M3) as pool:
+        pool.set_fp8_scales(np.ones(2), np.ones(2))
+        q = torch.zeros(1, 4, 64, dtype=torch.bfloat16, device="cuda")
+        t = torch.zeros(1, 2, dtype=torch.int32, device="cuda")
+        c = torch.full((1,), 20, dtype=torch.int32, device="cuda")
+        with pytest.raises(pkv.PagedKVError) as e:
+            pkv.paged_decode_attention_prefix(pool, q, t[0, :1], t, c, 0.125)
+        assert e.value.status == 5
+    with pkv.kv_pool_create(8, 16, 2, 64) as pool:
+        with pytest.raises(pkv.PagedKVError):
+            pkv.paged_decode_attention_prefix(pool, q, torch.zeros(3, dtype=torch.int32, device="cuda"), t, c, 0.125)
