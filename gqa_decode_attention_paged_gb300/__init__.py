@@ -51,7 +51,9 @@ class _Timing(ctypes.Structure):
                 ("decode_launches", ctypes.c_int64), ("merge_launches", ctypes.c_int64),
                 ("append_ms", ctypes.c_double), ("decode_ms", ctypes.c_double),
                 ("merge_ms", ctypes.c_double), ("timed_append", ctypes.c_int64),
-                ("timed_decode", ctypes.c_int64), ("timed_merge", ctypes.c_int64)]
+                ("timed_decode", ctypes.c_int64), ("timed_merge", ctypes.c_int64),
+                ("prefix_launches", ctypes.c_int64), ("prefix_ms", ctypes.c_double),
+                ("timed_prefix", ctypes.c_int64)]
 
 
 def library_path() -> str:

@@ -67,7 +67,6 @@ struct DecodeArgs {
     float qscale;          // scale * log2(e)
     const float *scales;   // FP8: [2 * n_kv] (k then v)
     __nv_bfloat16 *out;
-    int *counters;         // workspace [batch * n_kv], zero between calls
     float2 *ws_ml;         // workspace [slots][G] (max in log2 units, sum)
     float *ws_o;           // workspace [slots][G][D], unnormalised
     int slice_blocks;      // blocks per slice; 0 = ceil(total / all warps)
@@ -78,7 +77,7 @@ struct DecodeArgs {
     uint8_t *k_pool, *v_pool;
     // cascade decode only: the first skip_blocks table entries of every
     // sequence are a shared prefix whose attention comes from n_pre chunk
-    // partials (see MergeRefs); the kernel covers the blocks after it
+    // partials (see MergeArgs); the kernel covers the blocks after it
     int skip_blocks, n_pre;
     int64_t pre_base;
 };
@@ -121,48 +120,50 @@ struct Cfg {
     using Gm = Geo<D, FP8>;
     static constexpr int NW = Tune<D, G, FP8>::NW;
     static constexpr int kThreads = NW * 32;
+    // resident CTAs per SM the register budget is held to: 3 x 128 threads
+    // of at most 168 registers (the shared-memory ring allows no more for
+    // bf16 d128; the rare merge calls spill around themselves instead)
+    static constexpr int kMinBlocks = 3;
     static constexpr int kStages = std::min(8, std::max(2, Tune<D, G, FP8>::RING_KIB * 1024 / (NW * Gm::STAGE)));
     // shared-memory layout (bytes from a 1024-byte aligned base)
     static constexpr int kRing = NW * kStages * Gm::STAGE;
     static constexpr int kBars = kRing;
     static constexpr int kPhys = kBars + NW * kStages * 8;
-    static constexpr int kScratch = kPhys + NW * kStages * 4;  // [NW][16] floats: merge max/sum per head
-    static constexpr int kNewRow = kScratch + NW * 16 * 4;     // [NW][2 * D * 2] bytes: fused step's new K, V rows
+    static constexpr int kNewRow = (kPhys + NW * kStages * 4 + 15) / 16 * 16;  // [NW][2 * D * 2] bytes: fused
+                                                                                // step's new K, V rows
     static constexpr int kWarpTot = kNewRow + NW * 4 * D;
     static constexpr int kPs = kWarpTot + 4 * NW;  // ps[batch + 1], then clamped lengths cl[batch]
     static size_t smem_bytes(int batch) { return 1024 + (size_t)kPs + 4 * (size_t)(2 * batch + 1); }
     static_assert(G <= 8, "at most 8 query heads per KV head");
 };
 
-__device__ __forceinline__ int clamp_ctx(int c, int W, unsigned *err, bool report)
-{
-    const int cmax = W * kBlockSize;
-    if (c < 0 || c > cmax) {
-        if (report) atomicOr(err, PKV_DEVERR_CTX_RANGE);
-        c = c < 0 ? 0 : cmax;
-    }
-    return c;
-}
-
-// Exclusive prefix sum of block counts per sequence into ps[0..batch];
-// warp_tot is scratch for NW ints.
+// Exclusive prefix sum of block counts per sequence (after the first `skip`
+// table entries) into ps[0..batch], and the clamped lengths into cl (if not
+// null); range errors go to *err when err is not null.  warp_tot is scratch
+// for NW ints.  The decode and merge kernels both derive their work from it.
 template <int NW>
-__device__ void scan_blocks(const DecodeArgs &a, int32_t *ps, int32_t *cl, int *warp_tot)
+__device__ void scan_blocks(const int32_t *lens, int batch, int W, int skip, unsigned *err, int32_t *ps,
+                            int32_t *cl, int *warp_tot)
 {
     constexpr int NT = NW * 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int carry = 0;
-    for (int base = 0; base < a.batch; base += NT) {
+    for (int base = 0; base < batch; base += NT) {
         const int b = base + tid;
         int n = 0;
-        if (b < a.batch) {
-            int c = clamp_ctx(a.context_lens[b], a.W, a.err, blockIdx.x == 0);
-            if (c < a.skip_blocks * kBlockSize) {  // cascade: every sequence holds the whole prefix
-                if (blockIdx.x == 0) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
-                c = a.skip_blocks * kBlockSize;
+        if (b < batch) {
+            int c = lens[b];
+            const int cmax = W * kBlockSize;
+            if (c < 0 || c > cmax) {
+                if (err) atomicOr(err, PKV_DEVERR_CTX_RANGE);
+                c = c < 0 ? 0 : cmax;
             }
-            cl[b] = c;
-            n = (c + kBlockSize - 1) / kBlockSize - a.skip_blocks;  // blocks after the shared prefix
+            if (c < skip * kBlockSize) {  // cascade: every sequence holds the whole prefix
+                if (err) atomicOr(err, PKV_DEVERR_CTX_RANGE);
+                c = skip * kBlockSize;
+            }
+            if (cl) cl[b] = c;
+            n = (c + kBlockSize - 1) / kBlockSize - skip;  // blocks after the shared prefix
         }
         int x = n;
 #pragma unroll
@@ -179,11 +180,11 @@ __device__ void scan_blocks(const DecodeArgs &a, int32_t *ps, int32_t *cl, int *
             before += (w < warp) ? t : 0;
             tot += t;
         }
-        if (b < a.batch) ps[b] = carry + before + x - n;
+        if (b < batch) ps[b] = carry + before + x - n;
         carry += tot;
         __syncthreads();
     }
-    if (tid == 0) ps[a.batch] = carry;
+    if (tid == 0) ps[batch] = carry;
     __syncthreads();
 }
 
@@ -398,98 +399,192 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs &a, int b, int g, 
     }
 }
 
-// Log-sum-exp merge of the n pieces of (b, g), stored in workspace slots
-// s_first + b*n_kv + g, ..., in slice order, by one warp:
-//   M = max m_p, L = sum 2^(m_p - M) l_p, out = sum 2^(m_p - M) O_p / L.
-// Lanes first split the pieces to get M and L per head (warp reductions, kept
-// in `scratch`), then each lane sums 4-column chunks of O over the pieces with
-// independent loads.  Reads go to L2 (other SMs wrote the pieces).
-struct MergeRefs {
+// ---------------------------------------------------------------------------
+// Merge of split runs: the split-KV reduction
+//
+// A (sequence, KV head) run that the decode kernel cut into several pieces
+// (and, in cascade decode, every run) leaves partials (m, l, O) in workspace
+// slots; this kernel, launched right behind the decode kernel, combines them
+// by log-sum-exp in a fixed order (the n_pre prefix chunks, then the tail
+// pieces in slice order):
+//   M = max m_p,  L = sum 2^(m_p - M) l_p,  out = sum 2^(m_p - M) O_p / L.
+// The split runs are found from the decode kernel's block prefix sums: slice
+// boundary k (stream item k * share) splits the run it falls strictly inside,
+// and a run is merged by the boundary that first splits it.  One wave of CTAs
+// walks the boundaries (in cascade decode, all runs); the warps of a CTA share
+// one run, each summing a quarter of its G x D output columns.
+// ---------------------------------------------------------------------------
+
+constexpr int kMergeThreads = 128;
+constexpr int kMergeWarps = kMergeThreads / 32;
+
+struct MergeArgs {
     const float2 *ws_ml;
     const float *ws_o;
     __nv_bfloat16 *out;
-    int *counters;
-    int n_kv, n_q, batch;
+    const int32_t *context_lens;
+    int n_kv, n_q, batch, W, skip_blocks;
+    int n_warps, slice_blocks;  // the decode grid's warps and slice length (0: automatic)
     int64_t pre_base;  // cascade: slot of prefix chunk 0 for (b=0, g=0); chunk k of (b, g) is
     int n_pre;         // pre_base + (k * batch + b) * n_kv + g; n_pre = 0 without a shared prefix
 };
 
-// Log-sum-exp merge, by one warp, of every piece of (b, g): the n_pre prefix
-// chunks (cascade decode) and the n pieces in workspace slots
-// s_first + b*n_kv + g, ..., in that fixed order:
-//   M = max m_p, L = sum 2^(m_p - M) l_p, out = sum 2^(m_p - M) O_p / L.
-// Lanes first split the pieces to get M and L per head (warp reductions, kept
-// in `scratch`), then each lane sums 4-column chunks of O over the pieces with
-// independent loads.  Reads go to L2 (other SMs wrote the pieces).
+// One warp: chunks [c_lo, c_hi) (float4 chunks of the G x D output rows) of
+// run (b, g) with pieces `np` (n_pre prefix chunks, then tail slots from
+// `base`).  Lane p reads piece p's (m, l) and keeps its weights, which lanes
+// take by shuffle; PB pieces' rows are in flight at a time, the first PB
+// requested together with the (m, l).  Every sum has a fixed order.
 template <int D, int G>
-__device__ __noinline__ void merge_pieces(MergeRefs a, int b, int g, int s_first, int n, int lane, float *scratch)
+__device__ __forceinline__ void merge_run_warp(const MergeArgs &a, int b, int g, int np, int64_t base, int c_lo,
+                                               int c_hi, int lane)
 {
-    __threadfence();
-    const int64_t base = (int64_t)s_first + (int64_t)b * a.n_kv + g;  // slot of tail piece 0
-    const int np = a.n_pre + n;
+    constexpr int CW = (G * D / 4 + kMergeWarps - 1) / kMergeWarps;  // chunks per warp
+    constexpr int KW = (CW + 31) / 32;                                 // chunks per lane
+    constexpr int PB = 8 / KW;
     auto slot = [&](int p) -> int64_t {
         return p < a.n_pre ? a.pre_base + ((int64_t)p * a.batch + b) * a.n_kv + g : base + (p - a.n_pre);
     };
+    auto load_o = [&](int p, float4 (&x)[KW]) {
+        const float4 *src = reinterpret_cast<const float4 *>(a.ws_o + slot(p) * G * D);
+#pragma unroll
+        for (int k = 0; k < KW; ++k) {
+            const int c = c_lo + lane + 32 * k;
+            x[k] = c < c_hi ? __ldcg(src + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    float4 buf[PB][KW];
+#pragma unroll
+    for (int i = 0; i < PB; ++i)
+        if (i < np) load_o(i, buf[i]);
+    float own_m[G], lm[G], ll[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        own_m[h] = -INFINITY;
+        lm[h] = -INFINITY;
+        ll[h] = 0.0f;
+    }
+    for (int p0 = 0; p0 < np; p0 += 32) {
+        if (p0 + lane < np) {
+            const float2 *src = a.ws_ml + slot(p0 + lane) * G;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float2 v = __ldcg(src + h);
+                if (p0 == 0) own_m[h] = v.x;
+                const float mn = fmaxf(lm[h], v.x);
+                ll[h] = mn == -INFINITY ? 0.0f : ll[h] * exp2f(lm[h] - mn) + v.y * exp2f(v.x - mn);
+                lm[h] = mn;
+            }
+        }
+    }
     float M[G], L[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        M[h] = -INFINITY;
-        L[h] = 0.0f;
+        float mx = lm[h];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
+        float sl = mx == -INFINITY ? 0.0f : ll[h] * exp2f(lm[h] - mx);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) sl += __shfl_xor_sync(kFull, sl, off);
+        M[h] = mx;
+        L[h] = sl;
+        own_m[h] = mx == -INFINITY ? 0.0f : exp2f(own_m[h] - mx);  // now the weight of piece `lane`
     }
-    for (int p = lane; p < np; p += 32) {
-        const int64_t sp = slot(p);
+    float4 acc[KW];
 #pragma unroll
-        for (int h = 0; h < G; ++h) M[h] = fmaxf(M[h], __ldcg(&a.ws_ml[sp * G + h]).x);
-    }
+    for (int k = 0; k < KW; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int p = 0; p < np; p += PB) {
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+        for (int i = 0; i < PB; ++i) {
+            const int pi = p + i;
+            if (pi < np) {
+                float wv[G];
+                if (pi < 32) {
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) M[h] = fmaxf(M[h], __shfl_xor_sync(kFull, M[h], off));
-    for (int p = lane; p < np; p += 32) {
-        const int64_t sp = slot(p);
+                    for (int h = 0; h < G; ++h) wv[h] = __shfl_sync(kFull, own_m[h], pi);
+                } else {
+                    const float2 *src = a.ws_ml + slot(pi) * G;
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float2 v = __ldcg(&a.ws_ml[sp * G + h]);
-            if (M[h] != -INFINITY) L[h] = fmaf(exp2f(v.x - M[h]), v.y, L[h]);
-        }
-    }
+                    for (int h = 0; h < G; ++h) wv[h] = M[h] == -INFINITY ? 0.0f : exp2f(__ldcg(src + h).x - M[h]);
+                }
 #pragma unroll
-    for (int h = 0; h < G; ++h)
+                for (int k = 0; k < KW; ++k) {
+                    const int h = (c_lo + lane + 32 * k) * 4 / D;  // < G for chunks in range
+                    float w = wv[0];
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) L[h] += __shfl_xor_sync(kFull, L[h], off);
-    if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            scratch[h] = M[h];
-            scratch[8 + h] = L[h];
-        }
-    }
-    __syncwarp();
-    constexpr int CHUNKS = G * D / 4;  // float4 chunks of the G x D output
-    __nv_bfloat16 *ob = a.out + ((int64_t)b * a.n_q + g * G) * D;
-    for (int q = lane; q < CHUNKS; q += 32) {
-        const int h = (q * 4) / D;
-        const float Mh = scratch[h], Lh = scratch[8 + h];
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (Mh != -INFINITY) {
-#pragma unroll 4
-            for (int p = 0; p < np; ++p) {
-                const int64_t sp = slot(p);
-                const float sc = exp2f(__ldcg(&a.ws_ml[sp * G + h]).x - Mh);
-                const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.ws_o + sp * G * D) + q);
-                acc.x = fmaf(sc, x.x, acc.x);
-                acc.y = fmaf(sc, x.y, acc.y);
-                acc.z = fmaf(sc, x.z, acc.z);
-                acc.w = fmaf(sc, x.w, acc.w);
+                    for (int hh = 1; hh < G; ++hh) w = h == hh ? wv[hh] : w;
+                    acc[k].x = fmaf(w, buf[i][k].x, acc[k].x);
+                    acc[k].y = fmaf(w, buf[i][k].y, acc[k].y);
+                    acc[k].z = fmaf(w, buf[i][k].z, acc[k].z);
+                    acc[k].w = fmaf(w, buf[i][k].w, acc[k].w);
+                }
+                if (pi + PB < np) load_o(pi + PB, buf[i]);
             }
         }
-        const float r = Lh > 0.0f ? 1.0f / Lh : 0.0f;
-        __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * r, acc.y * r);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * r, acc.w * r);
-        uint2 pk = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
-        *reinterpret_cast<uint2 *>(ob + q * 4) = pk;
     }
-    if (lane == 0 && n > 0) a.counters[b * a.n_kv + g] = 0;
+    __nv_bfloat16 *ob = a.out + ((int64_t)b * a.n_q + g * G) * D;
+#pragma unroll
+    for (int k = 0; k < KW; ++k) {
+        const int c = c_lo + lane + 32 * k;
+        if (c < c_hi) {
+            const int h = c * 4 / D;
+            float Lh = L[0];
+#pragma unroll
+            for (int hh = 1; hh < G; ++hh) Lh = h == hh ? L[hh] : Lh;
+            const float r = Lh > 0.0f ? 1.0f / Lh : 0.0f;
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x * r, acc[k].y * r);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z * r, acc[k].w * r);
+            *reinterpret_cast<uint2 *>(ob + c * 4) =
+                make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+        }
+    }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(MergeArgs a)
+{
+    constexpr int CHUNKS = G * D / 4;
+    constexpr int CW = (CHUNKS + kMergeWarps - 1) / kMergeWarps;
+    extern __shared__ int32_t ps[];  // [batch + 1]
+    __shared__ int warp_tot[kMergeWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // The decode kernel's slicing, rederived from the lengths (its inputs, not
+    // its outputs) while it still runs; only the partials need the wait.
+    scan_blocks<kMergeWarps>(a.context_lens, a.batch, a.W, a.skip_blocks, nullptr, ps, nullptr, warp_tot);
+    const int total = a.n_kv * ps[a.batch];
+    const int share = a.slice_blocks > 0 ? a.slice_blocks : max(1, (total + a.n_warps - 1) / a.n_warps);
+    griddep_wait();  // the decode kernel's partials
+    griddep_launch_dependents();
+    const int n_items = a.n_pre > 0 ? a.batch * a.n_kv : max(0, (total + share - 1) / share - 1);
+    const int c_lo = min(CHUNKS, warp * CW), c_hi = min(CHUNKS, c_lo + CW);
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        int b, g;
+        if (a.n_pre > 0) {  // cascade: every run takes in the prefix chunks
+            b = it / a.n_kv;
+            g = it - b * a.n_kv;
+        } else {  // slice boundary it + 1
+            const int f = (it + 1) * share;
+            int lo = 0, hi = a.batch - 1;  // largest b with n_kv * ps[b] <= f
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (a.n_kv * ps[mid] <= f) lo = mid; else hi = mid - 1;
+            }
+            b = lo;
+            const int nb = ps[b + 1] - ps[b];
+            const int r = f - a.n_kv * ps[b];
+            g = r / nb;
+            const int j = r - g * nb;  // the boundary's block within the run
+            if (j == 0 || j > share) continue;  // at a run start, or not the run's first split
+        }
+        const int nblk = ps[b + 1] - ps[b];
+        int s_first = 0, n = 0;
+        if (nblk > 0) {
+            const int start = a.n_kv * ps[b] + g * nblk;
+            s_first = start / share;
+            n = (start + nblk - 1) / share - s_first + 1;
+        }
+        const int64_t base = (int64_t)s_first + (int64_t)b * a.n_kv + g;  // slot of tail piece 0
+        if (c_lo < c_hi) merge_run_warp<D, G>(a, b, g, a.n_pre + n, base, c_lo, c_hi, lane);
+    }
 }
 
 // Fused step, part 1 (start of the piece that holds a sequence's last
@@ -577,7 +672,7 @@ __device__ __forceinline__ void append_row(const DecodeArgs &a, int g, int phys,
 // permutation of d applied identically to both operands and undone when the
 // output is written, so the products are unchanged.
 template <int D, int G, bool FP8, bool APPEND = false>
-__global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
+__global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMinBlocks)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, DecodeArgs a)
 {
     using C = Cfg<D, G, FP8>;
@@ -595,7 +690,6 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
     int *phys_st = reinterpret_cast<int *>(smem + C::kPhys) + warp * S;
     int *warp_tot = reinterpret_cast<int *>(smem + C::kWarpTot);
     int32_t *ps = reinterpret_cast<int32_t *>(smem + C::kPs);
-    float *scratch = reinterpret_cast<float *>(smem + C::kScratch) + warp * 16;
     uint8_t *rowbuf = smem + C::kNewRow + warp * 4 * D;  // fused step: this warp's new K and V rows
 
     if (tid == 0) {
@@ -607,7 +701,8 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
     int32_t *cl = ps + a.batch + 1;
     griddep_wait();  // inputs may come from the previous kernel on the stream
     griddep_launch_dependents();
-    scan_blocks<NW>(a, ps, cl, warp_tot);  // ends with __syncthreads; the last CTA-wide barrier
+    scan_blocks<NW>(a.context_lens, a.batch, a.W, a.skip_blocks, blockIdx.x == 0 ? a.err : nullptr, ps, cl,
+                    warp_tot);  // ends with __syncthreads; the last CTA-wide barrier
     Stream st;
     st.ps = ps;
     st.batch = a.batch;
@@ -617,14 +712,11 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
     st.share = a.slice_blocks > 0 ? a.slice_blocks : max(1, (st.total + st.n_warps - 1) / st.n_warps);
     st.n_slices = (st.total + st.share - 1) / st.share;
     const int me = (int)blockIdx.x * NW + warp;
-    for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {  // nothing to stream for b
-        if (ps[b + 1] != ps[b]) continue;
-        if (a.n_pre == 0) {  // empty sequence: zero rows
+    if (a.n_pre == 0) {  // empty sequences: zero rows (cascade: the merge kernel writes them)
+        for (int b = blockIdx.x; b < a.batch; b += gridDim.x) {
+            if (ps[b + 1] != ps[b]) continue;
             uint4 *o = reinterpret_cast<uint4 *>(a.out + (int64_t)b * a.n_q * D);
             for (int i = tid; i < a.n_q * D / 8; i += kThreads) o[i] = make_uint4(0, 0, 0, 0);
-        } else {  // cascade, prefix only: the prefix chunks alone
-            MergeRefs mr{a.ws_ml, a.ws_o, a.out, a.counters, a.n_kv, a.n_q, a.batch, a.pre_base, a.n_pre};
-            for (int g = warp; g < a.n_kv; g += NW) merge_pieces<D, G>(mr, b, g, 0, 0, lane, scratch);
         }
     }
 
@@ -860,8 +952,8 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
                 }
             }
         } else {
-            // a part of (b, g): publish (m, l, O); the warp completing the count
-            // merges every piece of (b, g), i.e. the slices its run overlaps.
+            // a part of (b, g) (or, in cascade decode, its tail): publish (m, l, O)
+            // for the merge kernel
             const int64_t slot = (int64_t)pc.slice + (int64_t)pc.b * a.n_kv + pc.g;  // unique along the stream
             float *wo = a.ws_o + slot * G * D;
 #pragma unroll
@@ -877,19 +969,6 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
                 if (h0) a.ws_ml[slot * G + 2 * c4] = make_float2(m0, l0);
                 if (h1) a.ws_ml[slot * G + 2 * c4 + 1] = make_float2(m1, l1);
             }
-            __syncwarp();  // orders the lanes' stores before lane 0's fence (cumulative)
-            const int start = a.n_kv * ps[pc.b] + pc.g * pc.nblk;
-            const int s_first = start / st.share, s_last = (start + pc.nblk - 1) / st.share;
-            int prev = 0;
-            if (lane == 0) {
-                __threadfence();
-                prev = atomicAdd(&a.counters[pc.b * a.n_kv + pc.g], 1);
-            }
-            prev = __shfl_sync(kFull, prev, 0);
-            if (prev == s_last - s_first) {
-                MergeRefs mr{a.ws_ml, a.ws_o, a.out, a.counters, a.n_kv, a.n_q, a.batch, a.pre_base, a.n_pre};
-                merge_pieces<D, G>(mr, pc.b, pc.g, s_first, s_last - s_first + 1, lane, scratch);
-            }
         }
         pc = nx;
         have = have_nx;
@@ -902,31 +981,37 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads)
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Workspace: counters [batch * n_kv] int (zero between calls), then partial
-// (max, sum) and O for up to n_slices + batch * n_kv pieces.
+// Workspace: partial (max, sum) and O for up to n_slices + batch * n_kv
+// pieces.  Nothing in it needs to start at zero: every partial the merge
+// kernel reads was written by the decode launch before it.
 struct WsLayout {
-    size_t counters, ml, o, total;
+    size_t ml, o, total;
 };
 
 static WsLayout ws_layout(int batch, int n_q, int n_kv, int d_head, int64_t slots)
 {
     const int G = n_q / n_kv;
     WsLayout w;
-    w.counters = 0;
-    w.ml = align256(4 * (size_t)batch * n_kv);
+    w.ml = 0;
     w.o = w.ml + align256(8 * (size_t)slots * G);
     w.total = w.o + 4 * (size_t)slots * G * d_head;
     return w;
 }
 
-// Upper bound on pieces (workspace slots): one per slice plus one per
-// (sequence, head) run; `warps` is the grid's total warp count.
-static int64_t max_slots(pkv_pool *pool, int batch, int n_kv, int max_blocks_per_seq, int warps)
+// Upper bound on the slices of the stream; `warps` is the grid's total warp
+// count.
+static int64_t max_slices(pkv_pool *pool, int batch, int n_kv, int max_blocks_per_seq, int warps)
 {
     const int slice_blocks = pool->partition_tokens / kBlockSize;
     const int64_t total = (int64_t)batch * n_kv * max_blocks_per_seq;
-    const int64_t n_slices = slice_blocks > 0 ? (total + slice_blocks - 1) / slice_blocks : (int64_t)warps;
-    return n_slices + (int64_t)batch * n_kv;
+    return slice_blocks > 0 ? (total + slice_blocks - 1) / slice_blocks : (int64_t)warps;
+}
+
+// Upper bound on pieces (workspace slots): one per slice plus one per
+// (sequence, head) run.
+static int64_t max_slots(pkv_pool *pool, int batch, int n_kv, int max_blocks_per_seq, int warps)
+{
+    return max_slices(pool, batch, n_kv, max_blocks_per_seq, warps) + (int64_t)batch * n_kv;
 }
 
 // Persistent grid of the decode kernel for (d_head, G, dtype) at `batch`.
@@ -962,6 +1047,51 @@ static pkv_status decode_grid(pkv_pool *pool, int batch, int max_blocks_per_seq,
     return PKV_OK;
 }
 
+// Point the decode arguments at workspace `ws` laid out as L.
+static void bind_workspace(DecodeArgs &a, uint8_t *ws, const WsLayout &L)
+{
+    a.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
+    a.ws_o = reinterpret_cast<float *>(ws + L.o);
+}
+
+// The merge kernel behind a decode launch with arguments `a`; its CTAs wait
+// (programmatic dependent launch) for the decode grid to finish.  max_items
+// bounds the slice boundaries, i.e. the workspace slots.
+template <int D, int G>
+static pkv_status launch_merge(pkv_pool *pool, const DecodeArgs &a, int n_warps, int64_t max_items, cudaStream_t s)
+{
+    MergeArgs m;
+    m.ws_ml = a.ws_ml;
+    m.ws_o = a.ws_o;
+    m.out = a.out;
+    m.context_lens = a.context_lens;
+    m.n_kv = a.n_kv;
+    m.n_q = a.n_q;
+    m.batch = a.batch;
+    m.W = a.W;
+    m.skip_blocks = a.skip_blocks;
+    m.n_warps = n_warps;
+    m.slice_blocks = a.slice_blocks;
+    m.pre_base = a.pre_base;
+    m.n_pre = a.n_pre;
+    // one wave: as many CTAs as are resident at once, at most one per work item
+    static int occ = 0;
+    static std::once_flag once;
+    const size_t smem = 4 * ((size_t)a.batch + 1);
+    std::call_once(once, [&] {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, merge_kernel<D, G>, kMergeThreads,
+                                                          4 * (kMaxBatch + 1)) != cudaSuccess)
+            occ = 1;
+    });
+    const int64_t items = a.n_pre > 0 ? (int64_t)a.batch * a.n_kv : max_items;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)pool->num_sms * std::max(1, occ)));
+    LaunchScope ls(pool, kMerge, s);
+    cudaError_t e = launch_pdl(merge_kernel<D, G>, dim3((unsigned)grid), dim3(kMergeThreads), smem, s, m);
+    ls.done();
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+    return PKV_OK;
+}
+
 template <int D, int G, bool FP8>
 static pkv_status launch_decode(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
 {
@@ -973,16 +1103,13 @@ static pkv_status launch_decode(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
     const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
     st = ensure_workspace(pool, L.total);
     if (st != PKV_OK) return st;
-    uint8_t *ws = static_cast<uint8_t *>(pool->ws);
-    a.counters = reinterpret_cast<int *>(ws + L.counters);
-    a.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
-    a.ws_o = reinterpret_cast<float *>(ws + L.o);
+    bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
     LaunchScope ls(pool, kDecode, s);
     cudaError_t e = launch_pdl(decode_kernel<D, G, FP8>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
                                pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-    return PKV_OK;
+    return launch_merge<D, G>(pool, a, grid * C::NW, max_slices(pool, a.batch, a.n_kv, a.W, grid * C::NW) - 1, s);
 }
 
 template <int D, bool FP8>
@@ -1086,7 +1213,6 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
     a.out = static_cast<__nv_bfloat16 *>(out);
-    a.counters = nullptr;
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
     a.slice_blocks = pool->partition_tokens / kBlockSize;
@@ -1119,16 +1245,13 @@ static pkv_status launch_step(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
     const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
     st = ensure_workspace(pool, L.total);
     if (st != PKV_OK) return st;
-    uint8_t *ws = static_cast<uint8_t *>(pool->ws);
-    a.counters = reinterpret_cast<int *>(ws + L.counters);
-    a.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
-    a.ws_o = reinterpret_cast<float *>(ws + L.o);
+    bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
     LaunchScope ls(pool, kDecode, s);
     cudaError_t e = launch_pdl(decode_kernel<D, G, FP8, true>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
                                pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
-    return PKV_OK;
+    return launch_merge<D, G>(pool, a, grid * C::NW, max_slices(pool, a.batch, a.n_kv, a.W, grid * C::NW) - 1, s);
 }
 
 template <int D, bool FP8>
@@ -1182,7 +1305,6 @@ static pkv_status step_device(pkv_pool *pool, const void *q, const void *k_new, 
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
     a.out = static_cast<__nv_bfloat16 *>(out);
-    a.counters = nullptr;
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
     a.slice_blocks = pool->partition_tokens / kBlockSize;
@@ -1463,10 +1585,7 @@ static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32
     const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, tail_slots + (int64_t)n_chunks * a.batch * a.n_kv);
     st = ensure_workspace(pool, L.total);
     if (st != PKV_OK) return st;
-    uint8_t *ws = static_cast<uint8_t *>(pool->ws);
-    a.counters = reinterpret_cast<int *>(ws + L.counters);
-    a.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
-    a.ws_o = reinterpret_cast<float *>(ws + L.o);
+    bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
     a.skip_blocks = n_prefix_blocks;
     a.n_pre = n_chunks;
     a.pre_base = tail_slots;
@@ -1485,18 +1604,20 @@ static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32
     pa.err = a.err;
     const int row_tiles = (a.batch * G + kPrefixWarps * 16 - 1) / (kPrefixWarps * 16);
     {
-        LaunchScope ls(pool, kMerge, s);  // counted as the cascade's extra launch
+        LaunchScope ls(pool, kPrefix, s);
         cudaError_t e = launch_pdl(prefix_kernel<D, G>, dim3(n_chunks, a.n_kv, row_tiles), dim3(kPrefixWarps * 32), 0,
                                    s, pool->tm_k, pool->tm_v, pa);
         ls.done();
         if (e != cudaSuccess) return cuda_fail(e, "prefix launch");
     }
-    LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl(decode_kernel<D, G, false>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
-                               pool->tm_v, a);
-    ls.done();
-    if (e != cudaSuccess) return cuda_fail(e, "decode launch (cascade tail)");
-    return PKV_OK;
+    {
+        LaunchScope ls(pool, kDecode, s);
+        cudaError_t e = launch_pdl(decode_kernel<D, G, false>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
+                                   pool->tm_v, a);
+        ls.done();
+        if (e != cudaSuccess) return cuda_fail(e, "decode launch (cascade tail)");
+    }
+    return launch_merge<D, G>(pool, a, grid * C::NW, max_slices(pool, a.batch, a.n_kv, a.W, grid * C::NW) - 1, s);
 }
 
 template <int D>
@@ -1545,7 +1666,6 @@ extern "C" pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
     a.out = static_cast<__nv_bfloat16 *>(out);
-    a.counters = nullptr;
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
     a.slice_blocks = pool->partition_tokens / kBlockSize;
@@ -1614,21 +1734,15 @@ static pkv_status launch_decode_noalloc(pkv_pool *pool, DecodeArgs a, uint8_t *s
                     "paged_decode_attention_noalloc: this call needs %zu bytes of scratch but the static array "
                     "holds %zu; use paged_decode_attention (it grows a workspace) or a smaller batch",
                     L.total, kNoAllocScratchBytes);
-    a.counters = reinterpret_cast<int *>(scratch + L.counters);
-    a.ws_ml = reinterpret_cast<float2 *>(scratch + L.ml);
-    a.ws_o = reinterpret_cast<float *>(scratch + L.o);
-    // The array keeps the previous call's contents; the piece counters must
-    // start at zero.
-    cudaError_t e = cudaMemsetAsync(a.counters, 0, sizeof(int) * (size_t)a.batch * a.n_kv, s);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(noalloc counters)");
-    {
-        std::lock_guard<std::mutex> g(pool->mu);
-        pool->launches[kDecode] += 1;
-    }
-    decode_kernel<D, G, FP8><<<(unsigned)grid, C::kThreads, smem, s>>>(pool->tm_k, pool->tm_v, a);
-    e = cudaGetLastError();
+    // The array keeps the previous call's contents; nothing in this layout
+    // needs to start at zero (every partial is written before it is read).
+    bind_workspace(a, scratch, L);
+    LaunchScope ls(pool, kDecode, s);
+    cudaError_t e = launch_pdl(decode_kernel<D, G, FP8>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
+                               pool->tm_v, a);
+    ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch (noalloc)");
-    return PKV_OK;
+    return launch_merge<D, G>(pool, a, grid * C::NW, max_slices(pool, a.batch, a.n_kv, a.W, grid * C::NW) - 1, s);
 }
 
 template <int D, bool FP8>
@@ -1698,7 +1812,6 @@ extern "C" pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void 
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
     a.out = static_cast<__nv_bfloat16 *>(out);
-    a.counters = nullptr;
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
     a.slice_blocks = pool->partition_tokens / kBlockSize;

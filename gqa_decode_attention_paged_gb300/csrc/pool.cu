@@ -71,11 +71,6 @@ pkv_status ensure_workspace(pkv_pool *pool, size_t bytes)
         pool->ws = nullptr;
         return cuda_fail(e, "cudaMalloc(workspace)");
     }
-    // The decode kernel's per-(sequence, head) piece counters live at the
-    // start of the workspace and must read zero between calls.
-    e = cudaMemset(pool->ws, 0, want);
-    if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
     pool->ws_bytes = want;
     return PKV_OK;
 }
@@ -327,9 +322,6 @@ pkv_status pkv_get_error(pkv_pool *pool, int32_t clear, uint32_t *bits)
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = cudaMemcpy(&v, pool->err, sizeof v, cudaMemcpyDeviceToHost);
     if (e == cudaSuccess && clear) e = cudaMemset(pool->err, 0, sizeof(unsigned));
-    // A timed-out decode may leave piece counters behind: reset the workspace.
-    if (e == cudaSuccess && clear && (v & PKV_DEVERR_TIMEOUT) && pool->ws)
-        e = cudaMemset(pool->ws, 0, pool->ws_bytes);
     if (e == cudaSuccess && clear) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "pkv_get_error");
     if (bits) *bits = v;
@@ -383,7 +375,10 @@ pkv_status pkv_timing_read(pkv_pool *pool, int32_t reset, pkv_timing *out)
         out->append_launches = pool->launches[kAppend];
         out->decode_launches = pool->launches[kDecode];
         out->merge_launches = pool->launches[kMerge];
-        out->launches = out->append_launches + out->decode_launches + out->merge_launches;
+        out->prefix_launches = pool->launches[kPrefix];
+        out->launches = out->append_launches + out->decode_launches + out->merge_launches + out->prefix_launches;
+        out->prefix_ms = pool->ms[kPrefix];
+        out->timed_prefix = pool->timed[kPrefix];
         out->append_ms = pool->ms[kAppend];
         out->decode_ms = pool->ms[kDecode];
         out->merge_ms = pool->ms[kMerge];

@@ -81,11 +81,14 @@ typedef struct {
     int64_t launches;        /* every kernel launch the library enqueued */
     int64_t append_launches;
     int64_t decode_launches;
-    int64_t merge_launches;  /* cascade prefix-stage launches (split-KV merges run inside decode) */
+    int64_t merge_launches;  /* split-KV merge launches (one behind every decode launch) */
     double append_ms;        /* summed event time of timed launches */
     double decode_ms;
     double merge_ms;
     int64_t timed_append, timed_decode, timed_merge;
+    int64_t prefix_launches; /* cascade decode: shared-prefix stage launches */
+    double prefix_ms;
+    int64_t timed_prefix;
 } pkv_timing;
 
 /* Create a pool of `num_blocks` blocks of `block_size` token slots, for
@@ -120,9 +123,9 @@ pkv_status kv_pool_layout(const pkv_pool *pool, pkv_layout *out);
 
 /* How paged_decode_attention splits work.  0 (the default): the batch's
  * (sequence, KV head, block) work is cut into one equal slice per resident
- * CTA, so every SM gets the same number of blocks whatever the length mix.
+ * warp, so every SM gets the same number of blocks whatever the length mix.
  * Otherwise: slices of `tokens` tokens (a multiple of 16 in [16, 2^20]),
- * taken round-robin by the CTAs.  Results agree up to rounding either way.
+ * taken round-robin by the warps.  Results agree up to rounding either way.
  * Errors: ERANGE. */
 pkv_status kv_pool_set_partition_tokens(pkv_pool *pool, int32_t tokens);
 
@@ -179,12 +182,11 @@ pkv_status paged_kv_append(pkv_pool *pool, const void *k_new, const void *v_new,
  *   out           device bf16 [batch][n_q][d_head], 16-byte aligned; rounded
  *                 to nearest even from fp32.
  * batch == 0 is a no-op; batch <= 8192 and batch * n_kv * max_blocks_per_seq
- * < 2^30.  One kernel launch: pieces of a sequence that land on different
- * thread blocks are merged by whichever block finishes its piece last.  Uses
- * the pool's split-KV workspace, growing it (cudaMalloc + cudaMemset,
- * outside any stream capture) when the call needs more.  After a timeout
- * bit (PKV_DEVERR_TIMEOUT), pkv_get_error(pool, 1, ...) also resets the
- * workspace.
+ * < 2^30.  Two kernel launches: the decode kernel, which writes every
+ * sequence it finishes whole and leaves partials for the ones split across
+ * thread blocks, and a merge kernel (a programmatic dependent launch) that
+ * combines those partials.  Uses the pool's split-KV workspace, growing it
+ * (cudaMalloc, outside any stream capture) when the call needs more.
  * Errors: EINVAL, EUNSUPPORTED (group size), ENOMEM, ECUDA. */
 pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int32_t n_q,
                                   const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -200,7 +202,8 @@ pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int32_t n_q,
  * ("KV cache, PagedAttention and FlashAttention", Problem 4 address
  * arithmetic), followed by paged_decode_attention -- the pool bytes and the
  * output are the same -- but the row is written by the thread block that
- * reads that block anyway, so the step costs one kernel launch.
+ * reads that block anyway, so the step costs the decode's two launches and
+ * no append launch.
  *   k_new, v_new  device bf16 [batch][n_kv][d_head], 16-byte aligned: the
  *                 new token of each sequence (ignored where context_len == 0).
  *   other arguments as paged_decode_attention.  A sequence's last block must
@@ -229,8 +232,9 @@ pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host, const void
  * Same result as paged_decode_attention (up to rounding order):
  *   stage 1 attends every query row of each KV head to the prefix with
  *   tensor-core tiles and keeps a (max, sum, output) partial per 256-token
- *   chunk; stage 2 decodes each sequence's blocks after the prefix and
- *   merges them with the prefix partials by log-sum-exp.  Two launches.
+ *   chunk; stage 2 decodes each sequence's blocks after the prefix; the
+ *   merge kernel combines each sequence's prefix and tail partials by
+ *   log-sum-exp.  Three launches.
  *   prefix_blocks    device int32 [n_prefix_blocks]: physical ids of the
  *                    shared prefix, which is the first n_prefix_blocks * 16
  *                    tokens of every sequence: block_tables[b][0..n) must
@@ -262,10 +266,10 @@ pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *q, int32_t 
  *     looks the array's device address up (cudaGetSymbolAddress); make that
  *     first call before any stream capture.
  *   - All calls, from every pool and stream, share the one array and it
- *     keeps the last call's contents; each call clears the counters it needs
- *     (cudaMemsetAsync on `stream`).  Calls that overlap on the GPU race on
- *     the array and give wrong results: order them on one stream, or
- *     serialise them.
+ *     keeps the last call's contents; nothing in it needs clearing (every
+ *     partial a call reads, the same call wrote first).  Calls that overlap
+ *     on the GPU race on the array and give wrong results: order them on one
+ *     stream, or serialise them.
  * Errors: as paged_decode_attention, plus ERANGE (scratch too small) and
  * EINVAL (pool's device not current). */
 pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void *q, int32_t n_q,

@@ -159,8 +159,10 @@ def test_timing_counts_launches():
         pool.timing_enable(True)
         run_step(pool, w)
         t = pool.timing_read(reset=True)
-    assert t["append_launches"] == 1 and t["decode_launches"] == 1 and t["merge_launches"] == 0
-    assert t["timed_decode"] == 1 and t["decode_ms"] > 0
+    # append, decode, and the split-KV merge behind the decode
+    assert t["append_launches"] == 1 and t["decode_launches"] == 1 and t["merge_launches"] == 1
+    assert t["prefix_launches"] == 0 and t["launches"] == 3
+    assert t["timed_decode"] == 1 and t["decode_ms"] > 0 and t["timed_merge"] == 1
 
 
 def test_workspace_reserve_then_decode():
