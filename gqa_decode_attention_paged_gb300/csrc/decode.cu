@@ -408,11 +408,11 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs &a, int b, int g, 
 // by log-sum-exp in a fixed order (the n_pre prefix chunks, then the tail
 // pieces in slice order):
 //   M = max m_p,  L = sum 2^(m_p - M) l_p,  out = sum 2^(m_p - M) O_p / L.
-// The split runs are found from the decode kernel's block prefix sums: slice
-// boundary k (stream item k * share) splits the run it falls strictly inside,
-// and a run is merged by the boundary that first splits it.  One wave of CTAs
-// walks the boundaries (in cascade decode, all runs); the warps of a CTA share
-// one run, each summing a quarter of its G x D output columns.
+// A run is split when its first and last blocks fall in different slices of
+// the decode kernel's stream, which the kernel rederives from the lengths.
+// One wave of CTAs walks the runs: a CTA per run when there are no more runs
+// than CTAs (its warps each summing a quarter of the run's G x D output
+// columns), else a warp per run.
 // ---------------------------------------------------------------------------
 
 constexpr int kMergeThreads = 128;
@@ -429,17 +429,17 @@ struct MergeArgs {
     int n_pre;         // pre_base + (k * batch + b) * n_kv + g; n_pre = 0 without a shared prefix
 };
 
-// One warp: chunks [c_lo, c_hi) (float4 chunks of the G x D output rows) of
-// run (b, g) with pieces `np` (n_pre prefix chunks, then tail slots from
-// `base`).  Lane p reads piece p's (m, l) and keeps its weights, which lanes
-// take by shuffle; PB pieces' rows are in flight at a time, the first PB
-// requested together with the (m, l).  Every sum has a fixed order.
-template <int D, int G>
+// One warp: chunks [c_lo, c_hi) (float4 chunks of the G x D output rows, at
+// most CW of them) of run (b, g) with `np` pieces (n_pre prefix chunks, then
+// tail slots from `base`).  Lane p reads piece p's (m, l) and keeps its
+// weights, which lanes take by shuffle; PB pieces' rows are in flight at a
+// time, the first PB requested together with the (m, l).  Every sum has a
+// fixed order.
+template <int D, int G, int CW>
 __device__ __forceinline__ void merge_run_warp(const MergeArgs &a, int b, int g, int np, int64_t base, int c_lo,
                                                int c_hi, int lane)
 {
-    constexpr int CW = (G * D / 4 + kMergeWarps - 1) / kMergeWarps;  // chunks per warp
-    constexpr int KW = (CW + 31) / 32;                                 // chunks per lane
+    constexpr int KW = (CW + 31) / 32;  // chunks per lane
     constexpr int PB = 8 / KW;
     auto slot = [&](int p) -> int64_t {
         return p < a.n_pre ? a.pre_base + ((int64_t)p * a.batch + b) * a.n_kv + g : base + (p - a.n_pre);
@@ -543,7 +543,7 @@ template <int D, int G>
 __global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(MergeArgs a)
 {
     constexpr int CHUNKS = G * D / 4;
-    constexpr int CW = (CHUNKS + kMergeWarps - 1) / kMergeWarps;
+    constexpr int CW = (CHUNKS + kMergeWarps - 1) / kMergeWarps;  // a CTA per run: columns per warp
     extern __shared__ int32_t ps[];  // [batch + 1]
     __shared__ int warp_tot[kMergeWarps];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -554,36 +554,35 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(MergeArgs a)
     const int share = a.slice_blocks > 0 ? a.slice_blocks : max(1, (total + a.n_warps - 1) / a.n_warps);
     griddep_wait();  // the decode kernel's partials
     griddep_launch_dependents();
-    const int n_items = a.n_pre > 0 ? a.batch * a.n_kv : max(0, (total + share - 1) / share - 1);
-    const int c_lo = min(CHUNKS, warp * CW), c_hi = min(CHUNKS, c_lo + CW);
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        int b, g;
-        if (a.n_pre > 0) {  // cascade: every run takes in the prefix chunks
-            b = it / a.n_kv;
-            g = it - b * a.n_kv;
-        } else {  // slice boundary it + 1
-            const int f = (it + 1) * share;
-            int lo = 0, hi = a.batch - 1;  // largest b with n_kv * ps[b] <= f
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (a.n_kv * ps[mid] <= f) lo = mid; else hi = mid - 1;
-            }
-            b = lo;
-            const int nb = ps[b + 1] - ps[b];
-            const int r = f - a.n_kv * ps[b];
-            g = r / nb;
-            const int j = r - g * nb;  // the boundary's block within the run
-            if (j == 0 || j > share) continue;  // at a run start, or not the run's first split
-        }
+    const int runs = a.batch * a.n_kv;
+    // (s_first, piece count) of run r; 0 pieces for an empty tail
+    auto pieces = [&](int r, int &b, int &g, int &s_first) -> int {
+        b = r / a.n_kv;
+        g = r - b * a.n_kv;
         const int nblk = ps[b + 1] - ps[b];
-        int s_first = 0, n = 0;
-        if (nblk > 0) {
-            const int start = a.n_kv * ps[b] + g * nblk;
-            s_first = start / share;
-            n = (start + nblk - 1) / share - s_first + 1;
-        }
+        s_first = 0;
+        if (nblk == 0) return 0;
+        const int start = a.n_kv * ps[b] + g * nblk;
+        s_first = start / share;
+        return (start + nblk - 1) / share - s_first + 1;
+    };
+    if (runs <= (int)gridDim.x) {  // a CTA per run
+        const int r = blockIdx.x;
+        if (r >= runs) return;
+        int b, g, s_first;
+        const int n = pieces(r, b, g, s_first);
+        if (a.n_pre == 0 && n <= 1) return;  // written whole by the decode kernel (or empty)
+        const int c_lo = min(CHUNKS, warp * CW), c_hi = min(CHUNKS, c_lo + CW);
         const int64_t base = (int64_t)s_first + (int64_t)b * a.n_kv + g;  // slot of tail piece 0
-        if (c_lo < c_hi) merge_run_warp<D, G>(a, b, g, a.n_pre + n, base, c_lo, c_hi, lane);
+        if (c_lo < c_hi) merge_run_warp<D, G, CW>(a, b, g, a.n_pre + n, base, c_lo, c_hi, lane);
+    } else {  // a warp per run
+        for (int r = blockIdx.x * kMergeWarps + warp; r < runs; r += gridDim.x * kMergeWarps) {
+            int b, g, s_first;
+            const int n = pieces(r, b, g, s_first);
+            if (a.n_pre == 0 && n <= 1) continue;
+            const int64_t base = (int64_t)s_first + (int64_t)b * a.n_kv + g;
+            merge_run_warp<D, G, CHUNKS>(a, b, g, a.n_pre + n, base, 0, CHUNKS, lane);
+        }
     }
 }
 
@@ -1054,11 +1053,11 @@ static void bind_workspace(DecodeArgs &a, uint8_t *ws, const WsLayout &L)
     a.ws_o = reinterpret_cast<float *>(ws + L.o);
 }
 
-// The merge kernel behind a decode launch with arguments `a`; its CTAs wait
-// (programmatic dependent launch) for the decode grid to finish.  max_items
-// bounds the slice boundaries, i.e. the workspace slots.
+// The merge kernel behind a decode launch with arguments `a` on a grid of
+// n_warps warps; its CTAs wait (programmatic dependent launch) for the
+// decode grid to finish.
 template <int D, int G>
-static pkv_status launch_merge(pkv_pool *pool, const DecodeArgs &a, int n_warps, int64_t max_items, cudaStream_t s)
+static pkv_status launch_merge(pkv_pool *pool, const DecodeArgs &a, int n_warps, cudaStream_t s)
 {
     MergeArgs m;
     m.ws_ml = a.ws_ml;
@@ -1083,8 +1082,8 @@ static pkv_status launch_merge(pkv_pool *pool, const DecodeArgs &a, int n_warps,
                                                           4 * (kMaxBatch + 1)) != cudaSuccess)
             occ = 1;
     });
-    const int64_t items = a.n_pre > 0 ? (int64_t)a.batch * a.n_kv : max_items;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(items, (int64_t)pool->num_sms * std::max(1, occ)));
+    const int64_t runs = (int64_t)a.batch * a.n_kv;
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(runs, (int64_t)pool->num_sms * std::max(1, occ)));
     LaunchScope ls(pool, kMerge, s);
     cudaError_t e = launch_pdl(merge_kernel<D, G>, dim3((unsigned)grid), dim3(kMergeThreads), smem, s, m);
     ls.done();
@@ -1109,7 +1108,7 @@ static pkv_status launch_decode(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
                                pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-    return launch_merge<D, G>(pool, a, grid * C::NW, max_slices(pool, a.batch, a.n_kv, a.W, grid * C::NW) - 1, s);
+    return launch_merge<D, G>(pool, a, grid * C::NW, s);
 }
 
 template <int D, bool FP8>
@@ -1251,7 +1250,7 @@ static pkv_status launch_step(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
                                pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
-    return launch_merge<D, G>(pool, a, grid * C::NW, max_slices(pool, a.batch, a.n_kv, a.W, grid * C::NW) - 1, s);
+    return launch_merge<D, G>(pool, a, grid * C::NW, s);
 }
 
 template <int D, bool FP8>
@@ -1617,7 +1616,7 @@ static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32
         ls.done();
         if (e != cudaSuccess) return cuda_fail(e, "decode launch (cascade tail)");
     }
-    return launch_merge<D, G>(pool, a, grid * C::NW, max_slices(pool, a.batch, a.n_kv, a.W, grid * C::NW) - 1, s);
+    return launch_merge<D, G>(pool, a, grid * C::NW, s);
 }
 
 template <int D>
@@ -1742,7 +1741,7 @@ static pkv_status launch_decode_noalloc(pkv_pool *pool, DecodeArgs a, uint8_t *s
                                pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch (noalloc)");
-    return launch_merge<D, G>(pool, a, grid * C::NW, max_slices(pool, a.batch, a.n_kv, a.W, grid * C::NW) - 1, s);
+    return launch_merge<D, G>(pool, a, grid * C::NW, s);
 }
 
 template <int D, bool FP8>
