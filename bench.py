@@ -531,13 +531,15 @@ def run_ours(args):
                        l2=("flushed (512 MB write) between steps" if args.flush_l2 else
                            f"inputs larger than L2: {acct['kv_unique'] / 1e6:.0f} MB of KV per call vs 129 MB L2"),
                        work_split=(f"slices of {args.partition_tokens} tokens" if args.partition_tokens
-                                   else "one equal slice of the batch's blocks per resident CTA")),
+                                   else "one equal slice of the batch's blocks per resident warp")),
         "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "bytes_per_launch": step_bytes, "avg_launch_ms": dec_ms, "peak_source": peak_note,
                      "traffic_source": traffic_note, "kernel_source_sha": sha},
-        "kernels_ms_avg": {"decode_kernel": dec_ms},
-        "step_call": "paged_decode_step (append + decode, one launch)",
+        "kernels_ms_avg": {"decode_kernel": dec_ms,
+                           "merge_kernel": tm["merge_ms"] / max(1, tm["timed_merge"])},
+        "step_call": "paged_decode_step (the append fused into the decode kernel, then the split-KV merge "
+                     "kernel: two launches)",
         "two_call_step_ms": two_call_ms,
         "step_frac_of_peak": value / world / peak,
         "gpu_launches": launches,

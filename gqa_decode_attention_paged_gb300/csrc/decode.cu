@@ -1389,15 +1389,15 @@ namespace pkv {
 // partial per 256-token chunk of the prefix.  Stage 2 is the decode kernel
 // started past the prefix blocks; it merges its pieces with these partials.
 
-constexpr int kPrefixChunkBlocks = 16;  // prefix blocks per stage-1 CTA
-constexpr int kPrefixWarps = 4;         // 16 query rows per warp
-constexpr int kPrefixStages = 3;
+constexpr int kPrefixWarps = 4;        // 16 query rows per warp
+constexpr int kPrefixMaxStages = 16;   // stages of the copy ring: a chunk of up to 16 blocks is in flight at once
+constexpr int kPrefixMinChunk = 16;    // blocks per chunk at least (fewer chunks, fewer partials to merge)
 
 struct PrefixArgs {
     const __nv_bfloat16 *q;
     int n_q, n_kv, batch;
     const int32_t *prefix_blocks;
-    int n_prefix_blocks;
+    int n_prefix_blocks, chunk_blocks, stages;
     int64_t num_blocks;
     float qscale;
     float2 *ws_ml;
@@ -1412,29 +1412,37 @@ __global__ void __launch_bounds__(kPrefixWarps * 32)
 {
     using Gm = Geo<D, false>;
     constexpr int NT = D / 16;
-    constexpr int S = kPrefixStages;
-    __shared__ __align__(1024) uint8_t ring[S * Gm::STAGE];
-    __shared__ uint64_t bars[S];
-    __shared__ int phys_st[S];
+    const int S = a.stages;  // ring stages (dynamic shared memory)
+    extern __shared__ __align__(1024) uint8_t prefix_smem[];
+    uint8_t *ring = prefix_smem + ((1024u - (smem_u32(prefix_smem) & 1023u)) & 1023u);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + S * Gm::STAGE);
+    int *phys_st = reinterpret_cast<int *>(bars + kPrefixMaxStages);
+    int *tab = phys_st + kPrefixMaxStages;  // this chunk's block ids
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, c4 = lane & 3;
     const int chunk = blockIdx.x, g = blockIdx.y;
     const int R = a.batch * G;  // query rows of KV head g
     const int r0 = blockIdx.z * (kPrefixWarps * 16) + warp * 16;
-    const int j0 = chunk * kPrefixChunkBlocks, j1 = min(j0 + kPrefixChunkBlocks, a.n_prefix_blocks);
-    const uint64_t policy = l2_policy_evict_first();
+    const int j0 = chunk * a.chunk_blocks, j1 = min(j0 + a.chunk_blocks, a.n_prefix_blocks);
+    // every row tile of this head reads the same tiles: keep them in L2
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
     if (tid == 0) {
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
         fence_mbarrier_init();
     }
-    griddep_wait();
+    // Launched behind the tail decode, which never touches the prefix
+    // partials: let the merge kernel launch now, start at once (the inputs
+    // read here predate the decode launch), and wait for the decode grid
+    // only at the end, so that this grid's completion implies the decode's.
     griddep_launch_dependents();
+    for (int j = j0 + tid; j < j1; j += kPrefixWarps * 32) tab[j - j0] = a.prefix_blocks[j];
     __syncthreads();
     auto issue = [&](int j) {  // thread 0: block j of the prefix into stage (j - j0) % S
         const int st = (j - j0) % S;
-        const int phys = a.prefix_blocks[j];
+        const int phys = tab[j - j0];
         const bool ok = phys >= 0 && phys < a.num_blocks;
         phys_st[st] = ok ? phys : -1;
         if (ok) {
@@ -1575,11 +1583,31 @@ static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32
                                        int n_prefix_blocks, cudaStream_t s)
 {
     using C = Cfg<D, G, false>;
+    using Gm = Geo<D, false>;
     int grid = 0;
     size_t smem = 0;
     pkv_status st = decode_grid<D, G, false>(pool, a.batch, a.W, &grid, &smem);
     if (st != PKV_OK) return st;
-    const int n_chunks = (n_prefix_blocks + kPrefixChunkBlocks - 1) / kPrefixChunkBlocks;
+    // Prefix chunks: enough CTAs to cover the SMs, each chunk at least
+    // kPrefixMinChunk blocks (every chunk is one more partial per
+    // sequence to merge) and at most 1024.
+    const int row_tiles = (a.batch * G + kPrefixWarps * 16 - 1) / (kPrefixWarps * 16);
+    const int64_t per_chunk_ctas = (int64_t)a.n_kv * row_tiles;
+    int n_chunks = (int)std::min<int64_t>((pool->num_sms + per_chunk_ctas - 1) / per_chunk_ctas,
+                                          std::max(1, n_prefix_blocks / kPrefixMinChunk));
+    n_chunks = std::max(n_chunks, (n_prefix_blocks + 1023) / 1024);
+    const int chunk_blocks = (n_prefix_blocks + n_chunks - 1) / n_chunks;
+    n_chunks = (n_prefix_blocks + chunk_blocks - 1) / chunk_blocks;
+    const int stages = std::min(kPrefixMaxStages, chunk_blocks);
+    const size_t pre_smem = 1024 + (size_t)stages * Gm::STAGE + kPrefixMaxStages * 12 + 4 * (size_t)chunk_blocks;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(prefix_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)(1024 + kPrefixMaxStages * Gm::STAGE + kPrefixMaxStages * 12 + 4 * 1024));
+    });
+    if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(prefix)");
+
     const int64_t tail_slots = max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW);
     const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, tail_slots + (int64_t)n_chunks * a.batch * a.n_kv);
     st = ensure_workspace(pool, L.total);
@@ -1595,26 +1623,29 @@ static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32
     pa.batch = a.batch;
     pa.prefix_blocks = prefix_blocks;
     pa.n_prefix_blocks = n_prefix_blocks;
+    pa.chunk_blocks = chunk_blocks;
+    pa.stages = stages;
     pa.num_blocks = a.num_blocks;
     pa.qscale = a.qscale;
     pa.ws_ml = a.ws_ml;
     pa.ws_o = a.ws_o;
     pa.pre_base = tail_slots;
     pa.err = a.err;
-    const int row_tiles = (a.batch * G + kPrefixWarps * 16 - 1) / (kPrefixWarps * 16);
-    {
-        LaunchScope ls(pool, kPrefix, s);
-        cudaError_t e = launch_pdl(prefix_kernel<D, G>, dim3(n_chunks, a.n_kv, row_tiles), dim3(kPrefixWarps * 32), 0,
-                                   s, pool->tm_k, pool->tm_v, pa);
-        ls.done();
-        if (e != cudaSuccess) return cuda_fail(e, "prefix launch");
-    }
+    // Order: the tail decode, then the prefix stage (its CTAs fill the SMs
+    // the decode's warps leave as they finish), then the merge.
     {
         LaunchScope ls(pool, kDecode, s);
         cudaError_t e = launch_pdl(decode_kernel<D, G, false>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
                                    pool->tm_v, a);
         ls.done();
         if (e != cudaSuccess) return cuda_fail(e, "decode launch (cascade tail)");
+    }
+    {
+        LaunchScope ls(pool, kPrefix, s);
+        cudaError_t e = launch_pdl(prefix_kernel<D, G>, dim3(n_chunks, a.n_kv, row_tiles), dim3(kPrefixWarps * 32),
+                                   pre_smem, s, pool->tm_k, pool->tm_v, pa);
+        ls.done();
+        if (e != cudaSuccess) return cuda_fail(e, "prefix launch");
     }
     return launch_merge<D, G>(pool, a, grid * C::NW, s);
 }
