@@ -1,10 +1,10 @@
 """Benchmark: paged GQA decode attention on GB300.
 
 One step = the whole hot path over one batch: append the new token of every
-sequence into the paged pool and decode attention for every sequence, in one
-launch (paged_decode_step; the split-KV merge runs inside the kernel).  The
-same step as two calls (paged_kv_append, paged_decode_attention) is timed
-beside it.  The default workload is the Llama3-8B
+sequence into the paged pool and decode attention for every sequence
+(paged_decode_step: the append fused into the decode kernel, then the
+split-KV merge kernel).  The same step as two calls (paged_kv_append,
+paged_decode_attention) is timed beside it.  The default workload is the Llama3-8B
 attention shape (n_q=32, n_kv=8, d_head=128, batch 64, lengths uniform in
 [1024, 2048], bf16 KV); ``--workload`` picks another.
 
@@ -12,6 +12,10 @@ Prints one JSON line.  ``value`` is achieved KV-read bandwidth (algorithmic
 bytes: K and V of every cached token + q + out, per step) in GB/s over the
 device-timed region, summed over ranks; ``calls_per_s`` is decode calls per
 second.  ``--impl reference`` times the CPU oracle instead.
+
+``--mode blocks`` instead measures the block-management kernels (copy-on-write
+block copies, swap out / in over the CPU-GPU link) and ``--mode cascade``
+the cascade decode over a shared prefix; each prints its own JSON line.
 
 Run:  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
 N > 1 runs under torchrun as independent replicas (one per GPU, no
@@ -50,6 +54,7 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--flush-l2", action="store_true", help="write 512 MB between steps")
+    p.add_argument("--mode", default="decode", choices=["decode", "blocks", "cascade"])
     return p.parse_args(argv)
 
 
@@ -488,18 +493,17 @@ def run_ours(args):
         pool.close()
         return 0
 
-    # ---- parity on this very launch configuration (oracle, CPU) ----
-    import oracle  # noqa: F401  (test infrastructure: parity check and CPU baseline only)
-
-    m = oracle_setup(w)
-    ref = oracle_step(m, w, list(range(w.batch)))
-    got = out.float().cpu().numpy().astype(np.float64)
-    err = np.abs(got - ref)
-    parity = {"max_abs": float(err.max()), "mean_abs": float(err.mean()), "tol_max_abs": 1e-2,
-              "tol_mean_abs": 1e-3, "ok": bool(err.max() <= 1e-2 and err.mean() <= 1e-3)}
-
-    cpu = None
+    # ---- the CPU-baseline leg: the oracle (test infrastructure) runs this
+    # step on the host; its output of the full batch also gives the parity
+    # figures for this very launch configuration, then it is timed ----
+    cpu, parity = None, None
     if not args.no_cpu_baseline:
+        m = oracle_setup(w)
+        ref = oracle_step(m, w, list(range(w.batch)))
+        got = out.float().cpu().numpy().astype(np.float64)
+        err = np.abs(got - ref)
+        parity = {"max_abs": float(err.max()), "mean_abs": float(err.mean()), "tol_max_abs": 1e-2,
+                  "tol_mean_abs": 1e-3, "ok": bool(err.max() <= 1e-2 and err.mean() <= 1e-3)}
         gbs, secs, nseq, threads, _ = time_oracle(w, m, budget_s=12.0)
         cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{nseq} single-sequence oracle steps (append + decode, all {w.n_q} heads, "
@@ -557,10 +561,154 @@ def run_ours(args):
     return 0
 
 
+def _timed(fn, reps: int, warmup: int, stream) -> float:
+    """ms per call of fn(), CUDA events around `reps` back-to-back calls."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_blocks(args):
+    """Copy-on-write block copies and swaps on a Llama3-8B-shaped pool
+    (n_kv 8, d_head 128, bf16: 64 KiB per block, K and V)."""
+    import numpy as np
+    import torch
+
+    import gqa_decode_attention_paged_gb300 as pkv
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    NB, n = 8192, 2048  # 512 MiB pool; 2048 blocks = 128 MiB per direction
+    pool = pkv.kv_pool_create(NB, 16, 8, 128, pkv.BF16)
+    bb = pkv.kv_block_bytes(pool)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    pool.k_view().view(-1).copy_(torch.randint(0, 256, (NB * bb,), dtype=torch.uint8, device="cuda", generator=g))
+    pool.v_view().view(-1).copy_(torch.randint(0, 256, (NB * bb,), dtype=torch.uint8, device="cuda", generator=g))
+    perm = np.random.default_rng(3).permutation(NB).astype(np.int32)
+    src = torch.from_numpy(perm[:n]).cuda()
+    dst = torch.from_numpy(perm[n:2 * n]).cuda()
+    reps = max(3, min(args.steps, 200))
+    warm = max(3, args.warmup)
+    copy_ms = _timed(lambda: pkv.kv_block_copy(pool, src, dst, stream), reps, warm, stream)
+    # exact: every destination block equals its source, K and V
+    kv, vv = pool.k_view().view(NB, -1), pool.v_view().view(NB, -1)
+    copy_ok = bool(torch.equal(kv[dst.long()], kv[src.long()]) and torch.equal(vv[dst.long()], vv[src.long()]))
+    copy_bytes = 2 * n * 2 * bb  # read + write, K and V
+    host = torch.empty(n * 2 * bb, dtype=torch.uint8).pin_memory()
+    out_ms = _timed(lambda: pkv.kv_swap_out(pool, src, host, stream), reps // 4 + 3, warm, stream)
+    img_ok = bool(torch.equal(host.view(n, 2, bb)[:, 0].cuda(), kv[src.long()])
+                  and torch.equal(host.view(n, 2, bb)[:, 1].cuda(), vv[src.long()]))
+    in_ms = _timed(lambda: pkv.kv_swap_in(pool, host, dst, stream), reps // 4 + 3, warm, stream)
+    swap_bytes = n * 2 * bb
+    # the link's copy engine on the same bytes, for reference
+    dev_buf = torch.empty(swap_bytes, dtype=torch.uint8, device="cuda")
+    d2h_ms = _timed(lambda: host.copy_(dev_buf, non_blocking=True), reps // 4 + 3, warm, stream)
+    h2d_ms = _timed(lambda: dev_buf.copy_(host, non_blocking=True), reps // 4 + 3, warm, stream)
+    assert pool.get_error() == 0
+    peak, peak_note = measured_peaks()
+    gbs = lambda b, ms: b / (ms / 1e3) / 1e9  # noqa: E731
+    line = {
+        "metric": "paged KV block management: copy-on-write block copy GB/s (read+write) vs HBM peak; "
+                  "swap out/in GB/s vs the copy engine on the same link",
+        "mode": "blocks",
+        "value": gbs(copy_bytes, copy_ms),
+        "unit": "GB/s",
+        "higher_is_better": True,
+        "dtype": "bytes",
+        "data": "synthetic",
+        "config": {"workload": "llama3_8b_pool_blocks", "num_blocks": NB, "n_kv": 8, "d_head": 128,
+                   "kv_dtype": "bf16", "block_bytes_kv": 2 * bb, "blocks_moved": n},
+        "roofline": {"bound": "hbm", "kernel": "block_move_kernel<copy>", "achieved": gbs(copy_bytes, copy_ms),
+                     "peak": peak, "unit": "GB/s", "frac": gbs(copy_bytes, copy_ms) / peak,
+                     "peak_source": peak_note, "bytes_per_launch": copy_bytes, "avg_launch_ms": copy_ms},
+        "swap_out": {"value": gbs(swap_bytes, out_ms), "unit": "GB/s", "ms": out_ms,
+                     "copy_engine_d2h_gbs": gbs(swap_bytes, d2h_ms), "frac_of_copy_engine": d2h_ms / out_ms},
+        "swap_in": {"value": gbs(swap_bytes, in_ms), "unit": "GB/s", "ms": in_ms,
+                    "copy_engine_h2d_gbs": gbs(swap_bytes, h2d_ms), "frac_of_copy_engine": h2d_ms / in_ms},
+        "parity": {"copy_bit_exact": copy_ok, "swap_out_bit_exact": img_ok, "ok": copy_ok and img_ok},
+        "gpu_launches": int(pool.timing_read(reset=True)["block_launches"]),
+    }
+    print(json.dumps(line), flush=True)
+    pool.close()
+    return 0
+
+
+def run_cascade(args):
+    """Cascade decode (shared prefix read once) against plain decode on the
+    shared-prefix workload; bytes counted on unique KV slots."""
+    import numpy as np
+    import torch
+
+    import gqa_decode_attention_paged_gb300 as pkv
+    import workloads as wl
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    w = wl.shared_prefix()
+    acct = algorithmic_bytes(w)
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).cuda().view(dt)  # noqa: E731
+    pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head, pkv.BF16)
+    T = w.fill_slots.shape[0]
+    pkv.paged_kv_append(pool, dev(w.fill_k.view(np.int16), torch.bfloat16), dev(w.fill_v.view(np.int16), torch.bfloat16),
+                        dev(w.fill_slots, torch.int64))
+    pkv.paged_kv_append(pool, dev(w.step_k.view(np.int16), torch.bfloat16), dev(w.step_v.view(np.int16), torch.bfloat16),
+                        dev(w.step_slots, torch.int64))
+    q = dev(w.q.view(np.int16), torch.bfloat16)
+    tables = dev(w.block_tables, torch.int32)
+    lens = dev(w.context_lens, torch.int32)
+    n_pre = w.shared_prefix_tokens // 16
+    pre = dev(w.block_tables[0, :n_pre], torch.int32)
+    out_c, out_p = torch.empty_like(q), torch.empty_like(q)
+    reps, warm = max(3, min(args.steps, 500)), max(3, args.warmup)
+    casc_ms = _timed(lambda: pkv.paged_decode_attention_prefix(pool, q, pre, tables, lens, float(w.scale), out_c, stream),
+                     reps, warm, stream)
+    plain_ms = _timed(lambda: pkv.paged_decode_attention(pool, q, tables, lens, float(w.scale), out_p, stream),
+                      reps, warm, stream)
+    # the two paths on the same inputs (each is checked against the oracle by the tests)
+    err = (out_c.float() - out_p.float()).abs().cpu().numpy()
+    assert pool.get_error() == 0
+    peak, peak_note = measured_peaks()
+    gbs = acct["unique"] / (casc_ms / 1e3) / 1e9
+    line = {
+        "metric": "cascade decode over a shared prefix: unique KV-read GB/s vs GB300 HBM peak",
+        "mode": "cascade",
+        "value": gbs,
+        "unit": "GB/s",
+        "higher_is_better": True,
+        "ms_per_call": casc_ms,
+        "plain_decode_ms_per_call": plain_ms,
+        "speedup_vs_plain": plain_ms / casc_ms,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": dict(w.describe(), bytes_basis="unique KV slots", kv_bytes_unique=acct["kv_unique"],
+                       kv_bytes_logical=acct["kv_logical"]),
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_source": peak_note},
+        "agreement_with_plain_decode": {"max_abs": float(err.max()), "mean_abs": float(err.mean()),
+                                        "ok": bool(err.max() <= 1e-2 and err.mean() <= 1e-3)},
+    }
+    print(json.dumps(line), flush=True)
+    pool.close()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.mode == "blocks":
+        return run_blocks(args)
+    if args.mode == "cascade":
+        return run_cascade(args)
     return run_ours(args)
 
 

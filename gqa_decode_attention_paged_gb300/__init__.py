@@ -53,7 +53,8 @@ class _Timing(ctypes.Structure):
                 ("merge_ms", ctypes.c_double), ("timed_append", ctypes.c_int64),
                 ("timed_decode", ctypes.c_int64), ("timed_merge", ctypes.c_int64),
                 ("prefix_launches", ctypes.c_int64), ("prefix_ms", ctypes.c_double),
-                ("timed_prefix", ctypes.c_int64)]
+                ("timed_prefix", ctypes.c_int64), ("block_launches", ctypes.c_int64),
+                ("block_ms", ctypes.c_double), ("timed_block", ctypes.c_int64)]
 
 
 def library_path() -> str:
@@ -97,6 +98,21 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pkv_timing_enable.argtypes = [P, c.c_int32]
         lib.pkv_selftest_wait_timeout.argtypes = [P, c.c_uint64, P]
         lib.pkv_timing_read.argtypes = [P, c.c_int32, c.POINTER(_Timing)]
+        lib.kv_block_bytes.argtypes = [P]
+        lib.kv_block_bytes.restype = c.c_int64
+        lib.kv_block_copy.argtypes = [P, P, P, c.c_int64, P]
+        lib.kv_swap_out.argtypes = [P, P, c.c_int64, P, P]
+        lib.kv_swap_in.argtypes = [P, P, P, c.c_int64, P]
+        I32P = c.POINTER(c.c_int32)
+        lib.kv_alloc_create.argtypes = [c.c_int64, c.POINTER(P)]
+        lib.kv_alloc_destroy.argtypes = [P]
+        lib.kv_alloc_free_blocks.argtypes = [P]
+        lib.kv_alloc_free_blocks.restype = c.c_int64
+        lib.kv_alloc_refcount.argtypes = [P, c.c_int32, I32P]
+        lib.kv_alloc_take.argtypes = [P, c.c_int64, I32P]
+        lib.kv_alloc_share.argtypes = [P, I32P, c.c_int64]
+        lib.kv_alloc_release.argtypes = [P, I32P, c.c_int64]
+        lib.kv_alloc_prepare_write.argtypes = [P, I32P, c.c_int64, I32P, I32P, c.POINTER(c.c_int64)]
         lib.pkv_status_string.argtypes = [c.c_int]
         lib.pkv_status_string.restype = c.c_char_p
         lib.pkv_last_error_message.argtypes = []
@@ -105,7 +121,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                      "kv_pool_set_partition_tokens", "kv_pool_reserve_workspace", "paged_kv_append",
                      "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
                      "paged_decode_step_host", "paged_decode_attention_prefix", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read",
-                     "pkv_selftest_wait_timeout"):
+                     "pkv_selftest_wait_timeout", "kv_block_copy", "kv_swap_out", "kv_swap_in", "kv_alloc_create",
+                     "kv_alloc_destroy", "kv_alloc_refcount", "kv_alloc_take", "kv_alloc_share", "kv_alloc_release",
+                     "kv_alloc_prepare_write"):
             getattr(lib, name).restype = c.c_int
         _lib = lib
         return lib
@@ -373,7 +391,128 @@ def paged_decode_attention_noalloc(pool: Pool, q, block_tables, context_lens, sc
     return out
 
 
+def kv_block_bytes(pool: Pool) -> int:
+    """Bytes of one block in one array (K or V): n_kv x 16 x d_head x element size."""
+    return int(load().kv_block_bytes(pool.handle))
+
+
+def kv_block_copy(pool: Pool, src_blocks, dst_blocks, stream=None):
+    """Copy blocks src_blocks[i] -> dst_blocks[i] (int32 CUDA tensors [n]), K and V."""
+    import torch
+
+    n = int(src_blocks.shape[0])
+    sp = _dev_ptr(src_blocks, "src_blocks", torch.int32, 1, (n,))
+    dp = _dev_ptr(dst_blocks, "dst_blocks", torch.int32, 1, (n,))
+    _check(load().kv_block_copy(pool.handle, sp, dp, n, _stream_handle(stream)))
+
+
+def _pinned_ptr(t, name, nbytes):
+    import torch
+
+    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned():
+        raise TypeError(f"{name} must be a pinned CPU tensor (tensor.pin_memory())")
+    if not t.is_contiguous() or t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} must be contiguous and hold at least {nbytes} bytes")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def kv_swap_out(pool: Pool, blocks, host_dst, stream=None):
+    """Write blocks[i] (int32 CUDA tensor [n]) into pinned host tensor
+    ``host_dst`` as [n][2][kv_block_bytes] bytes (K then V)."""
+    import torch
+
+    n = int(blocks.shape[0])
+    bp = _dev_ptr(blocks, "blocks", torch.int32, 1, (n,))
+    hp = _pinned_ptr(host_dst, "host_dst", n * 2 * kv_block_bytes(pool))
+    _check(load().kv_swap_out(pool.handle, bp, n, hp, _stream_handle(stream)))
+    return host_dst
+
+
+def kv_swap_in(pool: Pool, host_src, blocks, stream=None):
+    """Fill blocks[i] (int32 CUDA tensor [n]) from pinned host tensor ``host_src``
+    laid out as kv_swap_out writes it."""
+    import torch
+
+    n = int(blocks.shape[0])
+    bp = _dev_ptr(blocks, "blocks", torch.int32, 1, (n,))
+    hp = _pinned_ptr(host_src, "host_src", n * 2 * kv_block_bytes(pool))
+    _check(load().kv_swap_in(pool.handle, hp, bp, n, _stream_handle(stream)))
+
+
+class BlockAllocator:
+    """Refcounted physical-block allocator (host): take, share, release, and
+    copy-on-write preparation.  Ids are Python ints / int32 numpy arrays."""
+
+    def __init__(self, num_blocks: int):
+        h = ctypes.c_void_p()
+        _check(load().kv_alloc_create(int(num_blocks), ctypes.byref(h)))
+        self.handle = h
+        self.num_blocks = int(num_blocks)
+
+    def close(self):
+        if self.handle:
+            load().kv_alloc_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    @staticmethod
+    def _ids(ids):
+        import numpy as np
+
+        a = np.ascontiguousarray(np.asarray(ids, dtype=np.int32).reshape(-1))
+        return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+    def free_blocks(self) -> int:
+        return int(load().kv_alloc_free_blocks(self.handle))
+
+    def refcount(self, block: int) -> int:
+        out = ctypes.c_int32()
+        _check(load().kv_alloc_refcount(self.handle, int(block), ctypes.byref(out)))
+        return int(out.value)
+
+    def take(self, n: int):
+        import numpy as np
+
+        out = np.zeros(int(n), dtype=np.int32)
+        _check(load().kv_alloc_take(self.handle, int(n), out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
+        return out
+
+    def share(self, ids):
+        a, p = self._ids(ids)
+        _check(load().kv_alloc_share(self.handle, p, a.size))
+
+    def release(self, ids):
+        a, p = self._ids(ids)
+        _check(load().kv_alloc_release(self.handle, p, a.size))
+
+    def prepare_write(self, ids):
+        """Returns (new_ids, copy_src, copy_dst): entries of ``ids`` whose block
+        is shared get a private copy target; run kv_block_copy on the pairs."""
+        import numpy as np
+
+        a, p = self._ids(ids)
+        a = a.copy()
+        p = a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+        src = np.zeros(max(1, a.size), dtype=np.int32)
+        dst = np.zeros(max(1, a.size), dtype=np.int32)
+        k = ctypes.c_int64()
+        _check(load().kv_alloc_prepare_write(self.handle, p, a.size, src.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                             dst.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), ctypes.byref(k)))
+        return a, src[:k.value].copy(), dst[:k.value].copy()
+
+
 __all__ = ["BF16", "FP8_E4M3", "Pool", "PagedKVError", "kv_pool_create", "paged_kv_append",
            "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
-           "paged_decode_step_host", "paged_decode_attention_prefix", "kv_bytes_per_token", "load",
-           "library_path"]
+           "paged_decode_step_host", "paged_decode_attention_prefix", "kv_bytes_per_token", "kv_block_bytes",
+           "kv_block_copy", "kv_swap_out", "kv_swap_in", "BlockAllocator", "load", "library_path"]

@@ -120,10 +120,10 @@ struct Cfg {
     using Gm = Geo<D, FP8>;
     static constexpr int NW = Tune<D, G, FP8>::NW;
     static constexpr int kThreads = NW * 32;
-    // resident CTAs per SM the register budget is held to: 3 x 128 threads
-    // of at most 168 registers (the shared-memory ring allows no more for
-    // bf16 d128; the rare merge calls spill around themselves instead)
-    static constexpr int kMinBlocks = 3;
+    // resident CTAs per SM the register budget is held to: 12 warps per SM,
+    // i.e. 3 x 128 threads of at most 168 registers for 4-warp CTAs (the
+    // shared-memory ring allows no more for bf16 d128)
+    static constexpr int kMinBlocks = 12 / NW > 0 ? 12 / NW : 1;
     static constexpr int kStages = std::min(8, std::max(2, Tune<D, G, FP8>::RING_KIB * 1024 / (NW * Gm::STAGE)));
     // shared-memory layout (bytes from a 1024-byte aligned base)
     static constexpr int kRing = NW * kStages * Gm::STAGE;

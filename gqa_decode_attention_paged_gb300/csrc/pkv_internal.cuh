@@ -22,7 +22,7 @@ constexpr int kBlockSize = 16;               // token slots per block
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded mbarrier waits: 2 s
 constexpr int kDefaultPartitionTokens = 0;  // 0: equal work per CTA
 
-enum KernelKind { kAppend = 0, kDecode = 1, kMerge = 2, kPrefix = 3, kNumKinds = 4 };
+enum KernelKind { kAppend = 0, kDecode = 1, kMerge = 2, kPrefix = 3, kBlocks = 4, kNumKinds = 5 };
 
 struct EventPair {
     cudaEvent_t start, stop;

@@ -376,7 +376,11 @@ pkv_status pkv_timing_read(pkv_pool *pool, int32_t reset, pkv_timing *out)
         out->decode_launches = pool->launches[kDecode];
         out->merge_launches = pool->launches[kMerge];
         out->prefix_launches = pool->launches[kPrefix];
-        out->launches = out->append_launches + out->decode_launches + out->merge_launches + out->prefix_launches;
+        out->block_launches = pool->launches[kBlocks];
+        out->block_ms = pool->ms[kBlocks];
+        out->timed_block = pool->timed[kBlocks];
+        out->launches = out->append_launches + out->decode_launches + out->merge_launches + out->prefix_launches +
+                        out->block_launches;
         out->prefix_ms = pool->ms[kPrefix];
         out->timed_prefix = pool->timed[kPrefix];
         out->append_ms = pool->ms[kAppend];

@@ -89,6 +89,9 @@ typedef struct {
     int64_t prefix_launches; /* cascade decode: shared-prefix stage launches */
     double prefix_ms;
     int64_t timed_prefix;
+    int64_t block_launches;  /* block copy / swap launches */
+    double block_ms;
+    int64_t timed_block;
 } pkv_timing;
 
 /* Create a pool of `num_blocks` blocks of `block_size` token slots, for
@@ -276,6 +279,85 @@ pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void *q, int32_t
                                           const int32_t *block_tables, int32_t max_blocks_per_seq,
                                           const int32_t *context_lens, int32_t batch, float scale,
                                           void *out, void *stream);
+
+/* ---------------------------------------------------------------------
+ * Block management: copy-on-write and swapping ("KV cache, PagedAttention
+ * and FlashAttention", Problem 4, "The idea": blocks are shared by
+ * reference count, a shared block is copied before it is written, and a
+ * preempted sequence's blocks may be swapped to CPU memory; "Memory
+ * Management in LLM Serving Systems", "Eviction: recompute or offload?").
+ * A block is block_bytes of K plus block_bytes of V: all n_kv heads' 16
+ * token rows, contiguous in each array.
+ * --------------------------------------------------------------------- */
+
+/* Bytes of one block in one array: n_kv x 16 x d_head x (2 bf16, 1 FP8).
+ * A swapped block occupies 2 x kv_block_bytes in a host buffer.  -1 for a
+ * NULL pool. */
+int64_t kv_block_bytes(const pkv_pool *pool);
+
+/* Copy blocks inside the pool: block dst_blocks[i] gets the K and V bytes of
+ * src_blocks[i], every head and token row (the copy of copy-on-write).
+ *   src_blocks, dst_blocks  device int32 [n]; no dst may appear twice or
+ *                           also as a src (unchecked; the copies run in
+ *                           parallel).  A pair with an id outside
+ *                           [0, num_blocks) is skipped and sets
+ *                           PKV_DEVERR_BLOCK_RANGE.
+ * One launch, HBM-bound.  Errors: EINVAL, ECUDA. */
+pkv_status kv_block_copy(pkv_pool *pool, const int32_t *src_blocks, const int32_t *dst_blocks, int64_t n,
+                         void *stream);
+
+/* Swap blocks out to host memory: entry i of host_dst receives block
+ * blocks[i] as [K bytes][V bytes], 2 x kv_block_bytes per entry.
+ *   blocks    device int32 [n]; out-of-range ids are skipped (their entry
+ *             left untouched) and set PKV_DEVERR_BLOCK_RANGE.
+ *   host_dst  pinned host memory (cudaHostAlloc, or cudaHostRegister),
+ *             16-byte aligned, n x 2 x kv_block_bytes bytes; the kernel
+ *             writes it directly over the CPU-GPU link.  It holds the data
+ *             once the work on `stream` has finished.
+ * One launch.  Errors: EINVAL (also for pageable host memory), ECUDA. */
+pkv_status kv_swap_out(pkv_pool *pool, const int32_t *blocks, int64_t n, void *host_dst, void *stream);
+
+/* Swap blocks in: block blocks[i] gets entry i of host_src (the layout
+ * kv_swap_out writes).  host_src: pinned, 16-byte aligned, caller-owned
+ * until the work on `stream` has finished.  Same errors as kv_swap_out. */
+pkv_status kv_swap_in(pkv_pool *pool, const void *host_src, const int32_t *blocks, int64_t n, void *stream);
+
+/* Refcounted block allocator (host side; the pages' block manager).  It
+ * tracks which of num_blocks physical blocks are in use and how many block
+ * table entries refer to each; the caller keeps the tables.  Free blocks
+ * are handed out lowest id first, so results are reproducible.  Thread-safe
+ * (one internal mutex).  All calls validate everything before changing
+ * anything. */
+typedef struct pkv_alloc pkv_alloc;
+
+/* num_blocks in [1, 2^31 - 1].  Errors: EINVAL, ENOMEM. */
+pkv_status kv_alloc_create(int64_t num_blocks, pkv_alloc **out);
+pkv_status kv_alloc_destroy(pkv_alloc *alloc);
+/* Free blocks; -1 for a NULL allocator. */
+int64_t kv_alloc_free_blocks(pkv_alloc *alloc);
+/* References to block id (0 = free).  Errors: EINVAL, ERANGE. */
+pkv_status kv_alloc_refcount(pkv_alloc *alloc, int32_t id, int32_t *out);
+/* Take n free blocks (reference count 1 each) into ids_out (host int32
+ * [n]), lowest ids first; all or nothing.  Errors: EINVAL, ENOMEM (fewer
+ * than n free). */
+pkv_status kv_alloc_take(pkv_alloc *alloc, int64_t n, int32_t *ids_out);
+/* Add one reference to each listed block (a table entry now shares it: a
+ * forked sequence, a common prefix).  Every id must be allocated.  Errors:
+ * EINVAL (free block), ERANGE. */
+pkv_status kv_alloc_share(pkv_alloc *alloc, const int32_t *ids, int64_t n);
+/* Drop one reference per listed entry; a block reaching 0 is free again.
+ * A block listed k times must hold at least k references.  Errors: EINVAL
+ * (a free block or too many releases), ERANGE. */
+pkv_status kv_alloc_release(pkv_alloc *alloc, const int32_t *ids, int64_t n);
+/* Copy-on-write, before writing into the blocks ids[0..n) (host int32, the
+ * caller's table entries): every entry whose block has other references is
+ * given a fresh block; the old block loses that reference; the pair
+ * (old, fresh) is appended to copy_src / copy_dst (host int32 [n]) and
+ * ids[i] is replaced.  *n_copies receives the pair count.  Run
+ * kv_block_copy on the pairs before writing.  All or nothing.  Errors:
+ * EINVAL, ERANGE, ENOMEM (not enough free blocks for the copies). */
+pkv_status kv_alloc_prepare_write(pkv_alloc *alloc, int32_t *ids, int64_t n, int32_t *copy_src, int32_t *copy_dst,
+                                  int64_t *n_copies);
 
 /* KV-cache bytes per token: 2 x layers x n_kv x d_head x bytes_per_value
  * ("KV cache, PagedAttention and FlashAttention", Problem 3, "The concepts";

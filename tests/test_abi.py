@@ -21,7 +21,7 @@ def _declared_functions():
     for h in HEADERS:
         text = open(h).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        for m in re.finditer(r"^\s*(?:const\s+)?(?:pkv_status|double|char|uint64_t|void)\s*\*?\s*(\w+)\s*\(",
+        for m in re.finditer(r"^\s*(?:const\s+)?(?:pkv_status|double|char|uint64_t|int64_t|void)\s*\*?\s*(\w+)\s*\(",
                              text, flags=re.M):
             names.append(m.group(1))
     return names
