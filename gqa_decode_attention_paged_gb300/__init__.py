@@ -89,6 +89,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                                        c.c_float, P, P]
         lib.paged_decode_attention_prefix.argtypes = [P, P, c.c_int32, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                                       c.c_float, P, P]
+        lib.paged_decode_attention_csr.argtypes = [P, P, c.c_int32, P, P, c.c_int64, P, c.c_int32, c.c_float, P, P]
         lib.paged_decode_step.argtypes = [P, P, P, P, c.c_int32, P, c.c_int32, P, c.c_int32, c.c_float, P, P]
         lib.paged_decode_step_host.argtypes = [P, P, P, P, c.c_int32, P, c.c_int32, P, c.c_int32, c.c_float,
                                                P, P]
@@ -120,6 +121,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         for name in ("kv_pool_create", "kv_pool_destroy", "kv_pool_set_fp8_scales", "kv_pool_layout",
                      "kv_pool_set_partition_tokens", "kv_pool_reserve_workspace", "paged_kv_append",
                      "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
+                     "paged_decode_attention_csr",
                      "paged_decode_step_host", "paged_decode_attention_prefix", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read",
                      "pkv_selftest_wait_timeout", "kv_block_copy", "kv_swap_out", "kv_swap_in", "kv_alloc_create",
                      "kv_alloc_destroy", "kv_alloc_refcount", "kv_alloc_take", "kv_alloc_share", "kv_alloc_release",
@@ -298,6 +300,25 @@ def paged_decode_attention(pool: Pool, q, block_tables, context_lens, scale: flo
     op = _dev_ptr(out, "out", torch.bfloat16, 3, tuple(q.shape))
     _check(load().paged_decode_attention(pool.handle, qp, n_q, tp, int(block_tables.shape[1]), cp, B,
                                          float(scale), op, _stream_handle(stream)))
+    return out
+
+
+def paged_decode_attention_csr(pool: Pool, q, kv_indptr, kv_indices, context_lens, scale: float, out=None,
+                               stream=None):
+    """Decode with the CSR page table: sequence b owns blocks
+    kv_indices[kv_indptr[b]:kv_indptr[b+1]] (int32 CUDA tensors)."""
+    import torch
+
+    qp = _dev_ptr(q, "q", torch.bfloat16, 3, (None, None, pool.d_head))
+    B, n_q = int(q.shape[0]), int(q.shape[1])
+    ip = _dev_ptr(kv_indptr, "kv_indptr", torch.int32, 1, (B + 1,))
+    xp = _dev_ptr(kv_indices, "kv_indices", torch.int32, 1)
+    cp = _dev_ptr(context_lens, "context_lens", torch.int32, 1, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    op = _dev_ptr(out, "out", torch.bfloat16, 3, tuple(q.shape))
+    _check(load().paged_decode_attention_csr(pool.handle, qp, n_q, ip, xp, int(kv_indices.shape[0]), cp, B,
+                                             float(scale), op, _stream_handle(stream)))
     return out
 
 
@@ -514,5 +535,6 @@ class BlockAllocator:
 
 __all__ = ["BF16", "FP8_E4M3", "Pool", "PagedKVError", "kv_pool_create", "paged_kv_append",
            "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
-           "paged_decode_step_host", "paged_decode_attention_prefix", "kv_bytes_per_token", "kv_block_bytes",
+           "paged_decode_step_host", "paged_decode_attention_prefix", "paged_decode_attention_csr",
+           "kv_bytes_per_token", "kv_block_bytes",
            "kv_block_copy", "kv_swap_out", "kv_swap_in", "BlockAllocator", "load", "library_path"]

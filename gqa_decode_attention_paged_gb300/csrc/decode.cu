@@ -60,8 +60,10 @@ struct DecodeArgs {
     int64_t num_blocks;
     int n_kv, n_q;
     const __nv_bfloat16 *q;
-    const int32_t *block_tables;
+    const int32_t *block_tables;  // dense [batch][W], or with indptr the CSR page list
     int W;
+    const int32_t *indptr;        // CSR form: sequence b owns block_tables[indptr[b] .. indptr[b+1]); null: dense
+    int64_t n_indices;            // CSR form: entries of block_tables
     const int32_t *context_lens;
     int batch;
     float qscale;          // scale * log2(e)
@@ -132,18 +134,22 @@ struct Cfg {
     static constexpr int kNewRow = (kPhys + NW * kStages * 4 + 15) / 16 * 16;  // [NW][2 * D * 2] bytes: fused
                                                                                 // step's new K, V rows
     static constexpr int kWarpTot = kNewRow + NW * 4 * D;
-    static constexpr int kPs = kWarpTot + 4 * NW;  // ps[batch + 1], then clamped lengths cl[batch]
-    static size_t smem_bytes(int batch) { return 1024 + (size_t)kPs + 4 * (size_t)(2 * batch + 1); }
+    // ps[batch + 1], then clamped lengths cl[batch], then table row starts rb[batch]
+    static constexpr int kPs = kWarpTot + 4 * NW;
+    static size_t smem_bytes(int batch) { return 1024 + (size_t)kPs + 4 * (size_t)(3 * batch + 1); }
     static_assert(G <= 8, "at most 8 query heads per KV head");
 };
 
 // Exclusive prefix sum of block counts per sequence (after the first `skip`
-// table entries) into ps[0..batch], and the clamped lengths into cl (if not
-// null); range errors go to *err when err is not null.  warp_tot is scratch
-// for NW ints.  The decode and merge kernels both derive their work from it.
+// table entries) into ps[0..batch], the clamped lengths into cl and each
+// sequence's first table entry into rb (each if not null); range errors go
+// to *err when err is not null.  A sequence's table row is W entries from
+// b * W (dense form) or entries indptr[b] .. indptr[b+1] of n_indices (CSR
+// form; a row outside that range counts as empty).  warp_tot is scratch for
+// NW ints.  The decode and merge kernels both derive their work from it.
 template <int NW>
-__device__ void scan_blocks(const int32_t *lens, int batch, int W, int skip, unsigned *err, int32_t *ps,
-                            int32_t *cl, int *warp_tot)
+__device__ void scan_blocks(const int32_t *lens, int batch, int W, const int32_t *indptr, int64_t n_indices,
+                            int skip, unsigned *err, int32_t *ps, int32_t *cl, int32_t *rb, int *warp_tot)
 {
     constexpr int NT = NW * 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -153,7 +159,16 @@ __device__ void scan_blocks(const int32_t *lens, int batch, int W, int skip, uns
         int n = 0;
         if (b < batch) {
             int c = lens[b];
-            const int cmax = W * kBlockSize;
+            int width = W, row = b * W;
+            if (indptr) {
+                const int32_t lo = indptr[b], hi = indptr[b + 1];
+                const bool ok = lo >= 0 && lo <= hi && (int64_t)hi <= n_indices;
+                if (!ok && err) atomicOr(err, PKV_DEVERR_BLOCK_RANGE);
+                width = ok ? hi - lo : 0;
+                row = ok ? lo : 0;
+            }
+            if (rb) rb[b] = row;
+            const int cmax = width > (INT32_MAX / kBlockSize) ? INT32_MAX : width * kBlockSize;
             if (c < 0 || c > cmax) {
                 if (err) atomicOr(err, PKV_DEVERR_CTX_RANGE);
                 c = c < 0 ? 0 : cmax;
@@ -275,9 +290,9 @@ __device__ __forceinline__ void seg_next(Seg &s, const Stream &st)
     s.n = min(32, s.p.j1 - s.j);
 }
 
-__device__ __forceinline__ int seg_load(const Seg &s, int lane, const DecodeArgs &a)
+__device__ __forceinline__ int seg_load(const Seg &s, int lane, const DecodeArgs &a, const int32_t *rb)
 {
-    return (s.live && lane < s.n) ? a.block_tables[(int64_t)s.p.b * a.W + a.skip_blocks + s.j + lane] : -1;
+    return (s.live && lane < s.n) ? a.block_tables[(int64_t)rb[s.p.b] + a.skip_blocks + s.j + lane] : -1;
 }
 
 // ---------------------------------------------------------------------------
@@ -423,6 +438,8 @@ struct MergeArgs {
     const float *ws_o;
     __nv_bfloat16 *out;
     const int32_t *context_lens;
+    const int32_t *indptr;  // CSR tables (null: dense)
+    int64_t n_indices;
     int n_kv, n_q, batch, W, skip_blocks;
     int n_warps, slice_blocks;  // the decode grid's warps and slice length (0: automatic)
     int64_t pre_base;  // cascade: slot of prefix chunk 0 for (b=0, g=0); chunk k of (b, g) is
@@ -549,7 +566,8 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(MergeArgs a)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // The decode kernel's slicing, rederived from the lengths (its inputs, not
     // its outputs) while it still runs; only the partials need the wait.
-    scan_blocks<kMergeWarps>(a.context_lens, a.batch, a.W, a.skip_blocks, nullptr, ps, nullptr, warp_tot);
+    scan_blocks<kMergeWarps>(a.context_lens, a.batch, a.W, a.indptr, a.n_indices, a.skip_blocks, nullptr, ps,
+                             nullptr, nullptr, warp_tot);
     const int total = a.n_kv * ps[a.batch];
     const int share = a.slice_blocks > 0 ? a.slice_blocks : max(1, (total + a.n_warps - 1) / a.n_warps);
     griddep_wait();  // the decode kernel's partials
@@ -698,10 +716,11 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
         fence_mbarrier_init();
     }
     int32_t *cl = ps + a.batch + 1;
+    int32_t *rb = cl + a.batch;
     griddep_wait();  // inputs may come from the previous kernel on the stream
     griddep_launch_dependents();
-    scan_blocks<NW>(a.context_lens, a.batch, a.W, a.skip_blocks, blockIdx.x == 0 ? a.err : nullptr, ps, cl,
-                    warp_tot);  // ends with __syncthreads; the last CTA-wide barrier
+    scan_blocks<NW>(a.context_lens, a.batch, a.W, a.indptr, a.n_indices, a.skip_blocks,
+                    blockIdx.x == 0 ? a.err : nullptr, ps, cl, rb, warp_tot);  // ends with __syncthreads
     Stream st;
     st.ps = ps;
     st.batch = a.batch;
@@ -726,10 +745,10 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
     // ---- producer (uniform across the warp; lane 0 issues the copies) ----
     Seg cur;
     seg_first(cur, st, me);
-    int tab_cur = seg_load(cur, lane, a);
+    int tab_cur = seg_load(cur, lane, a, rb);
     Seg nxt = cur;
     seg_next(nxt, st);
-    int tab_nxt = seg_load(nxt, lane, a);
+    int tab_nxt = seg_load(nxt, lane, a, rb);
     int seg_k = 0, n_issued = 0;
     auto issue_next = [&]() {
         if (!cur.live) return;
@@ -759,7 +778,7 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
             tab_cur = tab_nxt;
             seg_k = 0;
             seg_next(nxt, st);
-            tab_nxt = seg_load(nxt, lane, a);
+            tab_nxt = seg_load(nxt, lane, a, rb);
         }
     };
     for (int i = 0; i < S; ++i) issue_next();
@@ -1070,6 +1089,8 @@ static pkv_status launch_merge(pkv_pool *pool, const DecodeArgs &a, int n_warps,
     m.n_q = a.n_q;
     m.batch = a.batch;
     m.W = a.W;
+    m.indptr = a.indptr;
+    m.n_indices = a.n_indices;
     m.skip_blocks = a.skip_blocks;
     m.n_warps = n_warps;
     m.slice_blocks = a.slice_blocks;
@@ -1209,6 +1230,68 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.block_tables = block_tables;
     a.W = max_blocks_per_seq;
+    a.indptr = nullptr;
+    a.n_indices = 0;
+    a.context_lens = context_lens;
+    a.batch = batch;
+    a.qscale = scale * kLog2e;
+    a.scales = pool->scales;
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.ws_ml = nullptr;
+    a.ws_o = nullptr;
+    a.slice_blocks = pool->partition_tokens / kBlockSize;
+    a.err = pool->err;
+    a.k_new = a.v_new = nullptr;
+    a.k_pool = a.v_pool = nullptr;
+    a.skip_blocks = 0;
+    a.n_pre = 0;
+    a.pre_base = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pool->d_head == 128)
+        return fp8 ? dispatch_g<128, true>(pool, a, G, s) : dispatch_g<128, false>(pool, a, G, s);
+    return fp8 ? dispatch_g<64, true>(pool, a, G, s) : dispatch_g<64, false>(pool, a, G, s);
+}
+
+extern "C" pkv_status paged_decode_attention_csr(pkv_pool *pool, const void *q, int32_t n_q,
+                                                 const int32_t *kv_indptr, const int32_t *kv_indices,
+                                                 int64_t n_indices, const int32_t *context_lens, int32_t batch,
+                                                 float scale, void *out, void *stream)
+{
+    if (!pool) return fail(PKV_EINVAL, "paged_decode_attention_csr: NULL pool");
+    if (batch < 0) return fail(PKV_EINVAL, "paged_decode_attention_csr: batch < 0");
+    if (n_q <= 0 || n_q % pool->n_kv)
+        return fail(PKV_EINVAL, "paged_decode_attention_csr: n_q %d is not a positive multiple of n_kv %d", n_q,
+                    pool->n_kv);
+    const int G = n_q / pool->n_kv;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(PKV_EUNSUPPORTED, "paged_decode_attention_csr: n_q / n_kv = %d unsupported (1, 2, 4, 8)", G);
+    if (n_indices < 0) return fail(PKV_EINVAL, "paged_decode_attention_csr: n_indices < 0");
+    if (!isfinite(scale)) return fail(PKV_EINVAL, "paged_decode_attention_csr: scale is not finite");
+    if (batch == 0) return PKV_OK;
+    if (batch > kMaxBatch)
+        return fail(PKV_EUNSUPPORTED, "paged_decode_attention_csr: batch %d > %d", batch, kMaxBatch);
+    if ((int64_t)pool->n_kv * n_indices >= ((int64_t)1 << 30))
+        return fail(PKV_EUNSUPPORTED, "paged_decode_attention_csr: n_kv x n_indices too large");
+    if (!q || !kv_indptr || !context_lens || !out || (n_indices > 0 && !kv_indices))
+        return fail(PKV_EINVAL, "paged_decode_attention_csr: NULL device pointer");
+    if (((uintptr_t)q | (uintptr_t)out) & 15u)
+        return fail(PKV_EINVAL, "paged_decode_attention_csr: q and out must be 16-byte aligned");
+    if (((uintptr_t)kv_indptr | (uintptr_t)kv_indices | (uintptr_t)context_lens) & 3u)
+        return fail(PKV_EINVAL, "paged_decode_attention_csr: indptr, indices and lengths must be 4-byte aligned");
+    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
+    if (fp8 && !pool->scales_set)
+        return fail(PKV_EINVAL, "paged_decode_attention_csr: FP8 pool needs kv_pool_set_fp8_scales first");
+
+    DecodeArgs a;
+    a.num_blocks = pool->num_blocks;
+    a.n_kv = pool->n_kv;
+    a.n_q = n_q;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.block_tables = kv_indices;
+    // W only sizes the grid and the workspace here: batch x W bounds the blocks
+    a.W = (int)std::max<int64_t>(1, (n_indices + batch - 1) / batch);
+    a.indptr = kv_indptr;
+    a.n_indices = n_indices;
     a.context_lens = context_lens;
     a.batch = batch;
     a.qscale = scale * kLog2e;
@@ -1301,6 +1384,8 @@ static pkv_status step_device(pkv_pool *pool, const void *q, const void *k_new, 
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.block_tables = block_tables;
     a.W = max_blocks_per_seq;
+    a.indptr = nullptr;
+    a.n_indices = 0;
     a.context_lens = context_lens;
     a.batch = batch;
     a.qscale = scale * kLog2e;
@@ -1828,6 +1913,8 @@ extern "C" pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.block_tables = block_tables;
     a.W = max_blocks_per_seq;
+    a.indptr = nullptr;
+    a.n_indices = 0;
     a.context_lens = context_lens;
     a.batch = batch;
     a.qscale = scale * kLog2e;
@@ -1974,6 +2061,8 @@ extern "C" pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void 
     a.q = static_cast<const __nv_bfloat16 *>(q);
     a.block_tables = block_tables;
     a.W = max_blocks_per_seq;
+    a.indptr = nullptr;
+    a.n_indices = 0;
     a.context_lens = context_lens;
     a.batch = batch;
     a.qscale = scale * kLog2e;

@@ -196,6 +196,24 @@ pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int32_t n_q,
                                   const int32_t *context_lens, int32_t batch, float scale,
                                   void *out, void *stream);
 
+/* paged_decode_attention with the page table in the CSR form ("Memory
+ * Management in LLM Serving Systems", "Method 3: PagedAttention" and
+ * "Walking the table"): sequence b owns the blocks
+ * kv_indices[kv_indptr[b] .. kv_indptr[b+1]), logical block j of b being
+ * kv_indices[kv_indptr[b] + j].
+ *   kv_indptr     device int32 [batch + 1].  A row with kv_indptr[b] < 0,
+ *                 kv_indptr[b] > kv_indptr[b+1] or kv_indptr[b+1] >
+ *                 n_indices counts as empty and sets PKV_DEVERR_BLOCK_RANGE.
+ *   kv_indices    device int32 [n_indices] (may be NULL when n_indices is 0).
+ *   context_lens  device int32 [batch]; clamped to 16 x the row's length
+ *                 (PKV_DEVERR_CTX_RANGE).
+ * n_kv x n_indices < 2^30.  Other arguments, results and errors as
+ * paged_decode_attention (the same kernels read the table through the
+ * row offsets). */
+pkv_status paged_decode_attention_csr(pkv_pool *pool, const void *q, int32_t n_q, const int32_t *kv_indptr,
+                                      const int32_t *kv_indices, int64_t n_indices, const int32_t *context_lens,
+                                      int32_t batch, float scale, void *out, void *stream);
+
 /* One decode step in one launch: append each sequence's newest token and
  * attend over its whole cache ("The KV Cache from First Principles",
  * "Deriving the cache": compute k_t, v_t, append them, attend with the full
