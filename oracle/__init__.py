@@ -40,6 +40,7 @@ _lib = None
 
 BF16 = 0
 E4M3 = 1
+INT4 = 2
 
 
 def build(force: bool = False) -> str:
@@ -77,6 +78,14 @@ def _load():
         lib.orc_decode.argtypes = [P, P, c.c_int, c.c_int64, c.c_int, c.c_int, c.c_int,
                                    P, c.c_int, c.c_int, P, c.c_int, P, c.c_float, P, P, P, c.c_int]
         lib.orc_decode.restype = c.c_int
+        lib.orc_int4_code.argtypes = [c.c_float, c.c_float, c.c_float]
+        lib.orc_int4_code.restype = c.c_uint8
+        lib.orc_int4_row_params.argtypes = [P, c.c_int, c.POINTER(c.c_float), c.POINTER(c.c_float)]
+        lib.orc_append_int4.argtypes = [P, P, P, c.c_int64, c.c_int, c.c_int, c.c_int, P, P, P, c.c_int64, P, P]
+        lib.orc_append_int4.restype = c.c_int64
+        lib.orc_decode_int4.argtypes = [P, P, P, c.c_int64, c.c_int, c.c_int, c.c_int, P, c.c_int, c.c_int, P,
+                                        c.c_int, P, c.c_float, P, P, P, c.c_int]
+        lib.orc_decode_int4.restype = c.c_int
         lib.orc_hardware_threads.argtypes = []
         lib.orc_hardware_threads.restype = c.c_int
         _lib = lib
@@ -112,6 +121,19 @@ def quantise_e4m3(bf16_bits: int, scale: float) -> int:
     return int(_load().orc_quantise_e4m3(int(bf16_bits) & 0xFFFF, float(scale)))
 
 
+def int4_code(x: float, s: float, z: float) -> int:
+    """clamp(rint((x - z) / s), 0, 15) in fp32 (the 4-bit reading)."""
+    return int(_load().orc_int4_code(float(x), float(s), float(z)))
+
+
+def int4_row_params(row_bits: np.ndarray) -> tuple[float, float]:
+    """A value row's (s, z): z = min, s = (max - min) / 15 (1 if max == min), fp32."""
+    r = np.ascontiguousarray(row_bits, dtype=np.uint16)
+    sc, ze = ctypes.c_float(), ctypes.c_float()
+    _load().orc_int4_row_params(_ptr(r), r.size, ctypes.byref(sc), ctypes.byref(ze))
+    return float(sc.value), float(ze.value)
+
+
 class PoolMirror:
     """Host copy of a K/V block pool in the library's documented layout.
 
@@ -120,15 +142,20 @@ class PoolMirror:
     zero-filled, like a freshly created pool.
     """
 
-    def __init__(self, num_blocks, block_size, n_kv, d_head, dtype=BF16, k_scale=None, v_scale=None):
+    def __init__(self, num_blocks, block_size, n_kv, d_head, dtype=BF16, k_scale=None, v_scale=None,
+                 k_zero=None):
         self.num_blocks, self.block_size, self.n_kv, self.d_head = num_blocks, block_size, n_kv, d_head
         self.dtype = dtype
         el = np.uint16 if dtype == BF16 else np.uint8
-        shape = (num_blocks, n_kv, block_size, d_head)
+        cols = d_head // 2 if dtype == INT4 else d_head  # 4-bit: packed codes, two per byte
+        shape = (num_blocks, n_kv, block_size, cols)
         self.k = np.zeros(shape, dtype=el)
         self.v = np.zeros(shape, dtype=el)
+        # 4-bit pools: per-row value (s, z); k_scale / k_zero are then [n_kv, d_head]
+        self.v_params = np.zeros((num_blocks, n_kv, block_size, 2), dtype=np.float32) if dtype == INT4 else None
         self.k_scale = None if k_scale is None else np.ascontiguousarray(k_scale, dtype=np.float32)
         self.v_scale = None if v_scale is None else np.ascontiguousarray(v_scale, dtype=np.float32)
+        self.k_zero = None if k_zero is None else np.ascontiguousarray(k_zero, dtype=np.float32)
 
     def append(self, k_new_bits: np.ndarray, v_new_bits: np.ndarray, slot_mapping: np.ndarray) -> int:
         """Write tokens into their slots; returns how many slots were past the end."""
@@ -137,6 +164,12 @@ class PoolMirror:
         sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
         T = sm.shape[0]
         assert kb.shape == (T, self.n_kv, self.d_head) and vb.shape == kb.shape
+        if self.dtype == INT4:
+            if self.k_scale is None or self.k_zero is None:
+                raise ValueError("4-bit pool needs per-channel k_scale and k_zero")
+            return int(_load().orc_append_int4(_ptr(self.k), _ptr(self.v), _ptr(self.v_params), self.num_blocks,
+                                               self.block_size, self.n_kv, self.d_head, _ptr(kb), _ptr(vb),
+                                               _ptr(sm), T, _ptr(self.k_scale), _ptr(self.k_zero)))
         if self.dtype == E4M3 and (self.k_scale is None or self.v_scale is None):
             raise ValueError("E4M3 pool needs k_scale and v_scale")
         return int(_load().orc_append(_ptr(self.k), _ptr(self.v), self.dtype, self.num_blocks,
@@ -152,6 +185,14 @@ class PoolMirror:
         B, n_q, D = qb.shape
         assert D == self.d_head and bt.shape[0] == B and cl.shape == (B,)
         out = np.empty((B, n_q, D), dtype=np.float64)
+        if self.dtype == INT4:
+            rc = _load().orc_decode_int4(_ptr(self.k), _ptr(self.v), _ptr(self.v_params), self.num_blocks,
+                                         self.block_size, self.n_kv, self.d_head, _ptr(qb), B, n_q, _ptr(bt),
+                                         bt.shape[1], _ptr(cl), float(np.float32(scale)), _ptr(self.k_scale),
+                                         _ptr(self.k_zero), _ptr(out), int(threads or hardware_threads()))
+            if rc != 0:
+                raise ValueError(f"oracle decode failed with code {rc}")
+            return out
         rc = _load().orc_decode(_ptr(self.k), _ptr(self.v), self.dtype, self.num_blocks,
                                 self.block_size, self.n_kv, self.d_head, _ptr(qb), B, n_q,
                                 _ptr(bt), bt.shape[1], _ptr(cl), float(np.float32(scale)),

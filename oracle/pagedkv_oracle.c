@@ -30,6 +30,15 @@
  *       force over all finite codes (nearest, ties to the even code,
  *       saturating to +-448).  The pages say only "FP8"; E4M3 with a
  *       per-KV-head fp32 scale is the stated reading.
+ *   - 4-bit KV: the pages ask for "per-channel keys" and cite KIVI and
+ *       KVQuant ("KV cache, PagedAttention and FlashAttention", Problem 3,
+ *       "Trade-offs").  Reading: asymmetric 4-bit codes c in [0, 15] with
+ *       x ~ c * s + z; keys use one (s, z) per (KV head, channel), fixed on
+ *       the pool; values use one (s, z) per (token, KV head), from that
+ *       row's min and max (s = (max - min) / 15, or 1 when max == min;
+ *       z = min).  c = clamp(rint((x - z) / s), 0, 15) in fp32 with
+ *       round-half-to-even.  Codes are packed two per byte, the even
+ *       channel in the low nibble.
  *
  * Pool layout mirrored here (the documented contract of the library): K and V
  * are two separate arrays, each [num_blocks][n_kv][block_size][d_head], so
@@ -49,6 +58,7 @@
 
 #define ORC_BF16 0
 #define ORC_E4M3 1
+#define ORC_INT4 2
 
 /* ------------------------------------------------------------------------ */
 /* Sizing: "KV cache, PagedAttention and FlashAttention", Problem 3,          */
@@ -222,6 +232,84 @@ int64_t orc_append(void *k_pool, void *v_pool, int dtype, int64_t num_blocks, in
 /* Decode attention                                                           */
 /* ------------------------------------------------------------------------ */
 
+/* ------------------------------------------------------------------------ */
+/* 4-bit codes (the reading stated in the header).                            */
+/* ------------------------------------------------------------------------ */
+
+/* c = clamp(rint((x - z) / s), 0, 15), every step in fp32. */
+uint8_t orc_int4_code(float x, float s, float z)
+{
+    volatile float t = x - z;
+    volatile float u = t / s;
+    float r = rintf(u); /* round half to even in the default rounding mode */
+    if (!(r >= 0.0f)) r = 0.0f; /* also NaN */
+    if (r > 15.0f) r = 15.0f;
+    return (uint8_t)r;
+}
+
+/* A value row's (s, z): z = min, s = (max - min) / 15 in fp32, 1 if max == min. */
+void orc_int4_row_params(const uint16_t *row_bits, int d, float *s_out, float *z_out)
+{
+    float mn = orc_bf16_to_float(row_bits[0]), mx = mn;
+    for (int c = 1; c < d; ++c) {
+        float x = orc_bf16_to_float(row_bits[c]);
+        if (x < mn) mn = x;
+        if (x > mx) mx = x;
+    }
+    volatile float range = mx - mn;
+    volatile float s = range / 15.0f;
+    if (s == 0.0f) s = 1.0f;
+    *s_out = s;
+    *z_out = mn;
+}
+
+static void orc_put_nibble(uint8_t *row, int c, uint8_t code)
+{
+    uint8_t *b = row + c / 2;
+    if (c & 1) *b = (uint8_t)((*b & 0x0F) | (code << 4));
+    else *b = (uint8_t)((*b & 0xF0) | code);
+}
+
+static uint8_t orc_get_nibble(const uint8_t *row, int c)
+{
+    uint8_t b = row[c / 2];
+    return (c & 1) ? (uint8_t)(b >> 4) : (uint8_t)(b & 0x0F);
+}
+
+/* Append into a 4-bit pool mirror: K and V codes [num_blocks][n_kv][B][d/2]
+ * bytes, value params [num_blocks][n_kv][B][2] fp32 (s, z); key params
+ * k_scale, k_zero [n_kv][d].  Returns the number of slots past the pool. */
+int64_t orc_append_int4(uint8_t *k_codes, uint8_t *v_codes, float *v_params, int64_t num_blocks, int block_size,
+                        int n_kv, int d_head, const uint16_t *k_new, const uint16_t *v_new,
+                        const int64_t *slot_mapping, int64_t n_tokens, const float *k_scale, const float *k_zero)
+{
+    int64_t bad = 0;
+    for (int64_t t = 0; t < n_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= num_blocks * block_size) {
+            ++bad;
+            continue;
+        }
+        int64_t blk = slot / block_size, off = slot % block_size;
+        for (int g = 0; g < n_kv; ++g) {
+            int64_t r = (blk * n_kv + g) * block_size + off;
+            const uint16_t *kx = k_new + (t * n_kv + g) * (int64_t)d_head;
+            const uint16_t *vx = v_new + (t * n_kv + g) * (int64_t)d_head;
+            uint8_t *krow = k_codes + r * (d_head / 2), *vrow = v_codes + r * (d_head / 2);
+            for (int c = 0; c < d_head; ++c)
+                orc_put_nibble(krow, c, orc_int4_code(orc_bf16_to_float(kx[c]), k_scale[g * d_head + c],
+                                                      k_zero[g * d_head + c]));
+            float s, z;
+            orc_int4_row_params(vx, d_head, &s, &z);
+            for (int c = 0; c < d_head; ++c) orc_put_nibble(vrow, c, orc_int4_code(orc_bf16_to_float(vx[c]), s, z));
+            v_params[2 * r] = s;
+            v_params[2 * r + 1] = z;
+        }
+    }
+    return bad;
+}
+
 typedef struct {
     const void *k_pool, *v_pool;
     int dtype;
@@ -234,6 +322,7 @@ typedef struct {
     const int32_t *context_lens;
     double scale;
     const float *k_scale, *v_scale;
+    const float *k_zero, *v_params; /* 4-bit pools: key zero points; value (s, z) per row */
     double *out;
     /* work distribution */
     int64_t next_task;
@@ -285,6 +374,17 @@ static int orc_decode_one(orc_decode_job *job, int b, int g)
         }
         int64_t blk = slot / BS, off = slot % BS;
         int64_t base = ((blk * job->n_kv + g) * BS + off) * (int64_t)D;
+        if (job->dtype == ORC_INT4) { /* x = c * s + z, in fp64 */
+            int64_t r = (blk * job->n_kv + g) * BS + off;
+            const uint8_t *krow = (const uint8_t *)job->k_pool + r * (D / 2);
+            const uint8_t *vrow = (const uint8_t *)job->v_pool + r * (D / 2);
+            double vsc = job->v_params[2 * r], vz = job->v_params[2 * r + 1];
+            for (int d = 0; d < D; ++d) {
+                Kc[p * D + d] = orc_get_nibble(krow, d) * (double)job->k_scale[g * D + d] + job->k_zero[g * D + d];
+                Vc[p * D + d] = orc_get_nibble(vrow, d) * vsc + vz;
+            }
+            continue;
+        }
         for (int d = 0; d < D; ++d) {
             Kc[p * D + d] = orc_load(job->k_pool, job->dtype, base + d, ks);
             Vc[p * D + d] = orc_load(job->v_pool, job->dtype, base + d, vs);
@@ -355,6 +455,37 @@ int orc_decode(const void *k_pool, const void *v_pool, int dtype, int64_t num_bl
     job.block_tables = block_tables; job.max_blocks_per_seq = max_blocks_per_seq;
     job.context_lens = context_lens; job.scale = (double)scale;
     job.k_scale = k_scale; job.v_scale = v_scale; job.out = out;
+    pthread_mutex_init(&job.lock, NULL);
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 256) n_threads = 256;
+    pthread_t tids[256];
+    int started = 0;
+    for (int i = 1; i < n_threads; ++i)
+        if (pthread_create(&tids[started], NULL, orc_decode_worker, &job) == 0) ++started;
+    orc_decode_worker(&job);
+    for (int i = 0; i < started; ++i) pthread_join(tids[i], NULL);
+    pthread_mutex_destroy(&job.lock);
+    return job.status;
+}
+
+/* orc_decode for a 4-bit pool: codes k_codes / v_codes, value params
+ * v_params, key params k_scale / k_zero [n_kv][d_head] (see
+ * orc_append_int4).  Same arguments and results otherwise. */
+int orc_decode_int4(const uint8_t *k_codes, const uint8_t *v_codes, const float *v_params, int64_t num_blocks,
+                    int block_size, int n_kv, int d_head, const uint16_t *q, int batch, int n_q,
+                    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens, float scale,
+                    const float *k_scale, const float *k_zero, double *out, int n_threads)
+{
+    if (n_kv <= 0 || n_q <= 0 || n_q % n_kv != 0 || batch < 0 || d_head <= 0 || d_head % 2 || block_size <= 0)
+        return -3;
+    orc_decode_job job;
+    memset(&job, 0, sizeof job);
+    job.k_pool = k_codes; job.v_pool = v_codes; job.dtype = ORC_INT4;
+    job.num_blocks = num_blocks; job.block_size = block_size; job.n_kv = n_kv; job.d_head = d_head;
+    job.q = q; job.batch = batch; job.n_q = n_q;
+    job.block_tables = block_tables; job.max_blocks_per_seq = max_blocks_per_seq;
+    job.context_lens = context_lens; job.scale = (double)scale;
+    job.k_scale = k_scale; job.k_zero = k_zero; job.v_params = v_params; job.out = out;
     pthread_mutex_init(&job.lock, NULL);
     if (n_threads < 1) n_threads = 1;
     if (n_threads > 256) n_threads = 256;

@@ -485,3 +485,70 @@ def test_partitioned_online_softmax_with_lse_merge_equals_oracle():
             L = sum(math.exp(p[0] - M) * p[1] for p in parts)
             O = sum(math.exp(p[0] - M) * p[2] for p in parts) / L
             np.testing.assert_allclose(O, out[b, h], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# 4-bit KV (the reading of "per-channel keys", KIVI / KVQuant: "KV cache,
+# PagedAttention and FlashAttention", Problem 3, "Trade-offs"): asymmetric
+# codes c = clamp(rint((x - z) / s), 0, 15) in fp32, keys per (head, channel),
+# values per (token, head) from the row's min and max.
+# ---------------------------------------------------------------------------
+
+def test_int4_code_against_numpy_fp32_rint():
+    rng = np.random.default_rng(11)
+    xs = rng.normal(size=3000).astype(np.float32)
+    ss = (np.abs(rng.normal(size=3000)) + 0.01).astype(np.float32)
+    zs = rng.normal(size=3000).astype(np.float32)
+    # exact midpoints (ties must go to the even code) and out-of-range values
+    xs[:40] = (np.arange(40) % 15 + np.float32(0.5)) * np.float32(0.5) + np.float32(-1.0)
+    ss[:40], zs[:40] = 0.5, -1.0
+    xs[40:50], xs[50:60] = -50.0, 50.0
+    for x, s, z in zip(xs, ss, zs):
+        ref = int(np.clip(np.rint(np.float32(np.float32(x - z) / s)), 0, 15))
+        assert oracle.int4_code(x, s, z) == ref, (x, s, z)
+    assert oracle.int4_code(0.75, 0.5, -1.0) == 4  # 3.5 -> 4 (even)
+    assert oracle.int4_code(1.25, 0.5, -1.0) == 4  # 4.5 -> 4 (even)
+
+
+def test_int4_row_params_and_error_bound():
+    rng = np.random.default_rng(12)
+    const = wl.f32_to_bf16_bits(np.full(64, 0.375, np.float32))
+    assert oracle.int4_row_params(const) == (1.0, 0.375)  # max == min: s = 1, every code 0
+    for _ in range(50):
+        row = wl.f32_to_bf16_bits(rng.normal(size=128).astype(np.float32))
+        xf = wl.bf16_bits_to_f32(row)
+        s, z = oracle.int4_row_params(row)
+        assert z == xf.min() and s == np.float32(np.float32(xf.max() - xf.min()) / np.float32(15))
+        codes = [oracle.int4_code(x, s, z) for x in xf]
+        assert min(codes) == 0 and max(codes) == 15
+        err = np.abs(np.array(codes) * np.float64(s) + z - xf)
+        assert err.max() <= s / 2 * (1 + 1e-6)  # round to nearest: half a step at most
+
+
+def test_int4_mirror_layout_and_exact_values():
+    """Values exactly on the code grid round-trip: the 4-bit decode then
+    equals the bf16 decode of the same values, bit for bit, and the packed
+    bytes put the even channel in the low nibble."""
+    rng = np.random.default_rng(13)
+    n_kv, d, NB = 2, 64, 8
+    T = NB * 16  # every slot written (an unwritten 4-bit key reads back as its zero point)
+    ks, kz = np.full((n_kv, d), 0.25, np.float32), np.full((n_kv, d), -2.0, np.float32)
+    m4 = oracle.PoolMirror(NB, 16, n_kv, d, oracle.INT4, k_scale=ks, k_zero=kz)
+    mb = oracle.PoolMirror(NB, 16, n_kv, d)
+    kc = rng.integers(0, 16, size=(T, n_kv, d))
+    vc = rng.integers(0, 16, size=(T, n_kv, d))
+    vc[..., 0], vc[..., 1] = 0, 15  # every value row spans the grid: s = 0.25 exactly
+    kb = wl.f32_to_bf16_bits((kc * 0.25 - 2.0).astype(np.float32))
+    vb = wl.f32_to_bf16_bits((vc * 0.25 - 1.0).astype(np.float32))
+    slots = rng.permutation(NB * 16).astype(np.int64)
+    m4.append(kb, vb, slots)
+    mb.append(kb, vb, slots)
+    blk, off = slots[0] // 16, slots[0] % 16
+    assert m4.k[blk, 1, off, 0] == kc[0, 1, 0] | (kc[0, 1, 1] << 4)
+    assert tuple(m4.v_params[blk, 0, off]) == (0.25, -1.0)
+    table = np.full((2, NB), -1, dtype=np.int32)
+    table[0] = np.arange(NB)
+    table[1, :3] = [5, 0, 2]
+    lens = np.array([NB * 16, 40], dtype=np.int32)
+    q = wl.f32_to_bf16_bits(rng.normal(size=(2, 4, d)).astype(np.float32))
+    assert np.array_equal(m4.decode(q, table, lens, 0.125), mb.decode(q, table, lens, 0.125))
