@@ -112,8 +112,7 @@ def algorithmic_bytes(w) -> dict:
     and out."""
     import numpy as np
 
-    e = w.elem_bytes
-    per_token = 2 * w.n_kv * w.d_head * e
+    per_token = w.n_kv * w.kv_bytes_per_token_head  # K and V (4-bit: codes plus the value rows' scale and zero)
     logical_tokens = int(w.context_lens.astype(np.int64).sum())
     slots = set()
     if w.shared_prefix_tokens:
@@ -255,8 +254,8 @@ def gpu_id_for(device_index: int) -> str:
 def oracle_setup(w):
     import oracle
 
-    dt = oracle.BF16 if w.dtype == "bf16" else oracle.E4M3
-    m = oracle.PoolMirror(w.num_blocks, w.block_size, w.n_kv, w.d_head, dt, w.k_scale, w.v_scale)
+    dt = {"bf16": oracle.BF16, "fp8": oracle.E4M3, "int4": oracle.INT4}[w.dtype]
+    m = oracle.PoolMirror(w.num_blocks, w.block_size, w.n_kv, w.d_head, dt, w.k_scale, w.v_scale, w.k_zero)
     m.append(w.fill_k, w.fill_v, w.fill_slots)
     return m
 
@@ -360,10 +359,12 @@ def run_ours(args):
     step_bytes = acct["unique"] if use_unique else acct["logical"]
 
     dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(device).view(dt)  # noqa: E731
-    dt = pkv.BF16 if w.dtype == "bf16" else pkv.FP8_E4M3
+    dt = {"bf16": pkv.BF16, "fp8": pkv.FP8_E4M3, "int4": pkv.INT4}[w.dtype]
     pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head, dt)
     if w.dtype == "fp8":
         pool.set_fp8_scales(w.k_scale, w.v_scale)
+    if w.dtype == "int4":
+        pool.set_int4_key_params(w.k_scale, w.k_zero)
     if args.partition_tokens:
         pool.set_partition_tokens(args.partition_tokens)
     pool.reserve_workspace(w.batch, w.n_q, w.max_blocks_per_seq)
@@ -383,8 +384,12 @@ def run_ours(args):
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device) if args.flush_l2 else None
 
     def step():
-        # one pass of the hot path: append every sequence's new token, decode (one launch)
-        pkv.paged_decode_step(pool, q, k_new, v_new, tables, lens, float(w.scale), out, stream)
+        # one pass of the hot path: append every sequence's new token, decode
+        if w.dtype == "int4":  # no fused step for 4-bit pools: append, then decode
+            pkv.paged_kv_append(pool, k_new, v_new, slots, stream)
+            pkv.paged_decode_attention(pool, q, tables, lens, float(w.scale), out, stream)
+        else:
+            pkv.paged_decode_step(pool, q, k_new, v_new, tables, lens, float(w.scale), out, stream)
 
     def step_two_calls():
         pkv.paged_kv_append(pool, k_new, v_new, slots, stream)

@@ -19,6 +19,7 @@ from . import _build
 
 BF16 = 0
 FP8_E4M3 = 1
+INT4 = 2
 
 STATUS = {0: "PKV_OK", 1: "PKV_EINVAL", 2: "PKV_ERANGE", 3: "PKV_ENOMEM", 4: "PKV_ECUDA",
           5: "PKV_EUNSUPPORTED", 6: "PKV_EDEVICE"}
@@ -43,7 +44,8 @@ class _Layout(ctypes.Structure):
                 ("stride_head", ctypes.c_int64), ("stride_token", ctypes.c_int64),
                 ("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
                 ("n_kv", ctypes.c_int32), ("d_head", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("bytes_per_array", ctypes.c_int64)]
+                ("bytes_per_array", ctypes.c_int64), ("v_params", ctypes.c_void_p),
+                ("v_params_bytes", ctypes.c_int64)]
 
 
 class _Timing(ctypes.Structure):
@@ -79,6 +81,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                        c.POINTER(P)]
         lib.kv_pool_destroy.argtypes = [P]
         lib.kv_pool_set_fp8_scales.argtypes = [P, P, P]
+        lib.kv_pool_set_int4_key_params.argtypes = [P, P, P]
         lib.kv_pool_layout.argtypes = [P, c.POINTER(_Layout)]
         lib.kv_pool_set_partition_tokens.argtypes = [P, c.c_int32]
         lib.kv_pool_reserve_workspace.argtypes = [P, c.c_int32, c.c_int32, c.c_int32]
@@ -118,7 +121,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pkv_status_string.restype = c.c_char_p
         lib.pkv_last_error_message.argtypes = []
         lib.pkv_last_error_message.restype = c.c_char_p
-        for name in ("kv_pool_create", "kv_pool_destroy", "kv_pool_set_fp8_scales", "kv_pool_layout",
+        for name in ("kv_pool_create", "kv_pool_destroy", "kv_pool_set_fp8_scales", "kv_pool_set_int4_key_params",
+                     "kv_pool_layout",
                      "kv_pool_set_partition_tokens", "kv_pool_reserve_workspace", "paged_kv_append",
                      "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
                      "paged_decode_attention_csr",
@@ -214,6 +218,30 @@ class Pool:
         _check(load().kv_pool_set_fp8_scales(self.handle, ks.ctypes.data_as(ctypes.c_void_p),
                                              vs.ctypes.data_as(ctypes.c_void_p)))
 
+    def set_int4_key_params(self, k_scale, k_zero):
+        """4-bit pools: per-(KV head, channel) key scale and zero point, [n_kv, d_head] fp32 each."""
+        import numpy as np
+
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        kz = np.ascontiguousarray(k_zero, dtype=np.float32)
+        if ks.shape != (self.n_kv, self.d_head) or kz.shape != (self.n_kv, self.d_head):
+            raise ValueError(f"key parameters must have shape ({self.n_kv}, {self.d_head})")
+        _check(load().kv_pool_set_int4_key_params(self.handle, ks.ctypes.data_as(ctypes.c_void_p),
+                                                  kz.ctypes.data_as(ctypes.c_void_p)))
+
+    def v_params_view(self):
+        """4-bit pools: the value rows' (scale, zero point), float32 [num_blocks, n_kv, block_size, 2]."""
+        import torch
+
+        lay = self.layout()
+        ptr, n = lay["v_params"], lay["v_params_bytes"]
+
+        class _Holder:
+            __cuda_array_interface__ = {"shape": (n // 4,), "typestr": "<f4", "data": (ptr, False),
+                                        "version": 3, "strides": None}
+
+        return torch.as_tensor(_Holder(), device="cuda").view(self.num_blocks, self.n_kv, self.block_size, 2)
+
     def layout(self) -> dict:
         lay = _Layout()
         _check(load().kv_pool_layout(self.handle, ctypes.byref(lay)))
@@ -254,7 +282,6 @@ class Pool:
         import torch
 
         lay = self.layout()
-        elem = 2 if self.dtype == BF16 else 1
         n = lay["bytes_per_array"]
         ptr = lay[which]
 
@@ -263,7 +290,7 @@ class Pool:
                                         "version": 3, "strides": None}
 
         flat = torch.as_tensor(_Holder(), device="cuda")
-        return flat.view(self.num_blocks, self.n_kv, self.block_size, self.d_head * elem)
+        return flat.view(self.num_blocks, self.n_kv, self.block_size, n // (self.num_blocks * self.n_kv * self.block_size))
 
 
 def kv_pool_create(num_blocks: int, block_size: int, n_kv: int, d_head: int, dtype: int = BF16) -> Pool:
@@ -533,7 +560,7 @@ class BlockAllocator:
         return a, src[:k.value].copy(), dst[:k.value].copy()
 
 
-__all__ = ["BF16", "FP8_E4M3", "Pool", "PagedKVError", "kv_pool_create", "paged_kv_append",
+__all__ = ["BF16", "FP8_E4M3", "INT4", "Pool", "PagedKVError", "kv_pool_create", "paged_kv_append",
            "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
            "paged_decode_step_host", "paged_decode_attention_prefix", "paged_decode_attention_csr",
            "kv_bytes_per_token", "kv_block_bytes",

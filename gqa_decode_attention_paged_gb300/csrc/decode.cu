@@ -68,6 +68,8 @@ struct DecodeArgs {
     int batch;
     float qscale;          // scale * log2(e)
     const float *scales;   // FP8: [2 * n_kv] (k then v)
+    const float *k_params; // 4-bit: [2][n_kv][D] key scales, then zero points
+    const float *v_params; // 4-bit: [num_blocks][n_kv][16][2] value (scale, zero point)
     __nv_bfloat16 *out;
     float2 *ws_ml;         // workspace [slots][G] (max in log2 units, sum)
     float *ws_o;           // workspace [slots][G][D], unnormalised
@@ -84,13 +86,18 @@ struct DecodeArgs {
     int64_t pre_base;
 };
 
+// KV storage types the decode kernel is instantiated for (pkv_dtype values)
+constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvInt4 = 2;
+
 // Shared-memory geometry of one (block, KV head) tile as the TMA boxes lay it
-// out: NREG boxes of 16 rows x BOXB bytes (128-byte rows, or 64 bytes for
-// FP8 with d_head 64), each box swizzled within its own region.
-template <int D, bool FP8>
+// out: NREG boxes of 16 rows x BOXB bytes (128-byte rows; 64 bytes for FP8
+// with d_head 64 and 4-bit codes with d_head 128; 32 bytes for 4-bit codes
+// with d_head 64), each box swizzled within its own region.
+template <int D, int KV>
 struct Geo {
-    static constexpr int E = FP8 ? 1 : 2;
-    static constexpr int ROWB = D * E;                    // bytes of one token row
+    static constexpr bool FP8 = KV == kKvFp8, I4 = KV == kKvInt4;
+    static constexpr int E = FP8 || I4 ? 1 : 2;           // bytes per stored element (a byte of two codes)
+    static constexpr int ROWB = I4 ? D / 2 : D * E;       // bytes of one token row
     static constexpr int BOXB = ROWB > 128 ? 128 : ROWB;  // bytes of one box row
     static constexpr int NREG = ROWB / BOXB;              // boxes per tile
     static constexpr int RGN = kBlockSize * BOXB;         // bytes per box
@@ -103,7 +110,7 @@ struct Geo {
 // More warps hide the per-block dependency chain; each warp keeps at least
 // two stages so that one copy is in flight while it computes.  (Build-time
 // overrides PKV_DECODE_WARPS / PKV_RING_KIB exist for tuning sweeps.)
-template <int D, int G, bool FP8>
+template <int D, int G, int KV>
 struct Tune {
 #if defined(PKV_DECODE_WARPS) && defined(PKV_RING_KIB)
     static constexpr int NW = PKV_DECODE_WARPS;
@@ -117,22 +124,24 @@ struct Tune {
 #endif
 };
 
-template <int D, int G, bool FP8>
+template <int D, int G, int KV>
 struct Cfg {
-    using Gm = Geo<D, FP8>;
-    static constexpr int NW = Tune<D, G, FP8>::NW;
+    using Gm = Geo<D, KV>;
+    static constexpr int NW = Tune<D, G, KV>::NW;
     static constexpr int kThreads = NW * 32;
     // resident CTAs per SM the register budget is held to: 12 warps per SM,
     // i.e. 3 x 128 threads of at most 168 registers for 4-warp CTAs (the
     // shared-memory ring allows no more for bf16 d128)
     static constexpr int kMinBlocks = 12 / NW > 0 ? 12 / NW : 1;
-    static constexpr int kStages = std::min(8, std::max(2, Tune<D, G, FP8>::RING_KIB * 1024 / (NW * Gm::STAGE)));
+    static constexpr int kStages = std::min(8, std::max(2, Tune<D, G, KV>::RING_KIB * 1024 / (NW * Gm::STAGE)));
     // shared-memory layout (bytes from a 1024-byte aligned base)
     static constexpr int kRing = NW * kStages * Gm::STAGE;
     static constexpr int kBars = kRing;
     static constexpr int kPhys = kBars + NW * kStages * 8;
-    static constexpr int kNewRow = (kPhys + NW * kStages * 4 + 15) / 16 * 16;  // [NW][2 * D * 2] bytes: fused
-                                                                                // step's new K, V rows
+    // 4-bit KV: each stage's value (scale, zero point) pairs, [NW][kStages][16] float2
+    static constexpr int kVp = (kPhys + NW * kStages * 4 + 15) / 16 * 16;
+    static constexpr int kNewRow = kVp + (Gm::I4 ? NW * kStages * kBlockSize * 8 : 0);  // [NW][2 * D * 2] bytes:
+                                                                                          // fused step's new rows
     static constexpr int kWarpTot = kNewRow + NW * 4 * D;
     // ps[batch + 1], then clamped lengths cl[batch], then table row starts rb[batch]
     static constexpr int kPs = kWarpTot + 4 * NW;
@@ -385,7 +394,39 @@ template <int BOXB>
 __device__ __forceinline__ uint32_t swz(uint32_t off)
 {
     if constexpr (BOXB == 128) return off ^ ((off >> 3) & 0x70u);
-    else return off ^ ((off >> 3) & 0x30u);
+    else if constexpr (BOXB == 64) return off ^ ((off >> 3) & 0x30u);
+    else return off ^ ((off >> 3) & 0x10u);
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// 4-bit codes j and j+4 of a packed 32-bit word (nibble k holds code k) as
+// an exact f16 pair: each code, or-ed into the mantissa of 1024.0, minus 1024.
+__device__ __forceinline__ uint32_t i4_pair(uint32_t w, int j)
+{
+    const uint32_t t = ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
+    uint32_t r;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64006400u));
+    return r;
+}
+
+// The same code (nibble m of a row's packed words) of two token rows, as an
+// exact f16 pair (row a low, row b high).
+template <int m>
+__device__ __forceinline__ uint32_t i4_cross(const uint32_t *ra, const uint32_t *rb)
+{
+    constexpr uint32_t bi = (m % 8) / 2;  // byte within the word
+    constexpr uint32_t sel = bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12);
+    const uint32_t z = prmt(ra[m / 8], rb[m / 8], sel);
+    const uint32_t t = ((z >> (4 * (m & 1))) & 0x000F000Fu) | 0x64006400u;
+    uint32_t r;
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64006400u));
+    return r;
 }
 
 // q rows of one (sequence, KV head) group as m16n8k16 B fragments: thread
@@ -393,15 +434,29 @@ __device__ __forceinline__ uint32_t swz(uint32_t off)
 // heads g8 >= G).  bf16 KV: k-step ks covers d 16ks + {2c, 2c+1} and
 // 16ks + 8 + {2c, 2c+1}.  FP8 KV (f16 MMA): k-step 2kk+j covers
 // d 32kk + 8c + 4j + {0,1} and {2,3}, the order the E4M3 K fragments use.
-template <int D, int G, bool FP8>
+// 4-bit KV (f16 MMA): q' = q * k_scale[g] per channel (the keys' per-channel
+// scale folded into q; their zero points add the same constant to every
+// score of a head and cancel in the softmax); k-step ks of thread c4 covers
+// the channels of its packed key word w = ks / 2, base = c4 * D / 4 + 8w:
+// pairs (base + s, base + s + 4) and (base + s + 1, base + s + 5) with
+// s = 2 * (ks & 1), the order i4_pair extracts codes in.
+template <int D, int G, int KV>
 __device__ __forceinline__ void load_q_frags(const DecodeArgs &a, int b, int g, int g8, int c4,
                                              uint32_t (&qf)[D / 16][2])
 {
+    constexpr bool FP8 = KV == kKvFp8, I4 = KV == kKvInt4;
     const bool live = g8 < G;
     const __nv_bfloat16 *qrow = a.q + ((int64_t)b * a.n_q + g * G + (live ? g8 : 0)) * D;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-        if constexpr (!FP8) {
+        if constexpr (I4) {
+            const int base = c4 * (D / 4) + 8 * (ks >> 1), s0 = 2 * (ks & 1);
+            const float *sk = a.k_params + (int64_t)g * D + base + s0;
+            const __nv_bfloat16 *qq = qrow + base + s0;
+            auto qv = [&](int k) { return live ? __bfloat162float(qq[k]) * sk[k] : 0.0f; };
+            qf[ks][0] = pack2<true>(qv(0), qv(4));
+            qf[ks][1] = pack2<true>(qv(1), qv(5));
+        } else if constexpr (!FP8) {
             qf[ks][0] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c4) : 0u;
             qf[ks][1] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * c4) : 0u;
         } else {
@@ -623,9 +678,10 @@ __device__ __forceinline__ void fetch_new_row(const DecodeArgs &a, int b, int g,
 // ... and its bytes as the pool stores them: the bf16 copy, or for an E4M3
 // pool E4M3(fp32(x) / scale) rounded to nearest even and saturated, from
 // __fdiv_rn and a satfinite convert, exactly what paged_kv_append writes.
-template <int D, bool FP8>
+template <int D, int KV>
 __device__ __forceinline__ uint4 prepared_new_row(const DecodeArgs &a, int g, int lane, const uint8_t *rowbuf)
 {
+    constexpr bool FP8 = KV == kKvFp8;
     constexpr int NCH = D / 8;
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
@@ -652,11 +708,12 @@ __device__ __forceinline__ uint4 prepared_new_row(const DecodeArgs &a, int g, in
 // Fused step, part 2 (when the block has landed): write the prepared row into
 // the pool -- the append -- and into row r of the block's staged tiles, which
 // the TMA filled before the append.
-template <int D, bool FP8>
+template <int D, int KV>
 __device__ __forceinline__ void append_row(const DecodeArgs &a, int g, int phys, int r, int lane, uint4 prepared,
                                            uint8_t *stage)
 {
-    using Gm = Geo<D, FP8>;
+    using Gm = Geo<D, KV>;
+    constexpr bool FP8 = KV == kKvFp8;
     constexpr int NCH = D / 8;  // 8-element chunks per row
     if (lane >= 2 * NCH) return;
     const bool isv = lane >= NCH;
@@ -688,12 +745,14 @@ __device__ __forceinline__ void append_row(const DecodeArgs &a, int g, int phys,
 // pairs in registers; the MMA's k (and, for V, its m) order is a fixed
 // permutation of d applied identically to both operands and undone when the
 // output is written, so the products are unchanged.
-template <int D, int G, bool FP8, bool APPEND = false>
-__global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMinBlocks)
+template <int D, int G, int KV, bool APPEND = false>
+__global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBlocks)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, DecodeArgs a)
 {
-    using C = Cfg<D, G, FP8>;
+    using C = Cfg<D, G, KV>;
     using Gm = typename C::Gm;
+    constexpr bool FP8 = KV == kKvFp8, I4 = KV == kKvInt4;
+    static_assert(!(I4 && APPEND), "the fused step is not built for 4-bit pools");
     constexpr int S = C::kStages;
     constexpr int NW = C::NW;
     constexpr int NT = D / 16;  // 16-wide MMA tiles along d
@@ -708,6 +767,7 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
     int *warp_tot = reinterpret_cast<int *>(smem + C::kWarpTot);
     int32_t *ps = reinterpret_cast<int32_t *>(smem + C::kPs);
     uint8_t *rowbuf = smem + C::kNewRow + warp * 4 * D;  // fused step: this warp's new K and V rows
+    float2 *vpbuf = reinterpret_cast<float2 *>(smem + C::kVp) + warp * S * kBlockSize;  // 4-bit: value (s, z)
 
     if (tid == 0) {
         prefetch_tensormap(&tm_k);
@@ -761,12 +821,15 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
                 const int y = (int)(((int64_t)phys * a.n_kv + cur.p.g) * kBlockSize);
                 uint8_t *dst = ring + sidx * Gm::STAGE;
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(&bars[sidx], Gm::STAGE);
+                mbar_arrive_expect_tx(&bars[sidx], Gm::STAGE + (I4 ? kBlockSize * 8 : 0));
 #pragma unroll
                 for (int r = 0; r < Gm::NREG; ++r) {
                     tma_load_2d(dst + r * Gm::RGN, &tm_k, r * Gm::BOX_ELEMS, y, &bars[sidx], policy);
                     tma_load_2d(dst + Gm::TILE + r * Gm::RGN, &tm_v, r * Gm::BOX_ELEMS, y, &bars[sidx], policy);
                 }
+                if constexpr (I4)  // the block's value (scale, zero point) pairs: 128 contiguous bytes
+                    bulk_g2s(vpbuf + sidx * kBlockSize, a.v_params + (int64_t)y * 2, kBlockSize * 8, &bars[sidx],
+                             policy);
             } else {
                 atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
                 mbar_arrive(&bars[sidx]);
@@ -790,7 +853,7 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
     Piece pc;
     bool have = first_piece(st, me, pc);
     uint32_t qn[NT][2];
-    if (have) load_q_frags<D, G, FP8>(a, pc.b, pc.g, g8, c4, qn);
+    if (have) load_q_frags<D, G, KV>(a, pc.b, pc.g, g8, c4, qn);
     int consumed = 0;
     while (have) {
         Piece nx = pc;
@@ -803,7 +866,7 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
             qf[ks][0] = qn[ks][0];
             qf[ks][1] = qn[ks][1];
         }
-        if (have_nx) load_q_frags<D, G, FP8>(a, nx.b, nx.g, g8, c4, qn);
+        if (have_nx) load_q_frags<D, G, KV>(a, nx.b, nx.g, g8, c4, qn);
         const float qs = a.qscale * (FP8 ? a.scales[pc.g] : 1.0f);
         const int C_len = cl[pc.b];
         // Fused step: the warp owning the block of position C_len-1 appends the
@@ -816,6 +879,7 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
 #pragma unroll
         for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // heads 2c, 2c+1
+        float z0 = 0.0f, z1 = 0.0f;  // 4-bit: sum of p * (value zero point), heads 2c, 2c+1
 
         // One block: wait for its stage, (fused step, last block only) patch in
         // the new token, then scores, softmax and P.V.  The patching variant is
@@ -836,13 +900,35 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
                 const uint32_t vb = kb + Gm::TILE;
                 const int nv = min(kBlockSize, C_len - (a.skip_blocks + j) * kBlockSize);
                 if constexpr (decltype(patch)::value) {
-                    append_row<D, FP8>(a, pc.g, phys_st[sidx], nv - 1, lane,
-                                       prepared_new_row<D, FP8>(a, pc.g, lane, rowbuf), ring + sidx * Gm::STAGE);
+                    append_row<D, KV>(a, pc.g, phys_st[sidx], nv - 1, lane,
+                                       prepared_new_row<D, KV>(a, pc.g, lane, rowbuf), ring + sidx * Gm::STAGE);
                     __syncwarp();
                 }
                 // ---- S^T = K . Q^T ----
                 float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-                if constexpr (!FP8) {
+                if constexpr (I4) {
+                    // this thread's packed key words: channels c4*D/4 .. +D/4 of tokens g8, g8+8
+                    constexpr int WPT = D / 32;
+                    uint32_t kx[WPT], ky[WPT];
+                    if constexpr (WPT == 4) {
+                        const uint4 x = lds128(kb + swz<Gm::BOXB>(g8 * Gm::ROWB + 16 * c4));
+                        const uint4 y = lds128(kb + swz<Gm::BOXB>((g8 + 8) * Gm::ROWB + 16 * c4));
+                        kx[0] = x.x; kx[1] = x.y; kx[2] = x.z; kx[3] = x.w;
+                        ky[0] = y.x; ky[1] = y.y; ky[2] = y.z; ky[3] = y.w;
+                    } else {
+                        const uint2 x = lds64(kb + swz<Gm::BOXB>(g8 * Gm::ROWB + 8 * c4));
+                        const uint2 y = lds64(kb + swz<Gm::BOXB>((g8 + 8) * Gm::ROWB + 8 * c4));
+                        kx[0] = x.x; kx[1] = x.y;
+                        ky[0] = y.x; ky[1] = y.y;
+                    }
+#pragma unroll
+                    for (int ks = 0; ks < NT; ++ks) {
+                        const int w = ks >> 1, s0 = 2 * (ks & 1);
+                        const uint32_t fa[4] = {i4_pair(kx[w], s0), i4_pair(ky[w], s0), i4_pair(kx[w], s0 + 1),
+                                                i4_pair(ky[w], s0 + 1)};
+                        mma16816<true>((ks & 1) ? sb : sa, fa, qf[ks][0], qf[ks][1]);
+                    }
+                } else if constexpr (!FP8) {
 #pragma unroll
                     for (int ks = 0; ks < NT; ++ks) {
                         const int chunk = 2 * ks + half_k;
@@ -895,13 +981,57 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
                         o[t][3] *= al1;
                     }
                 }
-                const uint32_t pb0 = movm_t(pack2<FP8>(p0, p1));  // P^T rows: tokens 2c,2c+1 of head g
-                const uint32_t pb1 = movm_t(pack2<FP8>(p2, p3));  // tokens 2c+8, 2c+9
+                uint32_t pb0, pb1;  // P^T rows: tokens 2c, 2c+1 (pb0), 2c+8, 2c+9 (pb1) of head g
+                if constexpr (I4) {
+                    // v = c * s + z per token: P V = (P * s) C + (P . z); masked tokens weigh 0
+                    const float2 vp0 = g8 < nv ? vpbuf[sidx * kBlockSize + g8] : make_float2(0.f, 0.f);
+                    const float2 vp1 = g8 + 8 < nv ? vpbuf[sidx * kBlockSize + g8 + 8] : make_float2(0.f, 0.f);
+                    z0 = fmaf(z0, al0, fmaf(p0, vp0.y, p2 * vp1.y));
+                    z1 = fmaf(z1, al1, fmaf(p1, vp0.y, p3 * vp1.y));
+                    pb0 = movm_t(pack2<true>(p0 * vp0.x, p1 * vp0.x));
+                    pb1 = movm_t(pack2<true>(p2 * vp1.x, p3 * vp1.x));
+                } else {
+                    pb0 = movm_t(pack2<FP8>(p0, p1));
+                    pb1 = movm_t(pack2<FP8>(p2, p3));
+                }
                 // masked tokens' V must not reach the MMA (0 * non-finite garbage)
                 const uint32_t mk01 = (2 * c4 < nv ? 0x0000ffffu : 0u) | (2 * c4 + 1 < nv ? 0xffff0000u : 0u);
                 const uint32_t mk23 = (2 * c4 + 8 < nv ? 0x0000ffffu : 0u) | (2 * c4 + 9 < nv ? 0xffff0000u : 0u);
                 // ---- O^T += V^T . P^T ----
-                if constexpr (!FP8) {
+                if constexpr (I4) {
+                    // channels g8*D/8 .. +D/8 of tokens 2c, 2c+1, 2c+8, 2c+9: tile t row g8 is the span's
+                    // channel t, row g8+8 its channel NT + t (codes are finite: no masking needed)
+                    constexpr int WPR = D / 64;  // words per token row per thread (2 or 1)
+                    uint32_t r0[WPR], r1[WPR], r2[WPR], r3[WPR];
+                    const int rows[4] = {2 * c4, 2 * c4 + 1, 2 * c4 + 8, 2 * c4 + 9};
+                    uint32_t *rr[4] = {r0, r1, r2, r3};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if constexpr (WPR == 2) {
+                            const uint2 v = lds64(vb + swz<Gm::BOXB>(rows[q] * Gm::ROWB + 8 * g8));
+                            rr[q][0] = v.x;
+                            rr[q][1] = v.y;
+                        } else {
+                            rr[q][0] = lds32(vb + swz<Gm::BOXB>(rows[q] * Gm::ROWB + 4 * g8));
+                        }
+                    }
+                    auto tile = [&](auto tc) {
+                        constexpr int t = decltype(tc)::value;
+                        const uint32_t fa[4] = {i4_cross<t>(r0, r1), i4_cross<NT + t>(r0, r1), i4_cross<t>(r2, r3),
+                                                i4_cross<NT + t>(r2, r3)};
+                        mma16816<true>(o[t], fa, pb0, pb1);
+                    };
+                    tile(std::integral_constant<int, 0>{});
+                    tile(std::integral_constant<int, 1>{});
+                    tile(std::integral_constant<int, 2>{});
+                    tile(std::integral_constant<int, 3>{});
+                    if constexpr (NT == 8) {
+                        tile(std::integral_constant<int, 4>{});
+                        tile(std::integral_constant<int, 5>{});
+                        tile(std::integral_constant<int, 6>{});
+                        tile(std::integral_constant<int, 7>{});
+                    }
+                } else if constexpr (!FP8) {
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
                         const int chunk = 2 * t + half_v;
@@ -954,6 +1084,24 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
             l0 += __shfl_xor_sync(kFull, l0, off);
             l1 += __shfl_xor_sync(kFull, l1, off);
         }
+        if constexpr (I4) {  // the values' zero points: sum_p p_p z_p, the same for every channel
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                z0 += __shfl_xor_sync(kFull, z0, off);
+                z1 += __shfl_xor_sync(kFull, z1, off);
+            }
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                o[t][0] += z0;
+                o[t][1] += z1;
+                o[t][2] += z0;
+                o[t][3] += z1;
+            }
+        }
+        // channel of accumulator row g8 + 8i of tile t, per KV type
+        auto chan = [&](int t, int i) {
+            return I4 ? g8 * (D / 8) + NT * i + t : FP8 ? 32 * (t >> 1) + 4 * g8 + 2 * (t & 1) + i : 16 * t + g8 + 8 * i;
+        };
         const float vs = FP8 ? a.scales[a.n_kv + pc.g] : 1.0f;
         const bool h0 = 2 * c4 < G, h1 = 2 * c4 + 1 < G;  // this thread's heads exist
         if (pc.j0 == 0 && pc.j1 == pc.nblk && a.n_pre == 0) {
@@ -964,7 +1112,7 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
             for (int t = 0; t < NT; ++t) {
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                    const int d = FP8 ? 32 * (t >> 1) + 4 * g8 + 2 * (t & 1) + i : 16 * t + g8 + 8 * i;
+                    const int d = chan(t, i);
                     if (h0) ob[(2 * c4) * D + d] = __float2bfloat16_rn(o[t][2 * i] * r0);
                     if (h1) ob[(2 * c4 + 1) * D + d] = __float2bfloat16_rn(o[t][2 * i + 1] * r1);
                 }
@@ -978,7 +1126,7 @@ __global__ void __launch_bounds__(Cfg<D, G, FP8>::kThreads, Cfg<D, G, FP8>::kMin
             for (int t = 0; t < NT; ++t) {
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
-                    const int d = FP8 ? 32 * (t >> 1) + 4 * g8 + 2 * (t & 1) + i : 16 * t + g8 + 8 * i;
+                    const int d = chan(t, i);
                     if (h0) wo[(2 * c4) * D + d] = o[t][2 * i] * vs;
                     if (h1) wo[(2 * c4 + 1) * D + d] = o[t][2 * i + 1] * vs;
                 }
@@ -1033,12 +1181,12 @@ static int64_t max_slots(pkv_pool *pool, int batch, int n_kv, int max_blocks_per
 }
 
 // Persistent grid of the decode kernel for (d_head, G, dtype) at `batch`.
-template <int D, int G, bool FP8, bool APPEND = false>
+template <int D, int G, int KV, bool APPEND = false>
 static pkv_status decode_grid(pkv_pool *pool, int batch, int max_blocks_per_seq, int *grid, size_t *smem,
                               int reserve_ctas_per_sm = 0)
 {
-    using C = Cfg<D, G, FP8>;
-    auto kern = decode_kernel<D, G, FP8, APPEND>;
+    using C = Cfg<D, G, KV>;
+    auto kern = decode_kernel<D, G, KV, APPEND>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -1114,59 +1262,74 @@ static pkv_status launch_merge(pkv_pool *pool, const DecodeArgs &a, int n_warps,
     return PKV_OK;
 }
 
-template <int D, int G, bool FP8>
+template <int D, int G, int KV>
 static pkv_status launch_decode(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
 {
-    using C = Cfg<D, G, FP8>;
+    using C = Cfg<D, G, KV>;
     int grid = 0;
     size_t smem = 0;
-    pkv_status st = decode_grid<D, G, FP8>(pool, a.batch, a.W, &grid, &smem);
+    pkv_status st = decode_grid<D, G, KV>(pool, a.batch, a.W, &grid, &smem);
     if (st != PKV_OK) return st;
     const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
     st = ensure_workspace(pool, L.total);
     if (st != PKV_OK) return st;
     bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
     LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl(decode_kernel<D, G, FP8>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
+    cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
                                pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return launch_merge<D, G>(pool, a, grid * C::NW, s);
 }
 
-template <int D, bool FP8>
+template <int D, int KV>
+static pkv_status dispatch_g(pkv_pool *pool, const DecodeArgs &a, int G, cudaStream_t s);
+
+// The decode launch for the pool's KV type and head size.
+static pkv_status dispatch_kv(pkv_pool *pool, const DecodeArgs &a, int G, cudaStream_t s)
+{
+    const bool d128 = pool->d_head == 128;
+    if (pool->dtype == PKV_INT4)
+        return d128 ? dispatch_g<128, kKvInt4>(pool, a, G, s) : dispatch_g<64, kKvInt4>(pool, a, G, s);
+    if (pool->dtype == PKV_FP8_E4M3)
+        return d128 ? dispatch_g<128, kKvFp8>(pool, a, G, s) : dispatch_g<64, kKvFp8>(pool, a, G, s);
+    return d128 ? dispatch_g<128, kKvBf16>(pool, a, G, s) : dispatch_g<64, kKvBf16>(pool, a, G, s);
+}
+
+template <int D, int KV>
 static pkv_status dispatch_g(pkv_pool *pool, const DecodeArgs &a, int G, cudaStream_t s)
 {
     switch (G) {
-    case 1: return launch_decode<D, 1, FP8>(pool, a, s);
-    case 2: return launch_decode<D, 2, FP8>(pool, a, s);
-    case 4: return launch_decode<D, 4, FP8>(pool, a, s);
-    case 8: return launch_decode<D, 8, FP8>(pool, a, s);
+    case 1: return launch_decode<D, 1, KV>(pool, a, s);
+    case 2: return launch_decode<D, 2, KV>(pool, a, s);
+    case 4: return launch_decode<D, 4, KV>(pool, a, s);
+    case 8: return launch_decode<D, 8, KV>(pool, a, s);
     }
     return fail(PKV_EUNSUPPORTED, "decode: group size %d unsupported (1, 2, 4 or 8)", G);
 }
 
 // Total warps of the decode grid (the larger of the plain and fused-step
 // kernels, which may differ in occupancy).
-template <int D, int G, bool FP8>
+template <int D, int G, int KV>
 static pkv_status grid_warps(pkv_pool *pool, int batch, int max_blocks_per_seq, int *warps)
 {
     size_t smem = 0;
     int g0 = 0, g1 = 0;
-    pkv_status st = decode_grid<D, G, FP8>(pool, batch, max_blocks_per_seq, &g0, &smem);
-    if (st == PKV_OK) st = decode_grid<D, G, FP8, true>(pool, batch, max_blocks_per_seq, &g1, &smem);
-    *warps = std::max(g0, g1) * Cfg<D, G, FP8>::NW;
+    pkv_status st = decode_grid<D, G, KV>(pool, batch, max_blocks_per_seq, &g0, &smem);
+    if constexpr (KV != kKvInt4)  // the fused step's grid (no fused step for 4-bit pools)
+        if (st == PKV_OK) st = decode_grid<D, G, KV, true>(pool, batch, max_blocks_per_seq, &g1, &smem);
+    *warps = std::max(g0, g1) * Cfg<D, G, KV>::NW;
     return st;
 }
 
-template <int D, bool FP8>
+template <int D, int KV>
 static pkv_status grid_g(pkv_pool *pool, int G, int batch, int max_blocks_per_seq, int *warps)
 {
     switch (G) {
-    case 1: return grid_warps<D, 1, FP8>(pool, batch, max_blocks_per_seq, warps);
-    case 2: return grid_warps<D, 2, FP8>(pool, batch, max_blocks_per_seq, warps);
-    case 4: return grid_warps<D, 4, FP8>(pool, batch, max_blocks_per_seq, warps);
-    case 8: return grid_warps<D, 8, FP8>(pool, batch, max_blocks_per_seq, warps);
+    case 1: return grid_warps<D, 1, KV>(pool, batch, max_blocks_per_seq, warps);
+    case 2: return grid_warps<D, 2, KV>(pool, batch, max_blocks_per_seq, warps);
+    case 4: return grid_warps<D, 4, KV>(pool, batch, max_blocks_per_seq, warps);
+    case 8: return grid_warps<D, 8, KV>(pool, batch, max_blocks_per_seq, warps);
     }
     return fail(PKV_EUNSUPPORTED, "decode: group size %d unsupported (1, 2, 4 or 8)", G);
 }
@@ -1176,12 +1339,15 @@ pkv_status decode_workspace_bytes(pkv_pool *pool, int batch, int n_q, int max_bl
 {
     const int G = n_q / pool->n_kv;
     int warps = 0;
-    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
     const int W = max_blocks_per_seq;
-    pkv_status st = pool->d_head == 128 ? (fp8 ? grid_g<128, true>(pool, G, batch, W, &warps)
-                                               : grid_g<128, false>(pool, G, batch, W, &warps))
-                                        : (fp8 ? grid_g<64, true>(pool, G, batch, W, &warps)
-                                               : grid_g<64, false>(pool, G, batch, W, &warps));
+    const bool d128 = pool->d_head == 128;
+    pkv_status st;
+    if (pool->dtype == PKV_INT4)
+        st = d128 ? grid_g<128, kKvInt4>(pool, G, batch, W, &warps) : grid_g<64, kKvInt4>(pool, G, batch, W, &warps);
+    else if (pool->dtype == PKV_FP8_E4M3)
+        st = d128 ? grid_g<128, kKvFp8>(pool, G, batch, W, &warps) : grid_g<64, kKvFp8>(pool, G, batch, W, &warps);
+    else
+        st = d128 ? grid_g<128, kKvBf16>(pool, G, batch, W, &warps) : grid_g<64, kKvBf16>(pool, G, batch, W, &warps);
     if (st != PKV_OK) return st;
     *bytes = ws_layout(batch, n_q, pool->n_kv, pool->d_head,
                        max_slots(pool, batch, pool->n_kv, max_blocks_per_seq, warps)).total;
@@ -1219,9 +1385,10 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
         return fail(PKV_EINVAL, "paged_decode_attention: q and out must be 16-byte aligned");
     if (((uintptr_t)block_tables | (uintptr_t)context_lens) & 3u)
         return fail(PKV_EINVAL, "paged_decode_attention: tables and lengths must be 4-byte aligned");
-    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
-    if (fp8 && !pool->scales_set)
-        return fail(PKV_EINVAL, "paged_decode_attention: FP8 pool needs kv_pool_set_fp8_scales first");
+    if (!pool->scales_set && pool->dtype != PKV_BF16)
+        return fail(PKV_EINVAL, "paged_decode_attention: %s pool needs its %s first",
+                    pool->dtype == PKV_INT4 ? "4-bit" : "FP8",
+                    pool->dtype == PKV_INT4 ? "kv_pool_set_int4_key_params" : "kv_pool_set_fp8_scales");
 
     DecodeArgs a;
     a.num_blocks = pool->num_blocks;
@@ -1236,6 +1403,8 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
     a.batch = batch;
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
+    a.k_params = pool->k_params;
+    a.v_params = pool->v_params;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
@@ -1246,10 +1415,7 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
     a.skip_blocks = 0;
     a.n_pre = 0;
     a.pre_base = 0;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (pool->d_head == 128)
-        return fp8 ? dispatch_g<128, true>(pool, a, G, s) : dispatch_g<128, false>(pool, a, G, s);
-    return fp8 ? dispatch_g<64, true>(pool, a, G, s) : dispatch_g<64, false>(pool, a, G, s);
+    return dispatch_kv(pool, a, G, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" pkv_status paged_decode_attention_csr(pkv_pool *pool, const void *q, int32_t n_q,
@@ -1278,9 +1444,8 @@ extern "C" pkv_status paged_decode_attention_csr(pkv_pool *pool, const void *q, 
         return fail(PKV_EINVAL, "paged_decode_attention_csr: q and out must be 16-byte aligned");
     if (((uintptr_t)kv_indptr | (uintptr_t)kv_indices | (uintptr_t)context_lens) & 3u)
         return fail(PKV_EINVAL, "paged_decode_attention_csr: indptr, indices and lengths must be 4-byte aligned");
-    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
-    if (fp8 && !pool->scales_set)
-        return fail(PKV_EINVAL, "paged_decode_attention_csr: FP8 pool needs kv_pool_set_fp8_scales first");
+    if (!pool->scales_set && pool->dtype != PKV_BF16)
+        return fail(PKV_EINVAL, "paged_decode_attention_csr: quantised pool needs its scales first");
 
     DecodeArgs a;
     a.num_blocks = pool->num_blocks;
@@ -1296,6 +1461,8 @@ extern "C" pkv_status paged_decode_attention_csr(pkv_pool *pool, const void *q, 
     a.batch = batch;
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
+    a.k_params = pool->k_params;
+    a.v_params = pool->v_params;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
@@ -1306,10 +1473,7 @@ extern "C" pkv_status paged_decode_attention_csr(pkv_pool *pool, const void *q, 
     a.skip_blocks = 0;
     a.n_pre = 0;
     a.pre_base = 0;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (pool->d_head == 128)
-        return fp8 ? dispatch_g<128, true>(pool, a, G, s) : dispatch_g<128, false>(pool, a, G, s);
-    return fp8 ? dispatch_g<64, true>(pool, a, G, s) : dispatch_g<64, false>(pool, a, G, s);
+    return dispatch_kv(pool, a, G, static_cast<cudaStream_t>(stream));
 }
 
 namespace pkv {
@@ -1318,34 +1482,34 @@ namespace pkv {
 // Fused step: append each sequence's newest token and decode, one launch
 // ---------------------------------------------------------------------------
 
-template <int D, int G, bool FP8>
+template <int D, int G, int KV>
 static pkv_status launch_step(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
 {
-    using C = Cfg<D, G, FP8>;
+    using C = Cfg<D, G, KV>;
     int grid = 0;
     size_t smem = 0;
-    pkv_status st = decode_grid<D, G, FP8, true>(pool, a.batch, a.W, &grid, &smem);
+    pkv_status st = decode_grid<D, G, KV, true>(pool, a.batch, a.W, &grid, &smem);
     if (st != PKV_OK) return st;
     const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
     st = ensure_workspace(pool, L.total);
     if (st != PKV_OK) return st;
     bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
     LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl(decode_kernel<D, G, FP8, true>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
+    cudaError_t e = launch_pdl(decode_kernel<D, G, KV, true>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
                                pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
     return launch_merge<D, G>(pool, a, grid * C::NW, s);
 }
 
-template <int D, bool FP8>
+template <int D, int KV>
 static pkv_status dispatch_step(pkv_pool *pool, const DecodeArgs &a, int G, cudaStream_t s)
 {
     switch (G) {
-    case 1: return launch_step<D, 1, FP8>(pool, a, s);
-    case 2: return launch_step<D, 2, FP8>(pool, a, s);
-    case 4: return launch_step<D, 4, FP8>(pool, a, s);
-    case 8: return launch_step<D, 8, FP8>(pool, a, s);
+    case 1: return launch_step<D, 1, KV>(pool, a, s);
+    case 2: return launch_step<D, 2, KV>(pool, a, s);
+    case 4: return launch_step<D, 4, KV>(pool, a, s);
+    case 8: return launch_step<D, 8, KV>(pool, a, s);
     }
     return fail(PKV_EUNSUPPORTED, "decode step: group size %d unsupported (1, 2, 4 or 8)", G);
 }
@@ -1367,8 +1531,9 @@ static pkv_status check_step_args(const pkv_pool *pool, const char *who, int n_q
     if (batch > kMaxBatch) return fail(PKV_EUNSUPPORTED, "%s: batch %d > %d", who, batch, kMaxBatch);
     if ((int64_t)batch * pool->n_kv * max_blocks_per_seq >= ((int64_t)1 << 30))
         return fail(PKV_EUNSUPPORTED, "%s: batch x n_kv x max_blocks_per_seq too large", who);
-    if (pool->dtype == PKV_FP8_E4M3 && !pool->scales_set)
-        return fail(PKV_EINVAL, "%s: FP8 pool needs kv_pool_set_fp8_scales first", who);
+    if (pool->dtype != PKV_BF16 && !pool->scales_set)
+        return fail(PKV_EINVAL, "%s: quantised pool needs its scales first (kv_pool_set_fp8_scales or "
+                    "kv_pool_set_int4_key_params)", who);
     return PKV_OK;
 }
 
@@ -1390,6 +1555,8 @@ static pkv_status step_device(pkv_pool *pool, const void *q, const void *k_new, 
     a.batch = batch;
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
+    a.k_params = pool->k_params;
+    a.v_params = pool->v_params;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
@@ -1405,6 +1572,14 @@ static pkv_status step_device(pkv_pool *pool, const void *q, const void *k_new, 
     a.k_pool = static_cast<uint8_t *>(pool->k);
     a.v_pool = static_cast<uint8_t *>(pool->v);
     const bool fp8 = pool->dtype == PKV_FP8_E4M3;
+    if (pool->dtype == PKV_INT4) {  // 4-bit pools: the append kernel (it finds the slots), then decode
+        pkv_status st = append_step_int4(pool, k_new, v_new, block_tables, max_blocks_per_seq, context_lens,
+                                         batch, s);
+        if (st != PKV_OK) return st;
+        a.k_new = a.v_new = nullptr;
+        a.k_pool = a.v_pool = nullptr;
+        return dispatch_kv(pool, a, G, s);
+    }
     if (pool->d_head == 128) return fp8 ? dispatch_step<128, true>(pool, a, G, s) : dispatch_step<128, false>(pool, a, G, s);
     return fp8 ? dispatch_step<64, true>(pool, a, G, s) : dispatch_step<64, false>(pool, a, G, s);
 }
@@ -1919,6 +2094,8 @@ extern "C" pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *
     a.batch = batch;
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
+    a.k_params = pool->k_params;
+    a.v_params = pool->v_params;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
@@ -1974,13 +2151,13 @@ static pkv_status noalloc_scratch(int device, void **out)
     return PKV_OK;
 }
 
-template <int D, int G, bool FP8>
+template <int D, int G, int KV>
 static pkv_status launch_decode_noalloc(pkv_pool *pool, DecodeArgs a, uint8_t *scratch, cudaStream_t s)
 {
-    using C = Cfg<D, G, FP8>;
+    using C = Cfg<D, G, KV>;
     int grid = 0;
     size_t smem = 0;
-    pkv_status st = decode_grid<D, G, FP8>(pool, a.batch, a.W, &grid, &smem);
+    pkv_status st = decode_grid<D, G, KV>(pool, a.batch, a.W, &grid, &smem);
     if (st != PKV_OK) return st;
     const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
     if (L.total > kNoAllocScratchBytes)
@@ -1992,21 +2169,21 @@ static pkv_status launch_decode_noalloc(pkv_pool *pool, DecodeArgs a, uint8_t *s
     // needs to start at zero (every partial is written before it is read).
     bind_workspace(a, scratch, L);
     LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl(decode_kernel<D, G, FP8>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
+    cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
                                pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch (noalloc)");
     return launch_merge<D, G>(pool, a, grid * C::NW, s);
 }
 
-template <int D, bool FP8>
+template <int D, int KV>
 static pkv_status dispatch_g_noalloc(pkv_pool *pool, const DecodeArgs &a, int G, uint8_t *scratch, cudaStream_t s)
 {
     switch (G) {
-    case 1: return launch_decode_noalloc<D, 1, FP8>(pool, a, scratch, s);
-    case 2: return launch_decode_noalloc<D, 2, FP8>(pool, a, scratch, s);
-    case 4: return launch_decode_noalloc<D, 4, FP8>(pool, a, scratch, s);
-    case 8: return launch_decode_noalloc<D, 8, FP8>(pool, a, scratch, s);
+    case 1: return launch_decode_noalloc<D, 1, KV>(pool, a, scratch, s);
+    case 2: return launch_decode_noalloc<D, 2, KV>(pool, a, scratch, s);
+    case 4: return launch_decode_noalloc<D, 4, KV>(pool, a, scratch, s);
+    case 8: return launch_decode_noalloc<D, 8, KV>(pool, a, scratch, s);
     }
     return fail(PKV_EUNSUPPORTED, "decode: group size %d unsupported (1, 2, 4 or 8)", G);
 }
@@ -2042,8 +2219,8 @@ extern "C" pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void 
     if (((uintptr_t)block_tables | (uintptr_t)context_lens) & 3u)
         return fail(PKV_EINVAL, "paged_decode_attention_noalloc: tables and lengths must be 4-byte aligned");
     const bool fp8 = pool->dtype == PKV_FP8_E4M3;
-    if (fp8 && !pool->scales_set)
-        return fail(PKV_EINVAL, "paged_decode_attention_noalloc: FP8 pool needs kv_pool_set_fp8_scales first");
+    if (!pool->scales_set && pool->dtype != PKV_BF16)
+        return fail(PKV_EINVAL, "paged_decode_attention_noalloc: quantised pool needs its scales first");
     int cur = -1;
     cudaError_t e = cudaGetDevice(&cur);
     if (e != cudaSuccess) return cuda_fail(e, "paged_decode_attention_noalloc: cudaGetDevice");
@@ -2067,6 +2244,8 @@ extern "C" pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void 
     a.batch = batch;
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
+    a.k_params = pool->k_params;
+    a.v_params = pool->v_params;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
@@ -2080,6 +2259,10 @@ extern "C" pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void 
     uint8_t *sp = static_cast<uint8_t *>(scratch);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pool->d_head == 128)
-        return fp8 ? dispatch_g_noalloc<128, true>(pool, a, G, sp, s) : dispatch_g_noalloc<128, false>(pool, a, G, sp, s);
-    return fp8 ? dispatch_g_noalloc<64, true>(pool, a, G, sp, s) : dispatch_g_noalloc<64, false>(pool, a, G, sp, s);
+        return pool->dtype == PKV_INT4 ? dispatch_g_noalloc<128, kKvInt4>(pool, a, G, sp, s)
+               : fp8                   ? dispatch_g_noalloc<128, kKvFp8>(pool, a, G, sp, s)
+                                       : dispatch_g_noalloc<128, kKvBf16>(pool, a, G, sp, s);
+    return pool->dtype == PKV_INT4 ? dispatch_g_noalloc<64, kKvInt4>(pool, a, G, sp, s)
+           : fp8                   ? dispatch_g_noalloc<64, kKvFp8>(pool, a, G, sp, s)
+                                   : dispatch_g_noalloc<64, kKvBf16>(pool, a, G, sp, s);
 }

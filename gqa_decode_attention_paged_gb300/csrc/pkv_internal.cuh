@@ -39,6 +39,10 @@ struct pkv_pool {
     void *k = nullptr, *v = nullptr;  // device, [num_blocks][n_kv][block_size][d_head]
     size_t bytes_per_array = 0;
     float *scales = nullptr;          // device [2 * n_kv]: k scales then v scales
+    // 4-bit pools: per value row (scale, zero point) [num_blocks][n_kv][block_size][2] fp32,
+    // and the keys' per-channel parameters [2][n_kv][d_head] fp32 (scales, then zero points)
+    float *v_params = nullptr;
+    float *k_params = nullptr;
     // TMA descriptors of the K and V arrays viewed as 2-D [rows = blocks*n_kv*16][d_head],
     // boxes of 16 rows x min(row bytes, 128) bytes, swizzled (128 B, or 64 B for 64-byte rows).
     CUtensorMap tm_k, tm_v;
@@ -78,6 +82,8 @@ struct LaunchScope {
 };
 
 pkv_status ensure_workspace(pkv_pool *pool, size_t bytes);
+pkv_status append_step_int4(pkv_pool *pool, const void *k_new, const void *v_new, const int32_t *tables, int W,
+                            const int32_t *lens, int batch, cudaStream_t s);
 pkv_status ensure_staging(pkv_pool *pool, size_t bytes);
 pkv_status make_tensor_maps(pkv_pool *pool);
 

@@ -109,17 +109,21 @@ pkv_status make_tensor_maps(pkv_pool *pool)
         if (get_err == cudaSuccess && q != cudaDriverEntryPointSuccess) get_err = cudaErrorNotSupported;
     });
     if (get_err != cudaSuccess || !encode) return cuda_fail(get_err, "cuTensorMapEncodeTiled entry point");
+    // rows of d_head bf16, d_head E4M3 bytes, or d_head / 2 bytes of packed 4-bit codes
     const int elem = pool->dtype == PKV_BF16 ? 2 : 1;
-    const uint64_t row_bytes = (uint64_t)pool->d_head * elem;
+    const uint64_t row_elems = pool->dtype == PKV_INT4 ? (uint64_t)pool->d_head / 2 : (uint64_t)pool->d_head;
+    const uint64_t row_bytes = row_elems * elem;
     const uint64_t rows = (uint64_t)pool->num_blocks * pool->n_kv * pool->block_size;
     if (rows >= (1ull << 31)) return fail(PKV_EUNSUPPORTED, "kv_pool_create: more than 2^31 token rows");
     const uint32_t box_bytes = row_bytes > 128 ? 128 : (uint32_t)row_bytes;
-    cuuint64_t dims[2] = {(cuuint64_t)pool->d_head, rows};
+    cuuint64_t dims[2] = {(cuuint64_t)row_elems, rows};
     cuuint64_t strides[1] = {row_bytes};
     cuuint32_t box[2] = {box_bytes / (uint32_t)elem, (cuuint32_t)pool->block_size};
     cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType dt = elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    const CUtensorMapSwizzle sw = box_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUtensorMapSwizzle sw = box_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                    : CU_TENSOR_MAP_SWIZZLE_32B;
     for (int which = 0; which < 2; ++which) {
         CUresult r = encode(which ? &pool->tm_v : &pool->tm_k, dt, 2, which ? pool->v : pool->k, dims, strides,
                             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -190,10 +194,10 @@ pkv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv, 
     if (d_head != 64 && d_head != 128)
         return fail(PKV_EUNSUPPORTED, "kv_pool_create: d_head %d unsupported (64 or 128)", d_head);
     if (n_kv > 256) return fail(PKV_EUNSUPPORTED, "kv_pool_create: n_kv %d > 256", n_kv);
-    if (dtype != PKV_BF16 && dtype != PKV_FP8_E4M3)
+    if (dtype != PKV_BF16 && dtype != PKV_FP8_E4M3 && dtype != PKV_INT4)
         return fail(PKV_EINVAL, "kv_pool_create: unknown dtype %d", dtype);
-    const size_t elem = dtype == PKV_BF16 ? 2 : 1;
-    const size_t per_block = (size_t)n_kv * block_size * d_head * elem;
+    const size_t row_bytes = dtype == PKV_BF16 ? 2 * (size_t)d_head : dtype == PKV_FP8_E4M3 ? d_head : d_head / 2;
+    const size_t per_block = (size_t)n_kv * block_size * row_bytes;
     if ((size_t)num_blocks > ((size_t)1 << 46) / per_block)
         return fail(PKV_ERANGE, "kv_pool_create: pool too large");
 
@@ -220,6 +224,14 @@ pkv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv, 
     if (e == cudaSuccess) { what = "cudaMalloc(V pool)"; e = cudaMalloc(&p->v, p->bytes_per_array); }
     if (e == cudaSuccess) { what = "cudaMalloc(scales)"; e = cudaMalloc(&p->scales, sizeof(float) * 2 * n_kv); }
     if (e == cudaSuccess) { what = "cudaMalloc(error word)"; e = cudaMalloc(&p->err, sizeof(unsigned)); }
+    const size_t vp_bytes = (size_t)num_blocks * n_kv * block_size * 2 * sizeof(float);
+    if (e == cudaSuccess && dtype == PKV_INT4) {
+        what = "cudaMalloc(value params)";
+        e = cudaMalloc(&p->v_params, vp_bytes);
+        if (e == cudaSuccess) e = cudaMemset(p->v_params, 0, vp_bytes);
+        if (e == cudaSuccess) { what = "cudaMalloc(key params)"; e = cudaMalloc(&p->k_params, sizeof(float) * 2 * n_kv * d_head); }
+        if (e == cudaSuccess) e = cudaMemset(p->k_params, 0, sizeof(float) * 2 * n_kv * d_head);
+    }
     if (e == cudaSuccess) { what = "cudaMemset"; e = cudaMemset(p->k, 0, p->bytes_per_array); }
     if (e == cudaSuccess) e = cudaMemset(p->v, 0, p->bytes_per_array);
     if (e == cudaSuccess) e = cudaMemset(p->scales, 0, sizeof(float) * 2 * n_kv);
@@ -246,6 +258,8 @@ pkv_status kv_pool_destroy(pkv_pool *pool)
     cudaFree(pool->k);
     cudaFree(pool->v);
     cudaFree(pool->scales);
+    cudaFree(pool->v_params);
+    cudaFree(pool->k_params);
     cudaFree(pool->err);
     cudaFree(pool->ws);
     cudaFree(pool->stage);
@@ -278,13 +292,33 @@ pkv_status kv_pool_set_fp8_scales(pkv_pool *pool, const float *k_scale_host, con
     return PKV_OK;
 }
 
+pkv_status kv_pool_set_int4_key_params(pkv_pool *pool, const float *k_scale_host, const float *k_zero_host)
+{
+    if (!pool || !k_scale_host || !k_zero_host) return fail(PKV_EINVAL, "kv_pool_set_int4_key_params: NULL argument");
+    if (pool->dtype != PKV_INT4) return fail(PKV_EINVAL, "kv_pool_set_int4_key_params: pool is not 4-bit");
+    const size_t n = (size_t)pool->n_kv * pool->d_head;
+    std::vector<float> s(2 * n);
+    for (size_t i = 0; i < n; ++i) {
+        s[i] = k_scale_host[i];
+        s[n + i] = k_zero_host[i];
+        if (!(s[i] > 0.0f) || !isfinite(s[i]) || !isfinite(s[n + i]))
+            return fail(PKV_EINVAL, "kv_pool_set_int4_key_params: scales must be finite and > 0, zeros finite");
+    }
+    cudaError_t e = cudaMemcpy(pool->k_params, s.data(), sizeof(float) * s.size(), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "kv_pool_set_int4_key_params");
+    pool->scales_set = true;
+    return PKV_OK;
+}
+
 pkv_status kv_pool_layout(const pkv_pool *pool, pkv_layout *out)
 {
     if (!pool || !out) return fail(PKV_EINVAL, "kv_pool_layout: NULL argument");
     out->k = pool->k;
     out->v = pool->v;
-    out->stride_token = pool->d_head;
-    out->stride_head = (int64_t)pool->block_size * pool->d_head;
+    out->v_params = pool->v_params;
+    out->v_params_bytes = pool->v_params ? (int64_t)pool->num_blocks * pool->n_kv * pool->block_size * 8 : 0;
+    out->stride_token = pool->dtype == PKV_INT4 ? pool->d_head / 2 : pool->d_head;
+    out->stride_head = (int64_t)pool->block_size * out->stride_token;
     out->stride_block = (int64_t)pool->n_kv * out->stride_head;
     out->num_blocks = pool->num_blocks;
     out->block_size = pool->block_size;

@@ -47,7 +47,9 @@ typedef enum {
 
 typedef enum {
     PKV_BF16 = 0,      /* keys and values stored as bf16 */
-    PKV_FP8_E4M3 = 1   /* stored as FP8 E4M3 with a per-KV-head fp32 scale */
+    PKV_FP8_E4M3 = 1,  /* stored as FP8 E4M3 with a per-KV-head fp32 scale */
+    PKV_INT4 = 2       /* 4-bit codes: keys with a per-(KV head, channel) scale and zero point, values with a
+                          per-(token, KV head) scale and zero point (see kv_pool_set_int4_key_params) */
 } pkv_dtype;
 
 /* Bits of the sticky device error word (pkv_get_error). */
@@ -61,7 +63,11 @@ typedef struct pkv_pool pkv_pool; /* opaque; owns its device memory */
 /* Where a pool's blocks live.  K and V are two separate device arrays, each
  * laid out [num_blocks][n_kv][block_size][d_head]: element (blk, g, off, d)
  * of either array sits at blk*stride_block + g*stride_head + off*stride_token
- * + d (strides in elements), so one (block, KV head) tile is contiguous. */
+ * + d (strides in elements), so one (block, KV head) tile is contiguous.
+ * PKV_INT4 pools store packed codes instead: an "element" is one byte
+ * holding channels 2i (low nibble) and 2i+1 (high nibble), the row has
+ * d_head / 2 of them, and v_params holds each value row's fp32 (scale, zero
+ * point) pair, [num_blocks][n_kv][block_size][2]. */
 typedef struct {
     void *k;                 /* device */
     void *v;                 /* device */
@@ -74,6 +80,8 @@ typedef struct {
     int32_t d_head;
     int32_t dtype;           /* pkv_dtype */
     int64_t bytes_per_array; /* bytes of K (and, equally, of V) */
+    void *v_params;          /* device; PKV_INT4 only (NULL otherwise) */
+    int64_t v_params_bytes;
 } pkv_layout;
 
 /* Per-kernel timing gathered with CUDA events while timing is enabled. */
@@ -110,6 +118,18 @@ pkv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv, 
 /* Free the pool and everything it owns (synchronises the device first).
  * NULL is accepted. */
 pkv_status kv_pool_destroy(pkv_pool *pool);
+
+/* PKV_INT4 pools: set the keys' per-(KV head, channel) parameters from two
+ * host arrays of n_kv x d_head fp32 values, [g][channel]: a key value x is
+ * stored as the code c = clamp(rint((x - k_zero) / k_scale), 0, 15)
+ * (fp32, round half to even) and read back as c * k_scale + k_zero.  Values
+ * need no call: each appended value row gets its own scale (max - min) / 15
+ * (1 if max == min) and zero point min.  The pages ask for 4-bit KV with
+ * per-channel key scales ("KV cache, PagedAttention and FlashAttention",
+ * Problem 3, "Trade-offs"; KIVI, KVQuant); the rest is this library's
+ * reading.  Must be called before the first append or decode of a 4-bit
+ * pool; scales finite and > 0, zero points finite.  Errors: EINVAL. */
+pkv_status kv_pool_set_int4_key_params(pkv_pool *pool, const float *k_scale_host, const float *k_zero_host);
 
 /* FP8 pools: set the per-KV-head dequantisation scales from two host arrays
  * of n_kv fp32 values (stored value = E4M3(x / scale), read back as
@@ -224,7 +244,9 @@ pkv_status paged_decode_attention_csr(pkv_pool *pool, const void *q, int32_t n_q
  * arithmetic), followed by paged_decode_attention -- the pool bytes and the
  * output are the same -- but the row is written by the thread block that
  * reads that block anyway, so the step costs the decode's two launches and
- * no append launch.
+ * no append launch.  PKV_INT4 pools (whose value rows need their own min and
+ * max before they can be stored) run the append kernel first, finding each
+ * slot from the table, then the decode: three launches, same results.
  *   k_new, v_new  device bf16 [batch][n_kv][d_head], 16-byte aligned: the
  *                 new token of each sequence (ignored where context_len == 0).
  *   other arguments as paged_decode_attention.  A sequence's last block must

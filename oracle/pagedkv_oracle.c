@@ -36,7 +36,7 @@
  *       x ~ c * s + z; keys use one (s, z) per (KV head, channel), fixed on
  *       the pool; values use one (s, z) per (token, KV head), from that
  *       row's min and max (s = (max - min) / 15, or 1 when max == min;
- *       z = min).  c = clamp(rint((x - z) / s), 0, 15) in fp32 with
+ *       z = min, a negative zero taken as +0).  c = clamp(rint((x - z) / s), 0, 15) in fp32 with
  *       round-half-to-even.  Codes are packed two per byte, the even
  *       channel in the low nibble.
  *
@@ -259,8 +259,9 @@ void orc_int4_row_params(const uint16_t *row_bits, int d, float *s_out, float *z
     volatile float range = mx - mn;
     volatile float s = range / 15.0f;
     if (s == 0.0f) s = 1.0f;
+    volatile float z = mn + 0.0f; /* a negative-zero minimum is stored as +0 */
     *s_out = s;
-    *z_out = mn;
+    *z_out = z;
 }
 
 static void orc_put_nibble(uint8_t *row, int c, uint8_t code)

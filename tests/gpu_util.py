@@ -26,10 +26,12 @@ def i32_dev(x) -> torch.Tensor:
 
 
 def make_pool(w, partition_tokens: int | None = None) -> pkv.Pool:
-    dt = pkv.BF16 if w.dtype == "bf16" else pkv.FP8_E4M3
+    dt = {"bf16": pkv.BF16, "fp8": pkv.FP8_E4M3, "int4": pkv.INT4}[w.dtype]
     pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head, dt)
     if w.dtype == "fp8":
         pool.set_fp8_scales(w.k_scale, w.v_scale)
+    if w.dtype == "int4":
+        pool.set_int4_key_params(w.k_scale, w.k_zero)
     if partition_tokens:
         pool.set_partition_tokens(partition_tokens)
     return pool
@@ -58,8 +60,8 @@ def run_step(pool, w, dev=None):
 
 
 def mirror(w) -> oracle.PoolMirror:
-    dt = oracle.BF16 if w.dtype == "bf16" else oracle.E4M3
-    m = oracle.PoolMirror(w.num_blocks, w.block_size, w.n_kv, w.d_head, dt, w.k_scale, w.v_scale)
+    dt = {"bf16": oracle.BF16, "fp8": oracle.E4M3, "int4": oracle.INT4}[w.dtype]
+    m = oracle.PoolMirror(w.num_blocks, w.block_size, w.n_kv, w.d_head, dt, w.k_scale, w.v_scale, w.k_zero)
     m.append(w.fill_k, w.fill_v, w.fill_slots)
     m.append(w.step_k, w.step_v, w.step_slots)
     return m

@@ -21,15 +21,19 @@ and any thread count):
   block table points to; it is filled once.
 * FP8 scales (per KV head, separate for K and V) are the fp32 amax of that
   head's source values over every token of the workload, divided by 448.
+* 4-bit key parameters (per KV head and channel) are the channel's min over
+  every token of the workload (zero point) and (max - min) / 15 (scale);
+  value rows get theirs when appended.
 * ``scale`` is fp32(1/sqrt(d_head)).
 
-The five named workloads follow the shapes of the pages' examples: a tiny
+The named workloads follow the shapes of the pages' examples: a tiny
 paged case, the Llama3-8B attention shape ("Memory Management in LLM Serving
 Systems", "KV cache sizing"), the 70B long-context shape ("KV cache, PagedAttention
 and FlashAttention", Problem 3), an FP8 KV batch with log-normal lengths
 (Problem 3's FP8 row; the page's "Practise it" fragmentation exercise uses
-log-normal lengths) and a shared-prefix batch ("Memory Management in LLM
-Serving Systems", "Prefix sharing").
+log-normal lengths), a shared-prefix batch ("Memory Management in LLM
+Serving Systems", "Prefix sharing") and the Llama3-8B shape on a 4-bit KV
+pool (Problem 3's 4-bit row).
 """
 from __future__ import annotations
 
@@ -93,7 +97,7 @@ class Workload:
     n_kv: int
     d_head: int
     block_size: int
-    dtype: str  # "bf16" or "fp8"
+    dtype: str  # "bf16", "fp8" or "int4"
     num_blocks: int
     context_lens: np.ndarray  # int32 [B], lengths after the step's append
     block_tables: np.ndarray  # int32 [B, W]; -1 past each sequence's last block
@@ -105,8 +109,9 @@ class Workload:
     step_slots: np.ndarray  # int64 [B]; -1 for a sequence with no token this step
     q: np.ndarray  # uint16 [B, n_q, D]
     scale: np.float32
-    k_scale: np.ndarray | None = None  # float32 [n_kv]
+    k_scale: np.ndarray | None = None  # float32 [n_kv] (fp8), [n_kv, d_head] (int4)
     v_scale: np.ndarray | None = None
+    k_zero: np.ndarray | None = None   # float32 [n_kv, d_head] (int4 key zero points)
     shared_prefix_tokens: int = 0
     seed: int = 0
     notes: dict = field(default_factory=dict)
@@ -122,6 +127,14 @@ class Workload:
     @property
     def elem_bytes(self) -> int:
         return 2 if self.dtype == "bf16" else 1
+
+    @property
+    def kv_bytes_per_token_head(self) -> int:
+        """Bytes one cached token stores per KV head: K and V rows (4-bit: two
+        codes per byte, plus the value row's fp32 scale and zero point)."""
+        if self.dtype == "int4":
+            return self.d_head + 8
+        return 2 * self.d_head * self.elem_bytes
 
     def describe(self) -> dict:
         return {
@@ -208,7 +221,7 @@ def build(name: str, n_q: int, n_kv: int, d_head: int, context_lens, *, dtype: s
     step_v = normal_bf16_bits((B, n_kv, d_head), (seed, 4))
     q = normal_bf16_bits((B, n_q, d_head), (seed, 5))
 
-    k_scale = v_scale = None
+    k_scale = v_scale = k_zero = None
     if dtype == "fp8":
         def amax(fill, step):
             a = np.zeros(n_kv, dtype=np.float32)
@@ -221,20 +234,33 @@ def build(name: str, n_q: int, n_kv: int, d_head: int, context_lens, *, dtype: s
 
         k_scale = amax(fill_k, step_k)
         v_scale = amax(fill_v, step_v)
+    elif dtype == "int4":
+        # keys: per (KV head, channel) min and max over the workload's tokens
+        lo = np.full((n_kv, d_head), np.inf, dtype=np.float32)
+        hi = np.full((n_kv, d_head), -np.inf, dtype=np.float32)
+        for part in [fill_k[s:s + 65536] for s in range(0, T, 65536)] + ([step_k] if B else []):
+            x = bf16_bits_to_f32(part)
+            lo = np.minimum(lo, x.min(axis=0))
+            hi = np.maximum(hi, x.max(axis=0))
+        lo[~np.isfinite(lo)] = 0.0
+        hi[~np.isfinite(hi)] = 0.0
+        k_scale = ((hi - lo) / np.float32(15.0)).astype(np.float32)
+        k_scale[k_scale == 0] = 1.0
+        k_zero = lo.astype(np.float32)
     elif dtype != "bf16":
-        raise ValueError("dtype must be bf16 or fp8")
+        raise ValueError("dtype must be bf16, fp8 or int4")
 
     sc = np.float32(1.0 / math.sqrt(d_head)) if scale is None else np.float32(scale)
     return Workload(name=name, n_q=n_q, n_kv=n_kv, d_head=d_head, block_size=BS, dtype=dtype,
                     num_blocks=int(num_blocks), context_lens=cl.astype(np.int32),
                     block_tables=tables, fill_k=fill_k, fill_v=fill_v, fill_slots=fill_slots,
                     step_k=step_k, step_v=step_v, step_slots=step_slots, q=q, scale=sc,
-                    k_scale=k_scale, v_scale=v_scale, shared_prefix_tokens=shared_prefix_tokens,
+                    k_scale=k_scale, v_scale=v_scale, k_zero=k_zero, shared_prefix_tokens=shared_prefix_tokens,
                     seed=seed)
 
 
 # --------------------------------------------------------------------------
-# The five named workloads
+# The named workloads
 # --------------------------------------------------------------------------
 
 def tiny(seed: int = 1) -> Workload:
@@ -280,10 +306,20 @@ def shared_prefix(seed: int = 5, batch: int = 128) -> Workload:
                  max_blocks_per_seq=129)
 
 
+def int4_llama3(seed: int = 6, batch: int = 128) -> Workload:
+    """The Llama3-8B decode shape (n_q=32, n_kv=8, d_head=128, lengths
+    uniform in [1024, 2048]) on a 4-bit KV pool, batch 128 so that the
+    cache (about 210 MB) is larger than L2."""
+    rng = np.random.default_rng([seed, 100])
+    cl = rng.integers(1024, 2049, size=batch)
+    return build("llama3_8b_int4_b128", 32, 8, 128, cl, dtype="int4", seed=seed)
+
+
 NAMED = {
     "tiny": tiny,
     "llama3_8b": llama3_8b,
     "long_context_70b": long_context_70b,
     "fp8_lognormal": fp8_lognormal,
     "shared_prefix": shared_prefix,
+    "int4_llama3": int4_llama3,
 }
