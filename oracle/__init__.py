@@ -14,6 +14,9 @@ passage of the pages it follows:
 * ``slot_of`` -- same page, Problem 4, "The idea" (block = p // B,
   offset = p % B, physical block from the block table).
 * ``append`` -- "The KV Cache from First Principles", "Deriving the cache".
+* ``prefill`` -- a chunk of new tokens per sequence attending causally over
+  the cache: "Memory Management in LLM Serving Systems", "FlashAttention";
+  "The KV Cache from First Principles", "Deriving the cache".
 * ``decode`` -- "The KV Cache from First Principles", "Implementation" and
   "Grouped-query attention: the compromise"; max-subtracted softmax from
   "Memory Management in LLM Serving Systems", "FlashAttention".
@@ -86,6 +89,9 @@ def _load():
         lib.orc_decode_int4.argtypes = [P, P, P, c.c_int64, c.c_int, c.c_int, c.c_int, P, c.c_int, c.c_int, P,
                                         c.c_int, P, c.c_float, P, P, P, c.c_int]
         lib.orc_decode_int4.restype = c.c_int
+        lib.orc_prefill.argtypes = [P, P, c.c_int, c.c_int64, c.c_int, c.c_int, c.c_int, P, P, c.c_int, c.c_int,
+                                    P, c.c_int, P, c.c_float, P, P, P, c.c_int]
+        lib.orc_prefill.restype = c.c_int
         lib.orc_hardware_threads.argtypes = []
         lib.orc_hardware_threads.restype = c.c_int
         _lib = lib
@@ -200,4 +206,25 @@ class PoolMirror:
                                 int(threads or hardware_threads()))
         if rc != 0:
             raise ValueError(f"oracle decode failed with code {rc}")
+        return out
+
+    def prefill(self, q_bits: np.ndarray, qo_indptr: np.ndarray, block_tables: np.ndarray,
+                context_lens: np.ndarray, scale: float, threads: int | None = None) -> np.ndarray:
+        """fp64 causal attention ``[rows, n_q, d_head]`` of each sequence's chunk
+        of new tokens (rows qo_indptr[b] .. qo_indptr[b+1], the last positions of
+        its cache) over its cache."""
+        qb = np.ascontiguousarray(q_bits, dtype=np.uint16)
+        ip = np.ascontiguousarray(qo_indptr, dtype=np.int32)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        R, n_q, D = qb.shape
+        B = cl.shape[0]
+        assert D == self.d_head and ip.shape == (B + 1,) and bt.shape[0] == B and ip[-1] == R
+        out = np.empty((R, n_q, D), dtype=np.float64)
+        rc = _load().orc_prefill(_ptr(self.k), _ptr(self.v), self.dtype, self.num_blocks, self.block_size,
+                                 self.n_kv, self.d_head, _ptr(qb), _ptr(ip), B, n_q, _ptr(bt), bt.shape[1],
+                                 _ptr(cl), float(np.float32(scale)), _ptr(self.k_scale), _ptr(self.v_scale),
+                                 _ptr(out), int(threads or hardware_threads()))
+        if rc != 0:
+            raise ValueError(f"oracle prefill failed with code {rc}")
         return out

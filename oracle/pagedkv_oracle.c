@@ -26,6 +26,13 @@
  *        "Grouped-query attention: the compromise"; the max-subtracted
  *        softmax of "Memory Management in LLM Serving Systems",
  *        "FlashAttention").
+ *   - prefill (chunked) attention over the cache: a sequence's chunk of T new
+ *       tokens, already appended at positions C-T .. C-1, each attending to
+ *       every cached position up to and including its own (causal), with
+ *       the same per-head definition as decode ("Memory Management in LLM
+ *       Serving Systems", "FlashAttention" and its causal prefill; "The KV
+ *       Cache from First Principles", "Deriving the cache": the prefill
+ *       populates the cache and computes attention for the prompt).
  *   - FP8 E4M3 codec: decode from the bit-field definition, encode by brute
  *       force over all finite codes (nearest, ties to the even code,
  *       saturating to +-448).  The pages say only "FP8"; E4M3 with a
@@ -324,6 +331,7 @@ typedef struct {
     double scale;
     const float *k_scale, *v_scale;
     const float *k_zero, *v_params; /* 4-bit pools: key zero points; value (s, z) per row */
+    const int32_t *qo_indptr;       /* prefill: query rows of sequence b are qo_indptr[b] .. qo_indptr[b+1] */
     double *out;
     /* work distribution */
     int64_t next_task;
@@ -349,10 +357,16 @@ static int orc_decode_one(orc_decode_job *job, int b, int g)
     const int D = job->d_head, BS = job->block_size;
     const int group = job->n_q / job->n_kv;
     int64_t C = job->context_lens[b];
-    double *out_base = job->out + ((int64_t)b * job->n_q) * D;
+    if (job->qo_indptr && job->qo_indptr[b + 1] - job->qo_indptr[b] > C) return -1; /* chunk longer than the cache */
     if (C <= 0) {
-        for (int hh = 0; hh < group; ++hh)
-            for (int d = 0; d < D; ++d) out_base[(int64_t)(g * group + hh) * D + d] = 0.0;
+        int64_t r0 = b, r1 = (int64_t)b + 1;
+        if (job->qo_indptr) {
+            r0 = job->qo_indptr[b];
+            r1 = job->qo_indptr[b + 1];
+        }
+        for (int64_t r = r0; r < r1; ++r)
+            for (int hh = 0; hh < group; ++hh)
+                for (int d = 0; d < D; ++d) job->out[(r * job->n_q + g * group + hh) * D + d] = 0.0;
         return 0;
     }
     if (C > (int64_t)job->max_blocks_per_seq * BS) return -1;
@@ -391,25 +405,35 @@ static int orc_decode_one(orc_decode_job *job, int b, int g)
             Vc[p * D + d] = orc_load(job->v_pool, job->dtype, base + d, vs);
         }
     }
-    for (int hh = 0; hh < group; ++hh) {
-        int h = g * group + hh; /* query head h reads KV head h // group */
-        const uint16_t *qh = job->q + ((int64_t)b * job->n_q + h) * D;
-        double m = -INFINITY;
-        for (int64_t p = 0; p < C; ++p) {
-            double dot = 0.0;
-            for (int d = 0; d < D; ++d) dot += orc_bf16_to_double(qh[d]) * Kc[p * D + d];
-            s[p] = job->scale * dot;
-            if (s[p] > m) m = s[p];
+    /* decode: one query row (position C-1) per sequence; prefill: rows
+     * r0 .. r1-1 hold the chunk's tokens at positions C-T .. C-1 */
+    int64_t r0 = b, r1 = (int64_t)b + 1;
+    if (job->qo_indptr) {
+        r0 = job->qo_indptr[b];
+        r1 = job->qo_indptr[b + 1];
+    }
+    for (int64_t r = r0; r < r1; ++r) {
+        int64_t n_keys = C - (r1 - r) + 1; /* causal: keys 0 .. own position */
+        for (int hh = 0; hh < group; ++hh) {
+            int h = g * group + hh; /* query head h reads KV head h // group */
+            const uint16_t *qh = job->q + (r * job->n_q + h) * D;
+            double m = -INFINITY;
+            for (int64_t p = 0; p < n_keys; ++p) {
+                double dot = 0.0;
+                for (int d = 0; d < D; ++d) dot += orc_bf16_to_double(qh[d]) * Kc[p * D + d];
+                s[p] = job->scale * dot;
+                if (s[p] > m) m = s[p];
+            }
+            double denom = 0.0;
+            double *o = job->out + (r * job->n_q + h) * D;
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            for (int64_t p = 0; p < n_keys; ++p) {
+                double w = exp(s[p] - m);
+                denom += w;
+                for (int d = 0; d < D; ++d) o[d] += w * Vc[p * D + d];
+            }
+            for (int d = 0; d < D; ++d) o[d] /= denom;
         }
-        double denom = 0.0;
-        double *o = out_base + (int64_t)h * D;
-        for (int d = 0; d < D; ++d) o[d] = 0.0;
-        for (int64_t p = 0; p < C; ++p) {
-            double w = exp(s[p] - m);
-            denom += w;
-            for (int d = 0; d < D; ++d) o[d] += w * Vc[p * D + d];
-        }
-        for (int d = 0; d < D; ++d) o[d] /= denom;
     }
     free(Kc); free(Vc); free(s);
     return 0;
@@ -487,6 +511,40 @@ int orc_decode_int4(const uint8_t *k_codes, const uint8_t *v_codes, const float 
     job.block_tables = block_tables; job.max_blocks_per_seq = max_blocks_per_seq;
     job.context_lens = context_lens; job.scale = (double)scale;
     job.k_scale = k_scale; job.k_zero = k_zero; job.v_params = v_params; job.out = out;
+    pthread_mutex_init(&job.lock, NULL);
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 256) n_threads = 256;
+    pthread_t tids[256];
+    int started = 0;
+    for (int i = 1; i < n_threads; ++i)
+        if (pthread_create(&tids[started], NULL, orc_decode_worker, &job) == 0) ++started;
+    orc_decode_worker(&job);
+    for (int i = 0; i < started; ++i) pthread_join(tids[i], NULL);
+    pthread_mutex_destroy(&job.lock);
+    return job.status;
+}
+
+/* Prefill: query rows [qo_indptr[b], qo_indptr[b+1]) of q ([rows][n_q][d]
+ * bf16) are sequence b's newest tokens, at positions C-T .. C-1 of its cache
+ * (C = context_lens[b], T the row count), each attending causally.  out is
+ * [rows][n_q][d] fp64.  bf16 and E4M3 pools.  Returns as orc_decode (-1 also
+ * when a chunk is longer than its cache). */
+int orc_prefill(const void *k_pool, const void *v_pool, int dtype, int64_t num_blocks, int block_size, int n_kv,
+                int d_head, const uint16_t *q, const int32_t *qo_indptr, int batch, int n_q,
+                const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens, float scale,
+                const float *k_scale, const float *v_scale, double *out, int n_threads)
+{
+    if (n_kv <= 0 || n_q <= 0 || n_q % n_kv != 0 || batch < 0 || d_head <= 0 || block_size <= 0 || !qo_indptr ||
+        dtype == ORC_INT4)
+        return -3;
+    orc_decode_job job;
+    memset(&job, 0, sizeof job);
+    job.k_pool = k_pool; job.v_pool = v_pool; job.dtype = dtype;
+    job.num_blocks = num_blocks; job.block_size = block_size; job.n_kv = n_kv; job.d_head = d_head;
+    job.q = q; job.batch = batch; job.n_q = n_q; job.qo_indptr = qo_indptr;
+    job.block_tables = block_tables; job.max_blocks_per_seq = max_blocks_per_seq;
+    job.context_lens = context_lens; job.scale = (double)scale;
+    job.k_scale = k_scale; job.v_scale = v_scale; job.out = out;
     pthread_mutex_init(&job.lock, NULL);
     if (n_threads < 1) n_threads = 1;
     if (n_threads > 256) n_threads = 256;

@@ -552,3 +552,58 @@ def test_int4_mirror_layout_and_exact_values():
     lens = np.array([NB * 16, 40], dtype=np.int32)
     q = wl.f32_to_bf16_bits(rng.normal(size=(2, 4, d)).astype(np.float32))
     assert np.array_equal(m4.decode(q, table, lens, 0.125), mb.decode(q, table, lens, 0.125))
+
+
+# ---------------------------------------------------------------------------
+# Prefill (a chunk of new tokens per sequence, causal over the cache)
+# ---------------------------------------------------------------------------
+
+def _chunk_queries(w, chunks, seed):
+    rng = np.random.default_rng(seed)
+    R = int(sum(chunks))
+    q = wl.f32_to_bf16_bits(rng.normal(size=(R, w.n_q, w.d_head)).astype(np.float32))
+    indptr = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    return q, indptr
+
+
+def test_prefill_equals_masked_sdpa_over_the_cached_sequence():
+    """Each chunk token at position C-T+i sees keys 0..C-T+i: torch's fp64
+    scaled_dot_product_attention with that mask (GQA by repeating KV heads)."""
+    w = wl.build("pf_pin", 8, 2, 64, [1, 17, 40, 100], seed=91)
+    m = _mirror_for(w)
+    chunks = [1, 5, 40, 33]
+    q, indptr = _chunk_queries(w, chunks, 92)
+    out = m.prefill(q, indptr, w.block_tables, w.context_lens, w.scale)
+    G = w.n_q // w.n_kv
+    sc = float(np.float32(w.scale))
+    for b, T in enumerate(chunks):
+        C = int(w.context_lens[b])
+        k, v = _contiguous_kv(w, b)
+        kt = torch.from_numpy(k).permute(1, 0, 2).repeat_interleave(G, dim=0)[None]
+        vt = torch.from_numpy(v).permute(1, 0, 2).repeat_interleave(G, dim=0)[None]
+        qt = torch.from_numpy(_f64(q[indptr[b]:indptr[b + 1]])).permute(1, 0, 2)[None]
+        mask = torch.arange(C)[None, :] <= (C - T + torch.arange(T))[:, None]
+        ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=sc)
+        got = out[indptr[b]:indptr[b + 1]]
+        assert np.abs(got - ref[0].permute(1, 0, 2).numpy()).max() < 1e-12, b
+
+
+def test_prefill_one_token_chunks_are_decode_and_chunks_compose():
+    w = wl.build("pf_dec", 32, 8, 128, [300, 1, 17, 64], seed=93)
+    m = _mirror_for(w)
+    B = w.batch
+    one = np.arange(B + 1, dtype=np.int32)
+    assert np.array_equal(m.prefill(w.q, one, w.block_tables, w.context_lens, w.scale),
+                          m.decode(w.q, w.block_tables, w.context_lens, w.scale))
+    # a whole-sequence prefill's last rows are the prefill of the last chunk
+    full = [int(c) for c in w.context_lens]
+    q_full, ip_full = _chunk_queries(w, full, 94)
+    tail = [min(7, c) for c in full]
+    q_tail = np.concatenate([q_full[ip_full[b + 1] - tail[b]:ip_full[b + 1]] for b in range(B)])
+    ip_tail = np.concatenate([[0], np.cumsum(tail)]).astype(np.int32)
+    a = m.prefill(q_full, ip_full, w.block_tables, w.context_lens, w.scale)
+    t = m.prefill(q_tail, ip_tail, w.block_tables, w.context_lens, w.scale)
+    for b in range(B):
+        assert np.array_equal(a[ip_full[b + 1] - tail[b]:ip_full[b + 1]], t[ip_tail[b]:ip_tail[b + 1]])
+    with pytest.raises(ValueError):  # 3 new tokens for a sequence holding 1: a chunk longer than its cache
+        m.prefill(q_full[:3], np.array([0, 0, 3, 3, 3], np.int32), w.block_tables, w.context_lens, w.scale)
