@@ -54,7 +54,7 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--flush-l2", action="store_true", help="write 512 MB between steps")
-    p.add_argument("--mode", default="decode", choices=["decode", "blocks", "cascade"])
+    p.add_argument("--mode", default="decode", choices=["decode", "blocks", "cascade", "prefill"])
     return p.parse_args(argv)
 
 
@@ -706,10 +706,71 @@ def run_cascade(args):
     return 0
 
 
+def run_prefill(args):
+    """Chunked prefill attention: a 512-token chunk for each of the Llama3-8B
+    batch's 64 sequences (caches of 1024..2048 tokens, the chunk being their
+    last 512 positions), causal over the cache.  Tensor-bound: reported in
+    attention TFLOP/s (4 x n_q x d_head per query token and visible key)."""
+    import numpy as np
+    import torch
+
+    import gqa_decode_attention_paged_gb300 as pkv
+    import workloads as wl
+
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    w = wl.llama3_8b()
+    T = 512
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).cuda().view(dt)  # noqa: E731
+    pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head, pkv.BF16)
+    pkv.paged_kv_append(pool, dev(w.fill_k.view(np.int16), torch.bfloat16), dev(w.fill_v.view(np.int16), torch.bfloat16),
+                        dev(w.fill_slots, torch.int64))
+    pkv.paged_kv_append(pool, dev(w.step_k.view(np.int16), torch.bfloat16), dev(w.step_v.view(np.int16), torch.bfloat16),
+                        dev(w.step_slots, torch.int64))
+    rng = np.random.default_rng(11)
+    q_bits = wl.f32_to_bf16_bits(rng.normal(size=(w.batch * T, w.n_q, w.d_head)).astype(np.float32))
+    q = dev(q_bits.view(np.int16), torch.bfloat16)
+    indptr = dev(np.arange(0, w.batch * T + 1, T, dtype=np.int32), torch.int32)
+    tables = dev(w.block_tables, torch.int32)
+    lens = dev(w.context_lens, torch.int32)
+    out = torch.empty_like(q)
+    reps, warm = max(3, min(args.steps, 50)), max(3, args.warmup)
+    ms = _timed(lambda: pkv.paged_prefill_attention(pool, q, indptr, tables, lens, float(w.scale), out, stream),
+                reps, warm, stream)
+    assert pool.get_error() == 0
+    C = w.context_lens.astype(np.int64)
+    keys = int(sum(int(c) * T - T * (T - 1) // 2 for c in C))  # sum over chunk tokens of visible keys
+    flops = 4 * w.n_q * w.d_head * keys
+    tflops = flops / (ms / 1e3) / 1e12
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    line = {
+        "metric": "chunked prefill attention over the paged cache: attention TFLOP/s vs GB300 bf16 tensor peak",
+        "mode": "prefill",
+        "value": tflops,
+        "unit": "TFLOP/s",
+        "higher_is_better": True,
+        "ms_per_call": ms,
+        "dtype": "bf16 in, f32 accumulate",
+        "data": "synthetic",
+        "config": dict(w.describe(), chunk_tokens=T, query_rows=w.batch * T, visible_keys=keys),
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": tflops, "peak": peak,
+                     "unit": "TFLOP/s", "frac": tflops / peak,
+                     "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops: cuBLAS burst)" if peaks
+                     else "fallback"},
+    }
+    print(json.dumps(line), flush=True)
+    pool.close()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.mode == "prefill":
+        return run_prefill(args)
     if args.mode == "blocks":
         return run_blocks(args)
     if args.mode == "cascade":

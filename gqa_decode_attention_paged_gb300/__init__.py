@@ -93,6 +93,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.paged_decode_attention_prefix.argtypes = [P, P, c.c_int32, P, c.c_int32, P, c.c_int32, P, c.c_int32,
                                                       c.c_float, P, P]
         lib.paged_decode_attention_csr.argtypes = [P, P, c.c_int32, P, P, c.c_int64, P, c.c_int32, c.c_float, P, P]
+        lib.paged_prefill_attention.argtypes = [P, P, c.c_int64, c.c_int32, P, P, c.c_int32, P, c.c_int32,
+                                                c.c_float, P, P]
         lib.paged_decode_step.argtypes = [P, P, P, P, c.c_int32, P, c.c_int32, P, c.c_int32, c.c_float, P, P]
         lib.paged_decode_step_host.argtypes = [P, P, P, P, c.c_int32, P, c.c_int32, P, c.c_int32, c.c_float,
                                                P, P]
@@ -125,7 +127,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                      "kv_pool_layout",
                      "kv_pool_set_partition_tokens", "kv_pool_reserve_workspace", "paged_kv_append",
                      "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
-                     "paged_decode_attention_csr",
+                     "paged_decode_attention_csr", "paged_prefill_attention",
                      "paged_decode_step_host", "paged_decode_attention_prefix", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read",
                      "pkv_selftest_wait_timeout", "kv_block_copy", "kv_swap_out", "kv_swap_in", "kv_alloc_create",
                      "kv_alloc_destroy", "kv_alloc_refcount", "kv_alloc_take", "kv_alloc_share", "kv_alloc_release",
@@ -349,6 +351,28 @@ def paged_decode_attention_csr(pool: Pool, q, kv_indptr, kv_indices, context_len
     return out
 
 
+def paged_prefill_attention(pool: Pool, q, qo_indptr, block_tables, context_lens, scale: float, out=None,
+                            stream=None):
+    """Causal attention of each sequence's chunk of new tokens over its cache.
+    q: bf16 [rows, n_q, d_head] (the chunks, sequence by sequence);
+    qo_indptr: int32 [B + 1] (sequence b owns rows qo_indptr[b]:qo_indptr[b+1]);
+    block_tables: int32 [B, W]; context_lens: int32 [B] (including the chunk)."""
+    import torch
+
+    qp = _dev_ptr(q, "q", torch.bfloat16, 3, (None, None, pool.d_head))
+    rows, n_q = int(q.shape[0]), int(q.shape[1])
+    B = int(context_lens.shape[0])
+    ip = _dev_ptr(qo_indptr, "qo_indptr", torch.int32, 1, (B + 1,))
+    tp = _dev_ptr(block_tables, "block_tables", torch.int32, 2, (B, None))
+    cp = _dev_ptr(context_lens, "context_lens", torch.int32, 1, (B,))
+    if out is None:
+        out = torch.empty_like(q)
+    op = _dev_ptr(out, "out", torch.bfloat16, 3, tuple(q.shape))
+    _check(load().paged_prefill_attention(pool.handle, qp, rows, n_q, ip, tp, int(block_tables.shape[1]), cp, B,
+                                          float(scale), op, _stream_handle(stream)))
+    return out
+
+
 def paged_decode_attention_prefix(pool: Pool, q, prefix_blocks, block_tables, context_lens, scale: float,
                                   out=None, stream=None):
     """Cascade decode: every sequence starts with the shared prefix whose
@@ -563,5 +587,6 @@ class BlockAllocator:
 __all__ = ["BF16", "FP8_E4M3", "INT4", "Pool", "PagedKVError", "kv_pool_create", "paged_kv_append",
            "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
            "paged_decode_step_host", "paged_decode_attention_prefix", "paged_decode_attention_csr",
+           "paged_prefill_attention",
            "kv_bytes_per_token", "kv_block_bytes",
            "kv_block_copy", "kv_swap_out", "kv_swap_in", "BlockAllocator", "load", "library_path"]

@@ -292,6 +292,30 @@ pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *q, int32_t 
                                          const int32_t *context_lens, int32_t batch, float scale, void *out,
                                          void *stream);
 
+/* Prefill (chunked prefill) attention over the paged cache: for each
+ * sequence b, a chunk of T_b new tokens that paged_kv_append has already
+ * written at positions C_b - T_b .. C_b - 1 of its cache (C_b =
+ * context_lens[b]); token i of the chunk, query head h, attends to cached
+ * positions 0 .. C_b - T_b + i with KV head h // (n_q / n_kv) (causal;
+ * "Memory Management in LLM Serving Systems", "FlashAttention": exact
+ * attention in tiles with an online softmax; "The KV Cache from First
+ * Principles", "Deriving the cache": the prefill fills the cache and
+ * computes the prompt's attention).  T_b = 1 for every sequence is decode.
+ *   q          device bf16 [n_rows][n_q][d_head], 16-byte aligned: the
+ *              chunks' tokens, sequence by sequence.
+ *   qo_indptr  device int32 [batch + 1]: sequence b's tokens are rows
+ *              qo_indptr[b] .. qo_indptr[b+1] (qo_indptr[batch] == n_rows).
+ *   context_lens  device int32 [batch]: cache length including the chunk.
+ *              A chunk longer than its cache, or a length past the table,
+ *              sets PKV_DEVERR_CTX_RANGE.
+ *   out        device bf16 [n_rows][n_q][d_head].
+ * bf16 pools.  One launch; tensor-core tiles of 64 query rows per
+ * (sequence, KV head) stream that sequence's blocks once per tile.
+ * Errors: EINVAL, EUNSUPPORTED (FP8 / 4-bit pools, group size), ECUDA. */
+pkv_status paged_prefill_attention(pkv_pool *pool, const void *q, int64_t n_rows, int32_t n_q,
+                                   const int32_t *qo_indptr, const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t *context_lens, int32_t batch, float scale, void *out, void *stream);
+
 /* paged_decode_attention without any allocation.  The pages have no
  * counterpart to this call; it exists for callers that cannot allocate
  * device memory when they decode: an engine that reserved nearly all free

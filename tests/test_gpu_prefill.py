@@ -1,0 +1,67 @@
+"""Chunked prefill attention over the paged cache against the oracle: each
+sequence's chunk of new tokens (the last positions of its cache) attends
+causally; shapes span group sizes, head sizes, one-token chunks (decode),
+whole-sequence prefills, partial row tiles and empty chunks."""
+import numpy as np
+import pytest
+import torch
+
+import gqa_decode_attention_paged_gb300 as pkv
+import workloads as wl
+from gpu_util import assert_close, bf16_dev, fill, i32_dev, make_pool, mirror, out_f64, run_step
+
+pytestmark = pytest.mark.gpu
+
+
+def _chunks(w, chunks, seed):
+    rng = np.random.default_rng(seed)
+    q = wl.f32_to_bf16_bits(rng.normal(size=(int(sum(chunks)), w.n_q, w.d_head)).astype(np.float32))
+    return q, np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+
+
+CASES = [
+    (lambda: wl.build("pf_g4", 32, 8, 128, [1, 40, 300, 1000], seed=101), [1, 17, 300, 64]),
+    (lambda: wl.build("pf_g8", 64, 8, 128, [200, 33, 700], seed=102), [200, 0, 5]),
+    (lambda: wl.build("pf_d64", 8, 2, 64, [90, 5, 257, 16], seed=103), [90, 5, 100, 16]),
+    (lambda: wl.build("pf_mha", 4, 4, 64, [100, 31], seed=104), [60, 31]),
+    (lambda: wl.build("pf_g2", 16, 8, 128, [64, 512, 3], seed=105), [33, 512, 2]),
+]
+
+
+@pytest.mark.parametrize("make,chunks", CASES)
+def test_prefill_matches_oracle(make, chunks):
+    w = make()
+    with make_pool(w) as pool:
+        fill(pool, w)
+        run_step(pool, w)  # the last position of every sequence
+        q, indptr = _chunks(w, chunks, 7)
+        out = pkv.paged_prefill_attention(pool, bf16_dev(q), i32_dev(indptr), i32_dev(w.block_tables),
+                                          i32_dev(w.context_lens), float(w.scale))
+        torch.cuda.synchronize()
+        ref = mirror(w).prefill(q, indptr, w.block_tables, w.context_lens, w.scale)
+        assert_close(out_f64(out), ref, w.name)
+        assert pool.get_error() == 0
+
+
+def test_prefill_one_token_chunks_are_decode():
+    w = CASES[0][0]()
+    with make_pool(w) as pool:
+        fill(pool, w)
+        run_step(pool, w)
+        indptr = np.arange(w.batch + 1, dtype=np.int32)
+        out = pkv.paged_prefill_attention(pool, bf16_dev(w.q), i32_dev(indptr), i32_dev(w.block_tables),
+                                          i32_dev(w.context_lens), float(w.scale))
+        torch.cuda.synchronize()
+        assert_close(out_f64(out), mirror(w).decode(w.q, w.block_tables, w.context_lens, w.scale), "T = 1")
+
+
+def test_prefill_flags_a_chunk_longer_than_its_cache():
+    w = CASES[2][0]()
+    with make_pool(w) as pool:
+        fill(pool, w)
+        run_step(pool, w)
+        q, indptr = _chunks(w, [1, 9, 1, 1], 8)  # sequence 1 holds 5 tokens
+        pkv.paged_prefill_attention(pool, bf16_dev(q), i32_dev(indptr), i32_dev(w.block_tables),
+                                    i32_dev(w.context_lens), float(w.scale))
+        torch.cuda.synchronize()
+        assert pool.get_error(clear=True) & pkv.DEVERR_CTX_RANGE
