@@ -51,10 +51,7 @@
 
 namespace pkv {
 
-constexpr int kMaxBatch = 8192;
 constexpr int kMinBlocksPerWarp = 8;
-constexpr unsigned kFull = 0xffffffffu;
-constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeArgs {
     int64_t num_blocks;
@@ -1514,9 +1511,8 @@ static pkv_status dispatch_step(pkv_pool *pool, const DecodeArgs &a, int G, cuda
     return fail(PKV_EUNSUPPORTED, "decode step: group size %d unsupported (1, 2, 4 or 8)", G);
 }
 
-// Argument checks shared by the two step entry points (device pointers).
-static pkv_status check_step_args(const pkv_pool *pool, const char *who, int n_q, int max_blocks_per_seq, int batch,
-                                  float scale)
+pkv_status check_step_args(const pkv_pool *pool, const char *who, int n_q, int max_blocks_per_seq, int batch,
+                           float scale)
 {
     if (!pool) return fail(PKV_EINVAL, "%s: NULL pool", who);
     if (batch < 0) return fail(PKV_EINVAL, "%s: batch < 0", who);
@@ -2109,395 +2105,6 @@ extern "C" pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (pool->d_head == 128) return dispatch_prefix<128>(pool, a, G, prefix_blocks, n_prefix_blocks, s);
     return dispatch_prefix<64>(pool, a, G, prefix_blocks, n_prefix_blocks, s);
-}
-
-namespace pkv {
-
-// ---------------------------------------------------------------------------
-// Prefill (chunked) attention over the paged cache
-//
-// Sequence b has a chunk of T new tokens, already appended at positions
-// C-T .. C-1 of its cache (C = context_lens[b]); query row (token i, head hh
-// of KV head g's group) attends to positions 0 .. C-T+i (causal).  The rows
-// are the MMA M dimension as in the cascade prefix stage: CTA (row tile, g)
-// holds 64 rows (4 warps x 16) of one sequence and streams that sequence's
-// blocks 0 .. (its last row's position) / 16 once through a TMA ring, two
-// blocks per online-softmax step, masking every score past a row's
-// position.  Row tiles are dealt out over the sequences by a scan of the
-// chunk lengths, so the host needs only the total row count.
-// ---------------------------------------------------------------------------
-
-constexpr int kPrefillWarps = 4;
-constexpr int kPrefillRows = kPrefillWarps * 16;
-constexpr int kPrefillStages = 8;
-
-struct PrefillArgs {
-    const __nv_bfloat16 *q;    // [rows][n_q][D]
-    const int32_t *qo_indptr;  // [batch + 1]: rows of sequence b
-    const int32_t *block_tables;
-    int W;
-    const int32_t *context_lens;
-    int batch, n_q, n_kv;
-    int64_t num_blocks;
-    float qscale;  // scale * log2(e)
-    __nv_bfloat16 *out;  // [rows][n_q][D]
-    unsigned *err;
-};
-
-template <int D>
-struct PrefillSmem {
-    using Gm = Geo<D, kKvBf16>;
-    static constexpr int kRing = kPrefillStages * Gm::STAGE;
-    static constexpr int kBars = kRing;
-    static constexpr int kPhys = kBars + kPrefillStages * 8;
-    static constexpr int kWarpTot = kPhys + kPrefillStages * 4;
-    static constexpr int kTiles = kWarpTot + kPrefillWarps * 4;  // tile prefix sums [batch + 1]
-    static size_t bytes(int batch) { return 1024 + (size_t)kTiles + 4 * ((size_t)batch + 1); }
-};
-
-// x, y as a bf16 pair hi (round to nearest) and the bf16 pair of what hi
-// leaves out: hi + lo carries about 16 bits of x and y.
-__device__ __forceinline__ void split_bf16(float x, float y, uint32_t &hi, uint32_t &lo)
-{
-    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
-    const float2 hf = __bfloat1622float2(h);
-    const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
-    hi = *reinterpret_cast<const uint32_t *>(&h);
-    lo = *reinterpret_cast<const uint32_t *>(&l);
-}
-
-template <int D, int G>
-__global__ void __launch_bounds__(kPrefillWarps * 32, 3)
-    prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, PrefillArgs a)
-{
-    using Gm = Geo<D, kKvBf16>;
-    using L = PrefillSmem<D>;
-    constexpr int NT = D / 16;
-    constexpr int S = kPrefillStages;
-    constexpr int NTH = kPrefillWarps * 32;
-    extern __shared__ __align__(1024) uint8_t prefill_smem[];
-    uint8_t *sm = prefill_smem + ((1024u - (smem_u32(prefill_smem) & 1023u)) & 1023u);
-    uint8_t *ring = sm;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kBars);
-    int *phys_st = reinterpret_cast<int *>(sm + L::kPhys);
-    int *warp_tot = reinterpret_cast<int *>(sm + L::kWarpTot);
-    int32_t *tps = reinterpret_cast<int32_t *>(sm + L::kTiles);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g8 = lane >> 2, c4 = lane & 3;
-    const int g = blockIdx.y;
-    if (tid == 0) {
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
-        fence_mbarrier_init();
-    }
-    griddep_wait();  // q, tables and the appended chunk may come from the previous kernel
-    griddep_launch_dependents();
-    // row tiles per sequence, exclusive prefix sum into tps[0 .. batch]
-    {
-        int carry = 0;
-        for (int base = 0; base < a.batch; base += NTH) {
-            const int b = base + tid;
-            int n = 0;
-            if (b < a.batch) {
-                const int rows = max(0, a.qo_indptr[b + 1] - a.qo_indptr[b]) * G;
-                n = (rows + kPrefillRows - 1) / kPrefillRows;
-            }
-            int x = n;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(kFull, x, o);
-                if (lane >= o) x += y;
-            }
-            if (lane == 31) warp_tot[warp] = x;
-            __syncthreads();
-            int before = 0, tot = 0;
-#pragma unroll
-            for (int w = 0; w < kPrefillWarps; ++w) {
-                before += w < warp ? warp_tot[w] : 0;
-                tot += warp_tot[w];
-            }
-            if (b < a.batch) tps[b] = carry + before + x - n;
-            carry += tot;
-            __syncthreads();
-        }
-        if (tid == 0) tps[a.batch] = carry;
-        __syncthreads();
-    }
-    const int tile_id = blockIdx.x;
-    if (tile_id >= tps[a.batch]) return;  // the grid is an upper bound on the tiles
-    int lo = 0, hi = a.batch - 1;         // the sequence holding this tile: largest b with tps[b] <= tile_id
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (tps[mid] <= tile_id) lo = mid; else hi = mid - 1;
-    }
-    const int b = lo;
-    const int T = a.qo_indptr[b + 1] - a.qo_indptr[b];
-    const int R = T * G;  // rows of (b, g)
-    int C = a.context_lens[b];
-    if (C < T || C > a.W * kBlockSize) {  // a chunk longer than its cache, or a cache past the table
-        if (tid == 0) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
-        C = max(T, min(C, a.W * kBlockSize));
-        if (C > a.W * kBlockSize) return;  // nothing sensible to attend to; rows left unwritten
-    }
-    const int rt0 = (tile_id - tps[b]) * kPrefillRows;  // first local row of this tile
-    const int r0 = rt0 + warp * 16;
-    // positions: row r is token r / G at position C - T + r / G
-    const int last_row = min(R, rt0 + kPrefillRows) - 1;
-    const int n_blocks = (C - T + last_row / G) / kBlockSize + 1;  // blocks any row of the tile reaches
-    const int32_t *trow = a.block_tables + (int64_t)b * a.W;
-    const uint64_t policy = l2_policy_evict_first();
-    auto issue = [&](int j) {  // thread 0: block j of the sequence into stage j % S
-        const int st = j % S;
-        const int phys = trow[j];
-        const bool ok = phys >= 0 && phys < a.num_blocks;
-        phys_st[st] = ok ? phys : -1;
-        if (ok) {
-            const int y = (int)(((int64_t)phys * a.n_kv + g) * kBlockSize);
-            uint8_t *dst = ring + st * Gm::STAGE;
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&bars[st], Gm::STAGE);
-#pragma unroll
-            for (int r = 0; r < Gm::NREG; ++r) {
-                tma_load_2d(dst + r * Gm::RGN, &tm_k, r * Gm::BOX_ELEMS, y, &bars[st], policy);
-                tma_load_2d(dst + Gm::TILE + r * Gm::RGN, &tm_v, r * Gm::BOX_ELEMS, y, &bars[st], policy);
-            }
-        } else {
-            atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
-            mbar_arrive(&bars[st]);
-        }
-    };
-    if (tid == 0)
-        for (int j = 0; j < min(n_blocks, S); ++j) issue(j);
-
-    // this thread's rows g8, g8+8 of the warp: their positions (padding rows
-    // past R attend like the tile's last row and are not written)
-    const int ra = r0 + g8, rb = r0 + g8 + 8;
-    const int pos_a = C - T + min(ra, R - 1) / G, pos_b = C - T + min(rb, R - 1) / G;
-    uint32_t qa[NT][4];
-    {
-        const int64_t row0 = a.qo_indptr[b];
-        const __nv_bfloat16 *qa_row = a.q + ((row0 + min(ra, R - 1) / G) * a.n_q + g * G + min(ra, R - 1) % G) * D;
-        const __nv_bfloat16 *qb_row = a.q + ((row0 + min(rb, R - 1) / G) * a.n_q + g * G + min(rb, R - 1) % G) * D;
-#pragma unroll
-        for (int ks = 0; ks < NT; ++ks) {
-            const int d0 = 16 * ks + 2 * c4;
-            qa[ks][0] = ra < R ? *reinterpret_cast<const uint32_t *>(qa_row + d0) : 0u;
-            qa[ks][1] = rb < R ? *reinterpret_cast<const uint32_t *>(qb_row + d0) : 0u;
-            qa[ks][2] = ra < R ? *reinterpret_cast<const uint32_t *>(qa_row + d0 + 8) : 0u;
-            qa[ks][3] = rb < R ? *reinterpret_cast<const uint32_t *>(qb_row + d0 + 8) : 0u;
-        }
-    }
-    float o[2 * NT][4];  // O[16 rows x D]: n-tile t covers d 8t..8t+7
-#pragma unroll
-    for (int t = 0; t < 2 * NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // rows g8, g8 + 8
-    const int tk = (lane & 7) + (lane >> 4) * 8, hk = (lane >> 3) & 1;
-    const int tv = (lane & 7) + ((lane >> 3) & 1) * 8, hv = lane >> 4;
-    bool aborted = false;
-
-    for (int j = 0; j < n_blocks; j += 2) {
-        const bool two = j + 1 < n_blocks;
-        const int st0 = j % S, st1 = (j + 1) % S;
-        if (!aborted) {
-            bool ok = mbar_wait_bounded(&bars[st0], (uint32_t)(j / S) & 1u);
-            if (two) ok = mbar_wait_bounded(&bars[st1], (uint32_t)((j + 1) / S) & 1u) && ok;
-            aborted = __any_sync(kFull, !ok);
-            if (aborted && lane == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-        }
-        if (!aborted) {
-            const bool v0 = phys_st[st0] >= 0, v1 = two && phys_st[st1] >= 0;
-            const uint32_t kb0 = smem_u32(ring + st0 * Gm::STAGE);
-            const uint32_t kb1 = two ? smem_u32(ring + st1 * Gm::STAGE) : kb0;
-            float s[4][4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.0f;
-#pragma unroll
-            for (int ks = 0; ks < NT; ++ks) {
-                const int ch = 2 * ks + hk;
-                const uint32_t off = (ch >> 3) * Gm::RGN + swz<128>(tk * 128 + (ch & 7) * 16);
-                uint32_t f0[4], f1[4];
-                ldsm_x4(kb0 + off, f0);
-                ldsm_x4(kb1 + off, f1);
-                mma16816<false>(s[0], qa[ks], f0[0], f0[1]);
-                mma16816<false>(s[1], qa[ks], f0[2], f0[3]);
-                mma16816<false>(s[2], qa[ks], f1[0], f1[1]);
-                mma16816<false>(s[3], qa[ks], f1[2], f1[3]);
-            }
-            // row g8: sv[0..7], row g8+8: sv[8..15]; token of n-tile i, column e: 16 * (j + i / 2) + 8 * (i & 1) + 2c + e
-            float sv[16];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool live = i < 2 ? v0 : v1;
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tok = kBlockSize * (j + i / 2) + 8 * (i & 1) + 2 * c4 + e;
-                    sv[2 * i + e] = live && tok <= pos_a ? s[i][e] * a.qscale : -INFINITY;
-                    sv[8 + 2 * i + e] = live && tok <= pos_b ? s[i][2 + e] * a.qscale : -INFINITY;
-                }
-            }
-            float bm0 = sv[0], bm1 = sv[8];
-#pragma unroll
-            for (int i = 1; i < 8; ++i) {
-                bm0 = fmaxf(bm0, sv[i]);
-                bm1 = fmaxf(bm1, sv[8 + i]);
-            }
-#pragma unroll
-            for (int off = 1; off < 4; off <<= 1) {
-                bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
-                bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
-            }
-            // block 0 always holds a visible token (position 0 <= every row's),
-            // so after the first step every row's max is finite
-            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-            const float al0 = mn0 == -INFINITY ? 1.0f : exp2f(m0 - mn0);
-            const float al1 = mn1 == -INFINITY ? 1.0f : exp2f(m1 - mn1);
-            float p[16];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                p[i] = mn0 == -INFINITY ? 0.0f : exp2f(sv[i] - mn0);
-                p[8 + i] = mn1 == -INFINITY ? 0.0f : exp2f(sv[8 + i] - mn1);
-            }
-            l0 = fmaf(l0, al0, ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7])));
-            l1 = fmaf(l1, al1, ((p[8] + p[9]) + (p[10] + p[11])) + ((p[12] + p[13]) + (p[14] + p[15])));
-            m0 = mn0;
-            m1 = mn1;
-            if (__any_sync(kFull, al0 != 1.0f || al1 != 1.0f)) {
-#pragma unroll
-                for (int t = 0; t < 2 * NT; ++t) {
-                    o[t][0] *= al0;
-                    o[t][1] *= al0;
-                    o[t][2] *= al1;
-                    o[t][3] *= al1;
-                }
-            }
-            // P as bf16 high parts plus bf16 remainders (two MMAs each): a row that sees few keys
-            // gets no averaging of P's rounding, so P keeps ~16 bits instead of bf16's 8
-            uint32_t pa0[4], pa1[4], pl0[4], pl1[4];
-            split_bf16(p[0], p[1], pa0[0], pl0[0]);
-            split_bf16(p[8], p[9], pa0[1], pl0[1]);
-            split_bf16(p[2], p[3], pa0[2], pl0[2]);
-            split_bf16(p[10], p[11], pa0[3], pl0[3]);
-            split_bf16(p[4], p[5], pa1[0], pl1[0]);
-            split_bf16(p[12], p[13], pa1[1], pl1[1]);
-            split_bf16(p[6], p[7], pa1[2], pl1[2]);
-            split_bf16(p[14], p[15], pa1[3], pl1[3]);
-            const uint32_t vb0 = kb0 + Gm::TILE, vb1 = kb1 + Gm::TILE;
-#pragma unroll
-            for (int n2 = 0; n2 < NT; ++n2) {
-                const int ch = 2 * n2 + hv;
-                const uint32_t off = (ch >> 3) * Gm::RGN + swz<128>(tv * 128 + (ch & 7) * 16);
-                uint32_t f0[4], f1[4];
-                ldsm_x4_t(vb0 + off, f0);
-                ldsm_x4_t(vb1 + off, f1);
-                if (!v0) f0[0] = f0[1] = f0[2] = f0[3] = 0u;  // no data: keep stale bytes out of the MMA
-                if (!v1) f1[0] = f1[1] = f1[2] = f1[3] = 0u;
-                mma16816<false>(o[2 * n2], pa0, f0[0], f0[1]);
-                mma16816<false>(o[2 * n2 + 1], pa0, f0[2], f0[3]);
-                mma16816<false>(o[2 * n2], pa1, f1[0], f1[1]);
-                mma16816<false>(o[2 * n2 + 1], pa1, f1[2], f1[3]);
-                mma16816<false>(o[2 * n2], pl0, f0[0], f0[1]);
-                mma16816<false>(o[2 * n2 + 1], pl0, f0[2], f0[3]);
-                mma16816<false>(o[2 * n2], pl1, f1[0], f1[1]);
-                mma16816<false>(o[2 * n2 + 1], pl1, f1[2], f1[3]);
-            }
-        }
-        __syncthreads();  // every warp is done with this step's stages
-        if (tid == 0 && !aborted) {
-            if (j + S < n_blocks) issue(j + S);
-            if (j + 1 + S < n_blocks) issue(j + 1 + S);
-        }
-    }
-    if (aborted && tid == 0)  // drain this CTA's copies still in flight (bounded)
-        for (int j = 0; j < min(n_blocks, S); ++j) mbar_wait_bounded(&bars[j % S], 0, 100000000ull);
-
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-        l0 += __shfl_xor_sync(kFull, l0, off);
-        l1 += __shfl_xor_sync(kFull, l1, off);
-    }
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int r = r0 + g8 + 8 * half;
-        if (r >= R) continue;
-        const float lsum = half ? l1 : l0;
-        const float inv = lsum > 0.0f ? 1.0f / lsum : 0.0f;
-        __nv_bfloat16 *ob = a.out + ((int64_t)(a.qo_indptr[b] + r / G) * a.n_q + g * G + r % G) * D;
-#pragma unroll
-        for (int t = 0; t < 2 * NT; ++t)
-            *reinterpret_cast<__nv_bfloat162 *>(ob + 8 * t + 2 * c4) =
-                __floats2bfloat162_rn(o[t][2 * half] * inv, o[t][2 * half + 1] * inv);
-    }
-}
-
-template <int D, int G>
-static pkv_status launch_prefill(pkv_pool *pool, const PrefillArgs &a, int64_t n_rows, cudaStream_t s)
-{
-    using PL = PrefillSmem<D>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(prefill_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)PL::bytes(kMaxBatch));
-    });
-    if (attr_err != cudaSuccess) return cuda_fail(attr_err, "prefill kernel attributes");
-    // an upper bound on the row tiles: every sequence may end with a partial tile
-    const int64_t tiles = (n_rows * G + kPrefillRows - 1) / kPrefillRows + a.batch;
-    if (tiles > INT32_MAX) return fail(PKV_EUNSUPPORTED, "paged_prefill_attention: too many query rows");
-    LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl(prefill_kernel<D, G>, dim3((unsigned)tiles, a.n_kv), dim3(kPrefillWarps * 32),
-                               PL::bytes(a.batch), s, pool->tm_k, pool->tm_v, a);
-    ls.done();
-    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-    return PKV_OK;
-}
-
-template <int D>
-static pkv_status dispatch_prefill(pkv_pool *pool, const PrefillArgs &a, int G, int64_t n_rows, cudaStream_t s)
-{
-    switch (G) {
-    case 1: return launch_prefill<D, 1>(pool, a, n_rows, s);
-    case 2: return launch_prefill<D, 2>(pool, a, n_rows, s);
-    case 4: return launch_prefill<D, 4>(pool, a, n_rows, s);
-    case 8: return launch_prefill<D, 8>(pool, a, n_rows, s);
-    }
-    return fail(PKV_EUNSUPPORTED, "prefill: group size %d unsupported (1, 2, 4 or 8)", G);
-}
-
-}  // namespace pkv
-
-extern "C" pkv_status paged_prefill_attention(pkv_pool *pool, const void *q, int64_t n_rows, int32_t n_q,
-                                              const int32_t *qo_indptr, const int32_t *block_tables,
-                                              int32_t max_blocks_per_seq, const int32_t *context_lens,
-                                              int32_t batch, float scale, void *out, void *stream)
-{
-    pkv_status st = check_step_args(pool, "paged_prefill_attention", n_q, max_blocks_per_seq, batch, scale);
-    if (st != PKV_OK || batch == 0 || n_rows == 0) return st;
-    if (n_rows < 0) return fail(PKV_EINVAL, "paged_prefill_attention: n_rows < 0");
-    if (pool->dtype != PKV_BF16) return fail(PKV_EUNSUPPORTED, "paged_prefill_attention: bf16 pools only");
-    if (!q || !qo_indptr || !block_tables || !context_lens || !out)
-        return fail(PKV_EINVAL, "paged_prefill_attention: NULL device pointer");
-    if (((uintptr_t)q | (uintptr_t)out) & 15u)
-        return fail(PKV_EINVAL, "paged_prefill_attention: q and out must be 16-byte aligned");
-    if (((uintptr_t)qo_indptr | (uintptr_t)block_tables | (uintptr_t)context_lens) & 3u)
-        return fail(PKV_EINVAL, "paged_prefill_attention: indptr, tables and lengths must be 4-byte aligned");
-    PrefillArgs a;
-    a.q = static_cast<const __nv_bfloat16 *>(q);
-    a.qo_indptr = qo_indptr;
-    a.block_tables = block_tables;
-    a.W = max_blocks_per_seq;
-    a.context_lens = context_lens;
-    a.batch = batch;
-    a.n_q = n_q;
-    a.n_kv = pool->n_kv;
-    a.num_blocks = pool->num_blocks;
-    a.qscale = scale * kLog2e;
-    a.out = static_cast<__nv_bfloat16 *>(out);
-    a.err = pool->err;
-    const int G = n_q / pool->n_kv;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return pool->d_head == 128 ? dispatch_prefill<128>(pool, a, G, n_rows, s)
-                               : dispatch_prefill<64>(pool, a, G, n_rows, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -86,6 +86,17 @@ pkv_status append_step_int4(pkv_pool *pool, const void *k_new, const void *v_new
                             const int32_t *lens, int batch, cudaStream_t s);
 pkv_status ensure_staging(pkv_pool *pool, size_t bytes);
 pkv_status make_tensor_maps(pkv_pool *pool);
+// A 3-D tiled TMA map over a query array [n_rows][n_q][d_head] bf16: box of
+// min(d_head, 64) columns x `heads` heads x `tokens` rows, 128-byte swizzle.
+pkv_status make_q_map(CUtensorMap *map, const void *q, int64_t n_rows, int n_q, int d_head, int heads, int tokens);
+
+constexpr int kMaxBatch = 8192;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned kFull = 0xffffffffu;
+
+// Argument checks shared by the entry points that take device block tables.
+pkv_status check_step_args(const pkv_pool *pool, const char *who, int n_q, int max_blocks_per_seq, int batch,
+                           float scale);
 
 // ---------------------------------------------------------------------------
 // Device helpers (inline PTX)
@@ -183,6 +194,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst_smem, const CUtensorMap *m
         : "memory");
 }
 
+// Tiled 3-D TMA load of one box at element coordinates (x, y, z).
+__device__ __forceinline__ void tma_load_3d(void *dst_smem, const CUtensorMap *map, int x, int y, int z,
+                                            uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -275,6 +297,13 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_normal()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 

@@ -97,7 +97,7 @@ pkv_status ensure_staging(pkv_pool *pool, size_t bytes)
 // for tiled TMA: one box = 16 token rows of one (block, KV head) tile and up
 // to 128 bytes of each row, with the matching shared-memory swizzle so that
 // warp-wide fragment loads hit distinct banks.
-pkv_status make_tensor_maps(pkv_pool *pool)
+static pkv_status tiled_encoder(PFN_cuTensorMapEncodeTiled_v12000 *out)
 {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     static std::once_flag once;
@@ -109,6 +109,31 @@ pkv_status make_tensor_maps(pkv_pool *pool)
         if (get_err == cudaSuccess && q != cudaDriverEntryPointSuccess) get_err = cudaErrorNotSupported;
     });
     if (get_err != cudaSuccess || !encode) return cuda_fail(get_err, "cuTensorMapEncodeTiled entry point");
+    *out = encode;
+    return PKV_OK;
+}
+
+pkv_status make_q_map(CUtensorMap *map, const void *q, int64_t n_rows, int n_q, int d_head, int heads, int tokens)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode;
+    pkv_status st = tiled_encoder(&encode);
+    if (st != PKV_OK) return st;
+    cuuint64_t dims[3] = {(cuuint64_t)d_head, (cuuint64_t)n_q, (cuuint64_t)n_rows};
+    cuuint64_t strides[2] = {(cuuint64_t)d_head * 2, (cuuint64_t)n_q * d_head * 2};
+    cuuint32_t box[3] = {(cuuint32_t)(d_head < 64 ? d_head : 64), (cuuint32_t)heads, (cuuint32_t)tokens};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled (queries) failed (%d)", (int)r);
+    return PKV_OK;
+}
+
+pkv_status make_tensor_maps(pkv_pool *pool)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode;
+    pkv_status st = tiled_encoder(&encode);
+    if (st != PKV_OK) return st;
     // rows of d_head bf16, d_head E4M3 bytes, or d_head / 2 bytes of packed 4-bit codes
     const int elem = pool->dtype == PKV_BF16 ? 2 : 1;
     const uint64_t row_elems = pool->dtype == PKV_INT4 ? (uint64_t)pool->d_head / 2 : (uint64_t)pool->d_head;
