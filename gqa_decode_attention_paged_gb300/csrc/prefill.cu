@@ -49,12 +49,17 @@ namespace {
 constexpr int kRows = 128;               // query rows per tile (= TMEM lanes)
 constexpr int kKeys = 128;               // keys per step
 constexpr int kStepBlocks = kKeys / kBlockSize;
-constexpr int kSoftmaxWarps = 4;
-constexpr int kKWarp = 4, kVWarp = 5, kMmaWarp = 6;
-constexpr int kThreads = 7 * 32;
+constexpr int kSoftmaxWarps = 8;        // two per TMEM lane quarter: each takes half of a row's keys
+constexpr int kKWarp = 8, kVWarp = 9, kQkWarp = 10, kPvWarp = 11;
+constexpr int kThreads = 12 * 32;
 constexpr float kRescaleSlack = 8.0f;    // log2 of the largest P value allowed before O is rescaled
-constexpr uint32_t kTmemCols = 512;      // S0 at 0, S1 at 128, O at 256
+constexpr uint32_t kTmemCols = 512;      // S0 at 0, S1 at 128, O at 256, P at 448
 constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = 448;          // P as bf16 pairs: column j holds keys 2j (low half) and 2j + 1
+constexpr int kKStages = 3, kVStages = 2;
+// after O: four columns through which the two warps that own a lane quarter
+// exchange per-row values (their key halves' maxima, and at the end their
+// halves of the row sum), [phase parity][half]
 constexpr uint32_t kHalf = 128 * 128;    // bytes of one 64-column half of a 128-row tile
 
 struct Args {
@@ -75,14 +80,13 @@ template <int D>
 struct Layout {
     static constexpr uint32_t QT = kRows * D * 2;        // one Q tile
     static constexpr uint32_t KT = kKeys * D * 2;        // one K (or V) step
-    static constexpr uint32_t PT = kRows * kKeys * 2;    // P, bf16
     static constexpr uint32_t kQ = 0;                    // 2 Q buffers
-    static constexpr uint32_t kK = kQ + 2 * QT;          // 2 K stages
-    static constexpr uint32_t kV = kK + 2 * KT;          // 2 V stages
-    static constexpr uint32_t kP = kV + 2 * KT;
-    static constexpr uint32_t kBar = kP + PT;
-    enum { Q_FULL = 0, Q_FREE = 2, K_FULL = 4, K_EMPTY = 6, V_FULL = 8, V_EMPTY = 10, S_FULL = 12, S_FREE = 14,
-           P_FULL = 16, O_DONE = 17, DRAIN = 18, NBARS = 19 };
+    static constexpr uint32_t kK = kQ + 2 * QT;          // K stages
+    static constexpr uint32_t kV = kK + kKStages * KT;   // V stages
+    static constexpr uint32_t kBar = kV + kVStages * KT;
+    enum { Q_FULL = 0, Q_FREE = 2, K_FULL = 4, K_EMPTY = 4 + kKStages, V_FULL = 4 + 2 * kKStages,
+           V_EMPTY = V_FULL + kVStages, S_FULL = V_EMPTY + kVStages, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2,
+           O_DONE = P_FULL + 1, DRAIN = O_DONE + 1, PAIR = DRAIN + 2, NBARS = PAIR + 4 };  // DRAIN + issuer, PAIR + lane quarter
     static constexpr uint32_t kTmemSlot = kBar + NBARS * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kEnd = kAbort + 4;
@@ -110,12 +114,48 @@ __host__ __device__ constexpr uint32_t mma_idesc(int M, int N, int b_mn)
            ((uint32_t)(M >> 4) << 24);
 }
 
+// A from tensor memory (M rows in lanes, K packed along columns), B from shared memory.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
 {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
                  ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
                  : "memory");
+}
+
+// Tiled 2-D TMA load multicast to the CTAs of `mask` (same shared-memory offset
+// and mbarrier offset in each).
+__device__ __forceinline__ void tma_load_2d_mc(void *dst_smem, const CUtensorMap *map, int x, int y, uint64_t *bar,
+                                               uint16_t mask, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask), "l"(policy)
+        : "memory");
+}
+
+// Arrive once on `bar` in every CTA of `mask` when the MMAs this thread issued so far have completed.
+__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t mask)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 ::"r"(smem_u32(bar)), "h"(mask)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
 }
 
 // Arrive once on `bar` when every tcgen05 MMA this thread issued so far has completed.
@@ -154,6 +194,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r)
                  : "memory");
 }
 
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t *r)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r[0]) : "r"(taddr) : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -169,13 +219,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
-}
-
-// Byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled
-// tile of 128-byte rows starting on a 1024-byte boundary.
-__device__ __forceinline__ uint32_t swz_off(int row, int chunk)
-{
-    return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
 // ------------------------------------------------------------- tile walk
@@ -207,7 +250,7 @@ __device__ __forceinline__ void load_window(Walker &w, const Args &a, int lane)
         w.row0 = a.qo_indptr[bl];
         w.T = a.qo_indptr[bl + 1] - w.row0;
         w.C = a.context_lens[bl];
-        if (w.T > 0) n = (long long)a.n_kv * (((long long)w.T * G + kRows - 1) / kRows);
+        if (w.T > 0) n = (long long)a.n_kv * ((((long long)w.T * G + kRows - 1) / kRows + 1) / 2);
     }
     long long x = n;
 #pragma unroll
@@ -220,9 +263,13 @@ __device__ __forceinline__ void load_window(Walker &w, const Args &a, int lane)
     w.tot = __shfl_sync(kFull, x, 31);
 }
 
-// Tile x of the list; false past its end.  Warp-wide, uniform result.
+// Pair x of the list of row-tile pairs; this CTA (cluster rank `rank`) takes
+// row tile 2 i + rank of the pair's (sequence, KV head), i the pair's index
+// there (past the last row tile when the count is odd: no rows, the CTA only
+// keeps step with its partner).  Both CTAs stream the blocks the pair's last
+// row reaches.  False past the list's end.  Warp-wide, uniform result.
 template <int G>
-__device__ __forceinline__ bool find_tile(Walker &w, const Args &a, long long x, Tile &t, int lane)
+__device__ __forceinline__ bool find_tile(Walker &w, const Args &a, long long x, int rank, Tile &t, int lane)
 {
     while (x >= w.wbase + w.tot) {
         if (w.wb + 32 >= a.batch) return false;
@@ -241,7 +288,8 @@ __device__ __forceinline__ bool find_tile(Walker &w, const Args &a, long long x,
     const int per_head = n / a.n_kv;
     const int within = (int)(x - w.wbase - before);
     t.g = within / per_head;
-    t.rt0 = (within % per_head) * kRows;
+    const int pair_rt0 = 2 * (within % per_head) * kRows;
+    t.rt0 = pair_rt0 + rank * kRows;
     t.R = t.T * G;
     const int cap = a.W * kBlockSize;
     t.bad_ctx = C < t.T || C > cap;
@@ -251,7 +299,7 @@ __device__ __forceinline__ bool find_tile(Walker &w, const Args &a, long long x,
         t.n_blocks = t.n_steps = 0;
         return true;
     }
-    const int last_row = min(t.R, t.rt0 + kRows) - 1;
+    const int last_row = min(t.R, pair_rt0 + 2 * kRows) - 1;
     t.n_blocks = (C - t.T + last_row / G) / kBlockSize + 1;
     t.n_steps = (t.n_blocks + kStepBlocks - 1) / kStepBlocks;
     return true;
@@ -276,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kAbort);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rank = (int)cluster_ctarank();
 
     if (tid == 0) {
         prefetch_tensormap(&tm_q);
@@ -283,12 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tm_v);
         for (int i = 0; i < L::NBARS; ++i) {
             const bool by_warps = i == L::S_FREE || i == L::S_FREE + 1 || i == L::P_FULL;
-            mbar_init(&bar[i], by_warps ? kSoftmaxWarps : 1);
+            const bool both_ctas = (i >= L::K_EMPTY && i < L::K_EMPTY + kKStages) ||
+                                   (i >= L::V_EMPTY && i < L::V_EMPTY + kVStages);
+            mbar_init(&bar[i], by_warps ? kSoftmaxWarps : (i >= L::PAIR || both_ctas) ? 2 : 1);
         }
         *abort_flag = 0;
         fence_mbarrier_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kQkWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(sm + L::kTmemSlot)),
                      "r"(kTmemCols)
@@ -296,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers exist before either multicasts into the other
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + L::kTmemSlot);
     griddep_wait();  // queries, tables and the appended chunk may come from the previous kernel
@@ -315,6 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kKWarp || warp == kVWarp) {
         // ---------------------------------------------------------- producers
         const bool is_k = warp == kKWarp;
+        const int NS = is_k ? kKStages : kVStages;
         const CUtensorMap *map = is_k ? &tm_k : &tm_v;
         const uint32_t ring = is_k ? L::kK : L::kV;
         uint64_t *full = &bar[is_k ? L::K_FULL : L::V_FULL];
@@ -322,11 +374,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t policy = l2_policy_evict_normal();
         int gs = 0, qi = 0;
         bool ok = true;
-        for (long long x = blockIdx.x; ok; x += gridDim.x) {
+        for (long long x = blockIdx.x / 2; ok; x += gridDim.x / 2) {
             Tile t;
-            if (!find_tile<G>(wk, a, x, t, lane)) break;
+            if (!find_tile<G>(wk, a, x, rank, t, lane)) break;
             if (t.n_steps == 0) continue;
             if (*abort_flag) break;
+            const int32_t *trow = a.block_tables + (int64_t)t.b * a.W;
+            // block ids (lanes 0..7) one step ahead of the copies: the table read is off the refill path
+            int nxt = lane < kStepBlocks && lane < t.n_blocks ? trow[lane] : -1;
             if (is_k) {  // this tile's queries into Q buffer qi & 1
                 const int qb = qi & 1;
                 if (qi >= 2 && !(ok = wait_all(&bar[L::Q_FREE + qb], ((qi >> 1) + 1) & 1))) break;
@@ -339,207 +394,235 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ++qi;
             }
-            const int32_t *trow = a.block_tables + (int64_t)t.b * a.W;
-            for (int s = 0; s < t.n_steps; ++s, ++gs) {
-                const int st = gs & 1;
-                if (gs >= 2 && !(ok = wait_all(&empty[st], ((gs >> 1) + 1) & 1))) break;
-                const int blk = s * kStepBlocks + lane;
-                bool valid = false;
-                int phys = -1;
-                if (lane < kStepBlocks && blk < t.n_blocks) {
-                    phys = trow[blk];
-                    valid = phys >= 0 && phys < a.num_blocks;
-                    if (!valid && is_k) atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
-                }
-                if (lane == 0) mbar_arrive_expect_tx(&full[st], L::KT);
-                __syncwarp();
-                if (lane < kStepBlocks) {
-                    const int y = valid ? (int)((phys * (int64_t)a.n_kv + t.g) * kBlockSize) : a.oob_row;
-                    uint8_t *dst = sm + ring + st * L::KT + lane * (kBlockSize * 128);
-#pragma unroll
-                    for (int h = 0; h < NH; ++h) tma_load_2d(dst + h * kHalf, map, 64 * h, y, &full[st], policy);
-                }
-            }
-        }
-        // copies still in flight (after an abort) land before the CTA exits
-        for (int st = 0; st < 2 && gs - 1 - st >= 0; ++st) {
-            const int g2 = gs - 1 - st;
-            mbar_wait_bounded(&full[g2 & 1], (g2 >> 1) & 1);
-        }
-        if (is_k && qi > 0) mbar_wait_bounded(&bar[L::Q_FULL + ((qi - 1) & 1)], ((qi - 1) >> 1) & 1);
-        if (is_k && qi > 1) mbar_wait_bounded(&bar[L::Q_FULL + ((qi - 2) & 1)], ((qi - 2) >> 1) & 1);
-        if (!ok) set_abort();
-    } else if (warp == kMmaWarp) {
-        // ---------------------------------------------------------- MMA issue
-        constexpr uint32_t idesc_qk = mma_idesc(kRows, kKeys, 0);
-        constexpr uint32_t idesc_pv = mma_idesc(kRows, D, 1);
-        const uint32_t base = smem_u32(sm);
-        int gs = 0, qi = 0;
-        int pv_gs = -1;
-        bool pv_acc = false, ok = true;
-        auto issue_pv = [&](int g2, bool acc) -> bool {
-            if (!wait_all(&bar[L::P_FULL], g2 & 1)) return false;
-            if (!wait_all(&bar[L::V_FULL + (g2 & 1)], (g2 >> 1) & 1)) return false;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t pb = base + L::kP, vb = base + L::kV + (g2 & 1) * L::KT;
-#pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    const uint64_t ad = smem_desc(pb + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = smem_desc(vb + kk * 2048, kHalf, 1024);
-                    umma(tmem + kColO, ad, bd, idesc_pv, (acc || kk > 0) ? 1u : 0u);
-                }
-                umma_commit(&bar[L::O_DONE]);
-                umma_commit(&bar[L::V_EMPTY + (g2 & 1)]);
-            }
-            __syncwarp();
-            return true;
-        };
-        for (long long x = blockIdx.x; ok; x += gridDim.x) {
-            Tile t;
-            if (!find_tile<G>(wk, a, x, t, lane)) break;
-            if (t.n_steps == 0) continue;
-            if (*abort_flag) break;
-            const int qb = qi & 1;
-            if (!(ok = wait_all(&bar[L::Q_FULL + qb], (qi >> 1) & 1))) break;
-            for (int s = 0; s < t.n_steps && ok; ++s, ++gs) {
-                const int st = gs & 1;
-                if (!(ok = wait_all(&bar[L::K_FULL + st], (gs >> 1) & 1))) break;
-                if (gs >= 2 && !(ok = wait_all(&bar[L::S_FREE + st], ((gs >> 1) + 1) & 1))) break;
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t qbase = base + L::kQ + qb * L::QT, kbase = base + L::kK + st * L::KT;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                        umma(tmem + st * kKeys, smem_desc(qbase + off, 16, 1024), smem_desc(kbase + off, 16, 1024),
-                             idesc_qk, kk > 0 ? 1u : 0u);
-                    }
-                    umma_commit(&bar[L::S_FULL + st]);
-                    umma_commit(&bar[L::K_EMPTY + st]);
-                    if (s == t.n_steps - 1) umma_commit(&bar[L::Q_FREE + qb]);
-                }
-                __syncwarp();
-                if (pv_gs >= 0 && !(ok = issue_pv(pv_gs, pv_acc))) break;
-                pv_gs = gs;
-                pv_acc = s > 0;
-            }
-            ++qi;
-        }
-        if (ok && pv_gs >= 0) ok = issue_pv(pv_gs, pv_acc);
-        // every MMA issued so far has completed before the tensor memory is released
-        if (lane == 0) umma_commit(&bar[L::DRAIN]);
-        __syncwarp();
-        mbar_wait_bounded(&bar[L::DRAIN], 0);
-        if (!ok) set_abort();
-    } else {
-        // ---------------------------------------------------------- softmax
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        uint8_t *prow = sm + L::kP;
-        int gs = 0;
-        bool ok = true;
-        for (long long x = blockIdx.x; ok; x += gridDim.x) {
-            Tile t;
-            if (!find_tile<G>(wk, a, x, t, lane)) break;
-            if (t.bad_ctx && tid == 0 && t.rt0 == 0 && t.g == 0) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
-            if (t.n_steps == 0) continue;
-            if (*abort_flag) break;
-            const int r = t.rt0 + tid;
-            const int64_t orow_i = (int64_t)t.row0 + min(r, t.R - 1) / G;  // this row's query token
-            const bool in_out = orow_i >= 0 && orow_i < a.n_rows;
-            if (r < t.R && !in_out) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
-            const bool live = r < t.R && in_out;
-            const int pos = t.C - t.T + min(r, t.R - 1) / G;  // this row's position; it sees keys 0 .. pos
-            float mref = -INFINITY, l = 0.0f;
-            // block ids of the next step (lanes 0..7), read one step ahead: the same
-            // validity test as the producers, so a masked block is exactly a skipped one
-            const int32_t *trow = a.block_tables + (int64_t)t.b * a.W;
-            int nxt = lane < kStepBlocks && lane < t.n_blocks ? trow[lane] : -1;
             for (int s = 0; s < t.n_steps; ++s, ++gs) {
                 const int cur = nxt;
                 const int nb = (s + 1) * kStepBlocks + lane;
                 if (s + 1 < t.n_steps) nxt = lane < kStepBlocks && nb < t.n_blocks ? trow[nb] : -1;
-                const uint32_t mask = __ballot_sync(kFull, cur >= 0 && cur < a.num_blocks) & ((1u << kStepBlocks) - 1);
+                const int st = gs % NS, use = gs / NS;
+                if (use > 0 && !(ok = wait_all(&empty[st], (use - 1) & 1))) break;
+                const bool present = lane < kStepBlocks && s * kStepBlocks + lane < t.n_blocks;
+                const bool valid = present && cur >= 0 && cur < a.num_blocks;
+                if (present && !valid && is_k && lane / (kStepBlocks / 2) == rank) atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
+                if (lane == 0) mbar_arrive_expect_tx(&full[st], L::KT);
+                __syncwarp();
+                if (lane < kStepBlocks && lane / (kStepBlocks / 2) == rank) {  // this CTA's half, into both
+                    const int y = valid ? (int)((cur * (int64_t)a.n_kv + t.g) * kBlockSize) : a.oob_row;
+                    uint8_t *dst = sm + ring + st * L::KT + lane * (kBlockSize * 128);
+#pragma unroll
+                    for (int h = 0; h < NH; ++h)
+                        tma_load_2d_mc(dst + h * kHalf, map, 64 * h, y, &full[st], (uint16_t)0x3, policy);
+                }
+            }
+        }
+        // copies still in flight (after an abort) land before the CTA exits
+        for (int j = 1; j <= NS && gs - j >= 0; ++j) {
+            const int g2 = gs - j;
+            mbar_wait_bounded(&full[g2 % NS], (g2 / NS) & 1);
+        }
+        if (is_k && qi > 0) mbar_wait_bounded(&bar[L::Q_FULL + ((qi - 1) & 1)], ((qi - 1) >> 1) & 1);
+        if (is_k && qi > 1) mbar_wait_bounded(&bar[L::Q_FULL + ((qi - 2) & 1)], ((qi - 2) >> 1) & 1);
+        if (!ok) set_abort();
+    } else if (warp == kQkWarp || warp == kPvWarp) {
+        // ---------------------------------------------------------- MMA issue
+        // Two issuing warps, so that neither's waits and commits hold up the
+        // other: S = Q K^T runs up to two steps ahead (as far as the two S
+        // accumulators allow), O += P V starts as soon as a step's P is in
+        // tensor memory.  Each warp commits, and finally drains, its own MMAs.
+        const bool is_qk = warp == kQkWarp;
+        constexpr uint32_t idesc_qk = mma_idesc(kRows, kKeys, 0);
+        constexpr uint32_t idesc_pv = mma_idesc(kRows, D, 1);
+        const uint32_t base = smem_u32(sm);
+        int gs = 0, qi = 0;
+        bool ok = true;
+        for (long long x = blockIdx.x / 2; ok; x += gridDim.x / 2) {
+            Tile t;
+            if (!find_tile<G>(wk, a, x, rank, t, lane)) break;
+            if (t.n_steps == 0) continue;
+            if (*abort_flag) break;
+            const int qb = qi & 1;
+            if (is_qk && !(ok = wait_all(&bar[L::Q_FULL + qb], (qi >> 1) & 1))) break;
+            for (int s = 0; s < t.n_steps && ok; ++s, ++gs) {
+                if (is_qk) {
+                    const int st = gs & 1, kst = gs % kKStages;
+                    if (!(ok = wait_all(&bar[L::K_FULL + kst], (gs / kKStages) & 1))) break;
+                    if (gs >= 2 && !(ok = wait_all(&bar[L::S_FREE + st], ((gs >> 1) + 1) & 1))) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t qbase = base + L::kQ + qb * L::QT, kbase = base + L::kK + kst * L::KT;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                            umma(tmem + st * kKeys, smem_desc(qbase + off, 16, 1024),
+                                 smem_desc(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        umma_commit(&bar[L::S_FULL + st]);
+                        umma_commit_mc(&bar[L::K_EMPTY + kst], (uint16_t)0x3);
+                        if (s == t.n_steps - 1) umma_commit(&bar[L::Q_FREE + qb]);
+                    }
+                } else {
+                    const int vst = gs % kVStages;
+                    if (!(ok = wait_all(&bar[L::P_FULL], gs & 1))) break;
+                    if (!(ok = wait_all(&bar[L::V_FULL + vst], (gs / kVStages) & 1))) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t vb = base + L::kV + vst * L::KT;
+#pragma unroll
+                        for (int kk = 0; kk < kKeys / 16; ++kk) {
+                            const uint32_t at = tmem + kColP + 8 * kk;  // keys 16 kk .. 16 kk + 15 of P
+                            const uint64_t bd = smem_desc(vb + kk * 2048, kHalf, 1024);
+                            umma_ts(tmem + kColO, at, bd, idesc_pv, (s > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        umma_commit(&bar[L::O_DONE]);
+                        umma_commit_mc(&bar[L::V_EMPTY + vst], (uint16_t)0x3);
+                    }
+                }
+                __syncwarp();
+            }
+            ++qi;
+        }
+        // every MMA this warp issued has completed before the tensor memory is released
+        uint64_t *drain = &bar[L::DRAIN + (is_qk ? 0 : 1)];
+        if (lane == 0) umma_commit(drain);
+        __syncwarp();
+        mbar_wait_bounded(drain, 0);
+        if (!ok) set_abort();
+    } else {
+        // ---------------------------------------------------------- softmax
+        // warp w: TMEM lanes (rows) 32 (w & 3) .. + 31, keys 64 (w >> 2) .. + 63 of every step,
+        // and the same half of O's columns
+        constexpr int HK = kKeys / 2, HD = D / 2;
+        const int quarter = warp & 3, ch = warp >> 2;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t col_red = kColO + D;
+        uint64_t *pair = &bar[L::PAIR + quarter];
+        int pph = 0;  // exchanges with the partner warp so far (the pair barrier's phase)
+        // one per-row value each way with the partner warp; false on a timeout
+        auto exchange = [&](float mine, float &theirs) -> bool {
+            const uint32_t rc = tmem + lane_off + col_red + 2 * (pph & 1);
+            tmem_st1(rc + ch, __float_as_uint(mine));
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pair);
+            if (!wait_all(pair, pph & 1)) return false;
+            ++pph;
+            tc_fence_after();
+            uint32_t v;
+            tmem_ld1(rc + (ch ^ 1), &v);
+            tmem_wait_ld();
+            theirs = __uint_as_float(v);
+            return true;
+        };
+        int gs = 0;
+        bool ok = true;
+        for (long long x = blockIdx.x / 2; ok; x += gridDim.x / 2) {
+            Tile t;
+            if (!find_tile<G>(wk, a, x, rank, t, lane)) break;
+            if (t.bad_ctx && tid == 0 && t.rt0 == 0 && t.g == 0) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
+            if (t.n_steps == 0) continue;
+            if (*abort_flag) break;
+            const int r = t.rt0 + row;
+            const int64_t orow_i = (int64_t)t.row0 + min(r, t.R - 1) / G;  // this row's query token
+            const bool in_out = orow_i >= 0 && orow_i < a.n_rows;
+            if (r < t.R && !in_out && ch == 0) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
+            const bool live = r < t.R && in_out;
+            const int pos = t.C - t.T + min(r, t.R - 1) / G;  // this row's position; it sees keys 0 .. pos
+            float mref = -INFINITY;
+            float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // this half's row sum of the bf16-rounded P
+            // block ids of this warp's 4 blocks of the next step (lanes 0..3), read one step ahead:
+            // the same validity test as the producers, so a masked block is exactly a skipped one
+            constexpr int QB = kStepBlocks / 2;
+            const int32_t *trow = a.block_tables + (int64_t)t.b * a.W;
+            int nxt = lane < QB && ch * QB + lane < t.n_blocks ? trow[ch * QB + lane] : -1;
+            for (int s = 0; s < t.n_steps; ++s, ++gs) {
+                const int cur = nxt;
+                const int nb = (s + 1) * kStepBlocks + ch * QB + lane;
+                if (s + 1 < t.n_steps) nxt = lane < QB && nb < t.n_blocks ? trow[nb] : -1;
+                const uint32_t mask = __ballot_sync(kFull, lane < QB && cur >= 0 && cur < a.num_blocks) & ((1u << QB) - 1);
                 const int sb = gs & 1;
                 if (!(ok = wait_all(&bar[L::S_FULL + sb], (gs >> 1) & 1))) break;
                 tc_fence_after();
-                uint32_t sr[kKeys];
+                uint32_t sr[HK];
 #pragma unroll
-                for (int c = 0; c < kKeys / 32; ++c) tmem_ld32(tmem + lane_off + sb * kKeys + 32 * c, sr + 32 * c);
+                for (int c = 0; c < HK / 32; ++c) tmem_ld32(tmem + lane_off + sb * kKeys + ch * HK + 32 * c, sr + 32 * c);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[L::S_FREE + sb]);
 
-                const int key0 = s * kKeys;
-                float bm = -INFINITY;
-                if (mask == (1u << kStepBlocks) - 1 && key0 + kKeys - 1 <= pos) {
+                const int key0 = s * kKeys + ch * HK;  // position of this warp's first key
+                if (!(mask == (1u << QB) - 1 && key0 + HK - 1 <= pos)) {
 #pragma unroll
-                    for (int k = 0; k < kKeys; ++k) bm = fmaxf(bm, __uint_as_float(sr[k]));
-                } else {
-#pragma unroll
-                    for (int k = 0; k < kKeys; ++k) {
+                    for (int k = 0; k < HK; ++k) {
                         const bool vis = ((mask >> (k / kBlockSize)) & 1u) && key0 + k <= pos;
                         if (!vis) sr[k] = __float_as_uint(-INFINITY);
-                        bm = fmaxf(bm, __uint_as_float(sr[k]));
                     }
                 }
+                float m4[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) m4[i] = __uint_as_float(sr[i]);
+#pragma unroll
+                for (int k = 8; k < HK; ++k) m4[k & 7] = fmaxf(m4[k & 7], __uint_as_float(sr[k]));
+                const float bm_half = fmaxf(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])),
+                                            fmaxf(fmaxf(m4[4], m4[5]), fmaxf(m4[6], m4[7])));
+                // the row maximum over both halves
+                float bm_other;
+                if (!(ok = exchange(bm_half, bm_other))) break;
+                const float bm = fmaxf(bm_half, bm_other);
                 const float bms = bm * a.qscale;
                 const bool resc = bms > mref + kRescaleSlack;
                 float alpha = 1.0f;
                 if (resc) {
                     alpha = ex2(mref - bms);  // 0 when mref is -inf
                     mref = bms;
-                    l *= alpha;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) l4[i] *= alpha;
                 }
                 const float nm = mref == -INFINITY ? 0.0f : -mref;
-                uint32_t pk[kKeys / 2];
+                uint32_t pk[HK / 2];
 #pragma unroll
-                for (int i = 0; i < kKeys / 2; ++i) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), a.qscale, nm));
-                    const float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), a.qscale, nm));
-                    pk[i] = pack_bf16x2(p0, p1);
-                    l += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+                for (int i = 0; i < HK / 2; ++i) {
+                    pk[i] = pack_bf16x2(ex2(fmaf(__uint_as_float(sr[2 * i]), a.qscale, nm)),
+                                        ex2(fmaf(__uint_as_float(sr[2 * i + 1]), a.qscale, nm)));
+                    l4[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
                 }
                 if (s > 0) {  // the previous step's O += P V has finished: P is free, O is current
                     if (!(ok = wait_all(&bar[L::O_DONE], (gs - 1) & 1))) break;
                     tc_fence_after();
                     if (__any_sync(kFull, resc)) {
 #pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
+                        for (int c = 0; c < HD / 32; ++c) {
                             uint32_t o[32];
-                            tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
+                            tmem_ld32(tmem + lane_off + kColO + ch * HD + 32 * c, o);
                             tmem_wait_ld();
 #pragma unroll
                             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                            tmem_st32(tmem + lane_off + kColO + 32 * c, o);
+                            tmem_st32(tmem + lane_off + kColO + ch * HD + 32 * c, o);
                         }
                         tmem_wait_st();
                     }
                 }
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint32_t *v = pk + 32 * h + 4 * c;
-                        *reinterpret_cast<uint4 *>(prow + h * kHalf + swz_off(tid, c)) =
-                            make_uint4(v[0], v[1], v[2], v[3]);
-                    }
-                fence_proxy_async_smem();
+                tmem_st32(tmem + lane_off + kColP + ch * (HK / 2), pk);
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[L::P_FULL]);
             }
             if (!ok) break;
-            // epilogue: O / l for this tile's rows
+            // epilogue: O / l for this tile's rows, this warp's half of the columns
             if (!(ok = wait_all(&bar[L::O_DONE], (gs - 1) & 1))) break;
             tc_fence_after();
+            const float l_half = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+            float l_other;
+            if (!(ok = exchange(l_half, l_other))) break;
+            const float l = l_half + l_other;
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-            __nv_bfloat16 *orow = a.out + ((in_out ? orow_i : 0) * a.n_q + t.g * G + min(r, t.R - 1) % G) * D;
+            __nv_bfloat16 *orow = a.out + ((in_out ? orow_i : 0) * a.n_q + t.g * G + min(r, t.R - 1) % G) * D + ch * HD;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < HD / 32; ++c) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_off + kColO + 32 * c, o);
+                tmem_ld32(tmem + lane_off + kColO + ch * HD + 32 * c, o);
                 tmem_wait_ld();
                 if (live) {
 #pragma unroll
@@ -559,9 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();  // no copy or arrival from the partner is still on its way into this CTA
     tc_fence_after();
-    if (warp == kMmaWarp)
+    if (warp == kQkWarp)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
@@ -571,20 +654,36 @@ pkv_status launch(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, const 
     using L = Layout<D>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
+    static int max_clusters = 0;  // clusters of two that fit on the device at once
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)L::bytes);
+        if (attr_err != cudaSuccess) return;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * std::max(1, pool->num_sms / 2));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = L::bytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, prefill_tc_kernel<D, G>, &cfg);
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "prefill kernel attributes");
+    if (max_clusters < 1) return fail(PKV_ECUDA, "prefill: no cluster of two CTAs fits on the device");
     CUtensorMap tm_q;
     pkv_status st = make_q_map(&tm_q, q, n_rows, n_q, D, G, kRows / G);
     if (st != PKV_OK) return st;
-    // an upper bound on the tiles: every sequence may end with a partial row tile
-    const int64_t tiles = ((n_rows * G + kRows - 1) / kRows + a.batch) * a.n_kv;
-    const int grid = (int)std::min<int64_t>(tiles, std::max(1, pool->num_sms));
+    // an upper bound on the row-tile pairs (every sequence may end with a partial tile);
+    // clusters of two CTAs, one cluster per pair of SMs
+    const int64_t pairs = ((n_rows * G + kRows - 1) / kRows + a.batch) * a.n_kv;
+    const int grid = 2 * (int)std::min<int64_t>(pairs, max_clusters);
     LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl(prefill_tc_kernel<D, G>, dim3(grid), dim3(kThreads), L::bytes, s, tm_q, pool->tm_k,
-                               pool->tm_v, a);
+    cudaError_t e = launch_pdl_cluster(prefill_tc_kernel<D, G>, dim3(grid), dim3(kThreads), L::bytes, 2, s, tm_q,
+                                       pool->tm_k, pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return PKV_OK;
