@@ -56,7 +56,7 @@ constexpr float kRescaleSlack = 8.0f;    // log2 of the largest P value allowed 
 constexpr uint32_t kTmemCols = 512;      // S0 at 0, S1 at 128, O at 256, P at 448
 constexpr uint32_t kColO = 256;
 constexpr uint32_t kColP = 448;          // P as bf16 pairs: column j holds keys 2j (low half) and 2j + 1
-constexpr int kKStages = 3, kVStages = 2;
+constexpr int kKStages = 2, kVStages = 2;
 // after O: four columns through which the two warps that own a lane quarter
 // exchange per-row values (their key halves' maxima, and at the end their
 // halves of the row sum), [phase parity][half]
@@ -83,10 +83,12 @@ struct Layout {
     static constexpr uint32_t kQ = 0;                    // 2 Q buffers
     static constexpr uint32_t kK = kQ + 2 * QT;          // K stages
     static constexpr uint32_t kV = kK + kKStages * KT;   // V stages
-    static constexpr uint32_t kBar = kV + kVStages * KT;
+    static constexpr uint32_t kOut = kV + kVStages * KT;  // the finished tile, staged for coalesced stores
+    static constexpr uint32_t kBar = kOut + QT;
     enum { Q_FULL = 0, Q_FREE = 2, K_FULL = 4, K_EMPTY = 4 + kKStages, V_FULL = 4 + 2 * kKStages,
            V_EMPTY = V_FULL + kVStages, S_FULL = V_EMPTY + kVStages, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2,
-           O_DONE = P_FULL + 1, DRAIN = O_DONE + 1, PAIR = DRAIN + 2, NBARS = PAIR + 4 };  // DRAIN + issuer, PAIR + lane quarter
+           O_DONE = P_FULL + 1, DRAIN = O_DONE + 1, OUT_FULL = DRAIN + 2, OUT_FREE = OUT_FULL + 1,
+           PAIR = OUT_FREE + 1, NBARS = PAIR + 4 };  // DRAIN + issuer, PAIR + lane quarter
     static constexpr uint32_t kTmemSlot = kBar + NBARS * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kEnd = kAbort + 4;
@@ -214,6 +216,15 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+// acc += the two bf16 halves of `pk` (each widened exactly, added in fp32).
+__device__ __forceinline__ void add_bf16x2_to(float &acc, uint32_t pk)
+{
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %0, hi, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(pk));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;
@@ -234,31 +245,29 @@ struct Tile {
 // A window of 32 sequences held one per lane: each warp walks the tile list
 // itself, with the same arithmetic, so every role sees the same tiles.
 struct Walker {
-    int wb = 0;           // first sequence of the window
-    long long wbase = 0;  // tiles before sequence wb
-    long long incl = 0, tot = 0;
-    int n = 0, row0 = 0, T = 0, C = 0;
+    int wb = 0;     // first sequence of the window
+    int wbase = 0;  // pairs before sequence wb
+    int incl = 0, tot = 0;
+    int ph = 0, row0 = 0, T = 0, C = 0;  // this lane's sequence: pairs per KV head, rows, context
 };
 
 template <int G>
 __device__ __forceinline__ void load_window(Walker &w, const Args &a, int lane)
 {
     const int bl = w.wb + lane;
-    w.row0 = w.T = w.C = 0;
-    long long n = 0;
+    w.row0 = w.T = w.C = w.ph = 0;
     if (bl < a.batch) {
         w.row0 = a.qo_indptr[bl];
         w.T = a.qo_indptr[bl + 1] - w.row0;
         w.C = a.context_lens[bl];
-        if (w.T > 0) n = (long long)a.n_kv * ((((long long)w.T * G + kRows - 1) / kRows + 1) / 2);
+        if (w.T > 0) w.ph = ((w.T * G + kRows - 1) / kRows + 1) / 2;
     }
-    long long x = n;
+    int x = w.ph * a.n_kv;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(kFull, x, o);
+        const int y = __shfl_up_sync(kFull, x, o);
         if (lane >= o) x += y;
     }
-    w.n = (int)n;
     w.incl = x;
     w.tot = __shfl_sync(kFull, x, 31);
 }
@@ -269,7 +278,7 @@ __device__ __forceinline__ void load_window(Walker &w, const Args &a, int lane)
 // keeps step with its partner).  Both CTAs stream the blocks the pair's last
 // row reaches.  False past the list's end.  Warp-wide, uniform result.
 template <int G>
-__device__ __forceinline__ bool find_tile(Walker &w, const Args &a, long long x, int rank, Tile &t, int lane)
+__device__ __forceinline__ bool find_tile(Walker &w, const Args &a, int x, int rank, Tile &t, int lane)
 {
     while (x >= w.wbase + w.tot) {
         if (w.wb + 32 >= a.batch) return false;
@@ -279,16 +288,15 @@ __device__ __forceinline__ bool find_tile(Walker &w, const Args &a, long long x,
     }
     const unsigned hit = __ballot_sync(kFull, w.wbase + w.incl > x);
     const int l = __ffs(hit) - 1;
-    const long long before = __shfl_sync(kFull, w.incl - w.n, l);
-    const int n = __shfl_sync(kFull, w.n, l);
+    const int ph = __shfl_sync(kFull, w.ph, l);
+    const int before = __shfl_sync(kFull, w.incl - w.ph * a.n_kv, l);
     t.b = w.wb + l;
     t.row0 = __shfl_sync(kFull, w.row0, l);
     t.T = __shfl_sync(kFull, w.T, l);
     int C = __shfl_sync(kFull, w.C, l);
-    const int per_head = n / a.n_kv;
-    const int within = (int)(x - w.wbase - before);
-    t.g = within / per_head;
-    const int pair_rt0 = 2 * (within % per_head) * kRows;
+    const int within = x - w.wbase - before;
+    t.g = within / ph;
+    const int pair_rt0 = 2 * (within - t.g * ph) * kRows;
     t.rt0 = pair_rt0 + rank * kRows;
     t.R = t.T * G;
     const int cap = a.W * kBlockSize;
@@ -331,7 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         for (int i = 0; i < L::NBARS; ++i) {
-            const bool by_warps = i == L::S_FREE || i == L::S_FREE + 1 || i == L::P_FULL;
+            const bool by_warps = i == L::S_FREE || i == L::S_FREE + 1 || i == L::P_FULL || i == L::OUT_FULL ||
+                                  i == L::OUT_FREE;
             const bool both_ctas = (i >= L::K_EMPTY && i < L::K_EMPTY + kKStages) ||
                                    (i >= L::V_EMPTY && i < L::V_EMPTY + kVStages);
             mbar_init(&bar[i], by_warps ? kSoftmaxWarps : (i >= L::PAIR || both_ctas) ? 2 : 1);
@@ -374,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t policy = l2_policy_evict_normal();
         int gs = 0, qi = 0;
         bool ok = true;
-        for (long long x = blockIdx.x / 2; ok; x += gridDim.x / 2) {
+        for (int x = blockIdx.x / 2; ok; x += gridDim.x / 2) {
             Tile t;
             if (!find_tile<G>(wk, a, x, rank, t, lane)) break;
             if (t.n_steps == 0) continue;
@@ -434,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t base = smem_u32(sm);
         int gs = 0, qi = 0;
         bool ok = true;
-        for (long long x = blockIdx.x / 2; ok; x += gridDim.x / 2) {
+        for (int x = blockIdx.x / 2; ok; x += gridDim.x / 2) {
             Tile t;
             if (!find_tile<G>(wk, a, x, rank, t, lane)) break;
             if (t.n_steps == 0) continue;
@@ -514,31 +523,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             theirs = __uint_as_float(v);
             return true;
         };
-        int gs = 0;
+        constexpr int QB = kStepBlocks / 2;  // blocks of a step in this warp's key half
+        // this warp's block ids of step 0 of tile t (lanes 0..QB-1)
+        auto first_ids = [&](const Tile &t) -> int {
+            return lane < QB && ch * QB + lane < t.n_blocks ? a.block_tables[(int64_t)t.b * a.W + ch * QB + lane] : -1;
+        };
+        int gs = 0, n_out = 0;  // steps so far, tiles written out so far
         bool ok = true;
-        for (long long x = blockIdx.x / 2; ok; x += gridDim.x / 2) {
-            Tile t;
-            if (!find_tile<G>(wk, a, x, rank, t, lane)) break;
+        int x = blockIdx.x / 2;
+        Tile t, tn;
+        bool have = find_tile<G>(wk, a, x, rank, t, lane);
+        int nxt = have ? first_ids(t) : -1;
+        while (have && ok) {
+            // the next tile and its first block ids are found while this one runs
+            const bool have_n = find_tile<G>(wk, a, x + gridDim.x / 2, rank, tn, lane);
             if (t.bad_ctx && tid == 0 && t.rt0 == 0 && t.g == 0) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
-            if (t.n_steps == 0) continue;
-            if (*abort_flag) break;
+            if (t.n_steps == 0 || *abort_flag) {
+                if (*abort_flag) break;
+                x += gridDim.x / 2;
+                t = tn;
+                have = have_n;
+                nxt = have ? first_ids(t) : -1;
+                continue;
+            }
             const int r = t.rt0 + row;
             const int64_t orow_i = (int64_t)t.row0 + min(r, t.R - 1) / G;  // this row's query token
             const bool in_out = orow_i >= 0 && orow_i < a.n_rows;
             if (r < t.R && !in_out && ch == 0) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
-            const bool live = r < t.R && in_out;
             const int pos = t.C - t.T + min(r, t.R - 1) / G;  // this row's position; it sees keys 0 .. pos
             float mref = -INFINITY;
             float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // this half's row sum of the bf16-rounded P
-            // block ids of this warp's 4 blocks of the next step (lanes 0..3), read one step ahead:
-            // the same validity test as the producers, so a masked block is exactly a skipped one
-            constexpr int QB = kStepBlocks / 2;
+            // block ids of this warp's 4 blocks of the next step (lanes 0..3), read one step ahead
+            // (for the last step: the next tile's first ids): the same validity test as the
+            // producers, so a masked block is exactly a skipped one
             const int32_t *trow = a.block_tables + (int64_t)t.b * a.W;
-            int nxt = lane < QB && ch * QB + lane < t.n_blocks ? trow[ch * QB + lane] : -1;
             for (int s = 0; s < t.n_steps; ++s, ++gs) {
                 const int cur = nxt;
                 const int nb = (s + 1) * kStepBlocks + ch * QB + lane;
                 if (s + 1 < t.n_steps) nxt = lane < QB && nb < t.n_blocks ? trow[nb] : -1;
+                else nxt = have_n ? first_ids(tn) : -1;
                 const uint32_t mask = __ballot_sync(kFull, lane < QB && cur >= 0 && cur < a.num_blocks) & ((1u << QB) - 1);
                 const int sb = gs & 1;
                 if (!(ok = wait_all(&bar[L::S_FULL + sb], (gs >> 1) & 1))) break;
@@ -585,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < HK / 2; ++i) {
                     pk[i] = pack_bf16x2(ex2(fmaf(__uint_as_float(sr[2 * i]), a.qscale, nm)),
                                         ex2(fmaf(__uint_as_float(sr[2 * i + 1]), a.qscale, nm)));
-                    l4[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+                    add_bf16x2_to(l4[i & 3], pk[i]);
                 }
                 if (s > 0) {  // the previous step's O += P V has finished: P is free, O is current
                     if (!(ok = wait_all(&bar[L::O_DONE], (gs - 1) & 1))) break;
@@ -618,13 +641,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = exchange(l_half, l_other))) break;
             const float l = l_half + l_other;
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-            __nv_bfloat16 *orow = a.out + ((in_out ? orow_i : 0) * a.n_q + t.g * G + min(r, t.R - 1) % G) * D + ch * HD;
+            if (t.rt0 < t.R) {  // (a pair's second tile may hold no rows)
+                // this warp's half row of O / l into the staging tile, 16-byte chunks
+                // swizzled within each 128-byte half row (conflict-free writes and reads)
+                constexpr int RB = D * 2;  // bytes of an output row
+                uint8_t *stage = sm + L::kOut;
+                if (n_out > 0 && !(ok = wait_all(&bar[L::OUT_FREE], (n_out - 1) & 1))) break;
 #pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tmem + lane_off + kColO + ch * HD + 32 * c, o);
-                tmem_wait_ld();
-                if (live) {
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_off + kColO + ch * HD + 32 * c, o);
+                    tmem_wait_ld();
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint4 w;
@@ -632,11 +659,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                         w.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
                         w.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
                         w.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(orow + 32 * c + 8 * q4) = w;
+                        const int chunk = (ch * HD + 32 * c + 8 * q4) / 8;  // 16-byte chunk of the row
+                        *reinterpret_cast<uint4 *>(stage + row * RB + ((chunk >> 3) << 7) +
+                                                   (((chunk & 7) ^ (row & 7)) << 4)) = w;
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[L::OUT_FULL]);
+                if (!(ok = wait_all(&bar[L::OUT_FULL], n_out & 1))) break;
+                // coalesced: consecutive threads store consecutive 16-byte chunks of a row
+                constexpr int CPR = RB / 16;  // chunks per row
+                for (int i = warp * 32 + lane; i < kRows * CPR; i += kSoftmaxWarps * 32) {
+                    const int rr = i / CPR, chunk = i % CPR;
+                    const int rg = t.rt0 + rr;
+                    const int64_t tok = (int64_t)t.row0 + rg / G;
+                    if (rg < t.R && tok >= 0 && tok < a.n_rows) {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(stage + rr * RB + ((chunk >> 3) << 7) +
+                                                                         (((chunk & 7) ^ (rr & 7)) << 4));
+                        *reinterpret_cast<uint4 *>(a.out + (tok * a.n_q + t.g * G + rg % G) * D + chunk * 8) = w;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[L::OUT_FREE]);
+                ++n_out;
             }
             tc_fence_before();
+            x += gridDim.x / 2;
+            t = tn;
+            have = have_n;
         }
         if (!ok) set_abort();
     }
@@ -680,6 +730,8 @@ pkv_status launch(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, const 
     // an upper bound on the row-tile pairs (every sequence may end with a partial tile);
     // clusters of two CTAs, one cluster per pair of SMs
     const int64_t pairs = ((n_rows * G + kRows - 1) / kRows + a.batch) * a.n_kv;
+    if (pairs > INT32_MAX || n_rows * G > INT32_MAX)
+        return fail(PKV_EUNSUPPORTED, "paged_prefill_attention: too many query rows");
     const int grid = 2 * (int)std::min<int64_t>(pairs, max_clusters);
     LaunchScope ls(pool, kDecode, s);
     cudaError_t e = launch_pdl_cluster(prefill_tc_kernel<D, G>, dim3(grid), dim3(kThreads), L::bytes, 2, s, tm_q,
