@@ -1641,390 +1641,33 @@ namespace pkv {
 //
 // "Memory Management in LLM Serving Systems", "Prefix sharing": storing a
 // shared prefix once turns decode-time reads of n copies into one.  Stage 1
-// (prefix_kernel) attends all batch x G query rows of a KV head to the prefix
-// in one pass over its K and V tiles -- a real dense contraction, so the query
-// rows are the M dimension of 16x8x16 MMAs -- and stores a (max, sum, O)
-// partial per 256-token chunk of the prefix.  Stage 2 is the decode kernel
-// started past the prefix blocks; it merges its pieces with these partials.
-
-constexpr int kPrefixWarps = 4;       // 16 query rows per warp
-constexpr int kPrefixRows = kPrefixWarps * 16;
-constexpr int kPrefixStages = 8;      // ring stages: four 2-block steps in flight
-constexpr int kPrefixMaxChunk = 1024; // blocks per chunk at most (the chunk's table is staged in smem)
-
-struct PrefixArgs {
-    const __nv_bfloat16 *q;
-    int n_q, n_kv, batch;
-    const int32_t *prefix_blocks;
-    int n_prefix_blocks, chunk_blocks, cluster;  // cluster: chunks reduced together (CTAs per cluster)
-    int64_t num_blocks;
-    float qscale;
-    float2 *ws_ml;
-    float *ws_o;
-    int64_t pre_base;
-    unsigned *err;
-};
-
-// Shared memory of the prefix kernel: the copy ring, which after streaming
-// holds this CTA's partial O [kPrefixRows][D] fp32 for the cluster
-// reduction, then the partial (m, l) per row, the stage barriers, the stage
-// block ids and the chunk's block table.
-template <int D>
-struct PrefixSmem {
-    using Gm = Geo<D, false>;
-    static constexpr int kRing = std::max(kPrefixStages * Gm::STAGE, kPrefixRows * D * 4);
-    static constexpr int kMl = kRing;
-    static constexpr int kBars = kMl + kPrefixRows * 8;
-    static constexpr int kPhys = kBars + kPrefixStages * 8;
-    static constexpr int kW = kPhys + kPrefixStages * 4;  // [kPrefixRows][8] weights, then [kPrefixRows] (M, L)
-    static constexpr int kTab = kW + kPrefixRows * 8 * 4 + kPrefixRows * 8;
-    static size_t bytes(int chunk_blocks) { return 1024 + (size_t)kTab + 4 * (size_t)chunk_blocks; }
-};
-
-// Stage 1 of cascade decode: the partial attention of every query row of KV
-// head g (row r = query head g*G + r%G of sequence r/G) over the shared
-// prefix.  The prefix is cut into chunks; CTA (chunk, g, row tile) streams
-// its chunk's tiles once for 64 rows (4 warps x 16) with the rows as the MMA
-// M dimension: S = Q K^T (K tile as the B operand), P V with P from the score
-// accumulators.  Two blocks (32 tokens) per softmax step.  The chunks of a
-// thread-block cluster then combine their partials through distributed
-// shared memory, each CTA reducing a share of the rows, so that one (m, l, O)
-// per row and cluster reaches the workspace for the merge kernel.
-template <int D, int G>
-__global__ void __launch_bounds__(kPrefixWarps * 32, 3)
-    prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, PrefixArgs a)
-{
-    using Gm = Geo<D, false>;
-    using L = PrefixSmem<D>;
-    constexpr int NT = D / 16;
-    constexpr int S = kPrefixStages;
-    extern __shared__ __align__(1024) uint8_t prefix_smem[];
-    uint8_t *sm = prefix_smem + ((1024u - (smem_u32(prefix_smem) & 1023u)) & 1023u);
-    uint8_t *ring = sm;
-    float *part = reinterpret_cast<float *>(sm);  // [kPrefixRows][D], after streaming
-    float2 *part_ml = reinterpret_cast<float2 *>(sm + L::kMl);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::kBars);
-    int *phys_st = reinterpret_cast<int *>(sm + L::kPhys);
-    int *tab = reinterpret_cast<int *>(sm + L::kTab);
-    float(*wgt)[8] = reinterpret_cast<float(*)[8]>(sm + L::kW);
-    float2 *row_ml = reinterpret_cast<float2 *>(sm + L::kW + kPrefixRows * 8 * 4);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g8 = lane >> 2, c4 = lane & 3;
-    const int chunk = blockIdx.x, g = blockIdx.y;
-    const int rank = chunk % a.cluster, super = chunk / a.cluster;
-    const int R = a.batch * G;  // query rows of KV head g
-    const int rt0 = blockIdx.z * kPrefixRows;
-    const int r0 = rt0 + warp * 16;
-    const int j0 = min(chunk * a.chunk_blocks, a.n_prefix_blocks);
-    const int j1 = min(j0 + a.chunk_blocks, a.n_prefix_blocks);
-    // every row tile of this head reads the same tiles: keep them in L2
-    uint64_t policy;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(policy));
-    if (tid == 0) {
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
-        for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
-        fence_mbarrier_init();
-    }
-    // Launched behind the tail decode, which never touches the prefix
-    // partials: let the merge kernel launch now, start at once (the inputs
-    // read here predate the decode launch), and wait for the decode grid
-    // only at the end, so that this grid's completion implies the decode's.
-    griddep_launch_dependents();
-    for (int j = j0 + tid; j < j1; j += kPrefixWarps * 32) tab[j - j0] = a.prefix_blocks[j];
-    __syncthreads();
-    auto issue = [&](int j) {  // thread 0: block j of the prefix into stage (j - j0) % S
-        const int st = (j - j0) % S;
-        const int phys = tab[j - j0];
-        const bool ok = phys >= 0 && phys < a.num_blocks;
-        phys_st[st] = ok ? phys : -1;
-        if (ok) {
-            const int y = (int)(((int64_t)phys * a.n_kv + g) * kBlockSize);
-            uint8_t *dst = ring + st * Gm::STAGE;
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&bars[st], Gm::STAGE);
-#pragma unroll
-            for (int r = 0; r < Gm::NREG; ++r) {
-                tma_load_2d(dst + r * Gm::RGN, &tm_k, r * Gm::BOX_ELEMS, y, &bars[st], policy);
-                tma_load_2d(dst + Gm::TILE + r * Gm::RGN, &tm_v, r * Gm::BOX_ELEMS, y, &bars[st], policy);
-            }
-        } else {
-            atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
-            mbar_arrive(&bars[st]);
-        }
-    };
-    if (tid == 0)
-        for (int j = j0; j < min(j1, j0 + S); ++j) issue(j);
-
-    // Q rows r0 + g8 and r0 + g8 + 8 as A fragments (zero past the last row)
-    uint32_t qa[NT][4];
-    {
-        const int ra = r0 + g8, rb = r0 + g8 + 8;
-        const __nv_bfloat16 *qa_row = a.q + ((int64_t)(ra / G) * a.n_q + g * G + ra % G) * D;
-        const __nv_bfloat16 *qb_row = a.q + ((int64_t)(rb / G) * a.n_q + g * G + rb % G) * D;
-#pragma unroll
-        for (int ks = 0; ks < NT; ++ks) {
-            const int d0 = 16 * ks + 2 * c4;
-            qa[ks][0] = ra < R ? *reinterpret_cast<const uint32_t *>(qa_row + d0) : 0u;
-            qa[ks][1] = rb < R ? *reinterpret_cast<const uint32_t *>(qb_row + d0) : 0u;
-            qa[ks][2] = ra < R ? *reinterpret_cast<const uint32_t *>(qa_row + d0 + 8) : 0u;
-            qa[ks][3] = rb < R ? *reinterpret_cast<const uint32_t *>(qb_row + d0 + 8) : 0u;
-        }
-    }
-    float o[2 * NT][4];  // O[16 rows x D]: n-tile t covers d 8t..8t+7
-#pragma unroll
-    for (int t = 0; t < 2 * NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // rows g8, g8 + 8
-    // ldmatrix lane roles: K as B (rows = tokens, non-trans), V as B (.trans)
-    const int tk = (lane & 7) + (lane >> 4) * 8, hk = (lane >> 3) & 1;
-    const int tv = (lane & 7) + ((lane >> 3) & 1) * 8, hv = lane >> 4;
-    bool aborted = false;
-
-    for (int j = j0; j < j1; j += 2) {
-        const bool two = j + 1 < j1;  // the last step of an odd chunk holds one block
-        const int st0 = (j - j0) % S, st1 = (j + 1 - j0) % S;
-        if (!aborted) {
-            bool ok = mbar_wait_bounded(&bars[st0], (uint32_t)((j - j0) / S) & 1u);
-            if (two) ok = mbar_wait_bounded(&bars[st1], (uint32_t)((j + 1 - j0) / S) & 1u) && ok;
-            aborted = __any_sync(kFull, !ok);
-            if (aborted && lane == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
-        }
-        // One step over blocks j, j+1.  F: both present and holding data (every
-        // step but an odd chunk's last, or one with a bad block id), compiled
-        // without the masking selects.
-        auto step = [&](auto full) {
-            constexpr bool F = decltype(full)::value;
-            const bool v0 = F || phys_st[st0] >= 0, v1 = F || (two && phys_st[st1] >= 0);  // blocks that hold data
-            const uint32_t kb0 = smem_u32(ring + st0 * Gm::STAGE);
-            const uint32_t kb1 = two ? smem_u32(ring + st1 * Gm::STAGE) : kb0;
-            // S[16 rows x 32 tokens] = Q K^T: n-tiles of tokens 0-7, 8-15 of each block
-            float s[4][4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.0f;
-#pragma unroll
-            for (int ks = 0; ks < NT; ++ks) {
-                const int ch = 2 * ks + hk;
-                const uint32_t off = (ch >> 3) * Gm::RGN + swz<128>(tk * 128 + (ch & 7) * 16);
-                uint32_t f0[4], f1[4];
-                ldsm_x4(kb0 + off, f0);
-                ldsm_x4(kb1 + off, f1);
-                mma16816<false>(s[0], qa[ks], f0[0], f0[1]);
-                mma16816<false>(s[1], qa[ks], f0[2], f0[3]);
-                mma16816<false>(s[2], qa[ks], f1[0], f1[1]);
-                mma16816<false>(s[3], qa[ks], f1[2], f1[3]);
-            }
-            // row g8: sv[0..7], row g8+8: sv[8..15]; tokens of a block without data are masked
-            float sv[16];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool live = F || (i < 2 ? v0 : v1);
-                sv[2 * i] = live ? s[i][0] * a.qscale : -INFINITY;
-                sv[2 * i + 1] = live ? s[i][1] * a.qscale : -INFINITY;
-                sv[8 + 2 * i] = live ? s[i][2] * a.qscale : -INFINITY;
-                sv[8 + 2 * i + 1] = live ? s[i][3] * a.qscale : -INFINITY;
-            }
-            float bm0 = sv[0], bm1 = sv[8];
-#pragma unroll
-            for (int i = 1; i < 8; ++i) {
-                bm0 = fmaxf(bm0, sv[i]);
-                bm1 = fmaxf(bm1, sv[8 + i]);
-            }
-#pragma unroll
-            for (int off = 1; off < 4; off <<= 1) {
-                bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
-                bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
-            }
-            if (v0 || v1) {  // some token of this step holds data (uniform across the CTA)
-                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);  // finite: a live block has 16 tokens
-                const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-                float p[16];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    p[i] = exp2f(sv[i] - mn0);
-                    p[8 + i] = exp2f(sv[8 + i] - mn1);
-                }
-                l0 = fmaf(l0, al0, ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7])));
-                l1 = fmaf(l1, al1, ((p[8] + p[9]) + (p[10] + p[11])) + ((p[12] + p[13]) + (p[14] + p[15])));
-                m0 = mn0;
-                m1 = mn1;
-                if (__any_sync(kFull, al0 != 1.0f || al1 != 1.0f)) {
-#pragma unroll
-                    for (int t = 0; t < 2 * NT; ++t) {
-                        o[t][0] *= al0;
-                        o[t][1] *= al0;
-                        o[t][2] *= al1;
-                        o[t][3] *= al1;
-                    }
-                }
-                // P as the A operand of O += P V, one 16-token k-step per block
-                const uint32_t pa0[4] = {pack2<false>(p[0], p[1]), pack2<false>(p[8], p[9]),
-                                         pack2<false>(p[2], p[3]), pack2<false>(p[10], p[11])};
-                const uint32_t pa1[4] = {pack2<false>(p[4], p[5]), pack2<false>(p[12], p[13]),
-                                         pack2<false>(p[6], p[7]), pack2<false>(p[14], p[15])};
-                const uint32_t vb0 = kb0 + Gm::TILE, vb1 = kb1 + Gm::TILE;
-#pragma unroll
-                for (int n2 = 0; n2 < NT; ++n2) {
-                    const int ch = 2 * n2 + hv;
-                    const uint32_t off = (ch >> 3) * Gm::RGN + swz<128>(tv * 128 + (ch & 7) * 16);
-                    uint32_t f0[4], f1[4];
-                    ldsm_x4_t(vb0 + off, f0);
-                    ldsm_x4_t(vb1 + off, f1);
-                    if constexpr (!F) {  // no data: keep stale bytes out of the MMA
-                        if (!v0) f0[0] = f0[1] = f0[2] = f0[3] = 0u;
-                        if (!v1) f1[0] = f1[1] = f1[2] = f1[3] = 0u;
-                    }
-                    mma16816<false>(o[2 * n2], pa0, f0[0], f0[1]);
-                    mma16816<false>(o[2 * n2 + 1], pa0, f0[2], f0[3]);
-                    mma16816<false>(o[2 * n2], pa1, f1[0], f1[1]);
-                    mma16816<false>(o[2 * n2 + 1], pa1, f1[2], f1[3]);
-                }
-            }
-        };
-        if (!aborted) {
-            if (two && phys_st[st0] >= 0 && phys_st[st1] >= 0) step(std::true_type{});
-            else step(std::false_type{});
-        }
-        __syncthreads();  // every warp is done with this step's stages
-        if (tid == 0 && !aborted) {
-            if (j + S < j1) issue(j + S);
-            if (j + 1 + S < j1) issue(j + 1 + S);
-        }
-    }
-    if (aborted && tid == 0)  // drain this CTA's copies still in flight (bounded)
-        for (int j = j0; j < min(j1, j0 + S); ++j) mbar_wait_bounded(&bars[(j - j0) % S], 0, 100000000ull);
-
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-        l0 += __shfl_xor_sync(kFull, l0, off);
-        l1 += __shfl_xor_sync(kFull, l1, off);
-    }
-    // this CTA's partial into shared memory (the ring is free now)
-    __syncthreads();
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int row = warp * 16 + g8 + 8 * half;
-        float *po = part + row * D;
-#pragma unroll
-        for (int t = 0; t < 2 * NT; ++t)
-            *reinterpret_cast<float2 *>(po + 8 * t + 2 * c4) = make_float2(o[t][2 * half], o[t][2 * half + 1]);
-        if (c4 == 0) part_ml[row] = half ? make_float2(m1, l1) : make_float2(m0, l0);
-    }
-    cluster_sync_all();  // every chunk's partial of the cluster is in place
-    // This CTA reduces rows [rank * RP, (rank + 1) * RP) over the cluster's
-    // chunks, in rank order: first each row's M, L and chunk weights, then
-    // the O columns with every peer's load in flight at once.
-    const int RP = kPrefixRows / a.cluster;
-    const uint32_t part_base = smem_u32(part), ml_base = smem_u32(part_ml);
-    for (int row = tid; row < RP; row += kPrefixWarps * 32) {
-        const int lr = rank * RP + row;
-        float2 ml[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            ml[k] = k < a.cluster ? ld_cluster_f2(cluster_peer_addr(ml_base + lr * 8, (uint32_t)k))
-                                  : make_float2(-INFINITY, 0.0f);
-        float M = ml[0].x;
-#pragma unroll
-        for (int k = 1; k < 8; ++k) M = fmaxf(M, ml[k].x);
-        float Lsum = 0.0f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float w = ml[k].x == -INFINITY ? 0.0f : exp2f(ml[k].x - M);  // an empty chunk has no weight
-            wgt[row][k] = w;
-            Lsum = fmaf(w, ml[k].y, Lsum);
-        }
-        row_ml[row] = make_float2(M, Lsum);
-    }
-    __syncthreads();
-#pragma unroll 2
-    for (int e = tid; e < RP * (D / 4); e += kPrefixWarps * 32) {
-        const int row = e / (D / 4), c = e % (D / 4);
-        const int lr = rank * RP + row, r = rt0 + lr;
-        float4 x[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            x[k] = k < a.cluster ? ld_cluster_f4(cluster_peer_addr(part_base + (lr * D + 4 * c) * 4, (uint32_t)k))
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float w = wgt[row][k];
-            acc.x = fmaf(w, x[k].x, acc.x);
-            acc.y = fmaf(w, x[k].y, acc.y);
-            acc.z = fmaf(w, x[k].z, acc.z);
-            acc.w = fmaf(w, x[k].w, acc.w);
-        }
-        if (r < R) {
-            const int b = r / G, hh = r % G;
-            const int64_t slot = a.pre_base + ((int64_t)super * a.batch + b) * a.n_kv + g;
-            *reinterpret_cast<float4 *>(a.ws_o + (slot * G + hh) * D + 4 * c) = acc;
-            if (c == 0) a.ws_ml[slot * G + hh] = row_ml[row];
-        }
-    }
-    cluster_sync_all();  // peers may still read this CTA's shared memory until here
-    griddep_wait();      // this grid completes only after the tail decode grid
-}
+// is the decode kernel started past the prefix blocks (the sequences' own
+// tails).  Stage 2 attends all batch x G query rows of each KV head to the
+// prefix in one pass over its K and V tiles -- a dense contraction, run by
+// the tcgen05 prefill kernel in partial mode -- and stores a (max, sum, O)
+// partial per prefix chunk.  Stage 3, the merge kernel, combines the two.
 
 template <int D, int G>
 static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32_t *prefix_blocks,
                                        int n_prefix_blocks, cudaStream_t s)
 {
     using C = Cfg<D, G, false>;
-    using PL = PrefixSmem<D>;
     int grid = 0;
     size_t smem = 0;
     pkv_status st = decode_grid<D, G, false>(pool, a.batch, a.W, &grid, &smem);
     if (st != PKV_OK) return st;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    static int pre_occ = 1;
-    std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(prefix_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)PL::bytes(kPrefixMaxChunk));
-        if (attr_err == cudaSuccess)
-            attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&pre_occ, prefix_kernel<D, G>, kPrefixWarps * 32,
-                                                                     PL::bytes(kPrefixMaxChunk));
-    });
-    if (attr_err != cudaSuccess) return cuda_fail(attr_err, "prefix kernel attributes");
-    // Chunks: about as many CTAs as are resident at once, at least two
-    // blocks per chunk; the chunks of a cluster (up to 8) reduce together,
-    // so each sequence gets one prefix partial per cluster.
-    const int row_tiles = (a.batch * G + kPrefixRows - 1) / kPrefixRows;
-    const int64_t per_chunk_ctas = (int64_t)a.n_kv * row_tiles;
-    int want = (int)std::max<int64_t>(1, (int64_t)pool->num_sms * std::max(1, pre_occ) / per_chunk_ctas);
-    want = std::min(want, std::max(1, n_prefix_blocks / 2));
-    int cluster = 1;
-    while (cluster * 2 <= std::min(8, want)) cluster *= 2;
-    int n_super = std::max(1, want / cluster);
-    n_super = std::max(n_super, (n_prefix_blocks + cluster * kPrefixMaxChunk - 1) / (cluster * kPrefixMaxChunk));
-    const int chunk_blocks = (n_prefix_blocks + cluster * n_super - 1) / (cluster * n_super);
-    n_super = ((n_prefix_blocks + chunk_blocks - 1) / chunk_blocks + cluster - 1) / cluster;  // no empty cluster
-    const int n_chunks = cluster * n_super;
-
+    int chunk_blocks = 0, n_chunks = 0;
+    prefix_stage_chunks(pool, a.batch, a.n_q, n_prefix_blocks, &chunk_blocks, &n_chunks);
     const int64_t tail_slots = max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW);
-    const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, tail_slots + (int64_t)n_super * a.batch * a.n_kv);
+    const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, tail_slots + (int64_t)n_chunks * a.batch * a.n_kv);
     st = ensure_workspace(pool, L.total);
     if (st != PKV_OK) return st;
     bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
     a.skip_blocks = n_prefix_blocks;
-    a.n_pre = n_super;
+    a.n_pre = n_chunks;
     a.pre_base = tail_slots;
-    PrefixArgs pa;
-    pa.q = a.q;
-    pa.n_q = a.n_q;
-    pa.n_kv = a.n_kv;
-    pa.batch = a.batch;
-    pa.prefix_blocks = prefix_blocks;
-    pa.n_prefix_blocks = n_prefix_blocks;
-    pa.chunk_blocks = chunk_blocks;
-    pa.cluster = cluster;
-    pa.num_blocks = a.num_blocks;
-    pa.qscale = a.qscale;
-    pa.ws_ml = a.ws_ml;
-    pa.ws_o = a.ws_o;
-    pa.pre_base = tail_slots;
-    pa.err = a.err;
-    // Order: the tail decode, then the prefix stage (its CTAs fill the SMs
-    // the decode's warps leave as they finish), then the merge.
+    // Order: the tail decode, then the prefix stage (its CTAs take the SMs the
+    // decode leaves as it finishes), then the merge.
     {
         LaunchScope ls(pool, kDecode, s);
         cudaError_t e = launch_pdl(decode_kernel<D, G, false>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
@@ -2032,14 +1675,9 @@ static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32
         ls.done();
         if (e != cudaSuccess) return cuda_fail(e, "decode launch (cascade tail)");
     }
-    {
-        LaunchScope ls(pool, kPrefix, s);
-        cudaError_t e = launch_pdl_cluster(prefix_kernel<D, G>, dim3(n_chunks, a.n_kv, row_tiles),
-                                           dim3(kPrefixWarps * 32), PL::bytes(chunk_blocks), (unsigned)cluster, s,
-                                           pool->tm_k, pool->tm_v, pa);
-        ls.done();
-        if (e != cudaSuccess) return cuda_fail(e, "prefix launch");
-    }
+    st = launch_prefix_stage(pool, a.q, a.batch, a.n_q, prefix_blocks, n_prefix_blocks, chunk_blocks, n_chunks,
+                             a.qscale, a.ws_ml, a.ws_o, tail_slots, s);
+    if (st != PKV_OK) return st;
     return launch_merge<D, G>(pool, a, grid * C::NW, s);
 }
 

@@ -90,6 +90,15 @@ pkv_status make_tensor_maps(pkv_pool *pool);
 // min(d_head, 64) columns x `heads` heads x `tokens` rows, 128-byte swizzle.
 pkv_status make_q_map(CUtensorMap *map, const void *q, int64_t n_rows, int n_q, int d_head, int heads, int tokens);
 
+// The cascade's prefix stage on the tensor cores (the prefill kernel in
+// partial mode): every query row of every KV head against the shared blocks,
+// cut into n_chunks chunks of chunk_blocks; one (m, l, O) partial per chunk,
+// sequence and KV head into the merge workspace.
+void prefix_stage_chunks(pkv_pool *pool, int batch, int n_q, int n_prefix_blocks, int *chunk_blocks, int *n_chunks);
+pkv_status launch_prefix_stage(pkv_pool *pool, const void *q, int batch, int n_q, const int32_t *prefix_blocks,
+                               int n_prefix_blocks, int chunk_blocks, int n_chunks, float qscale, float2 *ws_ml,
+                               float *ws_o, int64_t pre_base, cudaStream_t s);
+
 constexpr int kMaxBatch = 8192;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned kFull = 0xffffffffu;

@@ -67,6 +67,14 @@ struct Args {
     const int32_t *block_tables;
     int W;
     const int32_t *context_lens;
+    // partial mode (the cascade's prefix stage): the "sequences" are chunks of
+    // a block list shared by every sequence; each chunk's rows are all batch x
+    // G query rows of a KV head; no causal mask; (m, l, O) partials out
+    const int32_t *shared_blocks;
+    int n_shared_blocks, chunk_blocks, n_chunks;
+    float2 *ws_ml;             // [slot][G] (reference max, row sum)
+    float *ws_o;               // [slot][G][D] unnormalised O
+    int64_t pre_base;          // slot of (chunk c, sequence b, KV head g): pre_base + (c * batch + b) * n_kv + g
     int batch, n_q, n_kv;
     int64_t num_blocks;
     int64_t n_rows;            // rows of q and out: stores past them are skipped (an inconsistent indptr)
@@ -251,15 +259,27 @@ struct Walker {
     int ph = 0, row0 = 0, T = 0, C = 0;  // this lane's sequence: pairs per KV head, rows, context
 };
 
-template <int G>
+template <int G, bool PARTIAL>
+__device__ __forceinline__ int n_items(const Args &a)
+{
+    return PARTIAL ? a.n_chunks : a.batch;
+}
+
+template <int G, bool PARTIAL>
 __device__ __forceinline__ void load_window(Walker &w, const Args &a, int lane)
 {
     const int bl = w.wb + lane;
     w.row0 = w.T = w.C = w.ph = 0;
-    if (bl < a.batch) {
-        w.row0 = a.qo_indptr[bl];
-        w.T = a.qo_indptr[bl + 1] - w.row0;
-        w.C = a.context_lens[bl];
+    if (bl < n_items<G, PARTIAL>(a)) {
+        if (PARTIAL) {  // chunk bl of the shared blocks: every sequence's query rows
+            w.row0 = 0;
+            w.T = a.batch;
+            w.C = min(a.chunk_blocks, a.n_shared_blocks - bl * a.chunk_blocks) * kBlockSize;
+        } else {
+            w.row0 = a.qo_indptr[bl];
+            w.T = a.qo_indptr[bl + 1] - w.row0;
+            w.C = a.context_lens[bl];
+        }
         if (w.T > 0) w.ph = ((w.T * G + kRows - 1) / kRows + 1) / 2;
     }
     int x = w.ph * a.n_kv;
@@ -277,14 +297,14 @@ __device__ __forceinline__ void load_window(Walker &w, const Args &a, int lane)
 // there (past the last row tile when the count is odd: no rows, the CTA only
 // keeps step with its partner).  Both CTAs stream the blocks the pair's last
 // row reaches.  False past the list's end.  Warp-wide, uniform result.
-template <int G>
+template <int G, bool PARTIAL>
 __device__ __forceinline__ bool find_tile(Walker &w, const Args &a, int x, int rank, Tile &t, int lane)
 {
     while (x >= w.wbase + w.tot) {
-        if (w.wb + 32 >= a.batch) return false;
+        if (w.wb + 32 >= n_items<G, PARTIAL>(a)) return false;
         w.wbase += w.tot;
         w.wb += 32;
-        load_window<G>(w, a, lane);
+        load_window<G, PARTIAL>(w, a, lane);
     }
     const unsigned hit = __ballot_sync(kFull, w.wbase + w.incl > x);
     const int l = __ffs(hit) - 1;
@@ -299,6 +319,13 @@ __device__ __forceinline__ bool find_tile(Walker &w, const Args &a, int x, int r
     const int pair_rt0 = 2 * (within - t.g * ph) * kRows;
     t.rt0 = pair_rt0 + rank * kRows;
     t.R = t.T * G;
+    if (PARTIAL) {  // whole blocks, all visible to every row
+        t.C = C;
+        t.bad_ctx = false;
+        t.n_blocks = C / kBlockSize;
+        t.n_steps = (t.n_blocks + kStepBlocks - 1) / kStepBlocks;
+        return true;
+    }
     const int cap = a.W * kBlockSize;
     t.bad_ctx = C < t.T || C > cap;
     if (t.bad_ctx) C = max(t.T, min(C, cap));
@@ -313,6 +340,13 @@ __device__ __forceinline__ bool find_tile(Walker &w, const Args &a, int x, int r
     return true;
 }
 
+// The block list a tile streams: its sequence's table row, or its chunk of the shared blocks.
+template <bool PARTIAL>
+__device__ __forceinline__ const int32_t *tile_blocks(const Args &a, const Tile &t)
+{
+    return PARTIAL ? a.shared_blocks + (int64_t)t.b * a.chunk_blocks : a.block_tables + (int64_t)t.b * a.W;
+}
+
 __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity)
 {
     return __all_sync(kFull, mbar_wait_bounded(bar, parity));
@@ -320,7 +354,7 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity)
 
 // ------------------------------------------------------------- the kernel
 
-template <int D, int G>
+template <int D, int G, bool PARTIAL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, Args a)
@@ -359,7 +393,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync_all();  // both CTAs' barriers exist before either multicasts into the other
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + L::kTmemSlot);
-    griddep_wait();  // queries, tables and the appended chunk may come from the previous kernel
+    // queries, tables and the appended chunk may come from the previous kernel.  In
+    // partial mode the previous kernel is the cascade's tail decode, whose output this
+    // kernel does not read: it waits at its end instead, so that the merge launched after
+    // it sees both.
+    if (!PARTIAL) griddep_wait();
     griddep_launch_dependents();
 
     auto set_abort = [&]() {
@@ -370,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     Walker wk;
-    load_window<G>(wk, a, lane);
+    load_window<G, PARTIAL>(wk, a, lane);
 
     if (warp == kKWarp || warp == kVWarp) {
         // ---------------------------------------------------------- producers
@@ -385,10 +423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int x = blockIdx.x / 2; ok; x += gridDim.x / 2) {
             Tile t;
-            if (!find_tile<G>(wk, a, x, rank, t, lane)) break;
+            if (!find_tile<G, PARTIAL>(wk, a, x, rank, t, lane)) break;
             if (t.n_steps == 0) continue;
             if (*abort_flag) break;
-            const int32_t *trow = a.block_tables + (int64_t)t.b * a.W;
+            const int32_t *trow = tile_blocks<PARTIAL>(a, t);
             // block ids (lanes 0..7) one step ahead of the copies: the table read is off the refill path
             int nxt = lane < kStepBlocks && lane < t.n_blocks ? trow[lane] : -1;
             if (is_k) {  // this tile's queries into Q buffer qi & 1
@@ -445,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int x = blockIdx.x / 2; ok; x += gridDim.x / 2) {
             Tile t;
-            if (!find_tile<G>(wk, a, x, rank, t, lane)) break;
+            if (!find_tile<G, PARTIAL>(wk, a, x, rank, t, lane)) break;
             if (t.n_steps == 0) continue;
             if (*abort_flag) break;
             const int qb = qi & 1;
@@ -526,17 +564,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int QB = kStepBlocks / 2;  // blocks of a step in this warp's key half
         // this warp's block ids of step 0 of tile t (lanes 0..QB-1)
         auto first_ids = [&](const Tile &t) -> int {
-            return lane < QB && ch * QB + lane < t.n_blocks ? a.block_tables[(int64_t)t.b * a.W + ch * QB + lane] : -1;
+            return lane < QB && ch * QB + lane < t.n_blocks ? tile_blocks<PARTIAL>(a, t)[ch * QB + lane] : -1;
         };
         int gs = 0, n_out = 0;  // steps so far, tiles written out so far
         bool ok = true;
         int x = blockIdx.x / 2;
         Tile t, tn;
-        bool have = find_tile<G>(wk, a, x, rank, t, lane);
+        bool have = find_tile<G, PARTIAL>(wk, a, x, rank, t, lane);
         int nxt = have ? first_ids(t) : -1;
         while (have && ok) {
             // the next tile and its first block ids are found while this one runs
-            const bool have_n = find_tile<G>(wk, a, x + gridDim.x / 2, rank, tn, lane);
+            const bool have_n = find_tile<G, PARTIAL>(wk, a, x + gridDim.x / 2, rank, tn, lane);
             if (t.bad_ctx && tid == 0 && t.rt0 == 0 && t.g == 0) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
             if (t.n_steps == 0 || *abort_flag) {
                 if (*abort_flag) break;
@@ -550,13 +588,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t orow_i = (int64_t)t.row0 + min(r, t.R - 1) / G;  // this row's query token
             const bool in_out = orow_i >= 0 && orow_i < a.n_rows;
             if (r < t.R && !in_out && ch == 0) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
-            const int pos = t.C - t.T + min(r, t.R - 1) / G;  // this row's position; it sees keys 0 .. pos
+            // this row's position: it sees keys 0 .. pos (every key of a shared chunk)
+            const int pos = PARTIAL ? t.C - 1 : t.C - t.T + min(r, t.R - 1) / G;
             float mref = -INFINITY;
             float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // this half's row sum of the bf16-rounded P
             // block ids of this warp's 4 blocks of the next step (lanes 0..3), read one step ahead
             // (for the last step: the next tile's first ids): the same validity test as the
             // producers, so a masked block is exactly a skipped one
-            const int32_t *trow = a.block_tables + (int64_t)t.b * a.W;
+            const int32_t *trow = tile_blocks<PARTIAL>(a, t);
             for (int s = 0; s < t.n_steps; ++s, ++gs) {
                 const int cur = nxt;
                 const int nb = (s + 1) * kStepBlocks + ch * QB + lane;
@@ -641,7 +680,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = exchange(l_half, l_other))) break;
             const float l = l_half + l_other;
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-            if (t.rt0 < t.R) {  // (a pair's second tile may hold no rows)
+            if (PARTIAL) {  // (m, l, O) of this row for the merge, this warp's half of O
+                const bool rv = r < t.R;
+                const int64_t slot = a.pre_base + ((int64_t)t.b * a.batch + (rv ? r / G : 0)) * a.n_kv + t.g;
+                float *wo = a.ws_o + (slot * G + r % G) * D + ch * HD;
+#pragma unroll
+                for (int c = 0; c < HD / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tmem + lane_off + kColO + ch * HD + 32 * c, o);
+                    tmem_wait_ld();
+                    if (rv) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            *reinterpret_cast<float4 *>(wo + 32 * c + 4 * q4) =
+                                make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
+                                            __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
+                    }
+                }
+                if (rv && ch == 0) a.ws_ml[slot * G + r % G] = make_float2(mref, l);
+            } else if (t.rt0 < t.R) {  // (a pair's second tile may hold no rows)
                 // this warp's half row of O / l into the staging tile, 16-byte chunks
                 // swizzled within each 128-byte half row (conflict-free writes and reads)
                 constexpr int RB = D * 2;  // bytes of an output row
@@ -694,20 +751,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     cluster_sync_all();  // no copy or arrival from the partner is still on its way into this CTA
     tc_fence_after();
+    if (PARTIAL) griddep_wait();
     if (warp == kQkWarp)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
-template <int D, int G>
-pkv_status launch(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, const Args &a, cudaStream_t s)
+// Clusters of two CTAs that fit on the device at once (one CTA per SM).
+template <int D, int G, bool PARTIAL>
+pkv_status setup(pkv_pool *pool, int *max_clusters)
 {
     using L = Layout<D>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
-    static int max_clusters = 0;  // clusters of two that fit on the device at once
+    static int clusters = 0;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(prefill_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)L::bytes);
+        attr_err = cudaFuncSetAttribute(prefill_tc_kernel<D, G, PARTIAL>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
         if (attr_err != cudaSuccess) return;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * std::max(1, pool->num_sms / 2));
@@ -720,35 +779,44 @@ pkv_status launch(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, const 
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        attr_err = cudaOccupancyMaxActiveClusters(&max_clusters, prefill_tc_kernel<D, G>, &cfg);
+        attr_err = cudaOccupancyMaxActiveClusters(&clusters, prefill_tc_kernel<D, G, PARTIAL>, &cfg);
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "prefill kernel attributes");
-    if (max_clusters < 1) return fail(PKV_ECUDA, "prefill: no cluster of two CTAs fits on the device");
-    CUtensorMap tm_q;
-    pkv_status st = make_q_map(&tm_q, q, n_rows, n_q, D, G, kRows / G);
-    if (st != PKV_OK) return st;
-    // an upper bound on the row-tile pairs (every sequence may end with a partial tile);
-    // clusters of two CTAs, one cluster per pair of SMs
-    const int64_t pairs = ((n_rows * G + kRows - 1) / kRows + a.batch) * a.n_kv;
-    if (pairs > INT32_MAX || n_rows * G > INT32_MAX)
-        return fail(PKV_EUNSUPPORTED, "paged_prefill_attention: too many query rows");
-    const int grid = 2 * (int)std::min<int64_t>(pairs, max_clusters);
-    LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl_cluster(prefill_tc_kernel<D, G>, dim3(grid), dim3(kThreads), L::bytes, 2, s, tm_q,
-                                       pool->tm_k, pool->tm_v, a);
-    ls.done();
-    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    if (clusters < 1) return fail(PKV_ECUDA, "prefill: no cluster of two CTAs fits on the device");
+    *max_clusters = clusters;
     return PKV_OK;
 }
 
-template <int D>
-pkv_status dispatch(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, int G, const Args &a, cudaStream_t s)
+// pairs: an upper bound on the row-tile pairs (the grid is at most one cluster per pair).
+template <int D, int G, bool PARTIAL>
+pkv_status launch(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, int64_t pairs, const Args &a,
+                  cudaStream_t s)
+{
+    using L = Layout<D>;
+    int max_clusters = 0;
+    pkv_status st = setup<D, G, PARTIAL>(pool, &max_clusters);
+    if (st != PKV_OK) return st;
+    CUtensorMap tm_q;
+    st = make_q_map(&tm_q, q, n_rows, n_q, D, G, kRows / G);
+    if (st != PKV_OK) return st;
+    const int grid = 2 * (int)std::min<int64_t>(pairs, max_clusters);
+    LaunchScope ls(pool, PARTIAL ? kPrefix : kDecode, s);
+    cudaError_t e = launch_pdl_cluster(prefill_tc_kernel<D, G, PARTIAL>, dim3(grid), dim3(kThreads), L::bytes, 2, s,
+                                       tm_q, pool->tm_k, pool->tm_v, a);
+    ls.done();
+    if (e != cudaSuccess) return cuda_fail(e, PARTIAL ? "prefix stage launch" : "prefill launch");
+    return PKV_OK;
+}
+
+template <int D, bool PARTIAL>
+pkv_status dispatch(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, int G, int64_t pairs, const Args &a,
+                    cudaStream_t s)
 {
     switch (G) {
-    case 1: return launch<D, 1>(pool, q, n_rows, n_q, a, s);
-    case 2: return launch<D, 2>(pool, q, n_rows, n_q, a, s);
-    case 4: return launch<D, 4>(pool, q, n_rows, n_q, a, s);
-    case 8: return launch<D, 8>(pool, q, n_rows, n_q, a, s);
+    case 1: return launch<D, 1, PARTIAL>(pool, q, n_rows, n_q, pairs, a, s);
+    case 2: return launch<D, 2, PARTIAL>(pool, q, n_rows, n_q, pairs, a, s);
+    case 4: return launch<D, 4, PARTIAL>(pool, q, n_rows, n_q, pairs, a, s);
+    case 8: return launch<D, 8, PARTIAL>(pool, q, n_rows, n_q, pairs, a, s);
     }
     return fail(PKV_EUNSUPPORTED, "prefill: group size %d unsupported (1, 2, 4 or 8)", G);
 }
@@ -788,8 +856,65 @@ extern "C" pkv_status paged_prefill_attention(pkv_pool *pool, const void *q, int
     a.qscale = scale * kLog2e;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.err = pool->err;
+    a.shared_blocks = nullptr;
+    a.n_shared_blocks = a.chunk_blocks = a.n_chunks = 0;
+    a.ws_ml = nullptr;
+    a.ws_o = nullptr;
+    a.pre_base = 0;
     const int G = n_q / pool->n_kv;
+    // an upper bound on the row-tile pairs: every sequence may end with a partial tile
+    const int64_t pairs = ((n_rows * G + kRows - 1) / kRows + batch) * pool->n_kv;
+    if (pairs > INT32_MAX || n_rows * G > INT32_MAX)
+        return fail(PKV_EUNSUPPORTED, "paged_prefill_attention: too many query rows");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return pool->d_head == 128 ? dispatch<128>(pool, q, n_rows, n_q, G, a, s)
-                               : dispatch<64>(pool, q, n_rows, n_q, G, a, s);
+    return pool->d_head == 128 ? dispatch<128, false>(pool, q, n_rows, n_q, G, pairs, a, s)
+                               : dispatch<64, false>(pool, q, n_rows, n_q, G, pairs, a, s);
 }
+
+namespace pkv {
+
+void prefix_stage_chunks(pkv_pool *pool, int batch, int n_q, int n_prefix_blocks, int *chunk_blocks, int *n_chunks)
+{
+    const int G = n_q / pool->n_kv;
+    const int64_t pairs_per_chunk = (int64_t)pool->n_kv * ((((int64_t)batch * G + kRows - 1) / kRows + 1) / 2);
+    // about one cluster per pair of SMs, and at least two steps of blocks per chunk
+    const int64_t want = std::max<int64_t>(1, (pool->num_sms / 2) / std::max<int64_t>(1, pairs_per_chunk));
+    const int64_t cap = std::max<int64_t>(1, (n_prefix_blocks + 2 * kStepBlocks - 1) / (2 * kStepBlocks));
+    const int nc = (int)std::min(want, cap);
+    *chunk_blocks = (n_prefix_blocks + nc - 1) / nc;
+    *n_chunks = (n_prefix_blocks + *chunk_blocks - 1) / *chunk_blocks;
+}
+
+pkv_status launch_prefix_stage(pkv_pool *pool, const void *q, int batch, int n_q, const int32_t *prefix_blocks,
+                               int n_prefix_blocks, int chunk_blocks, int n_chunks, float qscale, float2 *ws_ml,
+                               float *ws_o,
+                               int64_t pre_base, cudaStream_t s)
+{
+    const int G = n_q / pool->n_kv;
+    Args a;
+    a.qo_indptr = nullptr;
+    a.block_tables = nullptr;
+    a.W = 0;
+    a.context_lens = nullptr;
+    a.batch = batch;
+    a.n_q = n_q;
+    a.n_kv = pool->n_kv;
+    a.num_blocks = pool->num_blocks;
+    a.n_rows = batch;
+    a.oob_row = (int)(pool->num_blocks * pool->n_kv * kBlockSize);
+    a.qscale = qscale;
+    a.out = nullptr;
+    a.err = pool->err;
+    a.shared_blocks = prefix_blocks;
+    a.n_shared_blocks = n_prefix_blocks;
+    a.chunk_blocks = chunk_blocks;
+    a.n_chunks = n_chunks;
+    a.ws_ml = ws_ml;
+    a.ws_o = ws_o;
+    a.pre_base = pre_base;
+    const int64_t pairs = (int64_t)a.n_chunks * pool->n_kv * ((((int64_t)batch * G + kRows - 1) / kRows + 1) / 2);
+    return pool->d_head == 128 ? dispatch<128, true>(pool, q, batch, n_q, G, pairs, a, s)
+                               : dispatch<64, true>(pool, q, batch, n_q, G, pairs, a, s);
+}
+
+}  // namespace pkv

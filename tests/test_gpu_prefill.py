@@ -65,3 +65,51 @@ def test_prefill_flags_a_chunk_longer_than_its_cache():
                                     i32_dev(w.context_lens), float(w.scale))
         torch.cuda.synchronize()
         assert pool.get_error(clear=True) & pkv.DEVERR_CTX_RANGE
+
+
+def test_prefill_full_size_sampled_rows():
+    """The 64 x 512-token Llama3-8B chunk workload in the launch configuration
+    the benchmark times; sampled rows checked against the oracle: row i of a
+    chunk is the decode of its query over positions 0 .. C - T + i, so each
+    sample is an oracle decode with that context length."""
+    w = wl.llama3_8b()
+    T = 512
+    rng = np.random.default_rng(11)
+    q = wl.f32_to_bf16_bits(rng.normal(size=(w.batch * T, w.n_q, w.d_head)).astype(np.float32))
+    indptr = np.arange(0, w.batch * T + 1, T, dtype=np.int32)
+    with make_pool(w) as pool:
+        fill(pool, w)
+        run_step(pool, w)
+        out = pkv.paged_prefill_attention(pool, bf16_dev(q), i32_dev(indptr), i32_dev(w.block_tables),
+                                          i32_dev(w.context_lens), float(w.scale))
+        torch.cuda.synchronize()
+        assert pool.get_error() == 0
+        got = out_f64(out)
+    seqs = np.array([0, 1, 17, 31, 32, 46, 62, 63])
+    toks = np.array([0, 1, 31, 32, 127, 128, 300, 511])
+    sb, si = np.meshgrid(seqs, toks, indexing="ij")
+    sb, si = sb.ravel(), si.ravel()
+    rows = sb * T + si
+    lens = (w.context_lens[sb] - T + si + 1).astype(np.int32)
+    ref = mirror(w).decode(q[rows], w.block_tables[sb], lens, w.scale)
+    assert_close(got[rows], ref, "full-size sampled rows")
+
+
+def test_prefill_bad_block_is_flagged_and_other_sequences_exact():
+    w = CASES[0][0]()
+    q, indptr = _chunks(w, [1, 17, 300, 64], 9)
+    tables = w.block_tables.copy()
+    tables[2, 3] = w.num_blocks + 5  # sequence 2 reads a block id past the pool
+    with make_pool(w) as pool:
+        fill(pool, w)
+        run_step(pool, w)
+        out = pkv.paged_prefill_attention(pool, bf16_dev(q), i32_dev(indptr), i32_dev(tables),
+                                          i32_dev(w.context_lens), float(w.scale))
+        torch.cuda.synchronize()
+        assert pool.get_error(clear=True) & pkv.DEVERR_BLOCK_RANGE
+        got = out_f64(out)
+    keep = [0, 1, 3]
+    sub_rows = np.concatenate([np.arange(indptr[b], indptr[b + 1]) for b in keep])
+    sub_indptr = np.concatenate([[0], np.cumsum([indptr[b + 1] - indptr[b] for b in keep])]).astype(np.int32)
+    ref = mirror(w).prefill(q[sub_rows], sub_indptr, tables[keep], w.context_lens[keep], w.scale)
+    assert_close(got[sub_rows], ref, "sequences beside the bad one")
