@@ -402,28 +402,22 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
     return v;
 }
 
-// 4-bit codes j and j+4 of a packed 32-bit word (nibble k holds code k) as
-// an exact f16 pair: each code, or-ed into the mantissa of 1024.0, minus 1024.
-__device__ __forceinline__ uint32_t i4_pair(uint32_t w, int j)
-{
-    const uint32_t t = ((w >> (4 * j)) & 0x000F000Fu) | 0x64006400u;
-    uint32_t r;
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64006400u));
-    return r;
-}
+// 4-bit codes as f16 operands without a subtraction: a code c or-ed into
+// the mantissa of 1024.0 is exactly 1024 + c (low nibble of each half word),
+// or 1024 + 16 c (high nibble).  The decode kernel removes the offset and
+// the factor where they do not cancel by themselves (see load_q_frags and
+// the piece end).
+__device__ __forceinline__ uint32_t i4_lo(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
+__device__ __forceinline__ uint32_t i4_hi(uint32_t w) { return (w & 0x00F000F0u) | 0x64006400u; }
 
-// The same code (nibble m of a row's packed words) of two token rows, as an
-// exact f16 pair (row a low, row b high).
-template <int m>
-__device__ __forceinline__ uint32_t i4_cross(const uint32_t *ra, const uint32_t *rb)
+// Byte `bi` of the packed words of two token rows a, b in half words 0 and 1
+// of the result (row a low): i4_lo / i4_hi of it give the byte's two codes
+// for both rows.
+template <int bi>
+__device__ __forceinline__ uint32_t i4_rows(uint32_t wa, uint32_t wb)
 {
-    constexpr uint32_t bi = (m % 8) / 2;  // byte within the word
     constexpr uint32_t sel = bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12);
-    const uint32_t z = prmt(ra[m / 8], rb[m / 8], sel);
-    const uint32_t t = ((z >> (4 * (m & 1))) & 0x000F000Fu) | 0x64006400u;
-    uint32_t r;
-    asm("sub.f16x2 %0, %1, %2;" : "=r"(r) : "r"(t), "r"(0x64006400u));
-    return r;
+    return prmt(wa, wb, sel);
 }
 
 // q rows of one (sequence, KV head) group as m16n8k16 B fragments: thread
@@ -435,8 +429,12 @@ __device__ __forceinline__ uint32_t i4_cross(const uint32_t *ra, const uint32_t 
 // scale folded into q; their zero points add the same constant to every
 // score of a head and cancel in the softmax); k-step ks of thread c4 covers
 // the channels of its packed key word w = ks / 2, base = c4 * D / 4 + 8w:
-// pairs (base + s, base + s + 4) and (base + s + 1, base + s + 5) with
-// s = 2 * (ks & 1), the order i4_pair extracts codes in.
+// pairs (base + s, base + s + 4), taken from the low nibbles of the word's
+// half words (shifted right by 4s), and (base + s + 1, base + s + 5), from
+// the high nibbles, with s = 2 * (ks & 1).  The keys enter the MMA as
+// 1024 + c (low) and 1024 + 16 c (high), so the high channels' q' carries an
+// exact factor 1/16; the offsets add sum_d 1024 q'_d, again one constant per
+// head, which cancels in the softmax.
 template <int D, int G, int KV>
 __device__ __forceinline__ void load_q_frags(const DecodeArgs &a, int b, int g, int g8, int c4,
                                              uint32_t (&qf)[D / 16][2])
@@ -452,7 +450,7 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs &a, int b, int g, 
             const __nv_bfloat16 *qq = qrow + base + s0;
             auto qv = [&](int k) { return live ? __bfloat162float(qq[k]) * sk[k] : 0.0f; };
             qf[ks][0] = pack2<true>(qv(0), qv(4));
-            qf[ks][1] = pack2<true>(qv(1), qv(5));
+            qf[ks][1] = pack2<true>(qv(1) * 0.0625f, qv(5) * 0.0625f);
         } else if constexpr (!FP8) {
             qf[ks][0] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c4) : 0u;
             qf[ks][1] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * c4) : 0u;
@@ -876,7 +874,8 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
 #pragma unroll
         for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // heads 2c, 2c+1
-        float z0 = 0.0f, z1 = 0.0f;  // 4-bit: sum of p * (value zero point), heads 2c, 2c+1
+        float z0 = 0.0f, z1 = 0.0f;    // 4-bit: sum of p * (value zero point), heads 2c, 2c+1
+        float zs0 = 0.0f, zs1 = 0.0f;  // 4-bit: sum of the f16 (p * value scale) the MMA used
 
         // One block: wait for its stage, (fused step, last block only) patch in
         // the new token, then scores, softmax and P.V.  The patching variant is
@@ -920,9 +919,9 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                     }
 #pragma unroll
                     for (int ks = 0; ks < NT; ++ks) {
-                        const int w = ks >> 1, s0 = 2 * (ks & 1);
-                        const uint32_t fa[4] = {i4_pair(kx[w], s0), i4_pair(ky[w], s0), i4_pair(kx[w], s0 + 1),
-                                                i4_pair(ky[w], s0 + 1)};
+                        const int w = ks >> 1;
+                        const uint32_t x = (ks & 1) ? kx[w] >> 8 : kx[w], y = (ks & 1) ? ky[w] >> 8 : ky[w];
+                        const uint32_t fa[4] = {i4_lo(x), i4_lo(y), i4_hi(x), i4_hi(y)};
                         mma16816<true>((ks & 1) ? sb : sa, fa, qf[ks][0], qf[ks][1]);
                     }
                 } else if constexpr (!FP8) {
@@ -985,8 +984,13 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                     const float2 vp1 = g8 + 8 < nv ? vpbuf[sidx * kBlockSize + g8 + 8] : make_float2(0.f, 0.f);
                     z0 = fmaf(z0, al0, fmaf(p0, vp0.y, p2 * vp1.y));
                     z1 = fmaf(z1, al1, fmaf(p1, vp0.y, p3 * vp1.y));
-                    pb0 = movm_t(pack2<true>(p0 * vp0.x, p1 * vp0.x));
-                    pb1 = movm_t(pack2<true>(p2 * vp1.x, p3 * vp1.x));
+                    const uint32_t h0 = pack2<true>(p0 * vp0.x, p1 * vp0.x), h1 = pack2<true>(p2 * vp1.x, p3 * vp1.x);
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&h0));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&h1));
+                    zs0 = fmaf(zs0, al0, f0.x + f1.x);
+                    zs1 = fmaf(zs1, al1, f0.y + f1.y);
+                    pb0 = movm_t(h0);
+                    pb1 = movm_t(h1);
                 } else {
                     pb0 = movm_t(pack2<FP8>(p0, p1));
                     pb1 = movm_t(pack2<FP8>(p2, p3));
@@ -1012,10 +1016,13 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                             rr[q][0] = lds32(vb + swz<Gm::BOXB>(rows[q] * Gm::ROWB + 4 * g8));
                         }
                     }
+                    // tile t: byte t of the thread's span, row g8 its low code (channel 2t of the span),
+                    // row g8 + 8 its high code (channel 2t + 1), as 1024 + c and 1024 + 16 c
                     auto tile = [&](auto tc) {
                         constexpr int t = decltype(tc)::value;
-                        const uint32_t fa[4] = {i4_cross<t>(r0, r1), i4_cross<NT + t>(r0, r1), i4_cross<t>(r2, r3),
-                                                i4_cross<NT + t>(r2, r3)};
+                        const uint32_t z01 = i4_rows<t % 4>(r0[t / 4], r1[t / 4]);
+                        const uint32_t z23 = i4_rows<t % 4>(r2[t / 4], r3[t / 4]);
+                        const uint32_t fa[4] = {i4_lo(z01), i4_hi(z01), i4_lo(z23), i4_hi(z23)};
                         mma16816<true>(o[t], fa, pb0, pb1);
                     };
                     tile(std::integral_constant<int, 0>{});
@@ -1081,23 +1088,29 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
             l0 += __shfl_xor_sync(kFull, l0, off);
             l1 += __shfl_xor_sync(kFull, l1, off);
         }
-        if constexpr (I4) {  // the values' zero points: sum_p p_p z_p, the same for every channel
+        if constexpr (I4) {
+            // the MMA summed (P * s)(1024 + c) over low codes and (P * s)(1024 + 16 c) over high
+            // ones: take off 1024 sum (P * s), undo the 16, and add the values' zero points'
+            // sum_p p_p z_p (the same for every channel)
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
                 z0 += __shfl_xor_sync(kFull, z0, off);
                 z1 += __shfl_xor_sync(kFull, z1, off);
+                zs0 += __shfl_xor_sync(kFull, zs0, off);
+                zs1 += __shfl_xor_sync(kFull, zs1, off);
             }
+            const float c0 = 1024.0f * zs0, c1 = 1024.0f * zs1;
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                o[t][0] += z0;
-                o[t][1] += z1;
-                o[t][2] += z0;
-                o[t][3] += z1;
+                o[t][0] = (o[t][0] - c0) + z0;
+                o[t][1] = (o[t][1] - c1) + z1;
+                o[t][2] = (o[t][2] - c0) * 0.0625f + z0;
+                o[t][3] = (o[t][3] - c1) * 0.0625f + z1;
             }
         }
         // channel of accumulator row g8 + 8i of tile t, per KV type
         auto chan = [&](int t, int i) {
-            return I4 ? g8 * (D / 8) + NT * i + t : FP8 ? 32 * (t >> 1) + 4 * g8 + 2 * (t & 1) + i : 16 * t + g8 + 8 * i;
+            return I4 ? g8 * (D / 8) + 2 * t + i : FP8 ? 32 * (t >> 1) + 4 * g8 + 2 * (t & 1) + i : 16 * t + g8 + 8 * i;
         };
         const float vs = FP8 ? a.scales[a.n_kv + pc.g] : 1.0f;
         const bool h0 = 2 * c4 < G, h1 = 2 * c4 + 1 < G;  // this thread's heads exist
