@@ -755,7 +755,7 @@ def run_prefill(args):
         "dtype": "bf16 in, f32 accumulate",
         "data": "synthetic",
         "config": dict(w.describe(), chunk_tokens=T, query_rows=w.batch * T, visible_keys=keys),
-        "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": tflops, "peak": peak,
+        "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": tflops, "peak": peak,
                      "unit": "TFLOP/s", "frac": tflops / peak,
                      "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops: cuBLAS burst)" if peaks
                      else "fallback"},
