@@ -273,11 +273,12 @@ pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host, const void
  * once per sequence ("Memory Management in LLM Serving Systems", "Prefix
  * sharing": decode-time reads for the shared part drop from n x p to p).
  * Same result as paged_decode_attention (up to rounding order):
- *   stage 1 attends every query row of each KV head to the prefix with
- *   tensor-core tiles and keeps a (max, sum, output) partial per 256-token
- *   chunk; stage 2 decodes each sequence's blocks after the prefix; the
- *   merge kernel combines each sequence's prefix and tail partials by
- *   log-sum-exp.  Three launches.
+ *   stage 1 decodes each sequence's blocks after the prefix; stage 2
+ *   attends every query row of each KV head to the prefix on the tcgen05
+ *   tensor cores (the prefill kernel of paged_prefill_attention, without
+ *   the causal mask) and keeps a (max, sum, output) partial per prefix
+ *   chunk; the merge kernel combines each sequence's prefix and tail
+ *   partials by log-sum-exp.  Three launches.
  *   prefix_blocks    device int32 [n_prefix_blocks]: physical ids of the
  *                    shared prefix, which is the first n_prefix_blocks * 16
  *                    tokens of every sequence: block_tables[b][0..n) must
@@ -309,9 +310,14 @@ pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *q, int32_t 
  *              A chunk longer than its cache, or a length past the table,
  *              sets PKV_DEVERR_CTX_RANGE.
  *   out        device bf16 [n_rows][n_q][d_head].
- * bf16 pools.  One launch; tensor-core tiles of 64 query rows per
- * (sequence, KV head) stream that sequence's blocks once per tile.
- * Errors: EINVAL, EUNSUPPORTED (FP8 / 4-bit pools, group size), ECUDA. */
+ * bf16 pools.  One launch (clusters of two CTAs, one CTA per SM): tiles of
+ * 128 query rows per (sequence, KV head) on the tcgen05 tensor cores; the
+ * two CTAs of a cluster share each K/V tile of the sequence (TMA multicast).
+ * An out-of-range block id is skipped (its keys masked) and sets
+ * PKV_DEVERR_BLOCK_RANGE; a qo_indptr that points past n_rows skips those
+ * rows' stores and sets PKV_DEVERR_CTX_RANGE.
+ * Errors: EINVAL, EUNSUPPORTED (FP8 / 4-bit pools, group size, more than
+ * 2^31 query rows x group size), ECUDA. */
 pkv_status paged_prefill_attention(pkv_pool *pool, const void *q, int64_t n_rows, int32_t n_q,
                                    const int32_t *qo_indptr, const int32_t *block_tables, int32_t max_blocks_per_seq,
                                    const int32_t *context_lens, int32_t batch, float scale, void *out, void *stream);
