@@ -1076,8 +1076,167 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
             ++consumed;
             if (!aborted) issue_next();
         };
+        // 4-bit pools: two blocks per softmax step.  The 4-bit path is bound by each
+        // warp's per-block chain, not by HBM (a block carries a quarter of a bf16 block's
+        // bytes): one max, rescale decision and shuffle reduction for 32 tokens, and four
+        // independent score MMA chains, per two stages.
+        auto block2 = [&](int j) {
+            const int s0i = consumed % S, s1i = (consumed + 1) % S;
+            if (!aborted) {
+                bool ok = mbar_wait_bounded(&bars[s0i], (uint32_t)(consumed / S) & 1u);
+                ok = mbar_wait_bounded(&bars[s1i], (uint32_t)((consumed + 1) / S) & 1u) && ok;
+                aborted = __any_sync(kFull, !ok);
+                if (aborted) {
+                    drain_from = consumed;
+                    if (lane == 0) atomicOr(a.err, PKV_DEVERR_TIMEOUT);
+                }
+            }
+            const bool ok0 = phys_st[s0i] >= 0, ok1 = phys_st[s1i] >= 0;
+            if (!aborted && (ok0 || ok1)) {
+                const uint32_t kb0 = smem_u32(ring + s0i * Gm::STAGE), kb1 = smem_u32(ring + s1i * Gm::STAGE);
+                // valid tokens of each block (none for a block whose id was out of range)
+                const int nv0 = ok0 ? min(kBlockSize, C_len - (a.skip_blocks + j) * kBlockSize) : 0;
+                const int nv1 = ok1 ? min(kBlockSize, C_len - (a.skip_blocks + j + 1) * kBlockSize) : 0;
+                constexpr int WPT = D / 32;  // packed key words per token row per thread
+                auto kwords = [&](uint32_t kb, uint32_t (&kx)[WPT], uint32_t (&ky)[WPT]) {
+                    if constexpr (WPT == 4) {
+                        const uint4 x = lds128(kb + swz<Gm::BOXB>(g8 * Gm::ROWB + 16 * c4));
+                        const uint4 y = lds128(kb + swz<Gm::BOXB>((g8 + 8) * Gm::ROWB + 16 * c4));
+                        kx[0] = x.x; kx[1] = x.y; kx[2] = x.z; kx[3] = x.w;
+                        ky[0] = y.x; ky[1] = y.y; ky[2] = y.z; ky[3] = y.w;
+                    } else {
+                        const uint2 x = lds64(kb + swz<Gm::BOXB>(g8 * Gm::ROWB + 8 * c4));
+                        const uint2 y = lds64(kb + swz<Gm::BOXB>((g8 + 8) * Gm::ROWB + 8 * c4));
+                        kx[0] = x.x; kx[1] = x.y;
+                        ky[0] = y.x; ky[1] = y.y;
+                    }
+                };
+                float sa0[4] = {0.f, 0.f, 0.f, 0.f}, sb0[4] = {0.f, 0.f, 0.f, 0.f};
+                float sa1[4] = {0.f, 0.f, 0.f, 0.f}, sb1[4] = {0.f, 0.f, 0.f, 0.f};
+                {
+                    uint32_t kx0[WPT], ky0[WPT], kx1[WPT], ky1[WPT];
+                    kwords(kb0, kx0, ky0);
+                    kwords(kb1, kx1, ky1);
+#pragma unroll
+                    for (int ks = 0; ks < NT; ++ks) {
+                        const int w = ks >> 1;
+                        const uint32_t x0 = (ks & 1) ? kx0[w] >> 8 : kx0[w], y0 = (ks & 1) ? ky0[w] >> 8 : ky0[w];
+                        const uint32_t x1 = (ks & 1) ? kx1[w] >> 8 : kx1[w], y1 = (ks & 1) ? ky1[w] >> 8 : ky1[w];
+                        const uint32_t fa0[4] = {i4_lo(x0), i4_lo(y0), i4_hi(x0), i4_hi(y0)};
+                        const uint32_t fa1[4] = {i4_lo(x1), i4_lo(y1), i4_hi(x1), i4_hi(y1)};
+                        mma16816<true>((ks & 1) ? sb0 : sa0, fa0, qf[ks][0], qf[ks][1]);
+                        mma16816<true>((ks & 1) ? sb1 : sa1, fa1, qf[ks][0], qf[ks][1]);
+                    }
+                }
+                // s[0..3]: block 0 (tokens g8, g8 + 8 x heads 2c, 2c+1), s[4..7]: block 1
+                float s[8];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    s[i] = (sa0[i] + sb0[i]) * qs;
+                    s[4 + i] = (sa1[i] + sb1[i]) * qs;
+                }
+                if (g8 >= nv0) s[0] = s[1] = -INFINITY;
+                if (g8 + 8 >= nv0) s[2] = s[3] = -INFINITY;
+                if (g8 >= nv1) s[4] = s[5] = -INFINITY;
+                if (g8 + 8 >= nv1) s[6] = s[7] = -INFINITY;
+                // ---- online softmax over the 32 tokens (a valid block has a valid token 0) ----
+                float bm0 = fmaxf(fmaxf(s[0], s[2]), fmaxf(s[4], s[6]));
+                float bm1 = fmaxf(fmaxf(s[1], s[3]), fmaxf(s[5], s[7]));
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
+                    bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
+                }
+                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+                const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+                float p[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) p[i] = exp2f(s[i] - ((i & 1) ? mn1 : mn0));
+                l0 = fmaf(l0, al0, (p[0] + p[2]) + (p[4] + p[6]));
+                l1 = fmaf(l1, al1, (p[1] + p[3]) + (p[5] + p[7]));
+                m0 = mn0;
+                m1 = mn1;
+                if (__any_sync(kFull, al0 != 1.0f || al1 != 1.0f)) {
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        o[t][0] *= al0;
+                        o[t][1] *= al1;
+                        o[t][2] *= al0;
+                        o[t][3] *= al1;
+                    }
+                }
+                // v = c * s + z per token: P V = (P * s) C + (P . z); masked tokens weigh 0
+                const float2 zero2 = make_float2(0.f, 0.f);
+                const float2 vp00 = g8 < nv0 ? vpbuf[s0i * kBlockSize + g8] : zero2;
+                const float2 vp01 = g8 + 8 < nv0 ? vpbuf[s0i * kBlockSize + g8 + 8] : zero2;
+                const float2 vp10 = g8 < nv1 ? vpbuf[s1i * kBlockSize + g8] : zero2;
+                const float2 vp11 = g8 + 8 < nv1 ? vpbuf[s1i * kBlockSize + g8 + 8] : zero2;
+                z0 = fmaf(z0, al0, fmaf(p[0], vp00.y, p[2] * vp01.y) + fmaf(p[4], vp10.y, p[6] * vp11.y));
+                z1 = fmaf(z1, al1, fmaf(p[1], vp00.y, p[3] * vp01.y) + fmaf(p[5], vp10.y, p[7] * vp11.y));
+                const uint32_t h00 = pack2<true>(p[0] * vp00.x, p[1] * vp00.x);
+                const uint32_t h01 = pack2<true>(p[2] * vp01.x, p[3] * vp01.x);
+                const uint32_t h10 = pack2<true>(p[4] * vp10.x, p[5] * vp10.x);
+                const uint32_t h11 = pack2<true>(p[6] * vp11.x, p[7] * vp11.x);
+                const float2 f00 = __half22float2(*reinterpret_cast<const __half2 *>(&h00));
+                const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&h01));
+                const float2 f10 = __half22float2(*reinterpret_cast<const __half2 *>(&h10));
+                const float2 f11 = __half22float2(*reinterpret_cast<const __half2 *>(&h11));
+                zs0 = fmaf(zs0, al0, (f00.x + f01.x) + (f10.x + f11.x));
+                zs1 = fmaf(zs1, al1, (f00.y + f01.y) + (f10.y + f11.y));
+                const uint32_t pb00 = movm_t(h00), pb01 = movm_t(h01), pb10 = movm_t(h10), pb11 = movm_t(h11);
+                // ---- O^T += V^T . P^T, both blocks (codes are finite: no masking needed) ----
+                constexpr int WPR = D / 64;  // words per token row per thread (2 or 1)
+                auto vwords = [&](uint32_t vb, uint32_t (&r0)[WPR], uint32_t (&r1)[WPR], uint32_t (&r2)[WPR],
+                                  uint32_t (&r3)[WPR]) {
+                    const int rows[4] = {2 * c4, 2 * c4 + 1, 2 * c4 + 8, 2 * c4 + 9};
+                    uint32_t *rr[4] = {r0, r1, r2, r3};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if constexpr (WPR == 2) {
+                            const uint2 v = lds64(vb + swz<Gm::BOXB>(rows[q] * Gm::ROWB + 8 * g8));
+                            rr[q][0] = v.x;
+                            rr[q][1] = v.y;
+                        } else {
+                            rr[q][0] = lds32(vb + swz<Gm::BOXB>(rows[q] * Gm::ROWB + 4 * g8));
+                        }
+                    }
+                };
+                uint32_t u0[WPR], u1[WPR], u2[WPR], u3[WPR], w0[WPR], w1[WPR], w2[WPR], w3[WPR];
+                vwords(kb0 + Gm::TILE, u0, u1, u2, u3);
+                vwords(kb1 + Gm::TILE, w0, w1, w2, w3);
+                auto tile2 = [&](auto tc) {
+                    constexpr int t = decltype(tc)::value;
+                    const uint32_t za = i4_rows<t % 4>(u0[t / 4], u1[t / 4]), zb = i4_rows<t % 4>(u2[t / 4], u3[t / 4]);
+                    const uint32_t zc = i4_rows<t % 4>(w0[t / 4], w1[t / 4]), zd = i4_rows<t % 4>(w2[t / 4], w3[t / 4]);
+                    const uint32_t fa[4] = {i4_lo(za), i4_hi(za), i4_lo(zb), i4_hi(zb)};
+                    const uint32_t fb[4] = {i4_lo(zc), i4_hi(zc), i4_lo(zd), i4_hi(zd)};
+                    mma16816<true>(o[t], fa, pb00, pb01);
+                    mma16816<true>(o[t], fb, pb10, pb11);
+                };
+                tile2(std::integral_constant<int, 0>{});
+                tile2(std::integral_constant<int, 1>{});
+                tile2(std::integral_constant<int, 2>{});
+                tile2(std::integral_constant<int, 3>{});
+                if constexpr (NT == 8) {
+                    tile2(std::integral_constant<int, 4>{});
+                    tile2(std::integral_constant<int, 5>{});
+                    tile2(std::integral_constant<int, 6>{});
+                    tile2(std::integral_constant<int, 7>{});
+                }
+            }
+            __syncwarp();
+            consumed += 2;
+            if (!aborted) {
+                issue_next();
+                issue_next();
+            }
+        };
         const int j_plain = has_new ? pc.j1 - 1 : pc.j1;  // has_new: the piece ends with the last block
-        for (int j = pc.j0; j < j_plain; ++j) block(j, std::false_type{});
+        int j = pc.j0;
+        if constexpr (I4) {
+            for (; j + 1 < j_plain; j += 2) block2(j);
+        }
+        for (; j < j_plain; ++j) block(j, std::false_type{});
         if constexpr (APPEND) {
             if (has_new) block(j_plain, std::true_type{});
         }
