@@ -417,11 +417,13 @@ def paged_decode_step(pool: Pool, q, k_new, v_new, block_tables, context_lens, s
 def _host_ptr(t, name, dtype, shape):
     import torch
 
-    if not isinstance(t, torch.Tensor) or t.is_cuda:
+    if type(t) is not torch.Tensor and not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a CPU torch tensor")
-    if t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
-        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {shape}")
-    return ctypes.c_void_p(t.data_ptr())
+    if t.is_cuda:
+        raise TypeError(f"{name} must be a CPU torch tensor")
+    if t.dtype is not dtype or t.shape != shape or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)}")
+    return t.data_ptr()
 
 
 def paged_decode_step_host(pool: Pool, q, k_new, v_new, block_tables, context_lens, scale: float, out,
@@ -430,16 +432,18 @@ def paged_decode_step_host(pool: Pool, q, k_new, v_new, block_tables, context_le
     copies in, steps, copies ``out`` back and synchronises the stream."""
     import torch
 
-    B, n_q, D = (int(x) for x in q.shape)
-    W = int(block_tables.shape[1])
-    args = (_host_ptr(q, "q", torch.bfloat16, (B, n_q, D)),
-            _host_ptr(k_new, "k_new", torch.bfloat16, (B, pool.n_kv, D)),
-            _host_ptr(v_new, "v_new", torch.bfloat16, (B, pool.n_kv, D)))
-    tp = _host_ptr(block_tables, "block_tables", torch.int32, (B, W))
-    cp = _host_ptr(context_lens, "context_lens", torch.int32, (B,))
-    op = _host_ptr(out, "out", torch.bfloat16, (B, n_q, D))
-    _check(load().paged_decode_step_host(pool.handle, *args, n_q, tp, W, cp, B, float(scale), op,
-                                         _stream_handle(stream)))
+    B, n_q, D = q.shape
+    W = block_tables.shape[1]
+    kv_shape = (B, pool.n_kv, D)
+    bf16, i32 = torch.bfloat16, torch.int32
+    qp = _host_ptr(q, "q", bf16, q.shape)
+    kp = _host_ptr(k_new, "k_new", bf16, kv_shape)
+    vp = _host_ptr(v_new, "v_new", bf16, kv_shape)
+    tp = _host_ptr(block_tables, "block_tables", i32, (B, W))
+    cp = _host_ptr(context_lens, "context_lens", i32, (B,))
+    op = _host_ptr(out, "out", bf16, q.shape)
+    st = torch.cuda.current_stream().cuda_stream if stream is None else _stream_handle(stream).value
+    _check(load().paged_decode_step_host(pool.handle, qp, kp, vp, n_q, tp, W, cp, B, float(scale), op, st))
     return out
 
 

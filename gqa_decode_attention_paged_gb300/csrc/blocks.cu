@@ -98,17 +98,6 @@ static int64_t block_bytes_of(const pkv_pool *pool)
 
 // Device address of a pinned host buffer, or null when `p` is not pinned
 // host memory this device can reach.
-static void *mapped_host(const void *p)
-{
-    cudaPointerAttributes at;
-    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
-        cudaGetLastError();
-        return nullptr;
-    }
-    if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
-    return at.devicePointer;
-}
-
 }  // namespace pkv
 
 using namespace pkv;
@@ -149,7 +138,7 @@ extern "C" pkv_status kv_swap_out(pkv_pool *pool, const int32_t *blocks, int64_t
     if (!blocks || !host_dst) return fail(PKV_EINVAL, "kv_swap_out: NULL pointer");
     if (((uintptr_t)blocks & 3u) || ((uintptr_t)host_dst & 15u))
         return fail(PKV_EINVAL, "kv_swap_out: ids must be 4-byte and the host buffer 16-byte aligned");
-    void *dev = mapped_host(host_dst);
+    void *dev = mapped_host_ptr(host_dst);
     if (!dev) return fail(PKV_EINVAL, "kv_swap_out: host buffer is not pinned host memory (cudaHostAlloc / cudaHostRegister)");
     BlockMoveArgs a = {};
     a.src_k = static_cast<const uint8_t *>(pool->k);
@@ -171,7 +160,7 @@ extern "C" pkv_status kv_swap_in(pkv_pool *pool, const void *host_src, const int
     if (!blocks || !host_src) return fail(PKV_EINVAL, "kv_swap_in: NULL pointer");
     if (((uintptr_t)blocks & 3u) || ((uintptr_t)host_src & 15u))
         return fail(PKV_EINVAL, "kv_swap_in: ids must be 4-byte and the host buffer 16-byte aligned");
-    void *dev = mapped_host(host_src);
+    void *dev = mapped_host_ptr(host_src);
     if (!dev) return fail(PKV_EINVAL, "kv_swap_in: host buffer is not pinned host memory (cudaHostAlloc / cudaHostRegister)");
     BlockMoveArgs a = {};
     a.dst_k = static_cast<uint8_t *>(pool->k);

@@ -1771,6 +1771,41 @@ extern "C" pkv_status paged_decode_step(pkv_pool *pool, const void *q, const voi
                        out, static_cast<cudaStream_t>(stream));
 }
 
+namespace pkv {
+
+// Host-memory gather for paged_decode_step_host: the step's inputs are read
+// straight from pinned host memory (through its device mapping, over the
+// CPU-GPU link) into the device staging area by one kernel, instead of one
+// copy-engine transfer per array.
+struct HostGather {
+    const uint8_t *src[5];  // device addresses of mapped host buffers
+    uint8_t *dst[5];
+    int64_t bytes[5];
+    int n;
+};
+
+__global__ void __launch_bounds__(256) host_gather_kernel(HostGather g)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int i = 0; i < g.n; ++i) {
+        const uint8_t *src = g.src[i];
+        uint8_t *dst = g.dst[i];
+        const int64_t n = g.bytes[i];
+        if ((((uintptr_t)src | (uintptr_t)dst | (uintptr_t)n) & 15u) == 0) {
+            for (int64_t k = t0; k < n / 16; k += stride)
+                reinterpret_cast<uint4 *>(dst)[k] = reinterpret_cast<const uint4 *>(src)[k];
+        } else if ((((uintptr_t)src | (uintptr_t)dst | (uintptr_t)n) & 3u) == 0) {
+            for (int64_t k = t0; k < n / 4; k += stride)
+                reinterpret_cast<uint32_t *>(dst)[k] = reinterpret_cast<const uint32_t *>(src)[k];
+        } else {
+            for (int64_t k = t0; k < n; k += stride) dst[k] = src[k];
+        }
+    }
+}
+
+}  // namespace pkv
+
 extern "C" pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host, const void *k_new_host,
                                              const void *v_new_host, int32_t n_q, const int32_t *block_tables_host,
                                              int32_t max_blocks_per_seq, const int32_t *context_lens_host,
@@ -1792,14 +1827,36 @@ extern "C" pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const void *srcs[5] = {q_host, k_new_host, v_new_host, block_tables_host, context_lens_host};
     const size_t offs[5] = {o_q, o_k, o_v, o_t, o_l}, lens[5] = {bq, bkv, bkv, bt, bl};
-    for (int i = 0; i < 5; ++i) {
-        cudaError_t e = cudaMemcpyAsync(d + offs[i], srcs[i], lens[i], cudaMemcpyHostToDevice, s);
-        if (e != cudaSuccess) return cuda_fail(e, "paged_decode_step_host: copy in");
+    // Pinned (mapped) inputs: one gather kernel reads them all; otherwise one copy each.
+    HostGather g = {};
+    g.n = 5;
+    bool mapped = true;
+    for (int i = 0; i < 5 && mapped; ++i) {
+        g.src[i] = static_cast<const uint8_t *>(mapped_host_ptr(srcs[i]));
+        g.dst[i] = d + offs[i];
+        g.bytes[i] = (int64_t)lens[i];
+        mapped = g.src[i] != nullptr;
     }
+    if (mapped) {
+        const int64_t units = (int64_t)(bq + 2 * bkv + bt + bl) / 16;
+        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(2 * std::max(1, pool->num_sms), (units + 255) / 256));
+        host_gather_kernel<<<grid, 256, 0, s>>>(g);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "paged_decode_step_host: gather");
+    } else {
+        for (int i = 0; i < 5; ++i) {
+            cudaError_t e = cudaMemcpyAsync(d + offs[i], srcs[i], lens[i], cudaMemcpyHostToDevice, s);
+            if (e != cudaSuccess) return cuda_fail(e, "paged_decode_step_host: copy in");
+        }
+    }
+    // Pinned (mapped), 16-byte aligned output: the kernels write it directly; otherwise staged and copied.
+    void *out_dev = mapped_host_ptr(out_host);
+    const bool direct_out = out_dev && ((uintptr_t)out_dev & 15u) == 0;
     st = step_device(pool, d + o_q, d + o_k, d + o_v, n_q, reinterpret_cast<const int32_t *>(d + o_t),
-                     max_blocks_per_seq, reinterpret_cast<const int32_t *>(d + o_l), batch, scale, d + o_o, s);
+                     max_blocks_per_seq, reinterpret_cast<const int32_t *>(d + o_l), batch, scale,
+                     direct_out ? out_dev : d + o_o, s);
     if (st != PKV_OK) return st;
-    cudaError_t e = cudaMemcpyAsync(out_host, d + o_o, bq, cudaMemcpyDeviceToHost, s);
+    cudaError_t e = direct_out ? cudaSuccess : cudaMemcpyAsync(out_host, d + o_o, bq, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "paged_decode_step_host: copy out");
     return PKV_OK;

@@ -86,6 +86,9 @@ pkv_status append_step_int4(pkv_pool *pool, const void *k_new, const void *v_new
                             const int32_t *lens, int batch, cudaStream_t s);
 pkv_status ensure_staging(pkv_pool *pool, size_t bytes);
 pkv_status make_tensor_maps(pkv_pool *pool);
+// The device address of pinned host memory (cudaHostAlloc / cudaHostRegister,
+// mapped into the device's address space), or null for any other pointer.
+void *mapped_host_ptr(const void *p);
 // A 3-D tiled TMA map over a query array [n_rows][n_q][d_head] bf16: box of
 // min(d_head, 64) columns x `heads` heads x `tokens` rows, 128-byte swizzle.
 pkv_status make_q_map(CUtensorMap *map, const void *q, int64_t n_rows, int n_q, int d_head, int heads, int tokens);

@@ -113,6 +113,17 @@ static pkv_status tiled_encoder(PFN_cuTensorMapEncodeTiled_v12000 *out)
     return PKV_OK;
 }
 
+void *mapped_host_ptr(const void *p)
+{
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type != cudaMemoryTypeHost || !at.devicePointer) return nullptr;
+    return at.devicePointer;
+}
+
 pkv_status make_q_map(CUtensorMap *map, const void *q, int64_t n_rows, int n_q, int d_head, int heads, int tokens)
 {
     PFN_cuTensorMapEncodeTiled_v12000 encode;

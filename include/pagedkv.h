@@ -256,13 +256,16 @@ pkv_status paged_decode_step(pkv_pool *pool, const void *q, const void *k_new, c
                              const int32_t *block_tables, int32_t max_blocks_per_seq,
                              const int32_t *context_lens, int32_t batch, float scale, void *out, void *stream);
 
-/* paged_decode_step for a caller holding its inputs in host memory: copies
+/* paged_decode_step for a caller holding its inputs in host memory: brings
  * q, k_new, v_new, block_tables and context_lens (host pointers, same
- * shapes; pinned memory makes the copies asynchronous) into a pool-owned
- * device staging area (grown with cudaMalloc when a call needs more), runs
- * the step on `stream`, copies the output back to out_host and synchronises
- * `stream`, so out_host is ready on return.  Errors: as paged_decode_step,
- * plus ENOMEM / ECUDA from staging and copies. */
+ * shapes) into a pool-owned device staging area (grown with cudaMalloc when
+ * a call needs more), runs the step on `stream`, delivers the output to
+ * out_host and synchronises `stream`, so out_host is ready on return.
+ * Pinned host memory (cudaHostAlloc / cudaHostRegister, mapped into the
+ * device's address space): one gather kernel reads all five inputs over the
+ * CPU-GPU link, and the step's kernels write a 16-byte aligned out_host
+ * directly; pageable memory: one copy per array in and one out.
+ * Errors: as paged_decode_step, plus ENOMEM / ECUDA from staging and copies. */
 pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host, const void *k_new_host,
                                   const void *v_new_host, int32_t n_q, const int32_t *block_tables_host,
                                   int32_t max_blocks_per_seq, const int32_t *context_lens_host, int32_t batch,

@@ -59,15 +59,21 @@ def test_fused_step_against_oracle(make):
         assert_close(out_f64(out), ref, w.name)
 
 
-def test_host_step_equals_device_step():
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_step_equals_device_step(pinned):
+    """Pinned buffers take the gather kernel and the direct output; pageable
+    ones one copy per array.  Both equal the device-pointer step bit for bit."""
     w = wl.llama3_8b()
     with make_pool(w) as p1, make_pool(w) as p2:
         fill(p1, w)
         fill(p2, w)
         d = step_inputs(w)
         a = pkv.paged_decode_step(p1, d["q"], d["k"], d["v"], d["tables"], d["lens"], float(w.scale))
-        h = {k: v.cpu().pin_memory() for k, v in d.items()}
-        out = torch.empty(tuple(d["q"].shape), dtype=torch.bfloat16).pin_memory()
+        pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+        h = {k: pin(v.cpu()) for k, v in d.items()}
+        out = pin(torch.empty(tuple(d["q"].shape), dtype=torch.bfloat16))
         for _ in range(2):  # the staging area is reused on the second call
+            out.zero_()
             pkv.paged_decode_step_host(p2, h["q"], h["k"], h["v"], h["tables"], h["lens"], float(w.scale), out)
             assert torch.equal(a.cpu().view(torch.int16), out.view(torch.int16))
+        assert p2.get_error() == 0
