@@ -658,7 +658,10 @@ def run_cascade(args):
 
     torch.cuda.set_device(0)
     stream = torch.cuda.current_stream()
-    w = wl.shared_prefix()
+    # the named workload if it has a shared prefix (shared_prefix, shared_prefix_long), else shared_prefix
+    w = wl.NAMED[args.workload]() if args.workload in wl.NAMED else None
+    if w is None or not w.shared_prefix_tokens:
+        w = wl.shared_prefix()
     acct = algorithmic_bytes(w)
     dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).cuda().view(dt)  # noqa: E731
     pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head, pkv.BF16)

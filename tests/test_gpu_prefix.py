@@ -38,6 +38,23 @@ def test_cascade_matches_oracle_and_plain_decode(make, n_pre):
     assert np.abs(casc - plain).max() < 1e-2
 
 
+def test_cascade_long_prefix_sampled_sequences():
+    """The 8192-token shared prefix of the long cascade workload (the prefix
+    stage runs many chunks): sampled sequences against the oracle."""
+    w = wl.shared_prefix_long()
+    n_pre = w.shared_prefix_tokens // 16
+    with make_pool(w) as pool:
+        fill(pool, w)
+        d = step_inputs(w)
+        pkv.paged_kv_append(pool, d["k"], d["v"], d["slots"])
+        casc = out_f64(_cascade(pool, w, d, n_pre))
+        torch.cuda.synchronize()
+        assert pool.get_error() == 0
+    pick = np.array([0, 1, 37, 64, 100, 127])
+    ref = mirror(w).decode(w.q[pick], w.block_tables[pick], w.context_lens[pick], w.scale)
+    assert_close(casc[pick], ref, "long shared prefix")
+
+
 def test_cascade_with_prefix_only_sequences():
     w = wl.build("cp_empty", 32, 8, 128, [257, 300, 257], seed=65, shared_prefix_tokens=256)
     lens = w.context_lens.copy()

@@ -306,6 +306,18 @@ def shared_prefix(seed: int = 5, batch: int = 128) -> Workload:
                  max_blocks_per_seq=129)
 
 
+def shared_prefix_long(seed: int = 7, batch: int = 128) -> Workload:
+    """128 sequences sharing an 8192-token prefix (512 blocks, 32 MB of K/V),
+    each with a private tail of 0..1024 tokens plus the token this step
+    appends: the regime where plain decode re-reads the prefix once per
+    sequence (about 4 GB per call, from L2) and the cascade reads it once."""
+    rng = np.random.default_rng([seed, 100])
+    tails = rng.integers(0, 1025, size=batch)
+    cl = 8192 + tails + 1
+    return build("shared_prefix_long_b128", 32, 8, 128, cl, seed=seed, shared_prefix_tokens=8192,
+                 max_blocks_per_seq=577)
+
+
 def int4_llama3(seed: int = 6, batch: int = 128) -> Workload:
     """The Llama3-8B decode shape (n_q=32, n_kv=8, d_head=128, lengths
     uniform in [1024, 2048]) on a 4-bit KV pool, batch 128 so that the
@@ -321,5 +333,6 @@ NAMED = {
     "long_context_70b": long_context_70b,
     "fp8_lognormal": fp8_lognormal,
     "shared_prefix": shared_prefix,
+    "shared_prefix_long": shared_prefix_long,
     "int4_llama3": int4_llama3,
 }
