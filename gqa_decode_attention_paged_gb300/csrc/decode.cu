@@ -748,6 +748,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
     using Gm = typename C::Gm;
     constexpr bool FP8 = KV == kKvFp8, I4 = KV == kKvInt4;
     static_assert(!(I4 && APPEND), "the fused step is not built for 4-bit pools");
+    static_assert(!I4 || C::kStages >= 2, "4-bit pools take two ring stages per softmax step");
     constexpr int S = C::kStages;
     constexpr int NW = C::NW;
     constexpr int NT = D / 16;  // 16-wide MMA tiles along d
