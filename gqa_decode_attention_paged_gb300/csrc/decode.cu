@@ -1828,6 +1828,28 @@ extern "C" pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const void *srcs[5] = {q_host, k_new_host, v_new_host, block_tables_host, context_lens_host};
     const size_t offs[5] = {o_q, o_k, o_v, o_t, o_l}, lens[5] = {bq, bkv, bkv, bt, bl};
+    // Pinned buffers, no per-launch timing: the call's launches are replayed from a CUDA graph
+    // captured on an earlier call with the same arguments (one submission instead of three).
+    pkv_host_step_key key;
+    {
+        const void *ptrs[6] = {q_host, k_new_host, v_new_host, block_tables_host, context_lens_host, out_host};
+        for (int i = 0; i < 6; ++i) key.ptr[i] = ptrs[i];
+        key.n_q = n_q;
+        key.W = max_blocks_per_seq;
+        key.batch = batch;
+        key.partition_tokens = pool->partition_tokens;
+        memcpy(&key.scale_bits, &scale, 4);
+        key.stage = pool->stage;
+        key.ws = pool->ws;
+        key.ws_bytes = pool->ws_bytes;
+        key.stream = stream;
+    }
+    if (pool->host_graph && !pool->timing && key == pool->host_key) {
+        cudaError_t e = cudaGraphLaunch(pool->host_graph, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "paged_decode_step_host: graph replay");
+        return PKV_OK;
+    }
     // Pinned (mapped) inputs: one gather kernel reads them all; otherwise one copy each.
     HostGather g = {};
     g.n = 5;
@@ -1838,10 +1860,10 @@ extern "C" pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host,
         g.bytes[i] = (int64_t)lens[i];
         mapped = g.src[i] != nullptr;
     }
+    const int64_t units = (int64_t)(bq + 2 * bkv + bt + bl) / 16;
+    const int ggrid = (int)std::max<int64_t>(1, std::min<int64_t>(2 * std::max(1, pool->num_sms), (units + 255) / 256));
     if (mapped) {
-        const int64_t units = (int64_t)(bq + 2 * bkv + bt + bl) / 16;
-        const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(2 * std::max(1, pool->num_sms), (units + 255) / 256));
-        host_gather_kernel<<<grid, 256, 0, s>>>(g);
+        host_gather_kernel<<<ggrid, 256, 0, s>>>(g);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "paged_decode_step_host: gather");
     } else {
@@ -1860,6 +1882,39 @@ extern "C" pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host,
     cudaError_t e = direct_out ? cudaSuccess : cudaMemcpyAsync(out_host, d + o_o, bq, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return cuda_fail(e, "paged_decode_step_host: copy out");
+    if (mapped && direct_out && !pool->timing) {
+        // capture this call's launches for the next call with the same arguments (the buffers
+        // have their final size now); a capture that fails only means no replay
+        key.stage = pool->stage;
+        key.ws = pool->ws;
+        key.ws_bytes = pool->ws_bytes;
+        if (!pool->capture_stream && cudaStreamCreateWithFlags(&pool->capture_stream, cudaStreamNonBlocking) != cudaSuccess) {
+            pool->capture_stream = nullptr;
+            cudaGetLastError();
+            return PKV_OK;
+        }
+        cudaStream_t cs = pool->capture_stream;
+        cudaGraph_t graph = nullptr;
+        bool ok = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
+        if (ok) {
+            host_gather_kernel<<<ggrid, 256, 0, cs>>>(g);
+            ok = cudaGetLastError() == cudaSuccess;
+            if (ok)
+                ok = step_device(pool, d + o_q, d + o_k, d + o_v, n_q, reinterpret_cast<const int32_t *>(d + o_t),
+                                 max_blocks_per_seq, reinterpret_cast<const int32_t *>(d + o_l), batch, scale, out_dev,
+                                 cs) == PKV_OK;
+            const bool ended = cudaStreamEndCapture(cs, &graph) == cudaSuccess;
+            ok = ok && ended && graph;
+        }
+        cudaGraphExec_t exec = nullptr;
+        if (ok && cudaGraphInstantiate(&exec, graph, 0) == cudaSuccess) {
+            if (pool->host_graph) cudaGraphExecDestroy(pool->host_graph);
+            pool->host_graph = exec;
+            pool->host_key = key;
+        }
+        if (graph) cudaGraphDestroy(graph);
+        cudaGetLastError();  // a failed capture leaves no error behind for the caller
+    }
     return PKV_OK;
 }
 

@@ -31,6 +31,24 @@ struct EventPair {
 
 }  // namespace pkv
 
+// The arguments a paged_decode_step_host graph was captured with.
+struct pkv_host_step_key {
+    const void *ptr[6] = {};  // q, k_new, v_new, block_tables, context_lens, out (host)
+    int n_q = 0, W = 0, batch = 0, partition_tokens = 0;
+    uint32_t scale_bits = 0;
+    const void *stage = nullptr, *ws = nullptr;
+    size_t ws_bytes = 0;
+    void *stream = nullptr;
+    bool operator==(const pkv_host_step_key &o) const
+    {
+        for (int i = 0; i < 6; ++i)
+            if (ptr[i] != o.ptr[i]) return false;
+        return n_q == o.n_q && W == o.W && batch == o.batch && partition_tokens == o.partition_tokens &&
+               scale_bits == o.scale_bits && stage == o.stage && ws == o.ws && ws_bytes == o.ws_bytes &&
+               stream == o.stream;
+    }
+};
+
 struct pkv_pool {
     int device = 0;
     int num_sms = 0;
@@ -53,6 +71,11 @@ struct pkv_pool {
     void *stage = nullptr;            // device staging for paged_decode_step_host (grow-only)
     size_t stage_bytes = 0;
     int partition_tokens = pkv::kDefaultPartitionTokens;
+    // paged_decode_step_host: the launches of a call with pinned buffers, captured as a CUDA
+    // graph and replayed while the call's arguments and the pool's buffers stay the same
+    cudaGraphExec_t host_graph = nullptr;
+    pkv_host_step_key host_key;
+    cudaStream_t capture_stream = nullptr;
     // timing / launch accounting
     std::mutex mu;
     bool timing = false;

@@ -299,6 +299,8 @@ pkv_status kv_pool_destroy(pkv_pool *pool)
     cudaFree(pool->err);
     cudaFree(pool->ws);
     cudaFree(pool->stage);
+    if (pool->host_graph) cudaGraphExecDestroy(pool->host_graph);
+    if (pool->capture_stream) cudaStreamDestroy(pool->capture_stream);
     for (auto &pe : pool->pending) {
         cudaEventDestroy(pe.start);
         cudaEventDestroy(pe.stop);

@@ -72,8 +72,15 @@ def test_host_step_equals_device_step(pinned):
         pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
         h = {k: pin(v.cpu()) for k, v in d.items()}
         out = pin(torch.empty(tuple(d["q"].shape), dtype=torch.bfloat16))
-        for _ in range(2):  # the staging area is reused on the second call
+        for _ in range(2):  # the staging area is reused on the second call (pinned: a graph replay)
             out.zero_()
             pkv.paged_decode_step_host(p2, h["q"], h["k"], h["v"], h["tables"], h["lens"], float(w.scale), out)
             assert torch.equal(a.cpu().view(torch.int16), out.view(torch.int16))
+        # new queries in the same host buffer: the replay reads them
+        q2 = torch.flip(d["q"], dims=[0]).contiguous()
+        b = pkv.paged_decode_step(p1, q2, d["k"], d["v"], d["tables"], d["lens"], float(w.scale))
+        h["q"].copy_(q2.cpu())
+        out.zero_()
+        pkv.paged_decode_step_host(p2, h["q"], h["k"], h["v"], h["tables"], h["lens"], float(w.scale), out)
+        assert torch.equal(b.cpu().view(torch.int16), out.view(torch.int16))
         assert p2.get_error() == 0
