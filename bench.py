@@ -476,8 +476,9 @@ def run_ours(args):
         h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_t, h_c))
         d2h = h_out.numel() * h_out.element_size()
 
-        def e2e_step():  # copies in, appends, decodes, copies out, synchronises
-            pkv.paged_decode_step_host(pool, h_q, h_k, h_v, h_t, h_c, float(w.scale), h_out, stream)
+        # the public host-buffer step on fixed pinned buffers (reads them in, appends, decodes,
+        # writes the output back, synchronises)
+        e2e_step = pkv.HostStep(pool, h_q, h_k, h_v, h_t, h_c, float(w.scale), h_out, stream)
 
         for _ in range(min(args.warmup, 10)):
             e2e_step()
@@ -492,7 +493,7 @@ def run_ours(args):
         e2e = {"value": e2e_total / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": n_e2e, "ms_per_step": 1e3 * e2e_s / n_e2e,
                "calls_per_s": allreduce_sum(n_e2e, world, device) / e2e_s,
-               "call": "paged_decode_step_host (pinned host inputs and output)"}
+               "call": "HostStep: paged_decode_step_host on fixed pinned host inputs and output"}
 
     if rank != 0:
         pool.close()

@@ -447,6 +447,39 @@ def paged_decode_step_host(pool: Pool, q, k_new, v_new, block_tables, context_le
     return out
 
 
+class HostStep:
+    """paged_decode_step_host on a fixed set of host buffers: the arguments
+    are checked once here; each call runs one step on the buffers' current
+    contents (refill them in place between calls) and returns ``out``.  With
+    pinned buffers the library replays the step's launches from a CUDA graph
+    after the first call, so a call is one ctypes call, one graph launch and
+    one synchronise."""
+
+    def __init__(self, pool: Pool, q, k_new, v_new, block_tables, context_lens, scale: float, out, stream=None):
+        import torch
+
+        B, n_q, D = q.shape
+        W = block_tables.shape[1]
+        kv_shape = (B, pool.n_kv, D)
+        bf16, i32 = torch.bfloat16, torch.int32
+        ptrs = (_host_ptr(q, "q", bf16, q.shape), _host_ptr(k_new, "k_new", bf16, kv_shape),
+                _host_ptr(v_new, "v_new", bf16, kv_shape))
+        tp = _host_ptr(block_tables, "block_tables", i32, (B, W))
+        cp = _host_ptr(context_lens, "context_lens", i32, (B,))
+        op = _host_ptr(out, "out", bf16, q.shape)
+        st = torch.cuda.current_stream().cuda_stream if stream is None else _stream_handle(stream).value
+        self.out = out
+        self._keep = (pool, q, k_new, v_new, block_tables, context_lens, out)  # the buffers outlive the object
+        self._fn = load().paged_decode_step_host
+        self._args = (pool.handle, *ptrs, n_q, tp, W, cp, B, float(scale), op, st)
+
+    def __call__(self):
+        status = self._fn(*self._args)
+        if status:
+            _check(status)
+        return self.out
+
+
 def paged_decode_attention_noalloc(pool: Pool, q, block_tables, context_lens, scale: float, out=None,
                                    stream=None):
     """paged_decode_attention with its scratch in the library's fixed 16 MiB

@@ -84,3 +84,20 @@ def test_host_step_equals_device_step(pinned):
         pkv.paged_decode_step_host(p2, h["q"], h["k"], h["v"], h["tables"], h["lens"], float(w.scale), out)
         assert torch.equal(b.cpu().view(torch.int16), out.view(torch.int16))
         assert p2.get_error() == 0
+
+
+def test_host_step_object_equals_call():
+    w = wl.llama3_8b()
+    with make_pool(w) as p1, make_pool(w) as p2:
+        fill(p1, w)
+        fill(p2, w)
+        d = step_inputs(w)
+        h = {k: v.cpu().pin_memory() for k, v in d.items()}
+        out1 = torch.empty(tuple(d["q"].shape), dtype=torch.bfloat16).pin_memory()
+        out2 = torch.empty_like(out1).pin_memory()
+        pkv.paged_decode_step_host(p1, h["q"], h["k"], h["v"], h["tables"], h["lens"], float(w.scale), out1)
+        step = pkv.HostStep(p2, h["q"], h["k"], h["v"], h["tables"], h["lens"], float(w.scale), out2)
+        for _ in range(3):
+            assert step() is out2
+            assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+        assert p2.get_error() == 0
