@@ -269,7 +269,7 @@ def oracle_step(m, w, seqs):
     return m.decode(w.q[idx], w.block_tables[idx], w.context_lens[idx], w.scale)
 
 
-def time_oracle(w, m, budget_s: float, max_reps: int = 1000):
+def time_oracle(w, m, budget_s: float, max_reps: int = 20000):
     """Time oracle steps over rotating single sequences until budget_s; returns
     (GB/s, seconds, sequences done, threads)."""
     import numpy as np
@@ -567,13 +567,24 @@ def run_ours(args):
     return 0
 
 
-def _timed(fn, reps: int, warmup: int, stream) -> float:
-    """ms per call of fn(), CUDA events around `reps` back-to-back calls."""
+def _timed(fn, reps: int, warmup: int, stream, flush=None) -> float:
+    """ms per call of fn(): CUDA events around `reps` back-to-back calls, or,
+    with a `flush` buffer, an event pair around each call with the buffer
+    written (evicting L2) before it."""
     import torch
 
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
+    if flush is not None:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in evs:
+            flush.fill_(1)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / reps
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(reps):
@@ -678,10 +689,11 @@ def run_cascade(args):
     pre = dev(w.block_tables[0, :n_pre], torch.int32)
     out_c, out_p = torch.empty_like(q), torch.empty_like(q)
     reps, warm = max(3, min(args.steps, 500)), max(3, args.warmup)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda") if args.flush_l2 else None
     casc_ms = _timed(lambda: pkv.paged_decode_attention_prefix(pool, q, pre, tables, lens, float(w.scale), out_c, stream),
-                     reps, warm, stream)
+                     reps, warm, stream, flush)
     plain_ms = _timed(lambda: pkv.paged_decode_attention(pool, q, tables, lens, float(w.scale), out_p, stream),
-                      reps, warm, stream)
+                      reps, warm, stream, flush)
     # the two paths on the same inputs (each is checked against the oracle by the tests)
     err = (out_c.float() - out_p.float()).abs().cpu().numpy()
     assert pool.get_error() == 0
@@ -699,7 +711,9 @@ def run_cascade(args):
         "dtype": "f32",
         "data": "synthetic",
         "config": dict(w.describe(), bytes_basis="unique KV slots", kv_bytes_unique=acct["kv_unique"],
-                       kv_bytes_logical=acct["kv_logical"]),
+                       kv_bytes_logical=acct["kv_logical"],
+                       l2=("flushed (512 MB write) before each timed call" if flush is not None else
+                           "not flushed: back-to-back calls")),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_source": peak_note},
         "agreement_with_plain_decode": {"max_abs": float(err.max()), "mean_abs": float(err.mean()),
