@@ -424,7 +424,8 @@ __device__ __forceinline__ uint32_t i4_rows(uint32_t wa, uint32_t wb)
 // (g8, c4) holds head g8's pairs of d for every k-step (zero for padding
 // heads g8 >= G).  bf16 KV: k-step ks covers d 16ks + {2c, 2c+1} and
 // 16ks + 8 + {2c, 2c+1}.  FP8 KV (f16 MMA): k-step 2kk+j covers
-// d 32kk + 8c + 4j + {0,1} and {2,3}, the order the E4M3 K fragments use.
+// d 32kk + 8c + 4j + {0,1} and {2,3}, the order the E4M3 K fragments use;
+// they are left as loaded (bf16) for q_frags_to_f16.
 // 4-bit KV (f16 MMA): q' = q * k_scale[g] per channel (the keys' per-channel
 // scale folded into q; their zero points add the same constant to every
 // score of a head and cancel in the softmax); k-step ks of thread c4 covers
@@ -454,14 +455,29 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs &a, int b, int g, 
         } else if constexpr (!FP8) {
             qf[ks][0] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 2 * c4) : 0u;
             qf[ks][1] = live ? *reinterpret_cast<const uint32_t *>(qrow + 16 * ks + 8 + 2 * c4) : 0u;
-        } else {
+        } else {  // raw bf16 pairs; q_frags_to_f16 converts them when the piece starts
             const int d0 = 32 * (ks >> 1) + 8 * c4 + 4 * (ks & 1);
             const uint2 r = live ? *reinterpret_cast<const uint2 *>(qrow + d0) : make_uint2(0, 0);
-            const float2 x0 = bf16x2_to_f32x2(r.x), x1 = bf16x2_to_f32x2(r.y);
-            qf[ks][0] = pack2<true>(x0.x, x0.y);
-            qf[ks][1] = pack2<true>(x1.x, x1.y);
+            qf[ks][0] = r.x;
+            qf[ks][1] = r.y;
         }
     }
+}
+
+// FP8 KV: the loaded bf16 pairs of q -> the f16 pairs the MMAs take (exact
+// for |q| < 65504 apart from f16's shorter exponent range), done when the
+// piece starts so that the load's latency stays hidden behind the piece
+// before.
+template <int D>
+__device__ __forceinline__ void q_frags_to_f16(uint32_t (&qf)[D / 16][2])
+{
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float2 x = bf16x2_to_f32x2(qf[ks][i]);
+            qf[ks][i] = pack2<true>(x.x, x.y);
+        }
 }
 
 // ---------------------------------------------------------------------------
@@ -862,6 +878,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
             qf[ks][0] = qn[ks][0];
             qf[ks][1] = qn[ks][1];
         }
+        if constexpr (FP8) q_frags_to_f16<D>(qf);  // before qn is loaded again
         if (have_nx) load_q_frags<D, G, KV>(a, nx.b, nx.g, g8, c4, qn);
         const float qs = a.qscale * (FP8 ? a.scales[pc.g] : 1.0f);
         const int C_len = cl[pc.b];
