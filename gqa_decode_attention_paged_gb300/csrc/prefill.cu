@@ -233,6 +233,25 @@ __device__ __forceinline__ void add_bf16x2_to(float &acc, uint32_t pk)
         : "r"(pk));
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (a.x b.x + c.x, a.y b.y + c.y), each rounded as fmaf, in one paired instruction
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;
@@ -621,13 +640,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!vis) sr[k] = __float_as_uint(-INFINITY);
                     }
                 }
+                // row maximum of this half: 8 independent chains of 3-input maxima
+                static_assert(HK == 64, "the max chains assume 64 keys per warp and step");
                 float m4[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) m4[i] = __uint_as_float(sr[i]);
-#pragma unroll
-                for (int k = 8; k < HK; ++k) m4[k & 7] = fmaxf(m4[k & 7], __uint_as_float(sr[k]));
-                const float bm_half = fmaxf(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])),
-                                            fmaxf(fmaxf(m4[4], m4[5]), fmaxf(m4[6], m4[7])));
+                for (int j = 0; j < 8; ++j) {
+                    auto v = [&](int t) { return __uint_as_float(sr[j + 8 * t]); };
+                    m4[j] = fmaxf(fmax3(fmax3(fmax3(v(0), v(1), v(2)), v(3), v(4)), v(5), v(6)), v(7));
+                }
+                const float bm_half = fmax3(fmax3(m4[0], m4[1], m4[2]), fmax3(m4[3], m4[4], m4[5]),
+                                            fmaxf(m4[6], m4[7]));
                 // the row maximum over both halves
                 float bm_other;
                 if (!(ok = exchange(bm_half, bm_other))) break;
@@ -645,8 +667,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t pk[HK / 2];
 #pragma unroll
                 for (int i = 0; i < HK / 2; ++i) {
-                    pk[i] = pack_bf16x2(ex2(fmaf(__uint_as_float(sr[2 * i]), a.qscale, nm)),
-                                        ex2(fmaf(__uint_as_float(sr[2 * i + 1]), a.qscale, nm)));
+                    const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
+                                           make_float2(a.qscale, a.qscale), make_float2(nm, nm));
+                    pk[i] = pack_bf16x2(ex2(x.x), ex2(x.y));
                     add_bf16x2_to(l4[i & 3], pk[i]);
                 }
                 if (s > 0) {  // the previous step's O += P V has finished: P is free, O is current
