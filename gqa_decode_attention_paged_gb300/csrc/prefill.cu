@@ -16,25 +16,29 @@
 //     time share a few sequences' K/V in L2.  CTA c takes tiles c, c + grid,
 //     ...; every warp walks the list itself from the chunk lengths (a window
 //     of 32 sequences held in registers), so no role hands tiles to another.
-//   * warp 4 streams Q (one 3-D TMA box per 64 columns) and the K tiles of
+//   * warp 8 streams Q (one 3-D TMA box per 64 columns) and the K tiles of
 //     128 keys (8 blocks of 16 tokens, one 2-D TMA box per block and 64
-//     columns) into a two-stage ring; warp 5 streams the V tiles likewise.
+//     columns) into a two-stage ring; warp 9 streams the V tiles likewise.
 //     A missing block or an out-of-range block id loads a box past the end of
 //     the pool (zero filled) and is masked out of the scores.
-//   * warp 6 issues the MMAs from one thread: S = Q K^T for step j into one
-//     of two S accumulators in tensor memory (128 columns each), then
-//     O += P V for step j-1 (P from shared memory), so the tensor cores
-//     compute the next scores while the softmax warps work on the current.
-//   * warps 0-3 own one query row each (row = TMEM lane): they read the row's
-//     128 scores, mask by position and block validity, and keep the online
-//     softmax in the exp2 domain with a lazily updated reference maximum: the
-//     accumulator O is rescaled (read, scaled and written back in tensor
-//     memory) only when a row's maximum grows by more than 2^8, so P stays
-//     at most 256 and almost every step skips the rescale.  P is rounded to
-//     bf16 for the MMA and the row sum l adds the rounded values, so the
-//     result is exactly a convex combination of the V rows with the weights
-//     the MMA used.  After the tile's last step they read O, divide by l and
-//     store bf16.
+//   * warp 10 issues S = Q K^T for step j into one of two S accumulators in
+//     tensor memory (128 fp32 columns each); warp 11 issues O_h += P_h V_h
+//     for each key half h of a step as soon as that half's P is in tensor
+//     memory, so the tensor cores compute the next scores while the softmax
+//     warps work on the current ones.
+//   * warps 0-7 run the softmax: warp w owns TMEM lanes (rows) 32 (w & 3) ..
+//     + 31 and keys 64 (w >> 2) .. + 63 of every step.  Each key half of a
+//     row keeps its own online softmax in the exp2 domain (reference maximum,
+//     row sum, and its own accumulator O_h in tensor memory), so the two warps
+//     of a lane quarter never wait for each other inside a tile.  The
+//     reference maximum is raised lazily (O_h read, scaled and written back
+//     only when a half's maximum grows by more than 2^8), so P stays at most
+//     256 and almost every step skips the rescale.  P is rounded to bf16 for
+//     the MMA, written over the half's scores, and the row sum adds the
+//     rounded values, so the result is exactly a convex combination of the V
+//     rows with the weights the MMA used.  At the tile's end the two warps of
+//     a lane quarter swap (reference maximum, row sum) through shared memory,
+//     combine O = (2^(m_0 - m) O_0 + 2^(m_1 - m) O_1) / l and store bf16.
 // Every mbarrier wait is bounded; on a timeout the CTA records
 // PKV_DEVERR_TIMEOUT, every role stops, the MMA and copy pipes are drained
 // (bounded) and the tensor memory is released before the CTA exits.
@@ -53,13 +57,13 @@ constexpr int kSoftmaxWarps = 8;        // two per TMEM lane quarter: each takes
 constexpr int kKWarp = 8, kVWarp = 9, kQkWarp = 10, kPvWarp = 11;
 constexpr int kThreads = 12 * 32;
 constexpr float kRescaleSlack = 8.0f;    // log2 of the largest P value allowed before O is rescaled
-constexpr uint32_t kTmemCols = 512;      // S0 at 0, S1 at 128, O at 256, P at 448
+// Tensor memory: S0 at 0, S1 at 128 (fp32 scores of a step), then one O
+// accumulator per key half (O0 at 256, O1 at 256 + D).  A key half's P (bf16
+// pairs: column j holds keys 2j, 2j + 1 of the half) is written over the first
+// 32 columns of that half's own scores.
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;
-constexpr uint32_t kColP = 448;          // P as bf16 pairs: column j holds keys 2j (low half) and 2j + 1
 constexpr int kKStages = 2, kVStages = 2;
-// after O: four columns through which the two warps that own a lane quarter
-// exchange per-row values (their key halves' maxima, and at the end their
-// halves of the row sum), [phase parity][half]
 constexpr uint32_t kHalf = 128 * 128;    // bytes of one 64-column half of a 128-row tile
 
 struct Args {
@@ -93,13 +97,17 @@ struct Layout {
     static constexpr uint32_t kV = kK + kKStages * KT;   // V stages
     static constexpr uint32_t kOut = kV + kVStages * KT;  // the finished tile, staged for coalesced stores
     static constexpr uint32_t kBar = kOut + QT;
+    // P_FULL and O_DONE: one per key half; DRAIN: one per issuer; PAIR: one per lane quarter
     enum { Q_FULL = 0, Q_FREE = 2, K_FULL = 4, K_EMPTY = 4 + kKStages, V_FULL = 4 + 2 * kKStages,
            V_EMPTY = V_FULL + kVStages, S_FULL = V_EMPTY + kVStages, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2,
-           O_DONE = P_FULL + 1, DRAIN = O_DONE + 1, OUT_FULL = DRAIN + 2, OUT_FREE = OUT_FULL + 1,
-           PAIR = OUT_FREE + 1, NBARS = PAIR + 4 };  // DRAIN + issuer, PAIR + lane quarter
+           O_DONE = P_FULL + 2, DRAIN = O_DONE + 2, OUT_FULL = DRAIN + 2, OUT_FREE = OUT_FULL + 1,
+           PAIR = OUT_FREE + 1, NBARS = PAIR + 4 };
     static constexpr uint32_t kTmemSlot = kBar + NBARS * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
-    static constexpr uint32_t kEnd = kAbort + 4;
+    // a tile's end: each key half's (reference maximum as bf16 bits, row sum) per row, for the other half
+    static constexpr uint32_t kXm = (kAbort + 4 + 15) / 16 * 16;  // [2 halves][kRows] uint16
+    static constexpr uint32_t kXl = kXm + 2 * kRows * 2;          // [2 halves][kRows] float
+    static constexpr uint32_t kEnd = kXl + 2 * kRows * 4;
     static constexpr size_t bytes = 1024 + kEnd;
 };
 
@@ -204,15 +212,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r)
                  : "memory");
 }
 
-__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v)
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
-}
 
-__device__ __forceinline__ void tmem_ld1(uint32_t taddr, uint32_t *r)
-{
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r[0]) : "r"(taddr) : "memory");
-}
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -392,11 +392,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
         for (int i = 0; i < L::NBARS; ++i) {
-            const bool by_warps = i == L::S_FREE || i == L::S_FREE + 1 || i == L::P_FULL || i == L::OUT_FULL ||
-                                  i == L::OUT_FREE;
+            const bool by_warps = i == L::OUT_FULL || i == L::OUT_FREE;
+            const bool by_half = i == L::P_FULL || i == L::P_FULL + 1;  // the four warps of a key half
             const bool both_ctas = (i >= L::K_EMPTY && i < L::K_EMPTY + kKStages) ||
                                    (i >= L::V_EMPTY && i < L::V_EMPTY + kVStages);
-            mbar_init(&bar[i], by_warps ? kSoftmaxWarps : (i >= L::PAIR || both_ctas) ? 2 : 1);
+            mbar_init(&bar[i], by_warps ? kSoftmaxWarps : by_half ? kSoftmaxWarps / 2 : (i >= L::PAIR || both_ctas) ? 2 : 1);
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -526,19 +526,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (s == t.n_steps - 1) umma_commit(&bar[L::Q_FREE + qb]);
                     }
                 } else {
-                    const int vst = gs % kVStages;
-                    if (!(ok = wait_all(&bar[L::P_FULL], gs & 1))) break;
+                    // O_h += P_h V_h for each key half h as soon as its P is in tensor memory; the
+                    // step's S buffer (which holds the two P) is free once both have run
+                    const int vst = gs % kVStages, st = gs & 1;
                     if (!(ok = wait_all(&bar[L::V_FULL + vst], (gs / kVStages) & 1))) break;
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t vb = base + L::kV + vst * L::KT;
+                    const uint32_t vb = base + L::kV + vst * L::KT;
+                    for (int h = 0; h < 2; ++h) {
+                        if (!(ok = wait_all(&bar[L::P_FULL + h], gs & 1))) break;
+                        tc_fence_after();
+                        if (lane == 0) {
 #pragma unroll
-                        for (int kk = 0; kk < kKeys / 16; ++kk) {
-                            const uint32_t at = tmem + kColP + 8 * kk;  // keys 16 kk .. 16 kk + 15 of P
-                            const uint64_t bd = smem_desc(vb + kk * 2048, kHalf, 1024);
-                            umma_ts(tmem + kColO, at, bd, idesc_pv, (s > 0 || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < kKeys / 32; ++kk) {  // keys 64 h + 16 kk .. + 15
+                                const uint32_t at = tmem + st * kKeys + h * (kKeys / 2) + 8 * kk;
+                                const uint64_t bd = smem_desc(vb + (h * (kKeys / 32) + kk) * 2048, kHalf, 1024);
+                                umma_ts(tmem + kColO + h * D, at, bd, idesc_pv, (s > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            umma_commit(&bar[L::O_DONE + h]);
                         }
-                        umma_commit(&bar[L::O_DONE]);
+                        __syncwarp();
+                    }
+                    if (!ok) break;
+                    if (lane == 0) {
+                        umma_commit(&bar[L::S_FREE + st]);
                         umma_commit_mc(&bar[L::V_EMPTY + vst], (uint16_t)0x3);
                     }
                 }
@@ -554,32 +563,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) set_abort();
     } else {
         // ---------------------------------------------------------- softmax
-        // warp w: TMEM lanes (rows) 32 (w & 3) .. + 31, keys 64 (w >> 2) .. + 63 of every step,
-        // and the same half of O's columns
+        // warp w: TMEM lanes (rows) 32 (w & 3) .. + 31 and keys 64 (w >> 2) .. + 63 of every step.
+        // The two key halves of a row run separate online softmaxes (each its own reference
+        // maximum, row sum and O accumulator), so the two warps of a lane quarter never wait for
+        // each other inside a tile; at the tile's end they combine the halves by log-sum-exp.
         constexpr int HK = kKeys / 2, HD = D / 2;
         const int quarter = warp & 3, ch = warp >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t col_red = kColO + D;
         uint64_t *pair = &bar[L::PAIR + quarter];
-        int pph = 0;  // exchanges with the partner warp so far (the pair barrier's phase)
-        // one per-row value each way with the partner warp; false on a timeout
-        auto exchange = [&](float mine, float &theirs) -> bool {
-            const uint32_t rc = tmem + lane_off + col_red + 2 * (pph & 1);
-            tmem_st1(rc + ch, __float_as_uint(mine));
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(pair);
-            if (!wait_all(pair, pph & 1)) return false;
-            ++pph;
-            tc_fence_after();
-            uint32_t v;
-            tmem_ld1(rc + (ch ^ 1), &v);
-            tmem_wait_ld();
-            theirs = __uint_as_float(v);
-            return true;
-        };
+        int pph = 0;              // completed phases of the pair barrier (two per tile)
+        bool o_in_use = false;    // the partner may still read this half's O (previous tile)
+        uint16_t *xm = reinterpret_cast<uint16_t *>(sm + L::kXm);
+        float *xl = reinterpret_cast<float *>(sm + L::kXl);
         constexpr int QB = kStepBlocks / 2;  // blocks of a step in this warp's key half
         // this warp's block ids of step 0 of tile t (lanes 0..QB-1)
         auto first_ids = [&](const Tile &t) -> int {
@@ -609,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (r < t.R && !in_out && ch == 0) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
             // this row's position: it sees keys 0 .. pos (every key of a shared chunk)
             const int pos = PARTIAL ? t.C - 1 : t.C - t.T + min(r, t.R - 1) / G;
-            float mref = -INFINITY;
+            float mref = -INFINITY;  // this half's reference maximum: a bf16 value (sent exactly at the end)
             float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // this half's row sum of the bf16-rounded P
             // block ids of this warp's 4 blocks of the next step (lanes 0..3), read one step ahead
             // (for the last step: the next tile's first ids): the same validity test as the
@@ -628,9 +624,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < HK / 32; ++c) tmem_ld32(tmem + lane_off + sb * kKeys + ch * HK + 32 * c, sr + 32 * c);
                 tmem_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[L::S_FREE + sb]);
 
                 const int key0 = s * kKeys + ch * HK;  // position of this warp's first key
                 if (!(mask == (1u << QB) - 1 && key0 + HK - 1 <= pos)) {
@@ -650,16 +643,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float bm_half = fmax3(fmax3(m4[0], m4[1], m4[2]), fmax3(m4[3], m4[4], m4[5]),
                                             fmaxf(m4[6], m4[7]));
-                // the row maximum over both halves
-                float bm_other;
-                if (!(ok = exchange(bm_half, bm_other))) break;
-                const float bm = fmaxf(bm_half, bm_other);
-                const float bms = bm * a.qscale;
+                const float bms = bm_half * a.qscale;
                 const bool resc = bms > mref + kRescaleSlack;
                 float alpha = 1.0f;
                 if (resc) {
-                    alpha = ex2(mref - bms);  // 0 when mref is -inf
-                    mref = bms;
+                    const float mnew = __bfloat162float(__float2bfloat16_ru(bms));  // >= bms
+                    alpha = ex2(mref - mnew);  // 0 when mref is -inf
+                    mref = mnew;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) l4[i] *= alpha;
                 }
@@ -672,37 +662,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[i] = pack_bf16x2(ex2(x.x), ex2(x.y));
                     add_bf16x2_to(l4[i & 3], pk[i]);
                 }
-                if (s > 0) {  // the previous step's O += P V has finished: P is free, O is current
-                    if (!(ok = wait_all(&bar[L::O_DONE], (gs - 1) & 1))) break;
-                    tc_fence_after();
+                if (s > 0) {
+                    // this half's previous O += P V has finished (waited at every step and at the
+                    // tile's end, so the parity waits follow the barrier's phases one by one); only
+                    // then may O be rescaled
+                    if (!(ok = wait_all(&bar[L::O_DONE + ch], (gs - 1) & 1))) break;
                     if (__any_sync(kFull, resc)) {
+                        tc_fence_after();
 #pragma unroll
-                        for (int c = 0; c < HD / 32; ++c) {
+                        for (int c = 0; c < D / 32; ++c) {
                             uint32_t o[32];
-                            tmem_ld32(tmem + lane_off + kColO + ch * HD + 32 * c, o);
+                            tmem_ld32(tmem + lane_off + kColO + ch * D + 32 * c, o);
                             tmem_wait_ld();
 #pragma unroll
                             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                            tmem_st32(tmem + lane_off + kColO + ch * HD + 32 * c, o);
+                            tmem_st32(tmem + lane_off + kColO + ch * D + 32 * c, o);
                         }
-                        tmem_wait_st();
                     }
                 }
-                tmem_st32(tmem + lane_off + kColP + ch * (HK / 2), pk);
+                // P over this half's scores of the step (already read)
+                tmem_st32(tmem + lane_off + sb * kKeys + ch * HK, pk);
                 tmem_wait_st();
+                if (o_in_use) {  // the partner has read this half's O of the previous tile
+                    if (!(ok = wait_all(pair, pph & 1))) break;
+                    ++pph;
+                    o_in_use = false;
+                }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[L::P_FULL]);
+                if (lane == 0) mbar_arrive(&bar[L::P_FULL + ch]);
             }
             if (!ok) break;
-            // epilogue: O / l for this tile's rows, this warp's half of the columns
-            if (!(ok = wait_all(&bar[L::O_DONE], (gs - 1) & 1))) break;
-            tc_fence_after();
+            // epilogue: combine the two halves (log-sum-exp), then O / l for this tile's rows,
+            // this warp's half of the columns
+            if (!(ok = wait_all(&bar[L::O_DONE + ch], (gs - 1) & 1))) break;
             const float l_half = (l4[0] + l4[1]) + (l4[2] + l4[3]);
-            float l_other;
-            if (!(ok = exchange(l_half, l_other))) break;
-            const float l = l_half + l_other;
+            xm[ch * kRows + row] = __bfloat16_as_ushort(__float2bfloat16_rn(mref));  // exact: a bf16 value
+            xl[ch * kRows + row] = l_half;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pair);
+            if (!(ok = wait_all(pair, pph & 1))) break;  // both halves' O and (m, l) are final
+            ++pph;
+            tc_fence_after();
+            const float m_ot = __bfloat162float(__ushort_as_bfloat16(xm[(ch ^ 1) * kRows + row]));
+            const float l_ot = xl[(ch ^ 1) * kRows + row];
+            const float mrow = fmaxf(mref, m_ot);  // the row's reference maximum
+            const float f_me = mref == -INFINITY ? 0.0f : ex2(mref - mrow);
+            const float f_ot = m_ot == -INFINITY ? 0.0f : ex2(m_ot - mrow);
+            const float l = l_half * f_me + l_ot * f_ot;
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+            const float f0 = ch == 0 ? f_me : f_ot, f1 = ch == 0 ? f_ot : f_me;
+            // columns ch * HD + 32 c .. + 31 of the row's O = f0 O0 + f1 O1
+            auto load_o = [&](int c, uint32_t (&o)[32]) {
+                uint32_t o1[32];
+                tmem_ld32(tmem + lane_off + kColO + ch * HD + 32 * c, o);
+                tmem_ld32(tmem + lane_off + kColO + D + ch * HD + 32 * c, o1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    o[i] = __float_as_uint(fmaf(f1, __uint_as_float(o1[i]), f0 * __uint_as_float(o[i])));
+            };
             if (PARTIAL) {  // (m, l, O) of this row for the merge, this warp's half of O
                 const bool rv = r < t.R;
                 const int64_t slot = a.pre_base + ((int64_t)t.b * a.batch + (rv ? r / G : 0)) * a.n_kv + t.g;
@@ -710,8 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < HD / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_off + kColO + ch * HD + 32 * c, o);
-                    tmem_wait_ld();
+                    load_o(c, o);
                     if (rv) {
 #pragma unroll
                         for (int q4 = 0; q4 < 8; ++q4)
@@ -720,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
                     }
                 }
-                if (rv && ch == 0) a.ws_ml[slot * G + r % G] = make_float2(mref, l);
+                if (rv && ch == 0) a.ws_ml[slot * G + r % G] = make_float2(mrow, l);
             } else if (t.rt0 < t.R) {  // (a pair's second tile may hold no rows)
                 // this warp's half row of O / l into the staging tile, 16-byte chunks
                 // swizzled within each 128-byte half row (conflict-free writes and reads)
@@ -730,8 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < HD / 32; ++c) {
                     uint32_t o[32];
-                    tmem_ld32(tmem + lane_off + kColO + ch * HD + 32 * c, o);
-                    tmem_wait_ld();
+                    load_o(c, o);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint4 w;
@@ -763,7 +781,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&bar[L::OUT_FREE]);
                 ++n_out;
             }
+            // both halves' O of this tile are read: the partner's next P may let O += P V overwrite them
             tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pair);
+            o_in_use = true;
             x += gridDim.x / 2;
             t = tn;
             have = have_n;
