@@ -1879,7 +1879,24 @@ extern "C" pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host,
     }
     const int64_t units = (int64_t)(bq + 2 * bkv + bt + bl) / 16;
     const int ggrid = (int)std::max<int64_t>(1, std::min<int64_t>(2 * std::max(1, pool->num_sms), (units + 255) / 256));
-    if (mapped) {
+    // Pinned (mapped), 16-byte aligned output: the kernels write it directly; otherwise staged and copied.
+    void *out_dev = mapped_host_ptr(out_host);
+    const bool direct_out = out_dev && ((uintptr_t)out_dev & 15u) == 0;
+    // Mapped inputs aligned as the kernels read them (16 bytes for q and the new rows, 4 for the
+    // tables and lengths): the step's kernels read them in place over the CPU-GPU link, no gather.
+    const bool direct_in = mapped && direct_out &&
+                           (((uintptr_t)g.src[0] | (uintptr_t)g.src[1] | (uintptr_t)g.src[2]) & 15u) == 0 &&
+                           (((uintptr_t)g.src[3] | (uintptr_t)g.src[4]) & 3u) == 0;
+    const uint8_t *in[5];
+    for (int i = 0; i < 5; ++i) in[i] = direct_in ? g.src[i] : d + offs[i];
+    auto run_step = [&](cudaStream_t ss) {
+        return step_device(pool, in[0], in[1], in[2], n_q, reinterpret_cast<const int32_t *>(in[3]),
+                           max_blocks_per_seq, reinterpret_cast<const int32_t *>(in[4]), batch, scale,
+                           direct_out ? out_dev : d + o_o, ss);
+    };
+    if (direct_in) {
+        // nothing to gather
+    } else if (mapped) {
         host_gather_kernel<<<ggrid, 256, 0, s>>>(g);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "paged_decode_step_host: gather");
@@ -1889,12 +1906,7 @@ extern "C" pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host,
             if (e != cudaSuccess) return cuda_fail(e, "paged_decode_step_host: copy in");
         }
     }
-    // Pinned (mapped), 16-byte aligned output: the kernels write it directly; otherwise staged and copied.
-    void *out_dev = mapped_host_ptr(out_host);
-    const bool direct_out = out_dev && ((uintptr_t)out_dev & 15u) == 0;
-    st = step_device(pool, d + o_q, d + o_k, d + o_v, n_q, reinterpret_cast<const int32_t *>(d + o_t),
-                     max_blocks_per_seq, reinterpret_cast<const int32_t *>(d + o_l), batch, scale,
-                     direct_out ? out_dev : d + o_o, s);
+    st = run_step(s);
     if (st != PKV_OK) return st;
     cudaError_t e = direct_out ? cudaSuccess : cudaMemcpyAsync(out_host, d + o_o, bq, cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
@@ -1914,12 +1926,11 @@ extern "C" pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host,
         cudaGraph_t graph = nullptr;
         bool ok = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) == cudaSuccess;
         if (ok) {
-            host_gather_kernel<<<ggrid, 256, 0, cs>>>(g);
-            ok = cudaGetLastError() == cudaSuccess;
-            if (ok)
-                ok = step_device(pool, d + o_q, d + o_k, d + o_v, n_q, reinterpret_cast<const int32_t *>(d + o_t),
-                                 max_blocks_per_seq, reinterpret_cast<const int32_t *>(d + o_l), batch, scale, out_dev,
-                                 cs) == PKV_OK;
+            if (!direct_in) {
+                host_gather_kernel<<<ggrid, 256, 0, cs>>>(g);
+                ok = cudaGetLastError() == cudaSuccess;
+            }
+            if (ok) ok = run_step(cs) == PKV_OK;
             const bool ended = cudaStreamEndCapture(cs, &graph) == cudaSuccess;
             ok = ok && ended && graph;
         }

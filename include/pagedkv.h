@@ -262,9 +262,13 @@ pkv_status paged_decode_step(pkv_pool *pool, const void *q, const void *k_new, c
  * a call needs more), runs the step on `stream`, delivers the output to
  * out_host and synchronises `stream`, so out_host is ready on return.
  * Pinned host memory (cudaHostAlloc / cudaHostRegister, mapped into the
- * device's address space): one gather kernel reads all five inputs over the
- * CPU-GPU link, and the step's kernels write a 16-byte aligned out_host
- * directly; pageable memory: one copy per array in and one out.
+ * device's address space) with q, k_new, v_new and out_host 16-byte aligned
+ * (tables and lengths 4-byte): the step's kernels read the inputs in place
+ * over the CPU-GPU link and write out_host directly; other pinned inputs:
+ * one gather kernel reads them into the staging area first; pageable
+ * memory: one copy per array in and one out.  With pinned buffers the
+ * call's launches are replayed from a CUDA graph while the arguments stay
+ * the same.
  * Errors: as paged_decode_step, plus ENOMEM / ECUDA from staging and copies. */
 pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host, const void *k_new_host,
                                   const void *v_new_host, int32_t n_q, const int32_t *block_tables_host,
