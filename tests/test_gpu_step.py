@@ -59,17 +59,28 @@ def test_fused_step_against_oracle(make):
         assert_close(out_f64(out), ref, w.name)
 
 
-@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
-def test_host_step_equals_device_step(pinned):
-    """Pinned buffers take the gather kernel and the direct output; pageable
-    ones one copy per array.  Both equal the device-pointer step bit for bit."""
+def _pinned_offset(t):
+    """A copy of t in pinned memory that starts one element past the
+    allocation's start (2 bytes for bf16: not 16-byte aligned)."""
+    buf = torch.empty(t.numel() + 1, dtype=t.dtype).pin_memory()
+    v = buf[1:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("mode", ["pinned", "pinned_offset", "pageable"])
+def test_host_step_equals_device_step(mode):
+    """Aligned pinned buffers are read in place by the step's kernels and the
+    output written directly; pinned buffers off the 16-byte grid go through
+    the gather kernel and a staged output copy; pageable ones one copy per
+    array.  All equal the device-pointer step bit for bit."""
     w = wl.llama3_8b()
     with make_pool(w) as p1, make_pool(w) as p2:
         fill(p1, w)
         fill(p2, w)
         d = step_inputs(w)
         a = pkv.paged_decode_step(p1, d["q"], d["k"], d["v"], d["tables"], d["lens"], float(w.scale))
-        pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+        pin = {"pinned": lambda t: t.pin_memory(), "pinned_offset": _pinned_offset, "pageable": lambda t: t}[mode]
         h = {k: pin(v.cpu()) for k, v in d.items()}
         out = pin(torch.empty(tuple(d["q"].shape), dtype=torch.bfloat16))
         for _ in range(2):  # the staging area is reused on the second call (pinned: a graph replay)
