@@ -43,6 +43,25 @@ def test_int4_append_and_decode_match_oracle(make):
         assert pool.get_error() == 0
 
 
+def test_int4_full_workload_sampled():
+    """The bench's 4-bit workload at full size (Llama3-8B shape, batch 128),
+    stepped as the bench steps it (append, then decode): the whole pool's codes
+    and value parameters bit-exact, and sampled sequences' outputs against the
+    oracle's fp64 attention."""
+    w = wl.int4_llama3()
+    with make_pool(w) as pool:
+        fill(pool, w)
+        out = run_step(pool, w)
+        torch.cuda.synchronize()
+        assert pool.get_error() == 0
+        m = mirror(w)
+        _check_pool(pool, m)
+        rng = np.random.default_rng(7)
+        idx = np.sort(rng.choice(w.batch, size=12, replace=False))
+        ref = m.decode(w.q[idx], w.block_tables[idx], w.context_lens[idx], w.scale)
+        assert_close(out_f64(out)[idx], ref, w.name + " (sampled)")
+
+
 def test_int4_partitions_csr_and_noalloc_agree():
     w = CASES[1]()
     with make_pool(w, 64) as pool:
