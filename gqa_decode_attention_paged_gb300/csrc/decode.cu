@@ -1013,9 +1013,11 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                     pb0 = movm_t(pack2<FP8>(p0, p1));
                     pb1 = movm_t(pack2<FP8>(p2, p3));
                 }
-                // masked tokens' V must not reach the MMA (0 * non-finite garbage)
-                const uint32_t mk01 = (2 * c4 < nv ? 0x0000ffffu : 0u) | (2 * c4 + 1 < nv ? 0xffff0000u : 0u);
-                const uint32_t mk23 = (2 * c4 + 8 < nv ? 0x0000ffffu : 0u) | (2 * c4 + 9 < nv ? 0xffff0000u : 0u);
+                // masked tokens' V must not reach the MMA (0 * non-finite garbage); 4-bit codes are finite
+                [[maybe_unused]] const uint32_t mk01 =
+                    (2 * c4 < nv ? 0x0000ffffu : 0u) | (2 * c4 + 1 < nv ? 0xffff0000u : 0u);
+                [[maybe_unused]] const uint32_t mk23 =
+                    (2 * c4 + 8 < nv ? 0x0000ffffu : 0u) | (2 * c4 + 9 < nv ? 0xffff0000u : 0u);
                 // ---- O^T += V^T . P^T ----
                 if constexpr (I4) {
                     // channels g8*D/8 .. +D/8 of tokens 2c, 2c+1, 2c+8, 2c+9: tile t row g8 is the span's
@@ -1369,8 +1371,7 @@ static int64_t max_slots(pkv_pool *pool, int batch, int n_kv, int max_blocks_per
 
 // Persistent grid of the decode kernel for (d_head, G, dtype) at `batch`.
 template <int D, int G, int KV, bool APPEND = false>
-static pkv_status decode_grid(pkv_pool *pool, int batch, int max_blocks_per_seq, int *grid, size_t *smem,
-                              int reserve_ctas_per_sm = 0)
+static pkv_status decode_grid(pkv_pool *pool, int batch, int max_blocks_per_seq, int *grid, size_t *smem)
 {
     using C = Cfg<D, G, KV>;
     auto kern = decode_kernel<D, G, KV, APPEND>;
@@ -1397,7 +1398,6 @@ static pkv_status decode_grid(pkv_pool *pool, int batch, int max_blocks_per_seq,
     // batches do not pay for launching and merging across idle warps.
     const int64_t ub_blocks = (int64_t)batch * pool->n_kv * max_blocks_per_seq;
     const int64_t want = (ub_blocks + (int64_t)C::NW * kMinBlocksPerWarp - 1) / ((int64_t)C::NW * kMinBlocksPerWarp);
-    occ = std::max(1, occ - reserve_ctas_per_sm);
     *grid = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)pool->num_sms * occ, want));
     return PKV_OK;
 }
