@@ -1071,24 +1071,31 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                         mma16816<false>(o[t], fa, pb0, pb1);
                     }
                 } else {
+                    // 8 bytes (d = 64 Q + 8 g8 .. + 7) of each of the thread's four token rows per load;
+                    // each 4-byte half j feeds tiles 4 Q + 2 j (d + 4 j + {0, 1}) and 4 Q + 2 j + 1 (+ {2, 3})
 #pragma unroll
-                    for (int P = 0; P < D / 32; ++P) {
-                        const uint32_t db = 32 * P + 4 * g8;
-                        const uint32_t r0 = lds32(vb + swz<Gm::BOXB>((2 * c4) * Gm::ROWB + db));
-                        const uint32_t r1 = lds32(vb + swz<Gm::BOXB>((2 * c4 + 1) * Gm::ROWB + db));
-                        const uint32_t r2 = lds32(vb + swz<Gm::BOXB>((2 * c4 + 8) * Gm::ROWB + db));
-                        const uint32_t r3 = lds32(vb + swz<Gm::BOXB>((2 * c4 + 9) * Gm::ROWB + db));
-                        uint32_t fa[4], fb[4];
-                        e4m3x4_to_f16x4(prmt(r0, r1, 0x5140u), fa[0], fa[1]);  // d0, d1 of tokens 2c,2c+1
-                        e4m3x4_to_f16x4(prmt(r0, r1, 0x7362u), fb[0], fb[1]);  // d2, d3
-                        e4m3x4_to_f16x4(prmt(r2, r3, 0x5140u), fa[2], fa[3]);  // tokens 2c+8, 2c+9
-                        e4m3x4_to_f16x4(prmt(r2, r3, 0x7362u), fb[2], fb[3]);
-                        if (nv < kBlockSize) {
-                            fa[0] &= mk01; fa[1] &= mk01; fa[2] &= mk23; fa[3] &= mk23;
-                            fb[0] &= mk01; fb[1] &= mk01; fb[2] &= mk23; fb[3] &= mk23;
+                    for (int Q = 0; Q < D / 64; ++Q) {
+                        const uint32_t db = 64 * Q + 8 * g8;
+                        const uint2 v0 = lds64(vb + swz<Gm::BOXB>((2 * c4) * Gm::ROWB + db));
+                        const uint2 v1 = lds64(vb + swz<Gm::BOXB>((2 * c4 + 1) * Gm::ROWB + db));
+                        const uint2 v2 = lds64(vb + swz<Gm::BOXB>((2 * c4 + 8) * Gm::ROWB + db));
+                        const uint2 v3 = lds64(vb + swz<Gm::BOXB>((2 * c4 + 9) * Gm::ROWB + db));
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const uint32_t r0 = j ? v0.y : v0.x, r1 = j ? v1.y : v1.x;
+                            const uint32_t r2 = j ? v2.y : v2.x, r3 = j ? v3.y : v3.x;
+                            uint32_t fa[4], fb[4];
+                            e4m3x4_to_f16x4(prmt(r0, r1, 0x5140u), fa[0], fa[1]);  // d0, d1 of tokens 2c,2c+1
+                            e4m3x4_to_f16x4(prmt(r0, r1, 0x7362u), fb[0], fb[1]);  // d2, d3
+                            e4m3x4_to_f16x4(prmt(r2, r3, 0x5140u), fa[2], fa[3]);  // tokens 2c+8, 2c+9
+                            e4m3x4_to_f16x4(prmt(r2, r3, 0x7362u), fb[2], fb[3]);
+                            if (nv < kBlockSize) {
+                                fa[0] &= mk01; fa[1] &= mk01; fa[2] &= mk23; fa[3] &= mk23;
+                                fb[0] &= mk01; fb[1] &= mk01; fb[2] &= mk23; fb[3] &= mk23;
+                            }
+                            mma16816<true>(o[4 * Q + 2 * j], fa, pb0, pb1);
+                            mma16816<true>(o[4 * Q + 2 * j + 1], fb, pb0, pb1);
                         }
-                        mma16816<true>(o[2 * P], fa, pb0, pb1);
-                        mma16816<true>(o[2 * P + 1], fb, pb0, pb1);
                     }
                 }
             }
@@ -1289,7 +1296,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
         }
         // channel of accumulator row g8 + 8i of tile t, per KV type
         auto chan = [&](int t, int i) {
-            return I4 ? g8 * (D / 8) + 2 * t + i : FP8 ? 32 * (t >> 1) + 4 * g8 + 2 * (t & 1) + i : 16 * t + g8 + 8 * i;
+            return I4 ? g8 * (D / 8) + 2 * t + i : FP8 ? 64 * (t >> 2) + 8 * g8 + 2 * (t & 3) + i : 16 * t + g8 + 8 * i;
         };
         const float vs = FP8 ? a.scales[a.n_kv + pc.g] : 1.0f;
         const bool h0 = 2 * c4 < G, h1 = 2 * c4 + 1 < G;  // this thread's heads exist
