@@ -32,7 +32,7 @@ def lib():
     return pkv.load()
 
 
-def test_header_declares_the_north_star_calls():
+def test_header_declares_the_pool_append_and_decode_calls():
     names = _declared_functions()
     for n in ("kv_pool_create", "paged_kv_append", "paged_decode_attention", "kv_bytes_per_token"):
         assert n in names
