@@ -71,10 +71,12 @@ def test_page_walk_printed_example():
 
 
 def test_slot_of_rejects_out_of_pool_ids():
-    row = np.array([3, 99, -1], dtype=np.int32)
+    row = np.array([3, 99, -1, 64, 63], dtype=np.int32)
     assert oracle.slot_of(row, 5, 16, 64) == 3 * 16 + 5
     assert oracle.slot_of(row, 16, 16, 64) == -1
     assert oracle.slot_of(row, 40, 16, 64) == -1
+    assert oracle.slot_of(row, 48, 16, 64) == -1  # the id one past the pool
+    assert oracle.slot_of(row, 79, 16, 64) == 63 * 16 + 15  # the pool's last slot
 
 
 def test_waste_bound_of_generated_tables():
@@ -532,13 +534,19 @@ def test_int4_mirror_layout_and_exact_values():
     rng = np.random.default_rng(13)
     n_kv, d, NB = 2, 64, 8
     T = NB * 16  # every slot written (an unwritten 4-bit key reads back as its zero point)
-    ks, kz = np.full((n_kv, d), 0.25, np.float32), np.full((n_kv, d), -2.0, np.float32)
+    # per-(head, channel) key scales (powers of two) and zero points, so that a code times its scale plus
+    # its zero point is exact in bf16 and a key dequantised with another head's or channel's
+    # parameters is a different value
+    h, c = np.meshgrid(np.arange(n_kv), np.arange(d), indexing="ij")
+    ks = (2.0 ** -(1 + (h + c) % 3)).astype(np.float32)
+    kz = (-(1.0 + h) - 0.5 * (c % 4)).astype(np.float32)
     m4 = oracle.PoolMirror(NB, 16, n_kv, d, oracle.INT4, k_scale=ks, k_zero=kz)
     mb = oracle.PoolMirror(NB, 16, n_kv, d)
     kc = rng.integers(0, 16, size=(T, n_kv, d))
     vc = rng.integers(0, 16, size=(T, n_kv, d))
     vc[..., 0], vc[..., 1] = 0, 15  # every value row spans the grid: s = 0.25 exactly
-    kb = wl.f32_to_bf16_bits((kc * 0.25 - 2.0).astype(np.float32))
+    kb = wl.f32_to_bf16_bits((kc * ks + kz).astype(np.float32))
+    assert np.array_equal(wl.bf16_bits_to_f32(kb), kc * ks + kz)  # exact in bf16
     vb = wl.f32_to_bf16_bits((vc * 0.25 - 1.0).astype(np.float32))
     slots = rng.permutation(NB * 16).astype(np.int64)
     m4.append(kb, vb, slots)
