@@ -106,6 +106,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pkv_timing_read.argtypes = [P, c.c_int32, c.POINTER(_Timing)]
         lib.kv_block_bytes.argtypes = [P]
         lib.kv_block_bytes.restype = c.c_int64
+        lib.kv_swap_entry_bytes.argtypes = [P]
+        lib.kv_swap_entry_bytes.restype = c.c_int64
         lib.kv_block_copy.argtypes = [P, P, P, c.c_int64, P]
         lib.kv_swap_out.argtypes = [P, P, c.c_int64, P, P]
         lib.kv_swap_in.argtypes = [P, P, P, c.c_int64, P]
@@ -505,8 +507,14 @@ def kv_block_bytes(pool: Pool) -> int:
     return int(load().kv_block_bytes(pool.handle))
 
 
+def kv_swap_entry_bytes(pool: Pool) -> int:
+    """Bytes of one swapped block: K, V and (4-bit pools) the value rows' (scale, zero point)."""
+    return int(load().kv_swap_entry_bytes(pool.handle))
+
+
 def kv_block_copy(pool: Pool, src_blocks, dst_blocks, stream=None):
-    """Copy blocks src_blocks[i] -> dst_blocks[i] (int32 CUDA tensors [n]), K and V."""
+    """Copy blocks src_blocks[i] -> dst_blocks[i] (int32 CUDA tensors [n]): K, V and
+    (4-bit pools) the value rows' parameters."""
     import torch
 
     n = int(src_blocks.shape[0])
@@ -527,12 +535,13 @@ def _pinned_ptr(t, name, nbytes):
 
 def kv_swap_out(pool: Pool, blocks, host_dst, stream=None):
     """Write blocks[i] (int32 CUDA tensor [n]) into pinned host tensor
-    ``host_dst`` as [n][2][kv_block_bytes] bytes (K then V)."""
+    ``host_dst`` as [n][kv_swap_entry_bytes] bytes (K, V, then the value
+    rows' parameters of a 4-bit pool)."""
     import torch
 
     n = int(blocks.shape[0])
     bp = _dev_ptr(blocks, "blocks", torch.int32, 1, (n,))
-    hp = _pinned_ptr(host_dst, "host_dst", n * 2 * kv_block_bytes(pool))
+    hp = _pinned_ptr(host_dst, "host_dst", n * kv_swap_entry_bytes(pool))
     _check(load().kv_swap_out(pool.handle, bp, n, hp, _stream_handle(stream)))
     return host_dst
 
@@ -544,7 +553,7 @@ def kv_swap_in(pool: Pool, host_src, blocks, stream=None):
 
     n = int(blocks.shape[0])
     bp = _dev_ptr(blocks, "blocks", torch.int32, 1, (n,))
-    hp = _pinned_ptr(host_src, "host_src", n * 2 * kv_block_bytes(pool))
+    hp = _pinned_ptr(host_src, "host_src", n * kv_swap_entry_bytes(pool))
     _check(load().kv_swap_in(pool.handle, hp, bp, n, _stream_handle(stream)))
 
 
@@ -625,5 +634,5 @@ __all__ = ["BF16", "FP8_E4M3", "INT4", "Pool", "PagedKVError", "kv_pool_create",
            "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
            "paged_decode_step_host", "paged_decode_attention_prefix", "paged_decode_attention_csr",
            "paged_prefill_attention",
-           "kv_bytes_per_token", "kv_block_bytes",
+           "kv_bytes_per_token", "kv_block_bytes", "kv_swap_entry_bytes",
            "kv_block_copy", "kv_swap_out", "kv_swap_in", "BlockAllocator", "load", "library_path"]

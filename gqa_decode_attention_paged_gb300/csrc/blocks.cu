@@ -6,10 +6,13 @@
 // allocator that decides which blocks those are.
 //
 // A block of the pool is one contiguous byte range in the K array and one in
-// the V array ([num_blocks][n_kv][16][d_head] each), block_bytes long.  Every
-// kernel here moves whole blocks in 16-byte vectors, grid-stride over
-// (block, array, 16-byte chunk): a pure copy, bound by HBM for device copies
-// and by the CPU-GPU link for swaps.  Swaps read and write pinned host memory
+// the V array ([num_blocks][n_kv][16][row bytes] each), block_bytes long; a
+// 4-bit pool's block also owns its value rows' (scale, zero point) pairs, one
+// contiguous range of param_bytes in the value-parameter array.  A block's
+// entry in a host swap buffer is [K bytes][V bytes][value parameters].  Every
+// kernel here moves whole entries in 16-byte vectors, grid-stride over
+// (block, 16-byte chunk of the entry): a pure copy, bound by HBM for device
+// copies and by the CPU-GPU link for swaps.  Swaps read and write pinned host memory
 // directly from the kernel (the host buffer is mapped into the device's
 // address space), with no staging copy.
 #include "pkv_internal.cuh"
@@ -23,13 +26,26 @@
 namespace pkv {
 
 struct BlockMoveArgs {
-    const uint8_t *src_k, *src_v;  // device pool arrays (copy, swap-out) or null (swap-in)
-    uint8_t *dst_k, *dst_v;        // device pool arrays (copy, swap-in) or null (swap-out)
+    uint8_t *k, *v, *p;            // device pool arrays: K, V, value parameters (4-bit pools; else null)
     const int32_t *src_ids, *dst_ids;  // block ids per pair (copy: both; swap-out: src; swap-in: dst)
-    uint8_t *host;                 // swap buffer [n][2][block_bytes] (device address of pinned memory)
-    int64_t n, num_blocks, block_bytes;
+    uint8_t *host;                 // swap buffer [n][entry bytes] (device address of pinned memory)
+    int64_t n, num_blocks, block_bytes, param_bytes;  // entry bytes = 2 block_bytes + param_bytes
     unsigned *err;
 };
+
+// Byte `off` of a block's entry: its array and the offset of that byte from
+// block id 0 of the array is base + id * stride.
+struct EntryByte {
+    uint8_t *base;
+    int64_t stride, off;
+};
+
+__device__ __forceinline__ EntryByte entry_byte(const BlockMoveArgs &a, int64_t off)
+{
+    if (off < a.block_bytes) return {a.k, a.block_bytes, off};
+    if (off < 2 * a.block_bytes) return {a.v, a.block_bytes, off - a.block_bytes};
+    return {a.p, a.param_bytes, off - 2 * a.block_bytes};
+}
 
 enum MoveKind { kCopy = 0, kSwapOut = 1, kSwapIn = 2 };
 
@@ -38,42 +54,36 @@ __global__ void __launch_bounds__(256) block_move_kernel(BlockMoveArgs a)
 {
     griddep_wait();  // ids and blocks may come from the previous kernel on the stream
     griddep_launch_dependents();
-    const int64_t chunks = a.block_bytes / 16;      // per array
-    const int64_t total = a.n * 2 * chunks;         // (pair, array, chunk)
+    const int64_t entry = 2 * a.block_bytes + a.param_bytes;
+    const int64_t chunks = entry / 16;               // per block
+    const int64_t total = a.n * chunks;              // (pair, chunk)
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int64_t pair = i / (2 * chunks);
-        const int64_t rem = i - pair * 2 * chunks;
-        const int arr = (int)(rem / chunks);  // 0: K, 1: V
-        const int64_t c = rem - (int64_t)arr * chunks;
-        const int64_t off = c * 16;
+        const int64_t pair = i / chunks;
+        const int64_t c = i - pair * chunks;
+        const EntryByte e = entry_byte(a, c * 16);
         if constexpr (KIND == kCopy) {
             const int64_t s = a.src_ids[pair], d = a.dst_ids[pair];
             if (s < 0 || s >= a.num_blocks || d < 0 || d >= a.num_blocks) {
-                if (rem == 0) atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
+                if (c == 0) atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
                 continue;
             }
-            const uint8_t *src = (arr ? a.src_v : a.src_k) + s * a.block_bytes + off;
-            uint8_t *dst = (arr ? a.dst_v : a.dst_k) + d * a.block_bytes + off;
-            *reinterpret_cast<uint4 *>(dst) = ldg_nc_v4(src);
+            *reinterpret_cast<uint4 *>(e.base + d * e.stride + e.off) = ldg_nc_v4(e.base + s * e.stride + e.off);
         } else if constexpr (KIND == kSwapOut) {
             const int64_t s = a.src_ids[pair];
             if (s < 0 || s >= a.num_blocks) {
-                if (rem == 0) atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
+                if (c == 0) atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
                 continue;
             }
-            const uint8_t *src = (arr ? a.src_v : a.src_k) + s * a.block_bytes + off;
-            uint8_t *dst = a.host + (pair * 2 + arr) * a.block_bytes + off;
-            *reinterpret_cast<uint4 *>(dst) = ldg_nc_v4(src);
+            *reinterpret_cast<uint4 *>(a.host + pair * entry + c * 16) = ldg_nc_v4(e.base + s * e.stride + e.off);
         } else {
             const int64_t d = a.dst_ids[pair];
             if (d < 0 || d >= a.num_blocks) {
-                if (rem == 0) atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
+                if (c == 0) atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
                 continue;
             }
-            const uint8_t *src = a.host + (pair * 2 + arr) * a.block_bytes + off;
-            uint8_t *dst = (arr ? a.dst_v : a.dst_k) + d * a.block_bytes + off;
-            *reinterpret_cast<uint4 *>(dst) = *reinterpret_cast<const uint4 *>(src);
+            *reinterpret_cast<uint4 *>(e.base + d * e.stride + e.off) =
+                *reinterpret_cast<const uint4 *>(a.host + pair * entry + c * 16);
         }
     }
 }
@@ -81,7 +91,7 @@ __global__ void __launch_bounds__(256) block_move_kernel(BlockMoveArgs a)
 template <int KIND>
 static pkv_status launch_move(pkv_pool *pool, const BlockMoveArgs &a, cudaStream_t s, const char *what)
 {
-    const int64_t total = a.n * 2 * (a.block_bytes / 16);
+    const int64_t total = a.n * ((2 * a.block_bytes + a.param_bytes) / 16);
     int64_t blocks = (total + 255) / 256;
     blocks = std::max<int64_t>(1, std::min<int64_t>(blocks, (int64_t)pool->num_sms * 8));
     LaunchScope ls(pool, kBlocks, s);
@@ -93,7 +103,27 @@ static pkv_status launch_move(pkv_pool *pool, const BlockMoveArgs &a, cudaStream
 
 static int64_t block_bytes_of(const pkv_pool *pool)
 {
-    return (int64_t)pool->n_kv * kBlockSize * pool->d_head * (pool->dtype == PKV_FP8_E4M3 ? 1 : 2);
+    return (int64_t)(pool->bytes_per_array / (size_t)pool->num_blocks);
+}
+
+// A 4-bit block's value parameters: (scale, zero point) fp32 per token row.
+static int64_t param_bytes_of(const pkv_pool *pool)
+{
+    return pool->dtype == PKV_INT4 ? (int64_t)pool->n_kv * kBlockSize * 2 * (int64_t)sizeof(float) : 0;
+}
+
+static BlockMoveArgs move_args(pkv_pool *pool, int64_t n)
+{
+    BlockMoveArgs a = {};
+    a.k = static_cast<uint8_t *>(pool->k);
+    a.v = static_cast<uint8_t *>(pool->v);
+    a.p = reinterpret_cast<uint8_t *>(pool->v_params);
+    a.n = n;
+    a.num_blocks = pool->num_blocks;
+    a.block_bytes = block_bytes_of(pool);
+    a.param_bytes = param_bytes_of(pool);
+    a.err = pool->err;
+    return a;
 }
 
 // Device address of a pinned host buffer, or null when `p` is not pinned
@@ -107,6 +137,11 @@ extern "C" int64_t kv_block_bytes(const pkv_pool *pool)
     return pool ? block_bytes_of(pool) : -1;
 }
 
+extern "C" int64_t kv_swap_entry_bytes(const pkv_pool *pool)
+{
+    return pool ? 2 * block_bytes_of(pool) + param_bytes_of(pool) : -1;
+}
+
 extern "C" pkv_status kv_block_copy(pkv_pool *pool, const int32_t *src_blocks, const int32_t *dst_blocks, int64_t n,
                                     void *stream)
 {
@@ -116,17 +151,9 @@ extern "C" pkv_status kv_block_copy(pkv_pool *pool, const int32_t *src_blocks, c
     if (!src_blocks || !dst_blocks) return fail(PKV_EINVAL, "kv_block_copy: NULL device pointer");
     if (((uintptr_t)src_blocks | (uintptr_t)dst_blocks) & 3u)
         return fail(PKV_EINVAL, "kv_block_copy: block id arrays must be 4-byte aligned");
-    BlockMoveArgs a = {};
-    a.src_k = static_cast<const uint8_t *>(pool->k);
-    a.src_v = static_cast<const uint8_t *>(pool->v);
-    a.dst_k = static_cast<uint8_t *>(pool->k);
-    a.dst_v = static_cast<uint8_t *>(pool->v);
+    BlockMoveArgs a = move_args(pool, n);
     a.src_ids = src_blocks;
     a.dst_ids = dst_blocks;
-    a.n = n;
-    a.num_blocks = pool->num_blocks;
-    a.block_bytes = block_bytes_of(pool);
-    a.err = pool->err;
     return launch_move<kCopy>(pool, a, static_cast<cudaStream_t>(stream), "kv_block_copy");
 }
 
@@ -140,15 +167,9 @@ extern "C" pkv_status kv_swap_out(pkv_pool *pool, const int32_t *blocks, int64_t
         return fail(PKV_EINVAL, "kv_swap_out: ids must be 4-byte and the host buffer 16-byte aligned");
     void *dev = mapped_host_ptr(host_dst);
     if (!dev) return fail(PKV_EINVAL, "kv_swap_out: host buffer is not pinned host memory (cudaHostAlloc / cudaHostRegister)");
-    BlockMoveArgs a = {};
-    a.src_k = static_cast<const uint8_t *>(pool->k);
-    a.src_v = static_cast<const uint8_t *>(pool->v);
+    BlockMoveArgs a = move_args(pool, n);
     a.src_ids = blocks;
     a.host = static_cast<uint8_t *>(dev);
-    a.n = n;
-    a.num_blocks = pool->num_blocks;
-    a.block_bytes = block_bytes_of(pool);
-    a.err = pool->err;
     return launch_move<kSwapOut>(pool, a, static_cast<cudaStream_t>(stream), "kv_swap_out");
 }
 
@@ -162,15 +183,9 @@ extern "C" pkv_status kv_swap_in(pkv_pool *pool, const void *host_src, const int
         return fail(PKV_EINVAL, "kv_swap_in: ids must be 4-byte and the host buffer 16-byte aligned");
     void *dev = mapped_host_ptr(host_src);
     if (!dev) return fail(PKV_EINVAL, "kv_swap_in: host buffer is not pinned host memory (cudaHostAlloc / cudaHostRegister)");
-    BlockMoveArgs a = {};
-    a.dst_k = static_cast<uint8_t *>(pool->k);
-    a.dst_v = static_cast<uint8_t *>(pool->v);
+    BlockMoveArgs a = move_args(pool, n);
     a.dst_ids = blocks;
     a.host = static_cast<uint8_t *>(dev);
-    a.n = n;
-    a.num_blocks = pool->num_blocks;
-    a.block_bytes = block_bytes_of(pool);
-    a.err = pool->err;
     return launch_move<kSwapIn>(pool, a, static_cast<cudaStream_t>(stream), "kv_swap_in");
 }
 

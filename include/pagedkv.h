@@ -367,13 +367,19 @@ pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void *q, int32_t
  * token rows, contiguous in each array.
  * --------------------------------------------------------------------- */
 
-/* Bytes of one block in one array: n_kv x 16 x d_head x (2 bf16, 1 FP8).
- * A swapped block occupies 2 x kv_block_bytes in a host buffer.  -1 for a
- * NULL pool. */
+/* Bytes of one block in one array (K or V): n_kv x 16 x d_head x (2 bf16,
+ * 1 FP8, 1/2 4-bit).  -1 for a NULL pool. */
 int64_t kv_block_bytes(const pkv_pool *pool);
 
+/* Bytes of one swapped block in a host buffer: its K bytes, its V bytes and,
+ * for a 4-bit pool, its value rows' (scale, zero point) fp32 pairs
+ * (n_kv x 16 x 8 bytes), in that order.  2 x kv_block_bytes for bf16 and FP8
+ * pools.  -1 for a NULL pool. */
+int64_t kv_swap_entry_bytes(const pkv_pool *pool);
+
 /* Copy blocks inside the pool: block dst_blocks[i] gets the K and V bytes of
- * src_blocks[i], every head and token row (the copy of copy-on-write).
+ * src_blocks[i], every head and token row, and for a 4-bit pool the value
+ * rows' (scale, zero point) pairs too (the copy of copy-on-write).
  *   src_blocks, dst_blocks  device int32 [n]; no dst may appear twice or
  *                           also as a src (unchecked; the copies run in
  *                           parallel).  A pair with an id outside
@@ -384,11 +390,12 @@ pkv_status kv_block_copy(pkv_pool *pool, const int32_t *src_blocks, const int32_
                          void *stream);
 
 /* Swap blocks out to host memory: entry i of host_dst receives block
- * blocks[i] as [K bytes][V bytes], 2 x kv_block_bytes per entry.
+ * blocks[i] as [K bytes][V bytes][value parameters, 4-bit pools only],
+ * kv_swap_entry_bytes per entry.
  *   blocks    device int32 [n]; out-of-range ids are skipped (their entry
  *             left untouched) and set PKV_DEVERR_BLOCK_RANGE.
  *   host_dst  pinned host memory (cudaHostAlloc, or cudaHostRegister),
- *             16-byte aligned, n x 2 x kv_block_bytes bytes; the kernel
+ *             16-byte aligned, n x kv_swap_entry_bytes bytes; the kernel
  *             writes it directly over the CPU-GPU link.  It holds the data
  *             once the work on `stream` has finished.
  * One launch.  Errors: EINVAL (also for pageable host memory), ECUDA. */

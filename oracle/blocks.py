@@ -103,26 +103,36 @@ class AllocatorModel:
 
 
 def copy_blocks(mirror, src, dst) -> None:
-    """Block dst[i] of the mirror gets block src[i]'s K and V rows (all heads)."""
+    """Block dst[i] of the mirror gets block src[i]'s K and V rows (all heads)
+    and, in a 4-bit mirror, its value rows' (scale, zero point)."""
     for s, d in zip((int(x) for x in src), (int(x) for x in dst)):
         mirror.k[d] = mirror.k[s]
         mirror.v[d] = mirror.v[s]
+        if mirror.v_params is not None:
+            mirror.v_params[d] = mirror.v_params[s]
+
+
+def _parts(mirror):
+    """The arrays one block owns, in host-entry order: K, V, then (4-bit) the value parameters."""
+    return [mirror.k, mirror.v] + ([mirror.v_params] if mirror.v_params is not None else [])
 
 
 def swap_out(mirror, ids) -> bytes:
-    """The host image of blocks ``ids``: per block, its K bytes then its V bytes."""
+    """The host image of blocks ``ids``: per block, its K bytes, its V bytes and,
+    in a 4-bit mirror, its value parameters' bytes."""
     parts = []
     for i in (int(x) for x in ids):
-        parts.append(np.ascontiguousarray(mirror.k[i]).tobytes())
-        parts.append(np.ascontiguousarray(mirror.v[i]).tobytes())
+        for arr in _parts(mirror):
+            parts.append(np.ascontiguousarray(arr[i]).tobytes())
     return b"".join(parts)
 
 
 def swap_in(mirror, image: bytes, ids) -> None:
-    """Blocks ``ids`` of the mirror get the K and V bytes of ``image`` (as swap_out lays it out)."""
-    per = mirror.k[0].nbytes
+    """Blocks ``ids`` of the mirror get the bytes of ``image`` (as swap_out lays it out)."""
+    arrs = _parts(mirror)
+    entry = sum(arr[0].nbytes for arr in arrs)
     for n, i in enumerate(int(x) for x in ids):
-        k = np.frombuffer(image, dtype=mirror.k.dtype, count=mirror.k[0].size, offset=(2 * n) * per)
-        v = np.frombuffer(image, dtype=mirror.v.dtype, count=mirror.v[0].size, offset=(2 * n + 1) * per)
-        mirror.k[i] = k.reshape(mirror.k[0].shape)
-        mirror.v[i] = v.reshape(mirror.v[0].shape)
+        off = n * entry
+        for arr in arrs:
+            arr[i] = np.frombuffer(image, dtype=arr.dtype, count=arr[0].size, offset=off).reshape(arr[0].shape)
+            off += arr[0].nbytes

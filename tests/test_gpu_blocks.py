@@ -35,11 +35,15 @@ def _same_pool(pool, m, what):
     gk, gv = pool_bytes(pool)
     mk, mv = mirror_bytes(m)
     assert np.array_equal(gk, mk) and np.array_equal(gv, mv), what
+    if m.v_params is not None:  # 4-bit: the value rows' (scale, zero point), bit for bit
+        assert np.array_equal(pool.v_params_view().cpu().numpy().view(np.uint32), m.v_params.view(np.uint32)), what
 
 
 WORKLOADS = [
     lambda: wl.build("bk_bf16", 32, 8, 128, [700, 33, 160, 1000], seed=81),
     lambda: wl.build("bk_fp8_d64", 8, 2, 64, [300, 17, 90], dtype="fp8", seed=82),
+    lambda: wl.build("bk_int4", 32, 8, 128, [500, 33, 700], dtype="int4", seed=83),
+    lambda: wl.build("bk_int4_d64", 8, 2, 64, [300, 17, 90], dtype="int4", seed=84),
 ]
 
 
@@ -75,10 +79,14 @@ def test_swap_out_then_in_matches_oracle(make):
     w = make()
     pool, m = _filled(w)
     bb = pkv.kv_block_bytes(pool)
-    assert bb == w.n_kv * 16 * w.d_head * w.elem_bytes
+    eb = pkv.kv_swap_entry_bytes(pool)
+    if w.dtype == "int4":
+        assert bb == w.n_kv * 16 * w.d_head // 2 and eb == 2 * bb + w.n_kv * 16 * 8
+    else:
+        assert bb == w.n_kv * 16 * w.d_head * w.elem_bytes and eb == 2 * bb
     rng = np.random.default_rng(9)
     out_ids = rng.choice(w.num_blocks, size=min(25, w.num_blocks), replace=False).astype(np.int32)
-    host = torch.zeros(len(out_ids) * 2 * bb, dtype=torch.uint8).pin_memory()
+    host = torch.zeros(len(out_ids) * eb, dtype=torch.uint8).pin_memory()
     pkv.kv_swap_out(pool, i32_dev(out_ids), host)
     torch.cuda.synchronize()
     image = swap_out(m, out_ids)
@@ -170,3 +178,35 @@ def test_copy_on_write_fork_and_decode():
     assert pool.get_error() == 0
     pool.close()
     lib_alloc.close()
+
+
+def test_int4_blocks_moved_then_decoded():
+    """4-bit pool: the shortest sequence's blocks are copied to unused blocks
+    and its table pointed at the copies; random host bytes are then swapped
+    over the originals.  The pool (codes and value parameters) stays bit-exact
+    with the oracle's, and decode reads the copies' codes with their own
+    parameters."""
+    w = WORKLOADS[2]()
+    pool, m = _filled(w)
+    b = int(np.argmin(w.context_lens))
+    nb0 = -(-int(w.context_lens[b]) // 16)
+    used = set(int(x) for x in w.block_tables[w.block_tables >= 0].ravel())
+    free = np.array(sorted(set(range(w.num_blocks)) - used), dtype=np.int32)
+    assert 0 < nb0 <= len(free)
+    src = w.block_tables[b, :nb0].astype(np.int32)
+    dst = free[:nb0]
+    pkv.kv_block_copy(pool, i32_dev(src), i32_dev(dst))
+    copy_blocks(m, src, dst)
+    rng = np.random.default_rng(5)
+    junk = torch.from_numpy(rng.integers(0, 256, size=nb0 * pkv.kv_swap_entry_bytes(pool), dtype=np.uint8))
+    junk = junk.pin_memory()
+    pkv.kv_swap_in(pool, junk, i32_dev(src))
+    swap_in(m, junk.numpy().tobytes(), src)
+    _same_pool(pool, m, "after copy and swap-in")
+    bt = w.block_tables.copy()
+    bt[b, :nb0] = dst
+    out = pkv.paged_decode_attention(pool, bf16_dev(w.q), i32_dev(bt), i32_dev(w.context_lens), float(w.scale))
+    torch.cuda.synchronize()
+    assert_close(out_f64(out), m.decode(w.q, bt, w.context_lens, w.scale), "4-bit decode after block moves")
+    assert pool.get_error() == 0
+    pool.close()
