@@ -268,6 +268,13 @@ def oracle_step(m, w, seqs):
     return m.decode(w.q[idx], w.block_tables[idx], w.context_lens[idx], w.scale)
 
 
+def _bytes_per_sequence(w) -> list:
+    """Bytes one sequence's decode must move, as algorithmic_bytes counts them:
+    its cached K and V (4-bit: codes plus the value rows' scale and zero), q and out."""
+    per_token = w.n_kv * w.kv_bytes_per_token_head
+    return [int(c) * per_token + 2 * w.n_q * w.d_head * 2 for c in w.context_lens]
+
+
 def time_oracle(w, m, budget_s: float, max_reps: int = 20000):
     """Time oracle steps over rotating single sequences until budget_s; returns
     (GB/s, seconds, sequences done, threads)."""
@@ -275,7 +282,7 @@ def time_oracle(w, m, budget_s: float, max_reps: int = 20000):
 
     import oracle
 
-    per_seq = [int(c) * 2 * w.n_kv * w.d_head * w.elem_bytes + 2 * w.n_q * w.d_head * 2 for c in w.context_lens]
+    per_seq = _bytes_per_sequence(w)
     done_bytes, n, t0 = 0, 0, time.perf_counter()
     b = 0
     while n < max_reps:
@@ -303,7 +310,7 @@ def run_reference(args):
     m = oracle_setup(w)
     # Each step decodes one sequence (rotating); sized so the run ends in minutes.
     times = []
-    per_seq = [int(c) * 2 * w.n_kv * w.d_head * w.elem_bytes + 2 * w.n_q * w.d_head * 2 for c in w.context_lens]
+    per_seq = _bytes_per_sequence(w)
     total_bytes = 0
     budget = 150.0
     t_run = time.perf_counter()
