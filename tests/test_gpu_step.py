@@ -74,7 +74,22 @@ def test_host_step_equals_device_step(mode):
     output written directly; pinned buffers off the 16-byte grid go through
     the gather kernel and a staged output copy; pageable ones one copy per
     array.  All equal the device-pointer step bit for bit."""
-    w = wl.llama3_8b()
+    _host_vs_device_step(wl.llama3_8b(), mode)
+
+
+@pytest.mark.parametrize("make,mode", [
+    (lambda: wl.build("hs_fp8", 32, 8, 128, [300, 1, 77, 1000], dtype="fp8", seed=61), "pinned"),
+    (lambda: wl.build("hs_int4", 32, 8, 128, [300, 1, 77, 1000], dtype="int4", seed=62), "pinned"),
+    (lambda: wl.build("hs_int4_d64", 8, 2, 64, [90, 17, 0, 257], dtype="int4", seed=63), "pinned_offset"),
+])
+def test_host_step_other_kv_types(make, mode):
+    """The host-buffer step on FP8 and 4-bit pools (their own append and
+    decode kernels behind the same gather, graph and in-place reads) equals
+    the device-pointer step bit for bit."""
+    _host_vs_device_step(make(), mode)
+
+
+def _host_vs_device_step(w, mode):
     with make_pool(w) as p1, make_pool(w) as p2:
         fill(p1, w)
         fill(p2, w)
