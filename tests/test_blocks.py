@@ -10,6 +10,8 @@ import numpy as np
 import pytest
 
 import gqa_decode_attention_paged_gb300 as pkv
+import oracle
+from oracle import blocks as oracle_blocks
 from oracle.blocks import AllocatorModel
 
 
@@ -71,6 +73,46 @@ def test_model_duplicate_entries_in_one_write():
     m.share([b])
     new, copies = m.prepare_write([b, b])
     assert copies == [(b, 1)] and new == [1, b] and m.ref[:2] == [1, 1]
+
+
+def _mirror4(nb=5):
+    """A 4-bit mirror whose bytes and value parameters differ from block to block and row to row."""
+    m = oracle.PoolMirror(nb, 16, 2, 64, oracle.INT4, k_scale=np.ones((2, 64), np.float32),
+                          k_zero=np.zeros((2, 64), np.float32))
+    m.k[:] = (np.arange(m.k.size) % 251).reshape(m.k.shape)
+    m.v[:] = ((np.arange(m.v.size) * 7 + 3) % 253).reshape(m.v.shape)
+    m.v_params[:] = np.arange(m.v_params.size, dtype=np.float32).reshape(m.v_params.shape)
+    return m
+
+
+def _pin_block_ops(bm):
+    """Copy and swap on a mirror against the documented entry layout: a block's
+    K bytes, its V bytes, then (4-bit) its value parameters."""
+    m = _mirror4()
+    k0, v0, p0 = m.k.copy(), m.v.copy(), m.v_params.copy()
+    bm.copy_blocks(m, [1, 3], [4, 0])
+    for s_, d_ in ((1, 4), (3, 0)):
+        assert (m.k[d_] == k0[s_]).all() and (m.v[d_] == v0[s_]).all() and (m.v_params[d_] == p0[s_]).all()
+    for i in (1, 2, 3):
+        assert (m.k[i] == k0[i]).all() and (m.v[i] == v0[i]).all() and (m.v_params[i] == p0[i]).all()
+    m = _mirror4()
+    img = bm.swap_out(m, [2, 0])
+    assert img == b"".join(a[i].tobytes() for i in (2, 0) for a in (m.k, m.v, m.v_params))
+    m2 = _mirror4()
+    m2.k[:], m2.v[:], m2.v_params[:] = 0, 0, 0
+    bm.swap_in(m2, img, [3, 1])
+    for s_, d_ in ((2, 3), (0, 1)):
+        assert (m2.k[d_] == m.k[s_]).all() and (m2.v[d_] == m.v[s_]).all()
+        assert (m2.v_params[d_] == m.v_params[s_]).all()
+    assert not m2.k[[0, 2, 4]].any() and not m2.v[[0, 2, 4]].any() and not m2.v_params[[0, 2, 4]].any()
+    mb = oracle.PoolMirror(3, 16, 1, 64)  # bf16: no parameter part
+    mb.k[:] = (np.arange(mb.k.size) % 65000).reshape(mb.k.shape)
+    mb.v[:] = 9
+    assert bm.swap_out(mb, [1]) == mb.k[1].tobytes() + mb.v[1].tobytes()
+
+
+def test_model_block_copy_and_swap_layout():
+    _pin_block_ops(oracle_blocks)
 
 
 # ------------------------------------------------- library against the model

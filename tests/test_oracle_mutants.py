@@ -111,7 +111,7 @@ def _run_pins(src: str, lib: str) -> None:
                 fn(*c)
             except pytest.skip.Exception:
                 pass
-            except Exception:
+            except (Exception, pytest.fail.Exception):  # pytest.raises signals "did not raise" with the latter
                 failed.append(name)
     print(json.dumps(sorted(set(failed))))
 
@@ -145,6 +145,63 @@ def test_every_planted_mistake_fails_a_pin(tmp_path):
     # assertion: that also turns the pins red, so it counts as caught
     survivors = [MUTANTS[i][0] for i, (failed, err) in res.items() if failed == []]
     assert not survivors, f"mutants that pass every pin: {survivors}"
+
+
+# The oracle's block model (Python): (name, text in oracle/blocks.py, replacement)
+BLOCK_MUTANTS = [
+    ("copy leaves a 4-bit block's value parameters behind",
+     "mirror.v_params[d] = mirror.v_params[s]", "pass"),
+    ("copy runs from destination to source",
+     "mirror.k[d] = mirror.k[s]", "mirror.k[s] = mirror.k[d]"),
+    ("swap entry holds V before K",
+     "[mirror.k, mirror.v]", "[mirror.v, mirror.k]"),
+    ("swap-in reads every array from the entry's start",
+     "off += arr[0].nbytes", "pass"),
+    ("swap-in entries without the parameter part",
+     "off = n * entry", "off = n * 2 * mirror.k[0].nbytes"),
+    ("free blocks handed out highest id first",
+     "for i, r in enumerate(self.ref):", "for i, r in reversed(list(enumerate(self.ref))):"),
+    ("copy-on-write also copies private blocks",
+     "if self.ref[i] > 1:", "if self.ref[i] >= 1:"),
+    ("release lets a block go more often than it is referenced",
+     "self._check_held(ids, count_repeats=True)", "self._check_held(ids, count_repeats=False)"),
+    ("copy-on-write starts without enough free blocks",
+     "if self.free_blocks() < need:", "if self.free_blocks() < need - 1:"),
+    ("share adds two references",
+     "self.ref[i] += 1", "self.ref[i] += 2"),
+]
+
+
+def test_every_planted_mistake_in_the_block_model_fails_a_pin(monkeypatch):
+    import types
+
+    sys.path[:0] = [HERE]
+    import test_blocks as tb
+    with open(os.path.join(ROOT, "oracle", "blocks.py")) as f:
+        text = f.read()
+    pins = [lambda bm: tb._pin_block_ops(bm)] + [
+        (lambda fn: lambda bm: (monkeypatch.setattr(tb, "AllocatorModel", bm.AllocatorModel), fn()))(fn)
+        for name, fn in inspect.getmembers(tb, inspect.isfunction) if name.startswith("test_model_")]
+    survivors = []
+    for name, old, new in [("control", None, None)] + BLOCK_MUTANTS:
+        src = text
+        if old is not None:
+            assert src.count(old) == 1, f"{name}: the text must occur once in the block model"
+            src = src.replace(old, new)
+        bm = types.ModuleType("mutant_blocks")
+        exec(compile(src, f"<{name}>", "exec"), bm.__dict__)
+        failed = 0
+        for pin in pins:
+            try:
+                pin(bm)
+            except (Exception, pytest.fail.Exception):
+                failed += 1
+        monkeypatch.undo()
+        if old is None:
+            assert failed == 0, "the unmutated block model fails its pins"
+        elif failed == 0:
+            survivors.append(name)
+    assert not survivors, f"mutants of the block model that pass every pin: {survivors}"
 
 
 if __name__ == "__main__":
