@@ -71,6 +71,9 @@ struct pkv_pool {
     void *stage = nullptr;            // device staging for paged_decode_step_host (grow-only)
     size_t stage_bytes = 0;
     int partition_tokens = pkv::kDefaultPartitionTokens;
+    // device address of paged_decode_attention_noalloc's scratch array in the
+    // context the pool was created in (looked up by kv_pool_create)
+    void *noalloc_scratch = nullptr;
     // paged_decode_step_host: the launches of a call with pinned buffers, captured as a CUDA
     // graph and replayed while the call's arguments and the pool's buffers stay the same
     cudaGraphExec_t host_graph = nullptr;
@@ -105,6 +108,10 @@ struct LaunchScope {
 };
 
 pkv_status ensure_workspace(pkv_pool *pool, size_t bytes);
+// The device address of paged_decode_attention_noalloc's scratch array on the
+// current device (cudaGetSymbolAddress; loads the decode code if it is not
+// loaded yet, which reserves the array's memory).
+pkv_status noalloc_scratch_address(void **out);
 pkv_status append_step_int4(pkv_pool *pool, const void *k_new, const void *v_new, const int32_t *tables, int W,
                             const int32_t *lens, int batch, cudaStream_t s);
 pkv_status ensure_staging(pkv_pool *pool, size_t bytes);
@@ -272,60 +279,6 @@ static inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 blo
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-
-// launch_pdl for a kernel launched in thread-block clusters of `cluster_x`
-// CTAs along x (gridDim.x must be a multiple of it).
-template <typename... KArgs, typename... Args>
-static inline cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                             unsigned cluster_x, cudaStream_t s, Args &&...args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = cluster_x;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-
-// Thread-block cluster helpers: a full cluster barrier (release / acquire),
-// and loads from a peer CTA's shared memory (distributed shared memory).
-__device__ __forceinline__ void cluster_sync_all()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_peer_addr(uint32_t local_smem_addr, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem_addr), "r"(rank));
-    return r;
-}
-
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr)
-{
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr)
-{
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-    return v;
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first()

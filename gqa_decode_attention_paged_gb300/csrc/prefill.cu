@@ -13,9 +13,13 @@
 // Design (one persistent CTA per SM, warp-specialised):
 //   * a tile is 128 query rows of one (sequence, KV head); the tile list is
 //     sequence-major, then KV head, then row tile, so the CTAs running at one
-//     time share a few sequences' K/V in L2.  CTA c takes tiles c, c + grid,
-//     ...; every warp walks the list itself from the chunk lengths (a window
-//     of 32 sequences held in registers), so no role hands tiles to another.
+//     time share a few sequences' K/V in L2.  Row tiles go in pairs: CTAs 2i
+//     and 2i + 1 take the two tiles of pair i, i + grid / 2, ..., so both
+//     stream the same K/V tiles at about the same time (the second read comes
+//     from L2).  Each CTA copies every tile it uses into its own shared
+//     memory; nothing is shared between CTAs.  Every warp walks the list
+//     itself from the chunk lengths (a window of 32 sequences held in
+//     registers), so no role hands tiles to another.
 //   * warp 8 streams Q (one 3-D TMA box per 64 columns) and the K tiles of
 //     128 keys (8 blocks of 16 tokens, one 2-D TMA box per block and 64
 //     columns) into a two-stage ring; warp 9 streams the V tiles likewise.
@@ -147,33 +151,6 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
                  ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
                  : "memory");
-}
-
-// Tiled 2-D TMA load multicast to the CTAs of `mask` (same shared-memory offset
-// and mbarrier offset in each).
-__device__ __forceinline__ void tma_load_2d_mc(void *dst_smem, const CUtensorMap *map, int x, int y, uint64_t *bar,
-                                               uint16_t mask, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst_smem)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask), "l"(policy)
-        : "memory");
-}
-
-// Arrive once on `bar` in every CTA of `mask` when the MMAs this thread issued so far have completed.
-__device__ __forceinline__ void umma_commit_mc(uint64_t *bar, uint16_t mask)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-                 ::"r"(smem_u32(bar)), "h"(mask)
-                 : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
 }
 
 // Arrive once on `bar` when every tcgen05 MMA this thread issued so far has completed.
@@ -311,11 +288,11 @@ __device__ __forceinline__ void load_window(Walker &w, const Args &a, int lane)
     w.tot = __shfl_sync(kFull, x, 31);
 }
 
-// Pair x of the list of row-tile pairs; this CTA (cluster rank `rank`) takes
-// row tile 2 i + rank of the pair's (sequence, KV head), i the pair's index
-// there (past the last row tile when the count is odd: no rows, the CTA only
-// keeps step with its partner).  Both CTAs stream the blocks the pair's last
-// row reaches.  False past the list's end.  Warp-wide, uniform result.
+// Pair x of the list of row-tile pairs; this CTA (`rank` = its index within
+// the pair) takes row tile 2 i + rank of the pair's (sequence, KV head), i the
+// pair's index there (past the last row tile when the count is odd: no rows
+// and no steps).  The CTA streams the blocks its own last row reaches.  False
+// past the list's end.  Warp-wide, uniform result.
 template <int G, bool PARTIAL>
 __device__ __forceinline__ bool find_tile(Walker &w, const Args &a, int x, int rank, Tile &t, int lane)
 {
@@ -353,7 +330,11 @@ __device__ __forceinline__ bool find_tile(Walker &w, const Args &a, int x, int r
         t.n_blocks = t.n_steps = 0;
         return true;
     }
-    const int last_row = min(t.R, pair_rt0 + 2 * kRows) - 1;
+    if (t.rt0 >= t.R) {  // the second tile of a pair with an odd tile count: no rows
+        t.n_blocks = t.n_steps = 0;
+        return true;
+    }
+    const int last_row = min(t.R, t.rt0 + kRows) - 1;
     t.n_blocks = (C - t.T + last_row / G) / kBlockSize + 1;
     t.n_steps = (t.n_blocks + kStepBlocks - 1) / kStepBlocks;
     return true;
@@ -385,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + L::kBar);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kAbort);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rank = (int)cluster_ctarank();
+    const int rank = (int)(blockIdx.x & 1);  // which tile of a pair
 
     if (tid == 0) {
         prefetch_tensormap(&tm_q);
@@ -394,9 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < L::NBARS; ++i) {
             const bool by_warps = i == L::OUT_FULL || i == L::OUT_FREE;
             const bool by_half = i == L::P_FULL || i == L::P_FULL + 1;  // the four warps of a key half
-            const bool both_ctas = (i >= L::K_EMPTY && i < L::K_EMPTY + kKStages) ||
-                                   (i >= L::V_EMPTY && i < L::V_EMPTY + kVStages);
-            mbar_init(&bar[i], by_warps ? kSoftmaxWarps : by_half ? kSoftmaxWarps / 2 : (i >= L::PAIR || both_ctas) ? 2 : 1);
+            mbar_init(&bar[i], by_warps ? kSoftmaxWarps : by_half ? kSoftmaxWarps / 2 : i >= L::PAIR ? 2 : 1);
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -409,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
-    cluster_sync_all();  // both CTAs' barriers exist before either multicasts into the other
+    __syncthreads();  // the barriers and the tensor-memory address are visible to every warp
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + L::kTmemSlot);
     // queries, tables and the appended chunk may come from the previous kernel.  In
@@ -468,15 +447,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (use > 0 && !(ok = wait_all(&empty[st], (use - 1) & 1))) break;
                 const bool present = lane < kStepBlocks && s * kStepBlocks + lane < t.n_blocks;
                 const bool valid = present && cur >= 0 && cur < a.num_blocks;
-                if (present && !valid && is_k && lane / (kStepBlocks / 2) == rank) atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
+                if (present && !valid && is_k) atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
                 if (lane == 0) mbar_arrive_expect_tx(&full[st], L::KT);
                 __syncwarp();
-                if (lane < kStepBlocks && lane / (kStepBlocks / 2) == rank) {  // this CTA's half, into both
+                if (lane < kStepBlocks) {  // lane k copies block k of the step
                     const int y = valid ? (int)((cur * (int64_t)a.n_kv + t.g) * kBlockSize) : a.oob_row;
                     uint8_t *dst = sm + ring + st * L::KT + lane * (kBlockSize * 128);
 #pragma unroll
-                    for (int h = 0; h < NH; ++h)
-                        tma_load_2d_mc(dst + h * kHalf, map, 64 * h, y, &full[st], (uint16_t)0x3, policy);
+                    for (int h = 0; h < NH; ++h) tma_load_2d(dst + h * kHalf, map, 64 * h, y, &full[st], policy);
                 }
             }
         }
@@ -522,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  smem_desc(kbase + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                         }
                         umma_commit(&bar[L::S_FULL + st]);
-                        umma_commit_mc(&bar[L::K_EMPTY + kst], (uint16_t)0x3);
+                        umma_commit(&bar[L::K_EMPTY + kst]);
                         if (s == t.n_steps - 1) umma_commit(&bar[L::Q_FREE + qb]);
                     }
                 } else {
@@ -548,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) break;
                     if (lane == 0) {
                         umma_commit(&bar[L::S_FREE + st]);
-                        umma_commit_mc(&bar[L::V_EMPTY + vst], (uint16_t)0x3);
+                        umma_commit(&bar[L::V_EMPTY + vst]);
                     }
                 }
                 __syncwarp();
@@ -794,60 +772,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     tc_fence_before();
-    cluster_sync_all();  // no copy or arrival from the partner is still on its way into this CTA
+    __syncthreads();  // every role is done with the tensor memory
     tc_fence_after();
     if (PARTIAL) griddep_wait();
     if (warp == kQkWarp)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
-// Clusters of two CTAs that fit on the device at once (one CTA per SM).
+// CTAs of the kernel that fit on the device at once (one per SM), rounded
+// down to whole pairs.
 template <int D, int G, bool PARTIAL>
-pkv_status setup(pkv_pool *pool, int *max_clusters)
+pkv_status setup(pkv_pool *pool, int *max_pairs)
 {
     using L = Layout<D>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
-    static int clusters = 0;
+    static int occ = 0;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(prefill_tc_kernel<D, G, PARTIAL>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
-        if (attr_err != cudaSuccess) return;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(2 * std::max(1, pool->num_sms / 2));
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = L::bytes;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        attr_err = cudaOccupancyMaxActiveClusters(&clusters, prefill_tc_kernel<D, G, PARTIAL>, &cfg);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, prefill_tc_kernel<D, G, PARTIAL>,
+                                                                     kThreads, L::bytes);
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "prefill kernel attributes");
-    if (clusters < 1) return fail(PKV_ECUDA, "prefill: no cluster of two CTAs fits on the device");
-    *max_clusters = clusters;
+    if (occ < 1) return fail(PKV_ECUDA, "prefill: the kernel does not fit on an SM");
+    *max_pairs = std::max(1, occ * pool->num_sms / 2);
     return PKV_OK;
 }
 
-// pairs: an upper bound on the row-tile pairs (the grid is at most one cluster per pair).
+// pairs: an upper bound on the row-tile pairs (the grid is at most two CTAs per pair).
 template <int D, int G, bool PARTIAL>
 pkv_status launch(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, int64_t pairs, const Args &a,
                   cudaStream_t s)
 {
     using L = Layout<D>;
-    int max_clusters = 0;
-    pkv_status st = setup<D, G, PARTIAL>(pool, &max_clusters);
+    int max_pairs = 0;
+    pkv_status st = setup<D, G, PARTIAL>(pool, &max_pairs);
     if (st != PKV_OK) return st;
     CUtensorMap tm_q;
     st = make_q_map(&tm_q, q, n_rows, n_q, D, G, kRows / G);
     if (st != PKV_OK) return st;
-    const int grid = 2 * (int)std::min<int64_t>(pairs, max_clusters);
+    const int grid = 2 * (int)std::min<int64_t>(pairs, max_pairs);
     LaunchScope ls(pool, PARTIAL ? kPrefix : kDecode, s);
-    cudaError_t e = launch_pdl_cluster(prefill_tc_kernel<D, G, PARTIAL>, dim3(grid), dim3(kThreads), L::bytes, 2, s,
-                                       tm_q, pool->tm_k, pool->tm_v, a);
+    cudaError_t e = launch_pdl(prefill_tc_kernel<D, G, PARTIAL>, dim3(grid), dim3(kThreads), L::bytes, s, tm_q,
+                               pool->tm_k, pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, PARTIAL ? "prefix stage launch" : "prefill launch");
     return PKV_OK;
@@ -922,7 +891,7 @@ void prefix_stage_chunks(pkv_pool *pool, int batch, int n_q, int n_prefix_blocks
 {
     const int G = n_q / pool->n_kv;
     const int64_t pairs_per_chunk = (int64_t)pool->n_kv * ((((int64_t)batch * G + kRows - 1) / kRows + 1) / 2);
-    // about one cluster per pair of SMs, and at least two steps of blocks per chunk
+    // about one CTA pair per pair of SMs, and at least two steps of blocks per chunk
     const int64_t want = std::max<int64_t>(1, (pool->num_sms / 2) / std::max<int64_t>(1, pairs_per_chunk));
     const int64_t cap = std::max<int64_t>(1, (n_prefix_blocks + 2 * kStepBlocks - 1) / (2 * kStepBlocks));
     const int nc = (int)std::min(want, cap);

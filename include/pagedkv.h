@@ -100,6 +100,7 @@ typedef struct {
     int64_t block_launches;  /* block copy / swap launches */
     double block_ms;
     int64_t timed_block;
+    int64_t workspace_bytes; /* bytes of the pool's split-KV workspace allocated so far */
 } pkv_timing;
 
 /* Create a pool of `num_blocks` blocks of `block_size` token slots, for
@@ -317,9 +318,9 @@ pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *q, int32_t 
  *              A chunk longer than its cache, or a length past the table,
  *              sets PKV_DEVERR_CTX_RANGE.
  *   out        device bf16 [n_rows][n_q][d_head].
- * bf16 pools.  One launch (clusters of two CTAs, one CTA per SM): tiles of
- * 128 query rows per (sequence, KV head) on the tcgen05 tensor cores; the
- * two CTAs of a cluster share each K/V tile of the sequence (TMA multicast).
+ * bf16 pools.  One launch (one persistent CTA per SM): tiles of 128 query
+ * rows per (sequence, KV head) on the tcgen05 tensor cores; each CTA copies
+ * the K/V tiles it uses into its own shared memory (TMA, this GPU's pool).
  * An out-of-range block id is skipped (its keys masked) and sets
  * PKV_DEVERR_BLOCK_RANGE; a qo_indptr that points past n_rows skips those
  * rows' stores and sets PKV_DEVERR_CTX_RANGE.
@@ -336,15 +337,23 @@ pkv_status paged_prefill_attention(pkv_pool *pool, const void *q, int64_t n_rows
  * cudaMalloc/cudaFree may synchronise the whole device, which a caller
  * running other streams' work cannot accept in its decode loop.
  * Same arguments, results and errors as paged_decode_attention, but the
- * split-KV scratch is a fixed 16 MiB array inside the library (every GPU
- * that loads the library holds it until the process exits) instead of the
- * pool's workspace; nothing is allocated and no allocating routine is called.
+ * split-KV scratch is a fixed 16 MiB array inside the library instead of the
+ * pool's workspace; the call allocates nothing and calls no allocating
+ * routine, and the pool's workspace stays as it was (empty if this is the
+ * only decode call used).
+ *   - When the array's memory is taken: kv_pool_create looks up the array's
+ *     device address (cudaGetSymbolAddress, with the pool's device current)
+ *     and keeps it in the pool.  Under CUDA's lazy module loading that lookup
+ *     is what loads the decode code onto the GPU, so the 16 MiB is taken when
+ *     the first pool is created on a device, before the caller sizes the
+ *     rest of HBM, and stays taken until the process exits.  The call itself
+ *     makes no such lookup.
  *   - A call whose scratch would exceed 16 MiB (roughly: more pieces x query
  *     heads x d_head x 4 bytes than fit) fails with PKV_ERANGE before
  *     launching; use paged_decode_attention then.
- *   - The pool's device must be current.  The first call on each device
- *     looks the array's device address up (cudaGetSymbolAddress); make that
- *     first call before any stream capture.
+ *   - The pool's device must be current.  A pool belongs to the CUDA context
+ *     it was created in: after cudaDeviceReset, create new pools (the old
+ *     ones, and their scratch address, are no longer valid).
  *   - All calls, from every pool and stream, share the one array and it
  *     keeps the last call's contents; nothing in it needs clearing (every
  *     partial a call reads, the same call wrote first).  Calls that overlap
