@@ -56,7 +56,8 @@ class _Timing(ctypes.Structure):
                 ("timed_decode", ctypes.c_int64), ("timed_merge", ctypes.c_int64),
                 ("prefix_launches", ctypes.c_int64), ("prefix_ms", ctypes.c_double),
                 ("timed_prefix", ctypes.c_int64), ("block_launches", ctypes.c_int64),
-                ("block_ms", ctypes.c_double), ("timed_block", ctypes.c_int64)]
+                ("block_ms", ctypes.c_double), ("timed_block", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64)]
 
 
 def library_path() -> str:

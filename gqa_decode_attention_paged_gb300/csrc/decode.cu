@@ -2078,30 +2078,20 @@ extern "C" pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *
 // fixed, file-scope device array instead, so it never allocates.
 // ---------------------------------------------------------------------------
 
-constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB, held by every GPU that loads the library
+constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 namespace pkv {
 
-constexpr int kMaxDevices = 64;
-static std::mutex g_noalloc_mu;
-static void *g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on `device` (which must be current).
-// Looked up once per device with cudaGetSymbolAddress; in host code the
-// array's name is only a host-side stand-in, never a device address.
-static pkv_status noalloc_scratch(int device, void **out)
+// In host code the array's name is only a host-side stand-in, never a device
+// address: the address comes from cudaGetSymbolAddress, in the context that
+// is current.  kv_pool_create calls this and keeps the result in the pool.
+pkv_status noalloc_scratch_address(void **out)
 {
-    if (device < 0 || device >= kMaxDevices)
-        return fail(PKV_EUNSUPPORTED, "paged_decode_attention_noalloc: device ordinal %d >= %d", device, kMaxDevices);
-    std::lock_guard<std::mutex> g(g_noalloc_mu);
-    if (!g_noalloc_ptr[device]) {
-        void *ptr = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
-        g_noalloc_ptr[device] = ptr;
-    }
-    *out = g_noalloc_ptr[device];
+    void *ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
+    *out = ptr;
     return PKV_OK;
 }
 
@@ -2181,9 +2171,8 @@ extern "C" pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void 
     if (cur != pool->device)
         return fail(PKV_EINVAL, "paged_decode_attention_noalloc: make the pool's device (%d) current, not %d",
                     pool->device, cur);
-    void *scratch = nullptr;
-    pkv_status st = noalloc_scratch(cur, &scratch);
-    if (st != PKV_OK) return st;
+    void *scratch = pool->noalloc_scratch;  // looked up when the pool was created
+    if (!scratch) return fail(PKV_ECUDA, "paged_decode_attention_noalloc: the pool has no scratch address");
 
     DecodeArgs a;
     a.num_blocks = pool->num_blocks;

@@ -249,6 +249,13 @@ pkv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv, 
         delete p;
         return cuda_fail(e, "kv_pool_create: device query");
     }
+    // paged_decode_attention_noalloc's scratch: its address is looked up now, which
+    // (lazy module loading) also takes the array's memory now, before the pool's
+    st = noalloc_scratch_address(&p->noalloc_scratch);
+    if (st != PKV_OK) {
+        delete p;
+        return st;
+    }
     p->num_blocks = num_blocks;
     p->block_size = block_size;
     p->n_kv = n_kv;
@@ -458,6 +465,7 @@ pkv_status pkv_timing_read(pkv_pool *pool, int32_t reset, pkv_timing *out)
         out->append_ms = pool->ms[kAppend];
         out->decode_ms = pool->ms[kDecode];
         out->merge_ms = pool->ms[kMerge];
+        out->workspace_bytes = (int64_t)pool->ws_bytes;
         out->timed_append = pool->timed[kAppend];
         out->timed_decode = pool->timed[kDecode];
         out->timed_merge = pool->timed[kMerge];
