@@ -4,14 +4,19 @@ One step = the whole hot path over one batch: append the new token of every
 sequence into the paged pool and decode attention for every sequence
 (paged_decode_step: the append fused into the decode kernel, then the
 split-KV merge kernel).  The same step as two calls (paged_kv_append,
-paged_decode_attention) is timed beside it.  The default workload is the Llama3-8B
-attention shape (n_q=32, n_kv=8, d_head=128, batch 64, lengths uniform in
-[1024, 2048], bf16 KV); ``--workload`` picks another.
+paged_decode_attention) is timed beside it.  The default workload is the 70B
+long-context shape (n_q=64, n_kv=8, d_head=128, batch 16, every sequence at
+32768 tokens: 2 GiB of bf16 K and V read per call), the largest of the
+workloads; ``--workload`` picks another.
 
 Prints one JSON line.  ``value`` is achieved KV-read bandwidth (algorithmic
 bytes: K and V of every cached token + q + out, per step) in GB/s over the
 device-timed region, summed over ranks; ``calls_per_s`` is decode calls per
-second.  ``--impl reference`` times the CPU oracle instead.
+second.  ``roofline`` is the decode kernel's event-timed fraction of the
+measured copy peak; ``per_config`` gives the same fraction, the step time and
+the parity against the oracle for each of the other workloads (tiny,
+Llama3-8B, FP8 log-normal, shared prefix, 4-bit).  ``--impl reference`` times
+the CPU oracle instead.
 
 ``--mode blocks`` instead measures the block-management kernels (copy-on-write
 block copies, swap out / in over the CPU-GPU link) and ``--mode cascade``
@@ -45,14 +50,19 @@ FALLBACK_HBM_GBS = 6800.0
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=15000)
+    p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="llama3_8b")
+    p.add_argument("--workload", default="long_context_70b")
     p.add_argument("--partition-tokens", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--flush-l2", action="store_true", help="write 512 MB between steps")
+    p.add_argument("--flush-l2", action="store_true", help="evict L2 between steps (512 MB written, 256 MB read)")
+    p.add_argument("--no-per-config", action="store_true", help="skip the other workloads' per_config entries")
+    p.add_argument("--kernel-seconds", type=float, default=1.0,
+                   help="least duration of the per-kernel timing pass (the clock sampler runs through it)")
+    p.add_argument("--config-seconds", type=float, default=0.4,
+                   help="timed duration per workload of the per_config entries")
     p.add_argument("--mode", default="decode", choices=["decode", "blocks", "cascade", "prefill"])
     return p.parse_args(argv)
 
@@ -223,7 +233,7 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         inside = [r for r in rows if self.t_start and self.t_stop and self.t_start <= r[0] <= self.t_stop]
         used = inside
-        note = "samples taken during the timed region"
+        note = "samples taken during the sampled window"
         if not used:  # region shorter than the sampling period: nearest samples after its start
             used = sorted(rows, key=lambda r: abs(r[0] - (self.t_stop or r[0])))[:2]
             note = "timed region shorter than the 100 ms sampling period; nearest samples"
@@ -345,6 +355,194 @@ def run_reference(args):
     return 0
 
 
+class L2Flush:
+    """Evicts L2 between timed calls: writes a 512 MB buffer (larger than the
+    129 MB L2), then reads a separate 256 MB one, so that the timed call
+    starts with a cold L2 that holds no dirty lines of the flush (their write
+    back would otherwise land inside the timed call)."""
+
+    def __init__(self, device):
+        import torch
+
+        self.w = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+        self.r = torch.zeros(64 * 1024 * 1024, dtype=torch.int32, device=device)
+
+    def __call__(self):
+        self.w.fill_(1)
+        self.r.max()
+
+
+class DecodeRig:
+    """One workload's pool and step inputs on the device, and its step: the
+    fused append + decode call (paged_decode_step), or for 4-bit pools the
+    append then the decode."""
+
+    def __init__(self, w, device, partition_tokens: int = 0):
+        import numpy as np
+        import torch
+
+        import gqa_decode_attention_paged_gb300 as pkv
+
+        self.pkv, self.w, self.device = pkv, w, device
+        dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(device).view(dt)  # noqa: E731
+        dt = {"bf16": pkv.BF16, "fp8": pkv.FP8_E4M3, "int4": pkv.INT4}[w.dtype]
+        self.pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head, dt)
+        if w.dtype == "fp8":
+            self.pool.set_fp8_scales(w.k_scale, w.v_scale)
+        if w.dtype == "int4":
+            self.pool.set_int4_key_params(w.k_scale, w.k_zero)
+        if partition_tokens:
+            self.pool.set_partition_tokens(partition_tokens)
+        self.pool.reserve_workspace(w.batch, w.n_q, w.max_blocks_per_seq)
+        T = w.fill_slots.shape[0]
+        for s in range(0, T, 1 << 20):
+            e = min(T, s + (1 << 20))
+            pkv.paged_kv_append(self.pool, dev(w.fill_k[s:e].view(np.int16), torch.bfloat16),
+                                dev(w.fill_v[s:e].view(np.int16), torch.bfloat16), dev(w.fill_slots[s:e], torch.int64))
+        self.k_new = dev(w.step_k.view(np.int16), torch.bfloat16)
+        self.v_new = dev(w.step_v.view(np.int16), torch.bfloat16)
+        self.slots = dev(w.step_slots, torch.int64)
+        self.q = dev(w.q.view(np.int16), torch.bfloat16)
+        self.tables = dev(w.block_tables, torch.int32)
+        self.lens = dev(w.context_lens, torch.int32)
+        self.out = torch.empty_like(self.q)
+        self.stream = torch.cuda.current_stream()
+        self.scale = float(w.scale)
+        torch.cuda.synchronize()
+
+    def step(self):
+        """One pass of the hot path: append every sequence's new token, decode."""
+        pkv, p = self.pkv, self.pool
+        if self.w.dtype == "int4":  # no fused step for 4-bit pools: append, then decode
+            pkv.paged_kv_append(p, self.k_new, self.v_new, self.slots, self.stream)
+            pkv.paged_decode_attention(p, self.q, self.tables, self.lens, self.scale, self.out, self.stream)
+        else:
+            pkv.paged_decode_step(p, self.q, self.k_new, self.v_new, self.tables, self.lens, self.scale, self.out,
+                                  self.stream)
+
+    def step_two_calls(self):
+        pkv, p = self.pkv, self.pool
+        pkv.paged_kv_append(p, self.k_new, self.v_new, self.slots, self.stream)
+        pkv.paged_decode_attention(p, self.q, self.tables, self.lens, self.scale, self.out, self.stream)
+
+    def kernel_pass(self, n: int, flush=None) -> dict:
+        """n steps with a CUDA event pair recorded by the library around each
+        of its launches on the launching stream; per-kernel averages."""
+        import torch
+
+        self.pool.timing_read(reset=True)
+        self.pool.timing_enable(True)
+        for _ in range(n):
+            if flush is not None:
+                flush()
+            self.step()
+        torch.cuda.synchronize()
+        self.pool.timing_enable(False)
+        tm = self.pool.timing_read(reset=True)
+        return {"decode_ms": tm["decode_ms"] / max(1, tm["timed_decode"]),
+                "merge_ms": tm["merge_ms"] / max(1, tm["timed_merge"]),
+                "append_ms": tm["append_ms"] / max(1, tm["timed_append"]), "steps": n}
+
+    def timed_steps(self, n: int, flush=None) -> float:
+        """ms per step: events around n back-to-back steps, or with a flush,
+        an event pair around each step (the flush outside it)."""
+        import torch
+
+        if flush is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            for _ in range(n):
+                self.step()
+            e1.record(self.stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / n
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            flush()
+            a.record(self.stream)
+            self.step()
+            b.record(self.stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / n
+
+    def close(self):
+        import torch
+
+        self.pool.close()
+        for name in ("k_new", "v_new", "slots", "q", "tables", "lens", "out"):
+            setattr(self, name, None)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def parity_vs_oracle(w, got_bits) -> dict:
+    """The oracle's step on the whole batch against the GPU output (bf16
+    patterns, [B][n_q][d]); the tolerances of the parity tests."""
+    import numpy as np
+
+    import workloads as wl
+
+    m = oracle_setup(w)
+    ref = oracle_step(m, w, list(range(w.batch)))
+    got = wl.bf16_bits_to_f32(got_bits).reshape(ref.shape).astype(np.float64)
+    err = np.abs(got - ref)
+    return {"max_abs": float(err.max()), "mean_abs": float(err.mean()), "tol_max_abs": 1e-2, "tol_mean_abs": 1e-3,
+            "ok": bool(np.isfinite(got).all() and err.max() <= 1e-2 and err.mean() <= 1e-3),
+            "sample": f"every output of the batch ({w.batch} sequences x {w.n_q} heads x {w.d_head})"}, m
+
+
+def out_bits(t):
+    import numpy as np
+    import torch
+
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# Workloads whose KV is under ~4x L2 are timed with L2 flushed between calls.
+FLUSHED = {"tiny", "shared_prefix"}
+PER_CONFIG = ["long_context_70b", "llama3_8b", "fp8_lognormal", "shared_prefix", "int4_llama3", "tiny"]
+
+
+def measure_config(name: str, device, warmup: int, seconds: float, peak: float, sha: str) -> dict:
+    """One workload's decode-kernel roofline fraction, step time and parity
+    against the oracle (a per_config entry of the bench line)."""
+    import workloads as wl
+
+    w = wl.NAMED[name]()
+    acct = algorithmic_bytes(w)
+    shared = w.shared_prefix_tokens > 0
+    step_bytes = acct["unique"] if shared else acct["logical"]
+    flush = L2Flush(device) if name in FLUSHED else None
+    rig = DecodeRig(w, device)
+    try:
+        for _ in range(max(3, warmup)):
+            if flush is not None:
+                flush()
+            rig.step()
+        probe_ms = rig.timed_steps(5, flush)
+        n = int(max(50, min(2000 if flush is not None else 20000, seconds * 1e3 / max(probe_ms, 1e-3))))
+        step_ms = rig.timed_steps(n, flush)
+        kt = rig.kernel_pass(n, flush)
+        assert rig.pool.get_error() == 0, f"device error on {name}"
+        got = out_bits(rig.out)
+    finally:
+        rig.close()
+        del flush
+    parity, _ = parity_vs_oracle(w, got)
+    traffic, traffic_note = ncu_traffic(w.name, sha)
+    achieved = step_bytes / (kt["decode_ms"] / 1e3) / 1e9
+    return {
+        "workload": w.name, "kv_dtype": w.dtype, "bytes_per_launch": step_bytes,
+        "bytes_basis": "unique KV slots" if shared else "logical KV",
+        "l2": "flushed before every step (512 MB written, 256 MB read)" if name in FLUSHED else
+              f"inputs larger than L2 ({acct['kv_unique'] / 1e6:.0f} MB of KV per call)",
+        "decode_kernel_ms": kt["decode_ms"], "merge_kernel_ms": kt["merge_ms"],
+        "achieved_gbs": achieved, "frac": achieved / peak, "step_ms": step_ms,
+        "step_gbs": step_bytes / (step_ms / 1e3) / 1e9, "steps_timed": n,
+        "traffic": traffic, "traffic_source": traffic_note, "parity": parity,
+    }
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -363,109 +561,57 @@ def run_ours(args):
     acct = algorithmic_bytes(w)
     use_unique = w.shared_prefix_tokens > 0
     step_bytes = acct["unique"] if use_unique else acct["logical"]
-
-    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(device).view(dt)  # noqa: E731
-    dt = {"bf16": pkv.BF16, "fp8": pkv.FP8_E4M3, "int4": pkv.INT4}[w.dtype]
-    pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head, dt)
-    if w.dtype == "fp8":
-        pool.set_fp8_scales(w.k_scale, w.v_scale)
-    if w.dtype == "int4":
-        pool.set_int4_key_params(w.k_scale, w.k_zero)
-    if args.partition_tokens:
-        pool.set_partition_tokens(args.partition_tokens)
-    pool.reserve_workspace(w.batch, w.n_q, w.max_blocks_per_seq)
-    T = w.fill_slots.shape[0]
-    for s in range(0, T, 1 << 20):
-        e = min(T, s + (1 << 20))
-        pkv.paged_kv_append(pool, dev(w.fill_k[s:e].view(np.int16), torch.bfloat16),
-                            dev(w.fill_v[s:e].view(np.int16), torch.bfloat16), dev(w.fill_slots[s:e], torch.int64))
-    k_new = dev(w.step_k.view(np.int16), torch.bfloat16)
-    v_new = dev(w.step_v.view(np.int16), torch.bfloat16)
-    slots = dev(w.step_slots, torch.int64)
-    q = dev(w.q.view(np.int16), torch.bfloat16)
-    tables = dev(w.block_tables, torch.int32)
-    lens = dev(w.context_lens, torch.int32)
-    out = torch.empty_like(q)
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device) if args.flush_l2 else None
-
-    def step():
-        # one pass of the hot path: append every sequence's new token, decode
-        if w.dtype == "int4":  # no fused step for 4-bit pools: append, then decode
-            pkv.paged_kv_append(pool, k_new, v_new, slots, stream)
-            pkv.paged_decode_attention(pool, q, tables, lens, float(w.scale), out, stream)
-        else:
-            pkv.paged_decode_step(pool, q, k_new, v_new, tables, lens, float(w.scale), out, stream)
-
-    def step_two_calls():
-        pkv.paged_kv_append(pool, k_new, v_new, slots, stream)
-        pkv.paged_decode_attention(pool, q, tables, lens, float(w.scale), out, stream)
+    rig = DecodeRig(w, device, args.partition_tokens)
+    pool, stream = rig.pool, rig.stream
+    flush = L2Flush(device) if args.flush_l2 else None
 
     for _ in range(args.warmup):
-        step()
         if flush is not None:
-            flush.fill_(1)
+            flush()
+        rig.step()
     torch.cuda.synchronize()
     assert pool.get_error() == 0, "device error during warm-up"
 
-    # ---- device-timed region ----
+    # ---- device-timed region: exactly K steps ----
     sampler = ClockSampler(gpu_id_for(local_rank)) if rank == 0 else None
     if sampler:
         sampler.start()
     pool.timing_read(reset=True)  # zero the launch counters; no per-kernel events in this region
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    step_ms = []
     barrier(world)
     torch.cuda.synchronize()
     if sampler:
         sampler.mark("start")
-    if flush is None:
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        elapsed_ms = ev0.elapsed_time(ev1)
-    else:  # L2 flushed between steps; only the steps are timed
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-        for a, b in evs:
-            flush.fill_(1)
-            a.record(stream)
-            step()
-            b.record(stream)
-        torch.cuda.synchronize()
-        step_ms = [a.elapsed_time(b) for a, b in evs]
-        elapsed_ms = sum(step_ms)
+    t_wall0 = time.perf_counter()
+    step_ms_avg = rig.timed_steps(args.steps, flush)
+    elapsed_ms = step_ms_avg * args.steps
+    t_region = time.perf_counter() - t_wall0
     if sampler:
-        sampler.mark("stop")
+        sampler.mark("region_end")
     barrier(world)
     launches = int(pool.timing_read(reset=True)["launches"])
-    if sampler:
-        sampler.stop()
     assert pool.get_error() == 0, "device error in the timed region"
 
-    # kernel durations: the same steps again, with a CUDA event pair recorded
-    # by the library around each of its launches on the launching stream
-    n_k = max(1, min(args.steps, 1000))
-    pool.timing_enable(True)
-    for _ in range(n_k):
-        if flush is not None:
-            flush.fill_(1)
-        step()
-    torch.cuda.synchronize()
-    pool.timing_enable(False)
-    tm = pool.timing_read(reset=True)
+    # ---- kernel durations: the same step again, for at least --kernel-seconds,
+    # with a CUDA event pair recorded by the library around each of its launches
+    # on the launching stream; the clock sampler keeps running through it ----
+    n_k = int(max(args.steps, min(3000 if flush is not None else 50000,
+                                  args.kernel_seconds * 1e3 / max(step_ms_avg, 1e-3))))
+    kt = rig.kernel_pass(n_k, flush)
+    if sampler:
+        sampler.mark("stop")
+        sampler.stop()
     max_ms = allreduce_max(elapsed_ms, world, device)
     total_bytes = allreduce_sum(step_bytes * args.steps, world, device)
 
     # the same step as two calls (paged_kv_append, then paged_decode_attention), for comparison
-    n2 = max(1, min(args.steps, 1000))
+    n2 = max(3, min(n_k, 1000))
     for _ in range(3):
-        step_two_calls()
+        rig.step_two_calls()
     torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(n2):
-        step_two_calls()
+        rig.step_two_calls()
     ev1.record(stream)
     torch.cuda.synchronize()
     two_call_ms = ev0.elapsed_time(ev1) / n2
@@ -478,7 +624,7 @@ def run_ours(args):
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
         h_q, h_k, h_v = (pin(x.view(np.int16)).view(torch.bfloat16) for x in (w.q, w.step_k, w.step_v))
         h_t, h_c = pin(w.block_tables), pin(w.context_lens)
-        h_out = torch.empty(tuple(q.shape), dtype=torch.bfloat16).pin_memory()
+        h_out = torch.empty(tuple(rig.q.shape), dtype=torch.bfloat16).pin_memory()
         h2d = sum(x.numel() * x.element_size() for x in (h_q, h_k, h_v, h_t, h_c))
         d2h = h_out.numel() * h_out.element_size()
 
@@ -486,9 +632,9 @@ def run_ours(args):
         # writes the output back, synchronises)
         e2e_step = pkv.HostStep(pool, h_q, h_k, h_v, h_t, h_c, float(w.scale), h_out, stream)
 
-        for _ in range(min(args.warmup, 10)):
+        for _ in range(max(3, min(args.warmup, 10))):
             e2e_step()
-        n_e2e = max(1, min(args.steps, 2000))
+        n_e2e = int(max(args.steps, min(20000, 0.5e3 / max(step_ms_avg, 1e-3))))
         barrier(world)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
@@ -500,33 +646,41 @@ def run_ours(args):
                "d2h_bytes_per_step": int(d2h), "steps": n_e2e, "ms_per_step": 1e3 * e2e_s / n_e2e,
                "calls_per_s": allreduce_sum(n_e2e, world, device) / e2e_s,
                "call": "HostStep: paged_decode_step_host on fixed pinned host inputs and output"}
+    got_main = out_bits(rig.out)
+    rig.close()
+    del flush
 
     if rank != 0:
-        pool.close()
         return 0
+
+    peak, peak_note = measured_peaks()
+    sha = kernel_source_sha()
+    # ---- the other workloads: decode-kernel fraction and parity, one at a time ----
+    per_config = {}
+    if not args.no_per_config:
+        for name in PER_CONFIG:
+            if name == args.workload:
+                continue
+            per_config[name] = measure_config(name, device, args.warmup, args.config_seconds, peak, sha)
 
     # ---- the CPU-baseline leg: the oracle (test infrastructure) runs this
     # step on the host; its output of the full batch also gives the parity
     # figures for this very launch configuration, then it is timed ----
     cpu, parity = None, None
     if not args.no_cpu_baseline:
-        m = oracle_setup(w)
-        ref = oracle_step(m, w, list(range(w.batch)))
-        got = out.float().cpu().numpy().astype(np.float64)
-        err = np.abs(got - ref)
-        parity = {"max_abs": float(err.max()), "mean_abs": float(err.mean()), "tol_max_abs": 1e-2,
-                  "tol_mean_abs": 1e-3, "ok": bool(err.max() <= 1e-2 and err.mean() <= 1e-3)}
+        parity, m = parity_vs_oracle(w, got_main)
         gbs, secs, nseq, threads, _ = time_oracle(w, m, budget_s=12.0)
         cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{nseq} single-sequence oracle steps (append + decode, all {w.n_q} heads, "
                          f"fp64, {threads} threads) rotating over the workload's sequences, {secs:.1f} s"}
 
-    peak, peak_note = measured_peaks()
-    dec_ms = tm["decode_ms"] / max(1, tm["timed_decode"])
-    sha = kernel_source_sha()
+    dec_ms = kt["decode_ms"]
     traffic, traffic_note = ncu_traffic(w.name, sha)
     achieved = step_bytes / (dec_ms / 1e3) / 1e9
     clocks = sampler.summary() if sampler else None
+    if clocks is not None:
+        clocks["window"] = (f"the timed region ({args.steps} steps, {t_region * 1e3:.1f} ms) and the kernel-timing "
+                            f"pass right after it ({n_k} steps of the same workload)")
     line = {
         "metric": METRIC,
         "value": value,
@@ -544,7 +698,7 @@ def run_ours(args):
         "config": dict(w.describe(), parallelism="replicas" if world > 1 else "single GPU",
                        bytes_per_step=step_bytes, bytes_basis="unique KV slots" if use_unique else "logical KV",
                        kv_bytes_logical=acct["kv_logical"], kv_bytes_unique=acct["kv_unique"],
-                       l2=("flushed (512 MB write) between steps" if args.flush_l2 else
+                       l2=("flushed between steps (512 MB written, then 256 MB read)" if args.flush_l2 else
                            f"inputs larger than L2: {acct['kv_unique'] / 1e6:.0f} MB of KV per call vs 129 MB L2"),
                        work_split=(f"slices of {args.partition_tokens} tokens" if args.partition_tokens
                                    else "one equal slice of the batch's blocks per resident warp")),
@@ -552,16 +706,18 @@ def run_ours(args):
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "bytes_per_launch": step_bytes, "avg_launch_ms": dec_ms, "peak_source": peak_note,
                      "traffic_source": traffic_note, "kernel_source_sha": sha},
-        "kernels_ms_avg": {"decode_kernel": dec_ms,
-                           "merge_kernel": tm["merge_ms"] / max(1, tm["timed_merge"])},
-        "step_call": "paged_decode_step (the append fused into the decode kernel, then the split-KV merge "
-                     "kernel: two launches)",
+        "kernels_ms_avg": {"decode_kernel": dec_ms, "merge_kernel": kt["merge_ms"]},
+        "step_call": ("paged_kv_append, then paged_decode_attention (decode and split-KV merge kernels)"
+                      if w.dtype == "int4" else
+                      "paged_decode_step (the append fused into the decode kernel, then the split-KV merge "
+                      "kernel: two launches)"),
         "two_call_step_ms": two_call_ms,
         "step_frac_of_peak": value / world / peak,
         "gpu_launches": launches,
         "kernel_timing_steps": n_k,
         "clocks": clocks,
         "parity": parity,
+        "per_config": per_config,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "flops_per_step": acct["flops"],
@@ -569,7 +725,6 @@ def run_ours(args):
     if use_unique:
         line["effective_logical_gbs"] = acct["logical"] * args.steps * world / (max_ms / 1e3) / 1e9
     print(json.dumps(line))
-    pool.close()
     return 0
 
 
@@ -585,7 +740,7 @@ def _timed(fn, reps: int, warmup: int, stream, flush=None) -> float:
     if flush is not None:
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         for a, b in evs:
-            flush.fill_(1)
+            flush()
             a.record(stream)
             fn()
             b.record(stream)
@@ -695,7 +850,7 @@ def run_cascade(args):
     pre = dev(w.block_tables[0, :n_pre], torch.int32)
     out_c, out_p = torch.empty_like(q), torch.empty_like(q)
     reps, warm = max(3, min(args.steps, 500)), max(3, args.warmup)
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda") if args.flush_l2 else None
+    flush = L2Flush("cuda") if args.flush_l2 else None
     casc_ms = _timed(lambda: pkv.paged_decode_attention_prefix(pool, q, pre, tables, lens, float(w.scale), out_c, stream),
                      reps, warm, stream, flush)
     plain_ms = _timed(lambda: pkv.paged_decode_attention(pool, q, tables, lens, float(w.scale), out_p, stream),
@@ -718,7 +873,7 @@ def run_cascade(args):
         "data": "synthetic",
         "config": dict(w.describe(), bytes_basis="unique KV slots", kv_bytes_unique=acct["kv_unique"],
                        kv_bytes_logical=acct["kv_logical"],
-                       l2=("flushed (512 MB write) before each timed call" if flush is not None else
+                       l2=("flushed before each timed call (512 MB written, 256 MB read)" if flush is not None else
                            "not flushed: back-to-back calls")),
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_source": peak_note},
