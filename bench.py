@@ -64,6 +64,7 @@ def parse_args(argv=None):
     p.add_argument("--config-seconds", type=float, default=0.4,
                    help="timed duration per workload of the per_config entries")
     p.add_argument("--mode", default="decode", choices=["decode", "blocks", "cascade", "prefill"])
+    p.add_argument("--prefill-kv", default="bf16", choices=["bf16", "fp8"], help="--mode prefill: KV pool type")
     return p.parse_args(argv)
 
 
@@ -838,7 +839,6 @@ def run_cascade(args):
     acct = algorithmic_bytes(w)
     dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).cuda().view(dt)  # noqa: E731
     pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head, pkv.BF16)
-    T = w.fill_slots.shape[0]
     pkv.paged_kv_append(pool, dev(w.fill_k.view(np.int16), torch.bfloat16), dev(w.fill_v.view(np.int16), torch.bfloat16),
                         dev(w.fill_slots, torch.int64))
     pkv.paged_kv_append(pool, dev(w.step_k.view(np.int16), torch.bfloat16), dev(w.step_v.view(np.int16), torch.bfloat16),
@@ -847,6 +847,13 @@ def run_cascade(args):
     tables = dev(w.block_tables, torch.int32)
     lens = dev(w.context_lens, torch.int32)
     n_pre = w.shared_prefix_tokens // 16
+    # what the library's automatic mode picks for this prefix and batch, then the cascade forced
+    pool.timing_read(reset=True)
+    pkv.paged_decode_attention_prefix(pool, q, dev(w.block_tables[0, :n_pre], torch.int32), tables, lens,
+                                      float(w.scale), torch.empty_like(q), stream)
+    torch.cuda.synchronize()
+    auto_cascade = pool.timing_read(reset=True)["prefix_launches"] > 0
+    pool.set_cascade_mode(pkv.CASCADE_ALWAYS)
     pre = dev(w.block_tables[0, :n_pre], torch.int32)
     out_c, out_p = torch.empty_like(q), torch.empty_like(q)
     reps, warm = max(3, min(args.steps, 500)), max(3, args.warmup)
@@ -869,6 +876,7 @@ def run_cascade(args):
         "ms_per_call": casc_ms,
         "plain_decode_ms_per_call": plain_ms,
         "speedup_vs_plain": plain_ms / casc_ms,
+        "auto_mode_picks": "cascade" if auto_cascade else "plain decode",
         "dtype": "f32",
         "data": "synthetic",
         "config": dict(w.describe(), bytes_basis="unique KV slots", kv_bytes_unique=acct["kv_unique"],
@@ -899,9 +907,14 @@ def run_prefill(args):
     torch.cuda.set_device(0)
     stream = torch.cuda.current_stream()
     w = wl.llama3_8b()
+    if args.prefill_kv == "fp8":  # the same lengths on an FP8 E4M3 pool
+        w = wl.build("llama3_8b_fp8_b64", 32, 8, 128, w.context_lens, dtype="fp8", seed=12)
     T = 512
     dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).cuda().view(dt)  # noqa: E731
-    pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head, pkv.BF16)
+    pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head,
+                              pkv.FP8_E4M3 if args.prefill_kv == "fp8" else pkv.BF16)
+    if args.prefill_kv == "fp8":
+        pool.set_fp8_scales(w.k_scale, w.v_scale)
     pkv.paged_kv_append(pool, dev(w.fill_k.view(np.int16), torch.bfloat16), dev(w.fill_v.view(np.int16), torch.bfloat16),
                         dev(w.fill_slots, torch.int64))
     pkv.paged_kv_append(pool, dev(w.step_k.view(np.int16), torch.bfloat16), dev(w.step_v.view(np.int16), torch.bfloat16),
@@ -931,7 +944,8 @@ def run_prefill(args):
         "unit": "TFLOP/s",
         "higher_is_better": True,
         "ms_per_call": ms,
-        "dtype": "bf16 in, f32 accumulate",
+        "dtype": ("E4M3 K/V widened to f16, f16 q and P, f32 accumulate" if args.prefill_kv == "fp8"
+                  else "bf16 in, f32 accumulate"),
         "data": "synthetic",
         "config": dict(w.describe(), chunk_tokens=T, query_rows=w.batch * T, visible_keys=keys),
         "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel", "achieved": tflops, "peak": peak,

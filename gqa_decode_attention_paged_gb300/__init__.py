@@ -24,6 +24,9 @@ INT4 = 2
 STATUS = {0: "PKV_OK", 1: "PKV_EINVAL", 2: "PKV_ERANGE", 3: "PKV_ENOMEM", 4: "PKV_ECUDA",
           5: "PKV_EUNSUPPORTED", 6: "PKV_EDEVICE"}
 
+CASCADE_AUTO = 0
+CASCADE_ALWAYS = 1
+CASCADE_NEVER = 2
 DEVERR_SLOT_RANGE = 0x1
 DEVERR_BLOCK_RANGE = 0x2
 DEVERR_CTX_RANGE = 0x4
@@ -85,6 +88,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.kv_pool_set_int4_key_params.argtypes = [P, P, P]
         lib.kv_pool_layout.argtypes = [P, c.POINTER(_Layout)]
         lib.kv_pool_set_partition_tokens.argtypes = [P, c.c_int32]
+        lib.kv_pool_set_cascade_mode.argtypes = [P, c.c_int32]
         lib.kv_pool_reserve_workspace.argtypes = [P, c.c_int32, c.c_int32, c.c_int32]
         lib.paged_kv_append.argtypes = [P, P, P, P, c.c_int64, P]
         lib.paged_decode_attention.argtypes = [P, P, c.c_int32, P, c.c_int32, P, c.c_int32,
@@ -128,7 +132,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.pkv_last_error_message.restype = c.c_char_p
         for name in ("kv_pool_create", "kv_pool_destroy", "kv_pool_set_fp8_scales", "kv_pool_set_int4_key_params",
                      "kv_pool_layout",
-                     "kv_pool_set_partition_tokens", "kv_pool_reserve_workspace", "paged_kv_append",
+                     "kv_pool_set_partition_tokens", "kv_pool_set_cascade_mode", "kv_pool_reserve_workspace",
+                     "paged_kv_append",
                      "paged_decode_attention", "paged_decode_attention_noalloc", "paged_decode_step",
                      "paged_decode_attention_csr", "paged_prefill_attention",
                      "paged_decode_step_host", "paged_decode_attention_prefix", "pkv_get_error", "pkv_timing_enable", "pkv_timing_read",
@@ -254,6 +259,10 @@ class Pool:
 
     def set_partition_tokens(self, tokens: int):
         _check(load().kv_pool_set_partition_tokens(self.handle, int(tokens)))
+
+    def set_cascade_mode(self, mode: int):
+        """CASCADE_AUTO, CASCADE_ALWAYS or CASCADE_NEVER for paged_decode_attention_prefix."""
+        _check(load().kv_pool_set_cascade_mode(self.handle, int(mode)))
 
     def reserve_workspace(self, batch: int, n_q: int, max_blocks_per_seq: int):
         _check(load().kv_pool_reserve_workspace(self.handle, batch, n_q, max_blocks_per_seq))

@@ -1967,14 +1967,20 @@ namespace pkv {
 // the tcgen05 prefill kernel in partial mode -- and stores a (max, sum, O)
 // partial per prefix chunk.  Stage 3, the merge kernel, combines the two.
 
-template <int D, int G>
+// PKV_CASCADE_AUTO: the cascade once batch x prefix tokens reaches 2^17 (and the batch 8).  Measured
+// on GB300 (bf16, n_q 32, n_kv 8, d 128, tails of 0..1024 tokens): prefix 1024 x batch 64 and
+// 2048 x 16 run faster as plain decode, 1024 x 128, 2048 x 64 and 4096 x 32 as the cascade.
+constexpr int64_t kCascadeMinSharedTokens = 1 << 17;
+constexpr int kCascadeMinBatch = 8;
+
+template <int D, int G, int KV>
 static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32_t *prefix_blocks,
                                        int n_prefix_blocks, cudaStream_t s)
 {
-    using C = Cfg<D, G, false>;
+    using C = Cfg<D, G, KV>;
     int grid = 0;
     size_t smem = 0;
-    pkv_status st = decode_grid<D, G, false>(pool, a.batch, a.W, &grid, &smem);
+    pkv_status st = decode_grid<D, G, KV>(pool, a.batch, a.W, &grid, &smem);
     if (st != PKV_OK) return st;
     int chunk_blocks = 0, n_chunks = 0;
     prefix_stage_chunks(pool, a.batch, a.n_q, n_prefix_blocks, &chunk_blocks, &n_chunks);
@@ -1990,7 +1996,7 @@ static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32
     // decode leaves as it finishes), then the merge.
     {
         LaunchScope ls(pool, kDecode, s);
-        cudaError_t e = launch_pdl(decode_kernel<D, G, false>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
+        cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
                                    pool->tm_v, a);
         ls.done();
         if (e != cudaSuccess) return cuda_fail(e, "decode launch (cascade tail)");
@@ -2001,14 +2007,14 @@ static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32
     return launch_merge<D, G>(pool, a, grid * C::NW, s);
 }
 
-template <int D>
+template <int D, int KV>
 static pkv_status dispatch_prefix(pkv_pool *pool, const DecodeArgs &a, int G, const int32_t *pb, int npb, cudaStream_t s)
 {
     switch (G) {
-    case 1: return launch_prefix_decode<D, 1>(pool, a, pb, npb, s);
-    case 2: return launch_prefix_decode<D, 2>(pool, a, pb, npb, s);
-    case 4: return launch_prefix_decode<D, 4>(pool, a, pb, npb, s);
-    case 8: return launch_prefix_decode<D, 8>(pool, a, pb, npb, s);
+    case 1: return launch_prefix_decode<D, 1, KV>(pool, a, pb, npb, s);
+    case 2: return launch_prefix_decode<D, 2, KV>(pool, a, pb, npb, s);
+    case 4: return launch_prefix_decode<D, 4, KV>(pool, a, pb, npb, s);
+    case 8: return launch_prefix_decode<D, 8, KV>(pool, a, pb, npb, s);
     }
     return fail(PKV_EUNSUPPORTED, "cascade decode: group size %d unsupported (1, 2, 4 or 8)", G);
 }
@@ -2023,8 +2029,8 @@ extern "C" pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *
 {
     pkv_status st = check_step_args(pool, "paged_decode_attention_prefix", n_q, max_blocks_per_seq, batch, scale);
     if (st != PKV_OK || batch == 0) return st;
-    if (pool->dtype != PKV_BF16)
-        return fail(PKV_EUNSUPPORTED, "paged_decode_attention_prefix: bf16 pools only");
+    if (pool->dtype == PKV_INT4)
+        return fail(PKV_EUNSUPPORTED, "paged_decode_attention_prefix: bf16 and FP8 pools only (not 4-bit)");
     if (n_prefix_blocks <= 0 || n_prefix_blocks > max_blocks_per_seq)
         return fail(PKV_EINVAL, "paged_decode_attention_prefix: n_prefix_blocks %d not in [1, max_blocks_per_seq]",
                     n_prefix_blocks);
@@ -2061,8 +2067,18 @@ extern "C" pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *
     a.n_pre = 0;
     a.pre_base = 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (pool->d_head == 128) return dispatch_prefix<128>(pool, a, G, prefix_blocks, n_prefix_blocks, s);
-    return dispatch_prefix<64>(pool, a, G, prefix_blocks, n_prefix_blocks, s);
+    // Cascade or plain decode: with a short prefix the plain kernel's re-reads of it come
+    // from L2 and cost less than the cascade's prefix stage and merge.
+    const bool cascade = pool->cascade_mode == PKV_CASCADE_ALWAYS ||
+                         (pool->cascade_mode == PKV_CASCADE_AUTO && batch >= kCascadeMinBatch &&
+                          (int64_t)n_prefix_blocks * kBlockSize * batch >= kCascadeMinSharedTokens);
+    if (!cascade) return dispatch_kv(pool, a, G, s);
+    const bool fp8 = pool->dtype == PKV_FP8_E4M3;
+    if (pool->d_head == 128)
+        return fp8 ? dispatch_prefix<128, kKvFp8>(pool, a, G, prefix_blocks, n_prefix_blocks, s)
+                   : dispatch_prefix<128, kKvBf16>(pool, a, G, prefix_blocks, n_prefix_blocks, s);
+    return fp8 ? dispatch_prefix<64, kKvFp8>(pool, a, G, prefix_blocks, n_prefix_blocks, s)
+               : dispatch_prefix<64, kKvBf16>(pool, a, G, prefix_blocks, n_prefix_blocks, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -71,6 +71,7 @@ struct pkv_pool {
     void *stage = nullptr;            // device staging for paged_decode_step_host (grow-only)
     size_t stage_bytes = 0;
     int partition_tokens = pkv::kDefaultPartitionTokens;
+    int cascade_mode = PKV_CASCADE_AUTO;  // paged_decode_attention_prefix: cascade or plain decode
     // device address of paged_decode_attention_noalloc's scratch array in the
     // context the pool was created in (looked up by kv_pool_create)
     void *noalloc_scratch = nullptr;

@@ -384,6 +384,15 @@ pkv_status kv_pool_set_partition_tokens(pkv_pool *pool, int32_t tokens)
     return PKV_OK;
 }
 
+pkv_status kv_pool_set_cascade_mode(pkv_pool *pool, int32_t mode)
+{
+    if (!pool) return fail(PKV_EINVAL, "kv_pool_set_cascade_mode: NULL pool");
+    if (mode != PKV_CASCADE_AUTO && mode != PKV_CASCADE_ALWAYS && mode != PKV_CASCADE_NEVER)
+        return fail(PKV_EINVAL, "kv_pool_set_cascade_mode: unknown mode %d", mode);
+    pool->cascade_mode = mode;
+    return PKV_OK;
+}
+
 pkv_status kv_pool_reserve_workspace(pkv_pool *pool, int32_t batch, int32_t n_q, int32_t max_blocks_per_seq)
 {
     if (!pool || batch < 0 || n_q <= 0 || max_blocks_per_seq <= 0 || n_q % pool->n_kv)

@@ -88,6 +88,7 @@ struct Args {
     int64_t n_rows;            // rows of q and out: stores past them are skipped (an inconsistent indptr)
     int oob_row;               // a K/V row index past the end of the pool (zero-filled box)
     float qscale;              // scale * log2(e)
+    const float *scales;       // FP8 pools: [2 * n_kv] fp32, K scales then V scales
     __nv_bfloat16 *out;        // [rows][n_q][D]
     unsigned *err;
 };
@@ -105,7 +106,10 @@ struct Layout {
     enum { Q_FULL = 0, Q_FREE = 2, K_FULL = 4, K_EMPTY = 4 + kKStages, V_FULL = 4 + 2 * kKStages,
            V_EMPTY = V_FULL + kVStages, S_FULL = V_EMPTY + kVStages, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2,
            O_DONE = P_FULL + 2, DRAIN = O_DONE + 2, OUT_FULL = DRAIN + 2, OUT_FREE = OUT_FULL + 1,
-           PAIR = OUT_FREE + 1, NBARS = PAIR + 4 };
+           PAIR = OUT_FREE + 1,
+           // FP8 pools: the copies of Q, K and V complete on these; the producers convert
+           // the landed bytes to f16 in place and then complete Q_FULL, K_FULL, V_FULL
+           Q_RAW = PAIR + 4, K_RAW = Q_RAW + 2, V_RAW = K_RAW + kKStages, NBARS = V_RAW + kVStages };
     static constexpr uint32_t kTmemSlot = kBar + NBARS * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     // a tile's end: each key half's (reference maximum as bf16 bits, row sum) per row, for the other half
@@ -113,6 +117,7 @@ struct Layout {
     static constexpr uint32_t kXl = kXm + 2 * kRows * 2;          // [2 halves][kRows] float
     static constexpr uint32_t kEnd = kXl + 2 * kRows * 4;
     static constexpr size_t bytes = 1024 + kEnd;
+    static_assert(bytes <= 232448, "shared memory beyond the 227 KiB a CTA may use");
 };
 
 // ------------------------------------------------------------- tcgen05 PTX
@@ -128,11 +133,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, f32 accumulator, M x N,
-// A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1).
-__host__ __device__ constexpr uint32_t mma_idesc(int M, int N, int b_mn)
+// Instruction descriptor, kind::f16: bf16 (f16 = false) or f16 (f16 = true)
+// A and B, f32 accumulator, M x N, A K-major, B K-major (b_mn = 0) or
+// MN-major (b_mn = 1).
+__host__ __device__ constexpr uint32_t mma_idesc(int M, int N, int b_mn, bool f16 = false)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+    const uint32_t ab = f16 ? 0u : 1u;  // operand format: 0 f16, 1 bf16
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
 }
 
@@ -234,6 +241,154 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// acc += the two f16 halves of `pk` (each widened exactly, added in fp32).
+__device__ __forceinline__ void add_f16x2_to(float &acc, uint32_t pk)
+{
+    asm("{\n\t.reg .b16 lo, hi;\n\t.reg .f32 a, b;\n\tmov.b32 {lo, hi}, %1;\n\t"
+        "cvt.f32.f16 a, lo;\n\tcvt.f32.f16 b, hi;\n\tadd.rn.f32 %0, a, %0;\n\tadd.rn.f32 %0, b, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(pk));
+}
+
+// P as the operand the P V product takes: bf16 pairs, or f16 pairs for FP8 pools
+// (whose MMAs run in f16); the row sum adds the rounded values.
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi)
+{
+    return F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+
+template <bool F16>
+__device__ __forceinline__ void add_p_to(float &acc, uint32_t pk)
+{
+    if constexpr (F16) add_f16x2_to(acc, pk);
+    else add_bf16x2_to(acc, pk);
+}
+
+// ------------------------------------------------------------- FP8 pools: E4M3 -> f16 in shared memory
+
+// Four E4M3 bytes -> two f16x2 words (bytes 0, 1 -> lo; bytes 2, 3 -> hi); exact.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t &lo, uint32_t &hi)
+{
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// One step's K (or V) tile of an FP8 pool, converted in place by one warp.
+// The copies put the 128 E4M3 rows (row r = key r of the step, D bytes, the
+// pool's TMA swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7) for
+// 128-byte rows, c ^ ((r >> 1) & 3) for 64-byte rows) in the upper half of
+// the stage; the f16 tile goes where the bf16 copies would have put it: per
+// 64-column half, row r at r * 128 bytes, 16-byte chunk j at j ^ (r & 7).
+// Rows are read before any lane writes (warp-synchronous) and taken in
+// increasing order, so no write reaches an E4M3 row still to be read: for
+// D = 128 the second half's row r is exactly E4M3 row r; for D = 64 the f16
+// row r covers E4M3 rows 2r - 128 and 2r - 127, both at most r.
+template <int D>
+__device__ __forceinline__ void convert_kv_f16(uint8_t *stage, int lane)
+{
+    constexpr uint32_t KT = kKeys * D * 2;
+    const uint32_t out = smem_u32(stage), in = out + KT / 2;
+    if constexpr (D == 128) {
+        // lane: row 4 i + lane / 8 (two iterations at a time), E4M3 chunk c = lane % 8 (columns 16 c .. + 15)
+        const int c = lane & 7;
+#pragma unroll 1
+        for (int i = 0; i < kKeys / 4; i += 2) {
+            uint4 x[2];
+            int r[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                r[u] = 4 * (i + u) + (lane >> 3);
+                x[u] = lds128(in + r[u] * 128 + ((c ^ (r[u] & 7)) << 4));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                uint4 lo, hi;
+                e4m3x4_to_f16x4(x[u].x, lo.x, lo.y);
+                e4m3x4_to_f16x4(x[u].y, lo.z, lo.w);
+                e4m3x4_to_f16x4(x[u].z, hi.x, hi.y);
+                e4m3x4_to_f16x4(x[u].w, hi.z, hi.w);
+                const uint32_t row = out + (c >> 2) * kHalf + r[u] * 128;
+                const int j = 2 * (c & 3);
+                sts128(row + ((j ^ (r[u] & 7)) << 4), lo);
+                sts128(row + (((j + 1) ^ (r[u] & 7)) << 4), hi);
+            }
+            __syncwarp();
+        }
+    } else {
+        // lane: row 8 i + lane / 4, E4M3 chunk c = lane % 4
+        const int c = lane & 3;
+#pragma unroll 1
+        for (int i = 0; i < kKeys / 8; i += 2) {
+            uint4 x[2];
+            int r[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                r[u] = 8 * (i + u) + (lane >> 2);
+                x[u] = lds128(in + r[u] * 64 + ((c ^ ((r[u] >> 1) & 3)) << 4));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                uint4 lo, hi;
+                e4m3x4_to_f16x4(x[u].x, lo.x, lo.y);
+                e4m3x4_to_f16x4(x[u].y, lo.z, lo.w);
+                e4m3x4_to_f16x4(x[u].z, hi.x, hi.y);
+                e4m3x4_to_f16x4(x[u].w, hi.z, hi.w);
+                const uint32_t row = out + r[u] * 128;
+                const int j = 2 * c;
+                sts128(row + ((j ^ (r[u] & 7)) << 4), lo);
+                sts128(row + (((j + 1) ^ (r[u] & 7)) << 4), hi);
+            }
+            __syncwarp();
+        }
+    }
+}
+
+// A Q tile (bf16, as the copy left it) -> f16 in place, element by element
+// (exact for |q| in f16's normal range; larger values overflow f16).
+template <int D>
+__device__ __forceinline__ void convert_q_f16(uint8_t *qbuf, int lane)
+{
+    constexpr uint32_t QT = kRows * D * 2;
+    const uint32_t base = smem_u32(qbuf);
+#pragma unroll 4
+    for (uint32_t off = 16u * lane; off < QT; off += 16u * 32) {
+        uint4 v = lds128(base + off);
+        uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 f = bf16x2_to_f32x2(w[k]);
+            w[k] = pack_f16x2(f.x, f.y);
+        }
+        sts128(base + off, v);
+    }
 }
 
 // ------------------------------------------------------------- tile walk
@@ -354,7 +509,7 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity)
 
 // ------------------------------------------------------------- the kernel
 
-template <int D, int G, bool PARTIAL>
+template <int D, int G, bool PARTIAL, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, Args a)
@@ -375,7 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < L::NBARS; ++i) {
             const bool by_warps = i == L::OUT_FULL || i == L::OUT_FREE;
             const bool by_half = i == L::P_FULL || i == L::P_FULL + 1;  // the four warps of a key half
-            mbar_init(&bar[i], by_warps ? kSoftmaxWarps : by_half ? kSoftmaxWarps / 2 : i >= L::PAIR ? 2 : 1);
+            const bool by_pair = i >= L::PAIR && i < L::PAIR + 4;  // the two warps of a lane quarter
+            mbar_init(&bar[i], by_warps ? kSoftmaxWarps : by_half ? kSoftmaxWarps / 2 : by_pair ? 2 : 1);
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -416,9 +572,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ring = is_k ? L::kK : L::kV;
         uint64_t *full = &bar[is_k ? L::K_FULL : L::V_FULL];
         uint64_t *empty = &bar[is_k ? L::K_EMPTY : L::V_EMPTY];
+        // FP8 pools: the copies complete on `raw` instead; the E4M3 tile lands in the upper
+        // half of its stage and this warp converts it to f16 in place one step later (after
+        // issuing the next step's copies, so their latency overlaps the conversion), then
+        // completes `full`.  The K warp converts each tile's Q (bf16 -> f16) with the tile's
+        // first K step.
+        uint64_t *raw = &bar[is_k ? L::K_RAW : L::V_RAW];
+        uint64_t *land = F8 ? raw : full;
+        const int qland = F8 ? L::Q_RAW : L::Q_FULL;
         const uint64_t policy = l2_policy_evict_normal();
         int gs = 0, qi = 0;
+        int pend = -1, pend_q = -1;  // FP8: the step awaiting conversion, and the Q load to convert before it
         bool ok = true;
+        [[maybe_unused]] auto convert_pending = [&]() -> bool {
+            if (pend_q >= 0) {
+                const int qb = pend_q & 1;
+                if (!wait_all(&bar[L::Q_RAW + qb], (pend_q >> 1) & 1)) return false;
+                convert_q_f16<D>(sm + L::kQ + qb * L::QT, lane);
+                fence_proxy_async_smem();  // the MMAs read the converted tile through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[L::Q_FULL + qb]);
+            }
+            const int st = pend % NS;
+            if (!wait_all(&raw[st], (pend / NS) & 1)) return false;
+            convert_kv_f16<D>(sm + ring + st * L::KT, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[st]);
+            return true;
+        };
         for (int x = blockIdx.x / 2; ok; x += gridDim.x / 2) {
             Tile t;
             if (!find_tile<G, PARTIAL>(wk, a, x, rank, t, lane)) break;
@@ -427,16 +609,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t *trow = tile_blocks<PARTIAL>(a, t);
             // block ids (lanes 0..7) one step ahead of the copies: the table read is off the refill path
             int nxt = lane < kStepBlocks && lane < t.n_blocks ? trow[lane] : -1;
+            int q_load = -1;
             if (is_k) {  // this tile's queries into Q buffer qi & 1
                 const int qb = qi & 1;
                 if (qi >= 2 && !(ok = wait_all(&bar[L::Q_FREE + qb], ((qi >> 1) + 1) & 1))) break;
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&bar[L::Q_FULL + qb], L::QT);
+                    mbar_arrive_expect_tx(&bar[qland + qb], L::QT);
 #pragma unroll
                     for (int h = 0; h < NH; ++h)
                         tma_load_3d(sm + L::kQ + qb * L::QT + h * kHalf, &tm_q, 64 * h, t.g * G,
-                                    t.row0 + t.rt0 / G, &bar[L::Q_FULL + qb], policy);
+                                    t.row0 + t.rt0 / G, &bar[qland + qb], policy);
                 }
+                q_load = qi;
                 ++qi;
             }
             for (int s = 0; s < t.n_steps; ++s, ++gs) {
@@ -448,23 +632,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool present = lane < kStepBlocks && s * kStepBlocks + lane < t.n_blocks;
                 const bool valid = present && cur >= 0 && cur < a.num_blocks;
                 if (present && !valid && is_k) atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
-                if (lane == 0) mbar_arrive_expect_tx(&full[st], L::KT);
+                if (lane == 0) mbar_arrive_expect_tx(&land[st], F8 ? L::KT / 2 : L::KT);
                 __syncwarp();
                 if (lane < kStepBlocks) {  // lane k copies block k of the step
                     const int y = valid ? (int)((cur * (int64_t)a.n_kv + t.g) * kBlockSize) : a.oob_row;
-                    uint8_t *dst = sm + ring + st * L::KT + lane * (kBlockSize * 128);
+                    if constexpr (F8) {  // one box per block: 16 E4M3 rows of D bytes
+                        tma_load_2d(sm + ring + st * L::KT + L::KT / 2 + lane * (kBlockSize * D), map, 0, y,
+                                    &raw[st], policy);
+                    } else {
+                        uint8_t *dst = sm + ring + st * L::KT + lane * (kBlockSize * 128);
 #pragma unroll
-                    for (int h = 0; h < NH; ++h) tma_load_2d(dst + h * kHalf, map, 64 * h, y, &full[st], policy);
+                        for (int h = 0; h < NH; ++h) tma_load_2d(dst + h * kHalf, map, 64 * h, y, &full[st], policy);
+                    }
+                }
+                if constexpr (F8) {
+                    if (pend >= 0 && !(ok = convert_pending())) break;
+                    pend = gs;
+                    pend_q = s == 0 ? q_load : -1;
                 }
             }
+        }
+        if constexpr (F8) {
+            if (ok && pend >= 0 && !*abort_flag) ok = convert_pending();
         }
         // copies still in flight (after an abort) land before the CTA exits
         for (int j = 1; j <= NS && gs - j >= 0; ++j) {
             const int g2 = gs - j;
-            mbar_wait_bounded(&full[g2 % NS], (g2 / NS) & 1);
+            mbar_wait_bounded(&land[g2 % NS], (g2 / NS) & 1);
         }
-        if (is_k && qi > 0) mbar_wait_bounded(&bar[L::Q_FULL + ((qi - 1) & 1)], ((qi - 1) >> 1) & 1);
-        if (is_k && qi > 1) mbar_wait_bounded(&bar[L::Q_FULL + ((qi - 2) & 1)], ((qi - 2) >> 1) & 1);
+        if (is_k && qi > 0) mbar_wait_bounded(&bar[qland + ((qi - 1) & 1)], ((qi - 1) >> 1) & 1);
+        if (is_k && qi > 1) mbar_wait_bounded(&bar[qland + ((qi - 2) & 1)], ((qi - 2) >> 1) & 1);
         if (!ok) set_abort();
     } else if (warp == kQkWarp || warp == kPvWarp) {
         // ---------------------------------------------------------- MMA issue
@@ -473,8 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // accumulators allow), O += P V starts as soon as a step's P is in
         // tensor memory.  Each warp commits, and finally drains, its own MMAs.
         const bool is_qk = warp == kQkWarp;
-        constexpr uint32_t idesc_qk = mma_idesc(kRows, kKeys, 0);
-        constexpr uint32_t idesc_pv = mma_idesc(kRows, D, 1);
+        constexpr uint32_t idesc_qk = mma_idesc(kRows, kKeys, 0, F8);
+        constexpr uint32_t idesc_pv = mma_idesc(kRows, D, 1, F8);
         const uint32_t base = smem_u32(sm);
         int gs = 0, qi = 0;
         bool ok = true;
@@ -583,6 +780,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (r < t.R && !in_out && ch == 0) atomicOr(a.err, PKV_DEVERR_CTX_RANGE);
             // this row's position: it sees keys 0 .. pos (every key of a shared chunk)
             const int pos = PARTIAL ? t.C - 1 : t.C - t.T + min(r, t.R - 1) / G;
+            // FP8 pools: the K scale of this KV head folds into the score scale, the V scale
+            // into the final normalisation
+            const float qs = F8 ? a.qscale * a.scales[t.g] : a.qscale;
+            const float vs = F8 ? a.scales[a.n_kv + t.g] : 1.0f;
             float mref = -INFINITY;  // this half's reference maximum: a bf16 value (sent exactly at the end)
             float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // this half's row sum of the bf16-rounded P
             // block ids of this warp's 4 blocks of the next step (lanes 0..3), read one step ahead
@@ -621,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float bm_half = fmax3(fmax3(m4[0], m4[1], m4[2]), fmax3(m4[3], m4[4], m4[5]),
                                             fmaxf(m4[6], m4[7]));
-                const float bms = bm_half * a.qscale;
+                const float bms = bm_half * qs;
                 const bool resc = bms > mref + kRescaleSlack;
                 float alpha = 1.0f;
                 if (resc) {
@@ -636,9 +837,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < HK / 2; ++i) {
                     const float2 x = ffma2(make_float2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
-                                           make_float2(a.qscale, a.qscale), make_float2(nm, nm));
-                    pk[i] = pack_bf16x2(ex2(x.x), ex2(x.y));
-                    add_bf16x2_to(l4[i & 3], pk[i]);
+                                           make_float2(qs, qs), make_float2(nm, nm));
+                    pk[i] = pack_p<F8>(ex2(x.x), ex2(x.y));
+                    add_p_to<F8>(l4[i & 3], pk[i]);
                 }
                 if (s > 0) {
                     // this half's previous O += P V has finished (waited at every step and at the
@@ -689,8 +890,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float f_me = mref == -INFINITY ? 0.0f : ex2(mref - mrow);
             const float f_ot = m_ot == -INFINITY ? 0.0f : ex2(m_ot - mrow);
             const float l = l_half * f_me + l_ot * f_ot;
-            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-            const float f0 = ch == 0 ? f_me : f_ot, f1 = ch == 0 ? f_ot : f_me;
+            const float inv = l > 0.0f ? vs / l : 0.0f;
+            // partial mode: O carries the V scale (the merge divides by the summed l only)
+            const float pv = PARTIAL ? vs : 1.0f;
+            const float f0 = (ch == 0 ? f_me : f_ot) * pv, f1 = (ch == 0 ? f_ot : f_me) * pv;
             // columns ch * HD + 32 c .. + 31 of the row's O = f0 O0 + f1 O1
             auto load_o = [&](int c, uint32_t (&o)[32]) {
                 uint32_t o1[32];
@@ -781,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // CTAs of the kernel that fit on the device at once (one per SM), rounded
 // down to whole pairs.
-template <int D, int G, bool PARTIAL>
+template <int D, int G, bool PARTIAL, bool F8>
 pkv_status setup(pkv_pool *pool, int *max_pairs)
 {
     using L = Layout<D>;
@@ -789,10 +992,10 @@ pkv_status setup(pkv_pool *pool, int *max_pairs)
     static cudaError_t attr_err = cudaSuccess;
     static int occ = 0;
     std::call_once(once, [&] {
-        attr_err = cudaFuncSetAttribute(prefill_tc_kernel<D, G, PARTIAL>,
+        attr_err = cudaFuncSetAttribute(prefill_tc_kernel<D, G, PARTIAL, F8>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::bytes);
         if (attr_err == cudaSuccess)
-            attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, prefill_tc_kernel<D, G, PARTIAL>,
+            attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, prefill_tc_kernel<D, G, PARTIAL, F8>,
                                                                      kThreads, L::bytes);
     });
     if (attr_err != cudaSuccess) return cuda_fail(attr_err, "prefill kernel attributes");
@@ -802,37 +1005,50 @@ pkv_status setup(pkv_pool *pool, int *max_pairs)
 }
 
 // pairs: an upper bound on the row-tile pairs (the grid is at most two CTAs per pair).
-template <int D, int G, bool PARTIAL>
+template <int D, int G, bool PARTIAL, bool F8>
 pkv_status launch(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, int64_t pairs, const Args &a,
                   cudaStream_t s)
 {
     using L = Layout<D>;
     int max_pairs = 0;
-    pkv_status st = setup<D, G, PARTIAL>(pool, &max_pairs);
+    pkv_status st = setup<D, G, PARTIAL, F8>(pool, &max_pairs);
     if (st != PKV_OK) return st;
     CUtensorMap tm_q;
     st = make_q_map(&tm_q, q, n_rows, n_q, D, G, kRows / G);
     if (st != PKV_OK) return st;
     const int grid = 2 * (int)std::min<int64_t>(pairs, max_pairs);
     LaunchScope ls(pool, PARTIAL ? kPrefix : kDecode, s);
-    cudaError_t e = launch_pdl(prefill_tc_kernel<D, G, PARTIAL>, dim3(grid), dim3(kThreads), L::bytes, s, tm_q,
+    cudaError_t e = launch_pdl(prefill_tc_kernel<D, G, PARTIAL, F8>, dim3(grid), dim3(kThreads), L::bytes, s, tm_q,
                                pool->tm_k, pool->tm_v, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, PARTIAL ? "prefix stage launch" : "prefill launch");
     return PKV_OK;
 }
 
-template <int D, bool PARTIAL>
+template <int D, bool PARTIAL, bool F8>
+pkv_status dispatch_g(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, int G, int64_t pairs, const Args &a,
+                      cudaStream_t s)
+{
+    switch (G) {
+    case 1: return launch<D, 1, PARTIAL, F8>(pool, q, n_rows, n_q, pairs, a, s);
+    case 2: return launch<D, 2, PARTIAL, F8>(pool, q, n_rows, n_q, pairs, a, s);
+    case 4: return launch<D, 4, PARTIAL, F8>(pool, q, n_rows, n_q, pairs, a, s);
+    case 8: return launch<D, 8, PARTIAL, F8>(pool, q, n_rows, n_q, pairs, a, s);
+    }
+    return fail(PKV_EUNSUPPORTED, "prefill: group size %d unsupported (1, 2, 4 or 8)", G);
+}
+
+// The launch for the pool's head size and KV type (bf16 or FP8 E4M3).
+template <bool PARTIAL>
 pkv_status dispatch(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, int G, int64_t pairs, const Args &a,
                     cudaStream_t s)
 {
-    switch (G) {
-    case 1: return launch<D, 1, PARTIAL>(pool, q, n_rows, n_q, pairs, a, s);
-    case 2: return launch<D, 2, PARTIAL>(pool, q, n_rows, n_q, pairs, a, s);
-    case 4: return launch<D, 4, PARTIAL>(pool, q, n_rows, n_q, pairs, a, s);
-    case 8: return launch<D, 8, PARTIAL>(pool, q, n_rows, n_q, pairs, a, s);
-    }
-    return fail(PKV_EUNSUPPORTED, "prefill: group size %d unsupported (1, 2, 4 or 8)", G);
+    const bool f8 = pool->dtype == PKV_FP8_E4M3;
+    if (pool->d_head == 128)
+        return f8 ? dispatch_g<128, PARTIAL, true>(pool, q, n_rows, n_q, G, pairs, a, s)
+                  : dispatch_g<128, PARTIAL, false>(pool, q, n_rows, n_q, G, pairs, a, s);
+    return f8 ? dispatch_g<64, PARTIAL, true>(pool, q, n_rows, n_q, G, pairs, a, s)
+              : dispatch_g<64, PARTIAL, false>(pool, q, n_rows, n_q, G, pairs, a, s);
 }
 
 }  // namespace
@@ -849,7 +1065,8 @@ extern "C" pkv_status paged_prefill_attention(pkv_pool *pool, const void *q, int
     if (st != PKV_OK || batch == 0 || n_rows == 0) return st;
     if (n_rows < 0) return fail(PKV_EINVAL, "paged_prefill_attention: n_rows < 0");
     if (n_rows > INT32_MAX) return fail(PKV_EUNSUPPORTED, "paged_prefill_attention: more than 2^31 query rows");
-    if (pool->dtype != PKV_BF16) return fail(PKV_EUNSUPPORTED, "paged_prefill_attention: bf16 pools only");
+    if (pool->dtype == PKV_INT4)
+        return fail(PKV_EUNSUPPORTED, "paged_prefill_attention: bf16 and FP8 pools only (not 4-bit)");
     if (!q || !qo_indptr || !block_tables || !context_lens || !out)
         return fail(PKV_EINVAL, "paged_prefill_attention: NULL device pointer");
     if (((uintptr_t)q | (uintptr_t)out) & 15u)
@@ -868,6 +1085,7 @@ extern "C" pkv_status paged_prefill_attention(pkv_pool *pool, const void *q, int
     a.n_rows = n_rows;
     a.oob_row = (int)(pool->num_blocks * pool->n_kv * kBlockSize);
     a.qscale = scale * kLog2e;
+    a.scales = pool->scales;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.err = pool->err;
     a.shared_blocks = nullptr;
@@ -881,8 +1099,7 @@ extern "C" pkv_status paged_prefill_attention(pkv_pool *pool, const void *q, int
     if (pairs > INT32_MAX || n_rows * G > INT32_MAX)
         return fail(PKV_EUNSUPPORTED, "paged_prefill_attention: too many query rows");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return pool->d_head == 128 ? dispatch<128, false>(pool, q, n_rows, n_q, G, pairs, a, s)
-                               : dispatch<64, false>(pool, q, n_rows, n_q, G, pairs, a, s);
+    return dispatch<false>(pool, q, n_rows, n_q, G, pairs, a, s);
 }
 
 namespace pkv {
@@ -917,6 +1134,7 @@ pkv_status launch_prefix_stage(pkv_pool *pool, const void *q, int batch, int n_q
     a.n_rows = batch;
     a.oob_row = (int)(pool->num_blocks * pool->n_kv * kBlockSize);
     a.qscale = qscale;
+    a.scales = pool->scales;
     a.out = nullptr;
     a.err = pool->err;
     a.shared_blocks = prefix_blocks;
@@ -927,8 +1145,7 @@ pkv_status launch_prefix_stage(pkv_pool *pool, const void *q, int batch, int n_q
     a.ws_o = ws_o;
     a.pre_base = pre_base;
     const int64_t pairs = (int64_t)a.n_chunks * pool->n_kv * ((((int64_t)batch * G + kRows - 1) / kRows + 1) / 2);
-    return pool->d_head == 128 ? dispatch<128, true>(pool, q, batch, n_q, G, pairs, a, s)
-                               : dispatch<64, true>(pool, q, batch, n_q, G, pairs, a, s);
+    return dispatch<true>(pool, q, batch, n_q, G, pairs, a, s);
 }
 
 }  // namespace pkv

@@ -153,6 +153,19 @@ pkv_status kv_pool_layout(const pkv_pool *pool, pkv_layout *out);
  * Errors: ERANGE. */
 pkv_status kv_pool_set_partition_tokens(pkv_pool *pool, int32_t tokens);
 
+/* How paged_decode_attention_prefix runs on this pool.
+ *   PKV_CASCADE_AUTO (0, the default): the cascade (prefix read once for the
+ *     batch) when batch x prefix tokens is at least 2^17 and the batch at
+ *     least 8 sequences; plain paged decode over the whole tables otherwise,
+ *     where re-reading the prefix from L2 costs less than the cascade's
+ *     prefix stage and merge (the crossover measured on GB300).
+ *   PKV_CASCADE_ALWAYS (1), PKV_CASCADE_NEVER (2): force one of them.
+ * Results agree up to rounding either way.  Errors: EINVAL. */
+#define PKV_CASCADE_AUTO 0
+#define PKV_CASCADE_ALWAYS 1
+#define PKV_CASCADE_NEVER 2
+pkv_status kv_pool_set_cascade_mode(pkv_pool *pool, int32_t mode);
+
 /* Grow the pool's split-KV workspace now (it otherwise grows inside the
  * first decode call that needs more), so that later decode calls with at
  * most `batch` sequences, `n_q` query heads and `max_blocks_per_seq` table
@@ -280,7 +293,9 @@ pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host, const void
  * prefix: the prefix's K and V are read once for the whole batch instead of
  * once per sequence ("Memory Management in LLM Serving Systems", "Prefix
  * sharing": decode-time reads for the shared part drop from n x p to p).
- * Same result as paged_decode_attention (up to rounding order):
+ * Same result as paged_decode_attention (up to rounding order).  The pool's
+ * cascade mode (kv_pool_set_cascade_mode) decides whether the call runs the
+ * cascade or plain paged decode; the cascade:
  *   stage 1 decodes each sequence's blocks after the prefix; stage 2
  *   attends every query row of each KV head to the prefix on the tcgen05
  *   tensor cores (the prefill kernel of paged_prefill_attention, without
@@ -293,8 +308,9 @@ pkv_status paged_decode_step_host(pkv_pool *pool, const void *q_host, const void
  *                    equal prefix_blocks (not checked).
  *   context_lens[b]  at least n_prefix_blocks * 16 (shorter ones are
  *                    treated as prefix-only and set PKV_DEVERR_CTX_RANGE).
- * bf16 pools only (EUNSUPPORTED for FP8).  Other arguments and errors as
- * paged_decode_attention. */
+ * bf16 and FP8 pools (EUNSUPPORTED for 4-bit ones); on FP8 pools both
+ * stages read E4M3 bytes and apply the pool's per-head scales.  Other
+ * arguments and errors as paged_decode_attention. */
 pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *q, int32_t n_q,
                                          const int32_t *prefix_blocks, int32_t n_prefix_blocks,
                                          const int32_t *block_tables, int32_t max_blocks_per_seq,
@@ -318,13 +334,17 @@ pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *q, int32_t 
  *              A chunk longer than its cache, or a length past the table,
  *              sets PKV_DEVERR_CTX_RANGE.
  *   out        device bf16 [n_rows][n_q][d_head].
- * bf16 pools.  One launch (one persistent CTA per SM): tiles of 128 query
- * rows per (sequence, KV head) on the tcgen05 tensor cores; each CTA copies
- * the K/V tiles it uses into its own shared memory (TMA, this GPU's pool).
+ * bf16 and FP8 pools.  One launch (one persistent CTA per SM): tiles of 128
+ * query rows per (sequence, KV head) on the tcgen05 tensor cores; each CTA
+ * copies the K/V tiles it uses into its own shared memory (TMA, this GPU's
+ * pool).  On an FP8 pool the E4M3 tiles are widened to f16 in shared memory
+ * (exact) and the products run in f16 (q rounded to f16: |q| must stay in
+ * f16's range), with the K scale folded into the score scale and the V
+ * scale into the final normalisation.
  * An out-of-range block id is skipped (its keys masked) and sets
  * PKV_DEVERR_BLOCK_RANGE; a qo_indptr that points past n_rows skips those
  * rows' stores and sets PKV_DEVERR_CTX_RANGE.
- * Errors: EINVAL, EUNSUPPORTED (FP8 / 4-bit pools, group size, more than
+ * Errors: EINVAL, EUNSUPPORTED (4-bit pools, group size, more than
  * 2^31 query rows x group size), ECUDA. */
 pkv_status paged_prefill_attention(pkv_pool *pool, const void *q, int64_t n_rows, int32_t n_q,
                                    const int32_t *qo_indptr, const int32_t *block_tables, int32_t max_blocks_per_seq,

@@ -25,6 +25,12 @@ CASES = [
     (lambda: wl.build("pf_d64", 8, 2, 64, [90, 5, 257, 16], seed=103), [90, 5, 100, 16]),
     (lambda: wl.build("pf_mha", 4, 4, 64, [100, 31], seed=104), [60, 31]),
     (lambda: wl.build("pf_g2", 16, 8, 128, [64, 512, 3], seed=105), [33, 512, 2]),
+    # FP8 E4M3 pools: the oracle dequantises the same E4M3 bytes with the pool's per-head scales
+    (lambda: wl.build("pf_fp8_g4", 32, 8, 128, [1, 40, 300, 1000], dtype="fp8", seed=111), [1, 17, 300, 64]),
+    (lambda: wl.build("pf_fp8_g8", 64, 8, 128, [200, 33, 700], dtype="fp8", seed=112), [200, 0, 5]),
+    (lambda: wl.build("pf_fp8_d64", 8, 2, 64, [90, 5, 257, 16], dtype="fp8", seed=113), [90, 5, 100, 16]),
+    (lambda: wl.build("pf_fp8_mha", 4, 4, 64, [100, 31], dtype="fp8", seed=114), [60, 31]),
+    (lambda: wl.build("pf_fp8_g2", 16, 8, 128, [64, 512, 3], dtype="fp8", seed=115), [33, 512, 2]),
 ]
 
 
@@ -67,12 +73,15 @@ def test_prefill_flags_a_chunk_longer_than_its_cache():
         assert pool.get_error(clear=True) & pkv.DEVERR_CTX_RANGE
 
 
-def test_prefill_full_size_sampled_rows():
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_prefill_full_size_sampled_rows(dtype):
     """The 64 x 512-token Llama3-8B chunk workload in the launch configuration
-    the benchmark times; sampled rows checked against the oracle: row i of a
-    chunk is the decode of its query over positions 0 .. C - T + i, so each
-    sample is an oracle decode with that context length."""
-    w = wl.llama3_8b()
+    the benchmark times (and the same on an FP8 pool); sampled rows checked
+    against the oracle: row i of a chunk is the decode of its query over
+    positions 0 .. C - T + i, so each sample is an oracle decode with that
+    context length."""
+    w = wl.llama3_8b() if dtype == "bf16" else wl.build(
+        "llama3_8b_fp8_b64", 32, 8, 128, wl.llama3_8b().context_lens, dtype="fp8", seed=12)
     T = 512
     rng = np.random.default_rng(11)
     q = wl.f32_to_bf16_bits(rng.normal(size=(w.batch * T, w.n_q, w.d_head)).astype(np.float32))
@@ -113,3 +122,12 @@ def test_prefill_bad_block_is_flagged_and_other_sequences_exact():
     sub_indptr = np.concatenate([[0], np.cumsum([indptr[b + 1] - indptr[b] for b in keep])]).astype(np.int32)
     ref = mirror(w).prefill(q[sub_rows], sub_indptr, tables[keep], w.context_lens[keep], w.scale)
     assert_close(got[sub_rows], ref, "sequences beside the bad one")
+
+
+def test_prefill_rejects_4bit_pools():
+    with pkv.kv_pool_create(8, 16, 2, 64, pkv.INT4) as pool:
+        pool.set_int4_key_params(np.ones((2, 64)), np.zeros((2, 64)))
+        q = torch.zeros(4, 4, 64, dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(pkv.PagedKVError) as e:
+            pkv.paged_prefill_attention(pool, q, i32_dev([0, 4]), i32_dev(np.zeros((1, 2))), i32_dev([20]), 0.125)
+        assert e.value.status == 5
