@@ -117,9 +117,19 @@ struct Tune {
     // (3 CTAs = 12 warps per SM), FP8 d128 3 stages of 4 KiB (4 CTAs per SM).
     // Swept on GB300 over 2..8 warps and 32..128 KiB.
     static constexpr int NW = 4;
-    static constexpr int RING_KIB = 48;
+    // 4-bit: 64 KiB, 8 stages of 2 KiB per warp (a power of two, so a stage
+    // index is a mask); its three CTAs per SM are held by registers, not by
+    // shared memory
+    static constexpr int RING_KIB = KV == 2 ? 64 : 48;
 #endif
 };
+
+#ifndef PKV_I4_WARPS_PER_SM
+#define PKV_I4_WARPS_PER_SM 12
+#endif
+#ifndef PKV_F8_WARPS_PER_SM
+#define PKV_F8_WARPS_PER_SM 12
+#endif
 
 template <int D, int G, int KV>
 struct Cfg {
@@ -129,7 +139,8 @@ struct Cfg {
     // resident CTAs per SM the register budget is held to: 12 warps per SM,
     // i.e. 3 x 128 threads of at most 168 registers for 4-warp CTAs (the
     // shared-memory ring allows no more for bf16 d128)
-    static constexpr int kMinBlocks = 12 / NW > 0 ? 12 / NW : 1;
+    static constexpr int kWarpsPerSm = KV == 2 ? PKV_I4_WARPS_PER_SM : KV == 1 ? PKV_F8_WARPS_PER_SM : 12;
+    static constexpr int kMinBlocks = kWarpsPerSm / NW > 0 ? kWarpsPerSm / NW : 1;
     static constexpr int kStages = std::min(8, std::max(2, Tune<D, G, KV>::RING_KIB * 1024 / (NW * Gm::STAGE)));
     // shared-memory layout (bytes from a 1024-byte aligned base)
     static constexpr int kRing = NW * kStages * Gm::STAGE;
@@ -334,6 +345,16 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
                      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// 2^x with the MUFU approximation (relative error about 2^-22; results below
+// 2^-126 flush to 0, and 2^-inf = 0).  The 4-bit path's softmax uses it: its
+// per-block instruction count, not HBM, bounds that kernel.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Transpose an 8x8 matrix of 16-bit values held one row-pair per thread.
 __device__ __forceinline__ uint32_t movm_t(uint32_t x)
 {
@@ -449,7 +470,8 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs &a, int b, int g, 
             const int base = c4 * (D / 4) + 8 * (ks >> 1), s0 = 2 * (ks & 1);
             const float *sk = a.k_params + (int64_t)g * D + base + s0;
             const __nv_bfloat16 *qq = qrow + base + s0;
-            auto qv = [&](int k) { return live ? __bfloat162float(qq[k]) * sk[k] : 0.0f; };
+            // q' = q * k_scale * (scale * log2 e): the score scale folded in once per piece
+            auto qv = [&](int k) { return live ? __bfloat162float(qq[k]) * sk[k] * a.qscale : 0.0f; };
             qf[ks][0] = pack2<true>(qv(0), qv(4));
             qf[ks][1] = pack2<true>(qv(1) * 0.0625f, qv(5) * 0.0625f);
         } else if constexpr (!FP8) {
@@ -865,21 +887,29 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
     Piece pc;
     bool have = first_piece(st, me, pc);
     uint32_t qn[NT][2];
-    if (have) load_q_frags<D, G, KV>(a, pc.b, pc.g, g8, c4, qn);
+    if constexpr (!I4)
+        if (have) load_q_frags<D, G, KV>(a, pc.b, pc.g, g8, c4, qn);
     int consumed = 0;
     while (have) {
         Piece nx = pc;
         const bool have_nx = next_piece(st, nx);
         // q of head g8 of the group as MMA B fragments (zero for padding heads);
         // the next piece's are fetched now so their latency overlaps this one.
+        // 4-bit pools load them when the piece starts instead: their pieces are
+        // long (a quarter of a bf16 block's bytes per block) and the registers
+        // of a second set are worth more as occupancy.
         uint32_t qf[NT][2];
+        if constexpr (I4) {
+            load_q_frags<D, G, KV>(a, pc.b, pc.g, g8, c4, qf);
+        } else {
 #pragma unroll
-        for (int ks = 0; ks < NT; ++ks) {
-            qf[ks][0] = qn[ks][0];
-            qf[ks][1] = qn[ks][1];
+            for (int ks = 0; ks < NT; ++ks) {
+                qf[ks][0] = qn[ks][0];
+                qf[ks][1] = qn[ks][1];
+            }
+            if constexpr (FP8) q_frags_to_f16<D>(qf);  // before qn is loaded again
+            if (have_nx) load_q_frags<D, G, KV>(a, nx.b, nx.g, g8, c4, qn);
         }
-        if constexpr (FP8) q_frags_to_f16<D>(qf);  // before qn is loaded again
-        if (have_nx) load_q_frags<D, G, KV>(a, nx.b, nx.g, g8, c4, qn);
         const float qs = a.qscale * (FP8 ? a.scales[pc.g] : 1.0f);
         const int C_len = cl[pc.b];
         // Fused step: the warp owning the block of position C_len-1 appends the
@@ -968,7 +998,8 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                 }
                 float s[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) s[i] = (sa[i] + sb[i]) * qs;
+                for (int i = 0; i < 4; ++i) s[i] = I4 ? sa[i] + sb[i] : (sa[i] + sb[i]) * qs;  // 4-bit: qs is in q'
+
                 if (g8 >= nv) s[0] = s[1] = -INFINITY;
                 if (g8 + 8 >= nv) s[2] = s[3] = -INFINITY;
                 // ---- online softmax (token 0 of a block is always valid) ----
@@ -1125,30 +1156,25 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                 const int nv0 = ok0 ? min(kBlockSize, C_len - (a.skip_blocks + j) * kBlockSize) : 0;
                 const int nv1 = ok1 ? min(kBlockSize, C_len - (a.skip_blocks + j + 1) * kBlockSize) : 0;
                 constexpr int WPT = D / 32;  // packed key words per token row per thread
-                auto kwords = [&](uint32_t kb, uint32_t (&kx)[WPT], uint32_t (&ky)[WPT]) {
-                    if constexpr (WPT == 4) {
-                        const uint4 x = lds128(kb + swz<Gm::BOXB>(g8 * Gm::ROWB + 16 * c4));
-                        const uint4 y = lds128(kb + swz<Gm::BOXB>((g8 + 8) * Gm::ROWB + 16 * c4));
-                        kx[0] = x.x; kx[1] = x.y; kx[2] = x.z; kx[3] = x.w;
-                        ky[0] = y.x; ky[1] = y.y; ky[2] = y.z; ky[3] = y.w;
-                    } else {
-                        const uint2 x = lds64(kb + swz<Gm::BOXB>(g8 * Gm::ROWB + 8 * c4));
-                        const uint2 y = lds64(kb + swz<Gm::BOXB>((g8 + 8) * Gm::ROWB + 8 * c4));
-                        kx[0] = x.x; kx[1] = x.y;
-                        ky[0] = y.x; ky[1] = y.y;
-                    }
-                };
                 float sa0[4] = {0.f, 0.f, 0.f, 0.f}, sb0[4] = {0.f, 0.f, 0.f, 0.f};
                 float sa1[4] = {0.f, 0.f, 0.f, 0.f}, sb1[4] = {0.f, 0.f, 0.f, 0.f};
-                {
-                    uint32_t kx0[WPT], ky0[WPT], kx1[WPT], ky1[WPT];
-                    kwords(kb0, kx0, ky0);
-                    kwords(kb1, kx1, ky1);
+                // the thread's packed key words two at a time (8 bytes of each of its two token rows
+                // per block), so that only eight of them are live at once
 #pragma unroll
-                    for (int ks = 0; ks < NT; ++ks) {
-                        const int w = ks >> 1;
-                        const uint32_t x0 = (ks & 1) ? kx0[w] >> 8 : kx0[w], y0 = (ks & 1) ? ky0[w] >> 8 : ky0[w];
-                        const uint32_t x1 = (ks & 1) ? kx1[w] >> 8 : kx1[w], y1 = (ks & 1) ? ky1[w] >> 8 : ky1[w];
+                for (int hh = 0; hh < WPT / 2; ++hh) {
+                    auto kpair = [&](uint32_t kb, int row) {
+                        return lds64(kb + swz<Gm::BOXB>(row * Gm::ROWB + 4 * WPT * c4) + 8 * hh);
+                    };
+                    const uint2 kx0 = kpair(kb0, g8), ky0 = kpair(kb0, g8 + 8);
+                    const uint2 kx1 = kpair(kb1, g8), ky1 = kpair(kb1, g8 + 8);
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const int ks = 4 * hh + k4;
+                        const bool second = (k4 >> 1) != 0;  // word 2 hh + 1
+                        const uint32_t wx0 = second ? kx0.y : kx0.x, wy0 = second ? ky0.y : ky0.x;
+                        const uint32_t wx1 = second ? kx1.y : kx1.x, wy1 = second ? ky1.y : ky1.x;
+                        const uint32_t x0 = (ks & 1) ? wx0 >> 8 : wx0, y0 = (ks & 1) ? wy0 >> 8 : wy0;
+                        const uint32_t x1 = (ks & 1) ? wx1 >> 8 : wx1, y1 = (ks & 1) ? wy1 >> 8 : wy1;
                         const uint32_t fa0[4] = {i4_lo(x0), i4_lo(y0), i4_hi(x0), i4_hi(y0)};
                         const uint32_t fa1[4] = {i4_lo(x1), i4_lo(y1), i4_hi(x1), i4_hi(y1)};
                         mma16816<true>((ks & 1) ? sb0 : sa0, fa0, qf[ks][0], qf[ks][1]);
@@ -1159,8 +1185,8 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                 float s[8];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    s[i] = (sa0[i] + sb0[i]) * qs;
-                    s[4 + i] = (sa1[i] + sb1[i]) * qs;
+                    s[i] = sa0[i] + sb0[i];  // the score scale is folded into q'
+                    s[4 + i] = sa1[i] + sb1[i];
                 }
                 if (g8 >= nv0) s[0] = s[1] = -INFINITY;
                 if (g8 + 8 >= nv0) s[2] = s[3] = -INFINITY;
@@ -1175,10 +1201,10 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                     bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
                 }
                 const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-                const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+                const float al0 = ex2_approx(m0 - mn0), al1 = ex2_approx(m1 - mn1);
                 float p[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) p[i] = exp2f(s[i] - ((i & 1) ? mn1 : mn0));
+                for (int i = 0; i < 8; ++i) p[i] = ex2_approx(s[i] - ((i & 1) ? mn1 : mn0));
                 l0 = fmaf(l0, al0, (p[0] + p[2]) + (p[4] + p[6]));
                 l1 = fmaf(l1, al1, (p[1] + p[3]) + (p[5] + p[7]));
                 m0 = mn0;
@@ -1213,42 +1239,40 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                 const uint32_t pb00 = movm_t(h00), pb01 = movm_t(h01), pb10 = movm_t(h10), pb11 = movm_t(h11);
                 // ---- O^T += V^T . P^T, both blocks (codes are finite: no masking needed) ----
                 constexpr int WPR = D / 64;  // words per token row per thread (2 or 1)
-                auto vwords = [&](uint32_t vb, uint32_t (&r0)[WPR], uint32_t (&r1)[WPR], uint32_t (&r2)[WPR],
-                                  uint32_t (&r3)[WPR]) {
-                    const int rows[4] = {2 * c4, 2 * c4 + 1, 2 * c4 + 8, 2 * c4 + 9};
-                    uint32_t *rr[4] = {r0, r1, r2, r3};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        if constexpr (WPR == 2) {
-                            const uint2 v = lds64(vb + swz<Gm::BOXB>(rows[q] * Gm::ROWB + 8 * g8));
-                            rr[q][0] = v.x;
-                            rr[q][1] = v.y;
-                        } else {
-                            rr[q][0] = lds32(vb + swz<Gm::BOXB>(rows[q] * Gm::ROWB + 4 * g8));
-                        }
-                    }
+                // one packed value word of each of the thread's four token rows per block at a time
+                // (tiles 4 w .. 4 w + 3 use word w), so that only eight words are live at once
+                const int vrows[4] = {2 * c4, 2 * c4 + 1, 2 * c4 + 8, 2 * c4 + 9};
+                auto vword = [&](uint32_t vb, int q, int w) {
+                    return lds32(vb + swz<Gm::BOXB>(vrows[q] * Gm::ROWB + 4 * WPR * g8) + 4 * w);
                 };
-                uint32_t u0[WPR], u1[WPR], u2[WPR], u3[WPR], w0[WPR], w1[WPR], w2[WPR], w3[WPR];
-                vwords(kb0 + Gm::TILE, u0, u1, u2, u3);
-                vwords(kb1 + Gm::TILE, w0, w1, w2, w3);
-                auto tile2 = [&](auto tc) {
+                auto tile2 = [&](auto tc, const uint32_t (&u)[4], const uint32_t (&v)[4]) {
                     constexpr int t = decltype(tc)::value;
-                    const uint32_t za = i4_rows<t % 4>(u0[t / 4], u1[t / 4]), zb = i4_rows<t % 4>(u2[t / 4], u3[t / 4]);
-                    const uint32_t zc = i4_rows<t % 4>(w0[t / 4], w1[t / 4]), zd = i4_rows<t % 4>(w2[t / 4], w3[t / 4]);
+                    const uint32_t za = i4_rows<t % 4>(u[0], u[1]), zb = i4_rows<t % 4>(u[2], u[3]);
+                    const uint32_t zc = i4_rows<t % 4>(v[0], v[1]), zd = i4_rows<t % 4>(v[2], v[3]);
                     const uint32_t fa[4] = {i4_lo(za), i4_hi(za), i4_lo(zb), i4_hi(zb)};
                     const uint32_t fb[4] = {i4_lo(zc), i4_hi(zc), i4_lo(zd), i4_hi(zd)};
                     mma16816<true>(o[t], fa, pb00, pb01);
                     mma16816<true>(o[t], fb, pb10, pb11);
                 };
-                tile2(std::integral_constant<int, 0>{});
-                tile2(std::integral_constant<int, 1>{});
-                tile2(std::integral_constant<int, 2>{});
-                tile2(std::integral_constant<int, 3>{});
+                {
+                    const uint32_t u[4] = {vword(kb0 + Gm::TILE, 0, 0), vword(kb0 + Gm::TILE, 1, 0),
+                                           vword(kb0 + Gm::TILE, 2, 0), vword(kb0 + Gm::TILE, 3, 0)};
+                    const uint32_t v[4] = {vword(kb1 + Gm::TILE, 0, 0), vword(kb1 + Gm::TILE, 1, 0),
+                                           vword(kb1 + Gm::TILE, 2, 0), vword(kb1 + Gm::TILE, 3, 0)};
+                    tile2(std::integral_constant<int, 0>{}, u, v);
+                    tile2(std::integral_constant<int, 1>{}, u, v);
+                    tile2(std::integral_constant<int, 2>{}, u, v);
+                    tile2(std::integral_constant<int, 3>{}, u, v);
+                }
                 if constexpr (NT == 8) {
-                    tile2(std::integral_constant<int, 4>{});
-                    tile2(std::integral_constant<int, 5>{});
-                    tile2(std::integral_constant<int, 6>{});
-                    tile2(std::integral_constant<int, 7>{});
+                    const uint32_t u[4] = {vword(kb0 + Gm::TILE, 0, 1), vword(kb0 + Gm::TILE, 1, 1),
+                                           vword(kb0 + Gm::TILE, 2, 1), vword(kb0 + Gm::TILE, 3, 1)};
+                    const uint32_t v[4] = {vword(kb1 + Gm::TILE, 0, 1), vword(kb1 + Gm::TILE, 1, 1),
+                                           vword(kb1 + Gm::TILE, 2, 1), vword(kb1 + Gm::TILE, 3, 1)};
+                    tile2(std::integral_constant<int, 4>{}, u, v);
+                    tile2(std::integral_constant<int, 5>{}, u, v);
+                    tile2(std::integral_constant<int, 6>{}, u, v);
+                    tile2(std::integral_constant<int, 7>{}, u, v);
                 }
             }
             __syncwarp();
