@@ -281,7 +281,7 @@ def long_context_70b(seed: int = 3, batch: int = 16, context: int = 32768) -> Wo
     """70B long-context shape: n_q=64, n_kv=8, d_head=128, batch 16, every
     sequence at 32768 tokens (2 GiB of bf16 K+V read per call)."""
     need = batch * (context // BLOCK_SIZE)
-    return build("llama70b_longctx_b16_32k", 64, 8, 128, [context] * batch, seed=seed,
+    return build(f"llama70b_longctx_b{batch}_{context // 1024}k", 64, 8, 128, [context] * batch, seed=seed,
                  num_blocks=need + 64)
 
 
@@ -331,6 +331,8 @@ NAMED = {
     "tiny": tiny,
     "llama3_8b": llama3_8b,
     "long_context_70b": long_context_70b,
+    # the same kernel on 4 sequences (537 MB of KV): a profiling-sized case
+    "long_context_70b_b4": lambda: long_context_70b(batch=4),
     "fp8_lognormal": fp8_lognormal,
     "shared_prefix": shared_prefix,
     "shared_prefix_long": shared_prefix_long,
