@@ -307,28 +307,31 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
 // 64-column half, row r at r * 128 bytes, 16-byte chunk j at j ^ (r & 7).
 // Rows are read before any lane writes (warp-synchronous) and taken in
 // increasing order, so no write reaches an E4M3 row still to be read: for
-// D = 128 the second half's row r is exactly E4M3 row r; for D = 64 the f16
-// row r covers E4M3 rows 2r - 128 and 2r - 127, both at most r.
+// D = 128 the second half's row r is exactly E4M3 row r (so two warps may
+// convert disjoint row ranges at the same time); for D = 64 the f16 row r
+// covers E4M3 rows 2r - 128 and 2r - 127, both at most r (one warp, all rows).
+// D = 128: rows [row0, row0 + rows), rows a multiple of 16.
 template <int D>
-__device__ __forceinline__ void convert_kv_f16(uint8_t *stage, int lane)
+__device__ __forceinline__ void convert_kv_f16(uint8_t *stage, int lane, int row0 = 0, int rows = kKeys)
 {
     constexpr uint32_t KT = kKeys * D * 2;
     const uint32_t out = smem_u32(stage), in = out + KT / 2;
     if constexpr (D == 128) {
-        // lane: row 4 i + lane / 8 (two iterations at a time), E4M3 chunk c = lane % 8 (columns 16 c .. + 15)
+        // lane: row 4 i + lane / 8 (four iterations at a time), E4M3 chunk c = lane % 8 (columns 16 c .. + 15)
+        constexpr int U = 4;
         const int c = lane & 7;
 #pragma unroll 1
-        for (int i = 0; i < kKeys / 4; i += 2) {
-            uint4 x[2];
-            int r[2];
+        for (int i = row0 / 4; i < (row0 + rows) / 4; i += U) {
+            uint4 x[U];
+            int r[U];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < U; ++u) {
                 r[u] = 4 * (i + u) + (lane >> 3);
                 x[u] = lds128(in + r[u] * 128 + ((c ^ (r[u] & 7)) << 4));
             }
             __syncwarp();
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < U; ++u) {
                 uint4 lo, hi;
                 e4m3x4_to_f16x4(x[u].x, lo.x, lo.y);
                 e4m3x4_to_f16x4(x[u].y, lo.z, lo.w);
@@ -342,20 +345,21 @@ __device__ __forceinline__ void convert_kv_f16(uint8_t *stage, int lane)
             __syncwarp();
         }
     } else {
-        // lane: row 8 i + lane / 4, E4M3 chunk c = lane % 4
+        // lane: row 8 i + lane / 4 (four iterations at a time), E4M3 chunk c = lane % 4
+        constexpr int U = 4;
         const int c = lane & 3;
 #pragma unroll 1
-        for (int i = 0; i < kKeys / 8; i += 2) {
-            uint4 x[2];
-            int r[2];
+        for (int i = 0; i < kKeys / 8; i += U) {
+            uint4 x[U];
+            int r[U];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < U; ++u) {
                 r[u] = 8 * (i + u) + (lane >> 2);
                 x[u] = lds128(in + r[u] * 64 + ((c ^ ((r[u] >> 1) & 3)) << 4));
             }
             __syncwarp();
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < U; ++u) {
                 uint4 lo, hi;
                 e4m3x4_to_f16x4(x[u].x, lo.x, lo.y);
                 e4m3x4_to_f16x4(x[u].y, lo.z, lo.w);
@@ -522,6 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::kAbort);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int rank = (int)(blockIdx.x & 1);  // which tile of a pair
+    // FP8 pools with D = 128: each K (V) stage is widened to f16 half by the K (V) producer
+    // warp (rows 0..63, one step behind its copies) and half by the warp that issues the MMAs
+    // reading it (rows 64..127, just before it issues them)
+    constexpr bool kSplitConv = F8 && D == 128;
 
     if (tid == 0) {
         prefetch_tensormap(&tm_q);
@@ -531,7 +539,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool by_warps = i == L::OUT_FULL || i == L::OUT_FREE;
             const bool by_half = i == L::P_FULL || i == L::P_FULL + 1;  // the four warps of a key half
             const bool by_pair = i >= L::PAIR && i < L::PAIR + 4;  // the two warps of a lane quarter
-            mbar_init(&bar[i], by_warps ? kSoftmaxWarps : by_half ? kSoftmaxWarps / 2 : by_pair ? 2 : 1);
+            // FP8, D = 128: a K or V stage is converted half by its producer, half by its MMA warp
+            const bool by_conv = kSplitConv && ((i >= L::K_FULL && i < L::K_FULL + kKStages) ||
+                                                (i >= L::V_FULL && i < L::V_FULL + kVStages));
+            mbar_init(&bar[i], by_warps ? kSoftmaxWarps : by_half ? kSoftmaxWarps / 2 : (by_pair || by_conv) ? 2 : 1);
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -595,7 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int st = pend % NS;
             if (!wait_all(&raw[st], (pend / NS) & 1)) return false;
-            convert_kv_f16<D>(sm + ring + st * L::KT, lane);
+            if constexpr (kSplitConv) convert_kv_f16<D>(sm + ring + st * L::KT, lane, 0, kKeys / 2);
+            else convert_kv_f16<D>(sm + ring + st * L::KT, lane);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[st]);
@@ -685,6 +697,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < t.n_steps && ok; ++s, ++gs) {
                 if (is_qk) {
                     const int st = gs & 1, kst = gs % kKStages;
+                    if constexpr (kSplitConv) {  // rows 64..127 of this K stage
+                        if (!(ok = wait_all(&bar[L::K_RAW + kst], (gs / kKStages) & 1))) break;
+                        convert_kv_f16<D>(sm + L::kK + kst * L::KT, lane, kKeys / 2, kKeys / 2);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar[L::K_FULL + kst]);
+                    }
                     if (!(ok = wait_all(&bar[L::K_FULL + kst], (gs / kKStages) & 1))) break;
                     if (gs >= 2 && !(ok = wait_all(&bar[L::S_FREE + st], ((gs >> 1) + 1) & 1))) break;
                     tc_fence_after();
@@ -704,6 +723,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // O_h += P_h V_h for each key half h as soon as its P is in tensor memory; the
                     // step's S buffer (which holds the two P) is free once both have run
                     const int vst = gs % kVStages, st = gs & 1;
+                    if constexpr (kSplitConv) {  // rows 64..127 of this V stage
+                        if (!(ok = wait_all(&bar[L::V_RAW + vst], (gs / kVStages) & 1))) break;
+                        convert_kv_f16<D>(sm + L::kV + vst * L::KT, lane, kKeys / 2, kKeys / 2);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar[L::V_FULL + vst]);
+                    }
                     if (!(ok = wait_all(&bar[L::V_FULL + vst], (gs / kVStages) & 1))) break;
                     const uint32_t vb = base + L::kV + vst * L::KT;
                     for (int h = 0; h < 2; ++h) {
