@@ -345,6 +345,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
                      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Slack (log2 units) of the decode softmax's lazy reference maximum: P <= 2^slack.
+// 4-bit pools feed the MMA P times each token's value scale in f16, so their P
+// stays small enough for f16 whatever the value range.
+template <int KV>
+constexpr float kRefSlack = KV == 2 ? 2.0f : 8.0f;
+
 // 2^x with the MUFU approximation (relative error about 2^-22; results below
 // 2^-126 flush to 0, and 2^-inf = 0).  The 4-bit path's softmax uses it: its
 // per-block instruction count, not HBM, bounds that kernel.
@@ -924,6 +930,35 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;  // heads 2c, 2c+1
         float z0 = 0.0f, z1 = 0.0f;    // 4-bit: sum of p * (value zero point), heads 2c, 2c+1
         float zs0 = 0.0f, zs1 = 0.0f;  // 4-bit: sum of the f16 (p * value scale) the MMA used
+        // Lazy reference maximum.  m0, m1 are reference maxima of heads 2c, 2c+1 (the same in
+        // every lane of a head): a block's weights are 2^(s - m), and only when some lane's
+        // scores (this thread's maxima lm0, lm1) pass a reference by more than kRefSlack does
+        // the warp take the heads' maxima across lanes (three shuffle rounds), raise the
+        // references and rescale l and O by al.  So P <= 2^kRefSlack and most blocks skip the
+        // reduction.  The result is the same ratio sum p v / sum p in exact arithmetic.
+        auto ref_update = [&](float lm0, float lm1, float &al0, float &al1) {
+            if constexpr (KV != kKvFp8)  // FP8 pools take the maxima every block (measured faster there)
+                if (!__any_sync(kFull, lm0 > m0 + kRefSlack<KV> || lm1 > m1 + kRefSlack<KV>)) return;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                lm0 = fmaxf(lm0, __shfl_xor_sync(kFull, lm0, off));
+                lm1 = fmaxf(lm1, __shfl_xor_sync(kFull, lm1, off));
+            }
+            const float mn0 = fmaxf(m0, lm0), mn1 = fmaxf(m1, lm1);
+            al0 = exp2f(m0 - mn0);  // 0 while the reference is -inf
+            al1 = exp2f(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            if (__any_sync(kFull, al0 != 1.0f || al1 != 1.0f)) {
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    o[t][0] *= al0;
+                    o[t][1] *= al1;
+                    o[t][2] *= al0;
+                    o[t][3] *= al1;
+                }
+            }
+        };
 
         // One block: wait for its stage, (fused step, last block only) patch in
         // the new token, then scores, softmax and P.V.  The patching variant is
@@ -1002,30 +1037,13 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
 
                 if (g8 >= nv) s[0] = s[1] = -INFINITY;
                 if (g8 + 8 >= nv) s[2] = s[3] = -INFINITY;
-                // ---- online softmax (token 0 of a block is always valid) ----
-                float bm0 = fmaxf(s[0], s[2]), bm1 = fmaxf(s[1], s[3]);
-#pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
-                    bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
-                }
-                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-                const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-                const float p0 = exp2f(s[0] - mn0), p1 = exp2f(s[1] - mn1);
-                const float p2 = exp2f(s[2] - mn0), p3 = exp2f(s[3] - mn1);
+                // ---- online softmax (token 0 of a block is always valid), lazy reference maximum ----
+                float al0 = 1.0f, al1 = 1.0f;
+                ref_update(fmaxf(s[0], s[2]), fmaxf(s[1], s[3]), al0, al1);
+                const float p0 = exp2f(s[0] - m0), p1 = exp2f(s[1] - m1);
+                const float p2 = exp2f(s[2] - m0), p3 = exp2f(s[3] - m1);
                 l0 = fmaf(l0, al0, p0 + p2);
                 l1 = fmaf(l1, al1, p1 + p3);
-                m0 = mn0;
-                m1 = mn1;
-                if (__any_sync(kFull, al0 != 1.0f || al1 != 1.0f)) {
-#pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        o[t][0] *= al0;
-                        o[t][1] *= al1;
-                        o[t][2] *= al0;
-                        o[t][3] *= al1;
-                    }
-                }
                 uint32_t pb0, pb1;  // P^T rows: tokens 2c, 2c+1 (pb0), 2c+8, 2c+9 (pb1) of head g
                 if constexpr (I4) {
                     // v = c * s + z per token: P V = (P * s) C + (P . z); masked tokens weigh 0
@@ -1192,32 +1210,16 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                 if (g8 + 8 >= nv0) s[2] = s[3] = -INFINITY;
                 if (g8 >= nv1) s[4] = s[5] = -INFINITY;
                 if (g8 + 8 >= nv1) s[6] = s[7] = -INFINITY;
-                // ---- online softmax over the 32 tokens (a valid block has a valid token 0) ----
-                float bm0 = fmaxf(fmaxf(s[0], s[2]), fmaxf(s[4], s[6]));
-                float bm1 = fmaxf(fmaxf(s[1], s[3]), fmaxf(s[5], s[7]));
-#pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    bm0 = fmaxf(bm0, __shfl_xor_sync(kFull, bm0, off));
-                    bm1 = fmaxf(bm1, __shfl_xor_sync(kFull, bm1, off));
-                }
-                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-                const float al0 = ex2_approx(m0 - mn0), al1 = ex2_approx(m1 - mn1);
+                // ---- online softmax over the 32 tokens (a valid block has a valid token 0),
+                // lazy reference maximum ----
+                float al0 = 1.0f, al1 = 1.0f;
+                ref_update(fmaxf(fmaxf(s[0], s[2]), fmaxf(s[4], s[6])), fmaxf(fmaxf(s[1], s[3]), fmaxf(s[5], s[7])),
+                           al0, al1);
                 float p[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) p[i] = ex2_approx(s[i] - ((i & 1) ? mn1 : mn0));
+                for (int i = 0; i < 8; ++i) p[i] = ex2_approx(s[i] - ((i & 1) ? m1 : m0));
                 l0 = fmaf(l0, al0, (p[0] + p[2]) + (p[4] + p[6]));
                 l1 = fmaf(l1, al1, (p[1] + p[3]) + (p[5] + p[7]));
-                m0 = mn0;
-                m1 = mn1;
-                if (__any_sync(kFull, al0 != 1.0f || al1 != 1.0f)) {
-#pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        o[t][0] *= al0;
-                        o[t][1] *= al1;
-                        o[t][2] *= al0;
-                        o[t][3] *= al1;
-                    }
-                }
                 // v = c * s + z per token: P V = (P * s) C + (P . z); masked tokens weigh 0
                 const float2 zero2 = make_float2(0.f, 0.f);
                 const float2 vp00 = g8 < nv0 ? vpbuf[s0i * kBlockSize + g8] : zero2;
