@@ -352,8 +352,7 @@ template <int KV>
 constexpr float kRefSlack = KV == 2 ? 2.0f : 8.0f;
 
 // 2^x with the MUFU approximation (relative error about 2^-22; results below
-// 2^-126 flush to 0, and 2^-inf = 0).  The 4-bit path's softmax uses it: its
-// per-block instruction count, not HBM, bounds that kernel.
+// 2^-126 flush to 0, 2^-inf = 0 and 2^0 = 1).  The decode softmax's weights use it.
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;
@@ -945,8 +944,8 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                 lm1 = fmaxf(lm1, __shfl_xor_sync(kFull, lm1, off));
             }
             const float mn0 = fmaxf(m0, lm0), mn1 = fmaxf(m1, lm1);
-            al0 = exp2f(m0 - mn0);  // 0 while the reference is -inf
-            al1 = exp2f(m1 - mn1);
+            al0 = ex2_approx(m0 - mn0);  // 0 while the reference is -inf
+            al1 = ex2_approx(m1 - mn1);
             m0 = mn0;
             m1 = mn1;
             if (__any_sync(kFull, al0 != 1.0f || al1 != 1.0f)) {
@@ -1040,8 +1039,8 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                 // ---- online softmax (token 0 of a block is always valid), lazy reference maximum ----
                 float al0 = 1.0f, al1 = 1.0f;
                 ref_update(fmaxf(s[0], s[2]), fmaxf(s[1], s[3]), al0, al1);
-                const float p0 = exp2f(s[0] - m0), p1 = exp2f(s[1] - m1);
-                const float p2 = exp2f(s[2] - m0), p3 = exp2f(s[3] - m1);
+                const float p0 = ex2_approx(s[0] - m0), p1 = ex2_approx(s[1] - m1);
+                const float p2 = ex2_approx(s[2] - m0), p3 = ex2_approx(s[3] - m1);
                 l0 = fmaf(l0, al0, p0 + p2);
                 l1 = fmaf(l1, al1, p1 + p3);
                 uint32_t pb0, pb1;  // P^T rows: tokens 2c, 2c+1 (pb0), 2c+8, 2c+9 (pb1) of head g
