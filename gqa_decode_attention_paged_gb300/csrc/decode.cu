@@ -360,6 +360,11 @@ __device__ __forceinline__ float ex2_approx(float x)
     return y;
 }
 
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // Transpose an 8x8 matrix of 16-bit values held one row-pair per thread.
 __device__ __forceinline__ uint32_t movm_t(uint32_t x)
 {
@@ -818,6 +823,14 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
     int32_t *rb = cl + a.batch;
     griddep_wait();  // inputs may come from the previous kernel on the stream
     griddep_launch_dependents();
+    {
+        // the block tables and q into L2, one 128-byte line per thread of the grid, while the
+        // lengths are scanned: the warps' first table and q reads then hit L2
+        const int64_t line = ((int64_t)blockIdx.x * kThreads + tid) * 128;
+        const int64_t tab_bytes = 4 * (a.indptr ? a.n_indices : (int64_t)a.batch * a.W);
+        if (line < tab_bytes) prefetch_l2(reinterpret_cast<const uint8_t *>(a.block_tables) + line);
+        if (line < (int64_t)a.batch * a.n_q * D * 2) prefetch_l2(reinterpret_cast<const uint8_t *>(a.q) + line);
+    }
     scan_blocks<NW>(a.context_lens, a.batch, a.W, a.indptr, a.n_indices, a.skip_blocks,
                     blockIdx.x == 0 ? a.err : nullptr, ps, cl, rb, warp_tot);  // ends with __syncthreads
     Stream st;
