@@ -523,9 +523,10 @@ __device__ __forceinline__ void q_frags_to_f16(uint32_t (&qf)[D / 16][2])
 //   M = max m_p,  L = sum 2^(m_p - M) l_p,  out = sum 2^(m_p - M) O_p / L.
 // A run is split when its first and last blocks fall in different slices of
 // the decode kernel's stream, which the kernel rederives from the lengths.
-// One wave of CTAs walks the runs: a CTA per run when there are no more runs
-// than CTAs (its warps each summing a quarter of the run's G x D output
-// columns), else a warp per run.
+// One wave of CTAs walks the runs: two CTAs per run when the wave holds twice
+// as many CTAs as runs (each warp summing an eighth of the run's G x D output
+// columns), a CTA per run when it holds as many (a quarter each), else a
+// warp per run.
 // ---------------------------------------------------------------------------
 
 constexpr int kMergeThreads = 128;
@@ -682,7 +683,17 @@ __global__ void __launch_bounds__(kMergeThreads, 4) merge_kernel(MergeArgs a)
         s_first = start / share;
         return (start + nblk - 1) / share - s_first + 1;
     };
-    if (runs <= (int)gridDim.x) {  // a CTA per run
+    if (2 * runs <= (int)gridDim.x) {  // two CTAs per run, each half of the columns: more pieces in flight
+        constexpr int CW2 = (CHUNKS + 2 * kMergeWarps - 1) / (2 * kMergeWarps);
+        const int r = blockIdx.x >> 1, half = blockIdx.x & 1;
+        if (r >= runs) return;
+        int b, g, s_first;
+        const int n = pieces(r, b, g, s_first);
+        if (a.n_pre == 0 && n <= 1) return;  // written whole by the decode kernel (or empty)
+        const int c_lo = min(CHUNKS, (half * kMergeWarps + warp) * CW2), c_hi = min(CHUNKS, c_lo + CW2);
+        const int64_t base = (int64_t)s_first + (int64_t)b * a.n_kv + g;  // slot of tail piece 0
+        if (c_lo < c_hi) merge_run_warp<D, G, CW2>(a, b, g, a.n_pre + n, base, c_lo, c_hi, lane);
+    } else if (runs <= (int)gridDim.x) {  // a CTA per run
         const int r = blockIdx.x;
         if (r >= runs) return;
         int b, g, s_first;
@@ -1476,7 +1487,6 @@ static pkv_status launch_merge(pkv_pool *pool, const DecodeArgs &a, int n_warps,
     m.slice_blocks = a.slice_blocks;
     m.pre_base = a.pre_base;
     m.n_pre = a.n_pre;
-    // one wave: as many CTAs as are resident at once, at most one per work item
     static int occ = 0;
     static std::once_flag once;
     const size_t smem = 4 * ((size_t)a.batch + 1);
@@ -1485,8 +1495,10 @@ static pkv_status launch_merge(pkv_pool *pool, const DecodeArgs &a, int n_warps,
                                                           4 * (kMaxBatch + 1)) != cudaSuccess)
             occ = 1;
     });
+    // one wave: as many CTAs as are resident at once; two per run while that fits, else at most one per run
     const int64_t runs = (int64_t)a.batch * a.n_kv;
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(runs, (int64_t)pool->num_sms * std::max(1, occ)));
+    const int64_t slots = (int64_t)pool->num_sms * std::max(1, occ);
+    const int grid = (int)std::max<int64_t>(1, 2 * runs <= slots ? 2 * runs : std::min<int64_t>(runs, slots));
     LaunchScope ls(pool, kMerge, s);
     cudaError_t e = launch_pdl(merge_kernel<D, G>, dim3((unsigned)grid), dim3(kMergeThreads), smem, s, m);
     ls.done();
