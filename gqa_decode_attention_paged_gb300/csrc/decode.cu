@@ -2017,10 +2017,12 @@ namespace pkv {
 // the tcgen05 prefill kernel in partial mode -- and stores a (max, sum, O)
 // partial per prefix chunk.  Stage 3, the merge kernel, combines the two.
 
-// PKV_CASCADE_AUTO: the cascade once batch x prefix tokens reaches 2^17 (and the batch 8).  Measured
-// on GB300 (bf16, n_q 32, n_kv 8, d 128, tails of 0..1024 tokens): prefix 1024 x batch 64 and
-// 2048 x 16 run faster as plain decode, 1024 x 128, 2048 x 64 and 4096 x 32 as the cascade.
+// PKV_CASCADE_AUTO: the cascade once the prefix holds 2048 tokens and batch x prefix tokens reaches
+// 2^17 (and the batch 8).  Measured on GB300 (bf16, n_q 32, n_kv 8, d 128, tails of 0..1024
+// tokens, L2 warm and evicted): 1024-token prefixes run faster as plain decode at every batch up to
+// 128, as do 2048 x 16 and 8192 x 8; 2048 x 64, 4096 x 32 and 8192 x 16 faster as the cascade.
 constexpr int64_t kCascadeMinSharedTokens = 1 << 17;
+constexpr int kCascadeMinPrefixBlocks = 128;  // 2048 tokens
 constexpr int kCascadeMinBatch = 8;
 
 template <int D, int G, int KV>
@@ -2121,6 +2123,7 @@ extern "C" pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *
     // from L2 and cost less than the cascade's prefix stage and merge.
     const bool cascade = pool->cascade_mode == PKV_CASCADE_ALWAYS ||
                          (pool->cascade_mode == PKV_CASCADE_AUTO && batch >= kCascadeMinBatch &&
+                          n_prefix_blocks >= kCascadeMinPrefixBlocks &&
                           (int64_t)n_prefix_blocks * kBlockSize * batch >= kCascadeMinSharedTokens);
     if (!cascade) return dispatch_kv(pool, a, G, s);
     const bool fp8 = pool->dtype == PKV_FP8_E4M3;

@@ -155,10 +155,11 @@ pkv_status kv_pool_set_partition_tokens(pkv_pool *pool, int32_t tokens);
 
 /* How paged_decode_attention_prefix runs on this pool.
  *   PKV_CASCADE_AUTO (0, the default): the cascade (prefix read once for the
- *     batch) when batch x prefix tokens is at least 2^17 and the batch at
- *     least 8 sequences; plain paged decode over the whole tables otherwise,
- *     where re-reading the prefix from L2 costs less than the cascade's
- *     prefix stage and merge (the crossover measured on GB300).
+ *     batch) when the prefix holds at least 2048 tokens, batch x prefix
+ *     tokens is at least 2^17 and the batch at least 8 sequences; plain paged
+ *     decode over the whole tables otherwise, where re-reading the prefix
+ *     from L2 costs less than the cascade's prefix stage and merge (the
+ *     crossover measured on GB300).
  *   PKV_CASCADE_ALWAYS (1), PKV_CASCADE_NEVER (2): force one of them.
  * Results agree up to rounding either way.  Errors: EINVAL. */
 #define PKV_CASCADE_AUTO 0

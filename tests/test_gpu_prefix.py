@@ -66,12 +66,14 @@ def test_cascade_long_prefix_sampled_sequences():
 
 
 @pytest.mark.parametrize("make,cascade_expected", [
-    (lambda: wl.shared_prefix(), True),        # 1024-token prefix x batch 128 = 2^17: the cascade
+    (lambda: wl.shared_prefix(), False),       # 1024-token prefix, batch 128: plain decode
     (lambda: wl.shared_prefix_long(), True),   # 8192-token prefix, batch 128: the cascade
     (lambda: wl.build("cp_auto_b64", 32, 8, 128, np.random.default_rng(70).integers(1025, 1500, 64), seed=70,
                       shared_prefix_tokens=1024), False),  # 1024 x 64: plain decode
     (lambda: wl.build("cp_auto_b4", 32, 8, 128, [2100, 2500, 2049, 3000], seed=69,
                       shared_prefix_tokens=2048), False),  # long prefix but batch 4: plain decode
+    (lambda: wl.build("cp_auto_2k_b64", 32, 8, 128, np.random.default_rng(71).integers(2049, 2600, 64), seed=71,
+                      shared_prefix_tokens=2048), True),   # 2048 x 64 = 2^17: the cascade
 ])
 def test_cascade_mode_auto_picks_by_prefix_and_batch(make, cascade_expected):
     w = make()
