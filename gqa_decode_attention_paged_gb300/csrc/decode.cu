@@ -1399,7 +1399,7 @@ struct WsLayout {
     size_t ml, o, total;
 };
 
-static WsLayout ws_layout(int batch, int n_q, int n_kv, int d_head, int64_t slots)
+static WsLayout ws_layout(int n_q, int n_kv, int d_head, int64_t slots)
 {
     const int G = n_q / n_kv;
     WsLayout w;
@@ -1514,7 +1514,7 @@ static pkv_status launch_decode(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
     size_t smem = 0;
     pkv_status st = decode_grid<D, G, KV>(pool, a.batch, a.W, &grid, &smem);
     if (st != PKV_OK) return st;
-    const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
+    const WsLayout L = ws_layout(a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
     st = ensure_workspace(pool, L.total);
     if (st != PKV_OK) return st;
     bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
@@ -1593,7 +1593,7 @@ pkv_status decode_workspace_bytes(pkv_pool *pool, int batch, int n_q, int max_bl
     else
         st = d128 ? grid_g<128, kKvBf16>(pool, G, batch, W, &warps) : grid_g<64, kKvBf16>(pool, G, batch, W, &warps);
     if (st != PKV_OK) return st;
-    *bytes = ws_layout(batch, n_q, pool->n_kv, pool->d_head,
+    *bytes = ws_layout(n_q, pool->n_kv, pool->d_head,
                        max_slots(pool, batch, pool->n_kv, max_blocks_per_seq, warps)).total;
     return PKV_OK;
 }
@@ -1734,7 +1734,7 @@ static pkv_status launch_step(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
     size_t smem = 0;
     pkv_status st = decode_grid<D, G, KV, true>(pool, a.batch, a.W, &grid, &smem);
     if (st != PKV_OK) return st;
-    const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
+    const WsLayout L = ws_layout(a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
     st = ensure_workspace(pool, L.total);
     if (st != PKV_OK) return st;
     bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
@@ -2037,7 +2037,7 @@ static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32
     int chunk_blocks = 0, n_chunks = 0;
     prefix_stage_chunks(pool, a.batch, a.n_q, n_prefix_blocks, &chunk_blocks, &n_chunks);
     const int64_t tail_slots = max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW);
-    const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, tail_slots + (int64_t)n_chunks * a.batch * a.n_kv);
+    const WsLayout L = ws_layout(a.n_q, a.n_kv, D, tail_slots + (int64_t)n_chunks * a.batch * a.n_kv);
     st = ensure_workspace(pool, L.total);
     if (st != PKV_OK) return st;
     bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
@@ -2172,7 +2172,7 @@ static pkv_status launch_decode_noalloc(pkv_pool *pool, DecodeArgs a, uint8_t *s
     size_t smem = 0;
     pkv_status st = decode_grid<D, G, KV>(pool, a.batch, a.W, &grid, &smem);
     if (st != PKV_OK) return st;
-    const WsLayout L = ws_layout(a.batch, a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
+    const WsLayout L = ws_layout(a.n_q, a.n_kv, D, max_slots(pool, a.batch, a.n_kv, a.W, grid * C::NW));
     if (L.total > kNoAllocScratchBytes)
         return fail(PKV_ERANGE,
                     "paged_decode_attention_noalloc: this call needs %zu bytes of scratch but the static array "

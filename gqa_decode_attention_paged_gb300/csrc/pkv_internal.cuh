@@ -311,11 +311,5 @@ __device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t u)
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
-// Two E4M3 codes packed in 16 bits (low byte first) -> two fp32 (exact).
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t u16)
-{
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(u16), __NV_E4M3);
-    return __half22float2(*reinterpret_cast<__half2 *>(&h));
-}
 
 }  // namespace pkv

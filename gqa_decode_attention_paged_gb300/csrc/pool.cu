@@ -126,7 +126,7 @@ void *mapped_host_ptr(const void *p)
 
 pkv_status make_q_map(CUtensorMap *map, const void *q, int64_t n_rows, int n_q, int d_head, int heads, int tokens)
 {
-    PFN_cuTensorMapEncodeTiled_v12000 encode;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     pkv_status st = tiled_encoder(&encode);
     if (st != PKV_OK) return st;
     cuuint64_t dims[3] = {(cuuint64_t)d_head, (cuuint64_t)n_q, (cuuint64_t)n_rows};
@@ -142,7 +142,7 @@ pkv_status make_q_map(CUtensorMap *map, const void *q, int64_t n_rows, int n_q, 
 
 pkv_status make_tensor_maps(pkv_pool *pool)
 {
-    PFN_cuTensorMapEncodeTiled_v12000 encode;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     pkv_status st = tiled_encoder(&encode);
     if (st != PKV_OK) return st;
     // rows of d_head bf16, d_head E4M3 bytes, or d_head / 2 bytes of packed 4-bit codes
