@@ -65,6 +65,7 @@ def parse_args(argv=None):
                    help="timed duration per workload of the per_config entries")
     p.add_argument("--mode", default="decode", choices=["decode", "blocks", "cascade", "prefill"])
     p.add_argument("--prefill-kv", default="bf16", choices=["bf16", "fp8"], help="--mode prefill: KV pool type")
+    p.add_argument("--cascade-kv", default="bf16", choices=["bf16", "fp8"], help="--mode cascade: KV pool type")
     return p.parse_args(argv)
 
 
@@ -836,9 +837,15 @@ def run_cascade(args):
     w = wl.NAMED[args.workload]() if args.workload in wl.NAMED else None
     if w is None or not w.shared_prefix_tokens:
         w = wl.shared_prefix()
+    if args.cascade_kv == "fp8":  # the same lengths and shared prefix on an FP8 E4M3 pool
+        w = wl.build(w.name + "_fp8", w.n_q, w.n_kv, w.d_head, w.context_lens, dtype="fp8", seed=w.seed,
+                     shared_prefix_tokens=w.shared_prefix_tokens, max_blocks_per_seq=w.max_blocks_per_seq)
     acct = algorithmic_bytes(w)
     dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).cuda().view(dt)  # noqa: E731
-    pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head, pkv.BF16)
+    pool = pkv.kv_pool_create(w.num_blocks, w.block_size, w.n_kv, w.d_head,
+                              pkv.FP8_E4M3 if args.cascade_kv == "fp8" else pkv.BF16)
+    if args.cascade_kv == "fp8":
+        pool.set_fp8_scales(w.k_scale, w.v_scale)
     pkv.paged_kv_append(pool, dev(w.fill_k.view(np.int16), torch.bfloat16), dev(w.fill_v.view(np.int16), torch.bfloat16),
                         dev(w.fill_slots, torch.int64))
     pkv.paged_kv_append(pool, dev(w.step_k.view(np.int16), torch.bfloat16), dev(w.step_v.view(np.int16), torch.bfloat16),

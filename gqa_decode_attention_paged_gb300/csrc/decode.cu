@@ -2017,13 +2017,20 @@ namespace pkv {
 // the tcgen05 prefill kernel in partial mode -- and stores a (max, sum, O)
 // partial per prefix chunk.  Stage 3, the merge kernel, combines the two.
 
-// PKV_CASCADE_AUTO: the cascade once the prefix holds 2048 tokens and batch x prefix tokens reaches
-// 2^17 (and the batch 8).  Measured on GB300 (bf16, n_q 32, n_kv 8, d 128, tails of 0..1024
-// tokens, L2 warm and evicted): 1024-token prefixes run faster as plain decode at every batch up to
-// 128, as do 2048 x 16 and 8192 x 8; 2048 x 64, 4096 x 32 and 8192 x 16 faster as the cascade.
-constexpr int64_t kCascadeMinSharedTokens = 1 << 17;
-constexpr int kCascadeMinPrefixBlocks = 128;  // 2048 tokens
-constexpr int kCascadeMinBatch = 8;
+// PKV_CASCADE_AUTO: whether the cascade pays for this prefix and batch, measured on GB300 (n_q 32,
+// n_kv 8, d 128, tails of 0..1024 tokens, L2 warm and evicted).  bf16: from a 2048-token prefix
+// with batch x prefix tokens >= 2^17 (1024-token prefixes run faster as plain decode at every
+// batch up to 128, as do 2048 x 16 and 8192 x 8; 2048 x 64, 4096 x 32 and 8192 x 16 faster as the
+// cascade).  FP8: plain decode pays its E4M3 conversions again on every re-read of the prefix, so
+// the cascade pays earlier: from batch x prefix >= 2^16 with batch >= 64 (512 x 128, 1024 x 64),
+// or >= 2^17 (1024 x 128: 47.6 against 65.8 us); 2048 x 32 and 4096 x 16 stay plain.
+static bool cascade_pays(int dtype, int n_prefix_blocks, int batch)
+{
+    if (batch < 8) return false;
+    const int64_t shared = (int64_t)n_prefix_blocks * kBlockSize * batch;
+    if (dtype == PKV_FP8_E4M3) return shared >= (1 << 17) || (shared >= (1 << 16) && batch >= 64);
+    return n_prefix_blocks >= 128 && shared >= (1 << 17);
+}
 
 template <int D, int G, int KV>
 static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32_t *prefix_blocks,
@@ -2122,9 +2129,7 @@ extern "C" pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *
     // Cascade or plain decode: with a short prefix the plain kernel's re-reads of it come
     // from L2 and cost less than the cascade's prefix stage and merge.
     const bool cascade = pool->cascade_mode == PKV_CASCADE_ALWAYS ||
-                         (pool->cascade_mode == PKV_CASCADE_AUTO && batch >= kCascadeMinBatch &&
-                          n_prefix_blocks >= kCascadeMinPrefixBlocks &&
-                          (int64_t)n_prefix_blocks * kBlockSize * batch >= kCascadeMinSharedTokens);
+                         (pool->cascade_mode == PKV_CASCADE_AUTO && cascade_pays(pool->dtype, n_prefix_blocks, batch));
     if (!cascade) return dispatch_kv(pool, a, G, s);
     const bool fp8 = pool->dtype == PKV_FP8_E4M3;
     if (pool->d_head == 128)

@@ -155,11 +155,13 @@ pkv_status kv_pool_set_partition_tokens(pkv_pool *pool, int32_t tokens);
 
 /* How paged_decode_attention_prefix runs on this pool.
  *   PKV_CASCADE_AUTO (0, the default): the cascade (prefix read once for the
- *     batch) when the prefix holds at least 2048 tokens, batch x prefix
- *     tokens is at least 2^17 and the batch at least 8 sequences; plain paged
- *     decode over the whole tables otherwise, where re-reading the prefix
- *     from L2 costs less than the cascade's prefix stage and merge (the
- *     crossover measured on GB300).
+ *     batch) where it measured faster on GB300, plain paged decode over the
+ *     whole tables otherwise (where re-reading the prefix from L2 costs less
+ *     than the cascade's prefix stage and merge).  bf16 pools: a prefix of at
+ *     least 2048 tokens and batch x prefix tokens >= 2^17.  FP8 pools (whose
+ *     plain decode converts the prefix again for every sequence): batch x
+ *     prefix tokens >= 2^17, or >= 2^16 with a batch of at least 64.  Never
+ *     below a batch of 8.
  *   PKV_CASCADE_ALWAYS (1), PKV_CASCADE_NEVER (2): force one of them.
  * Results agree up to rounding either way.  Errors: EINVAL. */
 #define PKV_CASCADE_AUTO 0

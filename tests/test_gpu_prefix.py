@@ -74,6 +74,10 @@ def test_cascade_long_prefix_sampled_sequences():
                       shared_prefix_tokens=2048), False),  # long prefix but batch 4: plain decode
     (lambda: wl.build("cp_auto_2k_b64", 32, 8, 128, np.random.default_rng(71).integers(2049, 2600, 64), seed=71,
                       shared_prefix_tokens=2048), True),   # 2048 x 64 = 2^17: the cascade
+    (lambda: wl.build("cp_auto_fp8_b128", 32, 8, 128, np.random.default_rng(72).integers(1025, 2050, 128),
+                      dtype="fp8", seed=72, shared_prefix_tokens=1024), True),  # FP8, 1024 x 128: the cascade
+    (lambda: wl.build("cp_auto_fp8_b32", 32, 8, 128, np.random.default_rng(73).integers(1025, 2050, 32),
+                      dtype="fp8", seed=73, shared_prefix_tokens=1024), False),  # FP8, 1024 x 32: plain decode
 ])
 def test_cascade_mode_auto_picks_by_prefix_and_batch(make, cascade_expected):
     w = make()
