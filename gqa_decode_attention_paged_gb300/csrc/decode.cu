@@ -117,10 +117,12 @@ struct Tune {
     // (3 CTAs = 12 warps per SM), FP8 d128 3 stages of 4 KiB (4 CTAs per SM).
     // Swept on GB300 over 2..8 warps and 32..128 KiB.
     static constexpr int NW = 4;
-    // 4-bit: 64 KiB, 8 stages of 2 KiB per warp (a power of two, so a stage
-    // index is a mask); its three CTAs per SM are held by registers, not by
-    // shared memory
-    static constexpr int RING_KIB = KV == 2 ? 64 : 48;
+    // 4-bit: 32 KiB, 4 stages of 2 KiB per warp at d_head 128 (two block
+    // pairs; a power of two, so a stage index is a mask); its three CTAs per
+    // SM are held by registers, not by shared memory.  Measured on GB300: 4
+    // stages 61.6 us per launch against 62.8 us with 8 (Llama3-8B shape,
+    // batch 128).
+    static constexpr int RING_KIB = KV == 2 ? 32 : 48;
 #endif
 };
 
@@ -437,9 +439,14 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
 // the mantissa of 1024.0 is exactly 1024 + c (low nibble of each half word),
 // or 1024 + 16 c (high nibble).  The decode kernel removes the offset and
 // the factor where they do not cancel by themselves (see load_q_frags and
-// the piece end).
-__device__ __forceinline__ uint32_t i4_lo(uint32_t w) { return (w & 0x000F000Fu) | 0x64006400u; }
-__device__ __forceinline__ uint32_t i4_hi(uint32_t w) { return (w & 0x00F000F0u) | 0x64006400u; }
+// the piece end).  The or-ed exponent bits come from constant memory, which
+// the three-input logic instruction takes as an operand beside the mask
+// immediate; written as a second immediate, the compiler put the constant
+// into a register before each use, one more instruction per code pair (the
+// 4-bit decode then issued a sixth more instructions and ran 14% slower).
+__constant__ uint32_t kF16Exp1024 = 0x64006400u;  // 1024.0 in both halves of an f16 pair
+__device__ __forceinline__ uint32_t i4_lo(uint32_t w) { return (w & 0x000F000Fu) | kF16Exp1024; }
+__device__ __forceinline__ uint32_t i4_hi(uint32_t w) { return (w & 0x00F000F0u) | kF16Exp1024; }
 
 // Byte `bi` of the packed words of two token rows a, b in half words 0 and 1
 // of the result (row a low): i4_lo / i4_hi of it give the byte's two codes
@@ -912,6 +919,12 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
     // ldmatrix lane roles: K (A operand, rows = tokens) and V (A = V^T via .trans)
     const int row_k = (lane & 7) + ((lane >> 3) & 1) * 8, half_k = lane >> 4;
     const int row_v = (lane & 7) + (lane >> 4) * 8, half_v = (lane >> 3) & 1;
+    // 4-bit tiles: the thread's swizzled byte offsets in a K tile (row g8) and a V tile (row 2c).
+    // The box swizzle XORs bits 4-5 (64-byte rows) or bit 4 (32-byte rows) with bits of the row
+    // index that rows g8 and g8 + 8, and rows 2c, 2c + 1, 2c + 8, 2c + 9, share, so the thread's
+    // other rows sit at whole-row distances from these and need no swizzle of their own.
+    [[maybe_unused]] const uint32_t k_off = swz<Gm::BOXB>(g8 * Gm::ROWB + 4 * (D / 32) * c4);
+    [[maybe_unused]] const uint32_t v_off = Gm::TILE + swz<Gm::BOXB>(2 * c4 * Gm::ROWB + 4 * (D / 64) * g8);
 
     Piece pc;
     bool have = first_piece(st, me, pc);
@@ -1201,13 +1214,12 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                 float sa1[4] = {0.f, 0.f, 0.f, 0.f}, sb1[4] = {0.f, 0.f, 0.f, 0.f};
                 // the thread's packed key words two at a time (8 bytes of each of its two token rows
                 // per block), so that only eight of them are live at once
+                const uint32_t ka0 = kb0 + k_off, ka1 = kb1 + k_off;
 #pragma unroll
                 for (int hh = 0; hh < WPT / 2; ++hh) {
-                    auto kpair = [&](uint32_t kb, int row) {
-                        return lds64(kb + swz<Gm::BOXB>(row * Gm::ROWB + 4 * WPT * c4) + 8 * hh);
-                    };
-                    const uint2 kx0 = kpair(kb0, g8), ky0 = kpair(kb0, g8 + 8);
-                    const uint2 kx1 = kpair(kb1, g8), ky1 = kpair(kb1, g8 + 8);
+                    // rows g8 and g8 + 8 of each block, 8 bytes at a time
+                    const uint2 kx0 = lds64(ka0 + 8 * hh), ky0 = lds64(ka0 + 8 * Gm::ROWB + 8 * hh);
+                    const uint2 kx1 = lds64(ka1 + 8 * hh), ky1 = lds64(ka1 + 8 * Gm::ROWB + 8 * hh);
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {
                         const int ks = 4 * hh + k4;
@@ -1266,10 +1278,10 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                 constexpr int WPR = D / 64;  // words per token row per thread (2 or 1)
                 // one packed value word of each of the thread's four token rows per block at a time
                 // (tiles 4 w .. 4 w + 3 use word w), so that only eight words are live at once
-                const int vrows[4] = {2 * c4, 2 * c4 + 1, 2 * c4 + 8, 2 * c4 + 9};
-                auto vword = [&](uint32_t vb, int q, int w) {
-                    return lds32(vb + swz<Gm::BOXB>(vrows[q] * Gm::ROWB + 4 * WPR * g8) + 4 * w);
-                };
+                // rows 2c, 2c + 1, 2c + 8, 2c + 9: row distances 0, 1, 8, 9 from row 2c
+                constexpr int kVRow[4] = {0, 1, 8, 9};
+                auto vword = [&](uint32_t va, int q, int w) { return lds32(va + kVRow[q] * Gm::ROWB + 4 * w); };
+                const uint32_t va0 = kb0 + v_off, va1 = kb1 + v_off;
                 auto tile2 = [&](auto tc, const uint32_t (&u)[4], const uint32_t (&v)[4]) {
                     constexpr int t = decltype(tc)::value;
                     const uint32_t za = i4_rows<t % 4>(u[0], u[1]), zb = i4_rows<t % 4>(u[2], u[3]);
@@ -1280,20 +1292,16 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                     mma16816<true>(o[t], fb, pb10, pb11);
                 };
                 {
-                    const uint32_t u[4] = {vword(kb0 + Gm::TILE, 0, 0), vword(kb0 + Gm::TILE, 1, 0),
-                                           vword(kb0 + Gm::TILE, 2, 0), vword(kb0 + Gm::TILE, 3, 0)};
-                    const uint32_t v[4] = {vword(kb1 + Gm::TILE, 0, 0), vword(kb1 + Gm::TILE, 1, 0),
-                                           vword(kb1 + Gm::TILE, 2, 0), vword(kb1 + Gm::TILE, 3, 0)};
+                    const uint32_t u[4] = {vword(va0, 0, 0), vword(va0, 1, 0), vword(va0, 2, 0), vword(va0, 3, 0)};
+                    const uint32_t v[4] = {vword(va1, 0, 0), vword(va1, 1, 0), vword(va1, 2, 0), vword(va1, 3, 0)};
                     tile2(std::integral_constant<int, 0>{}, u, v);
                     tile2(std::integral_constant<int, 1>{}, u, v);
                     tile2(std::integral_constant<int, 2>{}, u, v);
                     tile2(std::integral_constant<int, 3>{}, u, v);
                 }
                 if constexpr (NT == 8) {
-                    const uint32_t u[4] = {vword(kb0 + Gm::TILE, 0, 1), vword(kb0 + Gm::TILE, 1, 1),
-                                           vword(kb0 + Gm::TILE, 2, 1), vword(kb0 + Gm::TILE, 3, 1)};
-                    const uint32_t v[4] = {vword(kb1 + Gm::TILE, 0, 1), vword(kb1 + Gm::TILE, 1, 1),
-                                           vword(kb1 + Gm::TILE, 2, 1), vword(kb1 + Gm::TILE, 3, 1)};
+                    const uint32_t u[4] = {vword(va0, 0, 1), vword(va0, 1, 1), vword(va0, 2, 1), vword(va0, 3, 1)};
+                    const uint32_t v[4] = {vword(va1, 0, 1), vword(va1, 1, 1), vword(va1, 2, 1), vword(va1, 3, 1)};
                     tile2(std::integral_constant<int, 4>{}, u, v);
                     tile2(std::integral_constant<int, 5>{}, u, v);
                     tile2(std::integral_constant<int, 6>{}, u, v);
