@@ -48,7 +48,7 @@ class _Layout(ctypes.Structure):
                 ("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
                 ("n_kv", ctypes.c_int32), ("d_head", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("bytes_per_array", ctypes.c_int64), ("v_params", ctypes.c_void_p),
-                ("v_params_bytes", ctypes.c_int64)]
+                ("v_params_bytes", ctypes.c_int64), ("alloc_bytes", ctypes.c_int64)]
 
 
 class _Timing(ctypes.Structure):
@@ -240,17 +240,15 @@ class Pool:
                                                   kz.ctypes.data_as(ctypes.c_void_p)))
 
     def v_params_view(self):
-        """4-bit pools: the value rows' (scale, zero point), float32 [num_blocks, n_kv, block_size, 2]."""
+        """4-bit pools: the value rows' (scale, zero point), float32 [num_blocks, n_kv, block_size, 2]
+        (a strided view into the pool's entries)."""
         import torch
 
         lay = self.layout()
-        ptr, n = lay["v_params"], lay["v_params_bytes"]
-
-        class _Holder:
-            __cuda_array_interface__ = {"shape": (n // 4,), "typestr": "<f4", "data": (ptr, False),
-                                        "version": 3, "strides": None}
-
-        return torch.as_tensor(_Holder(), device="cuda").view(self.num_blocks, self.n_kv, self.block_size, 2)
+        flat = self._alloc_bytes_view(lay).view(torch.float32)
+        off = (lay["v_params"] - lay["k"]) // 4
+        return flat.as_strided((self.num_blocks, self.n_kv, self.block_size, 2),
+                               (lay["stride_block"] // 4, lay["stride_head"] // 4, 2, 1), off)
 
     def layout(self) -> dict:
         lay = _Layout()
@@ -292,19 +290,29 @@ class Pool:
     def v_view(self):
         return self._view("v")
 
-    def _view(self, which):
+    @staticmethod
+    def _bytes_view(ptr, n):
         import torch
-
-        lay = self.layout()
-        n = lay["bytes_per_array"]
-        ptr = lay[which]
 
         class _Holder:  # exposes the pool's memory through the CUDA array interface
             __cuda_array_interface__ = {"shape": (n,), "typestr": "|u1", "data": (ptr, False),
                                         "version": 3, "strides": None}
 
-        flat = torch.as_tensor(_Holder(), device="cuda")
-        return flat.view(self.num_blocks, self.n_kv, self.block_size, n // (self.num_blocks * self.n_kv * self.block_size))
+        return torch.as_tensor(_Holder(), device="cuda")
+
+    def _alloc_bytes_view(self, lay):
+        """The whole allocation the K pointer starts (4-bit pools: every entry), as uint8."""
+        return self._bytes_view(lay["k"], lay["alloc_bytes"])
+
+    def _view(self, which):
+        lay = self.layout()
+        elem = 2 if self.dtype == BF16 else 1
+        row = self.d_head // 2 if self.dtype == INT4 else self.d_head * elem
+        shape = (self.num_blocks, self.n_kv, self.block_size, row)
+        strides = (lay["stride_block"] * elem, lay["stride_head"] * elem, lay["stride_token"] * elem, 1)
+        if self.dtype == INT4:  # key and value codes inside the entries
+            return self._alloc_bytes_view(lay).as_strided(shape, strides, lay[which] - lay["k"])
+        return self._bytes_view(lay[which], lay["bytes_per_array"]).as_strided(shape, strides, 0)
 
 
 def kv_pool_create(num_blocks: int, block_size: int, n_kv: int, d_head: int, dtype: int = BF16) -> Pool:

@@ -25,7 +25,7 @@ struct AppendArgs {
     int64_t n_tokens;
     const float *scales;                  // [2*n_kv] (FP8 only)
     const float *k_params;                // 4-bit: [2][n_kv][D] key scales, then zero points
-    float *v_params;                      // 4-bit: [rows][2] value (scale, zero point)
+                                          // (4-bit: k_pool is the first (block, KV head) entry)
     // 4-bit step mode (when step_tables is set): token t is sequence t's newest
     // one, at position context_lens[t] - 1 of its dense table row
     const int32_t *step_tables, *step_lens;
@@ -104,7 +104,8 @@ __device__ __forceinline__ uint32_t int4_code(float x, float s, float z)
 // each value row gets scale (max - min) / 15 (1 if the row is constant) and
 // zero point min + 0 (no negative zero), found by reducing min and max over
 // the D/8 lanes of the row.  Eight codes per lane, packed two per byte with
-// the even channel in the low nibble: one 32-bit store per lane and array.
+// the even channel in the low nibble: one 32-bit store per lane and array,
+// into the (block, KV head) entry (key codes, value codes, value parameters).
 template <int D>
 __global__ void __launch_bounds__(256) append_int4_kernel(AppendArgs a)
 {
@@ -141,7 +142,8 @@ __global__ void __launch_bounds__(256) append_int4_kernel(AppendArgs a)
             continue;
         }
         const int64_t blk = slot / kBlockSize;
-        const int64_t r = (blk * a.n_kv + g) * kBlockSize + (slot - blk * kBlockSize);  // pool row
+        const int off = (int)(slot - blk * kBlockSize);  // row in the block
+        uint8_t *entry = a.k_pool + (blk * a.n_kv + g) * i4_entry_bytes(D);
         const int64_t src = (t * a.n_kv + g) * D + sub * 8;
         const uint4 kr = ldg_nc_v4(a.k_new + src);
         const uint4 vr = ldg_nc_v4(a.v_new + src);
@@ -176,9 +178,9 @@ __global__ void __launch_bounds__(256) append_int4_kernel(AppendArgs a)
         const float z = __fadd_rn(mn, 0.0f);
 #pragma unroll
         for (int i = 0; i < 8; ++i) vc |= int4_code(vf[i], sc, z) << (4 * i);
-        *reinterpret_cast<uint32_t *>(a.k_pool + r * (D / 2) + sub * 4) = kc;
-        *reinterpret_cast<uint32_t *>(a.v_pool + r * (D / 2) + sub * 4) = vc;
-        if (sub == 0) *reinterpret_cast<float2 *>(a.v_params + 2 * r) = make_float2(sc, z);
+        *reinterpret_cast<uint32_t *>(entry + off * (D / 2) + sub * 4) = kc;
+        *reinterpret_cast<uint32_t *>(entry + i4_v_offset(D) + off * (D / 2) + sub * 4) = vc;
+        if (sub == 0) *reinterpret_cast<float2 *>(entry + i4_params_offset(D) + off * 8) = make_float2(sc, z);
     }
 }
 
@@ -237,7 +239,6 @@ pkv_status append_step_int4(pkv_pool *pool, const void *k_new, const void *v_new
     a.n_tokens = batch;
     a.scales = pool->scales;
     a.k_params = pool->k_params;
-    a.v_params = pool->v_params;
     a.step_tables = tables;
     a.step_lens = lens;
     a.step_W = W;
@@ -282,7 +283,6 @@ extern "C" pkv_status paged_kv_append(pkv_pool *pool, const void *k_new, const v
     a.n_tokens = n_tokens;
     a.scales = pool->scales;
     a.k_params = pool->k_params;
-    a.v_params = pool->v_params;
     a.step_tables = a.step_lens = nullptr;
     a.step_W = 0;
     a.err = pool->err;

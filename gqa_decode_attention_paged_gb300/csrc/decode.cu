@@ -66,7 +66,7 @@ struct DecodeArgs {
     float qscale;          // scale * log2(e)
     const float *scales;   // FP8: [2 * n_kv] (k then v)
     const float *k_params; // 4-bit: [2][n_kv][D] key scales, then zero points
-    const float *v_params; // 4-bit: [num_blocks][n_kv][16][2] value (scale, zero point)
+    const uint8_t *i4_entries;  // 4-bit: the pool's [num_blocks][n_kv] (block, KV head) entries
     __nv_bfloat16 *out;
     float2 *ws_ml;         // workspace [slots][G] (max in log2 units, sum)
     float *ws_o;           // workspace [slots][G][D], unnormalised
@@ -86,10 +86,12 @@ struct DecodeArgs {
 // KV storage types the decode kernel is instantiated for (pkv_dtype values)
 constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvInt4 = 2;
 
-// Shared-memory geometry of one (block, KV head) tile as the TMA boxes lay it
-// out: NREG boxes of 16 rows x BOXB bytes (128-byte rows; 64 bytes for FP8
-// with d_head 64 and 4-bit codes with d_head 128; 32 bytes for 4-bit codes
-// with d_head 64), each box swizzled within its own region.
+// Shared-memory geometry of one (block, KV head) stage.  bf16 and FP8: the K
+// tile then the V tile as the TMA boxes lay them out, NREG boxes of 16 rows x
+// BOXB bytes (128-byte rows; 64 bytes for FP8 with d_head 64), each box
+// swizzled within its own region.  4-bit: the pool's entry as one bulk copy
+// lays it out, unswizzled: 16 key rows of d/2 code bytes, 16 value rows, then
+// the value rows' 16 (scale, zero point) pairs at PARAMS.
 template <int D, int KV>
 struct Geo {
     static constexpr bool FP8 = KV == kKvFp8, I4 = KV == kKvInt4;
@@ -99,7 +101,9 @@ struct Geo {
     static constexpr int NREG = ROWB / BOXB;              // boxes per tile
     static constexpr int RGN = kBlockSize * BOXB;         // bytes per box
     static constexpr int TILE = NREG * RGN;               // K tile (or V tile) bytes
-    static constexpr int STAGE = 2 * TILE;                // K tile + V tile
+    static constexpr int PARAMS = 2 * TILE;               // 4-bit: offset of the value parameters
+    static constexpr int STAGE = 2 * TILE + (I4 ? kBlockSize * 8 : 0);
+    static_assert(!I4 || STAGE == i4_entry_bytes(D), "a 4-bit stage holds exactly one pool entry");
     static constexpr int BOX_ELEMS = BOXB / E;
 };
 
@@ -117,12 +121,11 @@ struct Tune {
     // (3 CTAs = 12 warps per SM), FP8 d128 3 stages of 4 KiB (4 CTAs per SM).
     // Swept on GB300 over 2..8 warps and 32..128 KiB.
     static constexpr int NW = 4;
-    // 4-bit: 32 KiB, 4 stages of 2 KiB per warp at d_head 128 (two block
-    // pairs; a power of two, so a stage index is a mask); its three CTAs per
-    // SM are held by registers, not by shared memory.  Measured on GB300: 4
-    // stages 61.6 us per launch against 62.8 us with 8 (Llama3-8B shape,
-    // batch 128).
-    static constexpr int RING_KIB = KV == 2 ? 32 : 48;
+    // 4-bit: 36 KiB, 4 stages of 2176 bytes per warp at d_head 128 (two block
+    // pairs), 8 of 1152 at d_head 64; its three CTAs per SM are held by
+    // registers, not by shared memory.  Measured on GB300: 4 stages 61.6 us
+    // per launch against 62.8 us with 8 (Llama3-8B shape, batch 128).
+    static constexpr int RING_KIB = KV == 2 ? 36 : 48;
 #endif
 };
 
@@ -148,10 +151,8 @@ struct Cfg {
     static constexpr int kRing = NW * kStages * Gm::STAGE;
     static constexpr int kBars = kRing;
     static constexpr int kPhys = kBars + NW * kStages * 8;
-    // 4-bit KV: each stage's value (scale, zero point) pairs, [NW][kStages][16] float2
-    static constexpr int kVp = (kPhys + NW * kStages * 4 + 15) / 16 * 16;
-    static constexpr int kNewRow = kVp + (Gm::I4 ? NW * kStages * kBlockSize * 8 : 0);  // [NW][2 * D * 2] bytes:
-                                                                                          // fused step's new rows
+    static constexpr int kNewRow = (kPhys + NW * kStages * 4 + 15) / 16 * 16;  // [NW][2 * D * 2] bytes:
+                                                                                 // fused step's new rows
     static constexpr int kWarpTot = kNewRow + NW * 4 * D;
     // ps[batch + 1], then clamped lengths cl[batch], then table row starts rb[batch]
     static constexpr int kPs = kWarpTot + 4 * NW;
@@ -433,6 +434,15 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
     uint4 v;
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
     return v;
+}
+
+// Byte offset of (row, byte) offset `off` inside a stage's K or V tile: TMA
+// boxes are swizzled, a 4-bit entry's bulk copy is not.
+template <class Gm>
+__device__ __forceinline__ uint32_t tile_off(uint32_t off)
+{
+    if constexpr (Gm::I4) return off;
+    else return swz<Gm::BOXB>(off);
 }
 
 // 4-bit codes as f16 operands without a subtraction: a code c or-ed into
@@ -829,11 +839,12 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
     int *warp_tot = reinterpret_cast<int *>(smem + C::kWarpTot);
     int32_t *ps = reinterpret_cast<int32_t *>(smem + C::kPs);
     uint8_t *rowbuf = smem + C::kNewRow + warp * 4 * D;  // fused step: this warp's new K and V rows
-    float2 *vpbuf = reinterpret_cast<float2 *>(smem + C::kVp) + warp * S * kBlockSize;  // 4-bit: value (s, z)
 
     if (tid == 0) {
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
+        if constexpr (!I4) {  // 4-bit pools are read by bulk copies, not through these maps
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
         for (int i = 0; i < NW * S; ++i) mbar_init(reinterpret_cast<uint64_t *>(smem + C::kBars) + i, 1);
         fence_mbarrier_init();
     }
@@ -888,18 +899,23 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
             const bool ok = phys >= 0 && phys < a.num_blocks;
             phys_st[sidx] = ok ? phys : -1;
             if (ok) {
-                const int y = (int)(((int64_t)phys * a.n_kv + cur.p.g) * kBlockSize);
+                const int64_t unit = (int64_t)phys * a.n_kv + cur.p.g;  // (block, KV head)
                 uint8_t *dst = ring + sidx * Gm::STAGE;
                 fence_proxy_async_smem();
-                mbar_arrive_expect_tx(&bars[sidx], Gm::STAGE + (I4 ? kBlockSize * 8 : 0));
+                mbar_arrive_expect_tx(&bars[sidx], Gm::STAGE);
+                if constexpr (I4) {
+                    // the whole entry (key codes, value codes, value parameters) in one copy: one
+                    // request stream per block instead of three (measured: the three small copies
+                    // alone held the 4-bit stream to 72% of the copy peak)
+                    bulk_g2s(dst, a.i4_entries + unit * Gm::STAGE, Gm::STAGE, &bars[sidx], policy);
+                } else {
+                    const int y = (int)(unit * kBlockSize);
 #pragma unroll
-                for (int r = 0; r < Gm::NREG; ++r) {
-                    tma_load_2d(dst + r * Gm::RGN, &tm_k, r * Gm::BOX_ELEMS, y, &bars[sidx], policy);
-                    tma_load_2d(dst + Gm::TILE + r * Gm::RGN, &tm_v, r * Gm::BOX_ELEMS, y, &bars[sidx], policy);
+                    for (int r = 0; r < Gm::NREG; ++r) {
+                        tma_load_2d(dst + r * Gm::RGN, &tm_k, r * Gm::BOX_ELEMS, y, &bars[sidx], policy);
+                        tma_load_2d(dst + Gm::TILE + r * Gm::RGN, &tm_v, r * Gm::BOX_ELEMS, y, &bars[sidx], policy);
+                    }
                 }
-                if constexpr (I4)  // the block's value (scale, zero point) pairs: 128 contiguous bytes
-                    bulk_g2s(vpbuf + sidx * kBlockSize, a.v_params + (int64_t)y * 2, kBlockSize * 8, &bars[sidx],
-                             policy);
             } else {
                 atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
                 mbar_arrive(&bars[sidx]);
@@ -919,12 +935,10 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
     // ldmatrix lane roles: K (A operand, rows = tokens) and V (A = V^T via .trans)
     const int row_k = (lane & 7) + ((lane >> 3) & 1) * 8, half_k = lane >> 4;
     const int row_v = (lane & 7) + (lane >> 4) * 8, half_v = (lane >> 3) & 1;
-    // 4-bit tiles: the thread's swizzled byte offsets in a K tile (row g8) and a V tile (row 2c).
-    // The box swizzle XORs bits 4-5 (64-byte rows) or bit 4 (32-byte rows) with bits of the row
-    // index that rows g8 and g8 + 8, and rows 2c, 2c + 1, 2c + 8, 2c + 9, share, so the thread's
-    // other rows sit at whole-row distances from these and need no swizzle of their own.
-    [[maybe_unused]] const uint32_t k_off = swz<Gm::BOXB>(g8 * Gm::ROWB + 4 * (D / 32) * c4);
-    [[maybe_unused]] const uint32_t v_off = Gm::TILE + swz<Gm::BOXB>(2 * c4 * Gm::ROWB + 4 * (D / 64) * g8);
+    // 4-bit stages: the thread's byte offsets in the K tile (row g8) and the V tile (row 2c); its
+    // other rows (g8 + 8; 2c + 1, 2c + 8, 2c + 9) sit at whole-row distances from these
+    [[maybe_unused]] const uint32_t k_off = g8 * Gm::ROWB + 4 * (D / 32) * c4;
+    [[maybe_unused]] const uint32_t v_off = Gm::TILE + 2 * c4 * Gm::ROWB + 4 * (D / 64) * g8;
 
     Piece pc;
     bool have = first_piece(st, me, pc);
@@ -1026,13 +1040,13 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                     constexpr int WPT = D / 32;
                     uint32_t kx[WPT], ky[WPT];
                     if constexpr (WPT == 4) {
-                        const uint4 x = lds128(kb + swz<Gm::BOXB>(g8 * Gm::ROWB + 16 * c4));
-                        const uint4 y = lds128(kb + swz<Gm::BOXB>((g8 + 8) * Gm::ROWB + 16 * c4));
+                        const uint4 x = lds128(kb + tile_off<Gm>(g8 * Gm::ROWB + 16 * c4));
+                        const uint4 y = lds128(kb + tile_off<Gm>((g8 + 8) * Gm::ROWB + 16 * c4));
                         kx[0] = x.x; kx[1] = x.y; kx[2] = x.z; kx[3] = x.w;
                         ky[0] = y.x; ky[1] = y.y; ky[2] = y.z; ky[3] = y.w;
                     } else {
-                        const uint2 x = lds64(kb + swz<Gm::BOXB>(g8 * Gm::ROWB + 8 * c4));
-                        const uint2 y = lds64(kb + swz<Gm::BOXB>((g8 + 8) * Gm::ROWB + 8 * c4));
+                        const uint2 x = lds64(kb + tile_off<Gm>(g8 * Gm::ROWB + 8 * c4));
+                        const uint2 y = lds64(kb + tile_off<Gm>((g8 + 8) * Gm::ROWB + 8 * c4));
                         kx[0] = x.x; kx[1] = x.y;
                         ky[0] = y.x; ky[1] = y.y;
                     }
@@ -1083,8 +1097,9 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                 uint32_t pb0, pb1;  // P^T rows: tokens 2c, 2c+1 (pb0), 2c+8, 2c+9 (pb1) of head g
                 if constexpr (I4) {
                     // v = c * s + z per token: P V = (P * s) C + (P . z); masked tokens weigh 0
-                    const float2 vp0 = g8 < nv ? vpbuf[sidx * kBlockSize + g8] : make_float2(0.f, 0.f);
-                    const float2 vp1 = g8 + 8 < nv ? vpbuf[sidx * kBlockSize + g8 + 8] : make_float2(0.f, 0.f);
+                    const float2 *vps = reinterpret_cast<const float2 *>(ring + sidx * Gm::STAGE + Gm::PARAMS);
+                    const float2 vp0 = g8 < nv ? vps[g8] : make_float2(0.f, 0.f);
+                    const float2 vp1 = g8 + 8 < nv ? vps[g8 + 8] : make_float2(0.f, 0.f);
                     z0 = fmaf(z0, al0, fmaf(p0, vp0.y, p2 * vp1.y));
                     z1 = fmaf(z1, al1, fmaf(p1, vp0.y, p3 * vp1.y));
                     const uint32_t h0 = pack2<true>(p0 * vp0.x, p1 * vp0.x), h1 = pack2<true>(p2 * vp1.x, p3 * vp1.x);
@@ -1114,11 +1129,11 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         if constexpr (WPR == 2) {
-                            const uint2 v = lds64(vb + swz<Gm::BOXB>(rows[q] * Gm::ROWB + 8 * g8));
+                            const uint2 v = lds64(vb + tile_off<Gm>(rows[q] * Gm::ROWB + 8 * g8));
                             rr[q][0] = v.x;
                             rr[q][1] = v.y;
                         } else {
-                            rr[q][0] = lds32(vb + swz<Gm::BOXB>(rows[q] * Gm::ROWB + 4 * g8));
+                            rr[q][0] = lds32(vb + tile_off<Gm>(rows[q] * Gm::ROWB + 4 * g8));
                         }
                     }
                     // tile t: byte t of the thread's span, row g8 its low code (channel 2t of the span),
@@ -1257,10 +1272,12 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                 l1 = fmaf(l1, al1, (p[1] + p[3]) + (p[5] + p[7]));
                 // v = c * s + z per token: P V = (P * s) C + (P . z); masked tokens weigh 0
                 const float2 zero2 = make_float2(0.f, 0.f);
-                const float2 vp00 = g8 < nv0 ? vpbuf[s0i * kBlockSize + g8] : zero2;
-                const float2 vp01 = g8 + 8 < nv0 ? vpbuf[s0i * kBlockSize + g8 + 8] : zero2;
-                const float2 vp10 = g8 < nv1 ? vpbuf[s1i * kBlockSize + g8] : zero2;
-                const float2 vp11 = g8 + 8 < nv1 ? vpbuf[s1i * kBlockSize + g8 + 8] : zero2;
+                const float2 *vps0 = reinterpret_cast<const float2 *>(ring + s0i * Gm::STAGE + Gm::PARAMS);
+                const float2 *vps1 = reinterpret_cast<const float2 *>(ring + s1i * Gm::STAGE + Gm::PARAMS);
+                const float2 vp00 = g8 < nv0 ? vps0[g8] : zero2;
+                const float2 vp01 = g8 + 8 < nv0 ? vps0[g8 + 8] : zero2;
+                const float2 vp10 = g8 < nv1 ? vps1[g8] : zero2;
+                const float2 vp11 = g8 + 8 < nv1 ? vps1[g8 + 8] : zero2;
                 z0 = fmaf(z0, al0, fmaf(p[0], vp00.y, p[2] * vp01.y) + fmaf(p[4], vp10.y, p[6] * vp11.y));
                 z1 = fmaf(z1, al1, fmaf(p[1], vp00.y, p[3] * vp01.y) + fmaf(p[5], vp10.y, p[7] * vp11.y));
                 const uint32_t h00 = pack2<true>(p[0] * vp00.x, p[1] * vp00.x);
@@ -1656,7 +1673,7 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
     a.k_params = pool->k_params;
-    a.v_params = pool->v_params;
+    a.i4_entries = pool->dtype == PKV_INT4 ? static_cast<const uint8_t *>(pool->k) : nullptr;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
@@ -1714,7 +1731,7 @@ extern "C" pkv_status paged_decode_attention_csr(pkv_pool *pool, const void *q, 
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
     a.k_params = pool->k_params;
-    a.v_params = pool->v_params;
+    a.i4_entries = pool->dtype == PKV_INT4 ? static_cast<const uint8_t *>(pool->k) : nullptr;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
@@ -1807,7 +1824,7 @@ static pkv_status step_device(pkv_pool *pool, const void *q, const void *k_new, 
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
     a.k_params = pool->k_params;
-    a.v_params = pool->v_params;
+    a.i4_entries = pool->dtype == PKV_INT4 ? static_cast<const uint8_t *>(pool->k) : nullptr;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
@@ -2122,7 +2139,7 @@ extern "C" pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
     a.k_params = pool->k_params;
-    a.v_params = pool->v_params;
+    a.i4_entries = pool->dtype == PKV_INT4 ? static_cast<const uint8_t *>(pool->k) : nullptr;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.ws_ml = nullptr;
     a.ws_o = nullptr;
@@ -2270,7 +2287,7 @@ extern "C" pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void 
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
     a.k_params = pool->k_params;
-    a.v_params = pool->v_params;
+    a.i4_entries = pool->dtype == PKV_INT4 ? static_cast<const uint8_t *>(pool->k) : nullptr;
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.ws_ml = nullptr;
     a.ws_o = nullptr;

@@ -22,6 +22,15 @@ constexpr int kBlockSize = 16;               // token slots per block
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded mbarrier waits: 2 s
 constexpr int kDefaultPartitionTokens = 0;  // 0: equal work per CTA
 
+// 4-bit pools keep everything one (block, KV head) needs in one contiguous
+// entry: its 16 key rows of d/2 code bytes, its 16 value rows of d/2 code
+// bytes, then its 16 value rows' fp32 (scale, zero point) pairs.  Entries are
+// [num_blocks][n_kv]; each is a multiple of 16 bytes, so the decode kernel
+// fetches one with a single bulk copy.
+constexpr int64_t i4_entry_bytes(int d_head) { return 16 * (int64_t)d_head + kBlockSize * 8; }
+constexpr int64_t i4_v_offset(int d_head) { return 8 * (int64_t)d_head; }       // value codes
+constexpr int64_t i4_params_offset(int d_head) { return 16 * (int64_t)d_head; }  // value (scale, zero)
+
 enum KernelKind { kAppend = 0, kDecode = 1, kMerge = 2, kPrefix = 3, kBlocks = 4, kNumKinds = 5 };
 
 struct EventPair {
@@ -54,15 +63,20 @@ struct pkv_pool {
     int num_sms = 0;
     int64_t num_blocks = 0;
     int block_size = 0, n_kv = 0, d_head = 0, dtype = 0;
-    void *k = nullptr, *v = nullptr;  // device, [num_blocks][n_kv][block_size][d_head]
-    size_t bytes_per_array = 0;
+    // device, [num_blocks][n_kv][block_size][d_head] each (bf16 and FP8 pools); 4-bit pools: one
+    // allocation of [num_blocks][n_kv] entries (i4_entry_bytes), k, v and v_params pointing at the
+    // first entry's key codes, value codes and value parameters
+    void *k = nullptr, *v = nullptr;
+    size_t bytes_per_array = 0;       // bytes of K (and of V) data; 4-bit pools: code bytes of each
+    size_t alloc_bytes = 0;           // bytes of the allocation k points into
     float *scales = nullptr;          // device [2 * n_kv]: k scales then v scales
-    // 4-bit pools: per value row (scale, zero point) [num_blocks][n_kv][block_size][2] fp32,
-    // and the keys' per-channel parameters [2][n_kv][d_head] fp32 (scales, then zero points)
+    // 4-bit pools: each value row's (scale, zero point), inside the entries, and the keys'
+    // per-channel parameters [2][n_kv][d_head] fp32 (scales, then zero points)
     float *v_params = nullptr;
     float *k_params = nullptr;
     // TMA descriptors of the K and V arrays viewed as 2-D [rows = blocks*n_kv*16][d_head],
-    // boxes of 16 rows x min(row bytes, 128) bytes, swizzled (128 B, or 64 B for 64-byte rows).
+    // boxes of 16 rows x min(row bytes, 128) bytes, swizzled (128 B, or 64 B for 64-byte rows);
+    // bf16 and FP8 pools only (4-bit entries are fetched by bulk copies).
     CUtensorMap tm_k, tm_v;
     bool scales_set = false;
     unsigned *err = nullptr;          // device sticky error word

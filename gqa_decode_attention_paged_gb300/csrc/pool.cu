@@ -263,20 +263,29 @@ pkv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv, 
     p->dtype = dtype;
     p->bytes_per_array = per_block * (size_t)num_blocks;
     const char *what = "cudaMalloc(K pool)";
-    e = cudaMalloc(&p->k, p->bytes_per_array);
-    if (e == cudaSuccess) { what = "cudaMalloc(V pool)"; e = cudaMalloc(&p->v, p->bytes_per_array); }
+    if (dtype == PKV_INT4) {
+        // one allocation of (block, KV head) entries: key codes, value codes, value parameters
+        p->alloc_bytes = (size_t)num_blocks * n_kv * (size_t)i4_entry_bytes(d_head);
+        what = "cudaMalloc(4-bit pool)";
+        e = cudaMalloc(&p->k, p->alloc_bytes);
+        if (e == cudaSuccess) {
+            p->v = static_cast<uint8_t *>(p->k) + i4_v_offset(d_head);
+            p->v_params = reinterpret_cast<float *>(static_cast<uint8_t *>(p->k) + i4_params_offset(d_head));
+        }
+    } else {
+        p->alloc_bytes = p->bytes_per_array;
+        e = cudaMalloc(&p->k, p->bytes_per_array);
+        if (e == cudaSuccess) { what = "cudaMalloc(V pool)"; e = cudaMalloc(&p->v, p->bytes_per_array); }
+    }
     if (e == cudaSuccess) { what = "cudaMalloc(scales)"; e = cudaMalloc(&p->scales, sizeof(float) * 2 * n_kv); }
     if (e == cudaSuccess) { what = "cudaMalloc(error word)"; e = cudaMalloc(&p->err, sizeof(unsigned)); }
-    const size_t vp_bytes = (size_t)num_blocks * n_kv * block_size * 2 * sizeof(float);
     if (e == cudaSuccess && dtype == PKV_INT4) {
-        what = "cudaMalloc(value params)";
-        e = cudaMalloc(&p->v_params, vp_bytes);
-        if (e == cudaSuccess) e = cudaMemset(p->v_params, 0, vp_bytes);
-        if (e == cudaSuccess) { what = "cudaMalloc(key params)"; e = cudaMalloc(&p->k_params, sizeof(float) * 2 * n_kv * d_head); }
+        what = "cudaMalloc(key params)";
+        e = cudaMalloc(&p->k_params, sizeof(float) * 2 * n_kv * d_head);
         if (e == cudaSuccess) e = cudaMemset(p->k_params, 0, sizeof(float) * 2 * n_kv * d_head);
     }
-    if (e == cudaSuccess) { what = "cudaMemset"; e = cudaMemset(p->k, 0, p->bytes_per_array); }
-    if (e == cudaSuccess) e = cudaMemset(p->v, 0, p->bytes_per_array);
+    if (e == cudaSuccess) { what = "cudaMemset"; e = cudaMemset(p->k, 0, p->alloc_bytes); }
+    if (e == cudaSuccess && dtype != PKV_INT4) e = cudaMemset(p->v, 0, p->bytes_per_array);
     if (e == cudaSuccess) e = cudaMemset(p->scales, 0, sizeof(float) * 2 * n_kv);
     if (e == cudaSuccess) e = cudaMemset(p->err, 0, sizeof(unsigned));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -285,7 +294,7 @@ pkv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv, 
         kv_pool_destroy(p);
         return s;
     }
-    st = make_tensor_maps(p);
+    st = dtype == PKV_INT4 ? PKV_OK : make_tensor_maps(p);
     if (st != PKV_OK) {
         kv_pool_destroy(p);
         return st;
@@ -299,9 +308,8 @@ pkv_status kv_pool_destroy(pkv_pool *pool)
     if (!pool) return PKV_OK;
     cudaDeviceSynchronize();
     cudaFree(pool->k);
-    cudaFree(pool->v);
+    if (pool->dtype != PKV_INT4) cudaFree(pool->v);  // 4-bit pools: v and v_params point into k's allocation
     cudaFree(pool->scales);
-    cudaFree(pool->v_params);
     cudaFree(pool->k_params);
     cudaFree(pool->err);
     cudaFree(pool->ws);
@@ -363,8 +371,10 @@ pkv_status kv_pool_layout(const pkv_pool *pool, pkv_layout *out)
     out->v_params = pool->v_params;
     out->v_params_bytes = pool->v_params ? (int64_t)pool->num_blocks * pool->n_kv * pool->block_size * 8 : 0;
     out->stride_token = pool->dtype == PKV_INT4 ? pool->d_head / 2 : pool->d_head;
-    out->stride_head = (int64_t)pool->block_size * out->stride_token;
+    out->stride_head = pool->dtype == PKV_INT4 ? i4_entry_bytes(pool->d_head)
+                                               : (int64_t)pool->block_size * out->stride_token;
     out->stride_block = (int64_t)pool->n_kv * out->stride_head;
+    out->alloc_bytes = (int64_t)pool->alloc_bytes;
     out->num_blocks = pool->num_blocks;
     out->block_size = pool->block_size;
     out->n_kv = pool->n_kv;

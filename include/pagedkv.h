@@ -60,28 +60,35 @@ typedef enum {
 
 typedef struct pkv_pool pkv_pool; /* opaque; owns its device memory */
 
-/* Where a pool's blocks live.  K and V are two separate device arrays, each
- * laid out [num_blocks][n_kv][block_size][d_head]: element (blk, g, off, d)
- * of either array sits at blk*stride_block + g*stride_head + off*stride_token
- * + d (strides in elements), so one (block, KV head) tile is contiguous.
- * PKV_INT4 pools store packed codes instead: an "element" is one byte
- * holding channels 2i (low nibble) and 2i+1 (high nibble), the row has
- * d_head / 2 of them, and v_params holds each value row's fp32 (scale, zero
- * point) pair, [num_blocks][n_kv][block_size][2]. */
+/* Where a pool's blocks live.  bf16 and FP8 pools: K and V are two separate
+ * device arrays, each laid out [num_blocks][n_kv][block_size][d_head]:
+ * element (blk, g, off, d) of either array sits at blk*stride_block +
+ * g*stride_head + off*stride_token + d (strides in elements), so one (block,
+ * KV head) tile is contiguous.
+ * PKV_INT4 pools store packed codes: an "element" is one byte holding
+ * channels 2i (low nibble) and 2i+1 (high nibble), a row has d_head / 2 of
+ * them.  Everything one (block, KV head) needs is one contiguous entry of
+ * stride_head = 16 * d_head + 128 bytes: its 16 key rows, its 16 value rows,
+ * then its 16 value rows' fp32 (scale, zero point) pairs; entries are
+ * [num_blocks][n_kv] in one allocation of alloc_bytes starting at k.  The
+ * same element formula holds for k and v (v = k + 8 * d_head), and value row
+ * (blk, g, off)'s pair sits at v_params + blk*stride_block + g*stride_head +
+ * 8*off bytes. */
 typedef struct {
     void *k;                 /* device */
     void *v;                 /* device */
-    int64_t stride_block;    /* n_kv * block_size * d_head */
-    int64_t stride_head;     /* block_size * d_head */
-    int64_t stride_token;    /* d_head */
+    int64_t stride_block;    /* n_kv * stride_head */
+    int64_t stride_head;     /* block_size * d_head (PKV_INT4: 16 * d_head + 128) */
+    int64_t stride_token;    /* d_head (PKV_INT4: d_head / 2) */
     int64_t num_blocks;
     int32_t block_size;
     int32_t n_kv;
     int32_t d_head;
     int32_t dtype;           /* pkv_dtype */
-    int64_t bytes_per_array; /* bytes of K (and, equally, of V) */
+    int64_t bytes_per_array; /* bytes of K (and, equally, of V) data */
     void *v_params;          /* device; PKV_INT4 only (NULL otherwise) */
-    int64_t v_params_bytes;
+    int64_t v_params_bytes;  /* bytes of value parameters in the pool (8 per token row) */
+    int64_t alloc_bytes;     /* bytes of the allocation k points into (PKV_INT4: the whole pool) */
 } pkv_layout;
 
 /* Per-kernel timing gathered with CUDA events while timing is enabled. */

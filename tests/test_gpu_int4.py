@@ -97,6 +97,11 @@ def test_int4_needs_key_params():
     lay = pool.layout()
     assert lay["stride_token"] == w.d_head // 2 and lay["bytes_per_array"] == w.num_blocks * w.n_kv * 16 * w.d_head // 2
     assert lay["v_params_bytes"] == w.num_blocks * w.n_kv * 16 * 8
+    # one contiguous (block, KV head) entry: key codes, value codes, value parameters
+    entry = 16 * w.d_head + 128
+    assert lay["stride_head"] == entry and lay["stride_block"] == w.n_kv * entry
+    assert lay["alloc_bytes"] == w.num_blocks * w.n_kv * entry
+    assert lay["v"] - lay["k"] == 8 * w.d_head and lay["v_params"] - lay["k"] == 16 * w.d_head
     pool.close()
 
 
