@@ -21,28 +21,33 @@
 //   * Warps are independent: after the prologue there is no CTA barrier.  A
 //     warp's slice meets one or more (sequence, head) runs; each meeting is a
 //     "piece".  The warp owns a ring of shared-memory stages that its lane 0
-//     fills with tiled TMA copies (cp.async.bulk.tensor, 128-byte swizzle,
-//     evict-first) of a block's K and V tiles, completing on an mbarrier;
-//     block-table entries are fetched a segment ahead with one coalesced
-//     load.  Every wait is bounded.
+//     fills with tiled TMA copies (cp.async.bulk.tensor, swizzled,
+//     evict-first) of a block's K and V tiles, completing on an mbarrier (a
+//     4-bit pool's (block, head) entry of key codes, value codes and value
+//     parameters arrives as one bulk copy); block-table entries are fetched a
+//     segment ahead with one coalesced load.  Every wait is bounded.
 //   * All G query heads of the group are served from one read of each tile
 //     ("Memory Management in LLM Serving Systems", FlashAttention: query
 //     heads sharing a KV head cut KV reads by the group factor): they are the
 //     N dimension of 16x8x16 tensor-core MMAs, S^T = K Q^T then O^T += V^T P^T.
 //   * Online softmax in fp32 with exp2 (scores pre-scaled by scale*log2 e):
-//     running max and sum per head, the accumulator rescaled only when the max
-//     moves, 1/l applied once at the end (Problem 5's recurrence;
+//     per head a reference maximum and a running sum; weights are taken
+//     against the reference, which is raised (and the sum and accumulator
+//     rescaled) only when a score passes it by more than a small slack, and
+//     1/l is applied once at the end (Problem 5's recurrence;
 //     FlashAttention-2's deferred normalisation).
 //   * Piece end: a piece that is its whole (sequence, head) writes bf16 `out`.
-//     Otherwise it stores (m, l, O) in the workspace and bumps that
-//     (sequence, head)'s counter; the warp that completes the count merges
-//     all pieces, in slice order, by log-sum-exp, M = max m_p,
-//     L = sum 2^(m_p-M) l_p, out = sum 2^(m_p-M) O_p / L, and resets the
-//     counter.  No warp ever waits for another, and the result does not
-//     depend on which warp finished last.
+//     Otherwise it stores (m, l, O) in the workspace, and merge_kernel,
+//     launched right behind as a programmatic dependent, combines each
+//     (sequence, head)'s pieces in slice order by log-sum-exp: M = max m_p,
+//     L = sum 2^(m_p-M) l_p, out = sum 2^(m_p-M) O_p / L.  No warp waits for
+//     another, and the result does not depend on which warp finished first.
 //   * FP8 KV: tiles are E4M3, converted to f16 pairs in registers for f16
 //     MMAs; the K scale is folded into the score scale and the V scale into
 //     the final normalisation.
+//   * 4-bit KV: codes enter f16 MMAs as 1024 + c (see i4_lo), the keys'
+//     per-channel scales are folded into q, and each value row's scale and
+//     zero point into P and a per-head correction at the piece end.
 #include <algorithm>
 #include <type_traits>
 #include <mutex>
