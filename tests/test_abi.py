@@ -112,3 +112,31 @@ def test_product_and_oracle_share_no_code():
                                  flags=re.M), f
             assert not re.search(r"#\s*include\s*[<\"]pagedkv\.h", txt), f
             assert "libpagedkv" not in txt, f
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    """The binding's ctypes mirrors of pkv_layout and pkv_timing have the
+    header's size and field offsets (a C program built from the header
+    prints them)."""
+    import shutil
+    import subprocess
+
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not found")
+    structs = {"pkv_layout": pkv._Layout, "pkv_timing": pkv._Timing}
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "pagedkv.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = {tuple(line.split()[:2]): int(line.split()[2]) for line in out if line}
+    for cname, py in structs.items():
+        assert got[(cname, "size")] == ctypes.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert got[(cname, f)] == getattr(py, f).offset, (cname, f)
