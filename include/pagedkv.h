@@ -403,7 +403,9 @@ pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void *q, int32_t
  * preempted sequence's blocks may be swapped to CPU memory; "Memory
  * Management in LLM Serving Systems", "Eviction: recompute or offload?").
  * A block is block_bytes of K plus block_bytes of V: all n_kv heads' 16
- * token rows, contiguous in each array.
+ * token rows (contiguous in each array for bf16 and FP8 pools; a 4-bit
+ * pool's block is its n_kv contiguous entries, key codes, value codes and
+ * value parameters per head, see pkv_layout).
  * --------------------------------------------------------------------- */
 
 /* Bytes of one block in one array (K or V): n_kv x 16 x d_head x (2 bf16,
