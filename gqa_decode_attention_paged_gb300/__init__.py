@@ -284,7 +284,7 @@ class Pool:
         return {f: getattr(t, f) for f, _ in _Timing._fields_}
 
     def k_view(self):
-        """The K pool as a torch uint8 tensor view [num_blocks, n_kv, block_size, d_head * elem]."""
+        """The key rows as a torch uint8 tensor view [num_blocks, n_kv, block_size, row bytes]."""
         return self._view("k")
 
     def v_view(self):
@@ -301,18 +301,17 @@ class Pool:
         return torch.as_tensor(_Holder(), device="cuda")
 
     def _alloc_bytes_view(self, lay):
-        """The whole allocation the K pointer starts (4-bit pools: every entry), as uint8."""
+        """The pool's whole allocation (every (block, KV head) entry), as uint8."""
         return self._bytes_view(lay["k"], lay["alloc_bytes"])
 
     def _view(self, which):
+        """Key or value rows inside the entries, as a strided uint8 view."""
         lay = self.layout()
         elem = 2 if self.dtype == BF16 else 1
         row = self.d_head // 2 if self.dtype == INT4 else self.d_head * elem
         shape = (self.num_blocks, self.n_kv, self.block_size, row)
         strides = (lay["stride_block"] * elem, lay["stride_head"] * elem, lay["stride_token"] * elem, 1)
-        if self.dtype == INT4:  # key and value codes inside the entries
-            return self._alloc_bytes_view(lay).as_strided(shape, strides, lay[which] - lay["k"])
-        return self._bytes_view(lay[which], lay["bytes_per_array"]).as_strided(shape, strides, 0)
+        return self._alloc_bytes_view(lay).as_strided(shape, strides, lay[which] - lay["k"])
 
 
 def kv_pool_create(num_blocks: int, block_size: int, n_kv: int, d_head: int, dtype: int = BF16) -> Pool:

@@ -17,7 +17,7 @@
 namespace pkv {
 
 struct AppendArgs {
-    uint8_t *k_pool, *v_pool;
+    uint8_t *k_pool;                      // the pool's first (block, KV head) entry
     int64_t num_blocks;
     int n_kv;
     const __nv_bfloat16 *k_new, *v_new;  // [T][n_kv][D]
@@ -25,7 +25,6 @@ struct AppendArgs {
     int64_t n_tokens;
     const float *scales;                  // [2*n_kv] (FP8 only)
     const float *k_params;                // 4-bit: [2][n_kv][D] key scales, then zero points
-                                          // (4-bit: k_pool is the first (block, KV head) entry)
     // 4-bit step mode (when step_tables is set): token t is sequence t's newest
     // one, at position context_lens[t] - 1 of its dense table row
     const int32_t *step_tables, *step_lens;
@@ -56,13 +55,15 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a)
         }
         const int64_t blk = slot / kBlockSize;
         const int64_t off = slot - blk * kBlockSize;
-        const int64_t dst = (((blk * a.n_kv + g) * kBlockSize + off) * D + sub * 8) * E;
+        // key row `off` of the (block, KV head) entry; its value row 16 rows further
+        const int64_t dst = ((blk * a.n_kv + g) * 2 * kBlockSize + off) * (D * E) + sub * 8 * E;
+        const int64_t vdst = dst + kBlockSize * D * E;
         const int64_t src = (t * a.n_kv + g) * D + sub * 8;
         const uint4 kr = ldg_nc_v4(a.k_new + src);
         const uint4 vr = ldg_nc_v4(a.v_new + src);
         if constexpr (!FP8) {
             *reinterpret_cast<uint4 *>(a.k_pool + dst) = kr;
-            *reinterpret_cast<uint4 *>(a.v_pool + dst) = vr;
+            *reinterpret_cast<uint4 *>(a.k_pool + vdst) = vr;
         } else {
             const float ks = a.scales[g];
             const float vs = a.scales[a.n_kv + g];
@@ -87,7 +88,7 @@ __global__ void __launch_bounds__(256) append_kernel(AppendArgs a)
                 }
             }
             *reinterpret_cast<uint2 *>(a.k_pool + dst) = make_uint2(ko[0], ko[1]);
-            *reinterpret_cast<uint2 *>(a.v_pool + dst) = make_uint2(vo[0], vo[1]);
+            *reinterpret_cast<uint2 *>(a.k_pool + vdst) = make_uint2(vo[0], vo[1]);
         }
     }
 }
@@ -230,7 +231,6 @@ pkv_status append_step_int4(pkv_pool *pool, const void *k_new, const void *v_new
 {
     AppendArgs a;
     a.k_pool = static_cast<uint8_t *>(pool->k);
-    a.v_pool = static_cast<uint8_t *>(pool->v);
     a.num_blocks = pool->num_blocks;
     a.n_kv = pool->n_kv;
     a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
@@ -274,7 +274,6 @@ extern "C" pkv_status paged_kv_append(pkv_pool *pool, const void *k_new, const v
         return fail(PKV_EINVAL, "paged_kv_append: 4-bit pool needs kv_pool_set_int4_key_params first");
     AppendArgs a;
     a.k_pool = static_cast<uint8_t *>(pool->k);
-    a.v_pool = static_cast<uint8_t *>(pool->v);
     a.num_blocks = pool->num_blocks;
     a.n_kv = pool->n_kv;
     a.k_new = static_cast<const __nv_bfloat16 *>(k_new);

@@ -5,12 +5,11 @@
 // blocks can be swapped to CPU memory), plus the host-side refcounted block
 // allocator that decides which blocks those are.
 //
-// A block of a bf16 or FP8 pool is one contiguous byte range in the K array
-// and one in the V array ([num_blocks][n_kv][16][row bytes] each), block_bytes
-// long.  A 4-bit pool's block is n_kv contiguous (block, KV head) entries of
-// key codes, value codes and value (scale, zero point) pairs.  A block's entry
-// in a host swap buffer is [K bytes][V bytes][value parameters] whatever the
-// pool: key codes of every head, then value codes, then parameters.  Every
+// A block of the pool is n_kv contiguous (block, KV head) entries of 16 key
+// rows and 16 value rows (and for a 4-bit pool 16 value (scale, zero point)
+// pairs).  A block's entry in a host swap buffer is [K bytes][V bytes][value
+// parameters, 4-bit pools only]: the key rows of every head, then the value
+// rows, then the parameters (block_bytes, block_bytes and param_bytes).  Every
 // kernel here moves whole entries in 16-byte vectors, grid-stride over
 // (block, 16-byte chunk of the entry): a pure copy, bound by HBM for device
 // copies and by the CPU-GPU link for swaps.  Swaps read and write pinned host memory
@@ -27,18 +26,18 @@
 namespace pkv {
 
 struct BlockMoveArgs {
-    uint8_t *k, *v;                // device pool arrays K, V (4-bit pools: k is the first entry)
+    uint8_t *pool;                 // the pool's first (block, KV head) entry
     const int32_t *src_ids, *dst_ids;  // block ids per pair (copy: both; swap-out: src; swap-in: dst)
     uint8_t *host;                 // swap buffer [n][entry bytes] (device address of pinned memory)
-    int64_t n, num_blocks, block_bytes, param_bytes;  // entry bytes = 2 block_bytes + param_bytes
-    int64_t i4_entry;              // 4-bit pools: bytes of a (block, KV head) entry; 0 otherwise
-    int64_t i4_codes;              // 4-bit pools: code bytes of one head's 16 rows (keys or values)
+    int64_t n, num_blocks, block_bytes, param_bytes;  // image entry bytes = 2 block_bytes + param_bytes
+    int64_t head_entry;            // bytes of a (block, KV head) entry in the pool
+    int64_t head_rows;             // bytes of one head's 16 key (or value) rows
     int n_kv;
     unsigned *err;
 };
 
-// Byte `off` of a block's entry: its array and the offset of that byte from
-// block id 0 of the array is base + id * stride.
+// Byte `off` of a block's swap-image entry: where it sits in the pool is
+// base + id * stride + off for block id.
 struct EntryByte {
     uint8_t *base;
     int64_t stride, off;
@@ -46,21 +45,18 @@ struct EntryByte {
 
 __device__ __forceinline__ EntryByte entry_byte(const BlockMoveArgs &a, int64_t off)
 {
-    if (a.i4_entry) {  // the head's entry, and the section within it (16-byte chunks never straddle heads)
-        int64_t sec = 0, per = a.i4_codes;
-        if (off >= 2 * a.block_bytes) {
-            off -= 2 * a.block_bytes;
-            sec = 2 * a.i4_codes;
-            per = kBlockSize * 8;
-        } else if (off >= a.block_bytes) {
-            off -= a.block_bytes;
-            sec = a.i4_codes;
-        }
-        const int64_t g = off / per;
-        return {a.k, a.n_kv * a.i4_entry, g * a.i4_entry + sec + (off - g * per)};
+    // the head's entry, and the section within it (16-byte chunks never straddle heads)
+    int64_t sec = 0, per = a.head_rows;
+    if (off >= 2 * a.block_bytes) {  // 4-bit value parameters
+        off -= 2 * a.block_bytes;
+        sec = 2 * a.head_rows;
+        per = kBlockSize * 8;
+    } else if (off >= a.block_bytes) {  // value rows
+        off -= a.block_bytes;
+        sec = a.head_rows;
     }
-    if (off < a.block_bytes) return {a.k, a.block_bytes, off};
-    return {a.v, a.block_bytes, off - a.block_bytes};
+    const int64_t g = off / per;
+    return {a.pool, a.n_kv * a.head_entry, g * a.head_entry + sec + (off - g * per)};
 }
 
 enum MoveKind { kCopy = 0, kSwapOut = 1, kSwapIn = 2 };
@@ -131,14 +127,13 @@ static int64_t param_bytes_of(const pkv_pool *pool)
 static BlockMoveArgs move_args(pkv_pool *pool, int64_t n)
 {
     BlockMoveArgs a = {};
-    a.k = static_cast<uint8_t *>(pool->k);
-    a.v = static_cast<uint8_t *>(pool->v);
+    a.pool = static_cast<uint8_t *>(pool->k);
     a.n = n;
     a.num_blocks = pool->num_blocks;
     a.block_bytes = block_bytes_of(pool);
     a.param_bytes = param_bytes_of(pool);
-    a.i4_entry = pool->dtype == PKV_INT4 ? i4_entry_bytes(pool->d_head) : 0;
-    a.i4_codes = (int64_t)kBlockSize * pool->d_head / 2;
+    a.head_entry = kv_entry_bytes(pool->dtype, pool->d_head);
+    a.head_rows = kv_v_offset(pool->dtype, pool->d_head);
     a.n_kv = pool->n_kv;
     a.err = pool->err;
     return a;

@@ -80,7 +80,7 @@ struct DecodeArgs {
     // fused step only: the token at position context_len-1 of each sequence,
     // [batch][n_kv][D] bf16, and the pool arrays it is appended to
     const __nv_bfloat16 *k_new, *v_new;
-    uint8_t *k_pool, *v_pool;
+    uint8_t *k_pool;  // the pool's first (block, KV head) entry
     // cascade decode only: the first skip_blocks table entries of every
     // sequence are a shared prefix whose attention comes from n_pre chunk
     // partials (see MergeArgs); the kernel covers the blocks after it
@@ -91,12 +91,14 @@ struct DecodeArgs {
 // KV storage types the decode kernel is instantiated for (pkv_dtype values)
 constexpr int kKvBf16 = 0, kKvFp8 = 1, kKvInt4 = 2;
 
-// Shared-memory geometry of one (block, KV head) stage.  bf16 and FP8: the K
-// tile then the V tile as the TMA boxes lay them out, NREG boxes of 16 rows x
-// BOXB bytes (128-byte rows; 64 bytes for FP8 with d_head 64), each box
-// swizzled within its own region.  4-bit: the pool's entry as one bulk copy
-// lays it out, unswizzled: 16 key rows of d/2 code bytes, 16 value rows, then
-// the value rows' 16 (scale, zero point) pairs at PARAMS.
+// Shared-memory geometry of one (block, KV head) stage.  bf16 and FP8: the
+// pool entry's 32 rows (16 key rows, then 16 value rows) as NREG TMA boxes of
+// 32 rows x BOXB bytes lay them out, one box per BOXB-byte column range
+// (128-byte boxes; 64 bytes for FP8 with d_head 64), each swizzled within its
+// own region: column range r's key rows at r x CSTRIDE, its value rows RGN
+// after them.  4-bit: the pool's entry as one bulk copy lays it out,
+// unswizzled: 16 key rows of d/2 code bytes, 16 value rows, then the value
+// rows' 16 (scale, zero point) pairs at PARAMS.
 template <int D, int KV>
 struct Geo {
     static constexpr bool FP8 = KV == kKvFp8, I4 = KV == kKvInt4;
@@ -106,6 +108,8 @@ struct Geo {
     static constexpr int NREG = ROWB / BOXB;              // boxes per tile
     static constexpr int RGN = kBlockSize * BOXB;         // bytes per box
     static constexpr int TILE = NREG * RGN;               // K tile (or V tile) bytes
+    static constexpr int CSTRIDE = 2 * RGN;               // between column ranges (key then value rows)
+    static constexpr int VOFF = RGN;                      // value rows after their column range's key rows
     static constexpr int PARAMS = 2 * TILE;               // 4-bit: offset of the value parameters
     static constexpr int STAGE = 2 * TILE + (I4 ? kBlockSize * 8 : 0);
     static_assert(!I4 || STAGE == i4_entry_bytes(D), "a 4-bit stage holds exactly one pool entry");
@@ -794,18 +798,18 @@ __device__ __forceinline__ void append_row(const DecodeArgs &a, int g, int phys,
     if (lane >= 2 * NCH) return;
     const bool isv = lane >= NCH;
     const int c = lane % NCH;
-    const int64_t row = ((int64_t)phys * a.n_kv + g) * kBlockSize + r;
-    uint8_t *tile = stage + (isv ? Gm::TILE : 0);
-    uint8_t *pool = isv ? a.v_pool : a.k_pool;
+    // pool row: key row r of the (block, KV head) entry, or its value row 16 rows further
+    const int64_t row = ((int64_t)phys * a.n_kv + g) * 2 * kBlockSize + (isv ? kBlockSize : 0) + r;
+    uint8_t *tile = stage + (isv ? Gm::VOFF : 0);
     if constexpr (!FP8) {
-        // chunk c is 16 bytes of the 256/128-byte row: box c / 8, 16-byte unit c % 8
-        const uint32_t off = (c >> 3) * Gm::RGN + swz<128>(r * 128 + (c & 7) * 16);
+        // chunk c is 16 bytes of the 256/128-byte row: column range c / 8, 16-byte unit c % 8
+        const uint32_t off = (c >> 3) * Gm::CSTRIDE + swz<128>(r * 128 + (c & 7) * 16);
         *reinterpret_cast<uint4 *>(tile + off) = prepared;
-        *reinterpret_cast<uint4 *>(pool + row * D * 2 + c * 16) = prepared;
+        *reinterpret_cast<uint4 *>(a.k_pool + row * D * 2 + c * 16) = prepared;
     } else {
         const uint2 q = make_uint2(prepared.x, prepared.y);
         *reinterpret_cast<uint2 *>(tile + swz<Gm::BOXB>(r * Gm::ROWB + c * 8)) = q;
-        *reinterpret_cast<uint2 *>(pool + row * D + c * 8) = q;
+        *reinterpret_cast<uint2 *>(a.k_pool + row * D + c * 8) = q;
     }
 }
 
@@ -823,7 +827,7 @@ __device__ __forceinline__ void append_row(const DecodeArgs &a, int g, int phys,
 // output is written, so the products are unchanged.
 template <int D, int G, int KV, bool APPEND = false>
 __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBlocks)
-    decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, DecodeArgs a)
+    decode_kernel(const __grid_constant__ CUtensorMap tm_kv, DecodeArgs a)
 {
     using C = Cfg<D, G, KV>;
     using Gm = typename C::Gm;
@@ -846,10 +850,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
     uint8_t *rowbuf = smem + C::kNewRow + warp * 4 * D;  // fused step: this warp's new K and V rows
 
     if (tid == 0) {
-        if constexpr (!I4) {  // 4-bit pools are read by bulk copies, not through these maps
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-        }
+        if constexpr (!I4) prefetch_tensormap(&tm_kv);  // 4-bit pools are read by bulk copies
         for (int i = 0; i < NW * S; ++i) mbar_init(reinterpret_cast<uint64_t *>(smem + C::kBars) + i, 1);
         fence_mbarrier_init();
     }
@@ -914,12 +915,11 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
                     // alone held the 4-bit stream to 72% of the copy peak)
                     bulk_g2s(dst, a.i4_entries + unit * Gm::STAGE, Gm::STAGE, &bars[sidx], policy);
                 } else {
-                    const int y = (int)(unit * kBlockSize);
+                    // the entry's 16 key and 16 value rows, one 32-row box per column range
+                    const int y = (int)(unit * 2 * kBlockSize);
 #pragma unroll
-                    for (int r = 0; r < Gm::NREG; ++r) {
-                        tma_load_2d(dst + r * Gm::RGN, &tm_k, r * Gm::BOX_ELEMS, y, &bars[sidx], policy);
-                        tma_load_2d(dst + Gm::TILE + r * Gm::RGN, &tm_v, r * Gm::BOX_ELEMS, y, &bars[sidx], policy);
-                    }
+                    for (int r = 0; r < Gm::NREG; ++r)
+                        tma_load_2d(dst + r * Gm::CSTRIDE, &tm_kv, r * Gm::BOX_ELEMS, y, &bars[sidx], policy);
                 }
             } else {
                 atomicOr(a.err, PKV_DEVERR_BLOCK_RANGE);
@@ -1031,7 +1031,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
             }
             if (!aborted && phys_st[sidx] >= 0) {
                 const uint32_t kb = smem_u32(ring + sidx * Gm::STAGE);
-                const uint32_t vb = kb + Gm::TILE;
+                const uint32_t vb = kb + (I4 ? Gm::TILE : Gm::VOFF);
                 const int nv = min(kBlockSize, C_len - (a.skip_blocks + j) * kBlockSize);
                 if constexpr (decltype(patch)::value) {
                     append_row<D, KV>(a, pc.g, phys_st[sidx], nv - 1, lane,
@@ -1066,7 +1066,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
 #pragma unroll
                     for (int ks = 0; ks < NT; ++ks) {
                         const int chunk = 2 * ks + half_k;
-                        const uint32_t off = (chunk >> 3) * Gm::RGN + swz<128>(row_k * 128 + (chunk & 7) * 16);
+                        const uint32_t off = (chunk >> 3) * Gm::CSTRIDE + swz<128>(row_k * 128 + (chunk & 7) * 16);
                         uint32_t fa[4];
                         ldsm_x4(kb + off, fa);
                         mma16816<false>((ks & 1) ? sb : sa, fa, qf[ks][0], qf[ks][1]);
@@ -1164,7 +1164,7 @@ __global__ void __launch_bounds__(Cfg<D, G, KV>::kThreads, Cfg<D, G, KV>::kMinBl
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
                         const int chunk = 2 * t + half_v;
-                        const uint32_t off = (chunk >> 3) * Gm::RGN + swz<128>(row_v * 128 + (chunk & 7) * 16);
+                        const uint32_t off = (chunk >> 3) * Gm::CSTRIDE + swz<128>(row_v * 128 + (chunk & 7) * 16);
                         uint32_t fa[4];
                         ldsm_x4_t(vb + off, fa);
                         if (nv < kBlockSize) {
@@ -1549,8 +1549,8 @@ static pkv_status launch_decode(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
     if (st != PKV_OK) return st;
     bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
     LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
-                               pool->tm_v, a);
+    cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_v,
+                               a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return launch_merge<D, G>(pool, a, grid * C::NW, s);
@@ -1685,7 +1685,7 @@ extern "C" pkv_status paged_decode_attention(pkv_pool *pool, const void *q, int3
     a.slice_blocks = pool->partition_tokens / kBlockSize;
     a.err = pool->err;
     a.k_new = a.v_new = nullptr;
-    a.k_pool = a.v_pool = nullptr;
+    a.k_pool = nullptr;
     a.skip_blocks = 0;
     a.n_pre = 0;
     a.pre_base = 0;
@@ -1743,7 +1743,7 @@ extern "C" pkv_status paged_decode_attention_csr(pkv_pool *pool, const void *q, 
     a.slice_blocks = pool->partition_tokens / kBlockSize;
     a.err = pool->err;
     a.k_new = a.v_new = nullptr;
-    a.k_pool = a.v_pool = nullptr;
+    a.k_pool = nullptr;
     a.skip_blocks = 0;
     a.n_pre = 0;
     a.pre_base = 0;
@@ -1769,8 +1769,8 @@ static pkv_status launch_step(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
     if (st != PKV_OK) return st;
     bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
     LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl(decode_kernel<D, G, KV, true>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
-                               pool->tm_v, a);
+    cudaError_t e = launch_pdl(decode_kernel<D, G, KV, true>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_v,
+                               a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
     return launch_merge<D, G>(pool, a, grid * C::NW, s);
@@ -1836,21 +1836,20 @@ static pkv_status step_device(pkv_pool *pool, const void *q, const void *k_new, 
     a.slice_blocks = pool->partition_tokens / kBlockSize;
     a.err = pool->err;
     a.k_new = a.v_new = nullptr;
-    a.k_pool = a.v_pool = nullptr;
+    a.k_pool = nullptr;
     a.skip_blocks = 0;
     a.n_pre = 0;
     a.pre_base = 0;
     a.k_new = static_cast<const __nv_bfloat16 *>(k_new);
     a.v_new = static_cast<const __nv_bfloat16 *>(v_new);
     a.k_pool = static_cast<uint8_t *>(pool->k);
-    a.v_pool = static_cast<uint8_t *>(pool->v);
     const bool fp8 = pool->dtype == PKV_FP8_E4M3;
     if (pool->dtype == PKV_INT4) {  // 4-bit pools: the append kernel (it finds the slots), then decode
         pkv_status st = append_step_int4(pool, k_new, v_new, block_tables, max_blocks_per_seq, context_lens,
                                          batch, s);
         if (st != PKV_OK) return st;
         a.k_new = a.v_new = nullptr;
-        a.k_pool = a.v_pool = nullptr;
+        a.k_pool = nullptr;
         return dispatch_kv(pool, a, G, s);
     }
     if (pool->d_head == 128) return fp8 ? dispatch_step<128, true>(pool, a, G, s) : dispatch_step<128, false>(pool, a, G, s);
@@ -2085,8 +2084,8 @@ static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32
     // decode leaves as it finishes), then the merge.
     {
         LaunchScope ls(pool, kDecode, s);
-        cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
-                                   pool->tm_v, a);
+        cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_v,
+                                   a);
         ls.done();
         if (e != cudaSuccess) return cuda_fail(e, "decode launch (cascade tail)");
     }
@@ -2151,7 +2150,7 @@ extern "C" pkv_status paged_decode_attention_prefix(pkv_pool *pool, const void *
     a.slice_blocks = pool->partition_tokens / kBlockSize;
     a.err = pool->err;
     a.k_new = a.v_new = nullptr;
-    a.k_pool = a.v_pool = nullptr;
+    a.k_pool = nullptr;
     a.skip_blocks = 0;
     a.n_pre = 0;
     a.pre_base = 0;
@@ -2217,8 +2216,8 @@ static pkv_status launch_decode_noalloc(pkv_pool *pool, DecodeArgs a, uint8_t *s
     // needs to start at zero (every partial is written before it is read).
     bind_workspace(a, scratch, L);
     LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_k,
-                               pool->tm_v, a);
+    cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_v,
+                               a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch (noalloc)");
     return launch_merge<D, G>(pool, a, grid * C::NW, s);
@@ -2299,7 +2298,7 @@ extern "C" pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void 
     a.slice_blocks = pool->partition_tokens / kBlockSize;
     a.err = pool->err;
     a.k_new = a.v_new = nullptr;
-    a.k_pool = a.v_pool = nullptr;
+    a.k_pool = nullptr;
     a.skip_blocks = 0;
     a.n_pre = 0;
     a.pre_base = 0;

@@ -22,14 +22,24 @@ constexpr int kBlockSize = 16;               // token slots per block
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // bounded mbarrier waits: 2 s
 constexpr int kDefaultPartitionTokens = 0;  // 0: equal work per CTA
 
-// 4-bit pools keep everything one (block, KV head) needs in one contiguous
-// entry: its 16 key rows of d/2 code bytes, its 16 value rows of d/2 code
-// bytes, then its 16 value rows' fp32 (scale, zero point) pairs.  Entries are
-// [num_blocks][n_kv]; each is a multiple of 16 bytes, so the decode kernel
-// fetches one with a single bulk copy.
-constexpr int64_t i4_entry_bytes(int d_head) { return 16 * (int64_t)d_head + kBlockSize * 8; }
-constexpr int64_t i4_v_offset(int d_head) { return 8 * (int64_t)d_head; }       // value codes
-constexpr int64_t i4_params_offset(int d_head) { return 16 * (int64_t)d_head; }  // value (scale, zero)
+// Every pool keeps what one (block, KV head) needs in one contiguous entry:
+// its 16 key rows, then its 16 value rows (d bf16, d E4M3 bytes, or d/2 bytes
+// of packed 4-bit codes per row), and for 4-bit pools then its 16 value rows'
+// fp32 (scale, zero point) pairs.  Entries are [num_blocks][n_kv] in one
+// allocation; each is a multiple of 16 bytes, so the decode kernel fetches
+// one with a single copy (one TMA box per 128-byte column, or one bulk copy).
+constexpr int64_t kv_row_bytes(int dtype, int d_head)
+{
+    return dtype == PKV_BF16 ? 2 * (int64_t)d_head : dtype == PKV_FP8_E4M3 ? d_head : d_head / 2;
+}
+constexpr int64_t kv_v_offset(int dtype, int d_head) { return kBlockSize * kv_row_bytes(dtype, d_head); }
+constexpr int64_t kv_entry_bytes(int dtype, int d_head)
+{
+    return 2 * kv_v_offset(dtype, d_head) + (dtype == PKV_INT4 ? kBlockSize * 8 : 0);
+}
+constexpr int64_t i4_entry_bytes(int d_head) { return kv_entry_bytes(PKV_INT4, d_head); }
+constexpr int64_t i4_v_offset(int d_head) { return kv_v_offset(PKV_INT4, d_head); }       // value codes
+constexpr int64_t i4_params_offset(int d_head) { return 2 * kv_v_offset(PKV_INT4, d_head); }  // value (scale, zero)
 
 enum KernelKind { kAppend = 0, kDecode = 1, kMerge = 2, kPrefix = 3, kBlocks = 4, kNumKinds = 5 };
 
@@ -63,20 +73,21 @@ struct pkv_pool {
     int num_sms = 0;
     int64_t num_blocks = 0;
     int block_size = 0, n_kv = 0, d_head = 0, dtype = 0;
-    // device, [num_blocks][n_kv][block_size][d_head] each (bf16 and FP8 pools); 4-bit pools: one
-    // allocation of [num_blocks][n_kv] entries (i4_entry_bytes), k, v and v_params pointing at the
-    // first entry's key codes, value codes and value parameters
+    // one allocation of [num_blocks][n_kv] entries (kv_entry_bytes); k, v (and for 4-bit pools
+    // v_params) point at the first entry's key rows, value rows (and value parameters)
     void *k = nullptr, *v = nullptr;
-    size_t bytes_per_array = 0;       // bytes of K (and of V) data; 4-bit pools: code bytes of each
+    size_t bytes_per_array = 0;       // bytes of K (and of V) data in the pool
     size_t alloc_bytes = 0;           // bytes of the allocation k points into
     float *scales = nullptr;          // device [2 * n_kv]: k scales then v scales
     // 4-bit pools: each value row's (scale, zero point), inside the entries, and the keys'
     // per-channel parameters [2][n_kv][d_head] fp32 (scales, then zero points)
     float *v_params = nullptr;
     float *k_params = nullptr;
-    // TMA descriptors of the K and V arrays viewed as 2-D [rows = blocks*n_kv*16][d_head],
-    // boxes of 16 rows x min(row bytes, 128) bytes, swizzled (128 B, or 64 B for 64-byte rows);
-    // bf16 and FP8 pools only (4-bit entries are fetched by bulk copies).
+    // TMA descriptors of the entries viewed as 2-D [rows = blocks*n_kv*32][d_head] (an entry's
+    // key rows at 32 u .. 32 u + 15, its value rows after them), boxes of min(row bytes, 128)
+    // bytes, swizzled (128 B, or 64 B for 64-byte rows): tm_k 16 rows high (one block's keys or
+    // values: prefill), tm_v 32 rows high (an entry's keys and values together: decode).  bf16
+    // and FP8 pools only (4-bit entries are fetched by bulk copies).
     CUtensorMap tm_k, tm_v;
     bool scales_set = false;
     unsigned *err = nullptr;          // device sticky error word

@@ -145,24 +145,25 @@ pkv_status make_tensor_maps(pkv_pool *pool)
     PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     pkv_status st = tiled_encoder(&encode);
     if (st != PKV_OK) return st;
-    // rows of d_head bf16, d_head E4M3 bytes, or d_head / 2 bytes of packed 4-bit codes
+    // the entries' rows: d_head bf16 or d_head E4M3 bytes each, 32 per entry (16 key rows, then 16
+    // value rows); 16-row boxes (tm_k) and 32-row boxes (tm_v) over the same rows
     const int elem = pool->dtype == PKV_BF16 ? 2 : 1;
-    const uint64_t row_elems = pool->dtype == PKV_INT4 ? (uint64_t)pool->d_head / 2 : (uint64_t)pool->d_head;
+    const uint64_t row_elems = (uint64_t)pool->d_head;
     const uint64_t row_bytes = row_elems * elem;
-    const uint64_t rows = (uint64_t)pool->num_blocks * pool->n_kv * pool->block_size;
-    if (rows >= (1ull << 31)) return fail(PKV_EUNSUPPORTED, "kv_pool_create: more than 2^31 token rows");
+    const uint64_t rows = (uint64_t)pool->num_blocks * pool->n_kv * 2 * pool->block_size;
+    if (rows >= (1ull << 31)) return fail(PKV_EUNSUPPORTED, "kv_pool_create: more than 2^31 key and value rows");
     const uint32_t box_bytes = row_bytes > 128 ? 128 : (uint32_t)row_bytes;
     cuuint64_t dims[2] = {(cuuint64_t)row_elems, rows};
     cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {box_bytes / (uint32_t)elem, (cuuint32_t)pool->block_size};
     cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType dt = elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     const CUtensorMapSwizzle sw = box_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
                                   : box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                     : CU_TENSOR_MAP_SWIZZLE_32B;
     for (int which = 0; which < 2; ++which) {
-        CUresult r = encode(which ? &pool->tm_v : &pool->tm_k, dt, 2, which ? pool->v : pool->k, dims, strides,
-                            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        cuuint32_t box[2] = {box_bytes / (uint32_t)elem, (cuuint32_t)((which ? 2 : 1) * pool->block_size)};
+        CUresult r = encode(which ? &pool->tm_v : &pool->tm_k, dt, 2, pool->k, dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     }
@@ -262,20 +263,14 @@ pkv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv, 
     p->d_head = d_head;
     p->dtype = dtype;
     p->bytes_per_array = per_block * (size_t)num_blocks;
-    const char *what = "cudaMalloc(K pool)";
-    if (dtype == PKV_INT4) {
-        // one allocation of (block, KV head) entries: key codes, value codes, value parameters
-        p->alloc_bytes = (size_t)num_blocks * n_kv * (size_t)i4_entry_bytes(d_head);
-        what = "cudaMalloc(4-bit pool)";
-        e = cudaMalloc(&p->k, p->alloc_bytes);
-        if (e == cudaSuccess) {
-            p->v = static_cast<uint8_t *>(p->k) + i4_v_offset(d_head);
+    // one allocation of (block, KV head) entries: key rows, value rows (and 4-bit value parameters)
+    p->alloc_bytes = (size_t)num_blocks * n_kv * (size_t)kv_entry_bytes(dtype, d_head);
+    const char *what = "cudaMalloc(pool)";
+    e = cudaMalloc(&p->k, p->alloc_bytes);
+    if (e == cudaSuccess) {
+        p->v = static_cast<uint8_t *>(p->k) + kv_v_offset(dtype, d_head);
+        if (dtype == PKV_INT4)
             p->v_params = reinterpret_cast<float *>(static_cast<uint8_t *>(p->k) + i4_params_offset(d_head));
-        }
-    } else {
-        p->alloc_bytes = p->bytes_per_array;
-        e = cudaMalloc(&p->k, p->bytes_per_array);
-        if (e == cudaSuccess) { what = "cudaMalloc(V pool)"; e = cudaMalloc(&p->v, p->bytes_per_array); }
     }
     if (e == cudaSuccess) { what = "cudaMalloc(scales)"; e = cudaMalloc(&p->scales, sizeof(float) * 2 * n_kv); }
     if (e == cudaSuccess) { what = "cudaMalloc(error word)"; e = cudaMalloc(&p->err, sizeof(unsigned)); }
@@ -285,7 +280,6 @@ pkv_status kv_pool_create(int64_t num_blocks, int32_t block_size, int32_t n_kv, 
         if (e == cudaSuccess) e = cudaMemset(p->k_params, 0, sizeof(float) * 2 * n_kv * d_head);
     }
     if (e == cudaSuccess) { what = "cudaMemset"; e = cudaMemset(p->k, 0, p->alloc_bytes); }
-    if (e == cudaSuccess && dtype != PKV_INT4) e = cudaMemset(p->v, 0, p->bytes_per_array);
     if (e == cudaSuccess) e = cudaMemset(p->scales, 0, sizeof(float) * 2 * n_kv);
     if (e == cudaSuccess) e = cudaMemset(p->err, 0, sizeof(unsigned));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -307,8 +301,7 @@ pkv_status kv_pool_destroy(pkv_pool *pool)
 {
     if (!pool) return PKV_OK;
     cudaDeviceSynchronize();
-    cudaFree(pool->k);
-    if (pool->dtype != PKV_INT4) cudaFree(pool->v);  // 4-bit pools: v and v_params point into k's allocation
+    cudaFree(pool->k);  // v (and v_params) point into the same allocation
     cudaFree(pool->scales);
     cudaFree(pool->k_params);
     cudaFree(pool->err);
@@ -370,9 +363,10 @@ pkv_status kv_pool_layout(const pkv_pool *pool, pkv_layout *out)
     out->v = pool->v;
     out->v_params = pool->v_params;
     out->v_params_bytes = pool->v_params ? (int64_t)pool->num_blocks * pool->n_kv * pool->block_size * 8 : 0;
+    // strides in elements (bytes for 4-bit pools): an entry is 2 x 16 rows (+ 4-bit parameters)
+    const int64_t elem = pool->dtype == PKV_BF16 ? 2 : 1;
     out->stride_token = pool->dtype == PKV_INT4 ? pool->d_head / 2 : pool->d_head;
-    out->stride_head = pool->dtype == PKV_INT4 ? i4_entry_bytes(pool->d_head)
-                                               : (int64_t)pool->block_size * out->stride_token;
+    out->stride_head = kv_entry_bytes(pool->dtype, pool->d_head) / elem;
     out->stride_block = (int64_t)pool->n_kv * out->stride_head;
     out->alloc_bytes = (int64_t)pool->alloc_bytes;
     out->num_blocks = pool->num_blocks;

@@ -86,7 +86,7 @@ struct Args {
     int batch, n_q, n_kv;
     int64_t num_blocks;
     int64_t n_rows;            // rows of q and out: stores past them are skipped (an inconsistent indptr)
-    int oob_row;               // a K/V row index past the end of the pool (zero-filled box)
+    int oob_row;               // a row index past the end of the pool's entry rows (zero-filled box)
     float qscale;              // scale * log2(e)
     const float *scales;       // FP8 pools: [2 * n_kv] fp32, K scales then V scales
     __nv_bfloat16 *out;        // [rows][n_q][D]
@@ -515,8 +515,7 @@ __device__ __forceinline__ bool wait_all(uint64_t *bar, uint32_t parity)
 
 template <int D, int G, bool PARTIAL, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, Args a)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv, Args a)
 {
     using L = Layout<D>;
     constexpr int NH = D / 64 > 0 ? D / 64 : 1;  // 64-column halves of a row
@@ -533,8 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         prefetch_tensormap(&tm_q);
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_kv);
         for (int i = 0; i < L::NBARS; ++i) {
             const bool by_warps = i == L::OUT_FULL || i == L::OUT_FREE;
             const bool by_half = i == L::P_FULL || i == L::P_FULL + 1;  // the four warps of a key half
@@ -579,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- producers
         const bool is_k = warp == kKWarp;
         const int NS = is_k ? kKStages : kVStages;
-        const CUtensorMap *map = is_k ? &tm_k : &tm_v;
+        const CUtensorMap *map = &tm_kv;  // 16-row boxes over the entries' key and value rows
         const uint32_t ring = is_k ? L::kK : L::kV;
         uint64_t *full = &bar[is_k ? L::K_FULL : L::V_FULL];
         uint64_t *empty = &bar[is_k ? L::K_EMPTY : L::V_EMPTY];
@@ -647,7 +645,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive_expect_tx(&land[st], F8 ? L::KT / 2 : L::KT);
                 __syncwarp();
                 if (lane < kStepBlocks) {  // lane k copies block k of the step
-                    const int y = valid ? (int)((cur * (int64_t)a.n_kv + t.g) * kBlockSize) : a.oob_row;
+                    // the block's key rows open its (block, KV head) entry, its value rows follow
+                    const int y = valid ? (int)((cur * (int64_t)a.n_kv + t.g) * 2 * kBlockSize + (is_k ? 0 : kBlockSize))
+                                        : a.oob_row;
                     if constexpr (F8) {  // one box per block: 16 E4M3 rows of D bytes
                         tma_load_2d(sm + ring + st * L::KT + L::KT / 2 + lane * (kBlockSize * D), map, 0, y,
                                     &raw[st], policy);
@@ -1045,7 +1045,7 @@ pkv_status launch(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, int64_
     const int grid = 2 * (int)std::min<int64_t>(pairs, max_pairs);
     LaunchScope ls(pool, PARTIAL ? kPrefix : kDecode, s);
     cudaError_t e = launch_pdl(prefill_tc_kernel<D, G, PARTIAL, F8>, dim3(grid), dim3(kThreads), L::bytes, s, tm_q,
-                               pool->tm_k, pool->tm_v, a);
+                               pool->tm_k, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, PARTIAL ? "prefix stage launch" : "prefill launch");
     return PKV_OK;
@@ -1109,7 +1109,7 @@ extern "C" pkv_status paged_prefill_attention(pkv_pool *pool, const void *q, int
     a.n_kv = pool->n_kv;
     a.num_blocks = pool->num_blocks;
     a.n_rows = n_rows;
-    a.oob_row = (int)(pool->num_blocks * pool->n_kv * kBlockSize);
+    a.oob_row = (int)(pool->num_blocks * pool->n_kv * 2 * kBlockSize);
     a.qscale = scale * kLog2e;
     a.scales = pool->scales;
     a.out = static_cast<__nv_bfloat16 *>(out);
@@ -1158,7 +1158,7 @@ pkv_status launch_prefix_stage(pkv_pool *pool, const void *q, int batch, int n_q
     a.n_kv = pool->n_kv;
     a.num_blocks = pool->num_blocks;
     a.n_rows = batch;
-    a.oob_row = (int)(pool->num_blocks * pool->n_kv * kBlockSize);
+    a.oob_row = (int)(pool->num_blocks * pool->n_kv * 2 * kBlockSize);
     a.qscale = qscale;
     a.scales = pool->scales;
     a.out = nullptr;

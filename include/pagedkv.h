@@ -60,35 +60,34 @@ typedef enum {
 
 typedef struct pkv_pool pkv_pool; /* opaque; owns its device memory */
 
-/* Where a pool's blocks live.  bf16 and FP8 pools: K and V are two separate
- * device arrays, each laid out [num_blocks][n_kv][block_size][d_head]:
- * element (blk, g, off, d) of either array sits at blk*stride_block +
- * g*stride_head + off*stride_token + d (strides in elements), so one (block,
- * KV head) tile is contiguous.
- * PKV_INT4 pools store packed codes: an "element" is one byte holding
- * channels 2i (low nibble) and 2i+1 (high nibble), a row has d_head / 2 of
- * them.  Everything one (block, KV head) needs is one contiguous entry of
- * stride_head = 16 * d_head + 128 bytes: its 16 key rows, its 16 value rows,
- * then its 16 value rows' fp32 (scale, zero point) pairs; entries are
- * [num_blocks][n_kv] in one allocation of alloc_bytes starting at k.  The
- * same element formula holds for k and v (v = k + 8 * d_head), and value row
- * (blk, g, off)'s pair sits at v_params + blk*stride_block + g*stride_head +
- * 8*off bytes. */
+/* Where a pool's blocks live.  Everything one (block, KV head) needs is one
+ * contiguous entry: its 16 key rows, then its 16 value rows (and for
+ * PKV_INT4 pools then its 16 value rows' fp32 (scale, zero point) pairs).
+ * Entries are [num_blocks][n_kv] in one allocation of alloc_bytes starting
+ * at k; v points at the first entry's value rows.  Element (blk, g, off, d)
+ * of the keys sits at k + blk*stride_block + g*stride_head +
+ * off*stride_token + d, and of the values at the same offset from v (strides
+ * in elements: bf16 values, E4M3 bytes, or bytes of packed codes).  A row is
+ * d_head values, or for PKV_INT4 d_head / 2 bytes each holding channels 2i
+ * (low nibble) and 2i+1 (high nibble).  stride_head is 32 * d_head elements
+ * (PKV_INT4: 16 * d_head + 128 bytes).  Value row (blk, g, off)'s 4-bit
+ * parameters sit at v_params + blk*stride_block + g*stride_head + 8*off
+ * bytes. */
 typedef struct {
     void *k;                 /* device */
     void *v;                 /* device */
     int64_t stride_block;    /* n_kv * stride_head */
-    int64_t stride_head;     /* block_size * d_head (PKV_INT4: 16 * d_head + 128) */
+    int64_t stride_head;     /* 2 * block_size * d_head (PKV_INT4: 16 * d_head + 128 bytes) */
     int64_t stride_token;    /* d_head (PKV_INT4: d_head / 2) */
     int64_t num_blocks;
     int32_t block_size;
     int32_t n_kv;
     int32_t d_head;
     int32_t dtype;           /* pkv_dtype */
-    int64_t bytes_per_array; /* bytes of K (and, equally, of V) data */
+    int64_t bytes_per_array; /* bytes of key (and, equally, of value) rows in the pool */
     void *v_params;          /* device; PKV_INT4 only (NULL otherwise) */
     int64_t v_params_bytes;  /* bytes of value parameters in the pool (8 per token row) */
-    int64_t alloc_bytes;     /* bytes of the allocation k points into (PKV_INT4: the whole pool) */
+    int64_t alloc_bytes;     /* bytes of the allocation k points into: the whole pool */
 } pkv_layout;
 
 /* Per-kernel timing gathered with CUDA events while timing is enabled. */
@@ -403,13 +402,11 @@ pkv_status paged_decode_attention_noalloc(pkv_pool *pool, const void *q, int32_t
  * preempted sequence's blocks may be swapped to CPU memory; "Memory
  * Management in LLM Serving Systems", "Eviction: recompute or offload?").
  * A block is block_bytes of K plus block_bytes of V: all n_kv heads' 16
- * token rows (contiguous in each array for bf16 and FP8 pools; a 4-bit
- * pool's block is its n_kv contiguous entries, key codes, value codes and
- * value parameters per head, see pkv_layout).
+ * token rows, held as its n_kv contiguous entries (see pkv_layout).
  * --------------------------------------------------------------------- */
 
-/* Bytes of one block in one array (K or V): n_kv x 16 x d_head x (2 bf16,
- * 1 FP8, 1/2 4-bit).  -1 for a NULL pool. */
+/* Bytes of one block's keys (or, equally, values): n_kv x 16 x d_head x
+ * (2 bf16, 1 FP8, 1/2 4-bit).  -1 for a NULL pool. */
 int64_t kv_block_bytes(const pkv_pool *pool);
 
 /* Bytes of one swapped block in a host buffer: its K bytes, its V bytes and,

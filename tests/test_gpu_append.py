@@ -108,12 +108,18 @@ def test_append_host_validation():
 
 
 def test_layout_is_the_documented_one():
+    # one (block, KV head) entry: 16 key rows then 16 value rows (strides in bf16 elements)
     with pkv.kv_pool_create(10, 16, 8, 128) as pool:
         lay = pool.layout()
         assert lay["stride_token"] == 128
-        assert lay["stride_head"] == 16 * 128
-        assert lay["stride_block"] == 8 * 16 * 128
+        assert lay["stride_head"] == 32 * 128
+        assert lay["stride_block"] == 8 * 32 * 128
         assert lay["bytes_per_array"] == 10 * 8 * 16 * 128 * 2
-        assert lay["k"] % 256 == 0 and lay["v"] % 256 == 0
+        assert lay["alloc_bytes"] == 2 * lay["bytes_per_array"]
+        assert lay["k"] % 256 == 0 and lay["v"] - lay["k"] == 16 * 128 * 2
         k, v = pool_bytes(pool)
         assert not k.any() and not v.any()  # zero-filled at creation
+    with pkv.kv_pool_create(10, 16, 8, 64, pkv.FP8_E4M3) as pool:
+        lay = pool.layout()
+        assert (lay["stride_token"], lay["stride_head"], lay["stride_block"]) == (64, 32 * 64, 8 * 32 * 64)
+        assert lay["v"] - lay["k"] == 16 * 64
