@@ -771,8 +771,9 @@ def run_blocks(args):
     pool = pkv.kv_pool_create(NB, 16, 8, 128, pkv.BF16)
     bb = pkv.kv_block_bytes(pool)
     g = torch.Generator(device="cuda").manual_seed(5)
-    pool.k_view().view(-1).copy_(torch.randint(0, 256, (NB * bb,), dtype=torch.uint8, device="cuda", generator=g))
-    pool.v_view().view(-1).copy_(torch.randint(0, 256, (NB * bb,), dtype=torch.uint8, device="cuda", generator=g))
+    kview, vview = pool.k_view(), pool.v_view()  # strided views into the pool's (block, head) entries
+    kview.copy_(torch.randint(0, 256, tuple(kview.shape), dtype=torch.uint8, device="cuda", generator=g))
+    vview.copy_(torch.randint(0, 256, tuple(vview.shape), dtype=torch.uint8, device="cuda", generator=g))
     perm = np.random.default_rng(3).permutation(NB).astype(np.int32)
     src = torch.from_numpy(perm[:n]).cuda()
     dst = torch.from_numpy(perm[n:2 * n]).cuda()
@@ -780,7 +781,7 @@ def run_blocks(args):
     warm = max(3, args.warmup)
     copy_ms = _timed(lambda: pkv.kv_block_copy(pool, src, dst, stream), reps, warm, stream)
     # exact: every destination block equals its source, K and V
-    kv, vv = pool.k_view().view(NB, -1), pool.v_view().view(NB, -1)
+    kv, vv = kview.reshape(NB, -1), vview.reshape(NB, -1)  # copies: read after the block copies ran
     copy_ok = bool(torch.equal(kv[dst.long()], kv[src.long()]) and torch.equal(vv[dst.long()], vv[src.long()]))
     copy_bytes = 2 * n * 2 * bb  # read + write, K and V
     host = torch.empty(n * 2 * bb, dtype=torch.uint8).pin_memory()

@@ -31,7 +31,8 @@ struct BlockMoveArgs {
     uint8_t *host;                 // swap buffer [n][entry bytes] (device address of pinned memory)
     int64_t n, num_blocks, block_bytes, param_bytes;  // image entry bytes = 2 block_bytes + param_bytes
     int64_t head_entry;            // bytes of a (block, KV head) entry in the pool
-    int64_t head_rows;             // bytes of one head's 16 key (or value) rows
+    int64_t head_rows;             // bytes of one head's 16 key (or value) rows: a power of two
+    int rows_shift;                // log2(head_rows)
     int n_kv;
     unsigned *err;
 };
@@ -45,18 +46,20 @@ struct EntryByte {
 
 __device__ __forceinline__ EntryByte entry_byte(const BlockMoveArgs &a, int64_t off)
 {
-    // the head's entry, and the section within it (16-byte chunks never straddle heads)
-    int64_t sec = 0, per = a.head_rows;
-    if (off >= 2 * a.block_bytes) {  // 4-bit value parameters
+    // the head's entry, and the section within it (16-byte chunks never straddle heads); section
+    // sizes are powers of two, so the head is a shift
+    int64_t sec = 0;
+    int sh = a.rows_shift;
+    if (off >= 2 * a.block_bytes) {  // 4-bit value parameters: 16 rows x 8 bytes per head
         off -= 2 * a.block_bytes;
         sec = 2 * a.head_rows;
-        per = kBlockSize * 8;
+        sh = 7;
     } else if (off >= a.block_bytes) {  // value rows
         off -= a.block_bytes;
         sec = a.head_rows;
     }
-    const int64_t g = off / per;
-    return {a.pool, a.n_kv * a.head_entry, g * a.head_entry + sec + (off - g * per)};
+    const int64_t g = off >> sh;
+    return {a.pool, a.n_kv * a.head_entry, g * a.head_entry + sec + (off & ((int64_t(1) << sh) - 1))};
 }
 
 enum MoveKind { kCopy = 0, kSwapOut = 1, kSwapIn = 2 };
@@ -73,7 +76,9 @@ __global__ void __launch_bounds__(256) block_move_kernel(BlockMoveArgs a)
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
         const int64_t pair = i / chunks;
         const int64_t c = i - pair * chunks;
-        const EntryByte e = entry_byte(a, c * 16);
+        // a copy moves the block's n_kv contiguous entries as they are; a swap maps each chunk of the
+        // host image to its place in the entries
+        const EntryByte e = KIND == kCopy ? EntryByte{a.pool, a.n_kv * a.head_entry, c * 16} : entry_byte(a, c * 16);
         if constexpr (KIND == kCopy) {
             const int64_t s = a.src_ids[pair], d = a.dst_ids[pair];
             if (s < 0 || s >= a.num_blocks || d < 0 || d >= a.num_blocks) {
@@ -134,6 +139,8 @@ static BlockMoveArgs move_args(pkv_pool *pool, int64_t n)
     a.param_bytes = param_bytes_of(pool);
     a.head_entry = kv_entry_bytes(pool->dtype, pool->d_head);
     a.head_rows = kv_v_offset(pool->dtype, pool->d_head);
+    a.rows_shift = 0;
+    while ((int64_t(1) << a.rows_shift) < a.head_rows) ++a.rows_shift;
     a.n_kv = pool->n_kv;
     a.err = pool->err;
     return a;
