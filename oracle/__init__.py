@@ -23,8 +23,11 @@ passage of the pages it follows:
 * ``e4m3_decode`` / ``e4m3_encode`` -- the E4M3 bit-field definition and a
   brute-force nearest-code encoder (the pages say "FP8"; E4M3 is the reading).
 
-Pool layout mirrored (the documented contract of the library): K and V are
-separate arrays ``[num_blocks][n_kv][block_size][d_head]``.
+Pool contents mirrored: the keys and the values as two logical arrays
+``[num_blocks][n_kv][block_size][d_head]``.  The library's pool places each
+(block, KV head)'s key rows and value rows side by side in one entry; the tests
+read its keys and values through the strides ``kv_pool_layout`` reports, as
+these same logical arrays.
 """
 from __future__ import annotations
 
@@ -141,7 +144,7 @@ def int4_row_params(row_bits: np.ndarray) -> tuple[float, float]:
 
 
 class PoolMirror:
-    """Host copy of a K/V block pool in the library's documented layout.
+    """Host copy of a K/V block pool's contents, as logical key and value arrays.
 
     ``k`` and ``v`` are raw element arrays: uint16 bf16 bit patterns or uint8
     E4M3 codes, shaped ``[num_blocks, n_kv, block_size, d_head]`` and

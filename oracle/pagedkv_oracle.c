@@ -47,10 +47,12 @@
  *       round-half-to-even.  Codes are packed two per byte, the even
  *       channel in the low nibble.
  *
- * Pool layout mirrored here (the documented contract of the library): K and V
- * are two separate arrays, each [num_blocks][n_kv][block_size][d_head], so
- * element (blk, g, off, d) sits at ((blk*n_kv + g)*block_size + off)*d_head + d.
- * Elements are bf16 (2 bytes, stored as raw 16-bit patterns) or E4M3 (1 byte).
+ * Pool contents mirrored here as two logical arrays, keys and values, each
+ * [num_blocks][n_kv][block_size][d_head], so element (blk, g, off, d) sits at
+ * ((blk*n_kv + g)*block_size + off)*d_head + d (the library stores a (block,
+ * KV head)'s key and value rows side by side; tests read them through its
+ * reported strides as these arrays).  Elements are bf16 (2 bytes, stored as
+ * raw 16-bit patterns) or E4M3 (1 byte).
  *
  * Build: gcc -O2 -std=c11 -shared -fPIC pagedkv_oracle.c -lm -lpthread.
  * No -ffast-math: fp32 division and fp64 arithmetic must be IEEE.
