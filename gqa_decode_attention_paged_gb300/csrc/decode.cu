@@ -1549,7 +1549,7 @@ static pkv_status launch_decode(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
     if (st != PKV_OK) return st;
     bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
     LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_v,
+    cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_entry,
                                a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -1769,7 +1769,7 @@ static pkv_status launch_step(pkv_pool *pool, DecodeArgs a, cudaStream_t s)
     if (st != PKV_OK) return st;
     bind_workspace(a, static_cast<uint8_t *>(pool->ws), L);
     LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl(decode_kernel<D, G, KV, true>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_v,
+    cudaError_t e = launch_pdl(decode_kernel<D, G, KV, true>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_entry,
                                a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
@@ -2084,7 +2084,7 @@ static pkv_status launch_prefix_decode(pkv_pool *pool, DecodeArgs a, const int32
     // decode leaves as it finishes), then the merge.
     {
         LaunchScope ls(pool, kDecode, s);
-        cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_v,
+        cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_entry,
                                    a);
         ls.done();
         if (e != cudaSuccess) return cuda_fail(e, "decode launch (cascade tail)");
@@ -2216,7 +2216,7 @@ static pkv_status launch_decode_noalloc(pkv_pool *pool, DecodeArgs a, uint8_t *s
     // needs to start at zero (every partial is written before it is read).
     bind_workspace(a, scratch, L);
     LaunchScope ls(pool, kDecode, s);
-    cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_v,
+    cudaError_t e = launch_pdl(decode_kernel<D, G, KV>, dim3(grid), dim3(C::kThreads), smem, s, pool->tm_entry,
                                a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, "decode launch (noalloc)");

@@ -85,10 +85,10 @@ struct pkv_pool {
     float *k_params = nullptr;
     // TMA descriptors of the entries viewed as 2-D [rows = blocks*n_kv*32][d_head] (an entry's
     // key rows at 32 u .. 32 u + 15, its value rows after them), boxes of min(row bytes, 128)
-    // bytes, swizzled (128 B, or 64 B for 64-byte rows): tm_k 16 rows high (one block's keys or
-    // values: prefill), tm_v 32 rows high (an entry's keys and values together: decode).  bf16
-    // and FP8 pools only (4-bit entries are fetched by bulk copies).
-    CUtensorMap tm_k, tm_v;
+    // bytes, swizzled (128 B, or 64 B for 64-byte rows): tm_block 16 rows high (one block's keys
+    // or values: prefill), tm_entry 32 rows high (an entry's keys and values together: decode).
+    // bf16 and FP8 pools only (4-bit entries are fetched by bulk copies).
+    CUtensorMap tm_block, tm_entry;
     bool scales_set = false;
     unsigned *err = nullptr;          // device sticky error word
     void *ws = nullptr;               // split-KV workspace (grow-only)

@@ -146,7 +146,7 @@ pkv_status make_tensor_maps(pkv_pool *pool)
     pkv_status st = tiled_encoder(&encode);
     if (st != PKV_OK) return st;
     // the entries' rows: d_head bf16 or d_head E4M3 bytes each, 32 per entry (16 key rows, then 16
-    // value rows); 16-row boxes (tm_k) and 32-row boxes (tm_v) over the same rows
+    // value rows); 16-row boxes (tm_block) and 32-row boxes (tm_entry) over the same rows
     const int elem = pool->dtype == PKV_BF16 ? 2 : 1;
     const uint64_t row_elems = (uint64_t)pool->d_head;
     const uint64_t row_bytes = row_elems * elem;
@@ -162,7 +162,7 @@ pkv_status make_tensor_maps(pkv_pool *pool)
                                                     : CU_TENSOR_MAP_SWIZZLE_32B;
     for (int which = 0; which < 2; ++which) {
         cuuint32_t box[2] = {box_bytes / (uint32_t)elem, (cuuint32_t)((which ? 2 : 1) * pool->block_size)};
-        CUresult r = encode(which ? &pool->tm_v : &pool->tm_k, dt, 2, pool->k, dims, strides, box, estr,
+        CUresult r = encode(which ? &pool->tm_entry : &pool->tm_block, dt, 2, pool->k, dims, strides, box, estr,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(PKV_ECUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);

@@ -1045,7 +1045,7 @@ pkv_status launch(pkv_pool *pool, const void *q, int64_t n_rows, int n_q, int64_
     const int grid = 2 * (int)std::min<int64_t>(pairs, max_pairs);
     LaunchScope ls(pool, PARTIAL ? kPrefix : kDecode, s);
     cudaError_t e = launch_pdl(prefill_tc_kernel<D, G, PARTIAL, F8>, dim3(grid), dim3(kThreads), L::bytes, s, tm_q,
-                               pool->tm_k, a);
+                               pool->tm_block, a);
     ls.done();
     if (e != cudaSuccess) return cuda_fail(e, PARTIAL ? "prefix stage launch" : "prefill launch");
     return PKV_OK;
